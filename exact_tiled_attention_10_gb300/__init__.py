@@ -1,0 +1,210 @@
+"""Exact tiled attention for GB300 (sm_103a): thin Python binding.
+
+Every step of the computation runs in the CUDA kernels of ``libfa_gb300.so``
+behind the C ABI of ``include/fa.h``; this module only marshals arguments
+(torch tensors -> device pointers, the current CUDA stream) and allocates
+outputs and scratch with torch.  There is no CPU fallback: if the library is
+missing or no CUDA device is present, calls raise.
+
+    o, lse = forward(q, k, v, causal=True)               # bf16 or float32
+    dq, dk, dv = backward(q, k, v, o, lse, do, causal=True)
+    q8, sq = quantize_fp8(q)                              # E4M3 + per-64-row scales
+    o8, lse8 = forward_fp8(q8, k8, v8, sq, sk, sv)
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+from typing import Optional, Tuple
+
+import torch
+
+__all__ = ["forward", "backward", "quantize_fp8", "forward_fp8", "check_device_status",
+           "bwd_workspace_size", "fwd_workspace_size", "library_path", "load_library", "FAError"]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libfa_gb300.so")
+_lock = threading.Lock()
+_lib = None
+
+FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = 0, 1, 2, 3, 4
+FA_BF16, FA_F32 = 0, 1
+_STATUS = {1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_CUDA", 4: "FA_ERR_TIMEOUT"}
+
+# C signatures of include/fa.h, as ctypes argtypes
+_vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+_SIGS = {
+    "fa_version": ([], _i),
+    "fa_last_error": ([], ctypes.c_char_p),
+    "fa_check_device_status": ([_vp], _i),
+    "fa_fwd": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _vp], _i),
+    "fa_fwd_workspace_size": ([_i, _i, _i, _i, _i], _sz),
+    "fa_fwd_ex": ([_i, _i, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _vp, _sz, _vp], _i),
+    "fa_bwd_workspace_size": ([_i, _i, _i, _i, _i], _sz),
+    "fa_bwd": ([_vp] * 9 + [_i, _i, _i, _i, _f, _i, _vp, _vp, _sz, _vp], _i),
+    "fa_bwd_ex": ([_i] + [_vp] * 9 + [_i, _i, _i, _i, _f, _i, _vp, _vp, _sz, _vp], _i),
+    "fa_fp8_num_blocks": ([_i], _i),
+    "fa_quantize_fp8": ([_vp, _vp, _vp, _i, _i, _i, _i, _vp], _i),
+    "fa_fwd_fp8": ([_vp] * 8 + [_i, _i, _i, _i, _f, _i, _vp, _vp], _i),
+}
+
+
+class FAError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__("%s: %s" % (_STATUS.get(status, str(status)), msg))
+        self.status = status
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Load libfa_gb300.so (built by ``build.build()``); raise if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise RuntimeError(
+                    "libfa_gb300.so is not built; run exact_tiled_attention_10_gb300.build.build() "
+                    "(the CUDA path has no fallback)")
+            lib = ctypes.CDLL(_LIB_PATH)
+            for name, (args, res) in _SIGS.items():
+                fn = getattr(lib, name)
+                fn.argtypes = args
+                fn.restype = res
+            _lib = lib
+    return _lib
+
+
+def _check(status: int):
+    if status != FA_OK:
+        raise FAError(status, load_library().fa_last_error().decode(errors="replace"))
+
+
+def _stream(t: torch.Tensor) -> int:
+    return torch.cuda.current_stream(t.device).cuda_stream
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None:
+            if not t.is_cuda:
+                raise ValueError("tensors must be on a CUDA device (no CPU fallback)")
+            if not t.is_contiguous():
+                raise ValueError("tensors must be contiguous")
+
+
+def _kv(kv_lens: Optional[torch.Tensor], B: int, device) -> Optional[torch.Tensor]:
+    if kv_lens is None:
+        return None
+    kv = kv_lens.to(device=device, dtype=torch.int32).contiguous()
+    if kv.shape != (B,):
+        raise ValueError("kv_lens must have shape [B]")
+    return kv
+
+
+def fwd_workspace_size(dtype: torch.dtype, B: int, H: int, N: int, d: int) -> int:
+    dt = FA_F32 if dtype == torch.float32 else FA_BF16
+    return int(load_library().fa_fwd_workspace_size(dt, B, H, N, d))
+
+
+def bwd_workspace_size(dtype: torch.dtype, B: int, H: int, N: int, d: int) -> int:
+    dt = FA_F32 if dtype == torch.float32 else FA_BF16
+    return int(load_library().fa_bwd_workspace_size(dt, B, H, N, d))
+
+
+def forward(q, k, v, causal: bool = False, scale: Optional[float] = None, kv_lens=None,
+            block_c: int = 0, out: Optional[torch.Tensor] = None,
+            lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None
+            ) -> Tuple[torch.Tensor, torch.Tensor]:
+    """O, LSE of softmax(scale Q K^T + mask) V.  q,k,v: [B,H,N,d] bf16 or float32."""
+    lib = load_library()
+    _need_cuda(q, k, v)
+    B, H, N, d = q.shape
+    if k.shape != q.shape or v.shape != q.shape or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must share shape and dtype")
+    if q.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("dtype must be bfloat16 or float32")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    kv = _kv(kv_lens, B, q.device)
+    o = torch.empty_like(q) if out is None else out
+    l = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    _need_cuda(o, l)
+    dt = FA_F32 if q.dtype == torch.float32 else FA_BF16
+    wsz = int(lib.fa_fwd_workspace_size(dt, B, H, N, d))
+    ws = workspace
+    if wsz and (ws is None or ws.numel() * ws.element_size() < wsz):
+        ws = torch.empty(wsz, dtype=torch.uint8, device=q.device)
+    _check(lib.fa_fwd_ex(dt, int(block_c), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(l), B, H, N, d,
+                         scale, int(bool(causal)), _ptr(kv), _ptr(ws) if wsz else None, wsz,
+                         _stream(q)))
+    return o, l
+
+
+def backward(q, k, v, o, lse, dout, causal: bool = False, scale: Optional[float] = None,
+             kv_lens=None, workspace: Optional[torch.Tensor] = None,
+             dq: Optional[torch.Tensor] = None, dk: Optional[torch.Tensor] = None,
+             dv: Optional[torch.Tensor] = None):
+    """dQ, dK, dV of L = sum(O * dout)."""
+    lib = load_library()
+    _need_cuda(q, k, v, o, lse, dout)
+    B, H, N, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    kv = _kv(kv_lens, B, q.device)
+    dt = FA_F32 if q.dtype == torch.float32 else FA_BF16
+    wsz = int(lib.fa_bwd_workspace_size(dt, B, H, N, d))
+    ws = workspace
+    if ws is None or ws.numel() * ws.element_size() < wsz:
+        ws = torch.empty(wsz, dtype=torch.uint8, device=q.device)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    _need_cuda(dq, dk, dv)
+    _check(lib.fa_bwd_ex(dt, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
+                         _ptr(dk), _ptr(dv), B, H, N, d, scale, int(bool(causal)), _ptr(kv),
+                         _ptr(ws), ws.numel() * ws.element_size(), _stream(q)))
+    return dq, dk, dv
+
+
+def quantize_fp8(x: torch.Tensor, out: Optional[torch.Tensor] = None,
+                 scales: Optional[torch.Tensor] = None):
+    """E4M3 codes (uint8 [B,H,N,d]) and float32 scales [B,H,ceil(N/64)] of a bf16 tensor."""
+    lib = load_library()
+    _need_cuda(x)
+    if x.dtype != torch.bfloat16:
+        raise ValueError("quantize_fp8 takes bfloat16 input")
+    B, H, N, d = x.shape
+    x8 = torch.empty(x.shape, dtype=torch.uint8, device=x.device) if out is None else out
+    sc = torch.empty((B, H, lib.fa_fp8_num_blocks(N)), dtype=torch.float32, device=x.device) \
+        if scales is None else scales
+    _check(lib.fa_quantize_fp8(_ptr(x), _ptr(x8), _ptr(sc), B, H, N, d, _stream(x)))
+    return x8, sc
+
+
+def forward_fp8(q8, k8, v8, sq, sk, sv, causal: bool = False, scale: Optional[float] = None,
+                kv_lens=None, out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None):
+    """FP8 E4M3 forward with per-64-row-block scales; O bf16, LSE float32."""
+    lib = load_library()
+    _need_cuda(q8, k8, v8, sq, sk, sv)
+    B, H, N, d = q8.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    kv = _kv(kv_lens, B, q8.device)
+    o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q8.device) if out is None else out
+    l = torch.empty((B, H, N), dtype=torch.float32, device=q8.device) if lse is None else lse
+    _check(lib.fa_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(v8), _ptr(sq), _ptr(sk), _ptr(sv), _ptr(o),
+                          _ptr(l), B, H, N, d, scale, int(bool(causal)), _ptr(kv), _stream(q8)))
+    return o, l
+
+
+def check_device_status(device=None) -> None:
+    """Synchronise the current stream and raise if a kernel recorded a timed-out wait."""
+    lib = load_library()
+    dev = torch.device("cuda") if device is None else torch.device(device)
+    _check(lib.fa_check_device_status(torch.cuda.current_stream(dev).cuda_stream))

@@ -1,0 +1,95 @@
+"""Build the CUDA library libfa_gb300.so in-tree (sm_103a only).
+
+Each .cu under csrc/ is compiled in parallel with nvcc, then linked into one
+shared library exposing the C ABI of include/fa.h.  No cmake, no torch
+extension machinery: plain nvcc, so the same command works on any host that
+has the CUDA 13 toolkit (x86_64 here, aarch64 on the GPU machines).
+"""
+from __future__ import annotations
+
+import concurrent.futures as cf
+import os
+import platform
+import shutil
+import subprocess
+import sys
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+CSRC = os.path.join(HERE, "csrc")
+BUILD = os.path.join(ROOT, "_build", "fa")
+LIB = os.path.join(HERE, "libfa_gb300.so")
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
+         "-I" + os.path.join(ROOT, "include")]
+
+
+def _nvcc() -> str:
+    for cand in (os.environ.get("NVCC"), shutil.which("nvcc"), "/usr/local/cuda/bin/nvcc"):
+        if cand and os.path.exists(cand):
+            return cand
+    raise RuntimeError("nvcc not found")
+
+
+def _sources():
+    return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
+
+
+def _deps():
+    hdrs = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
+    return hdrs + [os.path.join(ROOT, "include", "fa.h"), os.path.abspath(__file__)]
+
+
+def _stale(target, inputs):
+    if not os.path.exists(target):
+        return True
+    t = os.path.getmtime(target)
+    return any(os.path.getmtime(x) > t for x in inputs)
+
+
+def build(force: bool = False, verbose: bool = False, jobs: int | None = None) -> str:
+    nvcc = _nvcc()
+    os.makedirs(BUILD, exist_ok=True)
+    # objects and the library are host-architecture specific: rebuild everything
+    # when the tree was last built on another kind of host
+    stamp = os.path.join(BUILD, "host.txt")
+    host = platform.machine() + " " + nvcc
+    if not os.path.exists(stamp) or open(stamp).read() != host or not os.path.exists(LIB):
+        force = True
+    deps = _deps()
+    srcs = _sources()
+    objs = []
+    todo = []
+    for s in srcs:
+        o = os.path.join(BUILD, os.path.basename(s)[:-3] + ".o")
+        objs.append(o)
+        if force or _stale(o, [s] + deps):
+            todo.append((s, o))
+
+    def compile_one(so):
+        s, o = so
+        cmd = [nvcc] + ARCH + FLAGS + (["-Xptxas", "-v"] if verbose else []) + ["-c", s, "-o", o]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError("nvcc failed for %s:\n%s" % (s, r.stderr))
+        return s, r.stderr
+
+    if todo:
+        with cf.ThreadPoolExecutor(max_workers=jobs or min(len(todo), os.cpu_count() or 4)) as ex:
+            for s, err in ex.map(compile_one, todo):
+                if verbose and err:
+                    sys.stderr.write(err)
+    if force or todo or _stale(LIB, objs):
+        tmp = LIB + ".tmp.%d" % os.getpid()
+        cmd = [nvcc] + ARCH + ["-shared", "-o", tmp] + objs
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError("link failed:\n%s" % r.stderr)
+        os.replace(tmp, LIB)
+    with open(stamp, "w") as f:
+        f.write(host)
+    return LIB
+
+
+if __name__ == "__main__":
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))

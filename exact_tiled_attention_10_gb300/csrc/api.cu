@@ -1,0 +1,379 @@
+// C ABI of the library (declared in include/fa.h): argument validation, TMA
+// tensor-map construction, kernel dispatch and error reporting.  No device
+// memory is allocated here; every buffer, including scratch, is the caller's.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/fa.h"
+#include "common.cuh"
+
+namespace {
+
+__device__ unsigned int g_fa_error_word;
+
+thread_local char t_last_error[512] = "";
+
+fa_status fail(fa_status s, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(t_last_error, sizeof(t_last_error), fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+fa_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(FA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    bool ready = false;
+    int sms = 0;
+    int cc_major = 0;
+    unsigned int* err_word = nullptr;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+// Per-device facts, looked up once per device with that device current.
+fa_status device_info(DeviceInfo** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(FA_ERR_UNSUPPORTED, "device index %d out of range", dev);
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    DeviceInfo& d = g_dev[dev];
+    if (!d.ready) {
+        cudaDeviceProp prop;
+        e = cudaGetDeviceProperties(&prop, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceProperties");
+        d.sms = prop.multiProcessorCount;
+        d.cc_major = prop.major;
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_fa_error_word);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(error word)");
+        d.err_word = reinterpret_cast<unsigned int*>(p);
+        if (!g_encode) {
+            void* fn = nullptr;
+            cudaDriverEntryPointQueryResult q;
+            e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+            if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+                return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+            g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+        }
+        d.ready = true;
+    }
+    if (d.cc_major != 10) return fail(FA_ERR_UNSUPPORTED, "needs a compute capability 10.x (Blackwell) device");
+    *out = &d;
+    return FA_OK;
+}
+
+// 3-D view [BH][N][d] of a contiguous [B,H,N,d] tensor, box {box_inner, box_rows, 1}.
+fa_status make_map_3d(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const void* base, int d, int N, int BH,
+                      int box_inner, int box_rows, CUtensorMapSwizzle sw) {
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)d * elem_bytes, (cuuint64_t)N * d * elem_bytes};
+    cuuint32_t box[3] = {(cuuint32_t)box_inner, (cuuint32_t)box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return FA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+fa_status check_common(int B, int H, int N, int d, float scale) {
+    if (B <= 0 || H <= 0 || N <= 0) return fail(FA_ERR_INVALID_ARG, "B, H, N must be positive (got %d, %d, %d)", B, H, N);
+    if (!std::isfinite(scale)) return fail(FA_ERR_INVALID_ARG, "scale must be finite");
+    if (d != 64 && d != 128) return fail(FA_ERR_UNSUPPORTED, "head dim %d unsupported (64 or 128)", d);
+    if ((long long)B * H > (1ll << 30) || (long long)B * H * N * d > (1ll << 40))
+        return fail(FA_ERR_INVALID_ARG, "problem too large");
+    return FA_OK;
+}
+
+#define FA_CHECK_PTR(p)                                                                         \
+    do {                                                                                        \
+        if (!(p)) return fail(FA_ERR_INVALID_ARG, "%s must not be NULL", #p);                   \
+        if (!aligned16(p)) return fail(FA_ERR_INVALID_ARG, "%s must be 16-byte aligned", #p); \
+    } while (0)
+
+#define FA_TRY(x)                           \
+    do {                                    \
+        fa_status _s = (x);                 \
+        if (_s != FA_OK) return _s;         \
+    } while (0)
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int grid_for_items(long items, int sms) { return (int)(items < sms ? items : sms); }
+
+int bw_grid(const DeviceInfo* dev) { return dev->sms * 8; }
+
+struct BwdLayout {
+    size_t lse2, dvec, dqacc, q, k, v, dout, total;
+};
+
+BwdLayout bwd_layout(fa_dtype dt, int B, int H, int N, int d) {
+    const size_t BH = (size_t)B * H, Np = round_up((size_t)N, 128);
+    BwdLayout L;
+    size_t off = 0;
+    L.lse2 = off; off = round_up(off + BH * Np * 4, 256);
+    L.dvec = off; off = round_up(off + BH * Np * 4, 256);
+    L.dqacc = off; off = round_up(off + BH * Np * d * 4, 256);
+    const size_t nb = BH * N * d * 2;
+    if (dt == FA_F32) {
+        L.q = off; off = round_up(off + nb, 256);
+        L.k = off; off = round_up(off + nb, 256);
+        L.v = off; off = round_up(off + nb, 256);
+        L.dout = off; off = round_up(off + nb, 256);
+    } else {
+        L.q = L.k = L.v = L.dout = 0;
+    }
+    L.total = off;
+    return L;
+}
+
+fa_status fwd_impl(fa_dtype dtype, int block_c, bool fp8, const void* q, const void* k, const void* v, const float* sq,
+                   const float* sk, const float* sv, void* o, float* lse, int B, int H, int N, int d, float scale,
+                   int causal, const int* kv_lens, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    FA_TRY(check_common(B, H, N, d, scale));
+    FA_CHECK_PTR(q);
+    FA_CHECK_PTR(k);
+    FA_CHECK_PTR(v);
+    FA_CHECK_PTR(o);
+    FA_CHECK_PTR(lse);
+    if (fp8) {
+        if (d != 128) return fail(FA_ERR_UNSUPPORTED, "the FP8 forward needs d = 128");
+        FA_CHECK_PTR(sq);
+        FA_CHECK_PTR(sk);
+        FA_CHECK_PTR(sv);
+    }
+    if (block_c != 0 && block_c != 64 && block_c != 128) return fail(FA_ERR_INVALID_ARG, "block_c must be 0, 64 or 128");
+    if (fp8 && block_c == 64) return fail(FA_ERR_UNSUPPORTED, "the FP8 forward uses 128-key blocks");
+    if (dtype != FA_BF16 && dtype != FA_F32) return fail(FA_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+    DeviceInfo* dev = nullptr;
+    FA_TRY(device_info(&dev));
+    const int BH = B * H;
+    const size_t n = (size_t)BH * N * d;
+    const void *qb = q, *kb = k, *vb = v;
+    if (dtype == FA_F32) {
+        if (workspace_bytes < 3 * round_up(n * 2, 256)) return fail(FA_ERR_INVALID_ARG, "workspace too small");
+        FA_CHECK_PTR(workspace);
+        char* ws = reinterpret_cast<char*>(workspace);
+        void* qc = ws;
+        void* kc = ws + round_up(n * 2, 256);
+        void* vc = ws + 2 * round_up(n * 2, 256);
+        cudaError_t e;
+        if ((e = fa::launch_f32_to_bf16((const float*)q, qc, n, bw_grid(dev), stream)) != cudaSuccess) return cuda_fail(e, "launch");
+        if ((e = fa::launch_f32_to_bf16((const float*)k, kc, n, bw_grid(dev), stream)) != cudaSuccess) return cuda_fail(e, "launch");
+        if ((e = fa::launch_f32_to_bf16((const float*)v, vc, n, bw_grid(dev), stream)) != cudaSuccess) return cuda_fail(e, "launch");
+        qb = qc; kb = kc; vb = vc;
+    }
+    if (block_c == 0) block_c = (N <= 128 && !fp8) ? 64 : 128;
+    CUtensorMap tq, tk, tv;
+    if (fp8) {
+        FA_TRY(make_map_3d(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, qb, d, N, BH, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B));
+        FA_TRY(make_map_3d(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kb, d, N, BH, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B));
+        FA_TRY(make_map_3d(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, vb, d, N, BH, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B));
+    } else {
+        FA_TRY(make_map_3d(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, qb, d, N, BH, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B));
+        FA_TRY(make_map_3d(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kb, d, N, BH, 64, block_c, CU_TENSOR_MAP_SWIZZLE_128B));
+        FA_TRY(make_map_3d(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, vb, d, N, BH, 64, block_c, CU_TENSOR_MAP_SWIZZLE_128B));
+    }
+    fa::FwdParams p;
+    memset(&p, 0, sizeof(p));
+    p.B = B; p.H = H; p.N = N;
+    p.num_qp = (N + 255) / 256;
+    p.num_items = BH * p.num_qp;
+    p.scale = scale;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.kv_lens = kv_lens;
+    p.o = o;
+    p.lse = lse;
+    p.sq = sq; p.sk = sk; p.sv = sv;
+    p.nblk = (N + 63) / 64;
+    p.err = dev->err_word;
+    const int grid = grid_for_items(p.num_items, dev->sms);
+    cudaError_t e;
+    if (fp8)
+        e = fa::launch_fwd_fp8_d128(causal != 0, tq, tk, tv, p, grid, stream);
+    else if (d == 128)
+        e = fa::launch_fwd_bf16_d128(block_c, causal != 0, dtype == FA_F32, tq, tk, tv, p, grid, stream);
+    else
+        e = fa::launch_fwd_bf16_d64(block_c, causal != 0, dtype == FA_F32, tq, tk, tv, p, grid, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "forward launch");
+    return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_version(void) { return (0 << 16) | 1; }
+
+const char* fa_last_error(void) { return t_last_error; }
+
+fa_status fa_check_device_status(fa_stream_t stream) {
+    DeviceInfo* dev = nullptr;
+    FA_TRY(device_info(&dev));
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    unsigned int word = 0;
+    e = cudaMemcpy(&word, dev->err_word, sizeof(word), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+    if (word) {
+        const unsigned int zero = 0;
+        e = cudaMemcpy(dev->err_word, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return cuda_fail(e, "clearing the device error word");
+        return fail(FA_ERR_TIMEOUT, "a kernel pipeline wait timed out (error bits 0x%x)", word);
+    }
+    return FA_OK;
+}
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                 float scale, int causal, const int* kv_lens, fa_stream_t stream) {
+    return fwd_impl(FA_BF16, 0, false, q, k, v, nullptr, nullptr, nullptr, o, lse, B, H, N, d, scale, causal, kv_lens,
+                    nullptr, 0, stream);
+}
+
+size_t fa_fwd_workspace_size(fa_dtype dtype, int B, int H, int N, int d) {
+    if (dtype != FA_F32 || B <= 0 || H <= 0 || N <= 0 || d <= 0) return 0;
+    return 3 * round_up((size_t)B * H * N * d * 2, 256);
+}
+
+fa_status fa_fwd_ex(fa_dtype dtype, int block_c, const void* q, const void* k, const void* v, void* o, float* lse,
+                    int B, int H, int N, int d, float scale, int causal, const int* kv_lens, void* workspace,
+                    size_t workspace_bytes, fa_stream_t stream) {
+    return fwd_impl(dtype, block_c, false, q, k, v, nullptr, nullptr, nullptr, o, lse, B, H, N, d, scale, causal,
+                    kv_lens, workspace, workspace_bytes, stream);
+}
+
+size_t fa_bwd_workspace_size(fa_dtype dtype, int B, int H, int N, int d) {
+    if (B <= 0 || H <= 0 || N <= 0 || (d != 64 && d != 128)) return 0;
+    return bwd_layout(dtype, B, H, N, d).total;
+}
+
+fa_status fa_bwd_ex(fa_dtype dtype, const void* q, const void* k, const void* v, const void* o, const float* lse,
+                    const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal,
+                    const int* kv_lens, void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+    FA_TRY(check_common(B, H, N, d, scale));
+    FA_CHECK_PTR(q);
+    FA_CHECK_PTR(k);
+    FA_CHECK_PTR(v);
+    FA_CHECK_PTR(o);
+    FA_CHECK_PTR(lse);
+    FA_CHECK_PTR(dout);
+    FA_CHECK_PTR(dq);
+    FA_CHECK_PTR(dk);
+    FA_CHECK_PTR(dv);
+    FA_CHECK_PTR(workspace);
+    if (dtype != FA_BF16 && dtype != FA_F32) return fail(FA_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+    const BwdLayout L = bwd_layout(dtype, B, H, N, d);
+    if (workspace_bytes < L.total)
+        return fail(FA_ERR_INVALID_ARG, "workspace too small (%zu < %zu bytes)", workspace_bytes, L.total);
+    DeviceInfo* dev = nullptr;
+    FA_TRY(device_info(&dev));
+    const int BH = B * H;
+    const int Np = (int)round_up((size_t)N, 128);
+    char* ws = reinterpret_cast<char*>(workspace);
+    float* lse2 = reinterpret_cast<float*>(ws + L.lse2);
+    float* dvec = reinterpret_cast<float*>(ws + L.dvec);
+    float* dqacc = reinterpret_cast<float*>(ws + L.dqacc);
+    const void *qb = q, *kb = k, *vb = v, *gb = dout;
+    cudaError_t e;
+    const size_t n = (size_t)BH * N * d;
+    const bool f32 = dtype == FA_F32;
+    if (f32) {
+        if ((e = fa::launch_f32_to_bf16((const float*)q, ws + L.q, n, bw_grid(dev), stream)) != cudaSuccess) return cuda_fail(e, "launch");
+        if ((e = fa::launch_f32_to_bf16((const float*)k, ws + L.k, n, bw_grid(dev), stream)) != cudaSuccess) return cuda_fail(e, "launch");
+        if ((e = fa::launch_f32_to_bf16((const float*)v, ws + L.v, n, bw_grid(dev), stream)) != cudaSuccess) return cuda_fail(e, "launch");
+        if ((e = fa::launch_f32_to_bf16((const float*)dout, ws + L.dout, n, bw_grid(dev), stream)) != cudaSuccess) return cuda_fail(e, "launch");
+        qb = ws + L.q; kb = ws + L.k; vb = ws + L.v; gb = ws + L.dout;
+    }
+    // 1) preprocess: D, LSE*log2(e), zeroed dQ accumulator
+    if ((e = fa::launch_bwd_pre(o, dout, f32, lse, lse2, dvec, dqacc, BH, N, Np, d, bw_grid(dev), stream)) != cudaSuccess)
+        return cuda_fail(e, "backward preprocess launch");
+    // 2) main kernel
+    const int BR = (d == 128) ? 64 : 128;
+    CUtensorMap tq, tk, tv, tdo, tdq;
+    FA_TRY(make_map_3d(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, qb, d, N, BH, 64, BR, CU_TENSOR_MAP_SWIZZLE_128B));
+    FA_TRY(make_map_3d(&tdo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, gb, d, N, BH, 64, BR, CU_TENSOR_MAP_SWIZZLE_128B));
+    FA_TRY(make_map_3d(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kb, d, N, BH, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B));
+    FA_TRY(make_map_3d(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, vb, d, N, BH, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B));
+    {
+        cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)BH * Np};
+        cuuint64_t strides[1] = {(cuuint64_t)d * 4};
+        cuuint32_t box[2] = {32, 64};
+        cuuint32_t estr[2] = {1, 1};
+        CUresult r = g_encode(&tdq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, dqacc, dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled (dQ accumulator) failed (%d)", (int)r);
+    }
+    fa::BwdParams p;
+    memset(&p, 0, sizeof(p));
+    p.B = B; p.H = H; p.N = N; p.Np = Np;
+    p.num_kt = (N + 127) / 128;
+    p.num_items = BH * p.num_kt;
+    p.scale = scale;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.kv_lens = kv_lens;
+    p.lse2 = lse2;
+    p.dvec = dvec;
+    p.dq_acc = dqacc;
+    p.dk = dk;
+    p.dv = dv;
+    p.err = dev->err_word;
+    if ((e = fa::launch_bwd_main(d, causal != 0, f32, tq, tk, tv, tdo, tdq, p, grid_for_items(p.num_items, dev->sms),
+                                 stream)) != cudaSuccess)
+        return cuda_fail(e, "backward main launch");
+    // 3) dQ = scale * dQ_acc
+    if ((e = fa::launch_bwd_dq(dqacc, dq, f32, scale, BH, N, Np, d, bw_grid(dev), stream)) != cudaSuccess)
+        return cuda_fail(e, "dQ conversion launch");
+    return FA_OK;
+}
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                 void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal, const int* kv_lens,
+                 void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+    return fa_bwd_ex(FA_BF16, q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, causal, kv_lens, workspace,
+                     workspace_bytes, stream);
+}
+
+int fa_fp8_num_blocks(int N) { return N > 0 ? (N + 63) / 64 : 0; }
+
+fa_status fa_quantize_fp8(const void* x_bf16, void* x_e4m3, float* scales, int B, int H, int N, int d,
+                          fa_stream_t stream) {
+    FA_TRY(check_common(B, H, N, d, 1.0f));
+    FA_CHECK_PTR(x_bf16);
+    FA_CHECK_PTR(x_e4m3);
+    FA_CHECK_PTR(scales);
+    DeviceInfo* dev = nullptr;
+    FA_TRY(device_info(&dev));
+    cudaError_t e = fa::launch_quantize_fp8(x_bf16, x_e4m3, scales, B * H, N, d, dev->sms * 4, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "quantiser launch");
+    return FA_OK;
+}
+
+fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* sq, const float* sk,
+                     const float* sv, void* o, float* lse, int B, int H, int N, int d, float scale, int causal,
+                     const int* kv_lens, fa_stream_t stream) {
+    return fwd_impl(FA_BF16, 128, true, q8, k8, v8, sq, sk, sv, o, lse, B, H, N, d, scale, causal, kv_lens, nullptr, 0,
+                    stream);
+}
+
+}  // extern "C"

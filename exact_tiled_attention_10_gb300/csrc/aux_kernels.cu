@@ -1,0 +1,199 @@
+// Bandwidth-bound kernels around the two tensor-core kernels:
+//   * backward preprocess: D_i = rowsum(dO_i * O_i) (FA-v2 analysis page §5.2,
+//     attention-kernels wiki §04 "D_i = G_i . O_i"), the saved LSE moved to the
+//     log2 domain (+inf on rows with no visible key and on padding rows, so
+//     the backward's P is exactly 0 there), and the zeroed float32 dQ
+//     accumulator;
+//   * dQ conversion: dQ = scale * dQ_acc (the 1/sqrt(d) of wiki §04);
+//   * FP8 E4M3 per-block quantiser (chapter 18 §18.6.2: s = max|X| / 448);
+//   * float32 -> bf16 rounding of inputs for the float32 entry points.
+// All use 16-byte vector accesses and grid-stride loops over a grid sized in
+// multiples of the SM count.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace fa {
+namespace {
+
+__device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 t = __bfloat1622float2(h[i]);
+        f[2 * i] = t.x;
+        f[2 * i + 1] = t.y;
+    }
+}
+
+// One group of LPR lanes per row; each lane covers 8 consecutive elements.
+template <int D, bool IN_F32>
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const void* __restrict__ o, const void* __restrict__ dout,
+                                                      const float* __restrict__ lse, float* __restrict__ lse2,
+                                                      float* __restrict__ dvec, float* __restrict__ dq_acc, int BH,
+                                                      int N, int Np) {
+    constexpr int LPR = D / 8;                 // lanes per row
+    constexpr int RPW = 32 / LPR;              // rows per warp
+    const int lane = threadIdx.x & 31;
+    const int sub = lane / LPR, sl = lane % LPR;
+    const long total_rows = (long)BH * Np;
+    const long warps = (long)gridDim.x * (blockDim.x / 32);
+    const long gw = (long)blockIdx.x * (blockDim.x / 32) + (threadIdx.x / 32);
+    for (long r0 = gw * RPW; r0 < total_rows; r0 += warps * RPW) {
+        const long r = r0 + sub;
+        const bool valid_row = r < total_rows;
+        const long bh = valid_row ? r / Np : 0;
+        const int i = valid_row ? (int)(r - bh * Np) : 0;
+        float acc = 0.f;
+        if (valid_row && i < N) {
+            const size_t e = ((size_t)bh * N + i) * D + sl * 8;
+            float a[8], b[8];
+            if constexpr (IN_F32) {
+                const float4* po = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(o) + e);
+                const float4* pg = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(dout) + e);
+                const float4 o0 = __ldg(po), o1 = __ldg(po + 1), g0 = __ldg(pg), g1 = __ldg(pg + 1);
+                a[0] = o0.x; a[1] = o0.y; a[2] = o0.z; a[3] = o0.w; a[4] = o1.x; a[5] = o1.y; a[6] = o1.z; a[7] = o1.w;
+                b[0] = g0.x; b[1] = g0.y; b[2] = g0.z; b[3] = g0.w; b[4] = g1.x; b[5] = g1.y; b[6] = g1.z; b[7] = g1.w;
+            } else {
+                unpack8(__ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(o) + e)), a);
+                unpack8(__ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(dout) + e)), b);
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k) acc = fmaf(a[k], b[k], acc);
+        }
+#pragma unroll
+        for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (valid_row) {
+            float* qa = dq_acc + (size_t)r * D + sl * 8;
+            reinterpret_cast<float4*>(qa)[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+            reinterpret_cast<float4*>(qa)[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (sl == 0) {
+                float l2 = INFINITY;
+                if (i < N) {
+                    const float L = lse[(size_t)bh * N + i];
+                    l2 = (L == -INFINITY) ? INFINITY : L * 1.4426950408889634f;
+                }
+                lse2[r] = l2;
+                dvec[r] = (i < N) ? acc : 0.f;
+            }
+        }
+    }
+}
+
+// dQ[r, :] = scale * dQ_acc[r, :] for the N real rows of every head.
+template <bool OUT_F32>
+__global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ acc, void* __restrict__ dq, float scale,
+                                                     int BH, int N, int Np, int D) {
+    const long groups_per_row = D / 8;
+    const long total = (long)BH * N * groups_per_row;
+    for (long g = (long)blockIdx.x * blockDim.x + threadIdx.x; g < total; g += (long)gridDim.x * blockDim.x) {
+        const long row = g / groups_per_row;
+        const int c = (int)(g - row * groups_per_row) * 8;
+        const long bh = row / N;
+        const long i = row - bh * N;
+        const float4* src = reinterpret_cast<const float4*>(acc + ((size_t)bh * Np + i) * D + c);
+        const float4 a = __ldg(src), b = __ldg(src + 1);
+        const size_t e = (size_t)row * D + c;
+        if constexpr (OUT_F32) {
+            float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(dq) + e);
+            dst[0] = make_float4(a.x * scale, a.y * scale, a.z * scale, a.w * scale);
+            dst[1] = make_float4(b.x * scale, b.y * scale, b.z * scale, b.w * scale);
+        } else {
+            *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(dq) + e) =
+                make_uint4(pack_bf16x2(a.x * scale, a.y * scale), pack_bf16x2(a.z * scale, a.w * scale),
+                           pack_bf16x2(b.x * scale, b.y * scale), pack_bf16x2(b.z * scale, b.w * scale));
+        }
+    }
+}
+
+// One CTA (256 threads) per (head, 64-row block); d = 128 -> 8192 elements,
+// 32 per thread.  s = amax / 448 and x / s are IEEE float32 divisions; the
+// conversion rounds to nearest even and saturates to +-448.
+__global__ void __launch_bounds__(256) quantize_fp8_kernel(const __nv_bfloat16* __restrict__ x,
+                                                           uint8_t* __restrict__ x8, float* __restrict__ scales,
+                                                           int BH, int N, int D, int nblk) {
+    __shared__ float red[8];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int per_row = D / 8;  // uint4 groups per row
+    const int groups = 64 * per_row;
+    for (long blk = blockIdx.x; blk < (long)BH * nblk; blk += gridDim.x) {
+        const long bh = blk / nblk;
+        const int ib = (int)(blk - bh * nblk);
+        const int r0 = ib * 64;
+        const int rows = min(64, N - r0);
+        const size_t base = ((size_t)bh * N + r0) * D;
+        float amax = 0.f;
+        for (int g = threadIdx.x; g < rows * per_row; g += blockDim.x) {
+            float f[8];
+            unpack8(__ldg(reinterpret_cast<const uint4*>(x + base) + g), f);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fabsf(f[k]));
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+        if (lane == 0) red[warp] = amax;
+        __syncthreads();
+        float m = red[0];
+#pragma unroll
+        for (int w = 1; w < 8; ++w) m = fmaxf(m, red[w]);
+        const float s = (m > 0.f) ? __fdiv_rn(m, 448.f) : 1.f;
+        if (threadIdx.x == 0) scales[blk] = s;
+        for (int g = threadIdx.x; g < rows * per_row; g += blockDim.x) {
+            float f[8];
+            unpack8(__ldg(reinterpret_cast<const uint4*>(x + base) + g), f);
+            uint2 out;
+            out.x = pack_e4m3x4(__fdiv_rn(f[0], s), __fdiv_rn(f[1], s), __fdiv_rn(f[2], s), __fdiv_rn(f[3], s));
+            out.y = pack_e4m3x4(__fdiv_rn(f[4], s), __fdiv_rn(f[5], s), __fdiv_rn(f[6], s), __fdiv_rn(f[7], s));
+            reinterpret_cast<uint2*>(x8 + base)[g] = out;
+        }
+        __syncthreads();  // red[] is reused by the next block
+        (void)groups;
+    }
+}
+
+__global__ void __launch_bounds__(256) f32_to_bf16_kernel(const float* __restrict__ x, __nv_bfloat16* __restrict__ y,
+                                                          size_t n8) {
+    for (size_t g = (size_t)blockIdx.x * blockDim.x + threadIdx.x; g < n8; g += (size_t)gridDim.x * blockDim.x) {
+        const float4 a = __ldg(reinterpret_cast<const float4*>(x) + 2 * g);
+        const float4 b = __ldg(reinterpret_cast<const float4*>(x) + 2 * g + 1);
+        reinterpret_cast<uint4*>(y)[g] =
+            make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y), pack_bf16x2(b.z, b.w));
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_pre(const void* o, const void* dout, bool in_f32, const float* lse, float* lse2, float* dvec,
+                           float* dq_acc, int BH, int N, int Np, int d, int grid, cudaStream_t s) {
+    if (d == 128) {
+        if (in_f32) bwd_pre_kernel<128, true><<<grid, 256, 0, s>>>(o, dout, lse, lse2, dvec, dq_acc, BH, N, Np);
+        else bwd_pre_kernel<128, false><<<grid, 256, 0, s>>>(o, dout, lse, lse2, dvec, dq_acc, BH, N, Np);
+    } else {
+        if (in_f32) bwd_pre_kernel<64, true><<<grid, 256, 0, s>>>(o, dout, lse, lse2, dvec, dq_acc, BH, N, Np);
+        else bwd_pre_kernel<64, false><<<grid, 256, 0, s>>>(o, dout, lse, lse2, dvec, dq_acc, BH, N, Np);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dq(const float* dq_acc, void* dq, bool out_f32, float scale, int BH, int N, int Np, int d,
+                          int grid, cudaStream_t s) {
+    if (out_f32) bwd_dq_kernel<true><<<grid, 256, 0, s>>>(dq_acc, dq, scale, BH, N, Np, d);
+    else bwd_dq_kernel<false><<<grid, 256, 0, s>>>(dq_acc, dq, scale, BH, N, Np, d);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_fp8(const void* x, void* x8, float* scales, int BH, int N, int d, int grid,
+                                cudaStream_t s) {
+    const int nblk = (N + 63) / 64;
+    quantize_fp8_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(x), reinterpret_cast<uint8_t*>(x8),
+                                             scales, BH, N, d, nblk);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_f32_to_bf16(const float* x, void* y, size_t n, int grid, cudaStream_t s) {
+    f32_to_bf16_kernel<<<grid, 256, 0, s>>>(x, reinterpret_cast<__nv_bfloat16*>(y), n / 8);
+    return cudaGetLastError();
+}
+
+}  // namespace fa

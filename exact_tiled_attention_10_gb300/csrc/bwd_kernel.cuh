@@ -1,0 +1,529 @@
+// Persistent backward kernel of exact tiled attention for sm_103a.
+//
+// What it computes is Algorithm 2 of the FA-v2 analysis page
+// ("解析 FlashAttention（4）：FlashAttention-v2", §5.4), in that page's loop
+// order: the outer loop over key/value blocks j is the CTA work item, the inner
+// loop walks query blocks i.  Per (i, j):
+//   P  = exp(S - L_i)            S = scale Q_i K_j^T (masked), L_i = saved LSE
+//   dV_j += P^T dO_i
+//   dP = dO_i V_j^T
+//   dS = P (dP - D_i)            D_i = rowsum(dO_i O_i), from the preprocess
+//   dQ_i += dS K_j               (reduced into a float32 accumulator)
+//   dK_j += dS^T Q_i
+// with the 1/sqrt(d) factor of the attention-kernels wiki §04 applied to dK in
+// the epilogue and to dQ in the conversion kernel.  Rows with LSE = -inf
+// (no visible key) carry L*log2(e) = +inf so their P is exactly 0.
+//
+// GB300 mapping (one CTA per SM, persistent over (head, key block) items):
+//   * the key block (128 keys) is the M = 128 side of every MMA, so K_j, V_j
+//     stay in shared memory and dK_j, dV_j accumulate in TMEM for the item;
+//   * S^T = K_j Q_i^T and dP^T = V_j dO_i^T land in TMEM with one key per lane;
+//   * two compute warpgroups (warps 0-3, 4-7) each own half of the query
+//     columns: P^T goes back to TMEM (bf16, aliased on S^T) as the A operand of
+//     dV += P^T dO_i; dS^T is written to shared memory in the 128-byte-swizzle
+//     layout, which serves both as the K-major A operand of dK += dS^T Q_i and
+//     as the MN-major operand of the dQ product;
+//   * d = 128: dQ_i^T = K_j^T dS^T (M = 128 head-dim lanes, N = 64 queries);
+//     d = 64:  dQ_i = dS K_j (M = 128 query lanes, N = 64).  Either way all
+//     MMAs have M = 128;
+//   * warps 8-11 drain the dQ tile from TMEM into shared memory and add it to
+//     the float32 accumulator with asynchronous bulk reductions (TMA), each
+//     warp independently;
+//   * warp 12 issues TMA loads (K_j, V_j once per item; a 2-stage ring of
+//     Q_i, dO_i and the row statistics), warp 13 issues tcgen05.mma.
+#pragma once
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace fa {
+namespace bwd {
+
+constexpr int kThreads = 448;
+constexpr int kDqWarp0 = 8;
+constexpr int kProducerWarp = 12;
+constexpr int kMmaWarp = 13;
+
+template <int D_>
+struct Cfg {
+    static constexpr int D = D_;
+    static constexpr int BC = 128;                 // keys per item (TMEM lanes)
+    static constexpr int BR = (D == 128) ? 64 : 128;  // queries per inner step
+    static constexpr int HALF = BR / 2;            // query columns per compute warpgroup
+    static constexpr int ROW_BYTES = D * 2;
+    static constexpr int NBOX = ROW_BYTES / 128;
+    static constexpr int K_BOX = BC * 128, K_TILE = BC * ROW_BYTES;
+    static constexpr int Q_BOX = BR * 128, Q_TILE = BR * ROW_BYTES;
+    static constexpr int DS_BOX = BC * 128, DS_TILE = BC * BR * 2;
+    static constexpr int DQ_WARP_BYTES = 8192;     // per drain warp staging
+    static constexpr int STAGES = 2;
+    // TMEM columns
+    static constexpr int TM_DV = 0, TM_DK = D, TM_S = 2 * D, TM_DP = 2 * D + BR, TM_DQ = 2 * D + 2 * BR;
+    static constexpr int TM_COLS = 512;
+    static_assert(TM_DQ + 64 <= TM_COLS, "TMEM budget");
+    // shared memory map
+    static constexpr int OFF_K = 0;
+    static constexpr int OFF_V = OFF_K + K_TILE;
+    static constexpr int OFF_Q = OFF_V + K_TILE;
+    static constexpr int OFF_DO = OFF_Q + STAGES * Q_TILE;
+    static constexpr int OFF_DS = OFF_DO + STAGES * Q_TILE;
+    static constexpr int OFF_DQ = OFF_DS + 2 * DS_TILE;
+    static constexpr int OFF_STAT = OFF_DQ + 4 * DQ_WARP_BYTES;  // per stage: lse2[BR], D[BR]
+    static constexpr int STAT_BYTES = 2 * BR * 4;
+    static constexpr int OFF_BAR = OFF_STAT + STAGES * STAT_BYTES;
+    static constexpr int B_KVFULL = 0, B_KVEMPTY = 1;
+    static constexpr int B_QFULL = 2, B_QEMPTY = 2 + STAGES;
+    static constexpr int B_SFULL = 2 + 2 * STAGES, B_DPFULL = B_SFULL + 1, B_PFULL = B_SFULL + 2;
+    static constexpr int B_DSFULL = B_SFULL + 3, B_DSEMPTY = B_DSFULL + 2;
+    static constexpr int B_DQFULL = B_DSEMPTY + 2, B_DQEMPTY = B_DQFULL + 1;
+    static constexpr int B_ACCFULL = B_DQEMPTY + 1, B_ACCEMPTY = B_ACCFULL + 1;
+    static constexpr int B_DONE = B_ACCEMPTY + 1;
+    static constexpr int NBAR = B_DONE + 1;
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+    static constexpr int SMEM = OFF_MISC + 16 + 1024;
+    static_assert(SMEM <= 232448, "shared memory budget");
+    static constexpr uint32_t IDESC_S = idesc_make(kFmtBF16, kFmtBF16, 0, 0, 128, BR);   // S^T, dP^T
+    static constexpr uint32_t IDESC_ACC = idesc_make(kFmtBF16, kFmtBF16, 0, 1, 128, D);  // dV, dK
+    static constexpr uint32_t IDESC_DQ = idesc_make(kFmtBF16, kFmtBF16, 1, 1, 128, 64);  // dQ^T / dQ
+};
+
+struct Item {
+    int bh, b, kt, kvl, i0, n;
+};
+
+template <class C, bool CAUSAL>
+__device__ __forceinline__ Item get_item(int it, const BwdParams& p) {
+    Item I;
+    const int BH = p.B * p.H;
+    if (CAUSAL) {  // key blocks near the start see the most query rows: first
+        I.kt = it / BH;
+        I.bh = it % BH;
+    } else {
+        I.bh = it / p.num_kt;
+        I.kt = it % p.num_kt;
+    }
+    I.b = I.bh / p.H;
+    int kvl = p.N;
+    if (p.kv_lens) kvl = min(max(__ldg(p.kv_lens + I.b), 0), p.N);
+    I.kvl = kvl;
+    const int key0 = I.kt * C::BC;
+    const int iend = (p.N + C::BR - 1) / C::BR;
+    I.i0 = CAUSAL ? key0 / C::BR : 0;
+    I.n = (key0 >= kvl) ? 0 : max(iend - I.i0, 0);
+    return I;
+}
+
+template <bool OUT_F32>
+__device__ __forceinline__ void store_chunk32(void* base, size_t elem_off, const float (&v)[32]) {
+    if constexpr (OUT_F32) {
+        float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(base) + elem_off);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+    } else {
+        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(base) + elem_off);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            dst[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                                pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+    }
+}
+
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* m, uint32_t src, int c0, int c1) {
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(m)),
+        "r"(src), "r"(c0), "r"(c1)
+        : "memory");
+}
+
+template <class C, bool CAUSAL, bool OUT_F32>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+               const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+               const __grid_constant__ CUtensorMap tdq, const BwdParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    auto BAR = [&](int i) -> uint32_t { return sbase + C::OFF_BAR + 8 * i; };
+
+    if (threadIdx.x == 0) {
+        mbar_init(BAR(C::B_KVFULL), 1);
+        mbar_init(BAR(C::B_KVEMPTY), 1);
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(BAR(C::B_QFULL + s), 1);
+            mbar_init(BAR(C::B_QEMPTY + s), 1);
+        }
+        mbar_init(BAR(C::B_SFULL), 1);
+        mbar_init(BAR(C::B_DPFULL), 1);
+        mbar_init(BAR(C::B_PFULL), 256);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(BAR(C::B_DSFULL + s), 256);
+            mbar_init(BAR(C::B_DSEMPTY + s), 1);
+        }
+        mbar_init(BAR(C::B_DQFULL), 1);
+        mbar_init(BAR(C::B_DQEMPTY), 128);
+        mbar_init(BAR(C::B_ACCFULL), 1);
+        mbar_init(BAR(C::B_ACCEMPTY), 256);
+        mbar_init(BAR(C::B_DONE), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == kProducerWarp) {
+        tmem_alloc(smem_u32(tmem_slot), C::TM_COLS);
+        tmem_relinquish();
+        if (lane == 0) {
+            prefetch_tmap(&tq);
+            prefetch_tmap(&tk);
+            prefetch_tmap(&tv);
+            prefetch_tmap(&tdo);
+            if (C::D == 128) prefetch_tmap(&tdq);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == kProducerWarp) {
+        // ------------------------------------------------------------ TMA producer
+        int st = 0;
+        uint32_t ph = 0, kve = 0;
+        bool ok = true;
+        for (int it = blockIdx.x; it < p.num_items && ok; it += gridDim.x) {
+            const Item I = get_item<C, CAUSAL>(it, p);
+            if (I.n == 0) continue;
+            if (!(ok = wait_bounded_warp(BAR(C::B_KVEMPTY), kve ^ 1, abort_flag, p.err, kErrWaitBwdProducer))) break;
+            kve ^= 1;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(BAR(C::B_KVFULL), 2 * C::K_TILE);
+                for (int bx = 0; bx < C::NBOX; ++bx) {
+                    tma_load_3d(sbase + C::OFF_K + bx * C::K_BOX, &tk, BAR(C::B_KVFULL), bx * 64, I.kt * C::BC, I.bh);
+                    tma_load_3d(sbase + C::OFF_V + bx * C::K_BOX, &tv, BAR(C::B_KVFULL), bx * 64, I.kt * C::BC, I.bh);
+                }
+            }
+            __syncwarp();
+            for (int s = 0; s < I.n; ++s) {
+                const int i = I.i0 + s;
+                if (!(ok = wait_bounded_warp(BAR(C::B_QEMPTY + st), ph ^ 1, abort_flag, p.err, kErrWaitBwdProducer))) break;
+                if (lane == 0) {
+                    const uint32_t bar = BAR(C::B_QFULL + st);
+                    mbar_arrive_expect_tx(bar, 2 * C::Q_TILE + C::STAT_BYTES);
+                    for (int bx = 0; bx < C::NBOX; ++bx) {
+                        tma_load_3d(sbase + C::OFF_Q + st * C::Q_TILE + bx * C::Q_BOX, &tq, bar, bx * 64, i * C::BR, I.bh);
+                        tma_load_3d(sbase + C::OFF_DO + st * C::Q_TILE + bx * C::Q_BOX, &tdo, bar, bx * 64, i * C::BR, I.bh);
+                    }
+                    const size_t roff = (size_t)I.bh * p.Np + (size_t)i * C::BR;
+                    bulk_load(sbase + C::OFF_STAT + st * C::STAT_BYTES, p.lse2 + roff, C::BR * 4, bar);
+                    bulk_load(sbase + C::OFF_STAT + st * C::STAT_BYTES + C::BR * 4, p.dvec + roff, C::BR * 4, bar);
+                }
+                __syncwarp();
+                if (++st == C::STAGES) { st = 0; ph ^= 1; }
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------ MMA issuer
+        int st = 0, dsb = 0;
+        uint32_t qph = 0, kvph = 0, pph = 0, aeph = 0, dqeph = 0;
+        uint32_t dsph[2] = {0, 0};
+        const bool leader = (lane == 0);
+        const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V;
+        bool ok = true;
+        for (int it = blockIdx.x; it < p.num_items && ok; it += gridDim.x) {
+            const Item I = get_item<C, CAUSAL>(it, p);
+            if (I.n == 0) continue;
+            if (!(ok = wait_bounded_warp(BAR(C::B_KVFULL), kvph, abort_flag, p.err, kErrWaitBwdMma))) break;
+            kvph ^= 1;
+            for (int s = 0; s < I.n; ++s) {
+                const uint32_t sQ = sbase + C::OFF_Q + st * C::Q_TILE;
+                const uint32_t sDO = sbase + C::OFF_DO + st * C::Q_TILE;
+                const uint32_t sDS = sbase + C::OFF_DS + dsb * C::DS_TILE;
+                if (!(ok = wait_bounded_warp(BAR(C::B_QFULL + st), qph, abort_flag, p.err, kErrWaitBwdMma))) break;
+                tc_fence_after();
+                if (leader) {
+                    // S^T = K_j Q_i^T and dP^T = V_j dO_i^T (K-major operands)
+#pragma unroll
+                    for (int kk = 0; kk < C::D / 16; ++kk) {
+                        const uint32_t o = (kk / 4) * C::K_BOX + (kk % 4) * 32;
+                        const uint32_t oq = (kk / 4) * C::Q_BOX + (kk % 4) * 32;
+                        mma_f16_ss(tmem + C::TM_S, sdesc_sw128(sK + o, 16, 1024), sdesc_sw128(sQ + oq, 16, 1024),
+                                   C::IDESC_S, kk > 0);
+                    }
+                    mma_commit(BAR(C::B_SFULL));
+#pragma unroll
+                    for (int kk = 0; kk < C::D / 16; ++kk) {
+                        const uint32_t o = (kk / 4) * C::K_BOX + (kk % 4) * 32;
+                        const uint32_t oq = (kk / 4) * C::Q_BOX + (kk % 4) * 32;
+                        mma_f16_ss(tmem + C::TM_DP, sdesc_sw128(sV + o, 16, 1024), sdesc_sw128(sDO + oq, 16, 1024),
+                                   C::IDESC_S, kk > 0);
+                    }
+                    mma_commit(BAR(C::B_DPFULL));
+                }
+                __syncwarp();
+                // dV_j += P^T dO_i  (P^T from TMEM, dO_i MN-major)
+                if (!(ok = wait_bounded_warp(BAR(C::B_PFULL), pph, abort_flag, p.err, kErrWaitBwdMma))) break;
+                pph ^= 1;
+                if (s == 0) {
+                    if (!(ok = wait_bounded_warp(BAR(C::B_ACCEMPTY), aeph ^ 1, abort_flag, p.err, kErrWaitBwdMma))) break;
+                    aeph ^= 1;
+                }
+                tc_fence_after();
+                if (leader) {
+#pragma unroll
+                    for (int kk = 0; kk < C::BR / 16; ++kk)
+                        mma_f16_ts(tmem + C::TM_DV, tmem + C::TM_S + kk * 8,
+                                   sdesc_sw128(sDO + kk * 2048, C::Q_BOX, 1024), C::IDESC_ACC, (s > 0 || kk > 0));
+                }
+                __syncwarp();
+                // dK_j += dS^T Q_i  (dS^T K-major in smem, Q_i MN-major)
+                if (!(ok = wait_bounded_warp(BAR(C::B_DSFULL + dsb), dsph[dsb], abort_flag, p.err, kErrWaitBwdMma))) break;
+                dsph[dsb] ^= 1;
+                tc_fence_after();
+                if (leader) {
+#pragma unroll
+                    for (int kk = 0; kk < C::BR / 16; ++kk)
+                        mma_f16_ss(tmem + C::TM_DK, sdesc_sw128(sDS + (kk / 4) * C::DS_BOX + (kk % 4) * 32, 16, 1024),
+                                   sdesc_sw128(sQ + kk * 2048, C::Q_BOX, 1024), C::IDESC_ACC, (s > 0 || kk > 0));
+                    mma_commit(BAR(C::B_QEMPTY + st));
+                }
+                __syncwarp();
+                // dQ: d=128 -> dQ^T = K_j^T dS^T ; d=64 -> dQ = dS K_j  (both operands MN-major)
+                if (!(ok = wait_bounded_warp(BAR(C::B_DQEMPTY), dqeph ^ 1, abort_flag, p.err, kErrWaitBwdMma))) break;
+                dqeph ^= 1;
+                tc_fence_after();
+                if (leader) {
+#pragma unroll
+                    for (int kk = 0; kk < C::BC / 16; ++kk) {
+                        const uint64_t dk = sdesc_sw128(sK + kk * 2048, C::K_BOX, 1024);
+                        const uint64_t ds = sdesc_sw128(sDS + kk * 2048, C::DS_BOX, 1024);
+                        if (C::D == 128)
+                            mma_f16_ss(tmem + C::TM_DQ, dk, ds, C::IDESC_DQ, kk > 0);
+                        else
+                            mma_f16_ss(tmem + C::TM_DQ, ds, dk, C::IDESC_DQ, kk > 0);
+                    }
+                    mma_commit(BAR(C::B_DQFULL));
+                    mma_commit(BAR(C::B_DSEMPTY + dsb));
+                }
+                __syncwarp();
+                if (++st == C::STAGES) { st = 0; qph ^= 1; }
+                dsb ^= 1;
+            }
+            if (!ok) break;
+            if (leader) {
+                mma_commit(BAR(C::B_KVEMPTY));
+                mma_commit(BAR(C::B_ACCFULL));
+            }
+            __syncwarp();
+        }
+        if (leader) mma_commit(BAR(C::B_DONE));
+        __syncwarp();
+        wait_bounded_warp(BAR(C::B_DONE), 0, abort_flag, p.err, kErrWaitDrain);
+    } else if (warp < 8) {
+        // ------------------------------------------------------------ compute warpgroups
+        const int h = warp >> 2;  // query-column half
+        const int wq = warp & 3;
+        const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+        const int kr = wq * 32 + lane;  // key row of this thread within the block
+        int st = 0, dsb = 0;
+        uint32_t qph = 0, sph = 0, dpph = 0, acph = 0;
+        uint32_t dseph[2] = {0, 0};
+        bool ok = true;
+        for (int it = blockIdx.x; it < p.num_items && ok; it += gridDim.x) {
+            const Item I = get_item<C, CAUSAL>(it, p);
+            const int key = I.kt * C::BC + kr;
+            const size_t krow = (size_t)I.bh * p.N + key;
+            if (I.n == 0) {  // key block entirely beyond kv_len: zero gradients
+                if (key < p.N) {
+                    float z[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) z[e] = 0.f;
+                    void* dst = h ? p.dk : p.dv;
+#pragma unroll
+                    for (int c = 0; c < C::D; c += 32) store_chunk32<OUT_F32>(dst, krow * C::D + c, z);
+                }
+                continue;
+            }
+            for (int s = 0; s < I.n; ++s) {
+                const int i = I.i0 + s;
+                const int q0 = i * C::BR + h * C::HALF;  // first query column of this half
+                // statistics of this stage (LSE*log2e, D) -- readable once the stage is full
+                if (!(ok = wait_bounded_warp(BAR(C::B_QFULL + st), qph, abort_flag, p.err, kErrWaitBwdCompute))) break;
+                const float* lse2 = reinterpret_cast<const float*>(smem + C::OFF_STAT + st * C::STAT_BYTES) + h * C::HALF;
+                const float* dvec = lse2 + C::BR;
+                if (!(ok = wait_bounded_warp(BAR(C::B_SFULL), sph, abort_flag, p.err, kErrWaitBwdCompute))) break;
+                sph ^= 1;
+                tc_fence_after();
+                uint32_t sr[C::HALF];
+                if constexpr (C::HALF == 32)
+                    tmem_ld32_wait(tmem + lane_off + C::TM_S + h * C::HALF, *reinterpret_cast<uint32_t(*)[32]>(sr));
+                else
+                    tmem_ld64_wait(tmem + lane_off + C::TM_S + h * C::HALF, *reinterpret_cast<uint32_t(*)[64]>(sr));
+                const bool need_mask = (I.kt * C::BC + C::BC > I.kvl) ||
+                                       (CAUSAL && I.kt * C::BC + C::BC - 1 > i * C::BR);
+                const bool key_ok = key < I.kvl;
+                float pv[C::HALF];
+#pragma unroll
+                for (int c = 0; c < C::HALF; c += 4) {
+                    const float4 l4 = *reinterpret_cast<const float4*>(lse2 + c);
+                    pv[c + 0] = ex2_approx(fmaf(__uint_as_float(sr[c + 0]), p.scale_log2, -l4.x));
+                    pv[c + 1] = ex2_approx(fmaf(__uint_as_float(sr[c + 1]), p.scale_log2, -l4.y));
+                    pv[c + 2] = ex2_approx(fmaf(__uint_as_float(sr[c + 2]), p.scale_log2, -l4.z));
+                    pv[c + 3] = ex2_approx(fmaf(__uint_as_float(sr[c + 3]), p.scale_log2, -l4.w));
+                }
+                if (need_mask) {
+#pragma unroll
+                    for (int c = 0; c < C::HALF; ++c) {
+                        const int q = q0 + c;
+                        if (!key_ok || (CAUSAL && key > q)) pv[c] = 0.f;
+                    }
+                }
+                // P^T (bf16) over this half's S^T columns, as the A operand of dV += P^T dO
+                {
+                    uint32_t w[C::HALF / 2];
+#pragma unroll
+                    for (int c = 0; c < C::HALF / 2; ++c) w[c] = pack_bf16x2(pv[2 * c], pv[2 * c + 1]);
+                    const uint32_t tp = tmem + lane_off + C::TM_S + h * (C::HALF / 2);
+                    if constexpr (C::HALF == 32) {
+                        tmem_st16(tp, *reinterpret_cast<uint32_t(*)[16]>(w));
+                    } else {
+                        tmem_st32(tp, *reinterpret_cast<uint32_t(*)[32]>(w));
+                    }
+                    tmem_st_wait();
+                }
+                tc_fence_before();
+                mbar_arrive(BAR(C::B_PFULL));
+                // dS = P (dP - D)
+                if (!(ok = wait_bounded_warp(BAR(C::B_DPFULL), dpph, abort_flag, p.err, kErrWaitBwdCompute))) break;
+                dpph ^= 1;
+                tc_fence_after();
+                if (!(ok = wait_bounded_warp(BAR(C::B_DSEMPTY + dsb), dseph[dsb] ^ 1, abort_flag, p.err, kErrWaitBwdCompute))) break;
+                dseph[dsb] ^= 1;
+                // write dS^T row `kr` (queries h*HALF .. +HALF) into the swizzled tile,
+                // 32 dP columns at a time
+                uint8_t* dsrow = smem + C::OFF_DS + dsb * C::DS_TILE;
+#pragma unroll
+                for (int cc = 0; cc < C::HALF; cc += 32) {
+                    uint32_t dr[32];
+                    tmem_ld32_wait(tmem + lane_off + C::TM_DP + h * C::HALF + cc, dr);
+#pragma unroll
+                    for (int c8 = 0; c8 < 32; c8 += 8) {
+                        const int c = cc + c8;
+                        const int qc = h * C::HALF + c;  // query column within the block
+                        const int box = qc / 64, chunk = (qc % 64) / 8;
+                        const float4 d0 = *reinterpret_cast<const float4*>(dvec + c);
+                        const float4 d1 = *reinterpret_cast<const float4*>(dvec + c + 4);
+                        const float g0 = pv[c + 0] * (__uint_as_float(dr[c8 + 0]) - d0.x);
+                        const float g1 = pv[c + 1] * (__uint_as_float(dr[c8 + 1]) - d0.y);
+                        const float g2 = pv[c + 2] * (__uint_as_float(dr[c8 + 2]) - d0.z);
+                        const float g3 = pv[c + 3] * (__uint_as_float(dr[c8 + 3]) - d0.w);
+                        const float g4 = pv[c + 4] * (__uint_as_float(dr[c8 + 4]) - d1.x);
+                        const float g5 = pv[c + 5] * (__uint_as_float(dr[c8 + 5]) - d1.y);
+                        const float g6 = pv[c + 6] * (__uint_as_float(dr[c8 + 6]) - d1.z);
+                        const float g7 = pv[c + 7] * (__uint_as_float(dr[c8 + 7]) - d1.w);
+                        const uint4 v = make_uint4(pack_bf16x2(g0, g1), pack_bf16x2(g2, g3), pack_bf16x2(g4, g5),
+                                                   pack_bf16x2(g6, g7));
+                        *reinterpret_cast<uint4*>(dsrow + box * C::DS_BOX + kr * 128 + ((chunk ^ (kr & 7)) * 16)) = v;
+                    }
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(BAR(C::B_DSFULL + dsb));
+                if (++st == C::STAGES) { st = 0; qph ^= 1; }
+                dsb ^= 1;
+            }
+            if (!ok) break;
+            // epilogue: warpgroup 0 writes dV_j, warpgroup 1 writes scale * dK_j
+            if (!(ok = wait_bounded_warp(BAR(C::B_ACCFULL), acph, abort_flag, p.err, kErrWaitBwdCompute))) break;
+            acph ^= 1;
+            tc_fence_after();
+            const float mul = h ? p.scale : 1.f;
+            void* dst = h ? p.dk : p.dv;
+            const uint32_t tacc = tmem + lane_off + (h ? C::TM_DK : C::TM_DV);
+#pragma unroll 1
+            for (int c = 0; c < C::D; c += 32) {
+                uint32_t a[32];
+                tmem_ld32_wait(tacc + c, a);
+                float f[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(a[e]) * mul;
+                if (key < p.N) store_chunk32<OUT_F32>(dst, krow * C::D + c, f);
+            }
+            tc_fence_before();
+            mbar_arrive(BAR(C::B_ACCEMPTY));
+        }
+    } else if (warp < 12) {
+        // ------------------------------------------------------------ dQ drain warps
+        const int wq = warp - kDqWarp0;
+        const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+        const uint32_t stage = sbase + C::OFF_DQ + wq * C::DQ_WARP_BYTES;
+        float* stage_f = reinterpret_cast<float*>(smem + C::OFF_DQ + wq * C::DQ_WARP_BYTES);
+        uint32_t dqph = 0;
+        bool ok = true;
+        for (int it = blockIdx.x; it < p.num_items && ok; it += gridDim.x) {
+            const Item I = get_item<C, CAUSAL>(it, p);
+            for (int s = 0; s < I.n; ++s) {
+                const int i = I.i0 + s;
+                if (!(ok = wait_bounded_warp(BAR(C::B_DQFULL), dqph, abort_flag, p.err, kErrWaitBwdDq))) break;
+                dqph ^= 1;
+                tc_fence_after();
+                uint32_t v[64];
+                tmem_ld64_wait(tmem + lane_off + C::TM_DQ, v);
+                tc_fence_before();
+                mbar_arrive(BAR(C::B_DQEMPTY));
+                // the previous reduction of this warp must have finished reading the staging
+                if (lane == 0) bulk_wait_group_read<0>();
+                __syncwarp();
+                if constexpr (C::D == 128) {
+                    // lane = head-dim index (wq*32 + lane); column = query. Stage [64 q][32 d].
+#pragma unroll
+                    for (int q = 0; q < 64; ++q) stage_f[q * 32 + lane] = __uint_as_float(v[q]);
+                } else {
+                    // lane = query (wq*32 + lane); column = head dim. Stage [32 q][64 d], rotated chunks.
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) {
+                        const int c = (k + lane) & 15;
+                        *reinterpret_cast<float4*>(stage_f + lane * 64 + c * 4) =
+                            make_float4(__uint_as_float(v[4 * c]), __uint_as_float(v[4 * c + 1]),
+                                        __uint_as_float(v[4 * c + 2]), __uint_as_float(v[4 * c + 3]));
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    if constexpr (C::D == 128) {
+                        tma_reduce_add_2d(&tdq, stage, wq * 32, I.bh * p.Np + i * C::BR);
+                    } else {
+                        float* dst = p.dq_acc + ((size_t)I.bh * p.Np + (size_t)i * C::BR + wq * 32) * C::D;
+                        bulk_reduce_add_f32(dst, stage, C::DQ_WARP_BYTES);
+                    }
+                    bulk_commit_group();
+                }
+                __syncwarp();
+            }
+        }
+        if (lane == 0) bulk_wait_group<0>();
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kProducerWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TM_COLS);
+    }
+}
+
+template <class C, bool CAUSAL, bool OUT_F32>
+cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                   const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p, int grid,
+                   cudaStream_t stream) {
+    auto kern = bwd_kernel<C, CAUSAL, OUT_F32>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kThreads, C::SMEM, stream>>>(tq, tk, tv, tdo, tdq, p);
+    return cudaGetLastError();
+}
+
+}  // namespace bwd
+}  // namespace fa

@@ -1,0 +1,80 @@
+// Shared definitions of the device code: kernel parameter blocks, device error
+// codes and the launch entry points the C ABI layer calls.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace fa {
+
+// Bits of the device error word (set by a kernel whose pipeline wait timed out).
+enum : unsigned int {
+    kErrWaitFwdProducer = 1u << 0,
+    kErrWaitFwdMma = 1u << 1,
+    kErrWaitFwdSoftmax = 1u << 2,
+    kErrWaitBwdProducer = 1u << 3,
+    kErrWaitBwdMma = 1u << 4,
+    kErrWaitBwdCompute = 1u << 5,
+    kErrWaitBwdDq = 1u << 6,
+    kErrWaitDrain = 1u << 7,
+};
+
+constexpr int kNumSMsDefault = 152;
+
+struct FwdParams {
+    int B, H, N;
+    int num_qp;       // query-row pairs of 128-row tiles per head: ceil(N / 256)
+    int num_items;    // B * H * num_qp
+    float scale;      // softmax scale applied to Q K^T
+    float scale_log2; // scale * log2(e)
+    const int* kv_lens;
+    void* o;          // [B,H,N,d] bf16 or f32
+    float* lse;       // [B,H,N]
+    const float* sq;  // FP8 only: per-64-row-block scales [B,H,nblk]
+    const float* sk;
+    const float* sv;
+    int nblk;         // ceil(N / 64)
+    unsigned int* err;
+};
+
+struct BwdParams {
+    int B, H, N, Np;  // Np: N padded to a multiple of 128
+    int num_kt;       // key tiles per head: ceil(N / 128)
+    int num_items;    // B * H * num_kt
+    float scale;
+    float scale_log2;
+    const int* kv_lens;
+    const float* lse2;  // [B,H,Np] LSE * log2(e), +inf on rows with no visible key / padding
+    const float* dvec;  // [B,H,Np] D = rowsum(dO * O)
+    float* dq_acc;      // [B,H,Np,d] float32 accumulator (unscaled)
+    void* dk;           // [B,H,N,d]
+    void* dv;
+    unsigned int* err;
+};
+
+// Launch helpers implemented in the kernel translation units.  They return a
+// cudaError_t from the launch itself.
+cudaError_t launch_fwd_bf16_d64(int block_c, bool causal, bool out_f32, const CUtensorMap& tq,
+                                const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
+                                int grid, cudaStream_t stream);
+cudaError_t launch_fwd_bf16_d128(int block_c, bool causal, bool out_f32, const CUtensorMap& tq,
+                                 const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
+                                 int grid, cudaStream_t stream);
+cudaError_t launch_fwd_fp8_d128(bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
+                                const CUtensorMap& tv, const FwdParams& p, int grid,
+                                cudaStream_t stream);
+cudaError_t launch_bwd_main(int d, bool causal, bool out_f32, const CUtensorMap& tq,
+                            const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
+                            const CUtensorMap& tdq, const BwdParams& p, int grid,
+                            cudaStream_t stream);
+cudaError_t launch_bwd_pre(const void* o, const void* dout, bool in_f32, const float* lse,
+                           float* lse2, float* dvec, float* dq_acc, int BH, int N, int Np, int d,
+                           int grid, cudaStream_t stream);
+cudaError_t launch_bwd_dq(const float* dq_acc, void* dq, bool out_f32, float scale, int BH, int N,
+                          int Np, int d, int grid, cudaStream_t stream);
+cudaError_t launch_quantize_fp8(const void* x, void* x8, float* scales, int BH, int N, int d,
+                                int grid, cudaStream_t stream);
+cudaError_t launch_f32_to_bf16(const float* x, void* y, size_t n, int grid, cudaStream_t stream);
+
+}  // namespace fa

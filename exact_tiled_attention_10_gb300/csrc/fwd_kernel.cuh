@@ -1,0 +1,514 @@
+// Persistent forward kernel of exact tiled attention for sm_103a.
+//
+// What it computes is Algorithm 1 of the FA-v2 analysis page
+// ("解析 FlashAttention（4）：FlashAttention-v2", §4): for a block of query rows
+// it walks the key/value blocks keeping, per row, the running maximum m, the
+// running sum l and the unnormalised output O; it rescales the old state by
+// exp(m_old - m_new) (multiplication, as in that page's §2.3 scalar derivation
+// and the running-state formulas of the attention-kernels wiki §01), and
+// finally writes O / l and LSE = m + log l (§4 steps 6-7).  Masks follow
+// chapter 18 §18.2.2 (causal M_ij = -inf for j > i; padding masks columns,
+// Table 18-3); fully masked key blocks are skipped (§18.5.2), and a row with
+// no visible key gets O = 0, LSE = -inf (wiki §04).
+//
+// How it maps onto a GB300 SM (one CTA per SM, persistent over work items):
+//   * a work item is one (batch, head, pair of 128-row query tiles);
+//   * warp 8 (one lane) issues TMA loads of Q (once per item) and a ring of
+//     K and V tiles (128-byte swizzle, one box per 128 bytes of head dim);
+//   * warp 9 (one lane) issues tcgen05.mma: S_t = Q_t K_j^T into TMEM, then
+//     O_t += P_t V_j with P_t read from TMEM, alternating the two query tiles
+//     so the tensor core works on one tile while the other is in softmax;
+//   * warps 0-3 / 4-7 are the softmax warpgroups of tile 0 / tile 1: one
+//     thread per query row (= TMEM lane).  Each loads its S row, applies the
+//     mask on boundary blocks, updates (m, l) in the log2 domain, rescales its
+//     O row in TMEM only when the max grew by more than kRescaleSlack
+//     (conditional rescaling: exact, since O/l and m + log l do not depend on
+//     which reference max was used), writes P = 2^(S*c - m) back over its S
+//     columns as packed bf16 (or E4M3) for the P V MMA, and at the end of the
+//     item normalises O and stores O and LSE.
+//   TMEM (512 columns): S0 | S1 | O0 | O1 (fp32), P_t aliased on S_t.
+//   FP8 variant: Q8 K8 with per-64-row block scales s_q, s_k folded into the
+//   softmax multiplier, V's per-block scale folded into the E4M3 P operand.
+#pragma once
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace fa {
+namespace fwd {
+
+constexpr int kThreads = 384;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+// Conditional rescaling slack in the log2 domain: P values may reach 2^8
+// before the reference max is moved (bf16 path).  The FP8 path keeps the exact
+// max so that P <= 1 fits the E4M3 range after the value-scale fold.
+constexpr float kRescaleSlack = 8.0f;
+
+template <int D_, int BC_, bool FP8_>
+struct Cfg {
+    static constexpr int D = D_;
+    static constexpr int BC = BC_;
+    static constexpr bool FP8 = FP8_;
+    static constexpr int BR = 128;   // query rows per tile (= TMEM lanes)
+    static constexpr int QT = 2;     // query tiles per CTA work item
+    static constexpr int ELEM = FP8 ? 1 : 2;
+    static constexpr int ROW_BYTES = D * ELEM;
+    static constexpr int NBOX = ROW_BYTES / 128;  // 128-byte swizzle boxes along d
+    static constexpr int BOX_ELEMS = 128 / ELEM;
+    static constexpr int Q_BOX = BR * 128;
+    static constexpr int KV_BOX = BC * 128;
+    static constexpr int Q_TILE = BR * ROW_BYTES;
+    static constexpr int KV_TILE = BC * ROW_BYTES;
+    static constexpr int STAGES = (KV_TILE >= 32768) ? 2 : 3;
+    static constexpr int KSTEP = 32 / ELEM;         // K elements per MMA instruction
+    static constexpr int S_STEPS = ROW_BYTES / 32;  // MMAs per S tile
+    static constexpr int PV_STEPS = BC / KSTEP;     // MMAs per P V
+    static constexpr int TM_S0 = 0, TM_S1 = BC, TM_O0 = 2 * BC, TM_O1 = 2 * BC + D;
+    static constexpr int TM_COLS = 512;
+    static_assert(2 * BC + 2 * D <= TM_COLS, "TMEM budget");
+    // shared memory map (tile bases 1024-byte aligned)
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_K = OFF_Q + QT * Q_TILE;
+    static constexpr int OFF_V = OFF_K + STAGES * KV_TILE;
+    static constexpr int OFF_BAR = OFF_V + STAGES * KV_TILE;
+    // barrier indices
+    static constexpr int B_QFULL = 0, B_QEMPTY = 1;
+    static constexpr int B_KFULL = 2, B_KEMPTY = 2 + STAGES;
+    static constexpr int B_VFULL = 2 + 2 * STAGES, B_VEMPTY = 2 + 3 * STAGES;
+    static constexpr int B_SFULL = 2 + 4 * STAGES, B_PFULL = B_SFULL + 2;
+    static constexpr int B_OFULL = B_PFULL + 2, B_OEMPTY = B_OFULL + 2;
+    static constexpr int B_DONE = B_OEMPTY + 2;
+    static constexpr int NBAR = B_DONE + 1;
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+    static constexpr int SMEM = OFF_MISC + 16 + 1024;  // + base alignment slack
+    static constexpr uint32_t FMT = FP8 ? kFmtE4M3 : kFmtBF16;
+    static constexpr uint32_t IDESC_S = idesc_make(FMT, FMT, 0, 0, 128, BC);
+    static constexpr uint32_t IDESC_PV = idesc_make(FMT, FMT, 0, 1, 128, D);
+    static_assert(SMEM <= 232448, "shared memory budget");
+};
+
+struct Item {
+    int bh, b, row0, kvl;
+    int n[2];
+    int nmax;
+};
+
+template <class C, bool CAUSAL>
+__device__ __forceinline__ Item get_item(int it, const FwdParams& p) {
+    Item I;
+    const int BH = p.B * p.H;
+    int qp;
+    if (CAUSAL) {  // longest rows first
+        qp = p.num_qp - 1 - it / BH;
+        I.bh = it % BH;
+    } else {
+        qp = it % p.num_qp;
+        I.bh = it / p.num_qp;
+    }
+    I.b = I.bh / p.H;
+    int kvl = p.N;
+    if (p.kv_lens) kvl = min(max(__ldg(p.kv_lens + I.b), 0), p.N);
+    I.kvl = kvl;
+    I.row0 = qp * (C::QT * C::BR);
+    I.nmax = 0;
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        const int r0 = I.row0 + t * C::BR;
+        int n = 0;
+        if (r0 < p.N) {
+            int cols = kvl;
+            if (CAUSAL) cols = min(cols, r0 + C::BR);
+            n = (cols + C::BC - 1) / C::BC;
+        }
+        I.n[t] = n;
+        I.nmax = max(I.nmax, n);
+    }
+    return I;
+}
+
+// S_t = Q_t K^T over the head dimension (both operands K-major, 128B swizzle)
+template <class C>
+__device__ __forceinline__ void issue_S(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
+#pragma unroll
+    for (int kk = 0; kk < C::S_STEPS; ++kk) {
+        const uint32_t off_in = (kk % 4) * 32;
+        const uint64_t a = sdesc_sw128(q_smem + (kk / 4) * C::Q_BOX + off_in, 16, 1024);
+        const uint64_t b = sdesc_sw128(k_smem + (kk / 4) * C::KV_BOX + off_in, 16, 1024);
+        if constexpr (C::FP8)
+            mma_f8_ss(d_tmem, a, b, C::IDESC_S, kk > 0);
+        else
+            mma_f16_ss(d_tmem, a, b, C::IDESC_S, kk > 0);
+    }
+}
+
+// O_t (+)= P_t V over the keys; P_t from TMEM, V MN-major (head dim contiguous)
+template <class C>
+__device__ __forceinline__ void issue_PV(uint32_t o_tmem, uint32_t p_tmem, uint32_t v_smem,
+                                         bool accumulate) {
+#pragma unroll
+    for (int kk = 0; kk < C::PV_STEPS; ++kk) {
+        const uint64_t b = sdesc_sw128(v_smem + kk * C::KSTEP * 128, C::KV_BOX, 1024);
+        if constexpr (C::FP8)
+            mma_f8_ts(o_tmem, p_tmem + kk * 8, b, C::IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
+        else
+            mma_f16_ts(o_tmem, p_tmem + kk * 8, b, C::IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
+    }
+}
+
+template <class C, bool OUT_F32>
+__device__ __forceinline__ void store_row_chunk(void* o_row, int c0, const float (&v)[32]) {
+    if constexpr (OUT_F32) {
+        float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(o_row) + c0);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+    } else {
+        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(o_row) + c0);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            dst[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                                pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+    }
+}
+
+template <class C, bool CAUSAL, bool OUT_F32>
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+               const __grid_constant__ CUtensorMap tv, const FwdParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    auto BAR = [&](int i) -> uint32_t { return sbase + C::OFF_BAR + 8 * i; };
+
+    if (threadIdx.x == 0) {
+        mbar_init(BAR(C::B_QFULL), 1);
+        mbar_init(BAR(C::B_QEMPTY), 1);
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(BAR(C::B_KFULL + s), 1);
+            mbar_init(BAR(C::B_KEMPTY + s), 1);
+            mbar_init(BAR(C::B_VFULL + s), 1);
+            mbar_init(BAR(C::B_VEMPTY + s), 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(BAR(C::B_SFULL + t), 1);
+            mbar_init(BAR(C::B_PFULL + t), 128);
+            mbar_init(BAR(C::B_OFULL + t), 1);
+            mbar_init(BAR(C::B_OEMPTY + t), 128);
+        }
+        mbar_init(BAR(C::B_DONE), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == kProducerWarp) {
+        tmem_alloc(smem_u32(tmem_slot), C::TM_COLS);
+        tmem_relinquish();
+        if (lane == 0) {
+            prefetch_tmap(&tq);
+            prefetch_tmap(&tk);
+            prefetch_tmap(&tv);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == kProducerWarp) {
+        // ------------------------------------------------------------ TMA producer
+        // The whole warp walks the schedule (so it stays converged); lane 0 issues.
+        int st = 0;
+        uint32_t ph = 0, qe = 0;
+        bool ok = true;
+        for (int it = blockIdx.x; it < p.num_items && ok; it += gridDim.x) {
+            const Item I = get_item<C, CAUSAL>(it, p);
+            if (I.nmax == 0) continue;
+            if (!(ok = wait_bounded_warp(BAR(C::B_QEMPTY), qe ^ 1, abort_flag, p.err, kErrWaitFwdProducer))) break;
+            qe ^= 1;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(BAR(C::B_QFULL), C::QT * C::Q_TILE);
+                for (int t = 0; t < C::QT; ++t)
+                    for (int bx = 0; bx < C::NBOX; ++bx)
+                        tma_load_3d(sbase + C::OFF_Q + t * C::Q_TILE + bx * C::Q_BOX, &tq, BAR(C::B_QFULL),
+                                    bx * C::BOX_ELEMS, I.row0 + t * C::BR, I.bh);
+            }
+            __syncwarp();
+            for (int j = 0; j < I.nmax; ++j) {
+                if (!(ok = wait_bounded_warp(BAR(C::B_KEMPTY + st), ph ^ 1, abort_flag, p.err, kErrWaitFwdProducer))) break;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(BAR(C::B_KFULL + st), C::KV_TILE);
+                    for (int bx = 0; bx < C::NBOX; ++bx)
+                        tma_load_3d(sbase + C::OFF_K + st * C::KV_TILE + bx * C::KV_BOX, &tk, BAR(C::B_KFULL + st),
+                                    bx * C::BOX_ELEMS, j * C::BC, I.bh);
+                }
+                __syncwarp();
+                if (!(ok = wait_bounded_warp(BAR(C::B_VEMPTY + st), ph ^ 1, abort_flag, p.err, kErrWaitFwdProducer))) break;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(BAR(C::B_VFULL + st), C::KV_TILE);
+                    for (int bx = 0; bx < C::NBOX; ++bx)
+                        tma_load_3d(sbase + C::OFF_V + st * C::KV_TILE + bx * C::KV_BOX, &tv, BAR(C::B_VFULL + st),
+                                    bx * C::BOX_ELEMS, j * C::BC, I.bh);
+                }
+                __syncwarp();
+                if (++st == C::STAGES) { st = 0; ph ^= 1; }
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------ MMA issuer
+        // The whole warp walks the schedule and waits; lane 0 issues tcgen05.
+        int kst = 0, vst = 0;
+        uint32_t kph = 0, vph = 0, qph = 0;
+        uint32_t pph[2] = {0, 0}, oeph[2] = {0, 0};
+        const uint32_t tS[2] = {tmem + C::TM_S0, tmem + C::TM_S1};
+        const uint32_t tO[2] = {tmem + C::TM_O0, tmem + C::TM_O1};
+        const bool leader = (lane == 0);
+        bool ok = true;
+        for (int it = blockIdx.x; it < p.num_items && ok; it += gridDim.x) {
+            const Item I = get_item<C, CAUSAL>(it, p);
+            if (I.nmax == 0) continue;
+            if (!(ok = wait_bounded_warp(BAR(C::B_QFULL), qph, abort_flag, p.err, kErrWaitFwdMma))) break;
+            qph ^= 1;
+            if (!(ok = wait_bounded_warp(BAR(C::B_KFULL + kst), kph, abort_flag, p.err, kErrWaitFwdMma))) break;
+            tc_fence_after();
+            if (leader) {
+                for (int t = 0; t < 2; ++t)
+                    if (I.n[t] > 0) {
+                        issue_S<C>(tS[t], sbase + C::OFF_Q + t * C::Q_TILE, sbase + C::OFF_K + kst * C::KV_TILE);
+                        mma_commit(BAR(C::B_SFULL + t));
+                    }
+                mma_commit(BAR(C::B_KEMPTY + kst));
+            }
+            __syncwarp();
+            if (++kst == C::STAGES) { kst = 0; kph ^= 1; }
+            for (int j = 0; j < I.nmax && ok; ++j) {
+                bool vw = false, kw = false;
+                for (int t = 0; t < 2; ++t) {
+                    if (j >= I.n[t]) continue;
+                    if (!(ok = wait_bounded_warp(BAR(C::B_PFULL + t), pph[t], abort_flag, p.err, kErrWaitFwdMma))) break;
+                    pph[t] ^= 1;
+                    if (j == 0) {
+                        if (!(ok = wait_bounded_warp(BAR(C::B_OEMPTY + t), oeph[t] ^ 1, abort_flag, p.err, kErrWaitFwdMma))) break;
+                        oeph[t] ^= 1;
+                    }
+                    if (!vw) {
+                        if (!(ok = wait_bounded_warp(BAR(C::B_VFULL + vst), vph, abort_flag, p.err, kErrWaitFwdMma))) break;
+                        vw = true;
+                    }
+                    tc_fence_after();
+                    if (leader) issue_PV<C>(tO[t], tS[t], sbase + C::OFF_V + vst * C::KV_TILE, j > 0);
+                    if (j == I.n[t] - 1) {
+                        if (leader) mma_commit(BAR(C::B_OFULL + t));
+                    } else {
+                        if (!kw) {
+                            if (!(ok = wait_bounded_warp(BAR(C::B_KFULL + kst), kph, abort_flag, p.err, kErrWaitFwdMma))) break;
+                            kw = true;
+                            tc_fence_after();
+                        }
+                        if (leader) {
+                            issue_S<C>(tS[t], sbase + C::OFF_Q + t * C::Q_TILE, sbase + C::OFF_K + kst * C::KV_TILE);
+                            mma_commit(BAR(C::B_SFULL + t));
+                        }
+                    }
+                    __syncwarp();
+                }
+                if (!ok) break;
+                if (leader) mma_commit(BAR(C::B_VEMPTY + vst));
+                if (++vst == C::STAGES) { vst = 0; vph ^= 1; }
+                if (kw) {
+                    if (leader) mma_commit(BAR(C::B_KEMPTY + kst));
+                    if (++kst == C::STAGES) { kst = 0; kph ^= 1; }
+                }
+                __syncwarp();
+            }
+            if (!ok) break;
+            if (leader) mma_commit(BAR(C::B_QEMPTY));
+            __syncwarp();
+        }
+        // drain: every MMA this warp issued has completed before TMEM is freed
+        if (leader) mma_commit(BAR(C::B_DONE));
+        __syncwarp();
+        wait_bounded_warp(BAR(C::B_DONE), 0, abort_flag, p.err, kErrWaitDrain);
+    } else if (warp < 8) {
+        // ------------------------------------------------------------ softmax
+        const int t = warp >> 2;
+        const int wq = warp & 3;
+        const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+        const uint32_t tS = tmem + lane_off + (t ? C::TM_S1 : C::TM_S0);
+        const uint32_t tO = tmem + lane_off + (t ? C::TM_O1 : C::TM_O0);
+        const int r_in = wq * 32 + lane;
+        uint32_t sph = 0, oph = 0;
+        for (int it = blockIdx.x; it < p.num_items; it += gridDim.x) {
+            const Item I = get_item<C, CAUSAL>(it, p);
+            const int n = I.n[t];
+            const int tile_row0 = I.row0 + t * C::BR;
+            const int row = tile_row0 + r_in;
+            const size_t row_idx = (size_t)I.bh * p.N + row;
+            if (n == 0) {
+                if (row < p.N) {  // no visible key (kv_len = 0): O = 0, LSE = -inf
+                    float z[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) z[i] = 0.f;
+                    char* orow = reinterpret_cast<char*>(p.o) + row_idx * C::D * (OUT_F32 ? 4 : 2);
+#pragma unroll
+                    for (int c = 0; c < C::D; c += 32) store_row_chunk<C, OUT_F32>(orow, c, z);
+                    p.lse[row_idx] = -INFINITY;
+                }
+                continue;
+            }
+            // FP8: per-row query scale and the head's largest value-block scale
+            float sq_row = 1.f, sv_max = 1.f;
+            if (C::FP8) {
+                const float* svh = p.sv + (size_t)I.bh * p.nblk;
+                float mxs = 0.f;
+                for (int i = lane; i < p.nblk; i += 32) mxs = fmaxf(mxs, __ldg(svh + i));
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) mxs = fmaxf(mxs, __shfl_xor_sync(0xffffffffu, mxs, o));
+                sv_max = mxs;
+                if (row < p.N) sq_row = __ldg(p.sq + (size_t)I.bh * p.nblk + row / 64);
+            }
+            float m = -INFINITY, l = 0.f;
+            bool ok = true;
+            for (int j = 0; j < n; ++j) {
+                if (!(ok = wait_bounded_warp(BAR(C::B_SFULL + t), sph, abort_flag, p.err, kErrWaitFwdSoftmax))) break;
+                sph ^= 1;
+                tc_fence_after();
+                uint32_t sr[C::BC];
+                if constexpr (C::BC == 128) {
+                    tmem_ld128_wait(tS, sr);
+                } else {
+                    tmem_ld64_wait(tS, sr);
+                }
+                float s[C::BC];
+#pragma unroll
+                for (int c = 0; c < C::BC; ++c) s[c] = __uint_as_float(sr[c]);
+                const int col0 = j * C::BC;
+                const bool need_mask = (col0 + C::BC > I.kvl) || (CAUSAL && col0 + C::BC - 1 > tile_row0);
+                if (need_mask) {
+#pragma unroll
+                    for (int c = 0; c < C::BC; ++c) {
+                        const int col = col0 + c;
+                        if (col >= I.kvl || (CAUSAL && col > row)) s[c] = -INFINITY;
+                    }
+                }
+                // multipliers of the raw scores (log2 domain) per 64-key half
+                float cm[2], lg[2] = {0.f, 0.f}, inv_w[2] = {1.f, 1.f};
+                if (C::FP8) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int blk = j * 2 + h;
+                        const float skb = (blk < p.nblk) ? __ldg(p.sk + (size_t)I.bh * p.nblk + blk) : 1.f;
+                        const float svb = (blk < p.nblk) ? __ldg(p.sv + (size_t)I.bh * p.nblk + blk) : sv_max;
+                        cm[h] = p.scale_log2 * sq_row * skb;
+                        const float w = svb / sv_max * 448.f;
+                        lg[h] = __log2f(w);
+                        inv_w[h] = 1.f / w;
+                    }
+                } else {
+                    cm[0] = cm[1] = p.scale_log2;
+                }
+                float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < C::BC / 2; ++c) mx0 = fmaxf(mx0, s[c]);
+#pragma unroll
+                for (int c = C::BC / 2; c < C::BC; ++c) mx1 = fmaxf(mx1, s[c]);
+                const float mx2 = fmaxf(mx0 * cm[0], mx1 * cm[1]);
+                const float slack = C::FP8 ? 0.f : kRescaleSlack;
+                const bool need = mx2 > m + slack;
+                float alpha = 1.f;
+                if (need) {
+                    alpha = ex2_approx(m - mx2);  // 0 when m = -inf
+                    m = mx2;
+                    l *= alpha;
+                }
+                if (j > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll 1
+                    for (int c = 0; c < C::D; c += 32) {
+                        uint32_t ov[32];
+                        tmem_ld32_wait(tO + c, ov);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+                        tmem_st32(tO + c, ov);
+                    }
+                    tmem_st_wait();
+                }
+                const float mb = (m == -INFINITY) ? 0.f : m;
+                float lsum = 0.f;
+                constexpr int CH = C::FP8 ? 64 : 32;  // columns per 16-word TMEM store
+#pragma unroll
+                for (int ch = 0; ch < C::BC / CH; ++ch) {
+                    const int h = (ch * CH) / (C::BC / 2);
+                    const float cs = cm[h], cb = lg[h] - mb;
+                    uint32_t w[16];
+                    float acc0 = 0.f, acc1 = 0.f;
+                    if constexpr (C::FP8) {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const float p0 = ex2_approx(fmaf(s[ch * CH + 4 * e + 0], cs, cb));
+                            const float p1 = ex2_approx(fmaf(s[ch * CH + 4 * e + 1], cs, cb));
+                            const float p2 = ex2_approx(fmaf(s[ch * CH + 4 * e + 2], cs, cb));
+                            const float p3 = ex2_approx(fmaf(s[ch * CH + 4 * e + 3], cs, cb));
+                            acc0 += p0 + p1;
+                            acc1 += p2 + p3;
+                            w[e] = pack_e4m3x4(p0, p1, p2, p3);
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const float p0 = ex2_approx(fmaf(s[ch * CH + 2 * e + 0], cs, cb));
+                            const float p1 = ex2_approx(fmaf(s[ch * CH + 2 * e + 1], cs, cb));
+                            acc0 += p0;
+                            acc1 += p1;
+                            w[e] = pack_bf16x2(p0, p1);
+                        }
+                    }
+                    lsum += (acc0 + acc1) * inv_w[h];
+                    tmem_st16(tS + ch * 16, w);
+                }
+                l += lsum;
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(BAR(C::B_PFULL + t));
+            }
+            if (!ok) break;
+            if (!wait_bounded_warp(BAR(C::B_OFULL + t), oph, abort_flag, p.err, kErrWaitFwdSoftmax)) break;
+            oph ^= 1;
+            tc_fence_after();
+            float inv = (l > 0.f) ? 1.f / l : 0.f;
+            if (C::FP8) inv *= sv_max * (1.f / 448.f);
+            char* orow = reinterpret_cast<char*>(p.o) + row_idx * C::D * (OUT_F32 ? 4 : 2);
+#pragma unroll 1
+            for (int c = 0; c < C::D; c += 32) {
+                uint32_t ov[32];
+                tmem_ld32_wait(tO + c, ov);
+                float f[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(ov[i]) * inv;
+                if (row < p.N) store_row_chunk<C, OUT_F32>(orow, c, f);
+            }
+            tc_fence_before();
+            mbar_arrive(BAR(C::B_OEMPTY + t));
+            if (row < p.N) p.lse[row_idx] = (l > 0.f) ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kProducerWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TM_COLS);
+    }
+}
+
+template <class C, bool CAUSAL, bool OUT_F32>
+cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                   const FwdParams& p, int grid, cudaStream_t stream) {
+    auto kern = fwd_kernel<C, CAUSAL, OUT_F32>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kThreads, C::SMEM, stream>>>(tq, tk, tv, p);
+    return cudaGetLastError();
+}
+
+}  // namespace fwd
+}  // namespace fa

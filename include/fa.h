@@ -1,0 +1,149 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) exact tiled attention library.
+ *
+ * Exact multi-head attention O = softmax(scale * Q K^T + M) V computed tile by
+ * tile: the forward keeps a per-row online-softmax state and writes only O and
+ * the per-row log-sum-exp; the backward rebuilds each probability tile from
+ * that log-sum-exp.  Sources (titles of the pages the method is taken from):
+ *   [FA2]  "解析 FlashAttention（4）：FlashAttention-v2" -- §4 Algorithm 1
+ *          (forward), §5.2 (D = rowsum(dO*O)), §5.4 Algorithm 2 (backward).
+ *   [WIKI] "分块 Attention：重建概率，累计梯度" -- §01 running state, §04
+ *          gradients with 1/sqrt(d) on dQ and dK, fully-masked-row convention.
+ *   [CH18] "第18章 FlashAttention" -- §18.2.2 causal mask M_ij = -inf for
+ *          j > i and the padding (column) mask of Table 18-3; §18.6.2 FP8
+ *          E4M3 with per-block scale s = max|X| / 448; §18.7.1 API
+ *          (softmax_scale defaults to 1/sqrt(headdim), causal in-kernel).
+ *
+ * Common conventions for every entry point
+ * ----------------------------------------
+ *  * Tensors are DEVICE pointers owned by the caller, contiguous row-major:
+ *      q, k, v, o, dout, dq, dk, dv : [B, H, N, d]
+ *      lse                          : [B, H, N] float32, natural log of the
+ *                                     scaled scores; -inf on a fully masked row
+ *      kv_lens                      : [B] int32 on the device, or NULL (= N).
+ *    Every pointer must be 16-byte aligned (TMA requirement).
+ *  * Masking: key j is visible to query i iff j < kv_lens[b] and, when
+ *    causal != 0, j <= i (top-left aligned, N_q = N_k).  kv_lens[b] outside
+ *    [0, N] is clamped to that range.  A query row with no visible key gets
+ *    O = 0, LSE = -inf and zero gradients ([WIKI] §04).
+ *  * scale multiplies Q K^T; pass 1/sqrt(d) for standard attention.
+ *  * d must be 64 or 128 (bf16 paths); 128 for the FP8 path.  N >= 1.
+ *  * Calls are asynchronous on `stream` and never synchronise.  Argument
+ *    errors are detected on the host and returned before any launch; launch
+ *    failures return FA_ERR_CUDA.  Faults detected inside a kernel (a
+ *    pipeline wait that exceeded its time limit) set a device error word that
+ *    fa_check_device_status() reports as FA_ERR_TIMEOUT.
+ *  * The library allocates no device memory.  Scratch memory is passed in by
+ *    the caller as `workspace` (sizes from the *_workspace_size queries).
+ *  * On any non-OK status, fa_last_error() returns a message (thread-local).
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned pointer, ... */
+    FA_ERR_UNSUPPORTED = 2, /* head dim / dtype / device not supported        */
+    FA_ERR_CUDA = 3,        /* a CUDA runtime or driver call failed            */
+    FA_ERR_TIMEOUT = 4      /* a kernel gave up waiting (device error word)    */
+} fa_status;
+
+typedef enum { FA_BF16 = 0, FA_F32 = 1 } fa_dtype;
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* fa_stream_t;
+
+/* Library version, (major << 16) | minor. */
+int fa_version(void);
+
+/* Thread-local description of the last non-OK status ("" if none). */
+const char* fa_last_error(void);
+
+/* Waits for `stream`, then reads and clears the device error word.  Returns
+ * FA_ERR_TIMEOUT if a kernel recorded a timed-out pipeline wait since the last
+ * call, FA_ERR_CUDA if the stream itself reports an error, else FA_OK. */
+fa_status fa_check_device_status(fa_stream_t stream);
+
+/* ---------------------------------------------------------------- forward */
+
+/* bf16 forward ([FA2] §4 Algorithm 1).  q,k,v: bf16 inputs; o: bf16 output;
+ * lse: float32 [B,H,N].  Tiles of 128 query rows x 128 keys (64 keys when
+ * N <= 128). */
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                 int B, int H, int N, int d, float scale, int causal,
+                 const int* kv_lens, fa_stream_t stream);
+
+/* Extended forward.
+ *   dtype   FA_BF16: as fa_fwd.  FA_F32: q,k,v,o are float32; inputs are
+ *           rounded to bf16 (round-to-nearest-even) into `workspace`, the
+ *           tensor cores compute in bf16 with fp32 accumulation, and O is
+ *           written as float32.
+ *   block_c 0 = automatic, or 64 / 128 keys per tile.
+ *   workspace, workspace_bytes: at least fa_fwd_workspace_size(dtype,...)
+ *           bytes of device memory (NULL allowed when that size is 0). */
+size_t fa_fwd_workspace_size(fa_dtype dtype, int B, int H, int N, int d);
+fa_status fa_fwd_ex(fa_dtype dtype, int block_c, const void* q, const void* k, const void* v,
+                    void* o, float* lse, int B, int H, int N, int d, float scale, int causal,
+                    const int* kv_lens, void* workspace, size_t workspace_bytes,
+                    fa_stream_t stream);
+
+/* --------------------------------------------------------------- backward */
+
+/* Scratch for fa_bwd / fa_bwd_ex, in bytes: the row statistics
+ * LSE*log2(e) and D = rowsum(dO*O) ([FA2] §5.2), 2 x [B,H,Np] float32, plus
+ * the float32 dQ accumulator [B,H,Np,d] (Np = N rounded up to a multiple of
+ * 128), plus, for FA_F32, bf16 copies of q, k, v, o and dout. */
+size_t fa_bwd_workspace_size(fa_dtype dtype, int B, int H, int N, int d);
+
+/* bf16 backward of L = sum(O * dout) ([FA2] §5.4 Algorithm 2; [WIKI] §04):
+ * given q, k, v, the forward's o and lse and the upstream gradient dout,
+ * writes dq, dk, dv (bf16, overwritten, not accumulated).  Launches three
+ * kernels on `stream`: preprocess (D and zeroed dQ accumulator), the main
+ * kernel parallel over key blocks, and the dQ conversion. */
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o,
+                 const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                 int B, int H, int N, int d, float scale, int causal, const int* kv_lens,
+                 void* workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/* As fa_bwd with an element type: FA_F32 takes float32 q,k,v,o,dout and writes
+ * float32 dq,dk,dv (the tensor cores see bf16-rounded copies). */
+fa_status fa_bwd_ex(fa_dtype dtype, const void* q, const void* k, const void* v, const void* o,
+                    const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                    int B, int H, int N, int d, float scale, int causal, const int* kv_lens,
+                    void* workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/* -------------------------------------------------------------------- FP8 */
+
+/* Number of 64-row scale blocks per (b,h): ceil(N / 64). */
+int fa_fp8_num_blocks(int N);
+
+/* Per-block E4M3 quantisation ([CH18] §18.6.2).  For each (b, h) and each
+ * block of 64 consecutive rows x all d columns: amax = max|x|, s = amax / 448
+ * (s = 1 when amax = 0), x8 = E4M3(x / s) with round-to-nearest-even and
+ * saturation to +-448 (division and rounding in float32).
+ *   x_bf16: bf16 [B,H,N,d]; x_e4m3: uint8 [B,H,N,d]; scales: float32
+ *   [B,H,fa_fp8_num_blocks(N)]. */
+fa_status fa_quantize_fp8(const void* x_bf16, void* x_e4m3, float* scales,
+                          int B, int H, int N, int d, fa_stream_t stream);
+
+/* FP8 forward: q8/k8/v8 are E4M3 [B,H,N,d] with per-64-row-block scales
+ * sq/sk/sv (as written by fa_quantize_fp8), so that X ~= s_block * X8.
+ * S = scale * (s_q s_k) (Q8 K8^T) accumulates in float32; the softmax runs in
+ * float32; the probabilities are re-quantised to E4M3 (with the value scale of
+ * each key block folded in) for the P V product; O is written as bf16 and LSE
+ * as float32.  d must be 128. */
+fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* v8,
+                     const float* sq, const float* sk, const float* sv,
+                     void* o, float* lse, int B, int H, int N, int d, float scale,
+                     int causal, const int* kv_lens, fa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FA_GB300_H */

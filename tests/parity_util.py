@@ -1,0 +1,54 @@
+"""Helpers shared by the GPU parity tests: run the CUDA path and the oracle on
+the same seeded, bf16-rounded inputs and compare with the stated tolerances.
+
+Tolerances (from the method's accuracy targets for bf16 inputs with float32
+accumulation):  O max-abs <= 1e-2, LSE max-abs <= 1e-3,
+dQ/dK/dV max-abs <= 2e-2 * max|dX| (the oracle's), FP8 O max-abs <= 6e-2.
+"""
+import numpy as np
+import torch
+
+O_TOL = 1e-2
+LSE_TOL = 1e-3
+GRAD_REL_TOL = 2e-2
+FP8_O_TOL = 6e-2
+
+
+def to64(t):
+    return t.detach().to("cpu").double().numpy()
+
+
+def assert_lse(gpu, ref, tol=LSE_TOL, what="lse"):
+    gpu = np.asarray(gpu, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    ninf_g, ninf_r = np.isneginf(gpu), np.isneginf(ref)
+    assert np.array_equal(ninf_g, ninf_r), "%s: -inf pattern differs (%d vs %d rows)" % (
+        what, ninf_g.sum(), ninf_r.sum())
+    fin = ~ninf_r
+    assert np.all(np.isfinite(gpu[fin])), "%s: non-finite values" % what
+    err = np.max(np.abs(gpu[fin] - ref[fin])) if fin.any() else 0.0
+    assert err <= tol, "%s max-abs error %.3e > %.1e" % (what, err, tol)
+    return err
+
+
+def assert_close_abs(gpu, ref, tol, what):
+    gpu = np.asarray(gpu, dtype=np.float64)
+    assert np.all(np.isfinite(gpu)), "%s: non-finite values" % what
+    err = np.max(np.abs(gpu - ref)) if gpu.size else 0.0
+    assert err <= tol, "%s max-abs error %.3e > %.3e" % (what, err, tol)
+    return err
+
+
+def assert_grad(gpu, ref, what):
+    scale = max(np.max(np.abs(ref)) if ref.size else 0.0, 1e-30)
+    return assert_close_abs(gpu, ref, GRAD_REL_TOL * scale, what)
+
+
+def sample_rows(N, n, seed):
+    """Sorted unique rows: the first, last and both sides of every 64/128 boundary
+    near the start, plus random rows."""
+    rng = np.random.default_rng(seed)
+    fixed = [0, 1, 63, 64, 127, 128, 129, 255, 256, N - 129, N - 128, N - 2, N - 1]
+    rows = set(r for r in fixed if 0 <= r < N)
+    rows.update(rng.integers(0, N, size=n).tolist())
+    return sorted(rows)

@@ -1,0 +1,145 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle, element
+by element on small shapes that span several tiles and ragged tails, and on
+sampled rows at the full workload sizes in the launch configuration the
+benchmark times."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from exact_tiled_attention_10_gb300 import backward, check_device_status, forward
+from exact_tiled_attention_10_gb300.inputs import WORKLOADS, kv_lens_ragged, qkv
+from parity_util import (LSE_TOL, O_TOL, assert_close_abs, assert_grad, assert_lse, sample_rows,
+                         to64)
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _run_full(B, H, N, d, causal, kv=None, dtype=torch.bfloat16, seed=7, block_c=0, do_bwd=True):
+    q, k, v, do = qkv(B, H, N, d, seed, dtype=dtype, device=DEV)
+    kvd = None if kv is None else torch.tensor(kv, dtype=torch.int32, device=DEV)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = forward(q, k, v, causal=causal, scale=scale, kv_lens=kvd, block_c=block_c)
+    if do_bwd:
+        dq, dk, dv = backward(q, k, v, o, lse, do, causal=causal, scale=scale, kv_lens=kvd)
+    torch.cuda.synchronize()
+    check_device_status()
+    kvn = None if kv is None else np.asarray(kv, dtype=np.int32)
+    ref = oracle.bwd(to64(q), to64(k), to64(v), to64(do), scale, causal=causal, kv_lens=kvn)
+    assert_close_abs(to64(o), ref["o"], O_TOL, "O")
+    assert_lse(to64(lse), ref["lse"])
+    if do_bwd:
+        assert_grad(to64(dq), ref["dq"], "dQ")
+        assert_grad(to64(dk), ref["dk"], "dK")
+        assert_grad(to64(dv), ref["dv"], "dV")
+    return ref
+
+
+# ----------------------------------------------------------------- tiny config
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("block_c", [64, 128])
+def test_tiny_config(dtype, causal, block_c):
+    w = WORKLOADS["tiny"]
+    _run_full(w.B, w.H, w.N, w.d, causal, dtype=dtype, seed=w.seed, block_c=block_c)
+
+
+# ------------------------------------------------------ ragged tails, many tiles
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("N", [1, 17, 100, 129, 200, 257, 383, 520])
+@pytest.mark.parametrize("causal", [False, True])
+def test_ragged_lengths(d, N, causal):
+    _run_full(2, 2, N, d, causal, seed=100 + N)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_key_padding(d, causal):
+    N = 300
+    kv = [0, 1, 63, 64, 65, 128, 129, 300]
+    _run_full(len(kv), 2, N, d, causal, kv=kv, seed=31)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("block_c", [64, 128])
+def test_block_sizes_agree(d, block_c):
+    _run_full(1, 3, 640, d, True, seed=5, block_c=block_c, do_bwd=False)
+
+
+def test_repeat_is_consistent():
+    """Two runs of the same backward agree (dQ uses float32 reductions whose
+    order may differ; dK, dV are computed in one CTA and must be bitwise equal)."""
+    q, k, v, do = qkv(2, 4, 1024, 128, 3, device=DEV)
+    o, lse = forward(q, k, v, causal=True)
+    g1 = backward(q, k, v, o, lse, do, causal=True)
+    g2 = backward(q, k, v, o, lse, do, causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(g1[1], g2[1]) and torch.equal(g1[2], g2[2])
+    assert (g1[0].float() - g2[0].float()).abs().max().item() <= 1e-2 * g1[0].float().abs().max().item()
+    o2, lse2 = forward(q, k, v, causal=True)
+    assert torch.equal(o, o2) and torch.equal(lse, lse2)
+
+
+# ------------------------------------------------- full workload sizes, sampled
+def _sampled_check(w, causal, heads, n_rows=48, bwd=True, seed_off=0):
+    q, k, v, do = qkv(w.B, w.H, w.N, w.d, w.seed, device=DEV)
+    kv = kv_lens_ragged(w.B, w.N, w.seed, device=DEV) if w.ragged else None
+    o, lse = forward(q, k, v, causal=causal, kv_lens=kv)
+    if bwd:
+        dq, dk, dv = backward(q, k, v, o, lse, do, causal=causal, kv_lens=kv)
+    torch.cuda.synchronize()
+    check_device_status()
+    assert torch.isfinite(o.float()).all()
+    kvn = None if kv is None else kv.cpu().numpy()
+    for (b, h) in heads:
+        kvl = w.N if kvn is None else int(kvn[b])
+        rows = sample_rows(w.N, n_rows, seed=b * 131 + h + seed_off)
+        qh, kh, vh = to64(q[b, h]), to64(k[b, h]), to64(v[b, h])
+        o_ref, lse_ref = oracle.fwd_rows(qh, kh, vh, w.scale, causal, kvl, rows)
+        assert_close_abs(to64(o[b, h, rows]), o_ref, O_TOL, "O[%d,%d]" % (b, h))
+        assert_lse(to64(lse[b, h, rows]), lse_ref, what="LSE[%d,%d]" % (b, h))
+        if bwd:
+            keys = sample_rows(w.N, n_rows // 2, seed=b * 7 + h + 1 + seed_off)
+            g = oracle.bwd_rows(qh, kh, vh, to64(do[b, h]), w.scale, causal, kvl, rows, keys)
+            assert_grad(to64(dq[b, h, rows]), g["dq"], "dQ[%d,%d]" % (b, h))
+            assert_grad(to64(dk[b, h, keys]), g["dk"], "dK[%d,%d]" % (b, h))
+            assert_grad(to64(dv[b, h, keys]), g["dv"], "dV[%d,%d]" % (b, h))
+    return q, k, v, o, lse
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_mid_config_sampled(causal):
+    w = WORKLOADS["mid"]
+    _sampled_check(w, causal, heads=[(0, 0), (3, 15), (1, 7)])
+
+
+def test_long_head_config_sampled():
+    w = WORKLOADS["long_head"]
+    _sampled_check(w, True, heads=[(0, 0), (1, 15)])
+    _sampled_check(w, False, heads=[(1, 3)], bwd=False, seed_off=5)
+
+
+def test_ragged_config_sampled():
+    w = WORKLOADS["ragged"]
+    q, k, v, o, lse = _sampled_check(w, False, heads=[(1, 0), (5, 17), (7, 31)])
+    # batch item 0 has kv_len = 0: every row fully masked -> O = 0, LSE = -inf, zero grads
+    kv = kv_lens_ragged(w.B, w.N, w.seed, device=DEV)
+    assert int(kv[0]) == 0
+    do = qkv(w.B, w.H, w.N, w.d, w.seed, device=DEV)[3]
+    dq, dk, dv = backward(q, k, v, o, lse, do, kv_lens=kv)
+    torch.cuda.synchronize()
+    assert torch.all(o[0] == 0)
+    assert torch.all(torch.isneginf(lse[0]))
+    assert torch.all(dq[0] == 0) and torch.all(dk[0] == 0) and torch.all(dv[0] == 0)
+    # keys beyond kv_len get exactly zero dK, dV
+    for b in range(1, w.B):
+        L = int(kv[b])
+        assert torch.all(dk[b, :, L:] == 0) and torch.all(dv[b, :, L:] == 0)
+
+
+def test_long_seq_config_sampled():
+    w = WORKLOADS["long_seq"]
+    _sampled_check(w, True, heads=[(0, 0), (0, 5)], n_rows=32)
