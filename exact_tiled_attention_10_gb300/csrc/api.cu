@@ -169,30 +169,43 @@ fa_status fwd_impl(fa_dtype dtype, int block_c, bool fp8, const void* q, const v
     FA_TRY(device_info(&dev));
     const int BH = B * H;
     const size_t n = (size_t)BH * N * d;
-    const void *qb = q, *kb = k, *vb = v;
-    if (dtype == FA_F32) {
-        if (workspace_bytes < 3 * round_up(n * 2, 256)) return fail(FA_ERR_INVALID_ARG, "workspace too small");
+    const bool split = (dtype == FA_F32);
+    const void *qb = q, *kb = k, *vb = v, *qlo = q, *klo = k;
+    if (split) {
+        // float32 inputs: q, k as bf16 hi + lo parts (scores from three bf16
+        // products), v rounded to bf16
+        const size_t part = round_up(n * 2, 256);
+        if (workspace_bytes < 5 * part) return fail(FA_ERR_INVALID_ARG, "workspace too small");
         FA_CHECK_PTR(workspace);
         char* ws = reinterpret_cast<char*>(workspace);
-        void* qc = ws;
-        void* kc = ws + round_up(n * 2, 256);
-        void* vc = ws + 2 * round_up(n * 2, 256);
         cudaError_t e;
-        if ((e = fa::launch_f32_to_bf16((const float*)q, qc, n, bw_grid(dev), stream)) != cudaSuccess) return cuda_fail(e, "launch");
-        if ((e = fa::launch_f32_to_bf16((const float*)k, kc, n, bw_grid(dev), stream)) != cudaSuccess) return cuda_fail(e, "launch");
-        if ((e = fa::launch_f32_to_bf16((const float*)v, vc, n, bw_grid(dev), stream)) != cudaSuccess) return cuda_fail(e, "launch");
-        qb = qc; kb = kc; vb = vc;
+        if ((e = fa::launch_f32_split_bf16((const float*)q, ws, ws + part, n, bw_grid(dev), stream)) != cudaSuccess)
+            return cuda_fail(e, "float32 split launch");
+        if ((e = fa::launch_f32_split_bf16((const float*)k, ws + 2 * part, ws + 3 * part, n, bw_grid(dev), stream)) !=
+            cudaSuccess)
+            return cuda_fail(e, "float32 split launch");
+        if ((e = fa::launch_f32_to_bf16((const float*)v, ws + 4 * part, n, bw_grid(dev), stream)) != cudaSuccess)
+            return cuda_fail(e, "float32 -> bf16 launch");
+        qb = ws; qlo = ws + part; kb = ws + 2 * part; klo = ws + 3 * part; vb = ws + 4 * part;
+        if (d == 128 && block_c == 128)
+            return fail(FA_ERR_UNSUPPORTED, "float32 inputs with d = 128 use 64-key blocks");
+        if (block_c == 0) block_c = (d == 128 || N <= 128) ? 64 : 128;
     }
     if (block_c == 0) block_c = (N <= 128 && !fp8) ? 64 : 128;
-    CUtensorMap tq, tk, tv;
+    fa::FwdMaps m;
     if (fp8) {
-        FA_TRY(make_map_3d(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, qb, d, N, BH, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B));
-        FA_TRY(make_map_3d(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kb, d, N, BH, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B));
-        FA_TRY(make_map_3d(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, vb, d, N, BH, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B));
+        FA_TRY(make_map_3d(&m.q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, qb, d, N, BH, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B));
+        FA_TRY(make_map_3d(&m.k, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kb, d, N, BH, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B));
+        FA_TRY(make_map_3d(&m.v, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, vb, d, N, BH, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B));
+        m.q_lo = m.q;
+        m.k_lo = m.k;
     } else {
-        FA_TRY(make_map_3d(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, qb, d, N, BH, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B));
-        FA_TRY(make_map_3d(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kb, d, N, BH, 64, block_c, CU_TENSOR_MAP_SWIZZLE_128B));
-        FA_TRY(make_map_3d(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, vb, d, N, BH, 64, block_c, CU_TENSOR_MAP_SWIZZLE_128B));
+        const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+        FA_TRY(make_map_3d(&m.q, bf, 2, qb, d, N, BH, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B));
+        FA_TRY(make_map_3d(&m.k, bf, 2, kb, d, N, BH, 64, block_c, CU_TENSOR_MAP_SWIZZLE_128B));
+        FA_TRY(make_map_3d(&m.v, bf, 2, vb, d, N, BH, 64, block_c, CU_TENSOR_MAP_SWIZZLE_128B));
+        FA_TRY(make_map_3d(&m.q_lo, bf, 2, qlo, d, N, BH, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B));
+        FA_TRY(make_map_3d(&m.k_lo, bf, 2, klo, d, N, BH, 64, block_c, CU_TENSOR_MAP_SWIZZLE_128B));
     }
     fa::FwdParams p;
     memset(&p, 0, sizeof(p));
@@ -210,11 +223,11 @@ fa_status fwd_impl(fa_dtype dtype, int block_c, bool fp8, const void* q, const v
     const int grid = grid_for_items(p.num_items, dev->sms);
     cudaError_t e;
     if (fp8)
-        e = fa::launch_fwd_fp8_d128(causal != 0, tq, tk, tv, p, grid, stream);
+        e = fa::launch_fwd_fp8_d128(causal != 0, m, p, grid, stream);
     else if (d == 128)
-        e = fa::launch_fwd_bf16_d128(block_c, causal != 0, dtype == FA_F32, tq, tk, tv, p, grid, stream);
+        e = fa::launch_fwd_bf16_d128(block_c, causal != 0, dtype == FA_F32, split, m, p, grid, stream);
     else
-        e = fa::launch_fwd_bf16_d64(block_c, causal != 0, dtype == FA_F32, tq, tk, tv, p, grid, stream);
+        e = fa::launch_fwd_bf16_d64(block_c, causal != 0, dtype == FA_F32, split, m, p, grid, stream);
     if (e != cudaSuccess) return cuda_fail(e, "forward launch");
     return FA_OK;
 }
@@ -252,7 +265,7 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
 
 size_t fa_fwd_workspace_size(fa_dtype dtype, int B, int H, int N, int d) {
     if (dtype != FA_F32 || B <= 0 || H <= 0 || N <= 0 || d <= 0) return 0;
-    return 3 * round_up((size_t)B * H * N * d * 2, 256);
+    return 5 * round_up((size_t)B * H * N * d * 2, 256);
 }
 
 fa_status fa_fwd_ex(fa_dtype dtype, int block_c, const void* q, const void* k, const void* v, void* o, float* lse,
@@ -267,47 +280,47 @@ size_t fa_bwd_workspace_size(fa_dtype dtype, int B, int H, int N, int d) {
     return bwd_layout(dtype, B, H, N, d).total;
 }
 
-fa_status fa_bwd_ex(fa_dtype dtype, const void* q, const void* k, const void* v, const void* o, const float* lse,
-                    const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal,
-                    const int* kv_lens, void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+struct BwdCtx {
+    DeviceInfo* dev;
+    BwdLayout L;
+    int BH, Np;
+    char* ws;
+};
+
+fa_status bwd_setup(fa_dtype dtype, int B, int H, int N, int d, float scale, void* workspace, size_t workspace_bytes,
+                    BwdCtx* c) {
     FA_TRY(check_common(B, H, N, d, scale));
-    FA_CHECK_PTR(q);
-    FA_CHECK_PTR(k);
-    FA_CHECK_PTR(v);
-    FA_CHECK_PTR(o);
-    FA_CHECK_PTR(lse);
-    FA_CHECK_PTR(dout);
-    FA_CHECK_PTR(dq);
-    FA_CHECK_PTR(dk);
-    FA_CHECK_PTR(dv);
     FA_CHECK_PTR(workspace);
     if (dtype != FA_BF16 && dtype != FA_F32) return fail(FA_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
-    const BwdLayout L = bwd_layout(dtype, B, H, N, d);
-    if (workspace_bytes < L.total)
-        return fail(FA_ERR_INVALID_ARG, "workspace too small (%zu < %zu bytes)", workspace_bytes, L.total);
-    DeviceInfo* dev = nullptr;
-    FA_TRY(device_info(&dev));
-    const int BH = B * H;
-    const int Np = (int)round_up((size_t)N, 128);
-    char* ws = reinterpret_cast<char*>(workspace);
-    float* lse2 = reinterpret_cast<float*>(ws + L.lse2);
-    float* dvec = reinterpret_cast<float*>(ws + L.dvec);
-    float* dqacc = reinterpret_cast<float*>(ws + L.dqacc);
-    const void *qb = q, *kb = k, *vb = v, *gb = dout;
-    cudaError_t e;
-    const size_t n = (size_t)BH * N * d;
-    const bool f32 = dtype == FA_F32;
-    if (f32) {
-        if ((e = fa::launch_f32_to_bf16((const float*)q, ws + L.q, n, bw_grid(dev), stream)) != cudaSuccess) return cuda_fail(e, "launch");
-        if ((e = fa::launch_f32_to_bf16((const float*)k, ws + L.k, n, bw_grid(dev), stream)) != cudaSuccess) return cuda_fail(e, "launch");
-        if ((e = fa::launch_f32_to_bf16((const float*)v, ws + L.v, n, bw_grid(dev), stream)) != cudaSuccess) return cuda_fail(e, "launch");
-        if ((e = fa::launch_f32_to_bf16((const float*)dout, ws + L.dout, n, bw_grid(dev), stream)) != cudaSuccess) return cuda_fail(e, "launch");
-        qb = ws + L.q; kb = ws + L.k; vb = ws + L.v; gb = ws + L.dout;
-    }
-    // 1) preprocess: D, LSE*log2(e), zeroed dQ accumulator
-    if ((e = fa::launch_bwd_pre(o, dout, f32, lse, lse2, dvec, dqacc, BH, N, Np, d, bw_grid(dev), stream)) != cudaSuccess)
-        return cuda_fail(e, "backward preprocess launch");
-    // 2) main kernel
+    c->L = bwd_layout(dtype, B, H, N, d);
+    if (workspace_bytes < c->L.total)
+        return fail(FA_ERR_INVALID_ARG, "workspace too small (%zu < %zu bytes)", workspace_bytes, c->L.total);
+    FA_TRY(device_info(&c->dev));
+    c->BH = B * H;
+    c->Np = (int)round_up((size_t)N, 128);
+    c->ws = reinterpret_cast<char*>(workspace);
+    return FA_OK;
+}
+
+fa_status bwd_pre_impl(const BwdCtx& c, bool f32, const void* o, const float* lse, const void* dout, int N, int d,
+                       cudaStream_t stream) {
+    cudaError_t e = fa::launch_bwd_pre(o, dout, f32, lse, reinterpret_cast<float*>(c.ws + c.L.lse2),
+                                       reinterpret_cast<float*>(c.ws + c.L.dvec),
+                                       reinterpret_cast<float*>(c.ws + c.L.dqacc), c.BH, N, c.Np, d, bw_grid(c.dev),
+                                       stream);
+    if (e != cudaSuccess) return cuda_fail(e, "backward preprocess launch");
+    return FA_OK;
+}
+
+fa_status bwd_main_impl(const BwdCtx& c, bool f32, const void* qb, const void* kb, const void* vb, const void* gb,
+                        void* dk, void* dv, int B, int H, int N, int d, float scale, int causal, const int* kv_lens,
+                        cudaStream_t stream) {
+    const int BH = c.BH, Np = c.Np;
+    float* dqacc = reinterpret_cast<float*>(c.ws + c.L.dqacc);
     const int BR = (d == 128) ? 64 : 128;
     CUtensorMap tq, tk, tv, tdo, tdq;
     FA_TRY(make_map_3d(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, qb, d, N, BH, 64, BR, CU_TENSOR_MAP_SWIZZLE_128B));
@@ -332,19 +345,90 @@ fa_status fa_bwd_ex(fa_dtype dtype, const void* q, const void* k, const void* v,
     p.scale = scale;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.kv_lens = kv_lens;
-    p.lse2 = lse2;
-    p.dvec = dvec;
+    p.lse2 = reinterpret_cast<float*>(c.ws + c.L.lse2);
+    p.dvec = reinterpret_cast<float*>(c.ws + c.L.dvec);
     p.dq_acc = dqacc;
     p.dk = dk;
     p.dv = dv;
-    p.err = dev->err_word;
-    if ((e = fa::launch_bwd_main(d, causal != 0, f32, tq, tk, tv, tdo, tdq, p, grid_for_items(p.num_items, dev->sms),
-                                 stream)) != cudaSuccess)
-        return cuda_fail(e, "backward main launch");
-    // 3) dQ = scale * dQ_acc
-    if ((e = fa::launch_bwd_dq(dqacc, dq, f32, scale, BH, N, Np, d, bw_grid(dev), stream)) != cudaSuccess)
-        return cuda_fail(e, "dQ conversion launch");
+    p.err = c.dev->err_word;
+    cudaError_t e = fa::launch_bwd_main(d, causal != 0, f32, tq, tk, tv, tdo, tdq, p,
+                                        grid_for_items(p.num_items, c.dev->sms), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "backward main launch");
     return FA_OK;
+}
+
+fa_status bwd_dq_impl(const BwdCtx& c, bool f32, void* dq, int N, int d, float scale, cudaStream_t stream) {
+    cudaError_t e = fa::launch_bwd_dq(reinterpret_cast<float*>(c.ws + c.L.dqacc), dq, f32, scale, c.BH, N, c.Np, d,
+                                      bw_grid(c.dev), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "dQ conversion launch");
+    return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+fa_status fa_bwd_preprocess(const void* o, const float* lse, const void* dout, int B, int H, int N, int d,
+                            void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+    FA_CHECK_PTR(o);
+    FA_CHECK_PTR(lse);
+    FA_CHECK_PTR(dout);
+    BwdCtx c;
+    FA_TRY(bwd_setup(FA_BF16, B, H, N, d, 1.0f, workspace, workspace_bytes, &c));
+    return bwd_pre_impl(c, false, o, lse, dout, N, d, stream);
+}
+
+fa_status fa_bwd_main(const void* q, const void* k, const void* v, const void* dout, void* dk, void* dv, int B, int H,
+                      int N, int d, float scale, int causal, const int* kv_lens, void* workspace,
+                      size_t workspace_bytes, fa_stream_t stream) {
+    FA_CHECK_PTR(q);
+    FA_CHECK_PTR(k);
+    FA_CHECK_PTR(v);
+    FA_CHECK_PTR(dout);
+    FA_CHECK_PTR(dk);
+    FA_CHECK_PTR(dv);
+    BwdCtx c;
+    FA_TRY(bwd_setup(FA_BF16, B, H, N, d, scale, workspace, workspace_bytes, &c));
+    return bwd_main_impl(c, false, q, k, v, dout, dk, dv, B, H, N, d, scale, causal, kv_lens, stream);
+}
+
+fa_status fa_bwd_dq(void* dq, int B, int H, int N, int d, float scale, void* workspace, size_t workspace_bytes,
+                    fa_stream_t stream) {
+    FA_CHECK_PTR(dq);
+    BwdCtx c;
+    FA_TRY(bwd_setup(FA_BF16, B, H, N, d, scale, workspace, workspace_bytes, &c));
+    return bwd_dq_impl(c, false, dq, N, d, scale, stream);
+}
+
+fa_status fa_bwd_ex(fa_dtype dtype, const void* q, const void* k, const void* v, const void* o, const float* lse,
+                    const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal,
+                    const int* kv_lens, void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+    FA_CHECK_PTR(q);
+    FA_CHECK_PTR(k);
+    FA_CHECK_PTR(v);
+    FA_CHECK_PTR(o);
+    FA_CHECK_PTR(lse);
+    FA_CHECK_PTR(dout);
+    FA_CHECK_PTR(dq);
+    FA_CHECK_PTR(dk);
+    FA_CHECK_PTR(dv);
+    BwdCtx c;
+    FA_TRY(bwd_setup(dtype, B, H, N, d, scale, workspace, workspace_bytes, &c));
+    const bool f32 = dtype == FA_F32;
+    const void *qb = q, *kb = k, *vb = v, *gb = dout;
+    if (f32) {
+        const size_t n = (size_t)c.BH * N * d;
+        const void* src[4] = {q, k, v, dout};
+        const size_t dst[4] = {c.L.q, c.L.k, c.L.v, c.L.dout};
+        for (int i = 0; i < 4; ++i) {
+            cudaError_t e = fa::launch_f32_to_bf16((const float*)src[i], c.ws + dst[i], n, bw_grid(c.dev), stream);
+            if (e != cudaSuccess) return cuda_fail(e, "float32 -> bf16 launch");
+        }
+        qb = c.ws + c.L.q; kb = c.ws + c.L.k; vb = c.ws + c.L.v; gb = c.ws + c.L.dout;
+    }
+    FA_TRY(bwd_pre_impl(c, f32, o, lse, dout, N, d, stream));
+    FA_TRY(bwd_main_impl(c, f32, qb, kb, vb, gb, dk, dv, B, H, N, d, scale, causal, kv_lens, stream));
+    return bwd_dq_impl(c, f32, dq, N, d, scale, stream);
 }
 
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,

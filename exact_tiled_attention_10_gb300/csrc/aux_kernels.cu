@@ -162,7 +162,34 @@ __global__ void __launch_bounds__(256) f32_to_bf16_kernel(const float* __restric
     }
 }
 
+// x = hi + lo with hi = bf16(x), lo = bf16(x - hi): the pair carries ~16
+// significant bits, enough for float32-accurate scores from bf16 products.
+__global__ void __launch_bounds__(256) f32_split_kernel(const float* __restrict__ x, __nv_bfloat16* __restrict__ hi,
+                                                        __nv_bfloat16* __restrict__ lo, size_t n8) {
+    for (size_t g = (size_t)blockIdx.x * blockDim.x + threadIdx.x; g < n8; g += (size_t)gridDim.x * blockDim.x) {
+        const float4 a = __ldg(reinterpret_cast<const float4*>(x) + 2 * g);
+        const float4 b = __ldg(reinterpret_cast<const float4*>(x) + 2 * g + 1);
+        const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        float h[8], l[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            h[i] = __bfloat162float(__float2bfloat16_rn(v[i]));
+            l[i] = v[i] - h[i];
+        }
+        reinterpret_cast<uint4*>(hi)[g] =
+            make_uint4(pack_bf16x2(h[0], h[1]), pack_bf16x2(h[2], h[3]), pack_bf16x2(h[4], h[5]), pack_bf16x2(h[6], h[7]));
+        reinterpret_cast<uint4*>(lo)[g] =
+            make_uint4(pack_bf16x2(l[0], l[1]), pack_bf16x2(l[2], l[3]), pack_bf16x2(l[4], l[5]), pack_bf16x2(l[6], l[7]));
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_f32_split_bf16(const float* x, void* hi, void* lo, size_t n, int grid, cudaStream_t s) {
+    f32_split_kernel<<<grid, 256, 0, s>>>(x, reinterpret_cast<__nv_bfloat16*>(hi), reinterpret_cast<__nv_bfloat16*>(lo),
+                                          n / 8);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_bwd_pre(const void* o, const void* dout, bool in_f32, const float* lse, float* lse2, float* dvec,
                            float* dq_acc, int BH, int N, int Np, int d, int grid, cudaStream_t s) {

@@ -55,14 +55,16 @@ struct BwdParams {
 
 // Launch helpers implemented in the kernel translation units.  They return a
 // cudaError_t from the launch itself.
-cudaError_t launch_fwd_bf16_d64(int block_c, bool causal, bool out_f32, const CUtensorMap& tq,
-                                const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
-                                int grid, cudaStream_t stream);
-cudaError_t launch_fwd_bf16_d128(int block_c, bool causal, bool out_f32, const CUtensorMap& tq,
-                                 const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
-                                 int grid, cudaStream_t stream);
-cudaError_t launch_fwd_fp8_d128(bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
-                                const CUtensorMap& tv, const FwdParams& p, int grid,
+// Tensor maps of one forward launch: q, k, v and, for float32 inputs carried
+// as bf16 hi + lo parts, the low parts of q and k.
+struct FwdMaps {
+    CUtensorMap q, k, v, q_lo, k_lo;
+};
+cudaError_t launch_fwd_bf16_d64(int block_c, bool causal, bool out_f32, bool split, const FwdMaps& m,
+                                const FwdParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_fwd_bf16_d128(int block_c, bool causal, bool out_f32, bool split, const FwdMaps& m,
+                                 const FwdParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_fwd_fp8_d128(bool causal, const FwdMaps& m, const FwdParams& p, int grid,
                                 cudaStream_t stream);
 cudaError_t launch_bwd_main(int d, bool causal, bool out_f32, const CUtensorMap& tq,
                             const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
@@ -76,5 +78,7 @@ cudaError_t launch_bwd_dq(const float* dq_acc, void* dq, bool out_f32, float sca
 cudaError_t launch_quantize_fp8(const void* x, void* x8, float* scales, int BH, int N, int d,
                                 int grid, cudaStream_t stream);
 cudaError_t launch_f32_to_bf16(const float* x, void* y, size_t n, int grid, cudaStream_t stream);
+cudaError_t launch_f32_split_bf16(const float* x, void* hi, void* lo, size_t n, int grid,
+                                  cudaStream_t stream);
 
 }  // namespace fa

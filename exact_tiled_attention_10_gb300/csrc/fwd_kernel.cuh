@@ -44,11 +44,14 @@ constexpr int kMmaWarp = 9;
 // max so that P <= 1 fits the E4M3 range after the value-scale fold.
 constexpr float kRescaleSlack = 8.0f;
 
-template <int D_, int BC_, bool FP8_>
+template <int D_, int BC_, bool FP8_, bool SPLIT_ = false>
 struct Cfg {
     static constexpr int D = D_;
     static constexpr int BC = BC_;
     static constexpr bool FP8 = FP8_;
+    // SPLIT: float32 inputs carried as bf16 hi + lo parts; S = Qh Kh^T + Qh Kl^T + Ql Kh^T
+    static constexpr bool SPLIT = SPLIT_;
+    static constexpr int NPART = SPLIT ? 2 : 1;
     static constexpr int BR = 128;   // query rows per tile (= TMEM lanes)
     static constexpr int QT = 2;     // query tiles per CTA work item
     static constexpr int ELEM = FP8 ? 1 : 2;
@@ -59,7 +62,7 @@ struct Cfg {
     static constexpr int KV_BOX = BC * 128;
     static constexpr int Q_TILE = BR * ROW_BYTES;
     static constexpr int KV_TILE = BC * ROW_BYTES;
-    static constexpr int STAGES = (KV_TILE >= 32768) ? 2 : 3;
+    static constexpr int STAGES = (NPART * KV_TILE >= 32768) ? 2 : 3;
     static constexpr int KSTEP = 32 / ELEM;         // K elements per MMA instruction
     static constexpr int S_STEPS = ROW_BYTES / 32;  // MMAs per S tile
     static constexpr int PV_STEPS = BC / KSTEP;     // MMAs per P V
@@ -67,9 +70,11 @@ struct Cfg {
     static constexpr int TM_COLS = 512;
     static_assert(2 * BC + 2 * D <= TM_COLS, "TMEM budget");
     // shared memory map (tile bases 1024-byte aligned)
+    // Q: [part][tile]; K stage: [part] tiles; V stage: one tile
     static constexpr int OFF_Q = 0;
-    static constexpr int OFF_K = OFF_Q + QT * Q_TILE;
-    static constexpr int OFF_V = OFF_K + STAGES * KV_TILE;
+    static constexpr int K_STAGE = NPART * KV_TILE;
+    static constexpr int OFF_K = OFF_Q + NPART * QT * Q_TILE;
+    static constexpr int OFF_V = OFF_K + STAGES * K_STAGE;
     static constexpr int OFF_BAR = OFF_V + STAGES * KV_TILE;
     // barrier indices
     static constexpr int B_QFULL = 0, B_QEMPTY = 1;
@@ -126,18 +131,25 @@ __device__ __forceinline__ Item get_item(int it, const FwdParams& p) {
     return I;
 }
 
-// S_t = Q_t K^T over the head dimension (both operands K-major, 128B swizzle)
+// S_t = Q_t K^T over the head dimension (both operands K-major, 128B swizzle).
+// With SPLIT, the three products hi.hi + hi.lo + lo.hi accumulate in turn.
 template <class C>
 __device__ __forceinline__ void issue_S(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
 #pragma unroll
-    for (int kk = 0; kk < C::S_STEPS; ++kk) {
-        const uint32_t off_in = (kk % 4) * 32;
-        const uint64_t a = sdesc_sw128(q_smem + (kk / 4) * C::Q_BOX + off_in, 16, 1024);
-        const uint64_t b = sdesc_sw128(k_smem + (kk / 4) * C::KV_BOX + off_in, 16, 1024);
-        if constexpr (C::FP8)
-            mma_f8_ss(d_tmem, a, b, C::IDESC_S, kk > 0);
-        else
-            mma_f16_ss(d_tmem, a, b, C::IDESC_S, kk > 0);
+    for (int part = 0; part < (C::SPLIT ? 3 : 1); ++part) {
+        const uint32_t qs = q_smem + (part == 2 ? C::QT * C::Q_TILE : 0);
+        const uint32_t ks = k_smem + (part == 1 ? C::KV_TILE : 0);
+#pragma unroll
+        for (int kk = 0; kk < C::S_STEPS; ++kk) {
+            const uint32_t off_in = (kk % 4) * 32;
+            const uint64_t a = sdesc_sw128(qs + (kk / 4) * C::Q_BOX + off_in, 16, 1024);
+            const uint64_t b = sdesc_sw128(ks + (kk / 4) * C::KV_BOX + off_in, 16, 1024);
+            const uint32_t acc = (part > 0 || kk > 0) ? 1u : 0u;
+            if constexpr (C::FP8)
+                mma_f8_ss(d_tmem, a, b, C::IDESC_S, acc);
+            else
+                mma_f16_ss(d_tmem, a, b, C::IDESC_S, acc);
+        }
     }
 }
 
@@ -173,7 +185,8 @@ __device__ __forceinline__ void store_row_chunk(void* o_row, int c0, const float
 template <class C, bool CAUSAL, bool OUT_F32>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-               const __grid_constant__ CUtensorMap tv, const FwdParams p) {
+               const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tql,
+               const __grid_constant__ CUtensorMap tkl, const FwdParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -208,6 +221,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tmap(&tq);
             prefetch_tmap(&tk);
             prefetch_tmap(&tv);
+            if (C::SPLIT) {
+                prefetch_tmap(&tql);
+                prefetch_tmap(&tkl);
+            }
         }
     }
     tc_fence_before();
@@ -227,20 +244,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(ok = wait_bounded_warp(BAR(C::B_QEMPTY), qe ^ 1, abort_flag, p.err, kErrWaitFwdProducer))) break;
             qe ^= 1;
             if (lane == 0) {
-                mbar_arrive_expect_tx(BAR(C::B_QFULL), C::QT * C::Q_TILE);
-                for (int t = 0; t < C::QT; ++t)
-                    for (int bx = 0; bx < C::NBOX; ++bx)
-                        tma_load_3d(sbase + C::OFF_Q + t * C::Q_TILE + bx * C::Q_BOX, &tq, BAR(C::B_QFULL),
-                                    bx * C::BOX_ELEMS, I.row0 + t * C::BR, I.bh);
+                mbar_arrive_expect_tx(BAR(C::B_QFULL), C::NPART * C::QT * C::Q_TILE);
+                for (int part = 0; part < C::NPART; ++part)
+                    for (int t = 0; t < C::QT; ++t)
+                        for (int bx = 0; bx < C::NBOX; ++bx)
+                            tma_load_3d(sbase + C::OFF_Q + (part * C::QT + t) * C::Q_TILE + bx * C::Q_BOX,
+                                        part ? &tql : &tq, BAR(C::B_QFULL), bx * C::BOX_ELEMS,
+                                        I.row0 + t * C::BR, I.bh);
             }
             __syncwarp();
             for (int j = 0; j < I.nmax; ++j) {
                 if (!(ok = wait_bounded_warp(BAR(C::B_KEMPTY + st), ph ^ 1, abort_flag, p.err, kErrWaitFwdProducer))) break;
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(BAR(C::B_KFULL + st), C::KV_TILE);
-                    for (int bx = 0; bx < C::NBOX; ++bx)
-                        tma_load_3d(sbase + C::OFF_K + st * C::KV_TILE + bx * C::KV_BOX, &tk, BAR(C::B_KFULL + st),
-                                    bx * C::BOX_ELEMS, j * C::BC, I.bh);
+                    mbar_arrive_expect_tx(BAR(C::B_KFULL + st), C::K_STAGE);
+                    for (int part = 0; part < C::NPART; ++part)
+                        for (int bx = 0; bx < C::NBOX; ++bx)
+                            tma_load_3d(sbase + C::OFF_K + st * C::K_STAGE + part * C::KV_TILE + bx * C::KV_BOX,
+                                        part ? &tkl : &tk, BAR(C::B_KFULL + st), bx * C::BOX_ELEMS, j * C::BC, I.bh);
                 }
                 __syncwarp();
                 if (!(ok = wait_bounded_warp(BAR(C::B_VEMPTY + st), ph ^ 1, abort_flag, p.err, kErrWaitFwdProducer))) break;
@@ -274,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (leader) {
                 for (int t = 0; t < 2; ++t)
                     if (I.n[t] > 0) {
-                        issue_S<C>(tS[t], sbase + C::OFF_Q + t * C::Q_TILE, sbase + C::OFF_K + kst * C::KV_TILE);
+                        issue_S<C>(tS[t], sbase + C::OFF_Q + t * C::Q_TILE, sbase + C::OFF_K + kst * C::K_STAGE);
                         mma_commit(BAR(C::B_SFULL + t));
                     }
                 mma_commit(BAR(C::B_KEMPTY + kst));
@@ -306,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             tc_fence_after();
                         }
                         if (leader) {
-                            issue_S<C>(tS[t], sbase + C::OFF_Q + t * C::Q_TILE, sbase + C::OFF_K + kst * C::KV_TILE);
+                            issue_S<C>(tS[t], sbase + C::OFF_Q + t * C::Q_TILE, sbase + C::OFF_K + kst * C::K_STAGE);
                             mma_commit(BAR(C::B_SFULL + t));
                         }
                     }
@@ -442,16 +462,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t w[16];
                     float acc0 = 0.f, acc1 = 0.f;
                     if constexpr (C::FP8) {
+                        // l sums the E4M3-rounded weights the P V product actually
+                        // uses, so O stays a convex combination of the value rows
+                        __half2 hacc = __float2half2_rn(0.f);
 #pragma unroll
                         for (int e = 0; e < 16; ++e) {
                             const float p0 = ex2_approx(fmaf(s[ch * CH + 4 * e + 0], cs, cb));
                             const float p1 = ex2_approx(fmaf(s[ch * CH + 4 * e + 1], cs, cb));
                             const float p2 = ex2_approx(fmaf(s[ch * CH + 4 * e + 2], cs, cb));
                             const float p3 = ex2_approx(fmaf(s[ch * CH + 4 * e + 3], cs, cb));
-                            acc0 += p0 + p1;
-                            acc1 += p2 + p3;
                             w[e] = pack_e4m3x4(p0, p1, p2, p3);
+                            hacc = __hadd2(hacc, __hadd2(e4m3x2_to_half2(w[e] & 0xFFFFu), e4m3x2_to_half2(w[e] >> 16)));
                         }
+                        const float2 hs = __half22float2(hacc);
+                        acc0 = hs.x;
+                        acc1 = hs.y;
                     } else {
 #pragma unroll
                         for (int e = 0; e < 16; ++e) {
@@ -501,13 +526,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <class C, bool CAUSAL, bool OUT_F32>
-cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                   const FwdParams& p, int grid, cudaStream_t stream) {
+cudaError_t launch(const FwdMaps& m, const FwdParams& p, int grid, cudaStream_t stream) {
     auto kern = fwd_kernel<C, CAUSAL, OUT_F32>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads, C::SMEM, stream>>>(tq, tk, tv, p);
+    kern<<<grid, kThreads, C::SMEM, stream>>>(m.q, m.k, m.v, m.q_lo, m.k_lo, p);
     return cudaGetLastError();
+}
+
+template <class C>
+cudaError_t launch_any(bool causal, bool out_f32, const FwdMaps& m, const FwdParams& p, int grid, cudaStream_t s) {
+    if (causal) return out_f32 ? launch<C, true, true>(m, p, grid, s) : launch<C, true, false>(m, p, grid, s);
+    return out_f32 ? launch<C, false, true>(m, p, grid, s) : launch<C, false, false>(m, p, grid, s);
 }
 
 }  // namespace fwd

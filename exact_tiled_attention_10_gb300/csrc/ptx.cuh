@@ -6,6 +6,7 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 namespace fa {
 
@@ -283,6 +284,14 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
     asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));
     asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
     return (uint32_t)lo | ((uint32_t)hi << 16);
+}
+
+// Two E4M3 bytes (low byte = element 0) -> two halves, exact.
+__device__ __forceinline__ __half2 e4m3x2_to_half2(uint32_t two) {
+    uint32_t r;
+    const uint16_t in = (uint16_t)two;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(in));
+    return *reinterpret_cast<__half2*>(&r);
 }
 
 }  // namespace fa

@@ -80,11 +80,14 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
                  const int* kv_lens, fa_stream_t stream);
 
 /* Extended forward.
- *   dtype   FA_BF16: as fa_fwd.  FA_F32: q,k,v,o are float32; inputs are
- *           rounded to bf16 (round-to-nearest-even) into `workspace`, the
- *           tensor cores compute in bf16 with fp32 accumulation, and O is
+ *   dtype   FA_BF16: as fa_fwd.  FA_F32: q,k,v,o are float32.  q and k are
+ *           split into bf16 high and low parts (x = hi + lo, ~16 significant
+ *           bits) in `workspace` and the scores are formed from three bf16
+ *           tensor-core products, hi.hi + hi.lo + lo.hi, with float32
+ *           accumulation; v and the probabilities enter P V as bf16; O is
  *           written as float32.
- *   block_c 0 = automatic, or 64 / 128 keys per tile.
+ *   block_c 0 = automatic, or 64 / 128 keys per tile (FA_F32 with d = 128
+ *           needs 64).
  *   workspace, workspace_bytes: at least fa_fwd_workspace_size(dtype,...)
  *           bytes of device memory (NULL allowed when that size is 0). */
 size_t fa_fwd_workspace_size(fa_dtype dtype, int B, int H, int N, int d);
@@ -110,6 +113,24 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o,
                  const float* lse, const void* dout, void* dq, void* dk, void* dv,
                  int B, int H, int N, int d, float scale, int causal, const int* kv_lens,
                  void* workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/* The three phases fa_bwd runs, callable one by one (bf16 tensors, same
+ * workspace).  fa_bwd == fa_bwd_preprocess; fa_bwd_main; fa_bwd_dq.
+ *   fa_bwd_preprocess: D = rowsum(dout * o) ([FA2] §5.2), LSE * log2(e) and
+ *                      a zeroed float32 dQ accumulator, into `workspace`.
+ *   fa_bwd_main:       the key-block-parallel kernel ([FA2] §5.4): writes
+ *                      dk, dv and accumulates unscaled dQ into `workspace`.
+ *   fa_bwd_dq:         dq = scale * accumulator, as bf16.
+ * Each phase reads what the previous one wrote; call them in this order on
+ * one stream (or order the streams). */
+fa_status fa_bwd_preprocess(const void* o, const float* lse, const void* dout, int B, int H, int N,
+                            int d, void* workspace, size_t workspace_bytes, fa_stream_t stream);
+fa_status fa_bwd_main(const void* q, const void* k, const void* v, const void* dout, void* dk,
+                      void* dv, int B, int H, int N, int d, float scale, int causal,
+                      const int* kv_lens, void* workspace, size_t workspace_bytes,
+                      fa_stream_t stream);
+fa_status fa_bwd_dq(void* dq, int B, int H, int N, int d, float scale, void* workspace,
+                    size_t workspace_bytes, fa_stream_t stream);
 
 /* As fa_bwd with an element type: FA_F32 takes float32 q,k,v,o,dout and writes
  * float32 dq,dk,dv (the tensor cores see bf16-rounded copies). */
