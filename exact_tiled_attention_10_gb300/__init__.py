@@ -22,6 +22,7 @@ from typing import Optional, Tuple
 import torch
 
 __all__ = ["forward", "backward", "quantize_fp8", "forward_fp8", "check_device_status",
+           "selftest_wait_timeout",
            "bwd_workspace_size", "fwd_workspace_size", "library_path", "load_library", "FAError"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -39,6 +40,7 @@ _SIGS = {
     "fa_version": ([], _i),
     "fa_last_error": ([], ctypes.c_char_p),
     "fa_check_device_status": ([_vp], _i),
+    "fa_selftest_wait_timeout": ([ctypes.c_uint, _vp, _vp], _i),
     "fa_fwd": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _vp], _i),
     "fa_fwd_workspace_size": ([_i, _i, _i, _i, _i], _sz),
     "fa_fwd_ex": ([_i, _i, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _vp, _sz, _vp], _i),
@@ -204,6 +206,18 @@ def forward_fp8(q8, k8, v8, sq, sk, sv, causal: bool = False, scale: Optional[fl
     _check(lib.fa_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(v8), _ptr(sq), _ptr(sk), _ptr(sv), _ptr(o),
                           _ptr(l), B, H, N, d, scale, int(bool(causal)), _ptr(kv), _stream(q8)))
     return o, l
+
+
+def selftest_wait_timeout(limit_us: int = 20000, device=None) -> int:
+    """Run the bounded-wait self-test kernel; returns the device flag (0 = the
+    wait gave up as designed).  The error word it sets is reported by the next
+    check_device_status()."""
+    lib = load_library()
+    dev = torch.device("cuda") if device is None else torch.device(device)
+    flag = torch.full((4,), 7, dtype=torch.int32, device=dev)
+    _check(lib.fa_selftest_wait_timeout(int(limit_us), flag.data_ptr(),
+                                        torch.cuda.current_stream(dev).cuda_stream))
+    return int(flag[0].item())
 
 
 def check_device_status(device=None) -> None:

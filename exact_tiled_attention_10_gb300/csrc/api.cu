@@ -257,6 +257,16 @@ fa_status fa_check_device_status(fa_stream_t stream) {
     return FA_OK;
 }
 
+fa_status fa_selftest_wait_timeout(unsigned int limit_us, int* waited_out, fa_stream_t stream) {
+    FA_CHECK_PTR(waited_out);
+    if (limit_us == 0 || limit_us > 1000000u) return fail(FA_ERR_INVALID_ARG, "limit_us must be in [1, 1e6]");
+    DeviceInfo* dev = nullptr;
+    FA_TRY(device_info(&dev));
+    cudaError_t e = fa::launch_wait_selftest(dev->err_word, limit_us, waited_out, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
+    return FA_OK;
+}
+
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
                  float scale, int causal, const int* kv_lens, fa_stream_t stream) {
     return fwd_impl(FA_BF16, 0, false, q, k, v, nullptr, nullptr, nullptr, o, lse, B, H, N, d, scale, causal, kv_lens,

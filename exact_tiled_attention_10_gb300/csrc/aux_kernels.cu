@@ -183,7 +183,28 @@ __global__ void __launch_bounds__(256) f32_split_kernel(const float* __restrict_
     }
 }
 
+// One warp waits on an mbarrier that nothing ever arrives on, through the same
+// bounded wait every pipeline uses; it must give up after `limit_us`, record
+// the error bit and return (no trap, no hang).
+__global__ void wait_selftest_kernel(unsigned int* err, unsigned long long limit_ns, int* waited_out) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const bool ok = wait_bounded_warp(smem_u32(&bar), 0, &abort_flag, err, kErrWaitSelftest, limit_ns);
+    if (threadIdx.x == 0) *waited_out = ok ? 1 : 0;
+}
+
 }  // namespace
+
+cudaError_t launch_wait_selftest(unsigned int* err, unsigned int limit_us, int* waited_out, cudaStream_t s) {
+    wait_selftest_kernel<<<1, 32, 0, s>>>(err, (unsigned long long)limit_us * 1000ull, waited_out);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_f32_split_bf16(const float* x, void* hi, void* lo, size_t n, int grid, cudaStream_t s) {
     f32_split_kernel<<<grid, 256, 0, s>>>(x, reinterpret_cast<__nv_bfloat16*>(hi), reinterpret_cast<__nv_bfloat16*>(lo),

@@ -18,6 +18,7 @@ enum : unsigned int {
     kErrWaitBwdCompute = 1u << 5,
     kErrWaitBwdDq = 1u << 6,
     kErrWaitDrain = 1u << 7,
+    kErrWaitSelftest = 1u << 8,
 };
 
 constexpr int kNumSMsDefault = 152;
@@ -77,6 +78,8 @@ cudaError_t launch_bwd_dq(const float* dq_acc, void* dq, bool out_f32, float sca
                           int Np, int d, int grid, cudaStream_t stream);
 cudaError_t launch_quantize_fp8(const void* x, void* x8, float* scales, int BH, int N, int d,
                                 int grid, cudaStream_t stream);
+cudaError_t launch_wait_selftest(unsigned int* err, unsigned int limit_us, int* waited_out,
+                                 cudaStream_t stream);
 cudaError_t launch_f32_to_bf16(const float* x, void* y, size_t n, int grid, cudaStream_t stream);
 cudaError_t launch_f32_split_bf16(const float* x, void* hi, void* lo, size_t n, int grid,
                                   cudaStream_t stream);

@@ -388,6 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (row < p.N) sq_row = __ldg(p.sq + (size_t)I.bh * p.nblk + row / 64);
             }
             float m = -INFINITY, l = 0.f;
+            float lq = 0.f;  // FP8: sum of the E4M3-rounded weights (normalises O)
             bool ok = true;
             for (int j = 0; j < n; ++j) {
                 if (!(ok = wait_bounded_warp(BAR(C::B_SFULL + t), sph, abort_flag, p.err, kErrWaitFwdSoftmax))) break;
@@ -440,6 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     alpha = ex2_approx(m - mx2);  // 0 when m = -inf
                     m = mx2;
                     l *= alpha;
+                    if (C::FP8) lq *= alpha;
                 }
                 if (j > 0 && __any_sync(0xffffffffu, need)) {
 #pragma unroll 1
@@ -453,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_st_wait();
                 }
                 const float mb = (m == -INFINITY) ? 0.f : m;
-                float lsum = 0.f;
+                float lsum = 0.f, lqsum = 0.f;
                 constexpr int CH = C::FP8 ? 64 : 32;  // columns per 16-word TMEM store
 #pragma unroll
                 for (int ch = 0; ch < C::BC / CH; ++ch) {
@@ -462,8 +464,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t w[16];
                     float acc0 = 0.f, acc1 = 0.f;
                     if constexpr (C::FP8) {
-                        // l sums the E4M3-rounded weights the P V product actually
-                        // uses, so O stays a convex combination of the value rows
+                        // lq sums the E4M3-rounded weights the P V product actually
+                        // uses, so O stays a convex combination of the value rows;
+                        // l keeps the exact sum for the LSE
                         __half2 hacc = __float2half2_rn(0.f);
 #pragma unroll
                         for (int e = 0; e < 16; ++e) {
@@ -471,12 +474,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const float p1 = ex2_approx(fmaf(s[ch * CH + 4 * e + 1], cs, cb));
                             const float p2 = ex2_approx(fmaf(s[ch * CH + 4 * e + 2], cs, cb));
                             const float p3 = ex2_approx(fmaf(s[ch * CH + 4 * e + 3], cs, cb));
+                            acc0 += p0 + p1;
+                            acc1 += p2 + p3;
                             w[e] = pack_e4m3x4(p0, p1, p2, p3);
                             hacc = __hadd2(hacc, __hadd2(e4m3x2_to_half2(w[e] & 0xFFFFu), e4m3x2_to_half2(w[e] >> 16)));
                         }
                         const float2 hs = __half22float2(hacc);
-                        acc0 = hs.x;
-                        acc1 = hs.y;
+                        lqsum += (hs.x + hs.y) * inv_w[h];
                     } else {
 #pragma unroll
                         for (int e = 0; e < 16; ++e) {
@@ -491,6 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_st16(tS + ch * 16, w);
                 }
                 l += lsum;
+                if (C::FP8) lq += lqsum;
                 tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(BAR(C::B_PFULL + t));
@@ -500,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             oph ^= 1;
             tc_fence_after();
             float inv = (l > 0.f) ? 1.f / l : 0.f;
-            if (C::FP8) inv *= sv_max * (1.f / 448.f);
+            if (C::FP8) inv = (lq > 0.f) ? sv_max * (1.f / 448.f) / lq : 0.f;
             char* orow = reinterpret_cast<char*>(p.o) + row_idx * C::D * (OUT_F32 ? 4 : 2);
 #pragma unroll 1
             for (int c = 0; c < C::D; c += 32) {

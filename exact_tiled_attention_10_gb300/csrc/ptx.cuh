@@ -52,13 +52,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                             unsigned int* err, unsigned int code) {
+                                             unsigned int* err, unsigned int code,
+                                             uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (;;) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (global_timer_ns() - t0 > kWaitLimitNs) {
+        if (global_timer_ns() - t0 > limit_ns) {
             atomicOr(err, code);
             *abort_flag = 1;
             return false;
@@ -71,8 +72,9 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
 // never diverge).
 __device__ __forceinline__ bool wait_bounded_warp(uint32_t bar, uint32_t parity,
                                                   volatile int* abort_flag, unsigned int* err,
-                                                  unsigned int code) {
-    bool ok = wait_bounded(bar, parity, abort_flag, err, code);
+                                                  unsigned int code,
+                                                  uint64_t limit_ns = kWaitLimitNs) {
+    bool ok = wait_bounded(bar, parity, abort_flag, err, code, limit_ns);
     return __all_sync(0xffffffffu, ok);
 }
 

@@ -70,6 +70,14 @@ const char* fa_last_error(void);
  * call, FA_ERR_CUDA if the stream itself reports an error, else FA_OK. */
 fa_status fa_check_device_status(fa_stream_t stream);
 
+/* Failure-detection self-test: launches one warp that waits, through the same
+ * bounded pipeline wait the kernels use, on a barrier nothing ever arrives
+ * on.  It gives up after limit_us microseconds (1 .. 1e6), writes 0 to the
+ * device int *waited_out (1 would mean the wait completed), sets the device
+ * error word, and returns; the next fa_check_device_status() then reports
+ * FA_ERR_TIMEOUT and clears the word.  No trap, no hang, no fault. */
+fa_status fa_selftest_wait_timeout(unsigned int limit_us, int* waited_out, fa_stream_t stream);
+
 /* ---------------------------------------------------------------- forward */
 
 /* bf16 forward ([FA2] §4 Algorithm 1).  q,k,v: bf16 inputs; o: bf16 output;

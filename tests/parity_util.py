@@ -39,9 +39,21 @@ def assert_close_abs(gpu, ref, tol, what):
     return err
 
 
-def assert_grad(gpu, ref, what):
-    scale = max(np.max(np.abs(ref)) if ref.size else 0.0, 1e-30)
-    return assert_close_abs(gpu, ref, GRAD_REL_TOL * scale, what)
+# A gradient that is identically zero in exact arithmetic (e.g. dQ with a single
+# visible key) is computed on the GPU as P(dP - D) with dP from the tensor core
+# and D from a float32 row sum: a ~1e-7 residue.  The relative criterion then
+# degenerates, so an absolute floor of 1e-5 applies.
+GRAD_ABS_FLOOR = 1e-5
+
+
+def assert_grad(gpu, ref, what, tensor_maxabs=None):
+    """max|gpu - ref| <= 2e-2 * (max-abs of the whole gradient tensor).
+
+    `tensor_maxabs` is that max-abs when `ref` covers only sampled rows."""
+    scale = np.max(np.abs(ref)) if ref.size else 0.0
+    if tensor_maxabs is not None:
+        scale = max(scale, float(tensor_maxabs))
+    return assert_close_abs(gpu, ref, max(GRAD_REL_TOL * scale, GRAD_ABS_FLOOR), what)
 
 
 def sample_rows(N, n, seed):

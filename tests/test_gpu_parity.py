@@ -104,9 +104,13 @@ def _sampled_check(w, causal, heads, n_rows=48, bwd=True, seed_off=0):
         if bwd:
             keys = sample_rows(w.N, n_rows // 2, seed=b * 7 + h + 1 + seed_off)
             g = oracle.bwd_rows(qh, kh, vh, to64(do[b, h]), w.scale, causal, kvl, rows, keys)
-            assert_grad(to64(dq[b, h, rows]), g["dq"], "dQ[%d,%d]" % (b, h))
-            assert_grad(to64(dk[b, h, keys]), g["dk"], "dK[%d,%d]" % (b, h))
-            assert_grad(to64(dv[b, h, keys]), g["dv"], "dV[%d,%d]" % (b, h))
+            # the reference is known on sampled rows only; the tensor's max-abs
+            # comes from the full computed tensor (it matches the reference's to
+            # within the tolerance wherever both are known)
+            for name, x, ref, idx in (("dQ", dq, g["dq"], rows), ("dK", dk, g["dk"], keys),
+                                      ("dV", dv, g["dv"], keys)):
+                assert_grad(to64(x[b, h, idx]), ref, "%s[%d,%d]" % (name, b, h),
+                            tensor_maxabs=x.float().abs().max().item())
     return q, k, v, o, lse
 
 
