@@ -77,10 +77,10 @@ struct Cfg {
     static constexpr int OFF_V = OFF_K + STAGES * K_STAGE;
     static constexpr int OFF_BAR = OFF_V + STAGES * KV_TILE;
     // barrier indices
-    static constexpr int B_QFULL = 0, B_QEMPTY = 1;
-    static constexpr int B_KFULL = 2, B_KEMPTY = 2 + STAGES;
-    static constexpr int B_VFULL = 2 + 2 * STAGES, B_VEMPTY = 2 + 3 * STAGES;
-    static constexpr int B_SFULL = 2 + 4 * STAGES, B_PFULL = B_SFULL + 2;
+    static constexpr int B_QFULL = 0, B_QEMPTY = 2;  // one per query tile
+    static constexpr int B_KFULL = 4, B_KEMPTY = 4 + STAGES;
+    static constexpr int B_VFULL = 4 + 2 * STAGES, B_VEMPTY = 4 + 3 * STAGES;
+    static constexpr int B_SFULL = 4 + 4 * STAGES, B_PFULL = B_SFULL + 2;
     static constexpr int B_OFULL = B_PFULL + 2, B_OEMPTY = B_OFULL + 2;
     static constexpr int B_DONE = B_OEMPTY + 2;
     static constexpr int NBAR = B_DONE + 1;
@@ -196,8 +196,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto BAR = [&](int i) -> uint32_t { return sbase + C::OFF_BAR + 8 * i; };
 
     if (threadIdx.x == 0) {
-        mbar_init(BAR(C::B_QFULL), 1);
-        mbar_init(BAR(C::B_QEMPTY), 1);
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(BAR(C::B_QFULL + t), 1);
+            mbar_init(BAR(C::B_QEMPTY + t), 1);
+        }
         for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(BAR(C::B_KFULL + s), 1);
             mbar_init(BAR(C::B_KEMPTY + s), 1);
@@ -241,18 +243,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int it = blockIdx.x; it < p.num_items && ok; it += gridDim.x) {
             const Item I = get_item<C, CAUSAL>(it, p);
             if (I.nmax == 0) continue;
-            if (!(ok = wait_bounded_warp(BAR(C::B_QEMPTY), qe ^ 1, abort_flag, p.err, kErrWaitFwdProducer))) break;
-            qe ^= 1;
-            if (lane == 0) {
-                mbar_arrive_expect_tx(BAR(C::B_QFULL), C::NPART * C::QT * C::Q_TILE);
-                for (int part = 0; part < C::NPART; ++part)
-                    for (int t = 0; t < C::QT; ++t)
+            // Q tile t of this item may load as soon as the previous item's last
+            // S_t MMA has consumed the buffer (per-tile barriers), overlapping
+            // the previous item's final P V products and epilogue
+            for (int t = 0; t < C::QT && ok; ++t) {
+                if (!(ok = wait_bounded_warp(BAR(C::B_QEMPTY + t), qe ^ 1, abort_flag, p.err, kErrWaitFwdProducer))) break;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(BAR(C::B_QFULL + t), C::NPART * C::Q_TILE);
+                    for (int part = 0; part < C::NPART; ++part)
                         for (int bx = 0; bx < C::NBOX; ++bx)
                             tma_load_3d(sbase + C::OFF_Q + (part * C::QT + t) * C::Q_TILE + bx * C::Q_BOX,
-                                        part ? &tql : &tq, BAR(C::B_QFULL), bx * C::BOX_ELEMS,
+                                        part ? &tql : &tq, BAR(C::B_QFULL + t), bx * C::BOX_ELEMS,
                                         I.row0 + t * C::BR, I.bh);
+                }
+                __syncwarp();
             }
-            __syncwarp();
+            if (!ok) break;
+            qe ^= 1;
             for (int j = 0; j < I.nmax; ++j) {
                 if (!(ok = wait_bounded_warp(BAR(C::B_KEMPTY + st), ph ^ 1, abort_flag, p.err, kErrWaitFwdProducer))) break;
                 if (lane == 0) {
@@ -287,16 +294,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int it = blockIdx.x; it < p.num_items && ok; it += gridDim.x) {
             const Item I = get_item<C, CAUSAL>(it, p);
             if (I.nmax == 0) continue;
-            if (!(ok = wait_bounded_warp(BAR(C::B_QFULL), qph, abort_flag, p.err, kErrWaitFwdMma))) break;
+            for (int t = 0; t < 2 && ok; ++t)
+                ok = wait_bounded_warp(BAR(C::B_QFULL + t), qph, abort_flag, p.err, kErrWaitFwdMma);
+            if (!ok) break;
             qph ^= 1;
             if (!(ok = wait_bounded_warp(BAR(C::B_KFULL + kst), kph, abort_flag, p.err, kErrWaitFwdMma))) break;
             tc_fence_after();
             if (leader) {
-                for (int t = 0; t < 2; ++t)
+                for (int t = 0; t < 2; ++t) {
                     if (I.n[t] > 0) {
                         issue_S<C>(tS[t], sbase + C::OFF_Q + t * C::Q_TILE, sbase + C::OFF_K + kst * C::K_STAGE);
                         mma_commit(BAR(C::B_SFULL + t));
                     }
+                    if (I.n[t] <= 1) mma_commit(BAR(C::B_QEMPTY + t));  // Q_t no longer needed
+                }
                 mma_commit(BAR(C::B_KEMPTY + kst));
             }
             __syncwarp();
@@ -328,6 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (leader) {
                             issue_S<C>(tS[t], sbase + C::OFF_Q + t * C::Q_TILE, sbase + C::OFF_K + kst * C::K_STAGE);
                             mma_commit(BAR(C::B_SFULL + t));
+                            if (j + 2 == I.n[t]) mma_commit(BAR(C::B_QEMPTY + t));  // last S_t issued
                         }
                     }
                     __syncwarp();
@@ -342,8 +354,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
             }
             if (!ok) break;
-            if (leader) mma_commit(BAR(C::B_QEMPTY));
-            __syncwarp();
         }
         // drain: every MMA this warp issued has completed before TMEM is freed
         if (leader) mma_commit(BAR(C::B_DONE));
@@ -428,12 +438,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 } else {
                     cm[0] = cm[1] = p.scale_log2;
                 }
-                float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-                for (int c = 0; c < C::BC / 2; ++c) mx0 = fmaxf(mx0, s[c]);
-#pragma unroll
-                for (int c = C::BC / 2; c < C::BC; ++c) mx1 = fmaxf(mx1, s[c]);
-                const float mx2 = fmaxf(mx0 * cm[0], mx1 * cm[1]);
+                float mx2;
+                if constexpr (C::FP8) {
+                    mx2 = fmaxf(row_max<C::BC / 2>(s) * cm[0], row_max<C::BC / 2>(s + C::BC / 2) * cm[1]);
+                } else {
+                    mx2 = row_max<C::BC>(s) * cm[0];
+                }
                 const float slack = C::FP8 ? 0.f : kRescaleSlack;
                 const bool need = mx2 > m + slack;
                 float alpha = 1.f;
@@ -482,14 +492,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const float2 hs = __half22float2(hacc);
                         lqsum += (hs.x + hs.y) * inv_w[h];
                     } else {
+                        const float2 cs2 = make_float2(cs, cs), cb2 = make_float2(cb, cb);
+                        float2 a2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                        make_float2(0.f, 0.f)};
 #pragma unroll
                         for (int e = 0; e < 16; ++e) {
-                            const float p0 = ex2_approx(fmaf(s[ch * CH + 2 * e + 0], cs, cb));
-                            const float p1 = ex2_approx(fmaf(s[ch * CH + 2 * e + 1], cs, cb));
-                            acc0 += p0;
-                            acc1 += p1;
-                            w[e] = pack_bf16x2(p0, p1);
+                            const float2 x = ffma2(make_float2(s[ch * CH + 2 * e], s[ch * CH + 2 * e + 1]), cs2, cb2);
+                            const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                            a2[e & 3] = fadd2(a2[e & 3], pp);
+                            w[e] = pack_bf16x2(pp.x, pp.y);
                         }
+                        const float2 t2 = fadd2(fadd2(a2[0], a2[1]), fadd2(a2[2], a2[3]));
+                        acc0 = t2.x;
+                        acc1 = t2.y;
                     }
                     lsum += (acc0 + acc1) * inv_w[h];
                     tmem_st16(tS + ch * 16, w);
