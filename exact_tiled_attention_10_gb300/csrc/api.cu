@@ -383,7 +383,7 @@ fa_status fa_bwd_preprocess(const void* o, const float* lse, const void* dout, i
     FA_CHECK_PTR(o);
     FA_CHECK_PTR(lse);
     FA_CHECK_PTR(dout);
-    BwdCtx c;
+    BwdCtx c{};
     FA_TRY(bwd_setup(FA_BF16, B, H, N, d, 1.0f, workspace, workspace_bytes, &c));
     return bwd_pre_impl(c, false, o, lse, dout, N, d, stream);
 }
@@ -397,7 +397,7 @@ fa_status fa_bwd_main(const void* q, const void* k, const void* v, const void* d
     FA_CHECK_PTR(dout);
     FA_CHECK_PTR(dk);
     FA_CHECK_PTR(dv);
-    BwdCtx c;
+    BwdCtx c{};
     FA_TRY(bwd_setup(FA_BF16, B, H, N, d, scale, workspace, workspace_bytes, &c));
     return bwd_main_impl(c, false, q, k, v, dout, dk, dv, B, H, N, d, scale, causal, kv_lens, stream);
 }
@@ -405,7 +405,7 @@ fa_status fa_bwd_main(const void* q, const void* k, const void* v, const void* d
 fa_status fa_bwd_dq(void* dq, int B, int H, int N, int d, float scale, void* workspace, size_t workspace_bytes,
                     fa_stream_t stream) {
     FA_CHECK_PTR(dq);
-    BwdCtx c;
+    BwdCtx c{};
     FA_TRY(bwd_setup(FA_BF16, B, H, N, d, scale, workspace, workspace_bytes, &c));
     return bwd_dq_impl(c, false, dq, N, d, scale, stream);
 }
@@ -422,7 +422,7 @@ fa_status fa_bwd_ex(fa_dtype dtype, const void* q, const void* k, const void* v,
     FA_CHECK_PTR(dq);
     FA_CHECK_PTR(dk);
     FA_CHECK_PTR(dv);
-    BwdCtx c;
+    BwdCtx c{};
     FA_TRY(bwd_setup(dtype, B, H, N, d, scale, workspace, workspace_bytes, &c));
     const bool f32 = dtype == FA_F32;
     const void *qb = q, *kb = k, *vb = v, *gb = dout;

@@ -26,11 +26,15 @@
 //   * d = 128: dQ_i^T = K_j^T dS^T (M = 128 head-dim lanes, N = 64 queries);
 //     d = 64:  dQ_i = dS K_j (M = 128 query lanes, N = 64).  Either way all
 //     MMAs have M = 128;
+//   * d = 128 keeps two step slots in TMEM (S^T, and dP^T whose columns are
+//     reused for dQ^T once dS is formed), so the MMA warp issues the next
+//     steps' S and dP while the compute warpgroups work on the current one;
+//     d = 64 has room for one slot (plus a separate dQ region);
 //   * warps 8-11 drain the dQ tile from TMEM into shared memory and add it to
 //     the float32 accumulator with asynchronous bulk reductions (TMA), each
 //     warp independently;
-//   * warp 12 issues TMA loads (K_j, V_j once per item; a 2-stage ring of
-//     Q_i, dO_i and the row statistics), warp 13 issues tcgen05.mma.
+//   * warp 12 issues TMA loads (K_j, V_j once per item; a ring of Q_i, dO_i
+//     and the row statistics), warp 13 issues tcgen05.mma.
 #pragma once
 #include "common.cuh"
 #include "ptx.cuh"
@@ -46,20 +50,23 @@ constexpr int kMmaWarp = 13;
 template <int D_>
 struct Cfg {
     static constexpr int D = D_;
-    static constexpr int BC = 128;                 // keys per item (TMEM lanes)
+    static constexpr int BC = 128;                    // keys per item (TMEM lanes)
     static constexpr int BR = (D == 128) ? 64 : 128;  // queries per inner step
-    static constexpr int HALF = BR / 2;            // query columns per compute warpgroup
+    static constexpr int HALF = BR / 2;               // query columns per compute warpgroup
+    static constexpr int NSLOT = (D == 128) ? 2 : 1;  // TMEM step slots
+    static constexpr bool DQ_ALIAS = (NSLOT == 2);    // dQ reuses the slot's dP columns
     static constexpr int ROW_BYTES = D * 2;
     static constexpr int NBOX = ROW_BYTES / 128;
     static constexpr int K_BOX = BC * 128, K_TILE = BC * ROW_BYTES;
     static constexpr int Q_BOX = BR * 128, Q_TILE = BR * ROW_BYTES;
     static constexpr int DS_BOX = BC * 128, DS_TILE = BC * BR * 2;
-    static constexpr int DQ_WARP_BYTES = 8192;     // per drain warp staging
-    static constexpr int STAGES = 2;
-    // TMEM columns
-    static constexpr int TM_DV = 0, TM_DK = D, TM_S = 2 * D, TM_DP = 2 * D + BR, TM_DQ = 2 * D + 2 * BR;
+    static constexpr int DQ_WARP_BYTES = 8192;        // per drain warp staging
+    static constexpr int STAGES = NSLOT + 1;          // Q/dO ring
+    // TMEM columns: dV | dK | slot 0 (S, X) | slot 1 (S, X) | [dQ]
+    static constexpr int TM_DV = 0, TM_DK = D, TM_SLOT0 = 2 * D, TM_SLOT = 2 * BR;
+    static constexpr int TM_DQ = DQ_ALIAS ? -1 : TM_SLOT0 + NSLOT * TM_SLOT;
     static constexpr int TM_COLS = 512;
-    static_assert(TM_DQ + 64 <= TM_COLS, "TMEM budget");
+    static_assert(TM_SLOT0 + NSLOT * TM_SLOT + (DQ_ALIAS ? 0 : 64) <= TM_COLS, "TMEM budget");
     // shared memory map
     static constexpr int OFF_K = 0;
     static constexpr int OFF_V = OFF_K + K_TILE;
@@ -72,10 +79,11 @@ struct Cfg {
     static constexpr int OFF_BAR = OFF_STAT + STAGES * STAT_BYTES;
     static constexpr int B_KVFULL = 0, B_KVEMPTY = 1;
     static constexpr int B_QFULL = 2, B_QEMPTY = 2 + STAGES;
-    static constexpr int B_SFULL = 2 + 2 * STAGES, B_DPFULL = B_SFULL + 1, B_PFULL = B_SFULL + 2;
-    static constexpr int B_DSFULL = B_SFULL + 3, B_DSEMPTY = B_DSFULL + 2;
-    static constexpr int B_DQFULL = B_DSEMPTY + 2, B_DQEMPTY = B_DQFULL + 1;
-    static constexpr int B_ACCFULL = B_DQEMPTY + 1, B_ACCEMPTY = B_ACCFULL + 1;
+    static constexpr int B_SFULL = 2 + 2 * STAGES;  // [NSLOT] each below
+    static constexpr int B_DPFULL = B_SFULL + 2, B_PFULL = B_DPFULL + 2, B_DSFULL = B_PFULL + 2;
+    static constexpr int B_DSEMPTY = B_DSFULL + 2;  // [2] (dS buffers)
+    static constexpr int B_DQFULL = B_DSEMPTY + 2, B_DQEMPTY = B_DQFULL + 2;
+    static constexpr int B_ACCFULL = B_DQEMPTY + 2, B_ACCEMPTY = B_ACCFULL + 1;
     static constexpr int B_DONE = B_ACCEMPTY + 1;
     static constexpr int NBAR = B_DONE + 1;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
@@ -84,6 +92,9 @@ struct Cfg {
     static constexpr uint32_t IDESC_S = idesc_make(kFmtBF16, kFmtBF16, 0, 0, 128, BR);   // S^T, dP^T
     static constexpr uint32_t IDESC_ACC = idesc_make(kFmtBF16, kFmtBF16, 0, 1, 128, D);  // dV, dK
     static constexpr uint32_t IDESC_DQ = idesc_make(kFmtBF16, kFmtBF16, 1, 1, 128, 64);  // dQ^T / dQ
+    __host__ __device__ static constexpr int s_col(int slot) { return TM_SLOT0 + slot * TM_SLOT; }
+    __host__ __device__ static constexpr int x_col(int slot) { return TM_SLOT0 + slot * TM_SLOT + BR; }
+    __host__ __device__ static constexpr int dq_col(int slot) { return DQ_ALIAS ? x_col(slot) : TM_DQ; }
 };
 
 struct Item {
@@ -135,6 +146,55 @@ __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* m, uint32_t
         : "memory");
 }
 
+// ---- MMA groups (issued by one thread) ----
+// S^T = K_j Q_i^T  or  dP^T = V_j dO_i^T  (K-major operands)
+template <class C>
+__device__ __forceinline__ void mma_scores(uint32_t d_tmem, uint32_t kv_smem, uint32_t q_smem) {
+#pragma unroll
+    for (int kk = 0; kk < C::D / 16; ++kk) {
+        const uint32_t o = (kk / 4) * C::K_BOX + (kk % 4) * 32;
+        const uint32_t oq = (kk / 4) * C::Q_BOX + (kk % 4) * 32;
+        mma_f16_ss(d_tmem, sdesc_sw128(kv_smem + o, 16, 1024), sdesc_sw128(q_smem + oq, 16, 1024), C::IDESC_S,
+                   kk > 0);
+    }
+}
+// TMEM column of the packed P^T for queries [16 kk, 16 kk + 16): each compute
+// warpgroup h writes its half at the start of its own S^T columns (never into
+// columns the other warpgroup may still be reading).
+template <class C>
+__device__ __forceinline__ constexpr uint32_t p_col(int kk) {
+    return (uint32_t)(((kk * 16) / C::HALF) * C::HALF + ((kk * 16) % C::HALF) / 2);
+}
+// dV_j (+)= P^T dO_i  (P^T from TMEM, dO_i MN-major)
+template <class C>
+__device__ __forceinline__ void mma_dv(uint32_t tmem, uint32_t s_tmem, uint32_t do_smem, bool acc) {
+#pragma unroll
+    for (int kk = 0; kk < C::BR / 16; ++kk)
+        mma_f16_ts(tmem + C::TM_DV, s_tmem + p_col<C>(kk), sdesc_sw128(do_smem + kk * 2048, C::Q_BOX, 1024),
+                   C::IDESC_ACC, (acc || kk > 0) ? 1u : 0u);
+}
+// dK_j (+)= dS^T Q_i  (dS^T K-major in smem, Q_i MN-major)
+template <class C>
+__device__ __forceinline__ void mma_dk(uint32_t tmem, uint32_t ds_smem, uint32_t q_smem, bool acc) {
+#pragma unroll
+    for (int kk = 0; kk < C::BR / 16; ++kk)
+        mma_f16_ss(tmem + C::TM_DK, sdesc_sw128(ds_smem + (kk / 4) * C::DS_BOX + (kk % 4) * 32, 16, 1024),
+                   sdesc_sw128(q_smem + kk * 2048, C::Q_BOX, 1024), C::IDESC_ACC, (acc || kk > 0) ? 1u : 0u);
+}
+// d=128: dQ^T = K_j^T dS^T ; d=64: dQ = dS K_j  (both operands MN-major)
+template <class C>
+__device__ __forceinline__ void mma_dq(uint32_t d_tmem, uint32_t k_smem, uint32_t ds_smem) {
+#pragma unroll
+    for (int kk = 0; kk < C::BC / 16; ++kk) {
+        const uint64_t dk = sdesc_sw128(k_smem + kk * 2048, C::K_BOX, 1024);
+        const uint64_t ds = sdesc_sw128(ds_smem + kk * 2048, C::DS_BOX, 1024);
+        if (C::D == 128)
+            mma_f16_ss(d_tmem, dk, ds, C::IDESC_DQ, kk > 0);
+        else
+            mma_f16_ss(d_tmem, ds, dk, C::IDESC_DQ, kk > 0);
+    }
+}
+
 template <class C, bool CAUSAL, bool OUT_F32>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
@@ -155,15 +215,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(BAR(C::B_QFULL + s), 1);
             mbar_init(BAR(C::B_QEMPTY + s), 1);
         }
-        mbar_init(BAR(C::B_SFULL), 1);
-        mbar_init(BAR(C::B_DPFULL), 1);
-        mbar_init(BAR(C::B_PFULL), 256);
         for (int s = 0; s < 2; ++s) {
+            mbar_init(BAR(C::B_SFULL + s), 1);
+            mbar_init(BAR(C::B_DPFULL + s), 1);
+            mbar_init(BAR(C::B_PFULL + s), 256);
             mbar_init(BAR(C::B_DSFULL + s), 256);
             mbar_init(BAR(C::B_DSEMPTY + s), 1);
+            mbar_init(BAR(C::B_DQFULL + s), 1);
+            mbar_init(BAR(C::B_DQEMPTY + s), 128);
         }
-        mbar_init(BAR(C::B_DQFULL), 1);
-        mbar_init(BAR(C::B_DQEMPTY), 128);
         mbar_init(BAR(C::B_ACCFULL), 1);
         mbar_init(BAR(C::B_ACCEMPTY), 256);
         mbar_init(BAR(C::B_DONE), 1);
@@ -224,90 +284,92 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
-        int st = 0, dsb = 0;
-        uint32_t qph = 0, kvph = 0, pph = 0, aeph = 0, dqeph = 0;
-        uint32_t dsph[2] = {0, 0};
+        // Per item, with slot(s) = s % NSLOT:
+        //   prologue: S(s), dP(s) for s < NSLOT
+        //   step s:   dV(s) | S(s+NSLOT) | dK(s), dQ(s) | dP(s+1) if not yet issued
+        // so the compute warpgroups always have a later step's S / dP in flight.
+        int st = 0, st_ahead = 0;  // Q ring stage of step s / of the next step to open
+        uint32_t qph = 0, qph_ahead = 0, kvph = 0, aeph = 0;
+        uint32_t pph[2] = {0, 0}, dsph[2] = {0, 0}, dqeph[2] = {0, 0};
         const bool leader = (lane == 0);
         const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V;
         bool ok = true;
+        // open_step(slot): wait for the next step's Q/dO stage and issue its S
+        auto open_step = [&](int slot) -> bool {
+            if (!wait_bounded_warp(BAR(C::B_QFULL + st_ahead), qph_ahead, abort_flag, p.err, kErrWaitBwdMma)) return false;
+            tc_fence_after();
+            if (leader) {
+                mma_scores<C>(tmem + C::s_col(slot), sK, sbase + C::OFF_Q + st_ahead * C::Q_TILE);
+                mma_commit(BAR(C::B_SFULL + slot));
+            }
+            __syncwarp();
+            if (++st_ahead == C::STAGES) { st_ahead = 0; qph_ahead ^= 1; }
+            return true;
+        };
+        // issue_dp(slot, stage): dP^T of the step held in `stage` into the slot's X
+        // columns, once the dQ previously held there has been drained
+        auto issue_dp = [&](int slot, int stage) -> bool {
+            if (C::DQ_ALIAS) {
+                if (!wait_bounded_warp(BAR(C::B_DQEMPTY + slot), dqeph[slot] ^ 1, abort_flag, p.err, kErrWaitBwdMma))
+                    return false;
+                dqeph[slot] ^= 1;
+            }
+            tc_fence_after();
+            if (leader) {
+                mma_scores<C>(tmem + C::x_col(slot), sV, sbase + C::OFF_DO + stage * C::Q_TILE);
+                mma_commit(BAR(C::B_DPFULL + slot));
+            }
+            __syncwarp();
+            return true;
+        };
         for (int it = blockIdx.x; it < p.num_items && ok; it += gridDim.x) {
             const Item I = get_item<C, CAUSAL>(it, p);
             if (I.n == 0) continue;
             if (!(ok = wait_bounded_warp(BAR(C::B_KVFULL), kvph, abort_flag, p.err, kErrWaitBwdMma))) break;
             kvph ^= 1;
+            // prologue: S of the first NSLOT steps, then their dP
+            for (int s = 0; s < C::NSLOT && s < I.n && ok; ++s) ok = open_step(s);
+            for (int s = 0; s < C::NSLOT && s < I.n && ok; ++s) ok = issue_dp(s, (st + s) % C::STAGES);
+            if (!ok) break;
             for (int s = 0; s < I.n; ++s) {
+                const int slot = s % C::NSLOT;
+                const int dsb = s & 1;
                 const uint32_t sQ = sbase + C::OFF_Q + st * C::Q_TILE;
                 const uint32_t sDO = sbase + C::OFF_DO + st * C::Q_TILE;
                 const uint32_t sDS = sbase + C::OFF_DS + dsb * C::DS_TILE;
-                if (!(ok = wait_bounded_warp(BAR(C::B_QFULL + st), qph, abort_flag, p.err, kErrWaitBwdMma))) break;
-                tc_fence_after();
-                if (leader) {
-                    // S^T = K_j Q_i^T and dP^T = V_j dO_i^T (K-major operands)
-#pragma unroll
-                    for (int kk = 0; kk < C::D / 16; ++kk) {
-                        const uint32_t o = (kk / 4) * C::K_BOX + (kk % 4) * 32;
-                        const uint32_t oq = (kk / 4) * C::Q_BOX + (kk % 4) * 32;
-                        mma_f16_ss(tmem + C::TM_S, sdesc_sw128(sK + o, 16, 1024), sdesc_sw128(sQ + oq, 16, 1024),
-                                   C::IDESC_S, kk > 0);
-                    }
-                    mma_commit(BAR(C::B_SFULL));
-#pragma unroll
-                    for (int kk = 0; kk < C::D / 16; ++kk) {
-                        const uint32_t o = (kk / 4) * C::K_BOX + (kk % 4) * 32;
-                        const uint32_t oq = (kk / 4) * C::Q_BOX + (kk % 4) * 32;
-                        mma_f16_ss(tmem + C::TM_DP, sdesc_sw128(sV + o, 16, 1024), sdesc_sw128(sDO + oq, 16, 1024),
-                                   C::IDESC_S, kk > 0);
-                    }
-                    mma_commit(BAR(C::B_DPFULL));
-                }
-                __syncwarp();
-                // dV_j += P^T dO_i  (P^T from TMEM, dO_i MN-major)
-                if (!(ok = wait_bounded_warp(BAR(C::B_PFULL), pph, abort_flag, p.err, kErrWaitBwdMma))) break;
-                pph ^= 1;
+                // dV(s)
+                if (!(ok = wait_bounded_warp(BAR(C::B_PFULL + slot), pph[slot], abort_flag, p.err, kErrWaitBwdMma))) break;
+                pph[slot] ^= 1;
                 if (s == 0) {
                     if (!(ok = wait_bounded_warp(BAR(C::B_ACCEMPTY), aeph ^ 1, abort_flag, p.err, kErrWaitBwdMma))) break;
                     aeph ^= 1;
                 }
                 tc_fence_after();
-                if (leader) {
-#pragma unroll
-                    for (int kk = 0; kk < C::BR / 16; ++kk)
-                        mma_f16_ts(tmem + C::TM_DV, tmem + C::TM_S + kk * 8,
-                                   sdesc_sw128(sDO + kk * 2048, C::Q_BOX, 1024), C::IDESC_ACC, (s > 0 || kk > 0));
-                }
+                if (leader) mma_dv<C>(tmem, tmem + C::s_col(slot), sDO, s > 0);
                 __syncwarp();
-                // dK_j += dS^T Q_i  (dS^T K-major in smem, Q_i MN-major)
-                if (!(ok = wait_bounded_warp(BAR(C::B_DSFULL + dsb), dsph[dsb], abort_flag, p.err, kErrWaitBwdMma))) break;
-                dsph[dsb] ^= 1;
+                // S(s + NSLOT) into this slot (its P(s) is consumed by dV(s), issued before)
+                if (s + C::NSLOT < I.n && !(ok = open_step(slot))) break;
+                // dK(s), dQ(s)
+                if (!(ok = wait_bounded_warp(BAR(C::B_DSFULL + slot), dsph[slot], abort_flag, p.err, kErrWaitBwdMma))) break;
+                dsph[slot] ^= 1;
+                const int dqs = C::DQ_ALIAS ? slot : 0;
+                if (!C::DQ_ALIAS) {  // separate dQ region: previous tile drained?
+                    if (!(ok = wait_bounded_warp(BAR(C::B_DQEMPTY), dqeph[0] ^ 1, abort_flag, p.err, kErrWaitBwdMma))) break;
+                    dqeph[0] ^= 1;
+                }
                 tc_fence_after();
                 if (leader) {
-#pragma unroll
-                    for (int kk = 0; kk < C::BR / 16; ++kk)
-                        mma_f16_ss(tmem + C::TM_DK, sdesc_sw128(sDS + (kk / 4) * C::DS_BOX + (kk % 4) * 32, 16, 1024),
-                                   sdesc_sw128(sQ + kk * 2048, C::Q_BOX, 1024), C::IDESC_ACC, (s > 0 || kk > 0));
+                    mma_dk<C>(tmem, sDS, sQ, s > 0);
                     mma_commit(BAR(C::B_QEMPTY + st));
-                }
-                __syncwarp();
-                // dQ: d=128 -> dQ^T = K_j^T dS^T ; d=64 -> dQ = dS K_j  (both operands MN-major)
-                if (!(ok = wait_bounded_warp(BAR(C::B_DQEMPTY), dqeph ^ 1, abort_flag, p.err, kErrWaitBwdMma))) break;
-                dqeph ^= 1;
-                tc_fence_after();
-                if (leader) {
-#pragma unroll
-                    for (int kk = 0; kk < C::BC / 16; ++kk) {
-                        const uint64_t dk = sdesc_sw128(sK + kk * 2048, C::K_BOX, 1024);
-                        const uint64_t ds = sdesc_sw128(sDS + kk * 2048, C::DS_BOX, 1024);
-                        if (C::D == 128)
-                            mma_f16_ss(tmem + C::TM_DQ, dk, ds, C::IDESC_DQ, kk > 0);
-                        else
-                            mma_f16_ss(tmem + C::TM_DQ, ds, dk, C::IDESC_DQ, kk > 0);
-                    }
-                    mma_commit(BAR(C::B_DQFULL));
+                    mma_dq<C>(tmem + C::dq_col(slot), sK, sDS);
+                    mma_commit(BAR(C::B_DQFULL + dqs));
                     mma_commit(BAR(C::B_DSEMPTY + dsb));
                 }
                 __syncwarp();
+                // dP(s+1) for steps past the prologue
+                if (s + 1 < I.n && s + 1 >= C::NSLOT && !(ok = issue_dp((s + 1) % C::NSLOT, (st + 1) % C::STAGES)))
+                    break;
                 if (++st == C::STAGES) { st = 0; qph ^= 1; }
-                dsb ^= 1;
             }
             if (!ok) break;
             if (leader) {
@@ -316,6 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             __syncwarp();
         }
+        (void)qph;
         if (leader) mma_commit(BAR(C::B_DONE));
         __syncwarp();
         wait_bounded_warp(BAR(C::B_DONE), 0, abort_flag, p.err, kErrWaitDrain);
@@ -325,9 +388,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int wq = warp & 3;
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         const int kr = wq * 32 + lane;  // key row of this thread within the block
-        int st = 0, dsb = 0;
-        uint32_t qph = 0, sph = 0, dpph = 0, acph = 0;
-        uint32_t dseph[2] = {0, 0};
+        int st = 0;
+        uint32_t qph = 0, acph = 0;
+        uint32_t sph[2] = {0, 0}, dpph[2] = {0, 0}, dseph[2] = {0, 0};
         bool ok = true;
         for (int it = blockIdx.x; it < p.num_items && ok; it += gridDim.x) {
             const Item I = get_item<C, CAUSAL>(it, p);
@@ -345,31 +408,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                 continue;
             }
             for (int s = 0; s < I.n; ++s) {
+                const int slot = s % C::NSLOT;
+                const int dsb = s & 1;
                 const int i = I.i0 + s;
                 const int q0 = i * C::BR + h * C::HALF;  // first query column of this half
                 // statistics of this stage (LSE*log2e, D) -- readable once the stage is full
                 if (!(ok = wait_bounded_warp(BAR(C::B_QFULL + st), qph, abort_flag, p.err, kErrWaitBwdCompute))) break;
                 const float* lse2 = reinterpret_cast<const float*>(smem + C::OFF_STAT + st * C::STAT_BYTES) + h * C::HALF;
                 const float* dvec = lse2 + C::BR;
-                if (!(ok = wait_bounded_warp(BAR(C::B_SFULL), sph, abort_flag, p.err, kErrWaitBwdCompute))) break;
-                sph ^= 1;
+                if (!(ok = wait_bounded_warp(BAR(C::B_SFULL + slot), sph[slot], abort_flag, p.err, kErrWaitBwdCompute))) break;
+                sph[slot] ^= 1;
                 tc_fence_after();
                 uint32_t sr[C::HALF];
                 if constexpr (C::HALF == 32)
-                    tmem_ld32_wait(tmem + lane_off + C::TM_S + h * C::HALF, *reinterpret_cast<uint32_t(*)[32]>(sr));
+                    tmem_ld32_wait(tmem + lane_off + C::s_col(slot) + h * C::HALF, *reinterpret_cast<uint32_t(*)[32]>(sr));
                 else
-                    tmem_ld64_wait(tmem + lane_off + C::TM_S + h * C::HALF, *reinterpret_cast<uint32_t(*)[64]>(sr));
+                    tmem_ld64_wait(tmem + lane_off + C::s_col(slot) + h * C::HALF, *reinterpret_cast<uint32_t(*)[64]>(sr));
                 const bool need_mask = (I.kt * C::BC + C::BC > I.kvl) ||
                                        (CAUSAL && I.kt * C::BC + C::BC - 1 > i * C::BR);
                 const bool key_ok = key < I.kvl;
                 float pv[C::HALF];
+                const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
 #pragma unroll
                 for (int c = 0; c < C::HALF; c += 4) {
                     const float4 l4 = *reinterpret_cast<const float4*>(lse2 + c);
-                    pv[c + 0] = ex2_approx(fmaf(__uint_as_float(sr[c + 0]), p.scale_log2, -l4.x));
-                    pv[c + 1] = ex2_approx(fmaf(__uint_as_float(sr[c + 1]), p.scale_log2, -l4.y));
-                    pv[c + 2] = ex2_approx(fmaf(__uint_as_float(sr[c + 2]), p.scale_log2, -l4.z));
-                    pv[c + 3] = ex2_approx(fmaf(__uint_as_float(sr[c + 3]), p.scale_log2, -l4.w));
+                    const float2 x0 = ffma2(make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sl2,
+                                            make_float2(-l4.x, -l4.y));
+                    const float2 x1 = ffma2(make_float2(__uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3])), sl2,
+                                            make_float2(-l4.z, -l4.w));
+                    pv[c + 0] = ex2_approx(x0.x);
+                    pv[c + 1] = ex2_approx(x0.y);
+                    pv[c + 2] = ex2_approx(x1.x);
+                    pv[c + 3] = ex2_approx(x1.y);
                 }
                 if (need_mask) {
 #pragma unroll
@@ -383,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t w[C::HALF / 2];
 #pragma unroll
                     for (int c = 0; c < C::HALF / 2; ++c) w[c] = pack_bf16x2(pv[2 * c], pv[2 * c + 1]);
-                    const uint32_t tp = tmem + lane_off + C::TM_S + h * (C::HALF / 2);
+                    const uint32_t tp = tmem + lane_off + C::s_col(slot) + h * C::HALF;
                     if constexpr (C::HALF == 32) {
                         tmem_st16(tp, *reinterpret_cast<uint32_t(*)[16]>(w));
                     } else {
@@ -392,10 +462,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_st_wait();
                 }
                 tc_fence_before();
-                mbar_arrive(BAR(C::B_PFULL));
+                mbar_arrive(BAR(C::B_PFULL + slot));
                 // dS = P (dP - D)
-                if (!(ok = wait_bounded_warp(BAR(C::B_DPFULL), dpph, abort_flag, p.err, kErrWaitBwdCompute))) break;
-                dpph ^= 1;
+                if (!(ok = wait_bounded_warp(BAR(C::B_DPFULL + slot), dpph[slot], abort_flag, p.err, kErrWaitBwdCompute))) break;
+                dpph[slot] ^= 1;
                 tc_fence_after();
                 if (!(ok = wait_bounded_warp(BAR(C::B_DSEMPTY + dsb), dseph[dsb] ^ 1, abort_flag, p.err, kErrWaitBwdCompute))) break;
                 dseph[dsb] ^= 1;
@@ -405,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int cc = 0; cc < C::HALF; cc += 32) {
                     uint32_t dr[32];
-                    tmem_ld32_wait(tmem + lane_off + C::TM_DP + h * C::HALF + cc, dr);
+                    tmem_ld32_wait(tmem + lane_off + C::x_col(slot) + h * C::HALF + cc, dr);
 #pragma unroll
                     for (int c8 = 0; c8 < 32; c8 += 8) {
                         const int c = cc + c8;
@@ -428,9 +498,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
-                mbar_arrive(BAR(C::B_DSFULL + dsb));
+                mbar_arrive(BAR(C::B_DSFULL + slot));
                 if (++st == C::STAGES) { st = 0; qph ^= 1; }
-                dsb ^= 1;
             }
             if (!ok) break;
             // epilogue: warpgroup 0 writes dV_j, warpgroup 1 writes scale * dK_j
@@ -458,19 +527,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         const uint32_t stage = sbase + C::OFF_DQ + wq * C::DQ_WARP_BYTES;
         float* stage_f = reinterpret_cast<float*>(smem + C::OFF_DQ + wq * C::DQ_WARP_BYTES);
-        uint32_t dqph = 0;
+        uint32_t dqph[2] = {0, 0};
         bool ok = true;
         for (int it = blockIdx.x; it < p.num_items && ok; it += gridDim.x) {
             const Item I = get_item<C, CAUSAL>(it, p);
             for (int s = 0; s < I.n; ++s) {
                 const int i = I.i0 + s;
-                if (!(ok = wait_bounded_warp(BAR(C::B_DQFULL), dqph, abort_flag, p.err, kErrWaitBwdDq))) break;
-                dqph ^= 1;
+                const int dqs = C::DQ_ALIAS ? (s % C::NSLOT) : 0;
+                if (!(ok = wait_bounded_warp(BAR(C::B_DQFULL + dqs), dqph[dqs], abort_flag, p.err, kErrWaitBwdDq))) break;
+                dqph[dqs] ^= 1;
                 tc_fence_after();
                 uint32_t v[64];
-                tmem_ld64_wait(tmem + lane_off + C::TM_DQ, v);
+                tmem_ld64_wait(tmem + lane_off + C::dq_col(dqs), v);
                 tc_fence_before();
-                mbar_arrive(BAR(C::B_DQEMPTY));
+                mbar_arrive(BAR(C::B_DQEMPTY + dqs));
                 // the previous reduction of this warp must have finished reading the staging
                 if (lane == 0) bulk_wait_group_read<0>();
                 __syncwarp();
