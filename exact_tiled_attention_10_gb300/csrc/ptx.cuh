@@ -46,23 +46,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Every pipeline wait is bounded: after kWaitLimitNs the waiter records
+// Every pipeline wait is bounded: after about kWaitLimitNs the waiter records
 // `code` in the device error word, raises the CTA abort flag and returns
-// false, so a lost arrival can never hang the GPU.
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+// false, so a lost arrival can never hang the GPU.  The hot path is a bare
+// try_wait; the clock (SM cycles, converted at 1 cycle/ns, i.e. >= the limit
+// at any clock up to 1 GHz and ~2x shorter than stated at 2 GHz) and the abort
+// flag are only looked at every 64 polls.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // ~2 s at 1 GHz, ~1 s at 2 GHz
 
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                              unsigned int* err, unsigned int code,
                                              uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_timer_ns();
-    for (;;) {
+    const long long t0 = clock64();
+    for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (*abort_flag) return false;
-        if (global_timer_ns() - t0 > limit_ns) {
-            atomicOr(err, code);
-            *abort_flag = 1;
-            return false;
+        if ((i & 63u) == 0) {
+            if (*abort_flag) return false;
+            if ((uint64_t)(clock64() - t0) > limit_ns) {
+                atomicOr(err, code);
+                *abort_flag = 1;
+                return false;
+            }
         }
     }
 }
@@ -295,6 +300,30 @@ __device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
         : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
     return d;
 }
+// 2^x for a pair of floats on the FMA pipe (no MUFU), relative error <= 7.5e-5
+// for x >= -125 (below that the result is a tiny positive number <= 2^-124):
+//   r = round(x) (by adding 1.5*2^23), f = x - r in [-1/2, 1/2],
+//   2^f ~ c0 + c1 f + c2 f^2 + c3 f^3 (minimax in relative error on [-1/2, 1/2],
+//   coefficients from csrc/exp2_poly_fit.py), 2^r applied by adding r to the
+//   exponent field.
+constexpr float kExp2C0 = 9.999280735e-01f;
+constexpr float kExp2C1 = 6.932609855e-01f;
+constexpr float kExp2C2 = 2.426111222e-01f;
+constexpr float kExp2C3 = 5.517166906e-02f;
+__device__ __forceinline__ float2 exp2_poly2(float2 x) {
+    const float2 magic = make_float2(12582912.f, 12582912.f);
+    x.x = fmaxf(x.x, -125.f);
+    x.y = fmaxf(x.y, -125.f);
+    const float2 j = fadd2(x, magic);
+    const float2 r = fadd2(j, make_float2(-12582912.f, -12582912.f));
+    const float2 f = ffma2(r, make_float2(-1.f, -1.f), x);
+    float2 q = ffma2(make_float2(kExp2C3, kExp2C3), f, make_float2(kExp2C2, kExp2C2));
+    q = ffma2(q, f, make_float2(kExp2C1, kExp2C1));
+    q = ffma2(q, f, make_float2(kExp2C0, kExp2C0));
+    return make_float2(__uint_as_float(__float_as_uint(q.x) + (__float_as_uint(j.x) << 23)),
+                       __uint_as_float(__float_as_uint(q.y) + (__float_as_uint(j.y) << 23)));
+}
+
 // Max of n floats (n a multiple of 16, n >= 16) with 8 independent chains of
 // 3-input max, then a 3-level tree: short dependency chains, half the
 // instructions of a pairwise loop.
