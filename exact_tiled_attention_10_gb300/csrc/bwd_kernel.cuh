@@ -146,17 +146,15 @@ __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* m, uint32_t
         : "memory");
 }
 
-// ---- MMA groups (issued by one thread) ----
+// ---- MMA groups (warp-wide issue, one elected lane) ----
+// All descriptors arrive as precomputed bases; per-MMA offsets are constants.
 // S^T = K_j Q_i^T  or  dP^T = V_j dO_i^T  (K-major operands)
 template <class C>
-__device__ __forceinline__ void mma_scores(uint32_t d_tmem, uint32_t kv_smem, uint32_t q_smem) {
+__device__ __forceinline__ void mma_scores(uint32_t d_tmem, uint64_t kv_desc, uint64_t q_desc) {
 #pragma unroll
-    for (int kk = 0; kk < C::D / 16; ++kk) {
-        const uint32_t o = (kk / 4) * C::K_BOX + (kk % 4) * 32;
-        const uint32_t oq = (kk / 4) * C::Q_BOX + (kk % 4) * 32;
-        mma_f16_ss(d_tmem, sdesc_sw128(kv_smem + o, 16, 1024), sdesc_sw128(q_smem + oq, 16, 1024), C::IDESC_S,
-                   kk > 0);
-    }
+    for (int kk = 0; kk < C::D / 16; ++kk)
+        mma_f16_ss_w(d_tmem, desc_add(kv_desc, (kk / 4) * C::K_BOX + (kk % 4) * 32),
+                     desc_add(q_desc, (kk / 4) * C::Q_BOX + (kk % 4) * 32), C::IDESC_S, kk > 0);
 }
 // TMEM column of the packed P^T for queries [16 kk, 16 kk + 16): each compute
 // warpgroup h writes its half at the start of its own S^T columns (never into
@@ -165,33 +163,33 @@ template <class C>
 __device__ __forceinline__ constexpr uint32_t p_col(int kk) {
     return (uint32_t)(((kk * 16) / C::HALF) * C::HALF + ((kk * 16) % C::HALF) / 2);
 }
-// dV_j (+)= P^T dO_i  (P^T from TMEM, dO_i MN-major)
+// dV_j (+)= P^T dO_i  (P^T from TMEM, dO_i MN-major: do_mn = MN-major base)
 template <class C>
-__device__ __forceinline__ void mma_dv(uint32_t tmem, uint32_t s_tmem, uint32_t do_smem, bool acc) {
+__device__ __forceinline__ void mma_dv(uint32_t tmem, uint32_t s_tmem, uint64_t do_mn, bool acc) {
 #pragma unroll
     for (int kk = 0; kk < C::BR / 16; ++kk)
-        mma_f16_ts(tmem + C::TM_DV, s_tmem + p_col<C>(kk), sdesc_sw128(do_smem + kk * 2048, C::Q_BOX, 1024),
-                   C::IDESC_ACC, (acc || kk > 0) ? 1u : 0u);
+        mma_f16_ts_w(tmem + C::TM_DV, s_tmem + p_col<C>(kk), desc_add(do_mn, kk * 2048), C::IDESC_ACC,
+                     (acc || kk > 0) ? 1u : 0u);
 }
 // dK_j (+)= dS^T Q_i  (dS^T K-major in smem, Q_i MN-major)
 template <class C>
-__device__ __forceinline__ void mma_dk(uint32_t tmem, uint32_t ds_smem, uint32_t q_smem, bool acc) {
+__device__ __forceinline__ void mma_dk(uint32_t tmem, uint64_t ds_k, uint64_t q_mn, bool acc) {
 #pragma unroll
     for (int kk = 0; kk < C::BR / 16; ++kk)
-        mma_f16_ss(tmem + C::TM_DK, sdesc_sw128(ds_smem + (kk / 4) * C::DS_BOX + (kk % 4) * 32, 16, 1024),
-                   sdesc_sw128(q_smem + kk * 2048, C::Q_BOX, 1024), C::IDESC_ACC, (acc || kk > 0) ? 1u : 0u);
+        mma_f16_ss_w(tmem + C::TM_DK, desc_add(ds_k, (kk / 4) * C::DS_BOX + (kk % 4) * 32),
+                     desc_add(q_mn, kk * 2048), C::IDESC_ACC, (acc || kk > 0) ? 1u : 0u);
 }
 // d=128: dQ^T = K_j^T dS^T ; d=64: dQ = dS K_j  (both operands MN-major)
 template <class C>
-__device__ __forceinline__ void mma_dq(uint32_t d_tmem, uint32_t k_smem, uint32_t ds_smem) {
+__device__ __forceinline__ void mma_dq(uint32_t d_tmem, uint64_t k_mn, uint64_t ds_mn) {
 #pragma unroll
     for (int kk = 0; kk < C::BC / 16; ++kk) {
-        const uint64_t dk = sdesc_sw128(k_smem + kk * 2048, C::K_BOX, 1024);
-        const uint64_t ds = sdesc_sw128(ds_smem + kk * 2048, C::DS_BOX, 1024);
+        const uint64_t dk = desc_add(k_mn, kk * 2048);
+        const uint64_t ds = desc_add(ds_mn, kk * 2048);
         if (C::D == 128)
-            mma_f16_ss(d_tmem, dk, ds, C::IDESC_DQ, kk > 0);
+            mma_f16_ss_w(d_tmem, dk, ds, C::IDESC_DQ, kk > 0);
         else
-            mma_f16_ss(d_tmem, ds, dk, C::IDESC_DQ, kk > 0);
+            mma_f16_ss_w(d_tmem, ds, dk, C::IDESC_DQ, kk > 0);
     }
 }
 
@@ -291,18 +289,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         int st = 0, st_ahead = 0;  // Q ring stage of step s / of the next step to open
         uint32_t qph = 0, qph_ahead = 0, kvph = 0, aeph = 0;
         uint32_t pph[2] = {0, 0}, dsph[2] = {0, 0}, dqeph[2] = {0, 0};
-        const bool leader = (lane == 0);
-        const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V;
+        const uint64_t k_kd = sdesc_sw128(sbase + C::OFF_K, 16, 1024);
+        const uint64_t v_kd = sdesc_sw128(sbase + C::OFF_V, 16, 1024);
+        const uint64_t k_mn = sdesc_sw128(sbase + C::OFF_K, C::K_BOX, 1024);
+        const uint64_t q_kd0 = sdesc_sw128(sbase + C::OFF_Q, 16, 1024);
+        const uint64_t q_mn0 = sdesc_sw128(sbase + C::OFF_Q, C::Q_BOX, 1024);
+        const uint64_t do_kd0 = sdesc_sw128(sbase + C::OFF_DO, 16, 1024);
+        const uint64_t do_mn0 = sdesc_sw128(sbase + C::OFF_DO, C::Q_BOX, 1024);
+        const uint64_t ds_kd0 = sdesc_sw128(sbase + C::OFF_DS, 16, 1024);
+        const uint64_t ds_mn0 = sdesc_sw128(sbase + C::OFF_DS, C::DS_BOX, 1024);
         bool ok = true;
         // open_step(slot): wait for the next step's Q/dO stage and issue its S
         auto open_step = [&](int slot) -> bool {
             if (!wait_bounded_warp(BAR(C::B_QFULL + st_ahead), qph_ahead, abort_flag, p.err, kErrWaitBwdMma)) return false;
             tc_fence_after();
-            if (leader) {
-                mma_scores<C>(tmem + C::s_col(slot), sK, sbase + C::OFF_Q + st_ahead * C::Q_TILE);
-                mma_commit(BAR(C::B_SFULL + slot));
-            }
-            __syncwarp();
+            mma_scores<C>(tmem + C::s_col(slot), k_kd, desc_add(q_kd0, st_ahead * C::Q_TILE));
+            mma_commit_w(BAR(C::B_SFULL + slot));
             if (++st_ahead == C::STAGES) { st_ahead = 0; qph_ahead ^= 1; }
             return true;
         };
@@ -315,11 +317,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 dqeph[slot] ^= 1;
             }
             tc_fence_after();
-            if (leader) {
-                mma_scores<C>(tmem + C::x_col(slot), sV, sbase + C::OFF_DO + stage * C::Q_TILE);
-                mma_commit(BAR(C::B_DPFULL + slot));
-            }
-            __syncwarp();
+            mma_scores<C>(tmem + C::x_col(slot), v_kd, desc_add(do_kd0, stage * C::Q_TILE));
+            mma_commit_w(BAR(C::B_DPFULL + slot));
             return true;
         };
         for (int it = blockIdx.x; it < p.num_items && ok; it += gridDim.x) {
@@ -334,9 +333,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int s = 0; s < I.n; ++s) {
                 const int slot = s % C::NSLOT;
                 const int dsb = s & 1;
-                const uint32_t sQ = sbase + C::OFF_Q + st * C::Q_TILE;
-                const uint32_t sDO = sbase + C::OFF_DO + st * C::Q_TILE;
-                const uint32_t sDS = sbase + C::OFF_DS + dsb * C::DS_TILE;
                 // dV(s)
                 if (!(ok = wait_bounded_warp(BAR(C::B_PFULL + slot), pph[slot], abort_flag, p.err, kErrWaitBwdMma))) break;
                 pph[slot] ^= 1;
@@ -345,8 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     aeph ^= 1;
                 }
                 tc_fence_after();
-                if (leader) mma_dv<C>(tmem, tmem + C::s_col(slot), sDO, s > 0);
-                __syncwarp();
+                mma_dv<C>(tmem, tmem + C::s_col(slot), desc_add(do_mn0, st * C::Q_TILE), s > 0);
                 // S(s + NSLOT) into this slot (its P(s) is consumed by dV(s), issued before)
                 if (s + C::NSLOT < I.n && !(ok = open_step(slot))) break;
                 // dK(s), dQ(s)
@@ -358,29 +353,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                     dqeph[0] ^= 1;
                 }
                 tc_fence_after();
-                if (leader) {
-                    mma_dk<C>(tmem, sDS, sQ, s > 0);
-                    mma_commit(BAR(C::B_QEMPTY + st));
-                    mma_dq<C>(tmem + C::dq_col(slot), sK, sDS);
-                    mma_commit(BAR(C::B_DQFULL + dqs));
-                    mma_commit(BAR(C::B_DSEMPTY + dsb));
-                }
-                __syncwarp();
+                mma_dk<C>(tmem, desc_add(ds_kd0, dsb * C::DS_TILE), desc_add(q_mn0, st * C::Q_TILE), s > 0);
+                mma_commit_w(BAR(C::B_QEMPTY + st));
+                mma_dq<C>(tmem + C::dq_col(slot), k_mn, desc_add(ds_mn0, dsb * C::DS_TILE));
+                mma_commit_w(BAR(C::B_DQFULL + dqs));
+                mma_commit_w(BAR(C::B_DSEMPTY + dsb));
                 // dP(s+1) for steps past the prologue
                 if (s + 1 < I.n && s + 1 >= C::NSLOT && !(ok = issue_dp((s + 1) % C::NSLOT, (st + 1) % C::STAGES)))
                     break;
                 if (++st == C::STAGES) { st = 0; qph ^= 1; }
             }
             if (!ok) break;
-            if (leader) {
-                mma_commit(BAR(C::B_KVEMPTY));
-                mma_commit(BAR(C::B_ACCFULL));
-            }
-            __syncwarp();
+            mma_commit_w(BAR(C::B_KVEMPTY));
+            mma_commit_w(BAR(C::B_ACCFULL));
         }
         (void)qph;
-        if (leader) mma_commit(BAR(C::B_DONE));
-        __syncwarp();
+        mma_commit_w(BAR(C::B_DONE));
         wait_bounded_warp(BAR(C::B_DONE), 0, abort_flag, p.err, kErrWaitDrain);
     } else if (warp < 8) {
         // ------------------------------------------------------------ compute warpgroups

@@ -62,7 +62,13 @@ struct Cfg {
     static constexpr int KV_BOX = BC * 128;
     static constexpr int Q_TILE = BR * ROW_BYTES;
     static constexpr int KV_TILE = BC * ROW_BYTES;
-    static constexpr int STAGES = (NPART * KV_TILE >= 32768) ? 2 : 3;
+    // K is needed a step earlier than V (S(j+1) is issued before PV(j+1)), so it
+    // gets the deeper ring when shared memory allows
+    static constexpr int KV_BUDGET = 232448 - 2048 - NPART * QT * Q_TILE;
+    static constexpr int VSTAGES = (KV_TILE >= 32768 || SPLIT) ? 2 : 3;
+    static constexpr int KSTAGES_FIT = (KV_BUDGET - VSTAGES * KV_TILE) / (NPART * KV_TILE);
+    static constexpr int KSTAGES = KSTAGES_FIT > 4 ? 4 : KSTAGES_FIT;
+    static_assert(KSTAGES >= 2, "K ring");
     static constexpr int KSTEP = 32 / ELEM;         // K elements per MMA instruction
     static constexpr int S_STEPS = ROW_BYTES / 32;  // MMAs per S tile
     static constexpr int PV_STEPS = BC / KSTEP;     // MMAs per P V
@@ -74,13 +80,13 @@ struct Cfg {
     static constexpr int OFF_Q = 0;
     static constexpr int K_STAGE = NPART * KV_TILE;
     static constexpr int OFF_K = OFF_Q + NPART * QT * Q_TILE;
-    static constexpr int OFF_V = OFF_K + STAGES * K_STAGE;
-    static constexpr int OFF_BAR = OFF_V + STAGES * KV_TILE;
+    static constexpr int OFF_V = OFF_K + KSTAGES * K_STAGE;
+    static constexpr int OFF_BAR = OFF_V + VSTAGES * KV_TILE;
     // barrier indices
     static constexpr int B_QFULL = 0, B_QEMPTY = 2;  // one per query tile
-    static constexpr int B_KFULL = 4, B_KEMPTY = 4 + STAGES;
-    static constexpr int B_VFULL = 4 + 2 * STAGES, B_VEMPTY = 4 + 3 * STAGES;
-    static constexpr int B_SFULL = 4 + 4 * STAGES, B_PFULL = B_SFULL + 2;
+    static constexpr int B_KFULL = 4, B_KEMPTY = 4 + KSTAGES;
+    static constexpr int B_VFULL = 4 + 2 * KSTAGES, B_VEMPTY = B_VFULL + VSTAGES;
+    static constexpr int B_SFULL = B_VEMPTY + VSTAGES, B_PFULL = B_SFULL + 2;
     static constexpr int B_OFULL = B_PFULL + 2, B_OEMPTY = B_OFULL + 2;
     static constexpr int B_DONE = B_OEMPTY + 2;
     static constexpr int NBAR = B_DONE + 1;
@@ -133,37 +139,39 @@ __device__ __forceinline__ Item get_item(int it, const FwdParams& p) {
 
 // S_t = Q_t K^T over the head dimension (both operands K-major, 128B swizzle).
 // With SPLIT, the three products hi.hi + hi.lo + lo.hi accumulate in turn.
+// q_desc / k_desc: descriptors of the tile bases (hi parts); all per-MMA offsets
+// are compile-time constants added to the start-address field.
 template <class C>
-__device__ __forceinline__ void issue_S(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
+__device__ __forceinline__ void issue_S(uint32_t d_tmem, uint64_t q_desc, uint64_t k_desc) {
 #pragma unroll
     for (int part = 0; part < (C::SPLIT ? 3 : 1); ++part) {
-        const uint32_t qs = q_smem + (part == 2 ? C::QT * C::Q_TILE : 0);
-        const uint32_t ks = k_smem + (part == 1 ? C::KV_TILE : 0);
+        const uint64_t qd = desc_add(q_desc, part == 2 ? C::QT * C::Q_TILE : 0);
+        const uint64_t kd = desc_add(k_desc, part == 1 ? C::KV_TILE : 0);
 #pragma unroll
         for (int kk = 0; kk < C::S_STEPS; ++kk) {
             const uint32_t off_in = (kk % 4) * 32;
-            const uint64_t a = sdesc_sw128(qs + (kk / 4) * C::Q_BOX + off_in, 16, 1024);
-            const uint64_t b = sdesc_sw128(ks + (kk / 4) * C::KV_BOX + off_in, 16, 1024);
+            const uint64_t a = desc_add(qd, (kk / 4) * C::Q_BOX + off_in);
+            const uint64_t b = desc_add(kd, (kk / 4) * C::KV_BOX + off_in);
             const uint32_t acc = (part > 0 || kk > 0) ? 1u : 0u;
             if constexpr (C::FP8)
-                mma_f8_ss(d_tmem, a, b, C::IDESC_S, acc);
+                mma_f8_ss_w(d_tmem, a, b, C::IDESC_S, acc);
             else
-                mma_f16_ss(d_tmem, a, b, C::IDESC_S, acc);
+                mma_f16_ss_w(d_tmem, a, b, C::IDESC_S, acc);
         }
     }
 }
 
 // O_t (+)= P_t V over the keys; P_t from TMEM, V MN-major (head dim contiguous)
 template <class C>
-__device__ __forceinline__ void issue_PV(uint32_t o_tmem, uint32_t p_tmem, uint32_t v_smem,
-                                         bool accumulate) {
+__device__ __forceinline__ void issue_PV(uint32_t o_tmem, uint32_t p_tmem, uint64_t v_desc, bool accumulate) {
 #pragma unroll
     for (int kk = 0; kk < C::PV_STEPS; ++kk) {
-        const uint64_t b = sdesc_sw128(v_smem + kk * C::KSTEP * 128, C::KV_BOX, 1024);
+        const uint64_t b = desc_add(v_desc, kk * C::KSTEP * 128);
+        const uint32_t acc = (accumulate || kk > 0) ? 1u : 0u;
         if constexpr (C::FP8)
-            mma_f8_ts(o_tmem, p_tmem + kk * 8, b, C::IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
+            mma_f8_ts_w(o_tmem, p_tmem + kk * 8, b, C::IDESC_PV, acc);
         else
-            mma_f16_ts(o_tmem, p_tmem + kk * 8, b, C::IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
+            mma_f16_ts_w(o_tmem, p_tmem + kk * 8, b, C::IDESC_PV, acc);
     }
 }
 
@@ -200,9 +208,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(BAR(C::B_QFULL + t), 1);
             mbar_init(BAR(C::B_QEMPTY + t), 1);
         }
-        for (int s = 0; s < C::STAGES; ++s) {
+        for (int s = 0; s < C::KSTAGES; ++s) {
             mbar_init(BAR(C::B_KFULL + s), 1);
             mbar_init(BAR(C::B_KEMPTY + s), 1);
+        }
+        for (int s = 0; s < C::VSTAGES; ++s) {
             mbar_init(BAR(C::B_VFULL + s), 1);
             mbar_init(BAR(C::B_VEMPTY + s), 1);
         }
@@ -237,8 +247,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------ TMA producer
         // The whole warp walks the schedule (so it stays converged); lane 0 issues.
-        int st = 0;
-        uint32_t ph = 0, qe = 0;
+        int kst = 0, vst = 0;
+        uint32_t kph = 0, vph = 0, qe = 0;
         bool ok = true;
         for (int it = blockIdx.x; it < p.num_items && ok; it += gridDim.x) {
             const Item I = get_item<C, CAUSAL>(it, p);
@@ -260,36 +270,51 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok) break;
             qe ^= 1;
-            for (int j = 0; j < I.nmax; ++j) {
-                if (!(ok = wait_bounded_warp(BAR(C::B_KEMPTY + st), ph ^ 1, abort_flag, p.err, kErrWaitFwdProducer))) break;
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(BAR(C::B_KFULL + st), C::K_STAGE);
-                    for (int part = 0; part < C::NPART; ++part)
+            // K runs one tile ahead of V (K_0 K_1 V_0 K_2 V_1 ...): S(j+1) needs K_{j+1}
+            // before P V(j+1) needs V_{j+1}
+            for (int idx = 0; idx <= I.nmax && ok; ++idx) {
+                if (idx < I.nmax) {
+                    if (!(ok = wait_bounded_warp(BAR(C::B_KEMPTY + kst), kph ^ 1, abort_flag, p.err, kErrWaitFwdProducer))) break;
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(BAR(C::B_KFULL + kst), C::K_STAGE);
+                        for (int part = 0; part < C::NPART; ++part)
+                            for (int bx = 0; bx < C::NBOX; ++bx)
+                                tma_load_3d(sbase + C::OFF_K + kst * C::K_STAGE + part * C::KV_TILE + bx * C::KV_BOX,
+                                            part ? &tkl : &tk, BAR(C::B_KFULL + kst), bx * C::BOX_ELEMS, idx * C::BC, I.bh);
+                    }
+                    __syncwarp();
+                    if (++kst == C::KSTAGES) { kst = 0; kph ^= 1; }
+                }
+                if (idx >= 1) {
+                    const int j = idx - 1;
+                    if (!(ok = wait_bounded_warp(BAR(C::B_VEMPTY + vst), vph ^ 1, abort_flag, p.err, kErrWaitFwdProducer))) break;
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(BAR(C::B_VFULL + vst), C::KV_TILE);
                         for (int bx = 0; bx < C::NBOX; ++bx)
-                            tma_load_3d(sbase + C::OFF_K + st * C::K_STAGE + part * C::KV_TILE + bx * C::KV_BOX,
-                                        part ? &tkl : &tk, BAR(C::B_KFULL + st), bx * C::BOX_ELEMS, j * C::BC, I.bh);
+                            tma_load_3d(sbase + C::OFF_V + vst * C::KV_TILE + bx * C::KV_BOX, &tv, BAR(C::B_VFULL + vst),
+                                        bx * C::BOX_ELEMS, j * C::BC, I.bh);
+                    }
+                    __syncwarp();
+                    if (++vst == C::VSTAGES) { vst = 0; vph ^= 1; }
                 }
-                __syncwarp();
-                if (!(ok = wait_bounded_warp(BAR(C::B_VEMPTY + st), ph ^ 1, abort_flag, p.err, kErrWaitFwdProducer))) break;
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(BAR(C::B_VFULL + st), C::KV_TILE);
-                    for (int bx = 0; bx < C::NBOX; ++bx)
-                        tma_load_3d(sbase + C::OFF_V + st * C::KV_TILE + bx * C::KV_BOX, &tv, BAR(C::B_VFULL + st),
-                                    bx * C::BOX_ELEMS, j * C::BC, I.bh);
-                }
-                __syncwarp();
-                if (++st == C::STAGES) { st = 0; ph ^= 1; }
             }
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
-        // The whole warp walks the schedule and waits; lane 0 issues tcgen05.
+        // The whole warp walks the schedule and waits; one elected lane issues
+        // each tcgen05 op.  Shared-memory descriptors are built once here and
+        // advanced by constants, so the issue rate stays above the tensor rate.
         int kst = 0, vst = 0;
         uint32_t kph = 0, vph = 0, qph = 0;
         uint32_t pph[2] = {0, 0}, oeph[2] = {0, 0};
-        const uint32_t tS[2] = {tmem + C::TM_S0, tmem + C::TM_S1};
-        const uint32_t tO[2] = {tmem + C::TM_O0, tmem + C::TM_O1};
-        const bool leader = (lane == 0);
+        const uint64_t q_desc0 = sdesc_sw128(sbase + C::OFF_Q, 16, 1024);
+        const uint64_t k_desc0 = sdesc_sw128(sbase + C::OFF_K, 16, 1024);
+        const uint64_t v_desc0 = sdesc_sw128(sbase + C::OFF_V, C::KV_BOX, 1024);
+        auto q_desc = [&](int t) { return desc_add(q_desc0, t * C::Q_TILE); };
+        auto k_desc = [&](int st) { return desc_add(k_desc0, st * C::K_STAGE); };
+        auto v_desc = [&](int st) { return desc_add(v_desc0, st * C::KV_TILE); };
+        auto tS = [&](int t) { return tmem + (t ? C::TM_S1 : C::TM_S0); };
+        auto tO = [&](int t) { return tmem + (t ? C::TM_O1 : C::TM_O0); };
         bool ok = true;
         for (int it = blockIdx.x; it < p.num_items && ok; it += gridDim.x) {
             const Item I = get_item<C, CAUSAL>(it, p);
@@ -300,18 +325,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             qph ^= 1;
             if (!(ok = wait_bounded_warp(BAR(C::B_KFULL + kst), kph, abort_flag, p.err, kErrWaitFwdMma))) break;
             tc_fence_after();
-            if (leader) {
-                for (int t = 0; t < 2; ++t) {
-                    if (I.n[t] > 0) {
-                        issue_S<C>(tS[t], sbase + C::OFF_Q + t * C::Q_TILE, sbase + C::OFF_K + kst * C::K_STAGE);
-                        mma_commit(BAR(C::B_SFULL + t));
-                    }
-                    if (I.n[t] <= 1) mma_commit(BAR(C::B_QEMPTY + t));  // Q_t no longer needed
+            for (int t = 0; t < 2; ++t) {
+                if (I.n[t] > 0) {
+                    issue_S<C>(tS(t), q_desc(t), k_desc(kst));
+                    mma_commit_w(BAR(C::B_SFULL + t));
                 }
-                mma_commit(BAR(C::B_KEMPTY + kst));
+                if (I.n[t] <= 1) mma_commit_w(BAR(C::B_QEMPTY + t));  // Q_t no longer needed
             }
-            __syncwarp();
-            if (++kst == C::STAGES) { kst = 0; kph ^= 1; }
+            mma_commit_w(BAR(C::B_KEMPTY + kst));
+            if (++kst == C::KSTAGES) { kst = 0; kph ^= 1; }
             for (int j = 0; j < I.nmax && ok; ++j) {
                 bool vw = false, kw = false;
                 for (int t = 0; t < 2; ++t) {
@@ -327,37 +349,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                         vw = true;
                     }
                     tc_fence_after();
-                    if (leader) issue_PV<C>(tO[t], tS[t], sbase + C::OFF_V + vst * C::KV_TILE, j > 0);
+                    issue_PV<C>(tO(t), tS(t), v_desc(vst), j > 0);
                     if (j == I.n[t] - 1) {
-                        if (leader) mma_commit(BAR(C::B_OFULL + t));
+                        mma_commit_w(BAR(C::B_OFULL + t));
                     } else {
                         if (!kw) {
                             if (!(ok = wait_bounded_warp(BAR(C::B_KFULL + kst), kph, abort_flag, p.err, kErrWaitFwdMma))) break;
                             kw = true;
                             tc_fence_after();
                         }
-                        if (leader) {
-                            issue_S<C>(tS[t], sbase + C::OFF_Q + t * C::Q_TILE, sbase + C::OFF_K + kst * C::K_STAGE);
-                            mma_commit(BAR(C::B_SFULL + t));
-                            if (j + 2 == I.n[t]) mma_commit(BAR(C::B_QEMPTY + t));  // last S_t issued
-                        }
+                        issue_S<C>(tS(t), q_desc(t), k_desc(kst));
+                        mma_commit_w(BAR(C::B_SFULL + t));
+                        if (j + 2 == I.n[t]) mma_commit_w(BAR(C::B_QEMPTY + t));  // last S_t issued
                     }
-                    __syncwarp();
                 }
                 if (!ok) break;
-                if (leader) mma_commit(BAR(C::B_VEMPTY + vst));
-                if (++vst == C::STAGES) { vst = 0; vph ^= 1; }
+                mma_commit_w(BAR(C::B_VEMPTY + vst));
+                if (++vst == C::VSTAGES) { vst = 0; vph ^= 1; }
                 if (kw) {
-                    if (leader) mma_commit(BAR(C::B_KEMPTY + kst));
-                    if (++kst == C::STAGES) { kst = 0; kph ^= 1; }
+                    mma_commit_w(BAR(C::B_KEMPTY + kst));
+                    if (++kst == C::KSTAGES) { kst = 0; kph ^= 1; }
                 }
-                __syncwarp();
             }
             if (!ok) break;
         }
         // drain: every MMA this warp issued has completed before TMEM is freed
-        if (leader) mma_commit(BAR(C::B_DONE));
-        __syncwarp();
+        mma_commit_w(BAR(C::B_DONE));
         wait_bounded_warp(BAR(C::B_DONE), 0, abort_flag, p.err, kErrWaitDrain);
     } else if (warp < 8) {
         // ------------------------------------------------------------ softmax
