@@ -50,6 +50,8 @@ _SIGS = {
     "fa_bwd_preprocess": ([_vp, _vp, _vp, _i, _i, _i, _i, _vp, _sz, _vp], _i),
     "fa_bwd_main": ([_vp] * 6 + [_i, _i, _i, _i, _f, _i, _vp, _vp, _sz, _vp], _i),
     "fa_bwd_dq": ([_vp, _i, _i, _i, _i, _f, _vp, _sz, _vp], _i),
+    "fa_bwd_noalloc_max_scratch": ([], _sz),
+    "fa_bwd_noalloc": ([_vp] * 9 + [_i, _i, _i, _i, _f, _i, _vp, _vp], _i),
     "fa_fp8_num_blocks": ([_i], _i),
     "fa_quantize_fp8": ([_vp, _vp, _vp, _i, _i, _i, _i, _vp], _i),
     "fa_fwd_fp8": ([_vp] * 8 + [_i, _i, _i, _i, _f, _i, _vp, _vp], _i),

@@ -471,3 +471,66 @@ fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* v8, const float
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free backward.
+//
+// Some callers of this library cannot allocate device memory at all: for
+// example a plugin hosted inside a framework that owns the whole device-memory
+// pool and offers it no allocation hook, or a runtime that forbids allocation
+// once it has started so that its latency stays predictable.  For them the
+// backward's scratch (the row statistics and the float32 dQ accumulator) lives
+// in a fixed array of device memory that this library defines below; every GPU
+// that loads the library keeps it until the process exits.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = 128ull << 20;  // 128 MiB
+
+static __device__ __align__(256) unsigned char g_fa_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of the scratch array, looked up once per device (with that
+// device current).  In host code the array's name is only a stand-in symbol,
+// never a device address, so it is never passed to a kernel directly.
+void* g_noalloc_ptr[kMaxDevices] = {};
+std::mutex g_noalloc_mu;
+
+fa_status noalloc_scratch(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(FA_ERR_UNSUPPORTED, "device index %d out of range", dev);
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_fa_noalloc_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t fa_bwd_noalloc_max_scratch(void) { return kNoAllocScratchBytes; }
+
+fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                         const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale,
+                         int causal, const int* kv_lens, fa_stream_t stream) {
+    FA_TRY(check_common(B, H, N, d, scale));
+    const size_t need = fa_bwd_workspace_size(FA_BF16, B, H, N, d);
+    if (need > kNoAllocScratchBytes)
+        return fail(FA_ERR_INVALID_ARG,
+                    "fa_bwd_noalloc: this problem needs %zu bytes of scratch, more than the %zu-byte static array; "
+                    "use fa_bwd with a caller-provided workspace",
+                    need, kNoAllocScratchBytes);
+    void* scratch = nullptr;
+    FA_TRY(noalloc_scratch(&scratch));
+    return fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, causal, kv_lens, scratch,
+                  kNoAllocScratchBytes, stream);
+}
+
+}  // extern "C"

@@ -147,6 +147,27 @@ fa_status fa_bwd_ex(fa_dtype dtype, const void* q, const void* k, const void* v,
                     int B, int H, int N, int d, float scale, int causal, const int* kv_lens,
                     void* workspace, size_t workspace_bytes, fa_stream_t stream);
 
+/* Allocation-free backward (the pages have no counterpart: it only changes
+ * where the scratch lives).  For callers that cannot allocate device memory,
+ * e.g. a plugin inside a framework that owns the whole device-memory pool, or
+ * a runtime that forbids allocation after start-up.  Same arguments and
+ * results as fa_bwd, minus the workspace: the scratch is a fixed 128 MiB array
+ * of device memory defined in this library, which every GPU that loads the
+ * library keeps until the process exits.
+ *   - Problems whose scratch (fa_bwd_workspace_size(FA_BF16, ...)) exceeds
+ *     fa_bwd_noalloc_max_scratch() bytes are rejected with FA_ERR_INVALID_ARG.
+ *   - The first call on each device looks up the array's device address (no
+ *     allocation); make that first call before any stream capture.
+ *   - Every call uses the same array and leaves its contents behind; each call
+ *     re-initialises what it reads, but calls that overlap on the GPU (e.g. on
+ *     two streams) race on it and must be serialised by the caller.
+ *   - Calls no cudaMalloc / cudaFree and no allocating library routine. */
+size_t fa_bwd_noalloc_max_scratch(void);
+fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                         const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                         int B, int H, int N, int d, float scale, int causal,
+                         const int* kv_lens, fa_stream_t stream);
+
 /* -------------------------------------------------------------------- FP8 */
 
 /* Number of 64-row scale blocks per (b,h): ceil(N / 64). */
