@@ -249,7 +249,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         int st = 0;
         uint32_t ph = 0, kve = 0;
         bool ok = true;
-        for (int it = blockIdx.x; it < p.num_items && ok; it += gridDim.x) {
+        for (int rd = 0; rd < snake_rounds(p.num_items) && ok; ++rd) {
+            const int it = snake_item(rd, p.num_items);
+            if (it < 0) continue;
             const Item I = get_item<C, CAUSAL>(it, p);
             if (I.n == 0) continue;
             if (!(ok = wait_bounded_warp(BAR(C::B_KVEMPTY), kve ^ 1, abort_flag, p.err, kErrWaitBwdProducer))) break;
@@ -321,7 +323,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit_w(BAR(C::B_DPFULL + slot));
             return true;
         };
-        for (int it = blockIdx.x; it < p.num_items && ok; it += gridDim.x) {
+        for (int rd = 0; rd < snake_rounds(p.num_items) && ok; ++rd) {
+            const int it = snake_item(rd, p.num_items);
+            if (it < 0) continue;
             const Item I = get_item<C, CAUSAL>(it, p);
             if (I.n == 0) continue;
             if (!(ok = wait_bounded_warp(BAR(C::B_KVFULL), kvph, abort_flag, p.err, kErrWaitBwdMma))) break;
@@ -380,7 +384,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t qph = 0, acph = 0;
         uint32_t sph[2] = {0, 0}, dpph[2] = {0, 0}, dseph[2] = {0, 0};
         bool ok = true;
-        for (int it = blockIdx.x; it < p.num_items && ok; it += gridDim.x) {
+        for (int rd = 0; rd < snake_rounds(p.num_items) && ok; ++rd) {
+            const int it = snake_item(rd, p.num_items);
+            if (it < 0) continue;
             const Item I = get_item<C, CAUSAL>(it, p);
             const int key = I.kt * C::BC + kr;
             const size_t krow = (size_t)I.bh * p.N + key;
@@ -517,7 +523,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         float* stage_f = reinterpret_cast<float*>(smem + C::OFF_DQ + wq * C::DQ_WARP_BYTES);
         uint32_t dqph[2] = {0, 0};
         bool ok = true;
-        for (int it = blockIdx.x; it < p.num_items && ok; it += gridDim.x) {
+        for (int rd = 0; rd < snake_rounds(p.num_items) && ok; ++rd) {
+            const int it = snake_item(rd, p.num_items);
+            if (it < 0) continue;
             const Item I = get_item<C, CAUSAL>(it, p);
             for (int s = 0; s < I.n; ++s) {
                 const int i = I.i0 + s;

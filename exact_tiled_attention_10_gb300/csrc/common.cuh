@@ -23,6 +23,20 @@ enum : unsigned int {
 
 constexpr int kNumSMsDefault = 152;
 
+// Work order of the persistent kernels.  Items are numbered longest first
+// (causal: the query tiles, resp. key blocks, that see the most keys, resp.
+// queries); a CTA takes one item per round of gridDim.x items, and the rounds
+// alternate direction ("snake": CTA c takes rank r*G + c in even rounds and
+// r*G + G-1-c in odd ones), so that a CTA given a long item in one round gets
+// a short one in the next and the per-CTA totals stay near the mean.  Returns
+// -1 for a round in which this CTA has no item (the last, partial round).
+__device__ __forceinline__ int snake_item(int round, int num_items) {
+    const int G = (int)gridDim.x, c = (int)blockIdx.x;
+    const int it = round * G + ((round & 1) ? (G - 1 - c) : c);
+    return it < num_items ? it : -1;
+}
+__device__ __forceinline__ int snake_rounds(int num_items) { return (num_items + (int)gridDim.x - 1) / (int)gridDim.x; }
+
 struct FwdParams {
     int B, H, N;
     int num_qp;       // query-row pairs of 128-row tiles per head: ceil(N / 256)

@@ -39,10 +39,23 @@ namespace fwd {
 constexpr int kThreads = 384;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
+constexpr int kRegsSoftmax = 208, kRegsIssue = 88;
 // Conditional rescaling slack in the log2 domain: P values may reach 2^8
 // before the reference max is moved (bf16 path).  The FP8 path keeps the exact
 // max so that P <= 1 fits the E4M3 range after the value-scale fold.
 constexpr float kRescaleSlack = 8.0f;
+// Of every 8 pairs of exponentials in a key block without masked entries,
+// kPolyPer8 are evaluated by the cubic polynomial 2^x on the FMA pipe
+// (exp2_poly2) and the rest by the MUFU ex2 unit, so that the two units share
+// the work: MUFU alone (16 results per SM per cycle) would need as many cycles
+// per block as the two tensor-core products of that block.  The polynomial's
+// relative error (<= 7.5e-5) is far below the bf16 / E4M3 rounding of P.
+// Blocks with masked entries use MUFU only (ex2(-inf) = 0 exactly).
+#ifndef FA_FWD_POLY_PER8
+#define FA_FWD_POLY_PER8 0
+#endif
+constexpr int kPolyPer8 = FA_FWD_POLY_PER8;
+static_assert(kPolyPer8 >= 0 && kPolyPer8 <= 8, "share of polynomial exponentials");
 
 template <int D_, int BC_, bool FP8_, bool SPLIT_ = false>
 struct Cfg {
@@ -175,6 +188,60 @@ __device__ __forceinline__ void issue_PV(uint32_t o_tmem, uint32_t p_tmem, uint6
     }
 }
 
+// 2^x for a pair; pair index q (compile-time after unrolling) picks the unit
+template <bool POLY>
+__device__ __forceinline__ float2 exp2_pair(float2 x, int q) {
+    if (POLY && (q & 7) >= 8 - kPolyPer8) return exp2_poly2(x);
+    return make_float2(ex2_approx(x.x), ex2_approx(x.y));
+}
+
+// P = 2^(S * cm - m) for one row of a key block, written over the row's S
+// columns in TMEM as the A operand of the P V product (bf16 pairs, or E4M3
+// quadruples with the value-scale fold lg).  Returns the row sums: l (exact
+// weights, divided by the fold) and, for FP8, lq (the E4M3-rounded weights).
+template <class C, bool POLY>
+__device__ __forceinline__ void exp_block(const float (&s)[C::BC], const float (&cm)[2], const float (&lg)[2],
+                                          const float (&inv_w)[2], float mb, uint32_t tS, float& lsum,
+                                          float& lqsum) {
+    constexpr int CH = C::FP8 ? 64 : 32;  // columns per 16-word TMEM store
+    lsum = 0.f;
+    lqsum = 0.f;
+#pragma unroll
+    for (int ch = 0; ch < C::BC / CH; ++ch) {
+        const int h = (ch * CH) / (C::BC / 2);
+        const float2 cs2 = make_float2(cm[h], cm[h]), cb2 = make_float2(lg[h] - mb, lg[h] - mb);
+        uint32_t w[16];
+        float2 a2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        if constexpr (C::FP8) {
+            // lq sums the E4M3-rounded weights the P V product actually uses, so
+            // O stays a convex combination of the value rows; l keeps the exact
+            // sum for the LSE
+            __half2 hacc = __float2half2_rn(0.f);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const float* se = s + ch * CH + 4 * e;
+                const float2 p01 = exp2_pair<POLY>(ffma2(make_float2(se[0], se[1]), cs2, cb2), 2 * e);
+                const float2 p23 = exp2_pair<POLY>(ffma2(make_float2(se[2], se[3]), cs2, cb2), 2 * e + 1);
+                a2[e & 3] = fadd2(a2[e & 3], fadd2(p01, p23));
+                w[e] = pack_e4m3x4(p01.x, p01.y, p23.x, p23.y);
+                hacc = __hadd2(hacc, __hadd2(e4m3x2_to_half2(w[e] & 0xFFFFu), e4m3x2_to_half2(w[e] >> 16)));
+            }
+            const float2 hs = __half22float2(hacc);
+            lqsum += (hs.x + hs.y) * inv_w[h];
+        } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const float2 pp = exp2_pair<POLY>(ffma2(make_float2(s[ch * CH + 2 * e], s[ch * CH + 2 * e + 1]), cs2, cb2), e);
+                a2[e & 3] = fadd2(a2[e & 3], pp);
+                w[e] = pack_bf16x2(pp.x, pp.y);
+            }
+        }
+        const float2 t2 = fadd2(fadd2(a2[0], a2[1]), fadd2(a2[2], a2[3]));
+        lsum += (t2.x + t2.y) * inv_w[h];
+        tmem_st16(tS + ch * 16, w);
+    }
+}
+
 template <class C, bool OUT_F32>
 __device__ __forceinline__ void store_row_chunk(void* o_row, int c0, const float (&v)[32]) {
     if constexpr (OUT_F32) {
@@ -243,14 +310,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // registers: the softmax warpgroups take what the producer / MMA warpgroup
+    // (warps 8-11, 10 and 11 idle) does not need; 2 x 128 x kRegsSoftmax +
+    // 128 x kRegsIssue equals the launch allocation of 384 x 168
+    static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsIssue <= kThreads * 168, "register split");
 
+    if (warp >= 8) regs_dec<kRegsIssue>();
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------ TMA producer
         // The whole warp walks the schedule (so it stays converged); lane 0 issues.
         int kst = 0, vst = 0;
         uint32_t kph = 0, vph = 0, qe = 0;
         bool ok = true;
-        for (int it = blockIdx.x; it < p.num_items && ok; it += gridDim.x) {
+        for (int rd = 0; rd < snake_rounds(p.num_items) && ok; ++rd) {
+            const int it = snake_item(rd, p.num_items);
+            if (it < 0) continue;
             const Item I = get_item<C, CAUSAL>(it, p);
             if (I.nmax == 0) continue;
             // Q tile t of this item may load as soon as the previous item's last
@@ -316,7 +390,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto tS = [&](int t) { return tmem + (t ? C::TM_S1 : C::TM_S0); };
         auto tO = [&](int t) { return tmem + (t ? C::TM_O1 : C::TM_O0); };
         bool ok = true;
-        for (int it = blockIdx.x; it < p.num_items && ok; it += gridDim.x) {
+        for (int rd = 0; rd < snake_rounds(p.num_items) && ok; ++rd) {
+            const int it = snake_item(rd, p.num_items);
+            if (it < 0) continue;
             const Item I = get_item<C, CAUSAL>(it, p);
             if (I.nmax == 0) continue;
             for (int t = 0; t < 2 && ok; ++t)
@@ -378,6 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         wait_bounded_warp(BAR(C::B_DONE), 0, abort_flag, p.err, kErrWaitDrain);
     } else if (warp < 8) {
         // ------------------------------------------------------------ softmax
+        regs_inc<kRegsSoftmax>();
         const int t = warp >> 2;
         const int wq = warp & 3;
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
@@ -385,7 +462,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tO = tmem + lane_off + (t ? C::TM_O1 : C::TM_O0);
         const int r_in = wq * 32 + lane;
         uint32_t sph = 0, oph = 0;
-        for (int it = blockIdx.x; it < p.num_items; it += gridDim.x) {
+        for (int rd = 0; rd < snake_rounds(p.num_items); ++rd) {
+            const int it = snake_item(rd, p.num_items);
+            if (it < 0) continue;
             const Item I = get_item<C, CAUSAL>(it, p);
             const int n = I.n[t];
             const int tile_row0 = I.row0 + t * C::BR;
@@ -482,50 +561,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_st_wait();
                 }
                 const float mb = (m == -INFINITY) ? 0.f : m;
-                float lsum = 0.f, lqsum = 0.f;
-                constexpr int CH = C::FP8 ? 64 : 32;  // columns per 16-word TMEM store
-#pragma unroll
-                for (int ch = 0; ch < C::BC / CH; ++ch) {
-                    const int h = (ch * CH) / (C::BC / 2);
-                    const float cs = cm[h], cb = lg[h] - mb;
-                    uint32_t w[16];
-                    float acc0 = 0.f, acc1 = 0.f;
-                    if constexpr (C::FP8) {
-                        // lq sums the E4M3-rounded weights the P V product actually
-                        // uses, so O stays a convex combination of the value rows;
-                        // l keeps the exact sum for the LSE
-                        __half2 hacc = __float2half2_rn(0.f);
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const float p0 = ex2_approx(fmaf(s[ch * CH + 4 * e + 0], cs, cb));
-                            const float p1 = ex2_approx(fmaf(s[ch * CH + 4 * e + 1], cs, cb));
-                            const float p2 = ex2_approx(fmaf(s[ch * CH + 4 * e + 2], cs, cb));
-                            const float p3 = ex2_approx(fmaf(s[ch * CH + 4 * e + 3], cs, cb));
-                            acc0 += p0 + p1;
-                            acc1 += p2 + p3;
-                            w[e] = pack_e4m3x4(p0, p1, p2, p3);
-                            hacc = __hadd2(hacc, __hadd2(e4m3x2_to_half2(w[e] & 0xFFFFu), e4m3x2_to_half2(w[e] >> 16)));
-                        }
-                        const float2 hs = __half22float2(hacc);
-                        lqsum += (hs.x + hs.y) * inv_w[h];
-                    } else {
-                        const float2 cs2 = make_float2(cs, cs), cb2 = make_float2(cb, cb);
-                        float2 a2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                                        make_float2(0.f, 0.f)};
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const float2 x = ffma2(make_float2(s[ch * CH + 2 * e], s[ch * CH + 2 * e + 1]), cs2, cb2);
-                            const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-                            a2[e & 3] = fadd2(a2[e & 3], pp);
-                            w[e] = pack_bf16x2(pp.x, pp.y);
-                        }
-                        const float2 t2 = fadd2(fadd2(a2[0], a2[1]), fadd2(a2[2], a2[3]));
-                        acc0 = t2.x;
-                        acc1 = t2.y;
-                    }
-                    lsum += (acc0 + acc1) * inv_w[h];
-                    tmem_st16(tS + ch * 16, w);
-                }
+                float lsum, lqsum;
+                if (need_mask)
+                    exp_block<C, false>(s, cm, lg, inv_w, mb, tS, lsum, lqsum);
+                else
+                    exp_block<C, true>(s, cm, lg, inv_w, mb, tS, lsum, lqsum);
                 l += lsum;
                 if (C::FP8) lq += lqsum;
                 tmem_st_wait();

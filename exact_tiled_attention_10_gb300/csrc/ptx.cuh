@@ -325,6 +325,16 @@ constexpr uint32_t kFmtBF16 = 1;  // kind::f16
 constexpr uint32_t kFmtE4M3 = 0;  // kind::f8f6f4
 
 // ------------------------------------------------------------------ numerics
+// Per-warpgroup register budget (all four warps of the warpgroup execute it).
+// The sum over warpgroups must stay within the block's launch allocation.
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
     float d;
     asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
