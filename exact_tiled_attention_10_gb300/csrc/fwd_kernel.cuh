@@ -39,11 +39,18 @@ namespace fwd {
 constexpr int kThreads = 384;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr int kRegsSoftmax = 208, kRegsIssue = 88;
+constexpr int kRegsSoftmax = 192, kRegsIssue = 120;
 // Conditional rescaling slack in the log2 domain: P values may reach 2^8
 // before the reference max is moved (bf16 path).  The FP8 path keeps the exact
 // max so that P <= 1 fits the E4M3 range after the value-scale fold.
 constexpr float kRescaleSlack = 8.0f;
+// bf16 path: after the first block, P is computed with the current reference
+// max while the block's own row max is found in the same pass (3-input max on
+// the ALU pipe, beside the exponentials).  Only when some row's max exceeds
+// the reference by more than kRescaleSlack does the warp rescale O and l and
+// recompute the block's P (still in registers) with the new maximum: the same
+// reference sequence as taking the max first, without a separate max pass in
+// the common case.
 // Of every 8 pairs of exponentials in a key block without masked entries,
 // kPolyPer8 are evaluated by the cubic polynomial 2^x on the FMA pipe
 // (exp2_poly2) and the rest by the MUFU ex2 unit, so that the two units share
@@ -202,10 +209,13 @@ __device__ __forceinline__ float2 exp2_pair(float2 x, int q) {
 template <class C, bool POLY>
 __device__ __forceinline__ void exp_block(const float (&s)[C::BC], const float (&cm)[2], const float (&lg)[2],
                                           const float (&inv_w)[2], float mb, uint32_t tS, float& lsum,
-                                          float& lqsum) {
+                                          float& lqsum, float* smax = nullptr) {
     constexpr int CH = C::FP8 ? 64 : 32;  // columns per 16-word TMEM store
     lsum = 0.f;
     lqsum = 0.f;
+    // with smax: also the max of the raw scores of the block (3-input max on
+    // the ALU pipe, four independent chains)
+    float mxc[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
     for (int ch = 0; ch < C::BC / CH; ++ch) {
         const int h = (ch * CH) / (C::BC / 2);
@@ -234,12 +244,14 @@ __device__ __forceinline__ void exp_block(const float (&s)[C::BC], const float (
                 const float2 pp = exp2_pair<POLY>(ffma2(make_float2(s[ch * CH + 2 * e], s[ch * CH + 2 * e + 1]), cs2, cb2), e);
                 a2[e & 3] = fadd2(a2[e & 3], pp);
                 w[e] = pack_bf16x2(pp.x, pp.y);
+                if (smax) mxc[e & 3] = fmax3(mxc[e & 3], s[ch * CH + 2 * e], s[ch * CH + 2 * e + 1]);
             }
         }
         const float2 t2 = fadd2(fadd2(a2[0], a2[1]), fadd2(a2[2], a2[3]));
         lsum += (t2.x + t2.y) * inv_w[h];
         tmem_st16(tS + ch * 16, w);
     }
+    if (smax) *smax = fmaxf(fmaxf(mxc[0], mxc[1]), fmaxf(mxc[2], mxc[3]));
 }
 
 template <class C, bool OUT_F32>
@@ -534,40 +546,65 @@ __global__ void __launch_bounds__(kThreads, 1)
                 } else {
                     cm[0] = cm[1] = p.scale_log2;
                 }
-                float mx2;
-                if constexpr (C::FP8) {
-                    mx2 = fmaxf(row_max<C::BC / 2>(s) * cm[0], row_max<C::BC / 2>(s + C::BC / 2) * cm[1]);
-                } else {
-                    mx2 = row_max<C::BC>(s) * cm[0];
-                }
-                const float slack = C::FP8 ? 0.f : kRescaleSlack;
-                const bool need = mx2 > m + slack;
-                float alpha = 1.f;
-                if (need) {
-                    alpha = ex2_approx(m - mx2);  // 0 when m = -inf
-                    m = mx2;
-                    l *= alpha;
-                    if (C::FP8) lq *= alpha;
-                }
-                if (j > 0 && __any_sync(0xffffffffu, need)) {
+                // O *= f over the row (O holds the blocks whose P V has completed)
+                auto rescale_o = [&](float f) {
 #pragma unroll 1
                     for (int c = 0; c < C::D; c += 32) {
                         uint32_t ov[32];
                         tmem_ld32_wait(tO + c, ov);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+                        for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * f);
                         tmem_st32(tO + c, ov);
                     }
                     tmem_st_wait();
-                }
-                const float mb = (m == -INFINITY) ? 0.f : m;
+                };
                 float lsum, lqsum;
-                if (need_mask)
-                    exp_block<C, false>(s, cm, lg, inv_w, mb, tS, lsum, lqsum);
-                else
-                    exp_block<C, true>(s, cm, lg, inv_w, mb, tS, lsum, lqsum);
-                l += lsum;
-                if (C::FP8) lq += lqsum;
+                if constexpr (C::FP8) {
+                    // exact reference max first (P <= 1 must hold for the E4M3 fold)
+                    const float mx2 = fmaxf(row_max<C::BC / 2>(s) * cm[0], row_max<C::BC / 2>(s + C::BC / 2) * cm[1]);
+                    const bool need = mx2 > m;
+                    float alpha = 1.f;
+                    if (need) {
+                        alpha = ex2_approx(m - mx2);  // 0 when m = -inf
+                        m = mx2;
+                        l *= alpha;
+                        lq *= alpha;
+                    }
+                    if (j > 0 && __any_sync(0xffffffffu, need)) rescale_o(alpha);
+                    const float mb = (m == -INFINITY) ? 0.f : m;
+                    if (need_mask)
+                        exp_block<C, false>(s, cm, lg, inv_w, mb, tS, lsum, lqsum);
+                    else
+                        exp_block<C, true>(s, cm, lg, inv_w, mb, tS, lsum, lqsum);
+                    l += lsum;
+                    lq += lqsum;
+                } else {
+                    if (j == 0) m = row_max<C::BC>(s) * cm[0];  // first block: exact reference
+                    float mb = (m == -INFINITY) ? 0.f : m;
+                    float smax;
+                    if (need_mask)
+                        exp_block<C, false>(s, cm, lg, inv_w, mb, tS, lsum, lqsum, &smax);
+                    else
+                        exp_block<C, true>(s, cm, lg, inv_w, mb, tS, lsum, lqsum, &smax);
+                    const float mx = smax * cm[0];
+                    const bool need = mx > m + kRescaleSlack;
+                    if (__any_sync(0xffffffffu, need)) {
+                        float alpha = 1.f;
+                        if (need) {
+                            alpha = ex2_approx(m - mx);  // 0 when m = -inf
+                            m = mx;
+                            l *= alpha;
+                        }
+                        tmem_st_wait();  // the first pass's P stores land before they are overwritten
+                        if (j > 0) rescale_o(alpha);
+                        mb = (m == -INFINITY) ? 0.f : m;
+                        if (need_mask)
+                            exp_block<C, false>(s, cm, lg, inv_w, mb, tS, lsum, lqsum);
+                        else
+                            exp_block<C, true>(s, cm, lg, inv_w, mb, tS, lsum, lqsum);
+                    }
+                    l += lsum;
+                }
                 tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(BAR(C::B_PFULL + t));

@@ -71,6 +71,36 @@ def test_block_sizes_agree(d, block_c):
 
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
+def test_row_max_jumps_in_later_blocks(d, causal):
+    """Running-state updates when a later key block holds a far larger score
+    (FA-v2 analysis page §2.3: O is rescaled by exp(m_old - m_new) whenever the
+    maximum moves).  Every query gets a common direction u, key 300 (block 2)
+    scores about 25 above the rest in log2 units and key 600 (block 4) about 95,
+    so both the moderate move of the reference maximum and the large one are
+    exercised, for some rows of a warp and not others under the causal mask.
+    Only the forward is compared: with one key holding all the weight the
+    gradients nearly vanish (dS = P (dP - D) cancels), so an element-wise bound
+    relative to their tiny maximum would measure float32 cancellation only."""
+    B, H, N = 1, 2, 700
+    q, k, v = qkv(B, H, N, d, 404 + d, device=DEV, with_dout=False)
+    u = torch.ones(d, dtype=torch.float32, device=DEV) / math.sqrt(d)
+    gain = math.sqrt(d) / (5.0 * math.log2(math.e))  # key amplitude per log2 unit of score
+    qf = q.float() + 5.0 * u
+    kf = k.float()
+    kf[:, :, 300] = 25.0 * gain * u
+    kf[:, :, 600] = 95.0 * gain * u
+    q, k = qf.to(torch.bfloat16), kf.to(torch.bfloat16)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = forward(q, k, v, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    check_device_status()
+    o_ref, lse_ref = oracle.fwd(to64(q), to64(k), to64(v), scale, causal=causal)
+    assert_close_abs(to64(o), o_ref, O_TOL, "O")
+    assert_lse(to64(lse), lse_ref)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
 def test_repeat_is_bitwise_consistent(d, causal):
     """Race check: every key block's dK, dV is produced by one CTA in a fixed
     order, so repeated runs must agree bitwise (dQ is summed by float32
