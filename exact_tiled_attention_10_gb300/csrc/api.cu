@@ -340,10 +340,13 @@ fa_status bwd_main_impl(const BwdCtx& c, bool f32, const void* qb, const void* k
     {
         cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)BH * Np};
         cuuint64_t strides[1] = {(cuuint64_t)d * 4};
-        cuuint32_t box[2] = {32, 64};
+        // d = 128: [64 queries][32 head-dim] boxes, plain; d = 64: [32 queries][32 head-dim]
+        // boxes in the 128-byte swizzle the drain warps stage them in
+        cuuint32_t box[2] = {32, (cuuint32_t)(d == 128 ? 64 : 32)};
         cuuint32_t estr[2] = {1, 1};
         CUresult r = g_encode(&tdq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, dqacc, dims, strides, box, estr,
-                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              d == 128 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled (dQ accumulator) failed (%d)", (int)r);
     }

@@ -236,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tmap(&tk);
             prefetch_tmap(&tv);
             prefetch_tmap(&tdo);
-            if (C::D == 128) prefetch_tmap(&tdq);
+            prefetch_tmap(&tdq);
         }
     }
     tc_fence_before();
@@ -545,14 +545,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int q = 0; q < 64; ++q) stage_f[q * 32 + lane] = __uint_as_float(v[q]);
                 } else {
-                    // lane = query (wq*32 + lane); column = head dim. Stage [32 q][64 d], rotated chunks.
+                    // lane = query (wq*32 + lane); column = head dim.  Two [32 q][32 d]
+                    // boxes in the 128-byte-swizzle layout: 16-byte chunk c of row r
+                    // sits at chunk c ^ (r & 7), so eight consecutive lanes cover all
+                    // banks, and every register index stays a compile-time constant;
+                    // the tensor reduction undoes the swizzle on its way to global memory
+                    uint8_t* stage_b = reinterpret_cast<uint8_t*>(stage_f);
 #pragma unroll
-                    for (int k = 0; k < 16; ++k) {
-                        const int c = (k + lane) & 15;
-                        *reinterpret_cast<float4*>(stage_f + lane * 64 + c * 4) =
-                            make_float4(__uint_as_float(v[4 * c]), __uint_as_float(v[4 * c + 1]),
-                                        __uint_as_float(v[4 * c + 2]), __uint_as_float(v[4 * c + 3]));
-                    }
+                    for (int b = 0; b < 2; ++b)
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            *reinterpret_cast<float4*>(stage_b + b * 4096 + lane * 128 + ((c ^ (lane & 7)) * 16)) =
+                                make_float4(__uint_as_float(v[32 * b + 4 * c]), __uint_as_float(v[32 * b + 4 * c + 1]),
+                                            __uint_as_float(v[32 * b + 4 * c + 2]), __uint_as_float(v[32 * b + 4 * c + 3]));
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
@@ -560,8 +565,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if constexpr (C::D == 128) {
                         tma_reduce_add_2d(&tdq, stage, wq * 32, I.bh * p.Np + i * C::BR);
                     } else {
-                        float* dst = p.dq_acc + ((size_t)I.bh * p.Np + (size_t)i * C::BR + wq * 32) * C::D;
-                        bulk_reduce_add_f32(dst, stage, C::DQ_WARP_BYTES);
+                        tma_reduce_add_2d(&tdq, stage, 0, I.bh * p.Np + i * C::BR + wq * 32);
+                        tma_reduce_add_2d(&tdq, stage + 4096, 32, I.bh * p.Np + i * C::BR + wq * 32);
                     }
                     bulk_commit_group();
                 }
