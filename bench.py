@@ -237,6 +237,13 @@ class Step:
         self.o8 = t(B, H, N, d)
         self.lse8 = t(B, H, N, dt=torch.float32)
         self.flush = t(L2_FLUSH_BYTES, dt=torch.uint8)
+        # split-key plans (automatic): the causal bf16 forward is never split;
+        # the non-causal FP8 forward may be (its merge kernel is part of the call)
+        self.split_bf16 = self.lib.fa_fwd_split_count(B, H, N, d, int(causal), 0, 0)
+        self.split_fp8 = self.lib.fa_fwd_split_count(B, H, N, d, 0, 0, 0)
+        self.sws_bytes = max(self.lib.fa_fwd_split_workspace_size(B, H, N, d, int(causal), 0, 0),
+                             self.lib.fa_fwd_split_workspace_size(B, H, N, d, 0, 0, 0))
+        self.sws = t(max(self.sws_bytes, 256), dt=torch.uint8)
         self.scale = 1.0 / math.sqrt(d)
         F = flops_fwd(w, causal)
         self.flops = {"fwd": F, "bwd_pre": 0.0, "bwd_main": 2.5 * F, "bwd_dq": 0.0,
@@ -249,7 +256,7 @@ class Step:
                       "bwd_dq": B * H * Np * d * 4 + n * 2,
                       "quant_fp8": 3 * (n * 2 + n + B * H * nb * 4),
                       "fwd_fp8": 3 * n + n * 2 + B * H * N * 4}
-        self.launches_per_step = 8
+        self.launches_per_step = 8 + int(self.split_bf16 > 1) + int(self.split_fp8 > 1)
 
     def _ck(self, st):
         if st != 0:
@@ -261,8 +268,8 @@ class Step:
         p = lambda x: x.data_ptr()
         rec = (lambda i: events[i].record()) if events is not None else (lambda i: None)
         rec(0)
-        self._ck(lib.fa_fwd(p(self.q), p(self.k), p(self.v), p(self.o), p(self.lse), B, H, N, d,
-                            self.scale, int(self.causal), None, s))
+        self._ck(lib.fa_fwd_split(p(self.q), p(self.k), p(self.v), p(self.o), p(self.lse), B, H, N, d,
+                                  self.scale, int(self.causal), None, 0, p(self.sws), self.sws_bytes, s))
         rec(1)
         self._ck(lib.fa_bwd_preprocess(p(self.o), p(self.lse), p(self.do), B, H, N, d, p(self.ws),
                                        self.ws_bytes, s))
@@ -276,9 +283,9 @@ class Step:
         for x, x8, sc in zip((self.q, self.k, self.v), self.x8, self.sc):
             self._ck(lib.fa_quantize_fp8(p(x), p(x8), p(sc), B, H, N, d, s))
         rec(5)
-        self._ck(lib.fa_fwd_fp8(p(self.x8[0]), p(self.x8[1]), p(self.x8[2]), p(self.sc[0]),
-                                p(self.sc[1]), p(self.sc[2]), p(self.o8), p(self.lse8), B, H, N, d,
-                                self.scale, 0, None, s))
+        self._ck(lib.fa_fwd_fp8_split(p(self.x8[0]), p(self.x8[1]), p(self.x8[2]), p(self.sc[0]),
+                                      p(self.sc[1]), p(self.sc[2]), p(self.o8), p(self.lse8), B, H, N, d,
+                                      self.scale, 0, None, 0, p(self.sws), self.sws_bytes, s))
         rec(6)
 
     def flush_l2(self):

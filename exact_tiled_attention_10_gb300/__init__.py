@@ -21,7 +21,8 @@ from typing import Optional, Tuple
 
 import torch
 
-__all__ = ["forward", "backward", "quantize_fp8", "forward_fp8", "check_device_status",
+__all__ = ["forward", "forward_split", "backward", "quantize_fp8", "forward_fp8", "forward_fp8_split",
+           "split_count", "split_workspace_size", "check_device_status",
            "selftest_wait_timeout",
            "bwd_workspace_size", "fwd_workspace_size", "library_path", "load_library", "FAError"]
 
@@ -55,6 +56,10 @@ _SIGS = {
     "fa_fp8_num_blocks": ([_i], _i),
     "fa_quantize_fp8": ([_vp, _vp, _vp, _i, _i, _i, _i, _vp], _i),
     "fa_fwd_fp8": ([_vp] * 8 + [_i, _i, _i, _i, _f, _i, _vp, _vp], _i),
+    "fa_fwd_split_workspace_size": ([_i] * 7, _sz),
+    "fa_fwd_split_count": ([_i] * 7, _i),
+    "fa_fwd_split": ([_vp] * 5 + [_i, _i, _i, _i, _f, _i, _vp, _i, _vp, _sz, _vp], _i),
+    "fa_fwd_fp8_split": ([_vp] * 8 + [_i, _i, _i, _i, _f, _i, _vp, _i, _vp, _sz, _vp], _i),
 }
 
 
@@ -155,6 +160,49 @@ def forward(q, k, v, causal: bool = False, scale: Optional[float] = None, kv_len
     return o, l
 
 
+def split_count(B: int, H: int, N: int, d: int, causal: bool = False, kv_lens: bool = False,
+                num_splits: int = 0) -> int:
+    """Number of key ranges fa_fwd_split uses for this call (1 = not split)."""
+    return int(load_library().fa_fwd_split_count(B, H, N, d, int(bool(causal)), int(bool(kv_lens)),
+                                                 int(num_splits)))
+
+
+def split_workspace_size(B: int, H: int, N: int, d: int, causal: bool = False, kv_lens: bool = False,
+                         num_splits: int = 0) -> int:
+    return int(load_library().fa_fwd_split_workspace_size(B, H, N, d, int(bool(causal)), int(bool(kv_lens)),
+                                                          int(num_splits)))
+
+
+def _split_ws(B, H, N, d, causal, kv, num_splits, workspace, device):
+    wsz = split_workspace_size(B, H, N, d, causal, kv is not None, num_splits)
+    ws = workspace
+    if wsz and (ws is None or ws.numel() * ws.element_size() < wsz):
+        ws = torch.empty(wsz, dtype=torch.uint8, device=device)
+    return (_ptr(ws) if wsz else None), wsz
+
+
+def forward_split(q, k, v, causal: bool = False, scale: Optional[float] = None, kv_lens=None,
+                  num_splits: int = 0, out: Optional[torch.Tensor] = None,
+                  lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None
+                  ) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Split-key bf16 forward (FlashDecoding form): as forward(), with the key
+    sequence of each query block cut into ranges merged by a second kernel.
+    num_splits 0 = automatic, 1 = none, >= 2 = that many ranges per item."""
+    lib = load_library()
+    _need_cuda(q, k, v)
+    B, H, N, d = q.shape
+    if q.dtype != torch.bfloat16 or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("forward_split takes bfloat16 q, k, v")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    kv = _kv(kv_lens, B, q.device)
+    o = torch.empty_like(q) if out is None else out
+    l = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    wsp, wsz = _split_ws(B, H, N, d, causal, kv, num_splits, workspace, q.device)
+    _check(lib.fa_fwd_split(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(l), B, H, N, d, scale,
+                            int(bool(causal)), _ptr(kv), int(num_splits), wsp, wsz, _stream(q)))
+    return o, l
+
+
 def backward(q, k, v, o, lse, dout, causal: bool = False, scale: Optional[float] = None,
              kv_lens=None, workspace: Optional[torch.Tensor] = None,
              dq: Optional[torch.Tensor] = None, dk: Optional[torch.Tensor] = None,
@@ -207,6 +255,24 @@ def forward_fp8(q8, k8, v8, sq, sk, sv, causal: bool = False, scale: Optional[fl
     l = torch.empty((B, H, N), dtype=torch.float32, device=q8.device) if lse is None else lse
     _check(lib.fa_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(v8), _ptr(sq), _ptr(sk), _ptr(sv), _ptr(o),
                           _ptr(l), B, H, N, d, scale, int(bool(causal)), _ptr(kv), _stream(q8)))
+    return o, l
+
+
+def forward_fp8_split(q8, k8, v8, sq, sk, sv, causal: bool = False, scale: Optional[float] = None,
+                      kv_lens=None, num_splits: int = 0, out: Optional[torch.Tensor] = None,
+                      lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None):
+    """Split-key FP8 forward: forward_fp8 with the key ranges of forward_split."""
+    lib = load_library()
+    _need_cuda(q8, k8, v8, sq, sk, sv)
+    B, H, N, d = q8.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    kv = _kv(kv_lens, B, q8.device)
+    o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q8.device) if out is None else out
+    l = torch.empty((B, H, N), dtype=torch.float32, device=q8.device) if lse is None else lse
+    wsp, wsz = _split_ws(B, H, N, d, causal, kv, num_splits, workspace, q8.device)
+    _check(lib.fa_fwd_fp8_split(_ptr(q8), _ptr(k8), _ptr(v8), _ptr(sq), _ptr(sk), _ptr(sv), _ptr(o),
+                                _ptr(l), B, H, N, d, scale, int(bool(causal)), _ptr(kv), int(num_splits),
+                                wsp, wsz, _stream(q8)))
     return o, l
 
 

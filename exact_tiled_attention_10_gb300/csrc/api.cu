@@ -147,9 +147,75 @@ BwdLayout bwd_layout(fa_dtype dt, int B, int H, int N, int d) {
     return L;
 }
 
+// SM count of the current device, or the GB300's 152 when no device is
+// visible (so that the split plan can be inspected on a host without a GPU).
+int sm_count_or_default() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) {
+        cudaGetLastError();
+        return fa::kNumSMsDefault;
+    }
+    return sms;
+}
+
+// Split-key plan of a forward call.  Work is counted in key blocks of 128 with
+// a fixed cost of two blocks per work unit (prologue, epilogue).  Automatic
+// (requested = 0): whole items fill r full rounds of `sms` units and the
+// remaining items are cut into s in [2, 4] key ranges, choosing (r, s) with the
+// least estimated time (ties: more whole items, fewer ranges); kept only if it
+// beats the unsplit schedule by more than 5%.  Causal items (unequal lengths,
+// already balanced by the snake order) and key-padded batches are not split
+// automatically.  requested = 1: no split; >= 2: every item in that many
+// ranges (at most 64), the FlashDecoding form for few heads and long keys.
+struct SplitPlan {
+    int num_whole = 0, splits = 1;
+    long long partials = 0;
+    size_t o_bytes = 0, bytes = 0;
+};
+SplitPlan plan_split(int B, int H, int N, int d, bool causal, bool has_kv, int requested, int sms) {
+    SplitPlan P;
+    const long long items = (long long)B * H * ((N + 255) / 256);
+    const int nb = (N + 127) / 128;
+    long long whole = items;
+    int S = 1;
+    if (requested >= 2) {
+        S = requested < 64 ? requested : 64;
+        whole = 0;
+    } else if (requested == 0 && !causal && !has_kv && nb >= 2) {
+        const double unit = nb + 2.0;
+        const double base = (double)((items + sms - 1) / sms) * unit;
+        double best = base;
+        for (long long r = items / sms; r >= 0; --r) {
+            for (int s = 2; s <= 4 && s <= nb; ++s) {
+                const long long tail = items - r * sms;
+                const double t = (double)r * unit + (double)((tail * s + sms - 1) / sms) * ((double)nb / s + 2.0);
+                if (t < best - 1e-9) {
+                    best = t;
+                    S = s;
+                    whole = r * sms;
+                }
+            }
+        }
+        if (best > 0.95 * base) {
+            S = 1;
+            whole = items;
+        }
+    }
+    P.num_whole = (int)whole;
+    if (S > 1) {
+        P.splits = S;
+        P.partials = (items - whole) * S;
+        P.o_bytes = round_up((size_t)P.partials * 256 * d * 4, 256);
+        P.bytes = P.o_bytes + round_up((size_t)P.partials * 256 * 4, 256);
+    }
+    return P;
+}
+
 fa_status fwd_impl(fa_dtype dtype, int block_c, bool fp8, const void* q, const void* k, const void* v, const float* sq,
                    const float* sk, const float* sv, void* o, float* lse, int B, int H, int N, int d, float scale,
-                   int causal, const int* kv_lens, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+                   int causal, const int* kv_lens, void* workspace, size_t workspace_bytes, cudaStream_t stream,
+                   int num_splits = 1, void* split_ws = nullptr, size_t split_ws_bytes = 0) {
     FA_TRY(check_common(B, H, N, d, scale));
     FA_CHECK_PTR(q);
     FA_CHECK_PTR(k);
@@ -191,6 +257,10 @@ fa_status fwd_impl(fa_dtype dtype, int block_c, bool fp8, const void* q, const v
             return fail(FA_ERR_UNSUPPORTED, "float32 inputs with d = 128 use 64-key blocks");
         if (block_c == 0) block_c = (d == 128 || N <= 128) ? 64 : 128;
     }
+    if (num_splits < 0) return fail(FA_ERR_INVALID_ARG, "num_splits must be >= 0");
+    const SplitPlan P = (dtype == FA_BF16) ? plan_split(B, H, N, d, causal != 0, kv_lens != nullptr, num_splits, dev->sms)
+                                           : SplitPlan{};
+    if (P.splits > 1) block_c = 128;  // the split-key instances use 128-key blocks
     if (block_c == 0) block_c = (N <= 128 && !fp8) ? 64 : 128;
     fa::FwdMaps m;
     if (fp8) {
@@ -220,15 +290,32 @@ fa_status fwd_impl(fa_dtype dtype, int block_c, bool fp8, const void* q, const v
     p.sq = sq; p.sk = sk; p.sv = sv;
     p.nblk = (N + 63) / 64;
     p.err = dev->err_word;
-    const int grid = grid_for_items(p.num_items, dev->sms);
+    p.num_whole = (P.splits > 1) ? P.num_whole : p.num_items;
+    p.splits = P.splits;
+    p.num_units = p.num_whole + (int)P.partials;
+    if (P.splits > 1) {
+        if (!split_ws || split_ws_bytes < P.bytes)
+            return fail(FA_ERR_INVALID_ARG, "split workspace too small (%zu bytes, need %zu)", split_ws_bytes, P.bytes);
+        FA_CHECK_PTR(split_ws);
+        p.o_part = reinterpret_cast<float*>(split_ws);
+        p.lse_part = reinterpret_cast<float*>(reinterpret_cast<char*>(split_ws) + P.o_bytes);
+    }
+    const int grid = grid_for_items(p.num_units, dev->sms);
     cudaError_t e;
-    if (fp8)
+    if (P.splits > 1)
+        e = fa::launch_fwd_splitk(d, fp8, causal != 0, m, p, grid, stream);
+    else if (fp8)
         e = fa::launch_fwd_fp8_d128(causal != 0, m, p, grid, stream);
     else if (d == 128)
         e = fa::launch_fwd_bf16_d128(block_c, causal != 0, dtype == FA_F32, split, m, p, grid, stream);
     else
         e = fa::launch_fwd_bf16_d64(block_c, causal != 0, dtype == FA_F32, split, m, p, grid, stream);
     if (e != cudaSuccess) return cuda_fail(e, "forward launch");
+    if (P.splits > 1) {
+        e = fa::launch_lse_merge(p.o_part, p.lse_part, P.num_whole, p.num_items - P.num_whole, P.splits, causal != 0, BH,
+                                 p.num_qp, N, d, o, lse, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "split merge launch");
+    }
     return FA_OK;
 }
 
@@ -271,6 +358,23 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
                  float scale, int causal, const int* kv_lens, fa_stream_t stream) {
     return fwd_impl(FA_BF16, 0, false, q, k, v, nullptr, nullptr, nullptr, o, lse, B, H, N, d, scale, causal, kv_lens,
                     nullptr, 0, stream);
+}
+
+size_t fa_fwd_split_workspace_size(int B, int H, int N, int d, int causal, int has_kv_lens, int num_splits) {
+    if (B <= 0 || H <= 0 || N <= 0 || (d != 64 && d != 128) || num_splits < 0) return 0;
+    return plan_split(B, H, N, d, causal != 0, has_kv_lens != 0, num_splits, sm_count_or_default()).bytes;
+}
+
+int fa_fwd_split_count(int B, int H, int N, int d, int causal, int has_kv_lens, int num_splits) {
+    if (B <= 0 || H <= 0 || N <= 0 || (d != 64 && d != 128) || num_splits < 0) return 1;
+    return plan_split(B, H, N, d, causal != 0, has_kv_lens != 0, num_splits, sm_count_or_default()).splits;
+}
+
+fa_status fa_fwd_split(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                       float scale, int causal, const int* kv_lens, int num_splits, void* workspace,
+                       size_t workspace_bytes, fa_stream_t stream) {
+    return fwd_impl(FA_BF16, 0, false, q, k, v, nullptr, nullptr, nullptr, o, lse, B, H, N, d, scale, causal, kv_lens,
+                    nullptr, 0, stream, num_splits, workspace, workspace_bytes);
 }
 
 size_t fa_fwd_workspace_size(fa_dtype dtype, int B, int H, int N, int d) {
@@ -471,6 +575,14 @@ fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* v8, const float
                      const int* kv_lens, fa_stream_t stream) {
     return fwd_impl(FA_BF16, 128, true, q8, k8, v8, sq, sk, sv, o, lse, B, H, N, d, scale, causal, kv_lens, nullptr, 0,
                     stream);
+}
+
+fa_status fa_fwd_fp8_split(const void* q8, const void* k8, const void* v8, const float* sq, const float* sk,
+                           const float* sv, void* o, float* lse, int B, int H, int N, int d, float scale, int causal,
+                           const int* kv_lens, int num_splits, void* workspace, size_t workspace_bytes,
+                           fa_stream_t stream) {
+    return fwd_impl(FA_BF16, 128, true, q8, k8, v8, sq, sk, sv, o, lse, B, H, N, d, scale, causal, kv_lens, nullptr, 0,
+                    stream, num_splits, workspace, workspace_bytes);
 }
 
 }  // extern "C"

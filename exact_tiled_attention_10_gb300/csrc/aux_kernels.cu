@@ -6,7 +6,10 @@
 //     accumulator;
 //   * dQ conversion: dQ = scale * dQ_acc (the 1/sqrt(d) of wiki §04);
 //   * FP8 E4M3 per-block quantiser (chapter 18 §18.6.2: s = max|X| / 448);
-//   * float32 -> bf16 rounding of inputs for the float32 entry points.
+//   * float32 -> bf16 rounding of inputs for the float32 entry points;
+//   * the merge of the split-key forward's partial results (chapter 18
+//     §18.8.2, FlashDecoding: the reduction that combines the per-range
+//     statistics and outputs with the online-softmax weights).
 // All use 16-byte vector accesses and grid-stride loops over a grid sized in
 // multiples of the SM count.
 #include <cuda_bf16.h>
@@ -183,6 +186,61 @@ __global__ void __launch_bounds__(256) f32_split_kernel(const float* __restrict_
     }
 }
 
+// Split-key merge.  Partial t of a row holds O_t = (sum over its key range of
+// p v) / l_t and LSE_t = m_t + log l_t.  With M = max_t LSE_t,
+//   LSE = M + log sum_t exp(LSE_t - M),  O = sum_t exp(LSE_t - LSE) O_t,
+// which is the chapter's merge sum_t e^(m_t - m) O~_t / sum_t e^(m_t - m) l_t
+// (O~_t the unnormalised partial) rewritten with l_t e^(m_t) = e^(LSE_t).
+// All partials -inf (no visible key): O = 0, LSE = -inf.  One warp per row,
+// each lane D/32 consecutive head-dim values.
+template <int D>
+__global__ void lse_merge_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part, int num_whole,
+                                 int num_tail, int S, bool causal, int BH, int num_qp, int N,
+                                 __nv_bfloat16* __restrict__ o, float* __restrict__ lse) {
+    constexpr int V = D / 32;  // values per lane
+    const int lane = threadIdx.x & 31;
+    const long long nrows = (long long)num_tail * 256;
+    for (long long r = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < nrows;
+         r += ((long long)gridDim.x * blockDim.x) >> 5) {
+        const int ti = (int)(r >> 8), rr = (int)(r & 255);
+        int bh, qp;
+        fwd_item_coords(num_whole + ti, causal, BH, num_qp, bh, qp);
+        const int row = qp * 256 + rr;
+        if (row >= N) continue;
+        const size_t base = (size_t)ti * S * 256 + rr;  // partial (ti, 0) of this row
+        float M = -INFINITY;
+        for (int t = 0; t < S; ++t) M = fmaxf(M, __ldg(lse_part + base + (size_t)t * 256));
+        float acc[V];
+#pragma unroll
+        for (int i = 0; i < V; ++i) acc[i] = 0.f;
+        float out_lse = -INFINITY;
+        if (M != -INFINITY) {
+            float sw = 0.f;
+            for (int t = 0; t < S; ++t) sw += expf(__ldg(lse_part + base + (size_t)t * 256) - M);
+            out_lse = M + logf(sw);
+            for (int t = 0; t < S; ++t) {
+                const float w = expf(__ldg(lse_part + base + (size_t)t * 256) - out_lse);
+                const float* src = o_part + (base + (size_t)t * 256) * D + lane * V;
+                if constexpr (V == 4) {
+                    const float4 x = __ldg(reinterpret_cast<const float4*>(src));
+                    acc[0] += w * x.x; acc[1] += w * x.y; acc[2] += w * x.z; acc[3] += w * x.w;
+                } else {
+                    const float2 x = __ldg(reinterpret_cast<const float2*>(src));
+                    acc[0] += w * x.x; acc[1] += w * x.y;
+                }
+            }
+        }
+        const size_t orow = (size_t)bh * N + row;
+        __nv_bfloat16* dst = o + orow * D + lane * V;
+        if constexpr (V == 4) {
+            *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]));
+        } else {
+            *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[0], acc[1]);
+        }
+        if (lane == 0) lse[orow] = out_lse;
+    }
+}
+
 // One warp waits on an mbarrier that nothing ever arrives on, through the same
 // bounded wait every pipeline uses; it must give up after `limit_us`, record
 // the error bit and return (no trap, no hang).
@@ -200,6 +258,21 @@ __global__ void wait_selftest_kernel(unsigned int* err, unsigned long long limit
 }
 
 }  // namespace
+
+cudaError_t launch_lse_merge(const float* o_part, const float* lse_part, int num_whole, int num_tail, int splits,
+                             bool causal, int BH, int num_qp, int N, int d, void* o, float* lse, cudaStream_t stream) {
+    if (num_tail <= 0 || splits <= 1) return cudaSuccess;
+    const long long blocks = ((long long)num_tail * 256 + 7) / 8;  // 8 rows (warps) per block
+    const int grid = (int)(blocks < 152 * 32 ? blocks : 152 * 32);
+    __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(o);
+    if (d == 128)
+        lse_merge_kernel<128><<<grid, 256, 0, stream>>>(o_part, lse_part, num_whole, num_tail, splits, causal, BH,
+                                                        num_qp, N, ob, lse);
+    else
+        lse_merge_kernel<64><<<grid, 256, 0, stream>>>(o_part, lse_part, num_whole, num_tail, splits, causal, BH,
+                                                       num_qp, N, ob, lse);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_wait_selftest(unsigned int* err, unsigned int limit_us, int* waited_out, cudaStream_t s) {
     wait_selftest_kernel<<<1, 32, 0, s>>>(err, (unsigned long long)limit_us * 1000ull, waited_out);

@@ -37,10 +37,30 @@ __device__ __forceinline__ int snake_item(int round, int num_items) {
 }
 __device__ __forceinline__ int snake_rounds(int num_items) { return (num_items + (int)gridDim.x - 1) / (int)gridDim.x; }
 
+// Forward work item `it` (longest first) -> (head index bh, query-row pair qp).
+__host__ __device__ __forceinline__ void fwd_item_coords(int it, bool causal, int BH, int num_qp, int& bh, int& qp) {
+    if (causal) {  // the pairs that see the most keys first
+        qp = num_qp - 1 - it / BH;
+        bh = it % BH;
+    } else {
+        qp = it % num_qp;
+        bh = it / num_qp;
+    }
+}
+
 struct FwdParams {
     int B, H, N;
     int num_qp;       // query-row pairs of 128-row tiles per head: ceil(N / 256)
     int num_items;    // B * H * num_qp
+    // Split keys (FlashDecoding form): work units 0 .. num_whole-1 are whole
+    // items; each later item is cut into `splits` contiguous key ranges, one
+    // unit each, whose normalised O and LSE go to o_part / lse_part (unit
+    // u >= num_whole is partial u - num_whole) for the merge kernel.
+    int num_units;    // num_whole + (num_items - num_whole) * splits
+    int num_whole;
+    int splits;
+    float* o_part;    // [partials][256 rows][d] f32
+    float* lse_part;  // [partials][256 rows]
     float scale;      // softmax scale applied to Q K^T
     float scale_log2; // scale * log2(e)
     const int* kv_lens;
@@ -79,6 +99,8 @@ cudaError_t launch_fwd_bf16_d64(int block_c, bool causal, bool out_f32, bool spl
                                 const FwdParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_fwd_bf16_d128(int block_c, bool causal, bool out_f32, bool split, const FwdMaps& m,
                                  const FwdParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_fwd_splitk(int d, bool fp8, bool causal, const FwdMaps& m, const FwdParams& p, int grid,
+                              cudaStream_t stream);
 cudaError_t launch_fwd_fp8_d128(bool causal, const FwdMaps& m, const FwdParams& p, int grid,
                                 cudaStream_t stream);
 cudaError_t launch_bwd_main(int d, bool causal, bool out_f32, const CUtensorMap& tq,
@@ -92,6 +114,9 @@ cudaError_t launch_bwd_dq(const float* dq_acc, void* dq, bool out_f32, float sca
                           int Np, int d, int grid, cudaStream_t stream);
 cudaError_t launch_quantize_fp8(const void* x, void* x8, float* scales, int BH, int N, int d,
                                 int grid, cudaStream_t stream);
+// Merges the split-key partials of the forward into O (bf16) and LSE.
+cudaError_t launch_lse_merge(const float* o_part, const float* lse_part, int num_whole, int num_tail, int splits,
+                             bool causal, int BH, int num_qp, int N, int d, void* o, float* lse, cudaStream_t stream);
 cudaError_t launch_wait_selftest(unsigned int* err, unsigned int limit_us, int* waited_out,
                                  cudaStream_t stream);
 cudaError_t launch_f32_to_bf16(const float* x, void* y, size_t n, int grid, cudaStream_t stream);

@@ -120,22 +120,29 @@ struct Cfg {
 
 struct Item {
     int bh, b, row0, kvl;
-    int n[2];
+    int n[2];   // key blocks of tile 0 / tile 1 in this unit
     int nmax;
+    int j0;     // first key block of this unit
+    int part;   // partial index of a split unit, -1 for a whole item
 };
 
-template <class C, bool CAUSAL>
-__device__ __forceinline__ Item get_item(int it, const FwdParams& p) {
+// SPLITK: the kernel instance that also runs split-key units (compiled
+// separately so that the plain forward carries none of their bookkeeping).
+template <class C, bool CAUSAL, bool SPLITK>
+__device__ __forceinline__ Item get_item(int unit, const FwdParams& p) {
     Item I;
     const int BH = p.B * p.H;
-    int qp;
-    if (CAUSAL) {  // longest rows first
-        qp = p.num_qp - 1 - it / BH;
-        I.bh = it % BH;
-    } else {
-        qp = it % p.num_qp;
-        I.bh = it / p.num_qp;
+    int it = unit, s = 0, S = 1;
+    I.part = -1;
+    if (SPLITK && unit >= p.num_whole) {  // split unit: key range s of S of item `it`
+        const int t = unit - p.num_whole;
+        S = p.splits;
+        it = p.num_whole + t / S;
+        s = t % S;
+        I.part = t;
     }
+    int qp;
+    fwd_item_coords(it, CAUSAL, BH, p.num_qp, I.bh, qp);
     I.b = I.bh / p.H;
     int kvl = p.N;
     if (p.kv_lens) kvl = min(max(__ldg(p.kv_lens + I.b), 0), p.N);
@@ -153,6 +160,17 @@ __device__ __forceinline__ Item get_item(int it, const FwdParams& p) {
         }
         I.n[t] = n;
         I.nmax = max(I.nmax, n);
+    }
+    I.j0 = 0;
+    if (SPLITK && S > 1) {
+        const int j0 = (int)((long long)I.nmax * s / S), j1 = (int)((long long)I.nmax * (s + 1) / S);
+        I.nmax = 0;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            I.n[t] = max(0, min(j1, I.n[t]) - j0);
+            I.nmax = max(I.nmax, I.n[t]);
+        }
+        I.j0 = j0;
     }
     return I;
 }
@@ -269,7 +287,7 @@ __device__ __forceinline__ void store_row_chunk(void* o_row, int c0, const float
     }
 }
 
-template <class C, bool CAUSAL, bool OUT_F32>
+template <class C, bool CAUSAL, bool OUT_F32, bool SPLITK>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tql,
@@ -334,10 +352,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         int kst = 0, vst = 0;
         uint32_t kph = 0, vph = 0, qe = 0;
         bool ok = true;
-        for (int rd = 0; rd < snake_rounds(p.num_items) && ok; ++rd) {
-            const int it = snake_item(rd, p.num_items);
+        for (int rd = 0; rd < snake_rounds(p.num_units) && ok; ++rd) {
+            const int it = snake_item(rd, p.num_units);
             if (it < 0) continue;
-            const Item I = get_item<C, CAUSAL>(it, p);
+            const Item I = get_item<C, CAUSAL, SPLITK>(it, p);
             if (I.nmax == 0) continue;
             // Q tile t of this item may load as soon as the previous item's last
             // S_t MMA has consumed the buffer (per-tile barriers), overlapping
@@ -366,7 +384,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int part = 0; part < C::NPART; ++part)
                             for (int bx = 0; bx < C::NBOX; ++bx)
                                 tma_load_3d(sbase + C::OFF_K + kst * C::K_STAGE + part * C::KV_TILE + bx * C::KV_BOX,
-                                            part ? &tkl : &tk, BAR(C::B_KFULL + kst), bx * C::BOX_ELEMS, idx * C::BC, I.bh);
+                                            part ? &tkl : &tk, BAR(C::B_KFULL + kst), bx * C::BOX_ELEMS,
+                                            (I.j0 + idx) * C::BC, I.bh);
                     }
                     __syncwarp();
                     if (++kst == C::KSTAGES) { kst = 0; kph ^= 1; }
@@ -378,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mbar_arrive_expect_tx(BAR(C::B_VFULL + vst), C::KV_TILE);
                         for (int bx = 0; bx < C::NBOX; ++bx)
                             tma_load_3d(sbase + C::OFF_V + vst * C::KV_TILE + bx * C::KV_BOX, &tv, BAR(C::B_VFULL + vst),
-                                        bx * C::BOX_ELEMS, j * C::BC, I.bh);
+                                        bx * C::BOX_ELEMS, (I.j0 + j) * C::BC, I.bh);
                     }
                     __syncwarp();
                     if (++vst == C::VSTAGES) { vst = 0; vph ^= 1; }
@@ -402,10 +421,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto tS = [&](int t) { return tmem + (t ? C::TM_S1 : C::TM_S0); };
         auto tO = [&](int t) { return tmem + (t ? C::TM_O1 : C::TM_O0); };
         bool ok = true;
-        for (int rd = 0; rd < snake_rounds(p.num_items) && ok; ++rd) {
-            const int it = snake_item(rd, p.num_items);
+        for (int rd = 0; rd < snake_rounds(p.num_units) && ok; ++rd) {
+            const int it = snake_item(rd, p.num_units);
             if (it < 0) continue;
-            const Item I = get_item<C, CAUSAL>(it, p);
+            const Item I = get_item<C, CAUSAL, SPLITK>(it, p);
             if (I.nmax == 0) continue;
             for (int t = 0; t < 2 && ok; ++t)
                 ok = wait_bounded_warp(BAR(C::B_QFULL + t), qph, abort_flag, p.err, kErrWaitFwdMma);
@@ -474,23 +493,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tO = tmem + lane_off + (t ? C::TM_O1 : C::TM_O0);
         const int r_in = wq * 32 + lane;
         uint32_t sph = 0, oph = 0;
-        for (int rd = 0; rd < snake_rounds(p.num_items); ++rd) {
-            const int it = snake_item(rd, p.num_items);
+        for (int rd = 0; rd < snake_rounds(p.num_units); ++rd) {
+            const int it = snake_item(rd, p.num_units);
             if (it < 0) continue;
-            const Item I = get_item<C, CAUSAL>(it, p);
+            const Item I = get_item<C, CAUSAL, SPLITK>(it, p);
             const int n = I.n[t];
             const int tile_row0 = I.row0 + t * C::BR;
             const int row = tile_row0 + r_in;
             const size_t row_idx = (size_t)I.bh * p.N + row;
+            // destination of this row: O / LSE, or the unit's partial (split keys)
+            const size_t prow = (size_t)I.part * 256 + t * C::BR + r_in;
+            char* orow = reinterpret_cast<char*>(p.o) + row_idx * C::D * (OUT_F32 ? 4 : 2);
+            float* lse_dst = (SPLITK && I.part >= 0) ? p.lse_part + prow : p.lse + row_idx;
+            auto emit = [&](int c, const float (&f)[32]) {
+                if (SPLITK && I.part >= 0) {
+                    float4* dst = reinterpret_cast<float4*>(p.o_part + prow * C::D + c);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) dst[i] = make_float4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]);
+                } else {
+                    store_row_chunk<C, OUT_F32>(orow, c, f);
+                }
+            };
             if (n == 0) {
-                if (row < p.N) {  // no visible key (kv_len = 0): O = 0, LSE = -inf
+                if (row < p.N) {  // no visible key (kv_len = 0, or an empty key range): O = 0, LSE = -inf
                     float z[32];
 #pragma unroll
                     for (int i = 0; i < 32; ++i) z[i] = 0.f;
-                    char* orow = reinterpret_cast<char*>(p.o) + row_idx * C::D * (OUT_F32 ? 4 : 2);
 #pragma unroll
-                    for (int c = 0; c < C::D; c += 32) store_row_chunk<C, OUT_F32>(orow, c, z);
-                    p.lse[row_idx] = -INFINITY;
+                    for (int c = 0; c < C::D; c += 32) emit(c, z);
+                    *lse_dst = -INFINITY;
                 }
                 continue;
             }
@@ -521,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float s[C::BC];
 #pragma unroll
                 for (int c = 0; c < C::BC; ++c) s[c] = __uint_as_float(sr[c]);
-                const int col0 = j * C::BC;
+                const int col0 = (I.j0 + j) * C::BC;
                 const bool need_mask = (col0 + C::BC > I.kvl) || (CAUSAL && col0 + C::BC - 1 > tile_row0);
                 if (need_mask) {
 #pragma unroll
@@ -535,7 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (C::FP8) {
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
-                        const int blk = j * 2 + h;
+                        const int blk = (I.j0 + j) * 2 + h;
                         const float skb = (blk < p.nblk) ? __ldg(p.sk + (size_t)I.bh * p.nblk + blk) : 1.f;
                         const float svb = (blk < p.nblk) ? __ldg(p.sv + (size_t)I.bh * p.nblk + blk) : sv_max;
                         cm[h] = p.scale_log2 * sq_row * skb;
@@ -615,7 +646,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             float inv = (l > 0.f) ? 1.f / l : 0.f;
             if (C::FP8) inv = (lq > 0.f) ? sv_max * (1.f / 448.f) / lq : 0.f;
-            char* orow = reinterpret_cast<char*>(p.o) + row_idx * C::D * (OUT_F32 ? 4 : 2);
 #pragma unroll 1
             for (int c = 0; c < C::D; c += 32) {
                 uint32_t ov[32];
@@ -623,11 +653,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float f[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(ov[i]) * inv;
-                if (row < p.N) store_row_chunk<C, OUT_F32>(orow, c, f);
+                if (row < p.N) emit(c, f);
             }
             tc_fence_before();
             mbar_arrive(BAR(C::B_OEMPTY + t));
-            if (row < p.N) p.lse[row_idx] = (l > 0.f) ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+            if (row < p.N) *lse_dst = (l > 0.f) ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
         }
     }
 
@@ -639,13 +669,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <class C, bool CAUSAL, bool OUT_F32>
+template <class C, bool CAUSAL, bool OUT_F32, bool SPLITK = false>
 cudaError_t launch(const FwdMaps& m, const FwdParams& p, int grid, cudaStream_t stream) {
-    auto kern = fwd_kernel<C, CAUSAL, OUT_F32>;
+    auto kern = fwd_kernel<C, CAUSAL, OUT_F32, SPLITK>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     kern<<<grid, kThreads, C::SMEM, stream>>>(m.q, m.k, m.v, m.q_lo, m.k_lo, p);
     return cudaGetLastError();
+}
+
+template <class C>
+cudaError_t launch_splitk(bool causal, const FwdMaps& m, const FwdParams& p, int grid, cudaStream_t s) {
+    return causal ? launch<C, true, false, true>(m, p, grid, s) : launch<C, false, false, true>(m, p, grid, s);
 }
 
 template <class C>

@@ -12,7 +12,8 @@
  *   [CH18] "第18章 FlashAttention" -- §18.2.2 causal mask M_ij = -inf for
  *          j > i and the padding (column) mask of Table 18-3; §18.6.2 FP8
  *          E4M3 with per-block scale s = max|X| / 448; §18.7.1 API
- *          (softmax_scale defaults to 1/sqrt(headdim), causal in-kernel).
+ *          (softmax_scale defaults to 1/sqrt(headdim), causal in-kernel);
+ *          §18.8.2 FlashDecoding (split key sequence, merged partials).
  *
  * Common conventions for every entry point
  * ----------------------------------------
@@ -104,6 +105,34 @@ fa_status fa_fwd_ex(fa_dtype dtype, int block_c, const void* q, const void* k, c
                     const int* kv_lens, void* workspace, size_t workspace_bytes,
                     fa_stream_t stream);
 
+/* Split-key forward, bf16 ([CH18] §18.8.2, FlashDecoding: the key sequence of
+ * a query block is cut into contiguous ranges computed by separate thread
+ * blocks, and the per-range results are merged with the online-softmax
+ * weights).  Same inputs, outputs and semantics as fa_fwd; the work units
+ * are (head, 256 query rows, key range) and a second kernel merges the
+ * ranges: LSE = log sum_t exp(LSE_t), O = sum_t exp(LSE_t - LSE) O_t, where
+ * O_t and LSE_t are the normalised output and LSE of range t (equivalent to
+ * the chapter's merge of (m_t, l_t, unnormalised O_t), since
+ * l_t exp(m_t) = exp(LSE_t)).
+ *   num_splits  0: automatic -- whole items fill the full rounds of the
+ *               persistent grid and only the remainder is split (2..4 ranges)
+ *               when that shortens the last round; never for causal or
+ *               key-padded calls (their items are unequal).  1: no split
+ *               (exactly fa_fwd).  >= 2: every item in that many ranges (at
+ *               most 64).
+ *   workspace   device scratch for the partial results, at least
+ *               fa_fwd_split_workspace_size(...) bytes, 16-byte aligned (NULL
+ *               allowed when that size is 0).  FA_ERR_INVALID_ARG if smaller.
+ * The plan depends on the current device's SM count; fa_fwd_split_count
+ * returns the number of ranges the call will use (1 = not split). */
+size_t fa_fwd_split_workspace_size(int B, int H, int N, int d, int causal, int has_kv_lens,
+                                   int num_splits);
+int fa_fwd_split_count(int B, int H, int N, int d, int causal, int has_kv_lens, int num_splits);
+fa_status fa_fwd_split(const void* q, const void* k, const void* v, void* o, float* lse,
+                       int B, int H, int N, int d, float scale, int causal, const int* kv_lens,
+                       int num_splits, void* workspace, size_t workspace_bytes,
+                       fa_stream_t stream);
+
 /* --------------------------------------------------------------- backward */
 
 /* Scratch for fa_bwd / fa_bwd_ex, in bytes: the row statistics
@@ -192,6 +221,14 @@ fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* v8,
                      const float* sq, const float* sk, const float* sv,
                      void* o, float* lse, int B, int H, int N, int d, float scale,
                      int causal, const int* kv_lens, fa_stream_t stream);
+
+/* Split-key FP8 forward: fa_fwd_fp8 with the key ranges and merge of
+ * fa_fwd_split (same num_splits and workspace rules; d = 128). */
+fa_status fa_fwd_fp8_split(const void* q8, const void* k8, const void* v8,
+                           const float* sq, const float* sk, const float* sv,
+                           void* o, float* lse, int B, int H, int N, int d, float scale,
+                           int causal, const int* kv_lens, int num_splits, void* workspace,
+                           size_t workspace_bytes, fa_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -57,6 +57,31 @@ def test_version_and_sizes(lib):
     assert lib.fa_fp8_num_blocks(16384) == 256 and lib.fa_fp8_num_blocks(65) == 2
 
 
+def test_split_plan_without_gpu(lib):
+    """Split-key plan (fa_fwd_split_count / _workspace_size) for a 152-SM
+    device (the default when no GPU is visible).  Long_head (B=2 H=16 N=4096)
+    and long_seq (B=1 H=8 N=16384) both have 512 items of 256 query rows: 3
+    full rounds of 152 plus 56; splitting those 56 into 2 key ranges makes the
+    last round half as long (estimated 120 vs 136 key blocks, resp. 456 vs 520),
+    so 56 * 2 = 112 partials of 256 rows x (128 + 1) float32 values."""
+    cnt, wsz = lib.fa_fwd_split_count, lib.fa_fwd_split_workspace_size
+    cnt.restype, cnt.argtypes = ctypes.c_int, [ctypes.c_int] * 7
+    wsz.restype, wsz.argtypes = ctypes.c_size_t, [ctypes.c_int] * 7
+    expect = 112 * 256 * 128 * 4 + 112 * 256 * 4
+    for (B, H, N) in ((2, 16, 4096), (1, 8, 16384)):
+        assert cnt(B, H, N, 128, 0, 0, 0) == 2
+        assert wsz(B, H, N, 128, 0, 0, 0) == expect
+        assert cnt(B, H, N, 128, 1, 0, 0) == 1      # causal: not split automatically
+        assert cnt(B, H, N, 128, 0, 1, 0) == 1      # key-padded: not split automatically
+        assert wsz(B, H, N, 128, 1, 0, 0) == 0
+    assert cnt(1, 1, 128, 64, 0, 0, 0) == 1         # one key block
+    assert cnt(2, 2, 300, 64, 0, 0, 1) == 1         # explicit: no split
+    assert cnt(2, 2, 300, 64, 1, 0, 3) == 3         # explicit: every item in 3 ranges
+    assert wsz(2, 2, 300, 64, 1, 0, 3) == (2 * 2 * 2) * 3 * 256 * (64 + 1) * 4
+    assert cnt(2, 2, 300, 64, 0, 0, 1000) == 64     # capped
+    assert wsz(2, 2, 300, 64, 0, 0, -1) == 0
+
+
 def _fwd(lib, q, k, v, o, lse, B, H, N, d, scale=0.125, causal=0):
     lib.fa_fwd.restype = ctypes.c_int
     lib.fa_fwd.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_int] * 4 + [ctypes.c_float, ctypes.c_int,
