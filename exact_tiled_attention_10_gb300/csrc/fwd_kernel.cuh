@@ -538,8 +538,35 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             float m = -INFINITY, l = 0.f;
             float lq = 0.f;  // FP8: sum of the E4M3-rounded weights (normalises O)
+            // FP8: key / value scales of the two 64-key halves of block j, read one
+            // block ahead so that the global-memory latency stays off the step
+            float skn[2] = {1.f, 1.f}, svn[2] = {1.f, 1.f};
+            auto load_scales = [&](int jj) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int blk = (I.j0 + jj) * 2 + h;
+                    skn[h] = (blk < p.nblk) ? __ldg(p.sk + (size_t)I.bh * p.nblk + blk) : 1.f;
+                    svn[h] = (blk < p.nblk) ? __ldg(p.sv + (size_t)I.bh * p.nblk + blk) : sv_max;
+                }
+            };
+            if (C::FP8) load_scales(0);
             bool ok = true;
             for (int j = 0; j < n; ++j) {
+                // multipliers of the raw scores (log2 domain) per 64-key half, formed
+                // before the wait for S
+                float cm[2], lg[2] = {0.f, 0.f}, inv_w[2] = {1.f, 1.f};
+                if (C::FP8) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        cm[h] = p.scale_log2 * sq_row * skn[h];
+                        const float w = svn[h] / sv_max * 448.f;
+                        lg[h] = __log2f(w);
+                        inv_w[h] = 1.f / w;
+                    }
+                    if (j + 1 < n) load_scales(j + 1);
+                } else {
+                    cm[0] = cm[1] = p.scale_log2;
+                }
                 if (!(ok = wait_bounded_warp(BAR(C::B_SFULL + t), sph, abort_flag, p.err, kErrWaitFwdSoftmax))) break;
                 sph ^= 1;
                 tc_fence_after();
@@ -560,22 +587,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int col = col0 + c;
                         if (col >= I.kvl || (CAUSAL && col > row)) s[c] = -INFINITY;
                     }
-                }
-                // multipliers of the raw scores (log2 domain) per 64-key half
-                float cm[2], lg[2] = {0.f, 0.f}, inv_w[2] = {1.f, 1.f};
-                if (C::FP8) {
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int blk = (I.j0 + j) * 2 + h;
-                        const float skb = (blk < p.nblk) ? __ldg(p.sk + (size_t)I.bh * p.nblk + blk) : 1.f;
-                        const float svb = (blk < p.nblk) ? __ldg(p.sv + (size_t)I.bh * p.nblk + blk) : sv_max;
-                        cm[h] = p.scale_log2 * sq_row * skb;
-                        const float w = svb / sv_max * 448.f;
-                        lg[h] = __log2f(w);
-                        inv_w[h] = 1.f / w;
-                    }
-                } else {
-                    cm[0] = cm[1] = p.scale_log2;
                 }
                 // O *= f over the row (O holds the blocks whose P V has completed)
                 auto rescale_o = [&](float f) {
