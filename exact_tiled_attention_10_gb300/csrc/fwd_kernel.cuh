@@ -39,11 +39,17 @@ namespace fwd {
 constexpr int kThreads = 384;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr int kRegsSoftmax = 192, kRegsIssue = 120;
 // Conditional rescaling slack in the log2 domain: P values may reach 2^8
 // before the reference max is moved (bf16 path).  The FP8 path keeps the exact
 // max so that P <= 1 fits the E4M3 range after the value-scale fold.
 constexpr float kRescaleSlack = 8.0f;
+// FP8: the probabilities enter P V as E4M3 codes of P * w, w = (value-block
+// scale / head's largest value-block scale) * kFp8Fold.  The fold leaves room
+// for P up to 2^kFp8Slack (4 * 112 = 448, the E4M3 maximum), so the exact
+// reference max taken first needs to move (and O be rescaled) only when a
+// row's max grows by more than kFp8Slack.
+constexpr float kFp8Slack = 2.0f;
+constexpr float kFp8Fold = 112.0f;
 // bf16 path: after the first block, P is computed with the current reference
 // max while the block's own row max is found in the same pass (3-input max on
 // the ALU pipe, beside the exponentials).  Only when some row's max exceeds
@@ -113,6 +119,9 @@ struct Cfg {
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM = OFF_MISC + 16 + 1024;  // + base alignment slack
     static constexpr uint32_t FMT = FP8 ? kFmtE4M3 : kFmtBF16;
+    // registers per thread of the softmax warpgroups / the issuing warpgroup
+    // (setmaxnreg); 2 * 128 * REGS_SOFTMAX + 128 * REGS_ISSUE <= 384 * 168
+    static constexpr int REGS_SOFTMAX = FP8 ? 208 : 192, REGS_ISSUE = FP8 ? 88 : 120;
     static constexpr uint32_t IDESC_S = idesc_make(FMT, FMT, 0, 0, 128, BC);
     static constexpr uint32_t IDESC_PV = idesc_make(FMT, FMT, 0, 1, 128, D);
     static_assert(SMEM <= 232448, "shared memory budget");
@@ -341,11 +350,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     // registers: the softmax warpgroups take what the producer / MMA warpgroup
-    // (warps 8-11, 10 and 11 idle) does not need; 2 x 128 x kRegsSoftmax +
-    // 128 x kRegsIssue equals the launch allocation of 384 x 168
-    static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsIssue <= kThreads * 168, "register split");
+    // (warps 8-11, 10 and 11 idle) does not need; 2 x 128 x C::REGS_SOFTMAX +
+    // 128 x C::REGS_ISSUE equals the launch allocation of 384 x 168
+    static_assert(2 * 128 * C::REGS_SOFTMAX + 128 * C::REGS_ISSUE <= kThreads * 168, "register split");
 
-    if (warp >= 8) regs_dec<kRegsIssue>();
+    if (warp >= 8) regs_dec<C::REGS_ISSUE>();
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------ TMA producer
         // The whole warp walks the schedule (so it stays converged); lane 0 issues.
@@ -485,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         wait_bounded_warp(BAR(C::B_DONE), 0, abort_flag, p.err, kErrWaitDrain);
     } else if (warp < 8) {
         // ------------------------------------------------------------ softmax
-        regs_inc<kRegsSoftmax>();
+        regs_inc<C::REGS_SOFTMAX>();
         const int t = warp >> 2;
         const int wq = warp & 3;
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
@@ -538,6 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             float m = -INFINITY, l = 0.f;
             float lq = 0.f;  // FP8: sum of the E4M3-rounded weights (normalises O)
+            const float w_scale = C::FP8 ? kFp8Fold / sv_max : 0.f;  // FP8: w = value-block scale * w_scale
             // FP8: key / value scales of the two 64-key halves of block j, read one
             // block ahead so that the global-memory latency stays off the step
             float skn[2] = {1.f, 1.f}, svn[2] = {1.f, 1.f};
@@ -559,9 +569,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         cm[h] = p.scale_log2 * sq_row * skn[h];
-                        const float w = svn[h] / sv_max * 448.f;
+                        const float w = svn[h] * w_scale;
                         lg[h] = __log2f(w);
-                        inv_w[h] = 1.f / w;
+                        inv_w[h] = __frcp_rn(w);
                     }
                     if (j + 1 < n) load_scales(j + 1);
                 } else {
@@ -602,9 +612,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 };
                 float lsum, lqsum;
                 if constexpr (C::FP8) {
-                    // exact reference max first (P <= 1 must hold for the E4M3 fold)
+                    // reference max first (P <= 2^kFp8Slack must hold for the E4M3 fold)
                     const float mx2 = fmaxf(row_max<C::BC / 2>(s) * cm[0], row_max<C::BC / 2>(s + C::BC / 2) * cm[1]);
-                    const bool need = mx2 > m;
+                    const bool need = mx2 > m + kFp8Slack;
                     float alpha = 1.f;
                     if (need) {
                         alpha = ex2_approx(m - mx2);  // 0 when m = -inf
@@ -656,7 +666,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             oph ^= 1;
             tc_fence_after();
             float inv = (l > 0.f) ? 1.f / l : 0.f;
-            if (C::FP8) inv = (lq > 0.f) ? sv_max * (1.f / 448.f) / lq : 0.f;
+            if (C::FP8) inv = (lq > 0.f) ? sv_max * (1.f / kFp8Fold) / lq : 0.f;
 #pragma unroll 1
             for (int c = 0; c < C::D; c += 32) {
                 uint32_t ov[32];
