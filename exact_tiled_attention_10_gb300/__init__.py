@@ -56,6 +56,8 @@ _SIGS = {
     "fa_fp8_num_blocks": ([_i], _i),
     "fa_quantize_fp8": ([_vp, _vp, _vp, _i, _i, _i, _i, _vp], _i),
     "fa_fwd_fp8": ([_vp] * 8 + [_i, _i, _i, _i, _f, _i, _vp, _vp], _i),
+    "fa_fwd_gqa": ([_vp] * 5 + [_i, _i, _i, _i, _i, _f, _i, _vp, _vp], _i),
+    "fa_bwd_gqa": ([_vp] * 9 + [_i, _i, _i, _i, _i, _f, _i, _vp, _vp, _sz, _vp], _i),
     "fa_fwd_split_workspace_size": ([_i] * 7, _sz),
     "fa_fwd_split_count": ([_i] * 7, _i),
     "fa_fwd_split": ([_vp] * 5 + [_i, _i, _i, _i, _f, _i, _vp, _i, _vp, _sz, _vp], _i),
@@ -136,12 +138,16 @@ def forward(q, k, v, causal: bool = False, scale: Optional[float] = None, kv_len
             block_c: int = 0, out: Optional[torch.Tensor] = None,
             lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None
             ) -> Tuple[torch.Tensor, torch.Tensor]:
-    """O, LSE of softmax(scale Q K^T + mask) V.  q,k,v: [B,H,N,d] bf16 or float32."""
+    """O, LSE of softmax(scale Q K^T + mask) V.  q: [B,H,N,d] bf16 or float32;
+    k, v: [B,H,N,d], or bf16 [B,Hkv,N,d] with fewer key/value heads (H a
+    multiple of Hkv; query head h uses key/value head h // (H // Hkv))."""
     lib = load_library()
     _need_cuda(q, k, v)
     B, H, N, d = q.shape
-    if k.shape != q.shape or v.shape != q.shape or k.dtype != q.dtype or v.dtype != q.dtype:
-        raise ValueError("q, k, v must share shape and dtype")
+    Hkv = k.shape[1]
+    if (k.shape != (B, Hkv, N, d) or v.shape != k.shape or k.dtype != q.dtype or v.dtype != q.dtype
+            or H % Hkv != 0):
+        raise ValueError("q [B,H,N,d]; k, v [B,Hkv,N,d] with H a multiple of Hkv; one dtype")
     if q.dtype not in (torch.bfloat16, torch.float32):
         raise ValueError("dtype must be bfloat16 or float32")
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
@@ -149,6 +155,12 @@ def forward(q, k, v, causal: bool = False, scale: Optional[float] = None, kv_len
     o = torch.empty_like(q) if out is None else out
     l = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
     _need_cuda(o, l)
+    if Hkv != H:
+        if q.dtype != torch.bfloat16:
+            raise ValueError("shared key/value heads need bfloat16 tensors")
+        _check(lib.fa_fwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(l), B, H, Hkv, N, d, scale,
+                              int(bool(causal)), _ptr(kv), _stream(q)))
+        return o, l
     dt = FA_F32 if q.dtype == torch.float32 else FA_BF16
     wsz = int(lib.fa_fwd_workspace_size(dt, B, H, N, d))
     ws = workspace
@@ -207,10 +219,12 @@ def backward(q, k, v, o, lse, dout, causal: bool = False, scale: Optional[float]
              kv_lens=None, workspace: Optional[torch.Tensor] = None,
              dq: Optional[torch.Tensor] = None, dk: Optional[torch.Tensor] = None,
              dv: Optional[torch.Tensor] = None):
-    """dQ, dK, dV of L = sum(O * dout)."""
+    """dQ, dK, dV of L = sum(O * dout).  With fewer key/value heads (k, v
+    [B,Hkv,N,d]), dK and dV sum over the query heads sharing each one."""
     lib = load_library()
     _need_cuda(q, k, v, o, lse, dout)
     B, H, N, d = q.shape
+    Hkv = k.shape[1]
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     kv = _kv(kv_lens, B, q.device)
     dt = FA_F32 if q.dtype == torch.float32 else FA_BF16
@@ -219,9 +233,16 @@ def backward(q, k, v, o, lse, dout, causal: bool = False, scale: Optional[float]
     if ws is None or ws.numel() * ws.element_size() < wsz:
         ws = torch.empty(wsz, dtype=torch.uint8, device=q.device)
     dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(q) if dk is None else dk
-    dv = torch.empty_like(q) if dv is None else dv
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
     _need_cuda(dq, dk, dv)
+    if Hkv != H:
+        if q.dtype != torch.bfloat16 or H % Hkv != 0:
+            raise ValueError("shared key/value heads need bfloat16 tensors and H a multiple of Hkv")
+        _check(lib.fa_bwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
+                              _ptr(dk), _ptr(dv), B, H, Hkv, N, d, scale, int(bool(causal)), _ptr(kv),
+                              _ptr(ws), ws.numel() * ws.element_size(), _stream(q)))
+        return dq, dk, dv
     _check(lib.fa_bwd_ex(dt, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
                          _ptr(dk), _ptr(dv), B, H, N, d, scale, int(bool(causal)), _ptr(kv),
                          _ptr(ws), ws.numel() * ws.element_size(), _stream(q)))

@@ -215,8 +215,11 @@ SplitPlan plan_split(int B, int H, int N, int d, bool causal, bool has_kv, int r
 fa_status fwd_impl(fa_dtype dtype, int block_c, bool fp8, const void* q, const void* k, const void* v, const float* sq,
                    const float* sk, const float* sv, void* o, float* lse, int B, int H, int N, int d, float scale,
                    int causal, const int* kv_lens, void* workspace, size_t workspace_bytes, cudaStream_t stream,
-                   int num_splits = 1, void* split_ws = nullptr, size_t split_ws_bytes = 0) {
+                   int num_splits = 1, void* split_ws = nullptr, size_t split_ws_bytes = 0, int Hkv = 0) {
     FA_TRY(check_common(B, H, N, d, scale));
+    if (Hkv == 0) Hkv = H;
+    if (Hkv < 1 || H % Hkv != 0) return fail(FA_ERR_INVALID_ARG, "H (%d) must be a multiple of Hkv (%d)", H, Hkv);
+    if (Hkv != H && dtype != FA_BF16) return fail(FA_ERR_UNSUPPORTED, "shared key/value heads need bf16 inputs");
     FA_CHECK_PTR(q);
     FA_CHECK_PTR(k);
     FA_CHECK_PTR(v);
@@ -233,7 +236,7 @@ fa_status fwd_impl(fa_dtype dtype, int block_c, bool fp8, const void* q, const v
     if (dtype != FA_BF16 && dtype != FA_F32) return fail(FA_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
     DeviceInfo* dev = nullptr;
     FA_TRY(device_info(&dev));
-    const int BH = B * H;
+    const int BH = B * H, BHkv = B * Hkv;
     const size_t n = (size_t)BH * N * d;
     const bool split = (dtype == FA_F32);
     const void *qb = q, *kb = k, *vb = v, *qlo = q, *klo = k;
@@ -265,21 +268,21 @@ fa_status fwd_impl(fa_dtype dtype, int block_c, bool fp8, const void* q, const v
     fa::FwdMaps m;
     if (fp8) {
         FA_TRY(make_map_3d(&m.q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, qb, d, N, BH, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B));
-        FA_TRY(make_map_3d(&m.k, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kb, d, N, BH, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B));
-        FA_TRY(make_map_3d(&m.v, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, vb, d, N, BH, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B));
+        FA_TRY(make_map_3d(&m.k, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kb, d, N, BHkv, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B));
+        FA_TRY(make_map_3d(&m.v, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, vb, d, N, BHkv, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B));
         m.q_lo = m.q;
         m.k_lo = m.k;
     } else {
         const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
         FA_TRY(make_map_3d(&m.q, bf, 2, qb, d, N, BH, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B));
-        FA_TRY(make_map_3d(&m.k, bf, 2, kb, d, N, BH, 64, block_c, CU_TENSOR_MAP_SWIZZLE_128B));
-        FA_TRY(make_map_3d(&m.v, bf, 2, vb, d, N, BH, 64, block_c, CU_TENSOR_MAP_SWIZZLE_128B));
+        FA_TRY(make_map_3d(&m.k, bf, 2, kb, d, N, BHkv, 64, block_c, CU_TENSOR_MAP_SWIZZLE_128B));
+        FA_TRY(make_map_3d(&m.v, bf, 2, vb, d, N, BHkv, 64, block_c, CU_TENSOR_MAP_SWIZZLE_128B));
         FA_TRY(make_map_3d(&m.q_lo, bf, 2, qlo, d, N, BH, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B));
-        FA_TRY(make_map_3d(&m.k_lo, bf, 2, klo, d, N, BH, 64, block_c, CU_TENSOR_MAP_SWIZZLE_128B));
+        FA_TRY(make_map_3d(&m.k_lo, bf, 2, klo, d, N, BHkv, 64, block_c, CU_TENSOR_MAP_SWIZZLE_128B));
     }
     fa::FwdParams p;
     memset(&p, 0, sizeof(p));
-    p.B = B; p.H = H; p.N = N;
+    p.B = B; p.H = H; p.N = N; p.Hkv = Hkv;
     p.num_qp = (N + 255) / 256;
     p.num_items = BH * p.num_qp;
     p.scale = scale;
@@ -377,6 +380,13 @@ fa_status fa_fwd_split(const void* q, const void* k, const void* v, void* o, flo
                     nullptr, 0, stream, num_splits, workspace, workspace_bytes);
 }
 
+fa_status fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv, int N,
+                     int d, float scale, int causal, const int* kv_lens, fa_stream_t stream) {
+    if (Hkv < 1 || H % Hkv != 0) return fail(FA_ERR_INVALID_ARG, "H (%d) must be a multiple of Hkv (%d)", H, Hkv);
+    return fwd_impl(FA_BF16, 0, false, q, k, v, nullptr, nullptr, nullptr, o, lse, B, H, N, d, scale, causal, kv_lens,
+                    nullptr, 0, stream, 1, nullptr, 0, Hkv);
+}
+
 size_t fa_fwd_workspace_size(fa_dtype dtype, int B, int H, int N, int d) {
     if (dtype != FA_F32 || B <= 0 || H <= 0 || N <= 0 || d <= 0) return 0;
     return 5 * round_up((size_t)B * H * N * d * 2, 256);
@@ -432,15 +442,18 @@ fa_status bwd_pre_impl(const BwdCtx& c, bool f32, const void* o, const float* ls
 
 fa_status bwd_main_impl(const BwdCtx& c, bool f32, const void* qb, const void* kb, const void* vb, const void* gb,
                         void* dk, void* dv, int B, int H, int N, int d, float scale, int causal, const int* kv_lens,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, int Hkv = 0) {
     const int BH = c.BH, Np = c.Np;
+    if (Hkv == 0) Hkv = H;
+    if (Hkv < 1 || H % Hkv != 0) return fail(FA_ERR_INVALID_ARG, "H (%d) must be a multiple of Hkv (%d)", H, Hkv);
+    const int BHkv = B * Hkv;
     float* dqacc = reinterpret_cast<float*>(c.ws + c.L.dqacc);
     const int BR = (d == 128) ? 64 : 128;
     CUtensorMap tq, tk, tv, tdo, tdq;
     FA_TRY(make_map_3d(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, qb, d, N, BH, 64, BR, CU_TENSOR_MAP_SWIZZLE_128B));
     FA_TRY(make_map_3d(&tdo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, gb, d, N, BH, 64, BR, CU_TENSOR_MAP_SWIZZLE_128B));
-    FA_TRY(make_map_3d(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kb, d, N, BH, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B));
-    FA_TRY(make_map_3d(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, vb, d, N, BH, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B));
+    FA_TRY(make_map_3d(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kb, d, N, BHkv, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B));
+    FA_TRY(make_map_3d(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, vb, d, N, BHkv, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B));
     {
         cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)BH * Np};
         cuuint64_t strides[1] = {(cuuint64_t)d * 4};
@@ -456,9 +469,9 @@ fa_status bwd_main_impl(const BwdCtx& c, bool f32, const void* qb, const void* k
     }
     fa::BwdParams p;
     memset(&p, 0, sizeof(p));
-    p.B = B; p.H = H; p.N = N; p.Np = Np;
+    p.B = B; p.H = H; p.N = N; p.Np = Np; p.Hkv = Hkv;
     p.num_kt = (N + 127) / 128;
-    p.num_items = BH * p.num_kt;
+    p.num_items = BHkv * p.num_kt;
     p.scale = scale;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.kv_lens = kv_lens;
@@ -468,8 +481,9 @@ fa_status bwd_main_impl(const BwdCtx& c, bool f32, const void* qb, const void* k
     p.dk = dk;
     p.dv = dv;
     p.err = c.dev->err_word;
-    cudaError_t e = fa::launch_bwd_main(d, causal != 0, f32, tq, tk, tv, tdo, tdq, p,
-                                        grid_for_items(p.num_items, c.dev->sms), stream);
+    const int grid = grid_for_items(p.num_items, c.dev->sms);
+    cudaError_t e = (Hkv != H) ? fa::launch_bwd_main_gqa(d, causal != 0, tq, tk, tv, tdo, tdq, p, grid, stream)
+                               : fa::launch_bwd_main(d, causal != 0, f32, tq, tk, tv, tdo, tdq, p, grid, stream);
     if (e != cudaSuccess) return cuda_fail(e, "backward main launch");
     return FA_OK;
 }
@@ -546,6 +560,26 @@ fa_status fa_bwd_ex(fa_dtype dtype, const void* q, const void* k, const void* v,
     FA_TRY(bwd_pre_impl(c, f32, o, lse, dout, N, d, stream));
     FA_TRY(bwd_main_impl(c, f32, qb, kb, vb, gb, dk, dv, B, H, N, d, scale, causal, kv_lens, stream));
     return bwd_dq_impl(c, f32, dq, N, d, scale, stream);
+}
+
+fa_status fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                     void* dq, void* dk, void* dv, int B, int H, int Hkv, int N, int d, float scale, int causal,
+                     const int* kv_lens, void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+    FA_CHECK_PTR(q);
+    FA_CHECK_PTR(k);
+    FA_CHECK_PTR(v);
+    FA_CHECK_PTR(o);
+    FA_CHECK_PTR(lse);
+    FA_CHECK_PTR(dout);
+    FA_CHECK_PTR(dq);
+    FA_CHECK_PTR(dk);
+    FA_CHECK_PTR(dv);
+    if (Hkv < 1 || H % Hkv != 0) return fail(FA_ERR_INVALID_ARG, "H (%d) must be a multiple of Hkv (%d)", H, Hkv);
+    BwdCtx c{};
+    FA_TRY(bwd_setup(FA_BF16, B, H, N, d, scale, workspace, workspace_bytes, &c));
+    FA_TRY(bwd_pre_impl(c, false, o, lse, dout, N, d, stream));
+    FA_TRY(bwd_main_impl(c, false, q, k, v, dout, dk, dv, B, H, N, d, scale, causal, kv_lens, stream, Hkv));
+    return bwd_dq_impl(c, false, dq, N, d, scale, stream);
 }
 
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,

@@ -97,14 +97,22 @@ struct Cfg {
     __host__ __device__ static constexpr int dq_col(int slot) { return DQ_ALIAS ? x_col(slot) : TM_DQ; }
 };
 
+// A work item is one key block of one key/value head: bh = b * Hkv + kv head
+// (the K, V, dK, dV row).  Its steps run over the query heads sharing that
+// key/value head (qh0 .. qh0 + H/Hkv - 1; one head without sharing) and, for
+// each, the query blocks i0 .. i0 + ni - 1, so dK and dV sum over the group.
 struct Item {
     int bh, b, kt, kvl, i0, n;
+    int qh0, ni;  // first query head row (b * H + ...), query blocks per query head
 };
 
-template <class C, bool CAUSAL>
+// GQA: the kernel instance for shared key/value heads (compiled separately so
+// that the plain backward carries none of the group bookkeeping).
+template <class C, bool CAUSAL, bool GQA>
 __device__ __forceinline__ Item get_item(int it, const BwdParams& p) {
     Item I;
-    const int BH = p.B * p.H;
+    const int Hkv = GQA ? p.Hkv : p.H;
+    const int BH = p.B * Hkv;
     if (CAUSAL) {  // key blocks near the start see the most query rows: first
         I.kt = it / BH;
         I.bh = it % BH;
@@ -112,15 +120,28 @@ __device__ __forceinline__ Item get_item(int it, const BwdParams& p) {
         I.bh = it / p.num_kt;
         I.kt = it % p.num_kt;
     }
-    I.b = I.bh / p.H;
+    I.b = I.bh / Hkv;
+    const int group = GQA ? p.H / Hkv : 1;
+    I.qh0 = GQA ? I.b * p.H + (I.bh - I.b * Hkv) * group : I.bh;
     int kvl = p.N;
     if (p.kv_lens) kvl = min(max(__ldg(p.kv_lens + I.b), 0), p.N);
     I.kvl = kvl;
     const int key0 = I.kt * C::BC;
     const int iend = (p.N + C::BR - 1) / C::BR;
     I.i0 = CAUSAL ? key0 / C::BR : 0;
-    I.n = (key0 >= kvl) ? 0 : max(iend - I.i0, 0);
+    I.ni = (key0 >= kvl) ? 0 : max(iend - I.i0, 0);
+    I.n = I.ni * group;
     return I;
+}
+// Query head row bhq and query block i of consecutive steps of an item:
+// start with (qh0, i0), advance once per step (one query head: i = i0 + s).
+template <bool GQA>
+__device__ __forceinline__ void step_next(const Item& I, int& bhq, int& i) {
+    ++i;
+    if (GQA && i == I.i0 + I.ni) {
+        i = I.i0;
+        ++bhq;
+    }
 }
 
 template <bool OUT_F32>
@@ -193,7 +214,7 @@ __device__ __forceinline__ void mma_dq(uint32_t d_tmem, uint64_t k_mn, uint64_t 
     }
 }
 
-template <class C, bool CAUSAL, bool OUT_F32>
+template <class C, bool CAUSAL, bool OUT_F32, bool GQA>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
@@ -252,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int rd = 0; rd < snake_rounds(p.num_items) && ok; ++rd) {
             const int it = snake_item(rd, p.num_items);
             if (it < 0) continue;
-            const Item I = get_item<C, CAUSAL>(it, p);
+            const Item I = get_item<C, CAUSAL, GQA>(it, p);
             if (I.n == 0) continue;
             if (!(ok = wait_bounded_warp(BAR(C::B_KVEMPTY), kve ^ 1, abort_flag, p.err, kErrWaitBwdProducer))) break;
             kve ^= 1;
@@ -264,17 +285,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             __syncwarp();
-            for (int s = 0; s < I.n; ++s) {
-                const int i = I.i0 + s;
+            int bhq = I.qh0, i = I.i0;
+            for (int s = 0; s < I.n; ++s, step_next<GQA>(I, bhq, i)) {
                 if (!(ok = wait_bounded_warp(BAR(C::B_QEMPTY + st), ph ^ 1, abort_flag, p.err, kErrWaitBwdProducer))) break;
                 if (lane == 0) {
                     const uint32_t bar = BAR(C::B_QFULL + st);
                     mbar_arrive_expect_tx(bar, 2 * C::Q_TILE + C::STAT_BYTES);
                     for (int bx = 0; bx < C::NBOX; ++bx) {
-                        tma_load_3d(sbase + C::OFF_Q + st * C::Q_TILE + bx * C::Q_BOX, &tq, bar, bx * 64, i * C::BR, I.bh);
-                        tma_load_3d(sbase + C::OFF_DO + st * C::Q_TILE + bx * C::Q_BOX, &tdo, bar, bx * 64, i * C::BR, I.bh);
+                        tma_load_3d(sbase + C::OFF_Q + st * C::Q_TILE + bx * C::Q_BOX, &tq, bar, bx * 64, i * C::BR, bhq);
+                        tma_load_3d(sbase + C::OFF_DO + st * C::Q_TILE + bx * C::Q_BOX, &tdo, bar, bx * 64, i * C::BR, bhq);
                     }
-                    const size_t roff = (size_t)I.bh * p.Np + (size_t)i * C::BR;
+                    const size_t roff = (size_t)bhq * p.Np + (size_t)i * C::BR;
                     bulk_load(sbase + C::OFF_STAT + st * C::STAT_BYTES, p.lse2 + roff, C::BR * 4, bar);
                     bulk_load(sbase + C::OFF_STAT + st * C::STAT_BYTES + C::BR * 4, p.dvec + roff, C::BR * 4, bar);
                 }
@@ -326,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int rd = 0; rd < snake_rounds(p.num_items) && ok; ++rd) {
             const int it = snake_item(rd, p.num_items);
             if (it < 0) continue;
-            const Item I = get_item<C, CAUSAL>(it, p);
+            const Item I = get_item<C, CAUSAL, GQA>(it, p);
             if (I.n == 0) continue;
             if (!(ok = wait_bounded_warp(BAR(C::B_KVFULL), kvph, abort_flag, p.err, kErrWaitBwdMma))) break;
             kvph ^= 1;
@@ -387,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int rd = 0; rd < snake_rounds(p.num_items) && ok; ++rd) {
             const int it = snake_item(rd, p.num_items);
             if (it < 0) continue;
-            const Item I = get_item<C, CAUSAL>(it, p);
+            const Item I = get_item<C, CAUSAL, GQA>(it, p);
             const int key = I.kt * C::BC + kr;
             const size_t krow = (size_t)I.bh * p.N + key;
             if (I.n == 0) {  // key block entirely beyond kv_len: zero gradients
@@ -401,10 +422,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 continue;
             }
-            for (int s = 0; s < I.n; ++s) {
+            int bhq = I.qh0, i = I.i0;
+            for (int s = 0; s < I.n; ++s, step_next<GQA>(I, bhq, i)) {
                 const int slot = s % C::NSLOT;
                 const int dsb = s & 1;
-                const int i = I.i0 + s;
                 const int q0 = i * C::BR + h * C::HALF;  // first query column of this half
                 // statistics of this stage (LSE*log2e, D) -- readable once the stage is full
                 if (!(ok = wait_bounded_warp(BAR(C::B_QFULL + st), qph, abort_flag, p.err, kErrWaitBwdCompute))) break;
@@ -526,9 +547,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int rd = 0; rd < snake_rounds(p.num_items) && ok; ++rd) {
             const int it = snake_item(rd, p.num_items);
             if (it < 0) continue;
-            const Item I = get_item<C, CAUSAL>(it, p);
-            for (int s = 0; s < I.n; ++s) {
-                const int i = I.i0 + s;
+            const Item I = get_item<C, CAUSAL, GQA>(it, p);
+            int bhq = I.qh0, i = I.i0;
+            for (int s = 0; s < I.n; ++s, step_next<GQA>(I, bhq, i)) {
                 const int dqs = C::DQ_ALIAS ? (s % C::NSLOT) : 0;
                 if (!(ok = wait_bounded_warp(BAR(C::B_DQFULL + dqs), dqph[dqs], abort_flag, p.err, kErrWaitBwdDq))) break;
                 dqph[dqs] ^= 1;
@@ -563,10 +584,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) {
                     if constexpr (C::D == 128) {
-                        tma_reduce_add_2d(&tdq, stage, wq * 32, I.bh * p.Np + i * C::BR);
+                        tma_reduce_add_2d(&tdq, stage, wq * 32, bhq * p.Np + i * C::BR);
                     } else {
-                        tma_reduce_add_2d(&tdq, stage, 0, I.bh * p.Np + i * C::BR + wq * 32);
-                        tma_reduce_add_2d(&tdq, stage + 4096, 32, I.bh * p.Np + i * C::BR + wq * 32);
+                        tma_reduce_add_2d(&tdq, stage, 0, bhq * p.Np + i * C::BR + wq * 32);
+                        tma_reduce_add_2d(&tdq, stage + 4096, 32, bhq * p.Np + i * C::BR + wq * 32);
                     }
                     bulk_commit_group();
                 }
@@ -585,11 +606,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <class C, bool CAUSAL, bool OUT_F32>
+template <class C, bool CAUSAL, bool OUT_F32, bool GQA = false>
 cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                    const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p, int grid,
                    cudaStream_t stream) {
-    auto kern = bwd_kernel<C, CAUSAL, OUT_F32>;
+    auto kern = bwd_kernel<C, CAUSAL, OUT_F32, GQA>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     kern<<<grid, kThreads, C::SMEM, stream>>>(tq, tk, tv, tdo, tdq, p);

@@ -50,6 +50,7 @@ __host__ __device__ __forceinline__ void fwd_item_coords(int it, bool causal, in
 
 struct FwdParams {
     int B, H, N;
+    int Hkv;          // key/value heads (H % Hkv == 0): query head h reads key/value head h / (H / Hkv)
     int num_qp;       // query-row pairs of 128-row tiles per head: ceil(N / 256)
     int num_items;    // B * H * num_qp
     // Split keys (FlashDecoding form): work units 0 .. num_whole-1 are whole
@@ -75,8 +76,9 @@ struct FwdParams {
 
 struct BwdParams {
     int B, H, N, Np;  // Np: N padded to a multiple of 128
+    int Hkv;          // key/value heads (H % Hkv == 0); dK, dV are [B,Hkv,N,d]
     int num_kt;       // key tiles per head: ceil(N / 128)
-    int num_items;    // B * H * num_kt
+    int num_items;    // B * Hkv * num_kt
     float scale;
     float scale_log2;
     const int* kv_lens;
@@ -103,6 +105,9 @@ cudaError_t launch_fwd_splitk(int d, bool fp8, bool causal, const FwdMaps& m, co
                               cudaStream_t stream);
 cudaError_t launch_fwd_fp8_d128(bool causal, const FwdMaps& m, const FwdParams& p, int grid,
                                 cudaStream_t stream);
+cudaError_t launch_bwd_main_gqa(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
+                                const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
+                                const BwdParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_bwd_main(int d, bool causal, bool out_f32, const CUtensorMap& tq,
                             const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
                             const CUtensorMap& tdq, const BwdParams& p, int grid,

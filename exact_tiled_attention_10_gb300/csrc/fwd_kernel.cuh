@@ -129,6 +129,7 @@ struct Cfg {
 
 struct Item {
     int bh, b, row0, kvl;
+    int kvh;    // key/value head row of K, V (b * Hkv + h / group)
     int n[2];   // key blocks of tile 0 / tile 1 in this unit
     int nmax;
     int j0;     // first key block of this unit
@@ -153,6 +154,7 @@ __device__ __forceinline__ Item get_item(int unit, const FwdParams& p) {
     int qp;
     fwd_item_coords(it, CAUSAL, BH, p.num_qp, I.bh, qp);
     I.b = I.bh / p.H;
+    I.kvh = I.b * p.Hkv + (I.bh - I.b * p.H) / (p.H / p.Hkv);
     int kvl = p.N;
     if (p.kv_lens) kvl = min(max(__ldg(p.kv_lens + I.b), 0), p.N);
     I.kvl = kvl;
@@ -394,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             for (int bx = 0; bx < C::NBOX; ++bx)
                                 tma_load_3d(sbase + C::OFF_K + kst * C::K_STAGE + part * C::KV_TILE + bx * C::KV_BOX,
                                             part ? &tkl : &tk, BAR(C::B_KFULL + kst), bx * C::BOX_ELEMS,
-                                            (I.j0 + idx) * C::BC, I.bh);
+                                            (I.j0 + idx) * C::BC, I.kvh);
                     }
                     __syncwarp();
                     if (++kst == C::KSTAGES) { kst = 0; kph ^= 1; }
@@ -406,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mbar_arrive_expect_tx(BAR(C::B_VFULL + vst), C::KV_TILE);
                         for (int bx = 0; bx < C::NBOX; ++bx)
                             tma_load_3d(sbase + C::OFF_V + vst * C::KV_TILE + bx * C::KV_BOX, &tv, BAR(C::B_VFULL + vst),
-                                        bx * C::BOX_ELEMS, (I.j0 + j) * C::BC, I.bh);
+                                        bx * C::BOX_ELEMS, (I.j0 + j) * C::BC, I.kvh);
                     }
                     __syncwarp();
                     if (++vst == C::VSTAGES) { vst = 0; vph ^= 1; }
@@ -537,7 +539,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // FP8: per-row query scale and the head's largest value-block scale
             float sq_row = 1.f, sv_max = 1.f;
             if (C::FP8) {
-                const float* svh = p.sv + (size_t)I.bh * p.nblk;
+                const float* svh = p.sv + (size_t)I.kvh * p.nblk;
                 float mxs = 0.f;
                 for (int i = lane; i < p.nblk; i += 32) mxs = fmaxf(mxs, __ldg(svh + i));
 #pragma unroll
@@ -555,8 +557,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const int blk = (I.j0 + jj) * 2 + h;
-                    skn[h] = (blk < p.nblk) ? __ldg(p.sk + (size_t)I.bh * p.nblk + blk) : 1.f;
-                    svn[h] = (blk < p.nblk) ? __ldg(p.sv + (size_t)I.bh * p.nblk + blk) : sv_max;
+                    skn[h] = (blk < p.nblk) ? __ldg(p.sk + (size_t)I.kvh * p.nblk + blk) : 1.f;
+                    svn[h] = (blk < p.nblk) ? __ldg(p.sv + (size_t)I.kvh * p.nblk + blk) : sv_max;
                 }
             };
             if (C::FP8) load_scales(0);

@@ -133,6 +133,16 @@ fa_status fa_fwd_split(const void* q, const void* k, const void* v, void* o, flo
                        int num_splits, void* workspace, size_t workspace_bytes,
                        fa_stream_t stream);
 
+/* Shared key/value heads (grouped-query attention; multi-query for Hkv = 1),
+ * bf16.  q, o: [B,H,N,d]; k, v: [B,Hkv,N,d] with H a multiple of Hkv; query
+ * head h attends with key/value head h / (H / Hkv) -- the head broadcast of
+ * flash_attn_func API ([CH18] §18.7.1: with fewer key/value heads than query
+ * heads, K and V are broadcast over the head dimension).  Otherwise as
+ * fa_fwd.  FA_ERR_INVALID_ARG if H % Hkv != 0. */
+fa_status fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
+                     int B, int H, int Hkv, int N, int d, float scale, int causal,
+                     const int* kv_lens, fa_stream_t stream);
+
 /* --------------------------------------------------------------- backward */
 
 /* Scratch for fa_bwd / fa_bwd_ex, in bytes: the row statistics
@@ -150,6 +160,16 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o,
                  const float* lse, const void* dout, void* dq, void* dk, void* dv,
                  int B, int H, int N, int d, float scale, int causal, const int* kv_lens,
                  void* workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/* Backward with shared key/value heads (see fa_fwd_gqa), bf16: dq is
+ * [B,H,N,d]; dk, dv are [B,Hkv,N,d] and hold the sum over the H / Hkv query
+ * heads that share each key/value head (the gradient of the broadcast).
+ * Workspace: fa_bwd_workspace_size(FA_BF16, B, H, N, d). */
+fa_status fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o,
+                     const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                     int B, int H, int Hkv, int N, int d, float scale, int causal,
+                     const int* kv_lens, void* workspace, size_t workspace_bytes,
+                     fa_stream_t stream);
 
 /* The three phases fa_bwd runs, callable one by one (bf16 tensors, same
  * workspace).  fa_bwd == fa_bwd_preprocess; fa_bwd_main; fa_bwd_dq.
