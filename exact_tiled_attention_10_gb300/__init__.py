@@ -21,7 +21,7 @@ from typing import Optional, Tuple
 
 import torch
 
-__all__ = ["forward", "forward_split", "backward", "quantize_fp8", "forward_fp8", "forward_fp8_split",
+__all__ = ["forward", "forward_split", "forward_varlen", "backward_varlen", "backward", "quantize_fp8", "forward_fp8", "forward_fp8_split",
            "split_count", "split_workspace_size", "check_device_status",
            "selftest_wait_timeout",
            "bwd_workspace_size", "fwd_workspace_size", "library_path", "load_library", "FAError"]
@@ -57,6 +57,9 @@ _SIGS = {
     "fa_quantize_fp8": ([_vp, _vp, _vp, _i, _i, _i, _i, _vp], _i),
     "fa_fwd_fp8": ([_vp] * 8 + [_i, _i, _i, _i, _f, _i, _vp, _vp], _i),
     "fa_fwd_gqa": ([_vp] * 5 + [_i, _i, _i, _i, _i, _f, _i, _vp, _vp], _i),
+    "fa_fwd_varlen": ([_vp] * 6 + [_i, _i, _i, _i, _i, _i, _f, _i, _vp], _i),
+    "fa_bwd_varlen_workspace_size": ([_i] * 4, _sz),
+    "fa_bwd_varlen": ([_vp] * 10 + [_i, _i, _i, _i, _i, _i, _f, _i, _vp, _sz, _vp], _i),
     "fa_bwd_gqa": ([_vp] * 9 + [_i, _i, _i, _i, _i, _f, _i, _vp, _vp, _sz, _vp], _i),
     "fa_fwd_split_workspace_size": ([_i] * 7, _sz),
     "fa_fwd_split_count": ([_i] * 7, _i),
@@ -213,6 +216,56 @@ def forward_split(q, k, v, causal: bool = False, scale: Optional[float] = None, 
     _check(lib.fa_fwd_split(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(l), B, H, N, d, scale,
                             int(bool(causal)), _ptr(kv), int(num_splits), wsp, wsz, _stream(q)))
     return o, l
+
+
+def _cu(cu_seqlens, device):
+    cu = cu_seqlens.to(device=device, dtype=torch.int32).contiguous()
+    if cu.dim() != 1 or cu.numel() < 2:
+        raise ValueError("cu_seqlens must be a 1-D tensor of batch + 1 offsets")
+    return cu
+
+
+def forward_varlen(q, k, v, cu_seqlens, max_seqlen: int, causal: bool = False,
+                   scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                   lse: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Packed variable-length forward: q [total, H, d], k, v [total, Hkv, d]
+    (bf16), sequence b = tokens cu_seqlens[b] .. cu_seqlens[b+1]-1.  Returns
+    O [total, H, d] and LSE [H, total]."""
+    lib = load_library()
+    _need_cuda(q, k, v)
+    T, H, d = q.shape
+    Hkv = k.shape[1]
+    if (q.dtype != torch.bfloat16 or k.dtype != q.dtype or v.dtype != q.dtype or k.shape != (T, Hkv, d)
+            or v.shape != k.shape or H % Hkv != 0):
+        raise ValueError("q [total,H,d], k, v [total,Hkv,d] bfloat16 with H a multiple of Hkv")
+    cu = _cu(cu_seqlens, q.device)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = torch.empty_like(q) if out is None else out
+    l = torch.empty((H, T), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check(lib.fa_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(l), _ptr(cu), cu.numel() - 1, T,
+                             int(max_seqlen), H, Hkv, d, scale, int(bool(causal)), _stream(q)))
+    return o, l
+
+
+def backward_varlen(q, k, v, o, lse, dout, cu_seqlens, max_seqlen: int, causal: bool = False,
+                    scale: Optional[float] = None, workspace: Optional[torch.Tensor] = None):
+    """Backward of forward_varlen: dQ [total, H, d], dK, dV [total, Hkv, d]."""
+    lib = load_library()
+    _need_cuda(q, k, v, o, lse, dout)
+    T, H, d = q.shape
+    Hkv = k.shape[1]
+    cu = _cu(cu_seqlens, q.device)
+    batch = cu.numel() - 1
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    wsz = int(lib.fa_bwd_varlen_workspace_size(batch, int(max_seqlen), H, d))
+    ws = workspace
+    if ws is None or ws.numel() * ws.element_size() < wsz:
+        ws = torch.empty(wsz, dtype=torch.uint8, device=q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    _check(lib.fa_bwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
+                             _ptr(dv), _ptr(cu), batch, T, int(max_seqlen), H, Hkv, d, scale,
+                             int(bool(causal)), _ptr(ws), ws.numel() * ws.element_size(), _stream(q)))
+    return dq, dk, dv
 
 
 def backward(q, k, v, o, lse, dout, causal: bool = False, scale: Optional[float] = None,

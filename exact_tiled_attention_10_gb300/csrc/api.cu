@@ -94,6 +94,21 @@ fa_status make_map_3d(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, co
     return FA_OK;
 }
 
+// Token-major packed tensor [total, heads, d] (bf16): TMA dims (d, head, token),
+// boxes of 64 head-dim values x 1 head x box_rows consecutive tokens -- in
+// shared memory the same [box_rows][128 bytes] tile as the [B,H,N,d] maps give.
+fa_status make_map_tok(CUtensorMap* m, const void* base, int d, int heads, int total, int box_rows) {
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)total};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)heads * d * 2};
+    cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled (packed) failed (%d)", (int)r);
+    return FA_OK;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 fa_status check_common(int B, int H, int N, int d, float scale) {
@@ -387,6 +402,45 @@ fa_status fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float
                     nullptr, 0, stream, 1, nullptr, 0, Hkv);
 }
 
+fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens,
+                        int batch, int total, int max_seqlen, int H, int Hkv, int d, float scale, int causal,
+                        fa_stream_t stream) {
+    FA_TRY(check_common(batch, H, max_seqlen, d, scale));
+    if (total <= 0) return fail(FA_ERR_INVALID_ARG, "total must be positive");
+    if (Hkv < 1 || H % Hkv != 0) return fail(FA_ERR_INVALID_ARG, "H (%d) must be a multiple of Hkv (%d)", H, Hkv);
+    FA_CHECK_PTR(q);
+    FA_CHECK_PTR(k);
+    FA_CHECK_PTR(v);
+    FA_CHECK_PTR(o);
+    FA_CHECK_PTR(lse);
+    if (!cu_seqlens) return fail(FA_ERR_INVALID_ARG, "cu_seqlens must not be NULL");
+    DeviceInfo* dev = nullptr;
+    FA_TRY(device_info(&dev));
+    fa::FwdMaps m;
+    FA_TRY(make_map_tok(&m.q, q, d, H, total, 128));
+    FA_TRY(make_map_tok(&m.k, k, d, Hkv, total, 128));
+    FA_TRY(make_map_tok(&m.v, v, d, Hkv, total, 128));
+    m.q_lo = m.q;
+    m.k_lo = m.k;
+    fa::FwdParams p;
+    memset(&p, 0, sizeof(p));
+    p.B = batch; p.H = H; p.N = max_seqlen; p.Hkv = Hkv;
+    p.num_qp = (max_seqlen + 255) / 256;
+    p.num_items = batch * H * p.num_qp;
+    p.num_units = p.num_whole = p.num_items;
+    p.splits = 1;
+    p.scale = scale;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.o = o;
+    p.lse = lse;
+    p.cu_seqlens = cu_seqlens;
+    p.total = total;
+    p.err = dev->err_word;
+    cudaError_t e = fa::launch_fwd_varlen(d, causal != 0, m, p, grid_for_items(p.num_items, dev->sms), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "varlen forward launch");
+    return FA_OK;
+}
+
 size_t fa_fwd_workspace_size(fa_dtype dtype, int B, int H, int N, int d) {
     if (dtype != FA_F32 || B <= 0 || H <= 0 || N <= 0 || d <= 0) return 0;
     return 5 * round_up((size_t)B * H * N * d * 2, 256);
@@ -440,6 +494,21 @@ fa_status bwd_pre_impl(const BwdCtx& c, bool f32, const void* o, const float* ls
     return FA_OK;
 }
 
+// The float32 dQ accumulator [rows][d] as the target of the drain warps' tensor
+// reductions: d = 128: [64 queries][32 head-dim] boxes, plain; d = 64:
+// [32 queries][32 head-dim] boxes in the 128-byte swizzle they are staged in.
+fa_status make_map_dqacc(CUtensorMap* m, float* dqacc, int d, long long rows) {
+    cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)d * 4};
+    cuuint32_t box[2] = {32, (cuuint32_t)(d == 128 ? 64 : 32)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, dqacc, dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, d == 128 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled (dQ accumulator) failed (%d)", (int)r);
+    return FA_OK;
+}
+
 fa_status bwd_main_impl(const BwdCtx& c, bool f32, const void* qb, const void* kb, const void* vb, const void* gb,
                         void* dk, void* dv, int B, int H, int N, int d, float scale, int causal, const int* kv_lens,
                         cudaStream_t stream, int Hkv = 0) {
@@ -454,19 +523,7 @@ fa_status bwd_main_impl(const BwdCtx& c, bool f32, const void* qb, const void* k
     FA_TRY(make_map_3d(&tdo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, gb, d, N, BH, 64, BR, CU_TENSOR_MAP_SWIZZLE_128B));
     FA_TRY(make_map_3d(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kb, d, N, BHkv, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B));
     FA_TRY(make_map_3d(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, vb, d, N, BHkv, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B));
-    {
-        cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)BH * Np};
-        cuuint64_t strides[1] = {(cuuint64_t)d * 4};
-        // d = 128: [64 queries][32 head-dim] boxes, plain; d = 64: [32 queries][32 head-dim]
-        // boxes in the 128-byte swizzle the drain warps stage them in
-        cuuint32_t box[2] = {32, (cuuint32_t)(d == 128 ? 64 : 32)};
-        cuuint32_t estr[2] = {1, 1};
-        CUresult r = g_encode(&tdq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, dqacc, dims, strides, box, estr,
-                              CU_TENSOR_MAP_INTERLEAVE_NONE,
-                              d == 128 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
-                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-        if (r != CUDA_SUCCESS) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled (dQ accumulator) failed (%d)", (int)r);
-    }
+    FA_TRY(make_map_dqacc(&tdq, dqacc, d, (long long)BH * Np));
     fa::BwdParams p;
     memset(&p, 0, sizeof(p));
     p.B = B; p.H = H; p.N = N; p.Np = Np; p.Hkv = Hkv;
@@ -580,6 +637,73 @@ fa_status fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o,
     FA_TRY(bwd_pre_impl(c, false, o, lse, dout, N, d, stream));
     FA_TRY(bwd_main_impl(c, false, q, k, v, dout, dk, dv, B, H, N, d, scale, causal, kv_lens, stream, Hkv));
     return bwd_dq_impl(c, false, dq, N, d, scale, stream);
+}
+
+size_t fa_bwd_varlen_workspace_size(int batch, int max_seqlen, int H, int d) {
+    if (batch <= 0 || max_seqlen <= 0 || H <= 0 || (d != 64 && d != 128)) return 0;
+    const size_t R = (size_t)H * batch * round_up((size_t)max_seqlen, 128);
+    return 2 * round_up(R * 4, 256) + round_up(R * d * 4, 256);
+}
+
+fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                        const void* dout, void* dq, void* dk, void* dv, const int* cu_seqlens, int batch, int total,
+                        int max_seqlen, int H, int Hkv, int d, float scale, int causal, void* workspace,
+                        size_t workspace_bytes, fa_stream_t stream) {
+    FA_TRY(check_common(batch, H, max_seqlen, d, scale));
+    if (total <= 0) return fail(FA_ERR_INVALID_ARG, "total must be positive");
+    if (Hkv < 1 || H % Hkv != 0) return fail(FA_ERR_INVALID_ARG, "H (%d) must be a multiple of Hkv (%d)", H, Hkv);
+    FA_CHECK_PTR(q);
+    FA_CHECK_PTR(k);
+    FA_CHECK_PTR(v);
+    FA_CHECK_PTR(o);
+    FA_CHECK_PTR(lse);
+    FA_CHECK_PTR(dout);
+    FA_CHECK_PTR(dq);
+    FA_CHECK_PTR(dk);
+    FA_CHECK_PTR(dv);
+    FA_CHECK_PTR(workspace);
+    if (!cu_seqlens) return fail(FA_ERR_INVALID_ARG, "cu_seqlens must not be NULL");
+    const size_t need = fa_bwd_varlen_workspace_size(batch, max_seqlen, H, d);
+    if (workspace_bytes < need) return fail(FA_ERR_INVALID_ARG, "workspace too small (%zu < %zu bytes)", workspace_bytes, need);
+    DeviceInfo* dev = nullptr;
+    FA_TRY(device_info(&dev));
+    const int MSp = (int)round_up((size_t)max_seqlen, 128);
+    const size_t R = (size_t)H * batch * MSp;
+    char* ws = reinterpret_cast<char*>(workspace);
+    float* lse2 = reinterpret_cast<float*>(ws);
+    float* dvec = reinterpret_cast<float*>(ws + round_up(R * 4, 256));
+    float* dqacc = reinterpret_cast<float*>(ws + 2 * round_up(R * 4, 256));
+    cudaError_t e = fa::launch_bwd_pre_varlen(o, dout, lse, cu_seqlens, lse2, dvec, dqacc, H, batch, total, max_seqlen,
+                                              MSp, d, bw_grid(dev), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "varlen preprocess launch");
+    const int BR = (d == 128) ? 64 : 128;
+    CUtensorMap tq, tk, tv, tdo, tdq;
+    FA_TRY(make_map_tok(&tq, q, d, H, total, BR));
+    FA_TRY(make_map_tok(&tdo, dout, d, H, total, BR));
+    FA_TRY(make_map_tok(&tk, k, d, Hkv, total, 128));
+    FA_TRY(make_map_tok(&tv, v, d, Hkv, total, 128));
+    FA_TRY(make_map_dqacc(&tdq, dqacc, d, (long long)R));
+    fa::BwdParams p;
+    memset(&p, 0, sizeof(p));
+    p.B = batch; p.H = H; p.N = max_seqlen; p.Np = MSp; p.Hkv = Hkv;
+    p.num_kt = (max_seqlen + 127) / 128;
+    p.num_items = batch * Hkv * p.num_kt;
+    p.scale = scale;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.lse2 = lse2;
+    p.dvec = dvec;
+    p.dq_acc = dqacc;
+    p.dk = dk;
+    p.dv = dv;
+    p.cu_seqlens = cu_seqlens;
+    p.total = total;
+    p.err = dev->err_word;
+    e = fa::launch_bwd_main_varlen(d, causal != 0, tq, tk, tv, tdo, tdq, p, grid_for_items(p.num_items, dev->sms),
+                                   stream);
+    if (e != cudaSuccess) return cuda_fail(e, "varlen backward launch");
+    e = fa::launch_bwd_dq_varlen(dqacc, cu_seqlens, dq, scale, H, batch, max_seqlen, MSp, d, bw_grid(dev), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "varlen dQ conversion launch");
+    return FA_OK;
 }
 
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,

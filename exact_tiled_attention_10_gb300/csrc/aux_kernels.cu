@@ -110,6 +110,89 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ a
     }
 }
 
+// Packed variable-length sequences: the statistics and the dQ accumulator are
+// laid out per (head, sequence) as [H][batch][MSp] rows (MSp = max_seqlen
+// rounded up to 128), so that every query block of every sequence starts on
+// an aligned row and padding rows (position >= the sequence's length) carry
+// LSE*log2(e) = +inf, D = 0 (their P is 0 in the backward).  Row r = (h *
+// batch + b) * MSp + pos reads token cu_seqlens[b] + pos of O, dO [total, H, d].
+__device__ __forceinline__ int varlen_len(const int* cu, int b, int max_seqlen) {
+    return max(0, min(__ldg(cu + b + 1) - __ldg(cu + b), max_seqlen));
+}
+
+template <int D>
+__global__ void __launch_bounds__(256) bwd_pre_varlen_kernel(const __nv_bfloat16* __restrict__ o,
+                                                             const __nv_bfloat16* __restrict__ dout,
+                                                             const float* __restrict__ lse, const int* __restrict__ cu,
+                                                             float* __restrict__ lse2, float* __restrict__ dvec,
+                                                             float* __restrict__ dq_acc, int H, int batch, int total,
+                                                             int max_seqlen, int MSp) {
+    constexpr int LPR = D / 8;     // lanes per row
+    constexpr int RPW = 32 / LPR;  // rows per warp
+    const int lane = threadIdx.x & 31;
+    const int sub = lane / LPR, sl = lane % LPR;
+    const long total_rows = (long)H * batch * MSp;
+    const long warps = (long)gridDim.x * (blockDim.x / 32);
+    const long gw = (long)blockIdx.x * (blockDim.x / 32) + (threadIdx.x / 32);
+    for (long r0 = gw * RPW; r0 < total_rows; r0 += warps * RPW) {
+        const long r = r0 + sub;
+        const bool valid_row = r < total_rows;
+        const long hb = valid_row ? r / MSp : 0;
+        const int pos = valid_row ? (int)(r - hb * MSp) : 0;
+        const int h = (int)(hb / batch), b = (int)(hb - (long)h * batch);
+        const bool real = valid_row && pos < varlen_len(cu, b, max_seqlen);
+        const long token = real ? (long)__ldg(cu + b) + pos : 0;
+        float acc = 0.f;
+        if (real) {
+            const size_t e = ((size_t)token * H + h) * D + sl * 8;
+            float a[8], g[8];
+            unpack8(__ldg(reinterpret_cast<const uint4*>(o + e)), a);
+            unpack8(__ldg(reinterpret_cast<const uint4*>(dout + e)), g);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) acc = fmaf(a[k], g[k], acc);
+        }
+#pragma unroll
+        for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (valid_row) {
+            float* qa = dq_acc + (size_t)r * D + sl * 8;
+            reinterpret_cast<float4*>(qa)[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+            reinterpret_cast<float4*>(qa)[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (sl == 0) {
+                float l2 = INFINITY;
+                if (real) {
+                    const float L = lse[(size_t)h * total + token];
+                    l2 = (L == -INFINITY) ? INFINITY : L * 1.4426950408889634f;
+                }
+                lse2[r] = l2;
+                dvec[r] = real ? acc : 0.f;
+            }
+        }
+    }
+}
+
+// dQ[token, h, :] = scale * dQ_acc[(h * batch + b) * MSp + pos, :] for the real rows.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_dq_varlen_kernel(const float* __restrict__ acc, const int* __restrict__ cu,
+                                                            __nv_bfloat16* __restrict__ dq, float scale, int H,
+                                                            int batch, int max_seqlen, int MSp) {
+    constexpr int G = D / 8;  // 8-element groups per row
+    const long total = (long)H * batch * MSp * G;
+    for (long g = (long)blockIdx.x * blockDim.x + threadIdx.x; g < total; g += (long)gridDim.x * blockDim.x) {
+        const long r = g / G;
+        const int c = (int)(g - r * G) * 8;
+        const long hb = r / MSp;
+        const int pos = (int)(r - hb * MSp);
+        const int h = (int)(hb / batch), b = (int)(hb - (long)h * batch);
+        if (pos >= varlen_len(cu, b, max_seqlen)) continue;
+        const long token = (long)__ldg(cu + b) + pos;
+        const float4* src = reinterpret_cast<const float4*>(acc + (size_t)r * D + c);
+        const float4 x = __ldg(src), y = __ldg(src + 1);
+        *reinterpret_cast<uint4*>(dq + ((size_t)token * H + h) * D + c) =
+            make_uint4(pack_bf16x2(x.x * scale, x.y * scale), pack_bf16x2(x.z * scale, x.w * scale),
+                       pack_bf16x2(y.x * scale, y.y * scale), pack_bf16x2(y.z * scale, y.w * scale));
+    }
+}
+
 // One CTA (256 threads) per (head, 64-row block); d = 128 -> 8192 elements,
 // 32 per thread.  s = amax / 448 and x / s are IEEE float32 divisions; the
 // conversion rounds to nearest even and saturates to +-448.
@@ -271,6 +354,30 @@ cudaError_t launch_lse_merge(const float* o_part, const float* lse_part, int num
     else
         lse_merge_kernel<64><<<grid, 256, 0, stream>>>(o_part, lse_part, num_whole, num_tail, splits, causal, BH,
                                                        num_qp, N, ob, lse);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_pre_varlen(const void* o, const void* dout, const float* lse, const int* cu, float* lse2,
+                                  float* dvec, float* dq_acc, int H, int batch, int total, int max_seqlen, int MSp,
+                                  int d, int grid, cudaStream_t s) {
+    const __nv_bfloat16* ob = reinterpret_cast<const __nv_bfloat16*>(o);
+    const __nv_bfloat16* gb = reinterpret_cast<const __nv_bfloat16*>(dout);
+    if (d == 128)
+        bwd_pre_varlen_kernel<128><<<grid, 256, 0, s>>>(ob, gb, lse, cu, lse2, dvec, dq_acc, H, batch, total,
+                                                        max_seqlen, MSp);
+    else
+        bwd_pre_varlen_kernel<64><<<grid, 256, 0, s>>>(ob, gb, lse, cu, lse2, dvec, dq_acc, H, batch, total,
+                                                       max_seqlen, MSp);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dq_varlen(const float* acc, const int* cu, void* dq, float scale, int H, int batch,
+                                 int max_seqlen, int MSp, int d, int grid, cudaStream_t s) {
+    __nv_bfloat16* q = reinterpret_cast<__nv_bfloat16*>(dq);
+    if (d == 128)
+        bwd_dq_varlen_kernel<128><<<grid, 256, 0, s>>>(acc, cu, q, scale, H, batch, max_seqlen, MSp);
+    else
+        bwd_dq_varlen_kernel<64><<<grid, 256, 0, s>>>(acc, cu, q, scale, H, batch, max_seqlen, MSp);
     return cudaGetLastError();
 }
 

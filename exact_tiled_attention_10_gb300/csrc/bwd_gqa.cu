@@ -1,4 +1,5 @@
-// Backward kernel instances for shared key/value heads (bf16 gradients).
+// Backward kernel instances for shared key/value heads and for packed
+// variable-length sequences (bf16 gradients).
 #include "bwd_kernel.cuh"
 
 namespace fa {
@@ -13,6 +14,18 @@ cudaError_t launch_bwd_main_gqa(int d, bool causal, const CUtensorMap& tq, const
                       : bwd::launch<C128, false, false, true>(tq, tk, tv, tdo, tdq, p, grid, s);
     return causal ? bwd::launch<C64, true, false, true>(tq, tk, tv, tdo, tdq, p, grid, s)
                   : bwd::launch<C64, false, false, true>(tq, tk, tv, tdo, tdq, p, grid, s);
+}
+
+cudaError_t launch_bwd_main_varlen(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
+                                   const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
+                                   const BwdParams& p, int grid, cudaStream_t s) {
+    using C128 = bwd::Cfg<128>;
+    using C64 = bwd::Cfg<64>;
+    if (d == 128)
+        return causal ? bwd::launch<C128, true, false, true, true>(tq, tk, tv, tdo, tdq, p, grid, s)
+                      : bwd::launch<C128, false, false, true, true>(tq, tk, tv, tdo, tdq, p, grid, s);
+    return causal ? bwd::launch<C64, true, false, true, true>(tq, tk, tv, tdo, tdq, p, grid, s)
+                  : bwd::launch<C64, false, false, true, true>(tq, tk, tv, tdo, tdq, p, grid, s);
 }
 
 }  // namespace fa

@@ -104,11 +104,15 @@ struct Cfg {
 struct Item {
     int bh, b, kt, kvl, i0, n;
     int qh0, ni;  // first query head row (b * H + ...), query blocks per query head
+    int kvh, tb, seqlen;  // packed sequences: key/value head in the sequence, first token, length
 };
 
 // GQA: the kernel instance for shared key/value heads (compiled separately so
 // that the plain backward carries none of the group bookkeeping).
-template <class C, bool CAUSAL, bool GQA>
+// VARLEN (packed variable-length sequences, always with the GQA step loop):
+// qh0 / the step's bhq are head indices within the sequence, the K, V, dK, dV
+// rows are tokens tb + key, and the statistics rows are (h * B + b) * Np + ...
+template <class C, bool CAUSAL, bool GQA, bool VARLEN = false>
 __device__ __forceinline__ Item get_item(int it, const BwdParams& p) {
     Item I;
     const int Hkv = GQA ? p.Hkv : p.H;
@@ -122,12 +126,20 @@ __device__ __forceinline__ Item get_item(int it, const BwdParams& p) {
     }
     I.b = I.bh / Hkv;
     const int group = GQA ? p.H / Hkv : 1;
-    I.qh0 = GQA ? I.b * p.H + (I.bh - I.b * Hkv) * group : I.bh;
-    int kvl = p.N;
-    if (p.kv_lens) kvl = min(max(__ldg(p.kv_lens + I.b), 0), p.N);
+    I.kvh = I.bh - I.b * Hkv;
+    I.qh0 = VARLEN ? I.kvh * group : GQA ? I.b * p.H + I.kvh * group : I.bh;
+    I.tb = 0;
+    I.seqlen = p.N;
+    if (VARLEN) {
+        const int a = __ldg(p.cu_seqlens + I.b), e = __ldg(p.cu_seqlens + I.b + 1);
+        I.tb = a;
+        I.seqlen = max(0, min(e - a, p.N));
+    }
+    int kvl = I.seqlen;
+    if (!VARLEN && p.kv_lens) kvl = min(max(__ldg(p.kv_lens + I.b), 0), p.N);
     I.kvl = kvl;
     const int key0 = I.kt * C::BC;
-    const int iend = (p.N + C::BR - 1) / C::BR;
+    const int iend = ((VARLEN ? I.seqlen : p.N) + C::BR - 1) / C::BR;
     I.i0 = CAUSAL ? key0 / C::BR : 0;
     I.ni = (key0 >= kvl) ? 0 : max(iend - I.i0, 0);
     I.n = I.ni * group;
@@ -214,7 +226,7 @@ __device__ __forceinline__ void mma_dq(uint32_t d_tmem, uint64_t k_mn, uint64_t 
     }
 }
 
-template <class C, bool CAUSAL, bool OUT_F32, bool GQA>
+template <class C, bool CAUSAL, bool OUT_F32, bool GQA, bool VARLEN = false>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
@@ -273,15 +285,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int rd = 0; rd < snake_rounds(p.num_items) && ok; ++rd) {
             const int it = snake_item(rd, p.num_items);
             if (it < 0) continue;
-            const Item I = get_item<C, CAUSAL, GQA>(it, p);
+            const Item I = get_item<C, CAUSAL, GQA, VARLEN>(it, p);
             if (I.n == 0) continue;
             if (!(ok = wait_bounded_warp(BAR(C::B_KVEMPTY), kve ^ 1, abort_flag, p.err, kErrWaitBwdProducer))) break;
             kve ^= 1;
             if (lane == 0) {
                 mbar_arrive_expect_tx(BAR(C::B_KVFULL), 2 * C::K_TILE);
                 for (int bx = 0; bx < C::NBOX; ++bx) {
-                    tma_load_3d(sbase + C::OFF_K + bx * C::K_BOX, &tk, BAR(C::B_KVFULL), bx * 64, I.kt * C::BC, I.bh);
-                    tma_load_3d(sbase + C::OFF_V + bx * C::K_BOX, &tv, BAR(C::B_KVFULL), bx * 64, I.kt * C::BC, I.bh);
+                    const int c1 = VARLEN ? I.kvh : I.kt * C::BC, c2 = VARLEN ? I.tb + I.kt * C::BC : I.bh;
+                    tma_load_3d(sbase + C::OFF_K + bx * C::K_BOX, &tk, BAR(C::B_KVFULL), bx * 64, c1, c2);
+                    tma_load_3d(sbase + C::OFF_V + bx * C::K_BOX, &tv, BAR(C::B_KVFULL), bx * 64, c1, c2);
                 }
             }
             __syncwarp();
@@ -292,10 +305,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t bar = BAR(C::B_QFULL + st);
                     mbar_arrive_expect_tx(bar, 2 * C::Q_TILE + C::STAT_BYTES);
                     for (int bx = 0; bx < C::NBOX; ++bx) {
-                        tma_load_3d(sbase + C::OFF_Q + st * C::Q_TILE + bx * C::Q_BOX, &tq, bar, bx * 64, i * C::BR, bhq);
-                        tma_load_3d(sbase + C::OFF_DO + st * C::Q_TILE + bx * C::Q_BOX, &tdo, bar, bx * 64, i * C::BR, bhq);
+                        const int c1 = VARLEN ? bhq : i * C::BR, c2 = VARLEN ? I.tb + i * C::BR : bhq;
+                        tma_load_3d(sbase + C::OFF_Q + st * C::Q_TILE + bx * C::Q_BOX, &tq, bar, bx * 64, c1, c2);
+                        tma_load_3d(sbase + C::OFF_DO + st * C::Q_TILE + bx * C::Q_BOX, &tdo, bar, bx * 64, c1, c2);
                     }
-                    const size_t roff = (size_t)bhq * p.Np + (size_t)i * C::BR;
+                    const size_t roff = (size_t)(VARLEN ? bhq * p.B + I.b : bhq) * p.Np + (size_t)i * C::BR;
                     bulk_load(sbase + C::OFF_STAT + st * C::STAT_BYTES, p.lse2 + roff, C::BR * 4, bar);
                     bulk_load(sbase + C::OFF_STAT + st * C::STAT_BYTES + C::BR * 4, p.dvec + roff, C::BR * 4, bar);
                 }
@@ -347,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int rd = 0; rd < snake_rounds(p.num_items) && ok; ++rd) {
             const int it = snake_item(rd, p.num_items);
             if (it < 0) continue;
-            const Item I = get_item<C, CAUSAL, GQA>(it, p);
+            const Item I = get_item<C, CAUSAL, GQA, VARLEN>(it, p);
             if (I.n == 0) continue;
             if (!(ok = wait_bounded_warp(BAR(C::B_KVFULL), kvph, abort_flag, p.err, kErrWaitBwdMma))) break;
             kvph ^= 1;
@@ -408,11 +422,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int rd = 0; rd < snake_rounds(p.num_items) && ok; ++rd) {
             const int it = snake_item(rd, p.num_items);
             if (it < 0) continue;
-            const Item I = get_item<C, CAUSAL, GQA>(it, p);
+            const Item I = get_item<C, CAUSAL, GQA, VARLEN>(it, p);
             const int key = I.kt * C::BC + kr;
-            const size_t krow = (size_t)I.bh * p.N + key;
-            if (I.n == 0) {  // key block entirely beyond kv_len: zero gradients
-                if (key < p.N) {
+            // dK, dV row: [B,Hkv,N,d], or token-major [total, Hkv, d] for packed sequences
+            const size_t krow = VARLEN ? (size_t)(I.tb + key) * p.Hkv + I.kvh : (size_t)I.bh * p.N + key;
+            if (I.n == 0) {  // key block entirely beyond kv_len: zero gradients (packed: nothing to write)
+                if (!VARLEN && key < p.N) {
                     float z[32];
 #pragma unroll
                     for (int e = 0; e < 32; ++e) z[e] = 0.f;
@@ -531,7 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float f[32];
 #pragma unroll
                 for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(a[e]) * mul;
-                if (key < p.N) store_chunk32<OUT_F32>(dst, krow * C::D + c, f);
+                if (key < (VARLEN ? I.seqlen : p.N)) store_chunk32<OUT_F32>(dst, krow * C::D + c, f);
             }
             tc_fence_before();
             mbar_arrive(BAR(C::B_ACCEMPTY));
@@ -547,7 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int rd = 0; rd < snake_rounds(p.num_items) && ok; ++rd) {
             const int it = snake_item(rd, p.num_items);
             if (it < 0) continue;
-            const Item I = get_item<C, CAUSAL, GQA>(it, p);
+            const Item I = get_item<C, CAUSAL, GQA, VARLEN>(it, p);
             int bhq = I.qh0, i = I.i0;
             for (int s = 0; s < I.n; ++s, step_next<GQA>(I, bhq, i)) {
                 const int dqs = C::DQ_ALIAS ? (s % C::NSLOT) : 0;
@@ -584,10 +599,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) {
                     if constexpr (C::D == 128) {
-                        tma_reduce_add_2d(&tdq, stage, wq * 32, bhq * p.Np + i * C::BR);
+                        tma_reduce_add_2d(&tdq, stage, wq * 32, (VARLEN ? bhq * p.B + I.b : bhq) * p.Np + i * C::BR);
                     } else {
-                        tma_reduce_add_2d(&tdq, stage, 0, bhq * p.Np + i * C::BR + wq * 32);
-                        tma_reduce_add_2d(&tdq, stage + 4096, 32, bhq * p.Np + i * C::BR + wq * 32);
+                        const int qrow = (VARLEN ? bhq * p.B + I.b : bhq) * p.Np + i * C::BR + wq * 32;
+                        tma_reduce_add_2d(&tdq, stage, 0, qrow);
+                        tma_reduce_add_2d(&tdq, stage + 4096, 32, qrow);
                     }
                     bulk_commit_group();
                 }
@@ -606,11 +622,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <class C, bool CAUSAL, bool OUT_F32, bool GQA = false>
+template <class C, bool CAUSAL, bool OUT_F32, bool GQA = false, bool VARLEN = false>
 cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                    const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p, int grid,
                    cudaStream_t stream) {
-    auto kern = bwd_kernel<C, CAUSAL, OUT_F32, GQA>;
+    auto kern = bwd_kernel<C, CAUSAL, OUT_F32, GQA, VARLEN>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     kern<<<grid, kThreads, C::SMEM, stream>>>(tq, tk, tv, tdo, tdq, p);

@@ -64,13 +64,25 @@ struct FwdParams {
     float* lse_part;  // [partials][256 rows]
     float scale;      // softmax scale applied to Q K^T
     float scale_log2; // scale * log2(e)
-    const int* kv_lens;
+    // Packed variable-length sequences (VARLEN instance): sequence b holds
+    // tokens cu_seqlens[b] .. cu_seqlens[b+1]-1; q, o are [total, H, d], k, v
+    // [total, Hkv, d], lse [H, total]; B is the number of sequences and N the
+    // longest length.  They share storage with fields that instance does not
+    // read, so that the struct keeps its size: a larger parameter block had
+    // slowed the other forward instances by several percent.
+    union {
+        const int* kv_lens;     // [B] valid keys per batch item, or NULL
+        const int* cu_seqlens;  // [B + 1] (VARLEN)
+    };
     void* o;          // [B,H,N,d] bf16 or f32
     float* lse;       // [B,H,N]
     const float* sq;  // FP8 only: per-64-row-block scales [B,H,nblk]
     const float* sk;
     const float* sv;
-    int nblk;         // ceil(N / 64)
+    union {
+        int nblk;     // ceil(N / 64) (FP8)
+        int total;    // packed tokens (VARLEN)
+    };
     unsigned int* err;
 };
 
@@ -85,8 +97,12 @@ struct BwdParams {
     const float* lse2;  // [B,H,Np] LSE * log2(e), +inf on rows with no visible key / padding
     const float* dvec;  // [B,H,Np] D = rowsum(dO * O)
     float* dq_acc;      // [B,H,Np,d] float32 accumulator (unscaled)
-    void* dk;           // [B,H,N,d]
+    void* dk;           // [B,Hkv,N,d]
     void* dv;
+    // packed variable-length sequences (see FwdParams): B sequences, N the
+    // longest; statistics and dQ accumulator rows (h * B + b) * Np + position
+    const int* cu_seqlens;
+    int total;
     unsigned int* err;
 };
 
@@ -101,10 +117,15 @@ cudaError_t launch_fwd_bf16_d64(int block_c, bool causal, bool out_f32, bool spl
                                 const FwdParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_fwd_bf16_d128(int block_c, bool causal, bool out_f32, bool split, const FwdMaps& m,
                                  const FwdParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_fwd_varlen(int d, bool causal, const FwdMaps& m, const FwdParams& p, int grid,
+                              cudaStream_t stream);
 cudaError_t launch_fwd_splitk(int d, bool fp8, bool causal, const FwdMaps& m, const FwdParams& p, int grid,
                               cudaStream_t stream);
 cudaError_t launch_fwd_fp8_d128(bool causal, const FwdMaps& m, const FwdParams& p, int grid,
                                 cudaStream_t stream);
+cudaError_t launch_bwd_main_varlen(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
+                                   const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
+                                   const BwdParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_bwd_main_gqa(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
                                 const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
                                 const BwdParams& p, int grid, cudaStream_t stream);
@@ -122,6 +143,11 @@ cudaError_t launch_quantize_fp8(const void* x, void* x8, float* scales, int BH, 
 // Merges the split-key partials of the forward into O (bf16) and LSE.
 cudaError_t launch_lse_merge(const float* o_part, const float* lse_part, int num_whole, int num_tail, int splits,
                              bool causal, int BH, int num_qp, int N, int d, void* o, float* lse, cudaStream_t stream);
+cudaError_t launch_bwd_pre_varlen(const void* o, const void* dout, const float* lse, const int* cu, float* lse2,
+                                  float* dvec, float* dq_acc, int H, int batch, int total, int max_seqlen, int MSp,
+                                  int d, int grid, cudaStream_t stream);
+cudaError_t launch_bwd_dq_varlen(const float* acc, const int* cu, void* dq, float scale, int H, int batch,
+                                 int max_seqlen, int MSp, int d, int grid, cudaStream_t stream);
 cudaError_t launch_wait_selftest(unsigned int* err, unsigned int limit_us, int* waited_out,
                                  cudaStream_t stream);
 cudaError_t launch_f32_to_bf16(const float* x, void* y, size_t n, int grid, cudaStream_t stream);

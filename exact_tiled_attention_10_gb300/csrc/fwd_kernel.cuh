@@ -30,6 +30,8 @@
 //   FP8 variant: Q8 K8 with per-64-row block scales s_q, s_k folded into the
 //   softmax multiplier, V's per-block scale folded into the E4M3 P operand.
 #pragma once
+#include <type_traits>
+
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -136,11 +138,69 @@ struct Item {
     int part;   // partial index of a split unit, -1 for a whole item
 };
 
+// Packed variable-length sequences add the head within the sequence and the
+// sequence's first token and length.  (A separate type keeps the item of the
+// [B, H, N, d] instances at its size: the item lives in local memory there,
+// and three more fields cost several percent.)
+struct ItemPacked : Item {
+    int h, tb, seqlen;
+};
+
+template <bool VARLEN>
+using ItemT = typename std::conditional<VARLEN, ItemPacked, Item>::type;
+
+template <class IT>
+__host__ __device__ constexpr bool is_packed() { return std::is_same<IT, ItemPacked>::value; }
+
+// Key blocks of tile t.  The packed instance reads the field with constant
+// indices (its larger item otherwise went to local memory); the others index
+// directly, which schedules better.
+template <class IT>
+__device__ __forceinline__ int item_n(const IT& I, int t) {
+    if constexpr (is_packed<IT>()) return t ? I.n[1] : I.n[0];
+    else return I.n[t];
+}
+
+// Query rows of the item's sequence.
+template <class IT>
+__device__ __forceinline__ int item_rows(const IT& I, const FwdParams& p) {
+    if constexpr (is_packed<IT>()) return I.seqlen;
+    else return p.N;
+}
+
+// TMA coordinates (y, z) of query row r: maps [B*H][N][d], or token-major
+// [total][H][d] for packed sequences.
+template <class IT>
+__device__ __forceinline__ void q_coords(const IT& I, int r, int& y, int& z) {
+    if constexpr (is_packed<IT>()) { y = I.h; z = I.tb + r; }
+    else { y = r; z = I.bh; }
+}
+
+// TMA coordinates of key / value row r.
+template <class IT>
+__device__ __forceinline__ void kv_coords(const IT& I, int r, const FwdParams& p, int& y, int& z) {
+    if constexpr (is_packed<IT>()) { y = I.h / (p.H / p.Hkv); z = I.tb + r; }
+    else { y = r; z = I.kvh; }
+}
+
+// Row index of output row `row` (O has d elements per row) and of its LSE.
+template <class IT>
+__device__ __forceinline__ size_t out_row(const IT& I, int row, const FwdParams& p) {
+    if constexpr (is_packed<IT>()) return (size_t)(I.tb + row) * p.H + I.h;
+    else return (size_t)I.bh * p.N + row;
+}
+template <class IT>
+__device__ __forceinline__ size_t lse_index(const IT& I, int row, const FwdParams& p) {
+    if constexpr (is_packed<IT>()) return (size_t)I.h * p.total + I.tb + row;
+    else return (size_t)I.bh * p.N + row;
+}
+
 // SPLITK: the kernel instance that also runs split-key units (compiled
 // separately so that the plain forward carries none of their bookkeeping).
-template <class C, bool CAUSAL, bool SPLITK>
-__device__ __forceinline__ Item get_item(int unit, const FwdParams& p) {
-    Item I;
+// VARLEN: the instance for packed variable-length sequences.
+template <class C, bool CAUSAL, bool SPLITK, bool VARLEN>
+__device__ __forceinline__ ItemT<VARLEN> get_item(int unit, const FwdParams& p) {
+    ItemT<VARLEN> I;
     const int BH = p.B * p.H;
     int it = unit, s = 0, S = 1;
     I.part = -1;
@@ -154,9 +214,19 @@ __device__ __forceinline__ Item get_item(int unit, const FwdParams& p) {
     int qp;
     fwd_item_coords(it, CAUSAL, BH, p.num_qp, I.bh, qp);
     I.b = I.bh / p.H;
-    I.kvh = I.b * p.Hkv + (I.bh - I.b * p.H) / (p.H / p.Hkv);
-    int kvl = p.N;
-    if (p.kv_lens) kvl = min(max(__ldg(p.kv_lens + I.b), 0), p.N);
+    const int h = I.bh - I.b * p.H;
+    I.kvh = I.b * p.Hkv + h / (p.H / p.Hkv);
+    int kvl, rows;
+    if constexpr (VARLEN) {
+        const int a = __ldg(p.cu_seqlens + I.b), e = __ldg(p.cu_seqlens + I.b + 1);
+        I.h = h;
+        I.tb = a;
+        I.seqlen = max(0, min(e - a, p.N));
+        kvl = rows = I.seqlen;
+    } else {
+        kvl = rows = p.N;
+        if (p.kv_lens) kvl = min(max(__ldg(p.kv_lens + I.b), 0), p.N);
+    }
     I.kvl = kvl;
     I.row0 = qp * (C::QT * C::BR);
     I.nmax = 0;
@@ -164,7 +234,7 @@ __device__ __forceinline__ Item get_item(int unit, const FwdParams& p) {
     for (int t = 0; t < 2; ++t) {
         const int r0 = I.row0 + t * C::BR;
         int n = 0;
-        if (r0 < p.N) {
+        if (r0 < rows) {
             int cols = kvl;
             if (CAUSAL) cols = min(cols, r0 + C::BR);
             n = (cols + C::BC - 1) / C::BC;
@@ -298,7 +368,7 @@ __device__ __forceinline__ void store_row_chunk(void* o_row, int c0, const float
     }
 }
 
-template <class C, bool CAUSAL, bool OUT_F32, bool SPLITK>
+template <class C, bool CAUSAL, bool OUT_F32, bool SPLITK, bool VARLEN = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tql,
@@ -366,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int rd = 0; rd < snake_rounds(p.num_units) && ok; ++rd) {
             const int it = snake_item(rd, p.num_units);
             if (it < 0) continue;
-            const Item I = get_item<C, CAUSAL, SPLITK>(it, p);
+            const auto I = get_item<C, CAUSAL, SPLITK, VARLEN>(it, p);
             if (I.nmax == 0) continue;
             // Q tile t of this item may load as soon as the previous item's last
             // S_t MMA has consumed the buffer (per-tile barriers), overlapping
@@ -374,12 +444,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int t = 0; t < C::QT && ok; ++t) {
                 if (!(ok = wait_bounded_warp(BAR(C::B_QEMPTY + t), qe ^ 1, abort_flag, p.err, kErrWaitFwdProducer))) break;
                 if (lane == 0) {
+                    int y, z;
+                    q_coords(I, I.row0 + t * C::BR, y, z);
                     mbar_arrive_expect_tx(BAR(C::B_QFULL + t), C::NPART * C::Q_TILE);
                     for (int part = 0; part < C::NPART; ++part)
                         for (int bx = 0; bx < C::NBOX; ++bx)
                             tma_load_3d(sbase + C::OFF_Q + (part * C::QT + t) * C::Q_TILE + bx * C::Q_BOX,
-                                        part ? &tql : &tq, BAR(C::B_QFULL + t), bx * C::BOX_ELEMS,
-                                        I.row0 + t * C::BR, I.bh);
+                                        part ? &tql : &tq, BAR(C::B_QFULL + t), bx * C::BOX_ELEMS, y, z);
                 }
                 __syncwarp();
             }
@@ -391,12 +462,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (idx < I.nmax) {
                     if (!(ok = wait_bounded_warp(BAR(C::B_KEMPTY + kst), kph ^ 1, abort_flag, p.err, kErrWaitFwdProducer))) break;
                     if (lane == 0) {
+                        int y, z;
+                        kv_coords(I, (I.j0 + idx) * C::BC, p, y, z);
                         mbar_arrive_expect_tx(BAR(C::B_KFULL + kst), C::K_STAGE);
                         for (int part = 0; part < C::NPART; ++part)
                             for (int bx = 0; bx < C::NBOX; ++bx)
                                 tma_load_3d(sbase + C::OFF_K + kst * C::K_STAGE + part * C::KV_TILE + bx * C::KV_BOX,
-                                            part ? &tkl : &tk, BAR(C::B_KFULL + kst), bx * C::BOX_ELEMS,
-                                            (I.j0 + idx) * C::BC, I.kvh);
+                                            part ? &tkl : &tk, BAR(C::B_KFULL + kst), bx * C::BOX_ELEMS, y, z);
                     }
                     __syncwarp();
                     if (++kst == C::KSTAGES) { kst = 0; kph ^= 1; }
@@ -405,10 +477,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int j = idx - 1;
                     if (!(ok = wait_bounded_warp(BAR(C::B_VEMPTY + vst), vph ^ 1, abort_flag, p.err, kErrWaitFwdProducer))) break;
                     if (lane == 0) {
+                        int y, z;
+                        kv_coords(I, (I.j0 + j) * C::BC, p, y, z);
                         mbar_arrive_expect_tx(BAR(C::B_VFULL + vst), C::KV_TILE);
                         for (int bx = 0; bx < C::NBOX; ++bx)
                             tma_load_3d(sbase + C::OFF_V + vst * C::KV_TILE + bx * C::KV_BOX, &tv, BAR(C::B_VFULL + vst),
-                                        bx * C::BOX_ELEMS, (I.j0 + j) * C::BC, I.kvh);
+                                        bx * C::BOX_ELEMS, y, z);
                     }
                     __syncwarp();
                     if (++vst == C::VSTAGES) { vst = 0; vph ^= 1; }
@@ -435,7 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int rd = 0; rd < snake_rounds(p.num_units) && ok; ++rd) {
             const int it = snake_item(rd, p.num_units);
             if (it < 0) continue;
-            const Item I = get_item<C, CAUSAL, SPLITK>(it, p);
+            const auto I = get_item<C, CAUSAL, SPLITK, VARLEN>(it, p);
             if (I.nmax == 0) continue;
             for (int t = 0; t < 2 && ok; ++t)
                 ok = wait_bounded_warp(BAR(C::B_QFULL + t), qph, abort_flag, p.err, kErrWaitFwdMma);
@@ -444,18 +518,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(ok = wait_bounded_warp(BAR(C::B_KFULL + kst), kph, abort_flag, p.err, kErrWaitFwdMma))) break;
             tc_fence_after();
             for (int t = 0; t < 2; ++t) {
-                if (I.n[t] > 0) {
+                if (item_n(I, t) > 0) {
                     issue_S<C>(tS(t), q_desc(t), k_desc(kst));
                     mma_commit_w(BAR(C::B_SFULL + t));
                 }
-                if (I.n[t] <= 1) mma_commit_w(BAR(C::B_QEMPTY + t));  // Q_t no longer needed
+                if (item_n(I, t) <= 1) mma_commit_w(BAR(C::B_QEMPTY + t));  // Q_t no longer needed
             }
             mma_commit_w(BAR(C::B_KEMPTY + kst));
             if (++kst == C::KSTAGES) { kst = 0; kph ^= 1; }
             for (int j = 0; j < I.nmax && ok; ++j) {
                 bool vw = false, kw = false;
                 for (int t = 0; t < 2; ++t) {
-                    if (j >= I.n[t]) continue;
+                    if (j >= item_n(I, t)) continue;
                     if (!(ok = wait_bounded_warp(BAR(C::B_PFULL + t), pph[t], abort_flag, p.err, kErrWaitFwdMma))) break;
                     pph[t] ^= 1;
                     if (j == 0) {
@@ -468,7 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc_fence_after();
                     issue_PV<C>(tO(t), tS(t), v_desc(vst), j > 0);
-                    if (j == I.n[t] - 1) {
+                    if (j == item_n(I, t) - 1) {
                         mma_commit_w(BAR(C::B_OFULL + t));
                     } else {
                         if (!kw) {
@@ -478,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         issue_S<C>(tS(t), q_desc(t), k_desc(kst));
                         mma_commit_w(BAR(C::B_SFULL + t));
-                        if (j + 2 == I.n[t]) mma_commit_w(BAR(C::B_QEMPTY + t));  // last S_t issued
+                        if (j + 2 == item_n(I, t)) mma_commit_w(BAR(C::B_QEMPTY + t));  // last S_t issued
                     }
                 }
                 if (!ok) break;
@@ -507,15 +581,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int rd = 0; rd < snake_rounds(p.num_units); ++rd) {
             const int it = snake_item(rd, p.num_units);
             if (it < 0) continue;
-            const Item I = get_item<C, CAUSAL, SPLITK>(it, p);
-            const int n = I.n[t];
+            const auto I = get_item<C, CAUSAL, SPLITK, VARLEN>(it, p);
+            const int n = item_n(I, t);
             const int tile_row0 = I.row0 + t * C::BR;
             const int row = tile_row0 + r_in;
-            const size_t row_idx = (size_t)I.bh * p.N + row;
+            const int nrows = item_rows(I, p);
+            const size_t row_idx = out_row(I, row, p);
             // destination of this row: O / LSE, or the unit's partial (split keys)
             const size_t prow = (size_t)I.part * 256 + t * C::BR + r_in;
             char* orow = reinterpret_cast<char*>(p.o) + row_idx * C::D * (OUT_F32 ? 4 : 2);
-            float* lse_dst = (SPLITK && I.part >= 0) ? p.lse_part + prow : p.lse + row_idx;
+            float* lse_dst = (SPLITK && I.part >= 0)
+                                 ? p.lse_part + prow
+                                 : p.lse + lse_index(I, row, p);
             auto emit = [&](int c, const float (&f)[32]) {
                 if (SPLITK && I.part >= 0) {
                     float4* dst = reinterpret_cast<float4*>(p.o_part + prow * C::D + c);
@@ -526,7 +603,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             };
             if (n == 0) {
-                if (row < p.N) {  // no visible key (kv_len = 0, or an empty key range): O = 0, LSE = -inf
+                if (row < nrows) {  // no visible key (kv_len = 0, or an empty key range): O = 0, LSE = -inf
                     float z[32];
 #pragma unroll
                     for (int i = 0; i < 32; ++i) z[i] = 0.f;
@@ -676,11 +753,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float f[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(ov[i]) * inv;
-                if (row < p.N) emit(c, f);
+                if (row < nrows) emit(c, f);
             }
             tc_fence_before();
             mbar_arrive(BAR(C::B_OEMPTY + t));
-            if (row < p.N) *lse_dst = (l > 0.f) ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+            if (row < nrows) *lse_dst = (l > 0.f) ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
         }
     }
 
@@ -692,13 +769,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <class C, bool CAUSAL, bool OUT_F32, bool SPLITK = false>
+template <class C, bool CAUSAL, bool OUT_F32, bool SPLITK = false, bool VARLEN = false>
 cudaError_t launch(const FwdMaps& m, const FwdParams& p, int grid, cudaStream_t stream) {
-    auto kern = fwd_kernel<C, CAUSAL, OUT_F32, SPLITK>;
+    auto kern = fwd_kernel<C, CAUSAL, OUT_F32, SPLITK, VARLEN>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     kern<<<grid, kThreads, C::SMEM, stream>>>(m.q, m.k, m.v, m.q_lo, m.k_lo, p);
     return cudaGetLastError();
+}
+
+template <class C>
+cudaError_t launch_varlen(bool causal, const FwdMaps& m, const FwdParams& p, int grid, cudaStream_t s) {
+    return causal ? launch<C, true, false, false, true>(m, p, grid, s) : launch<C, false, false, false, true>(m, p, grid, s);
 }
 
 template <class C>

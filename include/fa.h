@@ -143,6 +143,19 @@ fa_status fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float
                      int B, int H, int Hkv, int N, int d, float scale, int causal,
                      const int* kv_lens, fa_stream_t stream);
 
+/* Packed variable-length sequences (flash_attn_varlen_func, [CH18] §18.7.1),
+ * bf16: sequence b holds tokens cu_seqlens[b] .. cu_seqlens[b+1]-1 of the
+ * token-major tensors q, o [total, H, d] and k, v [total, Hkv, d] (Hkv = H
+ * for ordinary multi-head attention); there is no attention across
+ * sequences and causal means key <= query within a sequence.  cu_seqlens:
+ * device int32 [batch + 1], non-decreasing, cu_seqlens[0] = 0 and
+ * cu_seqlens[batch] = total; max_seqlen >= every length (longer sequences
+ * are cut to max_seqlen).  lse: float32 [H, total].  A sequence of length 0
+ * produces nothing. */
+fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                        const int* cu_seqlens, int batch, int total, int max_seqlen, int H, int Hkv,
+                        int d, float scale, int causal, fa_stream_t stream);
+
 /* --------------------------------------------------------------- backward */
 
 /* Scratch for fa_bwd / fa_bwd_ex, in bytes: the row statistics
@@ -170,6 +183,20 @@ fa_status fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o,
                      int B, int H, int Hkv, int N, int d, float scale, int causal,
                      const int* kv_lens, void* workspace, size_t workspace_bytes,
                      fa_stream_t stream);
+
+/* Backward of fa_fwd_varlen (packed variable-length sequences, bf16): dq
+ * [total, H, d], dk, dv [total, Hkv, d] (summed over the query heads sharing
+ * a key/value head), same cu_seqlens / max_seqlen / lse as the forward.
+ * Workspace: fa_bwd_varlen_workspace_size(batch, max_seqlen, H, d) bytes --
+ * LSE*log2(e) and D per (head, sequence) padded to 128 rows, 2 x
+ * [H][batch][Np] float32, and the float32 dQ accumulator [H][batch][Np][d]
+ * (Np = max_seqlen rounded up to 128). */
+size_t fa_bwd_varlen_workspace_size(int batch, int max_seqlen, int H, int d);
+fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
+                        const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                        const int* cu_seqlens, int batch, int total, int max_seqlen, int H,
+                        int Hkv, int d, float scale, int causal, void* workspace,
+                        size_t workspace_bytes, fa_stream_t stream);
 
 /* The three phases fa_bwd runs, callable one by one (bf16 tensors, same
  * workspace).  fa_bwd == fa_bwd_preprocess; fa_bwd_main; fa_bwd_dq.
