@@ -18,6 +18,12 @@ Entry points and what pins each one (tests/test_oracle_*.py):
   fully-masked-row convention.
 * ``fwd_rows`` / ``bwd_rows`` -- the same definitions row by row, for shapes
   whose N x N matrices do not fit.  Pinned against ``fwd`` / ``bwd``.
+* the sliding window (``window=(left, right)`` on the four functions above,
+  chapter 18 §18.7.1 window_size).  Pinned by: float64 autograd of the
+  materialised formula with an explicit additive mask, the window (0, 0)
+  closed form (each query sees only its own key: O_i = v_i, LSE_i = S_ii,
+  dQ = dK = 0, dV_i = dO_i), window (-1, 0) equal to the causal mask,
+  windows wider than N equal to no window, and central finite differences.
 * ``tiled_fwd`` / ``tiled_bwd`` -- Algorithms 1 and 2 of the FA-v2 analysis
   page (§4, §5.4) with arbitrary Br/Bc.  Pinned against ``fwd`` / ``bwd`` on
   the pages' worked shapes (N=4,d=3,Br=Bc=2; the 5-position example with 2x2
@@ -67,19 +73,15 @@ def _load():
         if _lib is None:
             build()
             lib = ctypes.CDLL(_LIB)
-            lib.oracle_fwd.argtypes = [_dp, _dp, _dp, _dp, _dp, ctypes.c_int, ctypes.c_int,
-                                       ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int,
-                                       _ip, ctypes.c_int]
-            lib.oracle_bwd.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp,
-                                       ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                                       ctypes.c_double, ctypes.c_int, _ip, ctypes.c_int]
-            lib.oracle_fwd_rows.argtypes = [_dp, _dp, _dp, ctypes.c_int, ctypes.c_int,
-                                            ctypes.c_double, ctypes.c_int, ctypes.c_int, _ip,
-                                            ctypes.c_int, _dp, _dp]
-            lib.oracle_bwd_rows.argtypes = [_dp, _dp, _dp, _dp, ctypes.c_int, ctypes.c_int,
-                                            ctypes.c_double, ctypes.c_int, ctypes.c_int, _ip,
-                                            ctypes.c_int, _dp, _ip, ctypes.c_int, _dp, _dp, _dp,
-                                            _dp, ctypes.c_int]
+            _i = ctypes.c_int
+            lib.oracle_fwd_win.argtypes = [_dp, _dp, _dp, _dp, _dp, _i, _i, _i, _i, ctypes.c_double,
+                                           _i, _i, _i, _ip, _i]
+            lib.oracle_bwd_win.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp,
+                                           _i, _i, _i, _i, ctypes.c_double, _i, _i, _i, _ip, _i]
+            lib.oracle_fwd_rows_win.argtypes = [_dp, _dp, _dp, _i, _i, ctypes.c_double, _i, _i, _i, _i,
+                                                _ip, _i, _dp, _dp]
+            lib.oracle_bwd_rows_win.argtypes = [_dp, _dp, _dp, _dp, _i, _i, ctypes.c_double, _i, _i, _i,
+                                                _i, _ip, _i, _dp, _ip, _i, _dp, _dp, _dp, _dp, _i]
             lib.oracle_tiled_fwd.argtypes = [_dp, _dp, _dp, _dp, _dp, ctypes.c_int, ctypes.c_int,
                                              ctypes.c_int, ctypes.c_int, ctypes.c_double,
                                              ctypes.c_int, _ip, ctypes.c_int, ctypes.c_int,
@@ -118,25 +120,36 @@ def _kv(kv_lens, B):
     return arr, _ptr(arr, _ip)
 
 
+def _win(window):
+    """(left, right) of the sliding window; -1 (or None) = no bound on that side."""
+    if window is None:
+        return -1, -1
+    wl, wr = window
+    return (-1 if wl is None or wl < 0 else int(wl)), (-1 if wr is None or wr < 0 else int(wr))
+
+
 def default_threads() -> int:
     return int(_load().oracle_default_threads())
 
 
-def fwd(q, k, v, scale, causal=False, kv_lens=None, nthreads=0):
-    """Materialised forward. q,k,v: [B,H,N,d]. Returns (O [B,H,N,d], LSE [B,H,N]) fp64."""
+def fwd(q, k, v, scale, causal=False, kv_lens=None, nthreads=0, window=None):
+    """Materialised forward. q,k,v: [B,H,N,d]. Returns (O [B,H,N,d], LSE [B,H,N]) fp64.
+
+    window = (left, right): key j is visible to query i only if
+    i - left <= j <= i + right (chapter 18 §18.7.1 window_size; -1 = unbounded)."""
     lib = _load()
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, H, N, d = q.shape
     o = np.zeros_like(q)
     lse = np.zeros((B, H, N))
     kv, kvp = _kv(kv_lens, B)
-    rc = lib.oracle_fwd(_ptr(q, _dp), _ptr(k, _dp), _ptr(v, _dp), _ptr(o, _dp), _ptr(lse, _dp),
-                        B, H, N, d, float(scale), int(bool(causal)), kvp, int(nthreads))
+    rc = lib.oracle_fwd_win(_ptr(q, _dp), _ptr(k, _dp), _ptr(v, _dp), _ptr(o, _dp), _ptr(lse, _dp),
+                            B, H, N, d, float(scale), int(bool(causal)), *_win(window), kvp, int(nthreads))
     assert rc == 0
     return o, lse
 
 
-def bwd(q, k, v, dout, scale, causal=False, kv_lens=None, nthreads=0):
+def bwd(q, k, v, dout, scale, causal=False, kv_lens=None, nthreads=0, window=None):
     """Materialised backward of L = sum(O*dO).
 
     Returns dict with o, lse, dq, dk, dv, D (D by its definition sum_j P dP)."""
@@ -147,15 +160,15 @@ def bwd(q, k, v, dout, scale, causal=False, kv_lens=None, nthreads=0):
     lse = np.zeros((B, H, N))
     D = np.zeros((B, H, N))
     kv, kvp = _kv(kv_lens, B)
-    rc = lib.oracle_bwd(_ptr(q, _dp), _ptr(k, _dp), _ptr(v, _dp), _ptr(dout, _dp), _ptr(o, _dp),
-                        _ptr(lse, _dp), _ptr(dq, _dp), _ptr(dk, _dp), _ptr(dv, _dp),
-                        _ptr(D, _dp), B, H, N, d, float(scale), int(bool(causal)), kvp,
-                        int(nthreads))
+    rc = lib.oracle_bwd_win(_ptr(q, _dp), _ptr(k, _dp), _ptr(v, _dp), _ptr(dout, _dp), _ptr(o, _dp),
+                            _ptr(lse, _dp), _ptr(dq, _dp), _ptr(dk, _dp), _ptr(dv, _dp),
+                            _ptr(D, _dp), B, H, N, d, float(scale), int(bool(causal)), *_win(window),
+                            kvp, int(nthreads))
     assert rc == 0
     return dict(o=o, lse=lse, dq=dq, dk=dk, dv=dv, D=D)
 
 
-def fwd_rows(q_head, k_head, v_head, scale, causal, kv_len, rows):
+def fwd_rows(q_head, k_head, v_head, scale, causal, kv_len, rows, window=None):
     """Row-sampled forward of ONE head ([N,d] inputs). Returns (O_rows, LSE_rows)."""
     lib = _load()
     q, k, v = _f64(q_head), _f64(k_head), _f64(v_head)
@@ -163,14 +176,15 @@ def fwd_rows(q_head, k_head, v_head, scale, causal, kv_len, rows):
     rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int32))
     o = np.zeros((len(rows), d))
     lse = np.zeros(len(rows))
-    rc = lib.oracle_fwd_rows(_ptr(q, _dp), _ptr(k, _dp), _ptr(v, _dp), N, d, float(scale),
-                             int(bool(causal)), int(kv_len), _ptr(rows, _ip), len(rows),
-                             _ptr(o, _dp), _ptr(lse, _dp))
+    rc = lib.oracle_fwd_rows_win(_ptr(q, _dp), _ptr(k, _dp), _ptr(v, _dp), N, d, float(scale),
+                                 int(bool(causal)), int(kv_len), *_win(window), _ptr(rows, _ip),
+                                 len(rows), _ptr(o, _dp), _ptr(lse, _dp))
     assert rc == 0
     return o, lse
 
 
-def bwd_rows(q_head, k_head, v_head, dout_head, scale, causal, kv_len, rows, keys, nthreads=0):
+def bwd_rows(q_head, k_head, v_head, dout_head, scale, causal, kv_len, rows, keys, nthreads=0,
+             window=None):
     """Row-sampled backward of ONE head. Returns dict dq (rows), dk, dv (keys), lse, D (all rows)."""
     lib = _load()
     q, k, v, g = _f64(q_head), _f64(k_head), _f64(v_head), _f64(dout_head)
@@ -182,10 +196,11 @@ def bwd_rows(q_head, k_head, v_head, dout_head, scale, causal, kv_len, rows, key
     dv = np.zeros((max(len(keys), 1), d))
     lse = np.zeros(N)
     D = np.zeros(N)
-    rc = lib.oracle_bwd_rows(_ptr(q, _dp), _ptr(k, _dp), _ptr(v, _dp), _ptr(g, _dp), N, d,
-                             float(scale), int(bool(causal)), int(kv_len), _ptr(rows, _ip),
-                             len(rows), _ptr(dq, _dp), _ptr(keys, _ip), len(keys), _ptr(dk, _dp),
-                             _ptr(dv, _dp), _ptr(lse, _dp), _ptr(D, _dp), int(nthreads))
+    rc = lib.oracle_bwd_rows_win(_ptr(q, _dp), _ptr(k, _dp), _ptr(v, _dp), _ptr(g, _dp), N, d,
+                                 float(scale), int(bool(causal)), int(kv_len), *_win(window),
+                                 _ptr(rows, _ip), len(rows), _ptr(dq, _dp), _ptr(keys, _ip), len(keys),
+                                 _ptr(dk, _dp), _ptr(dv, _dp), _ptr(lse, _dp), _ptr(D, _dp),
+                                 int(nthreads))
     assert rc == 0
     return dict(dq=dq, dk=dk[:len(keys)], dv=dv[:len(keys)], lse=lse, D=D)
 

@@ -18,8 +18,12 @@
  *   lse                          : [B, H, N]      (double, natural log)
  *   kv_lens                      : [B] int or NULL (NULL = every key valid)
  *   key j is visible to query i  iff  j < kv_len(b)  and  (!causal or j <= i)
+ *     and, for the sliding window (wl, wr) of flash_attn_func's window_size
+ *     ([CH18] §18.7.1; -1 = no bound on that side),
+ *     (wl < 0 or j >= i - wl)  and  (wr < 0 or j <= i + wr)
  *     -- causal mask M_ij = -inf for j > i ([CH18] §18.2.2 eq. for M_ij);
  *        padding mask removes columns ([CH18] §18.2.2 Table 18-3).
+ *   Entry points without "_win" have no window (wl = wr = -1).
  *   S = scale * Q K^T ([CH18] §18.2.2; [WIKI] §04 "S = QK^T/sqrt(d)").
  *   A row with no visible key has O = 0, LSE = -inf and zero gradients
  *   ([WIKI] §04, the explicit fully-masked-row convention).
@@ -37,9 +41,11 @@
 #define OR_OK 0
 #define OR_ERR 1
 
-static int visible(int i, int j, int kv_len, int causal) {
+static int visible(int i, int j, int kv_len, int causal, int wl, int wr) {
     if (j >= kv_len) return 0;
     if (causal && j > i) return 0;
+    if (wl >= 0 && j < i - wl) return 0;
+    if (wr >= 0 && j > i + wr) return 0;
     return 1;
 }
 
@@ -110,11 +116,11 @@ static void run_items(item_fn fn, void* arg, long n_items, int nthreads) {
  * LSE.  Returns nothing; S and P are caller scratch. */
 static void naive_head_forward(const double* q, const double* k, const double* v,
                                double* o, double* lse, double* S, double* P,
-                               int N, int d, double scale, int causal, int kv_len) {
+                               int N, int d, double scale, int causal, int kv_len, int wl, int wr) {
     for (int i = 0; i < N; ++i) {
         for (int j = 0; j < N; ++j) {
             double s = -INFINITY;
-            if (visible(i, j, kv_len, causal)) {
+            if (visible(i, j, kv_len, causal, wl, wr)) {
                 double acc = 0.0;
                 for (int t = 0; t < d; ++t) acc += q[(size_t)i * d + t] * k[(size_t)j * d + t];
                 s = scale * acc;
@@ -151,7 +157,7 @@ static void naive_head_forward(const double* q, const double* k, const double* v
 typedef struct {
     const double *q, *k, *v, *dout;
     double *o, *lse, *dq, *dk, *dv, *Dout;
-    int B, H, N, d, causal;
+    int B, H, N, d, causal, wl, wr;
     double scale;
     const int* kv_lens;
 } naive_args;
@@ -164,19 +170,25 @@ static void naive_fwd_item(void* a_, long bh) {
     double* S = (double*)malloc(sizeof(double) * N * N);
     double* P = (double*)malloc(sizeof(double) * N * N);
     naive_head_forward(a->q + off, a->k + off, a->v + off, a->o + off, a->lse + (size_t)bh * N, S, P,
-                       a->N, a->d, a->scale, a->causal, kvlen_of(a->kv_lens, b, a->N));
+                       a->N, a->d, a->scale, a->causal, kvlen_of(a->kv_lens, b, a->N), a->wl, a->wr);
     free(S);
     free(P);
 }
 
 /* Forward: O = softmax(scale Q K^T + M) V and LSE, materialising S and P. */
+int oracle_fwd_win(const double* q, const double* k, const double* v, double* o, double* lse,
+                   int B, int H, int N, int d, double scale, int causal, int wl, int wr,
+                   const int* kv_lens, int nthreads) {
+    if (B <= 0 || H <= 0 || N <= 0 || d <= 0) return OR_ERR;
+    naive_args a = {q, k, v, NULL, o, lse, NULL, NULL, NULL, NULL, B, H, N, d, causal, wl, wr, scale, kv_lens};
+    run_items(naive_fwd_item, &a, (long)B * H, nthreads);
+    return OR_OK;
+}
+
 int oracle_fwd(const double* q, const double* k, const double* v, double* o, double* lse,
                int B, int H, int N, int d, double scale, int causal, const int* kv_lens,
                int nthreads) {
-    if (B <= 0 || H <= 0 || N <= 0 || d <= 0) return OR_ERR;
-    naive_args a = {q, k, v, NULL, o, lse, NULL, NULL, NULL, NULL, B, H, N, d, causal, scale, kv_lens};
-    run_items(naive_fwd_item, &a, (long)B * H, nthreads);
-    return OR_OK;
+    return oracle_fwd_win(q, k, v, o, lse, B, H, N, d, scale, causal, -1, -1, kv_lens, nthreads);
 }
 
 /* Backward of L = sum(O * dO) for one head, by the definitions of
@@ -196,7 +208,8 @@ static void naive_bwd_item(void* a_, long bh) {
     double* P = (double*)malloc(sizeof(double) * (size_t)N * N);
     double* dP = (double*)malloc(sizeof(double) * (size_t)N * N);
     double* D = (double*)malloc(sizeof(double) * (size_t)N);
-    naive_head_forward(q, k, v, o, lse, S, P, N, d, a->scale, a->causal, kvlen_of(a->kv_lens, b, N));
+    naive_head_forward(q, k, v, o, lse, S, P, N, d, a->scale, a->causal, kvlen_of(a->kv_lens, b, N), a->wl,
+                       a->wr);
     /* dP = dO V^T */
     for (int i = 0; i < N; ++i)
         for (int j = 0; j < N; ++j) {
@@ -240,14 +253,22 @@ static void naive_bwd_item(void* a_, long bh) {
 }
 
 /* Backward (also returns the forward O, LSE and, if D_out != NULL, D). */
+int oracle_bwd_win(const double* q, const double* k, const double* v, const double* dout,
+                   double* o, double* lse, double* dq, double* dk, double* dv, double* D_out,
+                   int B, int H, int N, int d, double scale, int causal, int wl, int wr,
+                   const int* kv_lens, int nthreads) {
+    if (B <= 0 || H <= 0 || N <= 0 || d <= 0) return OR_ERR;
+    naive_args a = {q, k, v, dout, o, lse, dq, dk, dv, D_out, B, H, N, d, causal, wl, wr, scale, kv_lens};
+    run_items(naive_bwd_item, &a, (long)B * H, nthreads);
+    return OR_OK;
+}
+
 int oracle_bwd(const double* q, const double* k, const double* v, const double* dout,
                double* o, double* lse, double* dq, double* dk, double* dv, double* D_out,
                int B, int H, int N, int d, double scale, int causal, const int* kv_lens,
                int nthreads) {
-    if (B <= 0 || H <= 0 || N <= 0 || d <= 0) return OR_ERR;
-    naive_args a = {q, k, v, dout, o, lse, dq, dk, dv, D_out, B, H, N, d, causal, scale, kv_lens};
-    run_items(naive_bwd_item, &a, (long)B * H, nthreads);
-    return OR_OK;
+    return oracle_bwd_win(q, k, v, dout, o, lse, dq, dk, dv, D_out, B, H, N, d, scale, causal, -1, -1,
+                          kv_lens, nthreads);
 }
 
 /* ======================================================================== */
@@ -257,9 +278,9 @@ int oracle_bwd(const double* q, const double* k, const double* v, const double* 
 
 /* O and LSE of selected query rows of one head (definition applied row by
  * row: the row's scores, its safe-softmax LSE, then P V). */
-int oracle_fwd_rows(const double* q, const double* k, const double* v, int N, int d, double scale,
-                    int causal, int kv_len, const int* rows, int nrows, double* o_rows,
-                    double* lse_rows) {
+int oracle_fwd_rows_win(const double* q, const double* k, const double* v, int N, int d, double scale,
+                        int causal, int kv_len, int wl, int wr, const int* rows, int nrows,
+                        double* o_rows, double* lse_rows) {
     if (N <= 0 || d <= 0) return OR_ERR;
     if (kv_len < 0) kv_len = 0;
     if (kv_len > N) kv_len = N;
@@ -270,7 +291,7 @@ int oracle_fwd_rows(const double* q, const double* k, const double* v, int N, in
         double mx = -INFINITY;
         for (int j = 0; j < N; ++j) {
             s[j] = -INFINITY;
-            if (visible(i, j, kv_len, causal)) {
+            if (visible(i, j, kv_len, causal, wl, wr)) {
                 double acc = 0.0;
                 for (int t = 0; t < d; ++t) acc += q[(size_t)i * d + t] * k[(size_t)j * d + t];
                 s[j] = scale * acc;
@@ -298,9 +319,15 @@ int oracle_fwd_rows(const double* q, const double* k, const double* v, int N, in
     return OR_OK;
 }
 
+int oracle_fwd_rows(const double* q, const double* k, const double* v, int N, int d, double scale,
+                    int causal, int kv_len, const int* rows, int nrows, double* o_rows,
+                    double* lse_rows) {
+    return oracle_fwd_rows_win(q, k, v, N, d, scale, causal, kv_len, -1, -1, rows, nrows, o_rows, lse_rows);
+}
+
 typedef struct {
     const double *q, *k, *v, *dout;
-    int N, d, causal, kv_len;
+    int N, d, causal, kv_len, wl, wr;
     double scale;
     double *lse, *D; /* [N] each, filled per row */
 } rowstat_args;
@@ -313,7 +340,7 @@ static void rowstat_item(void* a_, long i_) {
     double mx = -INFINITY;
     for (int j = 0; j < N; ++j) {
         s[j] = -INFINITY;
-        if (visible(i, j, a->kv_len, a->causal)) {
+        if (visible(i, j, a->kv_len, a->causal, a->wl, a->wr)) {
             double acc = 0.0;
             for (int t = 0; t < d; ++t) acc += a->q[(size_t)i * d + t] * a->k[(size_t)j * d + t];
             s[j] = a->scale * acc;
@@ -362,7 +389,7 @@ static void keygrad_item(void* a_, long c) {
     for (int r = 0; r < ka->nkeys; ++r) {
         int j = ka->keys[r];
         for (int i = i0; i < i1; ++i) {
-            if (!visible(i, j, a->kv_len, a->causal) || a->lse[i] == -INFINITY) continue;
+            if (!visible(i, j, a->kv_len, a->causal, a->wl, a->wr) || a->lse[i] == -INFINITY) continue;
             double acc = 0.0;
             for (int t = 0; t < d; ++t) acc += a->q[(size_t)i * d + t] * a->k[(size_t)j * d + t];
             double p = exp(a->scale * acc - a->lse[i]);
@@ -381,16 +408,16 @@ static void keygrad_item(void* a_, long c) {
  * LSE and D of every query row come from their definitions (rowstat_item),
  * then dQ_i = scale sum_j dS_ij k_j and dK_j = scale sum_i dS_ij q_i,
  * dV_j = sum_i P_ij dO_i.  Optionally returns the full-head LSE and D. */
-int oracle_bwd_rows(const double* q, const double* k, const double* v, const double* dout, int N,
-                    int d, double scale, int causal, int kv_len, const int* rows, int nrows,
-                    double* dq_rows, const int* keys, int nkeys, double* dk_rows, double* dv_rows,
-                    double* lse_all, double* D_all, int nthreads) {
+int oracle_bwd_rows_win(const double* q, const double* k, const double* v, const double* dout, int N,
+                        int d, double scale, int causal, int kv_len, int wl, int wr, const int* rows,
+                        int nrows, double* dq_rows, const int* keys, int nkeys, double* dk_rows,
+                        double* dv_rows, double* lse_all, double* D_all, int nthreads) {
     if (N <= 0 || d <= 0) return OR_ERR;
     if (kv_len < 0) kv_len = 0;
     if (kv_len > N) kv_len = N;
     double* lse = lse_all ? lse_all : (double*)malloc(sizeof(double) * (size_t)N);
     double* D = D_all ? D_all : (double*)malloc(sizeof(double) * (size_t)N);
-    rowstat_args rs = {q, k, v, dout, N, d, causal, kv_len, scale, lse, D};
+    rowstat_args rs = {q, k, v, dout, N, d, causal, kv_len, wl, wr, scale, lse, D};
     run_items(rowstat_item, &rs, N, nthreads);
     for (int r = 0; r < nrows; ++r) {
         int i = rows[r];
@@ -398,7 +425,7 @@ int oracle_bwd_rows(const double* q, const double* k, const double* v, const dou
         for (int t = 0; t < d; ++t) g[t] = 0.0;
         if (lse[i] == -INFINITY) continue;
         for (int j = 0; j < N; ++j) {
-            if (!visible(i, j, kv_len, causal)) continue;
+            if (!visible(i, j, kv_len, causal, wl, wr)) continue;
             double acc = 0.0;
             for (int t = 0; t < d; ++t) acc += q[(size_t)i * d + t] * k[(size_t)j * d + t];
             double p = exp(scale * acc - lse[i]);
@@ -434,6 +461,14 @@ int oracle_bwd_rows(const double* q, const double* k, const double* v, const dou
     if (!lse_all) free(lse);
     if (!D_all) free(D);
     return OR_OK;
+}
+
+int oracle_bwd_rows(const double* q, const double* k, const double* v, const double* dout, int N,
+                    int d, double scale, int causal, int kv_len, const int* rows, int nrows,
+                    double* dq_rows, const int* keys, int nkeys, double* dk_rows, double* dv_rows,
+                    double* lse_all, double* D_all, int nthreads) {
+    return oracle_bwd_rows_win(q, k, v, dout, N, d, scale, causal, kv_len, -1, -1, rows, nrows, dq_rows, keys,
+                               nkeys, dk_rows, dv_rows, lse_all, D_all, nthreads);
 }
 
 /* ======================================================================== */
