@@ -57,6 +57,8 @@ _SIGS = {
     "fa_quantize_fp8": ([_vp, _vp, _vp, _i, _i, _i, _i, _vp], _i),
     "fa_fwd_fp8": ([_vp] * 8 + [_i, _i, _i, _i, _f, _i, _vp, _vp], _i),
     "fa_fwd_gqa": ([_vp] * 5 + [_i, _i, _i, _i, _i, _f, _i, _vp, _vp], _i),
+    "fa_fwd_window": ([_vp] * 5 + [_i, _i, _i, _i, _i, _f, _i, _i, _i, _vp, _vp], _i),
+    "fa_bwd_window": ([_vp] * 9 + [_i, _i, _i, _i, _i, _f, _i, _i, _i, _vp, _vp, _sz, _vp], _i),
     "fa_fwd_varlen": ([_vp] * 6 + [_i, _i, _i, _i, _i, _i, _f, _i, _vp], _i),
     "fa_bwd_varlen_workspace_size": ([_i] * 4, _sz),
     "fa_bwd_varlen": ([_vp] * 10 + [_i, _i, _i, _i, _i, _i, _f, _i, _vp, _sz, _vp], _i),
@@ -137,13 +139,26 @@ def bwd_workspace_size(dtype: torch.dtype, B: int, H: int, N: int, d: int) -> in
     return int(load_library().fa_bwd_workspace_size(dt, B, H, N, d))
 
 
+def _window(window) -> Tuple[int, int]:
+    if window is None:
+        return -1, -1
+    wl, wr = window
+    wl = -1 if wl is None else int(wl)
+    wr = -1 if wr is None else int(wr)
+    if wl < -1 or wr < -1:
+        raise ValueError("window edges must be >= -1 (-1 = unbounded)")
+    return wl, wr
+
+
 def forward(q, k, v, causal: bool = False, scale: Optional[float] = None, kv_lens=None,
             block_c: int = 0, out: Optional[torch.Tensor] = None,
-            lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None
-            ) -> Tuple[torch.Tensor, torch.Tensor]:
+            lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+            window: Optional[Tuple[int, int]] = None) -> Tuple[torch.Tensor, torch.Tensor]:
     """O, LSE of softmax(scale Q K^T + mask) V.  q: [B,H,N,d] bf16 or float32;
     k, v: [B,H,N,d], or bf16 [B,Hkv,N,d] with fewer key/value heads (H a
-    multiple of Hkv; query head h uses key/value head h // (H // Hkv))."""
+    multiple of Hkv; query head h uses key/value head h // (H // Hkv)).
+    window = (left, right): sliding window, key j visible to query i only if
+    i - left <= j <= i + right (-1 = unbounded; bf16 only)."""
     lib = load_library()
     _need_cuda(q, k, v)
     B, H, N, d = q.shape
@@ -158,6 +173,13 @@ def forward(q, k, v, causal: bool = False, scale: Optional[float] = None, kv_len
     o = torch.empty_like(q) if out is None else out
     l = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
     _need_cuda(o, l)
+    wl, wr = _window(window)
+    if wl >= 0 or wr >= 0:
+        if q.dtype != torch.bfloat16:
+            raise ValueError("the sliding window needs bfloat16 tensors")
+        _check(lib.fa_fwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(l), B, H, Hkv, N, d, scale,
+                                 int(bool(causal)), wl, wr, _ptr(kv), _stream(q)))
+        return o, l
     if Hkv != H:
         if q.dtype != torch.bfloat16:
             raise ValueError("shared key/value heads need bfloat16 tensors")
@@ -271,9 +293,10 @@ def backward_varlen(q, k, v, o, lse, dout, cu_seqlens, max_seqlen: int, causal: 
 def backward(q, k, v, o, lse, dout, causal: bool = False, scale: Optional[float] = None,
              kv_lens=None, workspace: Optional[torch.Tensor] = None,
              dq: Optional[torch.Tensor] = None, dk: Optional[torch.Tensor] = None,
-             dv: Optional[torch.Tensor] = None):
+             dv: Optional[torch.Tensor] = None, window: Optional[Tuple[int, int]] = None):
     """dQ, dK, dV of L = sum(O * dout).  With fewer key/value heads (k, v
-    [B,Hkv,N,d]), dK and dV sum over the query heads sharing each one."""
+    [B,Hkv,N,d]), dK and dV sum over the query heads sharing each one.
+    window: the forward's sliding window (see forward)."""
     lib = load_library()
     _need_cuda(q, k, v, o, lse, dout)
     B, H, N, d = q.shape
@@ -289,6 +312,14 @@ def backward(q, k, v, o, lse, dout, causal: bool = False, scale: Optional[float]
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     _need_cuda(dq, dk, dv)
+    wl, wr = _window(window)
+    if wl >= 0 or wr >= 0:
+        if q.dtype != torch.bfloat16 or H % Hkv != 0:
+            raise ValueError("the sliding window needs bfloat16 tensors and H a multiple of Hkv")
+        _check(lib.fa_bwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
+                                 _ptr(dk), _ptr(dv), B, H, Hkv, N, d, scale, int(bool(causal)), wl, wr,
+                                 _ptr(kv), _ptr(ws), ws.numel() * ws.element_size(), _stream(q)))
+        return dq, dk, dv
     if Hkv != H:
         if q.dtype != torch.bfloat16 or H % Hkv != 0:
             raise ValueError("shared key/value heads need bfloat16 tensors and H a multiple of Hkv")

@@ -230,8 +230,14 @@ SplitPlan plan_split(int B, int H, int N, int d, bool causal, bool has_kv, int r
 fa_status fwd_impl(fa_dtype dtype, int block_c, bool fp8, const void* q, const void* k, const void* v, const float* sq,
                    const float* sk, const float* sv, void* o, float* lse, int B, int H, int N, int d, float scale,
                    int causal, const int* kv_lens, void* workspace, size_t workspace_bytes, cudaStream_t stream,
-                   int num_splits = 1, void* split_ws = nullptr, size_t split_ws_bytes = 0, int Hkv = 0) {
+                   int num_splits = 1, void* split_ws = nullptr, size_t split_ws_bytes = 0, int Hkv = 0,
+                   int win_left = -1, int win_right = -1) {
     FA_TRY(check_common(B, H, N, d, scale));
+    if (win_left < -1 || win_right < -1) return fail(FA_ERR_INVALID_ARG, "window edges must be >= -1");
+    const bool window = win_left >= 0 || win_right >= 0;
+    if (window && (dtype != FA_BF16 || fp8)) return fail(FA_ERR_UNSUPPORTED, "the sliding window needs bf16 inputs");
+    if (window && block_c == 64) return fail(FA_ERR_UNSUPPORTED, "the sliding window uses 128-key blocks");
+    if (window && num_splits > 1) return fail(FA_ERR_UNSUPPORTED, "the sliding window is not split over keys");
     if (Hkv == 0) Hkv = H;
     if (Hkv < 1 || H % Hkv != 0) return fail(FA_ERR_INVALID_ARG, "H (%d) must be a multiple of Hkv (%d)", H, Hkv);
     if (Hkv != H && dtype != FA_BF16) return fail(FA_ERR_UNSUPPORTED, "shared key/value heads need bf16 inputs");
@@ -276,8 +282,10 @@ fa_status fwd_impl(fa_dtype dtype, int block_c, bool fp8, const void* q, const v
         if (block_c == 0) block_c = (d == 128 || N <= 128) ? 64 : 128;
     }
     if (num_splits < 0) return fail(FA_ERR_INVALID_ARG, "num_splits must be >= 0");
-    const SplitPlan P = (dtype == FA_BF16) ? plan_split(B, H, N, d, causal != 0, kv_lens != nullptr, num_splits, dev->sms)
-                                           : SplitPlan{};
+    const SplitPlan P = (dtype == FA_BF16 && !window)
+                            ? plan_split(B, H, N, d, causal != 0, kv_lens != nullptr, num_splits, dev->sms)
+                            : SplitPlan{};
+    if (window) block_c = 128;
     if (P.splits > 1) block_c = 128;  // the split-key instances use 128-key blocks
     if (block_c == 0) block_c = (N <= 128 && !fp8) ? 64 : 128;
     fa::FwdMaps m;
@@ -320,7 +328,15 @@ fa_status fwd_impl(fa_dtype dtype, int block_c, bool fp8, const void* q, const v
     }
     const int grid = grid_for_items(p.num_units, dev->sms);
     cudaError_t e;
-    if (P.splits > 1)
+    if (window) {
+        // causal = the window's right edge at 0
+        fa::FwdParamsWin pw;
+        memset(&pw, 0, sizeof(pw));
+        static_cast<fa::FwdParams&>(pw) = p;
+        pw.win_left = win_left;
+        pw.win_right = causal ? 0 : win_right;
+        e = fa::launch_fwd_window(d, m, pw, grid, stream);
+    } else if (P.splits > 1)
         e = fa::launch_fwd_splitk(d, fp8, causal != 0, m, p, grid, stream);
     else if (fp8)
         e = fa::launch_fwd_fp8_d128(causal != 0, m, p, grid, stream);
@@ -400,6 +416,14 @@ fa_status fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float
     if (Hkv < 1 || H % Hkv != 0) return fail(FA_ERR_INVALID_ARG, "H (%d) must be a multiple of Hkv (%d)", H, Hkv);
     return fwd_impl(FA_BF16, 0, false, q, k, v, nullptr, nullptr, nullptr, o, lse, B, H, N, d, scale, causal, kv_lens,
                     nullptr, 0, stream, 1, nullptr, 0, Hkv);
+}
+
+fa_status fa_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv,
+                        int N, int d, float scale, int causal, int window_left, int window_right,
+                        const int* kv_lens, fa_stream_t stream) {
+    if (Hkv < 1 || H % Hkv != 0) return fail(FA_ERR_INVALID_ARG, "H (%d) must be a multiple of Hkv (%d)", H, Hkv);
+    return fwd_impl(FA_BF16, 0, false, q, k, v, nullptr, nullptr, nullptr, o, lse, B, H, N, d, scale, causal, kv_lens,
+                    nullptr, 0, stream, 1, nullptr, 0, Hkv, window_left, window_right);
 }
 
 fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens,
@@ -511,7 +535,7 @@ fa_status make_map_dqacc(CUtensorMap* m, float* dqacc, int d, long long rows) {
 
 fa_status bwd_main_impl(const BwdCtx& c, bool f32, const void* qb, const void* kb, const void* vb, const void* gb,
                         void* dk, void* dv, int B, int H, int N, int d, float scale, int causal, const int* kv_lens,
-                        cudaStream_t stream, int Hkv = 0) {
+                        cudaStream_t stream, int Hkv = 0, int win_left = -1, int win_right = -1) {
     const int BH = c.BH, Np = c.Np;
     if (Hkv == 0) Hkv = H;
     if (Hkv < 1 || H % Hkv != 0) return fail(FA_ERR_INVALID_ARG, "H (%d) must be a multiple of Hkv (%d)", H, Hkv);
@@ -539,8 +563,19 @@ fa_status bwd_main_impl(const BwdCtx& c, bool f32, const void* qb, const void* k
     p.dv = dv;
     p.err = c.dev->err_word;
     const int grid = grid_for_items(p.num_items, c.dev->sms);
-    cudaError_t e = (Hkv != H) ? fa::launch_bwd_main_gqa(d, causal != 0, tq, tk, tv, tdo, tdq, p, grid, stream)
-                               : fa::launch_bwd_main(d, causal != 0, f32, tq, tk, tv, tdo, tdq, p, grid, stream);
+    cudaError_t e;
+    if (win_left >= 0 || win_right >= 0) {
+        // causal = the window's right edge at 0
+        fa::BwdParamsWin pw;
+        memset(&pw, 0, sizeof(pw));
+        static_cast<fa::BwdParams&>(pw) = p;
+        pw.win_left = win_left;
+        pw.win_right = causal ? 0 : win_right;
+        e = fa::launch_bwd_main_window(d, tq, tk, tv, tdo, tdq, pw, grid, stream);
+    } else {
+        e = (Hkv != H) ? fa::launch_bwd_main_gqa(d, causal != 0, tq, tk, tv, tdo, tdq, p, grid, stream)
+                       : fa::launch_bwd_main(d, causal != 0, f32, tq, tk, tv, tdo, tdq, p, grid, stream);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "backward main launch");
     return FA_OK;
 }
@@ -636,6 +671,29 @@ fa_status fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o,
     FA_TRY(bwd_setup(FA_BF16, B, H, N, d, scale, workspace, workspace_bytes, &c));
     FA_TRY(bwd_pre_impl(c, false, o, lse, dout, N, d, stream));
     FA_TRY(bwd_main_impl(c, false, q, k, v, dout, dk, dv, B, H, N, d, scale, causal, kv_lens, stream, Hkv));
+    return bwd_dq_impl(c, false, dq, N, d, scale, stream);
+}
+
+fa_status fa_bwd_window(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                        const void* dout, void* dq, void* dk, void* dv, int B, int H, int Hkv, int N, int d,
+                        float scale, int causal, int window_left, int window_right, const int* kv_lens,
+                        void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+    FA_CHECK_PTR(q);
+    FA_CHECK_PTR(k);
+    FA_CHECK_PTR(v);
+    FA_CHECK_PTR(o);
+    FA_CHECK_PTR(lse);
+    FA_CHECK_PTR(dout);
+    FA_CHECK_PTR(dq);
+    FA_CHECK_PTR(dk);
+    FA_CHECK_PTR(dv);
+    if (Hkv < 1 || H % Hkv != 0) return fail(FA_ERR_INVALID_ARG, "H (%d) must be a multiple of Hkv (%d)", H, Hkv);
+    if (window_left < -1 || window_right < -1) return fail(FA_ERR_INVALID_ARG, "window edges must be >= -1");
+    BwdCtx c{};
+    FA_TRY(bwd_setup(FA_BF16, B, H, N, d, scale, workspace, workspace_bytes, &c));
+    FA_TRY(bwd_pre_impl(c, false, o, lse, dout, N, d, stream));
+    FA_TRY(bwd_main_impl(c, false, q, k, v, dout, dk, dv, B, H, N, d, scale, causal, kv_lens, stream, Hkv, window_left,
+                         window_right));
     return bwd_dq_impl(c, false, dq, N, d, scale, stream);
 }
 

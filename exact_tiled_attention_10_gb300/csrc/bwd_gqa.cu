@@ -1,5 +1,5 @@
-// Backward kernel instances for shared key/value heads and for packed
-// variable-length sequences (bf16 gradients).
+// Backward kernel instances for shared key/value heads, for packed
+// variable-length sequences and for the sliding window (bf16 gradients).
 #include "bwd_kernel.cuh"
 
 namespace fa {
@@ -26,6 +26,13 @@ cudaError_t launch_bwd_main_varlen(int d, bool causal, const CUtensorMap& tq, co
                       : bwd::launch<C128, false, false, true, true>(tq, tk, tv, tdo, tdq, p, grid, s);
     return causal ? bwd::launch<C64, true, false, true, true>(tq, tk, tv, tdo, tdq, p, grid, s)
                   : bwd::launch<C64, false, false, true, true>(tq, tk, tv, tdo, tdq, p, grid, s);
+}
+
+cudaError_t launch_bwd_main_window(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                   const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParamsWin& p, int grid,
+                                   cudaStream_t s) {
+    if (d == 128) return bwd::launch<bwd::Cfg<128>, false, false, true, false, true>(tq, tk, tv, tdo, tdq, p, grid, s);
+    return bwd::launch<bwd::Cfg<64>, false, false, true, false, true>(tq, tk, tv, tdo, tdq, p, grid, s);
 }
 
 }  // namespace fa

@@ -36,6 +36,8 @@
 //   * warp 12 issues TMA loads (K_j, V_j once per item; a ring of Q_i, dO_i
 //     and the row statistics), warp 13 issues tcgen05.mma.
 #pragma once
+#include <type_traits>
+
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -112,8 +114,13 @@ struct Item {
 // VARLEN (packed variable-length sequences, always with the GQA step loop):
 // qh0 / the step's bhq are head indices within the sequence, the K, V, dK, dV
 // rows are tokens tb + key, and the statistics rows are (h * B + b) * Np + ...
-template <class C, bool CAUSAL, bool GQA, bool VARLEN = false>
-__device__ __forceinline__ Item get_item(int it, const BwdParams& p) {
+// WINDOW: the sliding-window instance (p is a BwdParamsWin; causal is folded
+// into the window's right edge by the caller).
+template <bool WINDOW>
+using ParamsT = typename std::conditional<WINDOW, BwdParamsWin, BwdParams>::type;
+
+template <class C, bool CAUSAL, bool GQA, bool VARLEN = false, bool WINDOW = false>
+__device__ __forceinline__ Item get_item(int it, const ParamsT<WINDOW>& p) {
     Item I;
     const int Hkv = GQA ? p.Hkv : p.H;
     const int BH = p.B * Hkv;
@@ -141,7 +148,15 @@ __device__ __forceinline__ Item get_item(int it, const BwdParams& p) {
     const int key0 = I.kt * C::BC;
     const int iend = ((VARLEN ? I.seqlen : p.N) + C::BR - 1) / C::BR;
     I.i0 = CAUSAL ? key0 / C::BR : 0;
-    I.ni = (key0 >= kvl) ? 0 : max(iend - I.i0, 0);
+    if constexpr (WINDOW) {
+        // query rows that see some key of the block: [key0 - right, last key + left]
+        int ie = iend;
+        if (p.win_right >= 0) I.i0 = max(I.i0, max(0, key0 - p.win_right) / C::BR);
+        if (p.win_left >= 0 && key0 < kvl) ie = min(ie, (min(key0 + C::BC, kvl) - 1 + p.win_left) / C::BR + 1);
+        I.ni = (key0 >= kvl) ? 0 : max(ie - I.i0, 0);
+    } else {
+        I.ni = (key0 >= kvl) ? 0 : max(iend - I.i0, 0);
+    }
     I.n = I.ni * group;
     return I;
 }
@@ -226,11 +241,11 @@ __device__ __forceinline__ void mma_dq(uint32_t d_tmem, uint64_t k_mn, uint64_t 
     }
 }
 
-template <class C, bool CAUSAL, bool OUT_F32, bool GQA, bool VARLEN = false>
+template <class C, bool CAUSAL, bool OUT_F32, bool GQA, bool VARLEN = false, bool WINDOW = false>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
-               const __grid_constant__ CUtensorMap tdq, const BwdParams p) {
+               const __grid_constant__ CUtensorMap tdq, const ParamsT<WINDOW> p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -285,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int rd = 0; rd < snake_rounds(p.num_items) && ok; ++rd) {
             const int it = snake_item(rd, p.num_items);
             if (it < 0) continue;
-            const Item I = get_item<C, CAUSAL, GQA, VARLEN>(it, p);
+            const Item I = get_item<C, CAUSAL, GQA, VARLEN, WINDOW>(it, p);
             if (I.n == 0) continue;
             if (!(ok = wait_bounded_warp(BAR(C::B_KVEMPTY), kve ^ 1, abort_flag, p.err, kErrWaitBwdProducer))) break;
             kve ^= 1;
@@ -361,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int rd = 0; rd < snake_rounds(p.num_items) && ok; ++rd) {
             const int it = snake_item(rd, p.num_items);
             if (it < 0) continue;
-            const Item I = get_item<C, CAUSAL, GQA, VARLEN>(it, p);
+            const Item I = get_item<C, CAUSAL, GQA, VARLEN, WINDOW>(it, p);
             if (I.n == 0) continue;
             if (!(ok = wait_bounded_warp(BAR(C::B_KVFULL), kvph, abort_flag, p.err, kErrWaitBwdMma))) break;
             kvph ^= 1;
@@ -422,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int rd = 0; rd < snake_rounds(p.num_items) && ok; ++rd) {
             const int it = snake_item(rd, p.num_items);
             if (it < 0) continue;
-            const Item I = get_item<C, CAUSAL, GQA, VARLEN>(it, p);
+            const Item I = get_item<C, CAUSAL, GQA, VARLEN, WINDOW>(it, p);
             const int key = I.kt * C::BC + kr;
             // dK, dV row: [B,Hkv,N,d], or token-major [total, Hkv, d] for packed sequences
             const size_t krow = VARLEN ? (size_t)(I.tb + key) * p.Hkv + I.kvh : (size_t)I.bh * p.N + key;
@@ -454,8 +469,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ld32_wait(tmem + lane_off + C::s_col(slot) + h * C::HALF, *reinterpret_cast<uint32_t(*)[32]>(sr));
                 else
                     tmem_ld64_wait(tmem + lane_off + C::s_col(slot) + h * C::HALF, *reinterpret_cast<uint32_t(*)[64]>(sr));
-                const bool need_mask = (I.kt * C::BC + C::BC > I.kvl) ||
-                                       (CAUSAL && I.kt * C::BC + C::BC - 1 > i * C::BR);
+                bool need_mask = (I.kt * C::BC + C::BC > I.kvl) || (CAUSAL && I.kt * C::BC + C::BC - 1 > i * C::BR);
+                if constexpr (WINDOW)  // some pair of the tile outside the window
+                    need_mask = need_mask || (p.win_right >= 0 && I.kt * C::BC + C::BC - 1 > i * C::BR + p.win_right) ||
+                                (p.win_left >= 0 && I.kt * C::BC < i * C::BR + C::BR - 1 - p.win_left);
                 const bool key_ok = key < I.kvl;
                 float pv[C::HALF];
                 const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
@@ -475,7 +492,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int c = 0; c < C::HALF; ++c) {
                         const int q = q0 + c;
-                        if (!key_ok || (CAUSAL && key > q)) pv[c] = 0.f;
+                        bool off = !key_ok || (CAUSAL && key > q);
+                        if constexpr (WINDOW)
+                            off = off || (p.win_right >= 0 && key > q + p.win_right) || (p.win_left >= 0 && key < q - p.win_left);
+                        if (off) pv[c] = 0.f;
                     }
                 }
                 // P^T (bf16) over this half's S^T columns, as the A operand of dV += P^T dO
@@ -562,7 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int rd = 0; rd < snake_rounds(p.num_items) && ok; ++rd) {
             const int it = snake_item(rd, p.num_items);
             if (it < 0) continue;
-            const Item I = get_item<C, CAUSAL, GQA, VARLEN>(it, p);
+            const Item I = get_item<C, CAUSAL, GQA, VARLEN, WINDOW>(it, p);
             int bhq = I.qh0, i = I.i0;
             for (int s = 0; s < I.n; ++s, step_next<GQA>(I, bhq, i)) {
                 const int dqs = C::DQ_ALIAS ? (s % C::NSLOT) : 0;
@@ -622,11 +642,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <class C, bool CAUSAL, bool OUT_F32, bool GQA = false, bool VARLEN = false>
+template <class C, bool CAUSAL, bool OUT_F32, bool GQA = false, bool VARLEN = false, bool WINDOW = false>
 cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                   const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p, int grid,
+                   const CUtensorMap& tdo, const CUtensorMap& tdq, const ParamsT<WINDOW>& p, int grid,
                    cudaStream_t stream) {
-    auto kern = bwd_kernel<C, CAUSAL, OUT_F32, GQA, VARLEN>;
+    auto kern = bwd_kernel<C, CAUSAL, OUT_F32, GQA, VARLEN, WINDOW>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     kern<<<grid, kThreads, C::SMEM, stream>>>(tq, tk, tv, tdo, tdq, p);

@@ -106,6 +106,17 @@ struct BwdParams {
     unsigned int* err;
 };
 
+// Sliding window (flash_attn_func's window_size, chapter 18 §18.7.1): key j
+// is visible to query i only if i - win_left <= j <= i + win_right, -1
+// meaning no bound on that side.  Derived types, so that only the window
+// instances carry the two fields.
+struct FwdParamsWin : FwdParams {
+    int win_left, win_right;
+};
+struct BwdParamsWin : BwdParams {
+    int win_left, win_right;
+};
+
 // Launch helpers implemented in the kernel translation units.  They return a
 // cudaError_t from the launch itself.
 // Tensor maps of one forward launch: q, k, v and, for float32 inputs carried
@@ -117,6 +128,10 @@ cudaError_t launch_fwd_bf16_d64(int block_c, bool causal, bool out_f32, bool spl
                                 const FwdParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_fwd_bf16_d128(int block_c, bool causal, bool out_f32, bool split, const FwdMaps& m,
                                  const FwdParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_fwd_window(int d, const FwdMaps& m, const FwdParamsWin& p, int grid, cudaStream_t stream);
+cudaError_t launch_bwd_main_window(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                   const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParamsWin& p, int grid,
+                                   cudaStream_t stream);
 cudaError_t launch_fwd_varlen(int d, bool causal, const FwdMaps& m, const FwdParams& p, int grid,
                               cudaStream_t stream);
 cudaError_t launch_fwd_splitk(int d, bool fp8, bool causal, const FwdMaps& m, const FwdParams& p, int grid,

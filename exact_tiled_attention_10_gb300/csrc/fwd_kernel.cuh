@@ -146,18 +146,38 @@ struct ItemPacked : Item {
     int h, tb, seqlen;
 };
 
-template <bool VARLEN>
-using ItemT = typename std::conditional<VARLEN, ItemPacked, Item>::type;
+// Sliding window: each query tile has its own first key block, a[t] blocks
+// after the unit's first block j0 (the K / V stream covers the union of the
+// two tiles' ranges, which has no gaps).
+struct ItemWin : Item {
+    int a[2];
+};
+
+template <bool VARLEN, bool WINDOW = false>
+using ItemT = typename std::conditional<VARLEN, ItemPacked,
+                                        typename std::conditional<WINDOW, ItemWin, Item>::type>::type;
+
+template <bool WINDOW>
+using ParamsT = typename std::conditional<WINDOW, FwdParamsWin, FwdParams>::type;
 
 template <class IT>
 __host__ __device__ constexpr bool is_packed() { return std::is_same<IT, ItemPacked>::value; }
+template <class IT>
+__host__ __device__ constexpr bool is_window() { return std::is_same<IT, ItemWin>::value; }
+
+// First key block of tile t, relative to the unit's j0 (0 without a window).
+template <class IT>
+__device__ __forceinline__ int item_a(const IT& I, int t) {
+    if constexpr (is_window<IT>()) return t ? I.a[1] : I.a[0];
+    else return 0;
+}
 
 // Key blocks of tile t.  The packed instance reads the field with constant
 // indices (its larger item otherwise went to local memory); the others index
 // directly, which schedules better.
 template <class IT>
 __device__ __forceinline__ int item_n(const IT& I, int t) {
-    if constexpr (is_packed<IT>()) return t ? I.n[1] : I.n[0];
+    if constexpr (is_packed<IT>() || is_window<IT>()) return t ? I.n[1] : I.n[0];
     else return I.n[t];
 }
 
@@ -198,9 +218,10 @@ __device__ __forceinline__ size_t lse_index(const IT& I, int row, const FwdParam
 // SPLITK: the kernel instance that also runs split-key units (compiled
 // separately so that the plain forward carries none of their bookkeeping).
 // VARLEN: the instance for packed variable-length sequences.
-template <class C, bool CAUSAL, bool SPLITK, bool VARLEN>
-__device__ __forceinline__ ItemT<VARLEN> get_item(int unit, const FwdParams& p) {
-    ItemT<VARLEN> I;
+// WINDOW: the sliding-window instance (p is a FwdParamsWin).
+template <class C, bool CAUSAL, bool SPLITK, bool VARLEN, bool WINDOW = false>
+__device__ __forceinline__ ItemT<VARLEN, WINDOW> get_item(int unit, const ParamsT<WINDOW>& p) {
+    ItemT<VARLEN, WINDOW> I;
     const int BH = p.B * p.H;
     int it = unit, s = 0, S = 1;
     I.part = -1;
@@ -230,28 +251,59 @@ __device__ __forceinline__ ItemT<VARLEN> get_item(int unit, const FwdParams& p) 
     I.kvl = kvl;
     I.row0 = qp * (C::QT * C::BR);
     I.nmax = 0;
-#pragma unroll
-    for (int t = 0; t < 2; ++t) {
-        const int r0 = I.row0 + t * C::BR;
-        int n = 0;
-        if (r0 < rows) {
-            int cols = kvl;
-            if (CAUSAL) cols = min(cols, r0 + C::BR);
-            n = (cols + C::BC - 1) / C::BC;
-        }
-        I.n[t] = n;
-        I.nmax = max(I.nmax, n);
-    }
-    I.j0 = 0;
-    if (SPLITK && S > 1) {
-        const int j0 = (int)((long long)I.nmax * s / S), j1 = (int)((long long)I.nmax * (s + 1) / S);
-        I.nmax = 0;
+    if constexpr (WINDOW) {
+        // keys [lo, hi) cover every row of tile t: lo from its first row's left
+        // edge, hi from its last row's right edge (and kv_len / causal)
+        int lb[2], nb[2], J0 = 0x7fffffff, J1 = 0;
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
-            I.n[t] = max(0, min(j1, I.n[t]) - j0);
-            I.nmax = max(I.nmax, I.n[t]);
+            const int r0 = I.row0 + t * C::BR;
+            lb[t] = 0;
+            nb[t] = 0;
+            if (r0 < rows) {
+                const int rl = min(r0 + C::BR, rows) - 1;
+                int hi = kvl;
+                if (CAUSAL) hi = min(hi, rl + 1);
+                if (p.win_right >= 0) hi = min(hi, rl + p.win_right + 1);
+                const int lo = (p.win_left >= 0) ? max(0, r0 - p.win_left) : 0;
+                if (hi > lo) {
+                    lb[t] = lo / C::BC;
+                    nb[t] = (hi + C::BC - 1) / C::BC - lb[t];
+                    J0 = min(J0, lb[t]);
+                    J1 = max(J1, lb[t] + nb[t]);
+                }
+            }
         }
-        I.j0 = j0;
+        I.j0 = (J1 > 0) ? J0 : 0;
+        I.nmax = (J1 > 0) ? J1 - J0 : 0;
+        I.n[0] = nb[0];
+        I.n[1] = nb[1];
+        I.a[0] = nb[0] > 0 ? lb[0] - I.j0 : 0;
+        I.a[1] = nb[1] > 0 ? lb[1] - I.j0 : 0;
+    } else {
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            const int r0 = I.row0 + t * C::BR;
+            int n = 0;
+            if (r0 < rows) {
+                int cols = kvl;
+                if (CAUSAL) cols = min(cols, r0 + C::BR);
+                n = (cols + C::BC - 1) / C::BC;
+            }
+            I.n[t] = n;
+            I.nmax = max(I.nmax, n);
+        }
+        I.j0 = 0;
+        if (SPLITK && S > 1) {
+            const int j0 = (int)((long long)I.nmax * s / S), j1 = (int)((long long)I.nmax * (s + 1) / S);
+            I.nmax = 0;
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                I.n[t] = max(0, min(j1, I.n[t]) - j0);
+                I.nmax = max(I.nmax, I.n[t]);
+            }
+            I.j0 = j0;
+        }
     }
     return I;
 }
@@ -368,11 +420,11 @@ __device__ __forceinline__ void store_row_chunk(void* o_row, int c0, const float
     }
 }
 
-template <class C, bool CAUSAL, bool OUT_F32, bool SPLITK, bool VARLEN = false>
+template <class C, bool CAUSAL, bool OUT_F32, bool SPLITK, bool VARLEN = false, bool WINDOW = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tql,
-               const __grid_constant__ CUtensorMap tkl, const FwdParams p) {
+               const __grid_constant__ CUtensorMap tkl, const ParamsT<WINDOW> p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -436,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int rd = 0; rd < snake_rounds(p.num_units) && ok; ++rd) {
             const int it = snake_item(rd, p.num_units);
             if (it < 0) continue;
-            const auto I = get_item<C, CAUSAL, SPLITK, VARLEN>(it, p);
+            const auto I = get_item<C, CAUSAL, SPLITK, VARLEN, WINDOW>(it, p);
             if (I.nmax == 0) continue;
             // Q tile t of this item may load as soon as the previous item's last
             // S_t MMA has consumed the buffer (per-tile barriers), overlapping
@@ -509,7 +561,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int rd = 0; rd < snake_rounds(p.num_units) && ok; ++rd) {
             const int it = snake_item(rd, p.num_units);
             if (it < 0) continue;
-            const auto I = get_item<C, CAUSAL, SPLITK, VARLEN>(it, p);
+            const auto I = get_item<C, CAUSAL, SPLITK, VARLEN, WINDOW>(it, p);
             if (I.nmax == 0) continue;
             for (int t = 0; t < 2 && ok; ++t)
                 ok = wait_bounded_warp(BAR(C::B_QFULL + t), qph, abort_flag, p.err, kErrWaitFwdMma);
@@ -518,21 +570,36 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(ok = wait_bounded_warp(BAR(C::B_KFULL + kst), kph, abort_flag, p.err, kErrWaitFwdMma))) break;
             tc_fence_after();
             for (int t = 0; t < 2; ++t) {
-                if (item_n(I, t) > 0) {
-                    issue_S<C>(tS(t), q_desc(t), k_desc(kst));
-                    mma_commit_w(BAR(C::B_SFULL + t));
+                if (item_a(I, t) == 0) {  // (a tile that starts later issues its first S in the loop)
+                    if (item_n(I, t) > 0) {
+                        issue_S<C>(tS(t), q_desc(t), k_desc(kst));
+                        mma_commit_w(BAR(C::B_SFULL + t));
+                    }
+                    if (item_n(I, t) <= 1) mma_commit_w(BAR(C::B_QEMPTY + t));  // Q_t no longer needed
                 }
-                if (item_n(I, t) <= 1) mma_commit_w(BAR(C::B_QEMPTY + t));  // Q_t no longer needed
             }
             mma_commit_w(BAR(C::B_KEMPTY + kst));
             if (++kst == C::KSTAGES) { kst = 0; kph ^= 1; }
             for (int j = 0; j < I.nmax && ok; ++j) {
                 bool vw = false, kw = false;
                 for (int t = 0; t < 2; ++t) {
-                    if (j >= item_n(I, t)) continue;
+                    const int ta = item_a(I, t), te = ta + item_n(I, t);  // tile t: blocks [ta, te)
+                    if (j < ta || j >= te) {
+                        if (j + 1 == ta) {  // tile t starts with the next block: its first S
+                            if (!kw) {
+                                if (!(ok = wait_bounded_warp(BAR(C::B_KFULL + kst), kph, abort_flag, p.err, kErrWaitFwdMma))) break;
+                                kw = true;
+                                tc_fence_after();
+                            }
+                            issue_S<C>(tS(t), q_desc(t), k_desc(kst));
+                            mma_commit_w(BAR(C::B_SFULL + t));
+                            if (te - ta == 1) mma_commit_w(BAR(C::B_QEMPTY + t));
+                        }
+                        continue;
+                    }
                     if (!(ok = wait_bounded_warp(BAR(C::B_PFULL + t), pph[t], abort_flag, p.err, kErrWaitFwdMma))) break;
                     pph[t] ^= 1;
-                    if (j == 0) {
+                    if (j == ta) {
                         if (!(ok = wait_bounded_warp(BAR(C::B_OEMPTY + t), oeph[t] ^ 1, abort_flag, p.err, kErrWaitFwdMma))) break;
                         oeph[t] ^= 1;
                     }
@@ -541,8 +608,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         vw = true;
                     }
                     tc_fence_after();
-                    issue_PV<C>(tO(t), tS(t), v_desc(vst), j > 0);
-                    if (j == item_n(I, t) - 1) {
+                    issue_PV<C>(tO(t), tS(t), v_desc(vst), j > ta);
+                    if (j == te - 1) {
                         mma_commit_w(BAR(C::B_OFULL + t));
                     } else {
                         if (!kw) {
@@ -552,7 +619,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         issue_S<C>(tS(t), q_desc(t), k_desc(kst));
                         mma_commit_w(BAR(C::B_SFULL + t));
-                        if (j + 2 == item_n(I, t)) mma_commit_w(BAR(C::B_QEMPTY + t));  // last S_t issued
+                        if (j + 2 == te) mma_commit_w(BAR(C::B_QEMPTY + t));  // last S_t issued
                     }
                 }
                 if (!ok) break;
@@ -581,7 +648,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int rd = 0; rd < snake_rounds(p.num_units); ++rd) {
             const int it = snake_item(rd, p.num_units);
             if (it < 0) continue;
-            const auto I = get_item<C, CAUSAL, SPLITK, VARLEN>(it, p);
+            const auto I = get_item<C, CAUSAL, SPLITK, VARLEN, WINDOW>(it, p);
             const int n = item_n(I, t);
             const int tile_row0 = I.row0 + t * C::BR;
             const int row = tile_row0 + r_in;
@@ -633,7 +700,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto load_scales = [&](int jj) {
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    const int blk = (I.j0 + jj) * 2 + h;
+                    const int blk = (I.j0 + item_a(I, t) + jj) * 2 + h;
                     skn[h] = (blk < p.nblk) ? __ldg(p.sk + (size_t)I.kvh * p.nblk + blk) : 1.f;
                     svn[h] = (blk < p.nblk) ? __ldg(p.sv + (size_t)I.kvh * p.nblk + blk) : sv_max;
                 }
@@ -668,13 +735,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float s[C::BC];
 #pragma unroll
                 for (int c = 0; c < C::BC; ++c) s[c] = __uint_as_float(sr[c]);
-                const int col0 = (I.j0 + j) * C::BC;
-                const bool need_mask = (col0 + C::BC > I.kvl) || (CAUSAL && col0 + C::BC - 1 > tile_row0);
+                const int col0 = (I.j0 + item_a(I, t) + j) * C::BC;
+                bool need_mask = (col0 + C::BC > I.kvl) || (CAUSAL && col0 + C::BC - 1 > tile_row0);
+                if constexpr (WINDOW)  // blocks crossing some row's window edge
+                    need_mask = need_mask || (p.win_right >= 0 && col0 + C::BC - 1 > tile_row0 + p.win_right) ||
+                                (p.win_left >= 0 && col0 < tile_row0 + C::BR - 1 - p.win_left);
                 if (need_mask) {
 #pragma unroll
                     for (int c = 0; c < C::BC; ++c) {
                         const int col = col0 + c;
-                        if (col >= I.kvl || (CAUSAL && col > row)) s[c] = -INFINITY;
+                        bool off = col >= I.kvl || (CAUSAL && col > row);
+                        if constexpr (WINDOW)
+                            off = off || (p.win_right >= 0 && col > row + p.win_right) ||
+                                  (p.win_left >= 0 && col < row - p.win_left);
+                        if (off) s[c] = -INFINITY;
                     }
                 }
                 // O *= f over the row (O holds the blocks whose P V has completed)
@@ -769,13 +843,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <class C, bool CAUSAL, bool OUT_F32, bool SPLITK = false, bool VARLEN = false>
-cudaError_t launch(const FwdMaps& m, const FwdParams& p, int grid, cudaStream_t stream) {
-    auto kern = fwd_kernel<C, CAUSAL, OUT_F32, SPLITK, VARLEN>;
+template <class C, bool CAUSAL, bool OUT_F32, bool SPLITK = false, bool VARLEN = false, bool WINDOW = false>
+cudaError_t launch(const FwdMaps& m, const ParamsT<WINDOW>& p, int grid, cudaStream_t stream) {
+    auto kern = fwd_kernel<C, CAUSAL, OUT_F32, SPLITK, VARLEN, WINDOW>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     kern<<<grid, kThreads, C::SMEM, stream>>>(m.q, m.k, m.v, m.q_lo, m.k_lo, p);
     return cudaGetLastError();
+}
+
+// Sliding window (causal folded into the window's right edge by the caller).
+template <class C>
+cudaError_t launch_window(const FwdMaps& m, const FwdParamsWin& p, int grid, cudaStream_t s) {
+    return launch<C, false, false, false, false, true>(m, p, grid, s);
 }
 
 template <class C>

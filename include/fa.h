@@ -143,6 +143,19 @@ fa_status fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float
                      int B, int H, int Hkv, int N, int d, float scale, int causal,
                      const int* kv_lens, fa_stream_t stream);
 
+/* Sliding-window attention (flash_attn_func's window_size = (left, right),
+ * [CH18] §18.7.1; the block-skipping form of [CH18] §18.8.1), bf16, shapes
+ * as fa_fwd_gqa (Hkv = H for ordinary multi-head attention): key j is
+ * visible to query i only if i - window_left <= j <= i + window_right, -1
+ * meaning no bound on that side, on top of the causal (j <= i) and key
+ * padding masks.  Key blocks entirely outside a query tile's window are not
+ * loaded or multiplied.  A row with no visible key gets O = 0, LSE = -inf.
+ * FA_ERR_INVALID_ARG for an edge below -1; window (-1, -1) is fa_fwd_gqa. */
+fa_status fa_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse,
+                        int B, int H, int Hkv, int N, int d, float scale, int causal,
+                        int window_left, int window_right, const int* kv_lens,
+                        fa_stream_t stream);
+
 /* Packed variable-length sequences (flash_attn_varlen_func, [CH18] §18.7.1),
  * bf16: sequence b holds tokens cu_seqlens[b] .. cu_seqlens[b+1]-1 of the
  * token-major tensors q, o [total, H, d] and k, v [total, Hkv, d] (Hkv = H
@@ -183,6 +196,16 @@ fa_status fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o,
                      int B, int H, int Hkv, int N, int d, float scale, int causal,
                      const int* kv_lens, void* workspace, size_t workspace_bytes,
                      fa_stream_t stream);
+
+/* Backward of fa_fwd_window (same window and masks), bf16: dq [B,H,N,d];
+ * dk, dv [B,Hkv,N,d] summed over the query heads sharing a key/value head.
+ * Only query blocks inside some key's window are visited per key block.
+ * Workspace: fa_bwd_workspace_size(FA_BF16, B, H, N, d). */
+fa_status fa_bwd_window(const void* q, const void* k, const void* v, const void* o,
+                        const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                        int B, int H, int Hkv, int N, int d, float scale, int causal,
+                        int window_left, int window_right, const int* kv_lens,
+                        void* workspace, size_t workspace_bytes, fa_stream_t stream);
 
 /* Backward of fa_fwd_varlen (packed variable-length sequences, bf16): dq
  * [total, H, d], dk, dv [total, Hkv, d] (summed over the query heads sharing
