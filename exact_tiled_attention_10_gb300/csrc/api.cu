@@ -781,7 +781,7 @@ fa_status fa_quantize_fp8(const void* x_bf16, void* x_e4m3, float* scales, int B
     FA_CHECK_PTR(scales);
     DeviceInfo* dev = nullptr;
     FA_TRY(device_info(&dev));
-    cudaError_t e = fa::launch_quantize_fp8(x_bf16, x_e4m3, scales, B * H, N, d, dev->sms * 4, stream);
+    cudaError_t e = fa::launch_quantize_fp8(x_bf16, x_e4m3, scales, B * H, N, d, dev->sms * 8, stream);
     if (e != cudaSuccess) return cuda_fail(e, "quantiser launch");
     return FA_OK;
 }

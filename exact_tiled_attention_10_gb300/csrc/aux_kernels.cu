@@ -194,47 +194,58 @@ __global__ void __launch_bounds__(256) bwd_dq_varlen_kernel(const float* __restr
 }
 
 // One CTA (256 threads) per (head, 64-row block); d = 128 -> 8192 elements,
-// 32 per thread.  s = amax / 448 and x / s are IEEE float32 divisions; the
+// 32 per thread, read once and kept in registers across the block's absmax
+// reduction.  s = amax / 448 and x / s are IEEE float32 divisions; the
 // conversion rounds to nearest even and saturates to +-448.
 __global__ void __launch_bounds__(256) quantize_fp8_kernel(const __nv_bfloat16* __restrict__ x,
                                                            uint8_t* __restrict__ x8, float* __restrict__ scales,
                                                            int BH, int N, int D, int nblk) {
-    __shared__ float red[8];
+    constexpr int G = 4;  // uint4 groups (8 elements) per thread: 256 * 4 * 8 = 64 rows x 128
+    __shared__ float red[2][8];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int per_row = D / 8;  // uint4 groups per row
-    const int groups = 64 * per_row;
-    for (long blk = blockIdx.x; blk < (long)BH * nblk; blk += gridDim.x) {
+    int par = 0;
+    for (long blk = blockIdx.x; blk < (long)BH * nblk; blk += gridDim.x, par ^= 1) {
         const long bh = blk / nblk;
         const int ib = (int)(blk - bh * nblk);
         const int r0 = ib * 64;
         const int rows = min(64, N - r0);
         const size_t base = ((size_t)bh * N + r0) * D;
+        const int ng = rows * per_row;
+        uint4 raw[G];
+#pragma unroll
+        for (int i = 0; i < G; ++i) {
+            const int g = threadIdx.x + i * 256;
+            raw[i] = (g < ng) ? __ldg(reinterpret_cast<const uint4*>(x + base) + g) : make_uint4(0u, 0u, 0u, 0u);
+        }
         float amax = 0.f;
-        for (int g = threadIdx.x; g < rows * per_row; g += blockDim.x) {
+#pragma unroll
+        for (int i = 0; i < G; ++i) {
             float f[8];
-            unpack8(__ldg(reinterpret_cast<const uint4*>(x + base) + g), f);
+            unpack8(raw[i], f);
 #pragma unroll
             for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fabsf(f[k]));
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-        if (lane == 0) red[warp] = amax;
+        if (lane == 0) red[par][warp] = amax;  // double-buffered: no second barrier per block
         __syncthreads();
-        float m = red[0];
+        float m = red[par][0];
 #pragma unroll
-        for (int w = 1; w < 8; ++w) m = fmaxf(m, red[w]);
+        for (int w = 1; w < 8; ++w) m = fmaxf(m, red[par][w]);
         const float s = (m > 0.f) ? __fdiv_rn(m, 448.f) : 1.f;
         if (threadIdx.x == 0) scales[blk] = s;
-        for (int g = threadIdx.x; g < rows * per_row; g += blockDim.x) {
+#pragma unroll
+        for (int i = 0; i < G; ++i) {
+            const int g = threadIdx.x + i * 256;
+            if (g >= ng) continue;
             float f[8];
-            unpack8(__ldg(reinterpret_cast<const uint4*>(x + base) + g), f);
+            unpack8(raw[i], f);
             uint2 out;
             out.x = pack_e4m3x4(__fdiv_rn(f[0], s), __fdiv_rn(f[1], s), __fdiv_rn(f[2], s), __fdiv_rn(f[3], s));
             out.y = pack_e4m3x4(__fdiv_rn(f[4], s), __fdiv_rn(f[5], s), __fdiv_rn(f[6], s), __fdiv_rn(f[7], s));
             reinterpret_cast<uint2*>(x8 + base)[g] = out;
         }
-        __syncthreads();  // red[] is reused by the next block
-        (void)groups;
     }
 }
 
