@@ -24,6 +24,12 @@ Entry points and what pins each one (tests/test_oracle_*.py):
   closed form (each query sees only its own key: O_i = v_i, LSE_i = S_ii,
   dQ = dK = 0, dV_i = dO_i), window (-1, 0) equal to the causal mask,
   windows wider than N equal to no window, and central finite differences.
+* the block-sparse mask (``block_mask`` [nb][nb] of 0/1 over block_size
+  blocks, chapter 18 §18.8.1).  Pinned by: float64 autograd with the mask
+  expanded to elements by a Kronecker product, the all-ones mask equal to no
+  mask, the block-diagonal mask equal to independent attention on each block
+  (separate oracle calls on the slices), a row of blocks with no entry giving
+  O = 0 / LSE = -inf / zero gradients, and central finite differences.
 * ``tiled_fwd`` / ``tiled_bwd`` -- Algorithms 1 and 2 of the FA-v2 analysis
   page (§4, §5.4) with arbitrary Br/Bc.  Pinned against ``fwd`` / ``bwd`` on
   the pages' worked shapes (N=4,d=3,Br=Bc=2; the 5-position example with 2x2
@@ -74,14 +80,14 @@ def _load():
             build()
             lib = ctypes.CDLL(_LIB)
             _i = ctypes.c_int
-            lib.oracle_fwd_win.argtypes = [_dp, _dp, _dp, _dp, _dp, _i, _i, _i, _i, ctypes.c_double,
-                                           _i, _i, _i, _ip, _i]
-            lib.oracle_bwd_win.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp,
-                                           _i, _i, _i, _i, ctypes.c_double, _i, _i, _i, _ip, _i]
-            lib.oracle_fwd_rows_win.argtypes = [_dp, _dp, _dp, _i, _i, ctypes.c_double, _i, _i, _i, _i,
-                                                _ip, _i, _dp, _dp]
-            lib.oracle_bwd_rows_win.argtypes = [_dp, _dp, _dp, _dp, _i, _i, ctypes.c_double, _i, _i, _i,
-                                                _i, _ip, _i, _dp, _ip, _i, _dp, _dp, _dp, _dp, _i]
+            lib.oracle_fwd_mask.argtypes = [_dp, _dp, _dp, _dp, _dp, _i, _i, _i, _i, ctypes.c_double,
+                                            _i, _i, _i, _u8p, _i, _ip, _i]
+            lib.oracle_bwd_mask.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp,
+                                            _i, _i, _i, _i, ctypes.c_double, _i, _i, _i, _u8p, _i, _ip, _i]
+            lib.oracle_fwd_rows_mask.argtypes = [_dp, _dp, _dp, _i, _i, ctypes.c_double, _i, _i, _i, _i,
+                                                 _u8p, _i, _ip, _i, _dp, _dp]
+            lib.oracle_bwd_rows_mask.argtypes = [_dp, _dp, _dp, _dp, _i, _i, ctypes.c_double, _i, _i, _i,
+                                                 _i, _u8p, _i, _ip, _i, _dp, _ip, _i, _dp, _dp, _dp, _dp, _i]
             lib.oracle_tiled_fwd.argtypes = [_dp, _dp, _dp, _dp, _dp, ctypes.c_int, ctypes.c_int,
                                              ctypes.c_int, ctypes.c_int, ctypes.c_double,
                                              ctypes.c_int, _ip, ctypes.c_int, ctypes.c_int,
@@ -128,28 +134,45 @@ def _win(window):
     return (-1 if wl is None or wl < 0 else int(wl)), (-1 if wr is None or wr < 0 else int(wr))
 
 
+def _bm(block_mask, block_size, N):
+    """(array, pointer, block size) of a 0/1 block mask [ceil(N/bs)][ceil(N/bs)]."""
+    if block_mask is None:
+        return None, None, 0
+    bs = int(block_size)
+    nb = (N + bs - 1) // bs
+    arr = np.ascontiguousarray(np.asarray(block_mask, dtype=np.uint8) != 0, dtype=np.uint8)
+    assert arr.shape == (nb, nb), (arr.shape, nb)
+    return arr, _ptr(arr, _u8p), bs
+
+
 def default_threads() -> int:
     return int(_load().oracle_default_threads())
 
 
-def fwd(q, k, v, scale, causal=False, kv_lens=None, nthreads=0, window=None):
+def fwd(q, k, v, scale, causal=False, kv_lens=None, nthreads=0, window=None, block_mask=None,
+        block_size=128):
     """Materialised forward. q,k,v: [B,H,N,d]. Returns (O [B,H,N,d], LSE [B,H,N]) fp64.
 
     window = (left, right): key j is visible to query i only if
-    i - left <= j <= i + right (chapter 18 §18.7.1 window_size; -1 = unbounded)."""
+    i - left <= j <= i + right (chapter 18 §18.7.1 window_size; -1 = unbounded).
+    block_mask: 0/1 [nb][nb] over block_size x block_size blocks; key j is
+    visible to query i only if block_mask[i // bs][j // bs] (§18.8.1)."""
     lib = _load()
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, H, N, d = q.shape
     o = np.zeros_like(q)
     lse = np.zeros((B, H, N))
     kv, kvp = _kv(kv_lens, B)
-    rc = lib.oracle_fwd_win(_ptr(q, _dp), _ptr(k, _dp), _ptr(v, _dp), _ptr(o, _dp), _ptr(lse, _dp),
-                            B, H, N, d, float(scale), int(bool(causal)), *_win(window), kvp, int(nthreads))
+    bma, bmp, bs = _bm(block_mask, block_size, N)
+    rc = lib.oracle_fwd_mask(_ptr(q, _dp), _ptr(k, _dp), _ptr(v, _dp), _ptr(o, _dp), _ptr(lse, _dp),
+                             B, H, N, d, float(scale), int(bool(causal)), *_win(window), bmp, bs, kvp,
+                             int(nthreads))
     assert rc == 0
     return o, lse
 
 
-def bwd(q, k, v, dout, scale, causal=False, kv_lens=None, nthreads=0, window=None):
+def bwd(q, k, v, dout, scale, causal=False, kv_lens=None, nthreads=0, window=None, block_mask=None,
+        block_size=128):
     """Materialised backward of L = sum(O*dO).
 
     Returns dict with o, lse, dq, dk, dv, D (D by its definition sum_j P dP)."""
@@ -160,15 +183,17 @@ def bwd(q, k, v, dout, scale, causal=False, kv_lens=None, nthreads=0, window=Non
     lse = np.zeros((B, H, N))
     D = np.zeros((B, H, N))
     kv, kvp = _kv(kv_lens, B)
-    rc = lib.oracle_bwd_win(_ptr(q, _dp), _ptr(k, _dp), _ptr(v, _dp), _ptr(dout, _dp), _ptr(o, _dp),
-                            _ptr(lse, _dp), _ptr(dq, _dp), _ptr(dk, _dp), _ptr(dv, _dp),
-                            _ptr(D, _dp), B, H, N, d, float(scale), int(bool(causal)), *_win(window),
-                            kvp, int(nthreads))
+    bma, bmp, bs = _bm(block_mask, block_size, N)
+    rc = lib.oracle_bwd_mask(_ptr(q, _dp), _ptr(k, _dp), _ptr(v, _dp), _ptr(dout, _dp), _ptr(o, _dp),
+                             _ptr(lse, _dp), _ptr(dq, _dp), _ptr(dk, _dp), _ptr(dv, _dp),
+                             _ptr(D, _dp), B, H, N, d, float(scale), int(bool(causal)), *_win(window),
+                             bmp, bs, kvp, int(nthreads))
     assert rc == 0
     return dict(o=o, lse=lse, dq=dq, dk=dk, dv=dv, D=D)
 
 
-def fwd_rows(q_head, k_head, v_head, scale, causal, kv_len, rows, window=None):
+def fwd_rows(q_head, k_head, v_head, scale, causal, kv_len, rows, window=None, block_mask=None,
+             block_size=128):
     """Row-sampled forward of ONE head ([N,d] inputs). Returns (O_rows, LSE_rows)."""
     lib = _load()
     q, k, v = _f64(q_head), _f64(k_head), _f64(v_head)
@@ -176,15 +201,16 @@ def fwd_rows(q_head, k_head, v_head, scale, causal, kv_len, rows, window=None):
     rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int32))
     o = np.zeros((len(rows), d))
     lse = np.zeros(len(rows))
-    rc = lib.oracle_fwd_rows_win(_ptr(q, _dp), _ptr(k, _dp), _ptr(v, _dp), N, d, float(scale),
-                                 int(bool(causal)), int(kv_len), *_win(window), _ptr(rows, _ip),
-                                 len(rows), _ptr(o, _dp), _ptr(lse, _dp))
+    bma, bmp, bs = _bm(block_mask, block_size, N)
+    rc = lib.oracle_fwd_rows_mask(_ptr(q, _dp), _ptr(k, _dp), _ptr(v, _dp), N, d, float(scale),
+                                  int(bool(causal)), int(kv_len), *_win(window), bmp, bs, _ptr(rows, _ip),
+                                  len(rows), _ptr(o, _dp), _ptr(lse, _dp))
     assert rc == 0
     return o, lse
 
 
 def bwd_rows(q_head, k_head, v_head, dout_head, scale, causal, kv_len, rows, keys, nthreads=0,
-             window=None):
+             window=None, block_mask=None, block_size=128):
     """Row-sampled backward of ONE head. Returns dict dq (rows), dk, dv (keys), lse, D (all rows)."""
     lib = _load()
     q, k, v, g = _f64(q_head), _f64(k_head), _f64(v_head), _f64(dout_head)
@@ -196,11 +222,12 @@ def bwd_rows(q_head, k_head, v_head, dout_head, scale, causal, kv_len, rows, key
     dv = np.zeros((max(len(keys), 1), d))
     lse = np.zeros(N)
     D = np.zeros(N)
-    rc = lib.oracle_bwd_rows_win(_ptr(q, _dp), _ptr(k, _dp), _ptr(v, _dp), _ptr(g, _dp), N, d,
-                                 float(scale), int(bool(causal)), int(kv_len), *_win(window),
-                                 _ptr(rows, _ip), len(rows), _ptr(dq, _dp), _ptr(keys, _ip), len(keys),
-                                 _ptr(dk, _dp), _ptr(dv, _dp), _ptr(lse, _dp), _ptr(D, _dp),
-                                 int(nthreads))
+    bma, bmp, bs = _bm(block_mask, block_size, N)
+    rc = lib.oracle_bwd_rows_mask(_ptr(q, _dp), _ptr(k, _dp), _ptr(v, _dp), _ptr(g, _dp), N, d,
+                                  float(scale), int(bool(causal)), int(kv_len), *_win(window), bmp, bs,
+                                  _ptr(rows, _ip), len(rows), _ptr(dq, _dp), _ptr(keys, _ip), len(keys),
+                                  _ptr(dk, _dp), _ptr(dv, _dp), _ptr(lse, _dp), _ptr(D, _dp),
+                                  int(nthreads))
     assert rc == 0
     return dict(dq=dq, dk=dk[:len(keys)], dv=dv[:len(keys)], lse=lse, D=D)
 

@@ -23,7 +23,11 @@
  *     (wl < 0 or j >= i - wl)  and  (wr < 0 or j <= i + wr)
  *     -- causal mask M_ij = -inf for j > i ([CH18] §18.2.2 eq. for M_ij);
  *        padding mask removes columns ([CH18] §18.2.2 Table 18-3).
- *   Entry points without "_win" have no window (wl = wr = -1).
+ *     and, for a block-sparse mask ([CH18] §18.8.1: per query block the list
+ *     of key blocks to compute; here a dense 0/1 matrix bm [nqb][nkb] of
+ *     bs x bs blocks), bm[i / bs][j / bs] != 0.
+ *   Entry points without "_win" / "_mask" have no window (wl = wr = -1) and
+ *   no block mask.
  *   S = scale * Q K^T ([CH18] §18.2.2; [WIKI] §04 "S = QK^T/sqrt(d)").
  *   A row with no visible key has O = 0, LSE = -inf and zero gradients
  *   ([WIKI] §04, the explicit fully-masked-row convention).
@@ -41,12 +45,26 @@
 #define OR_OK 0
 #define OR_ERR 1
 
-static int visible(int i, int j, int kv_len, int causal, int wl, int wr) {
-    if (j >= kv_len) return 0;
-    if (causal && j > i) return 0;
-    if (wl >= 0 && j < i - wl) return 0;
-    if (wr >= 0 && j > i + wr) return 0;
+/* Which keys a query sees: key-padding length, causal flag, window edges,
+ * optional block mask (bm NULL = none). */
+typedef struct {
+    int kv_len, causal, wl, wr;
+    const unsigned char* bm;
+    int bs, nkb;
+} mask_t;
+
+static int visible(int i, int j, const mask_t* m) {
+    if (j >= m->kv_len) return 0;
+    if (m->causal && j > i) return 0;
+    if (m->wl >= 0 && j < i - m->wl) return 0;
+    if (m->wr >= 0 && j > i + m->wr) return 0;
+    if (m->bm && !m->bm[(size_t)(i / m->bs) * m->nkb + j / m->bs]) return 0;
     return 1;
+}
+
+static mask_t make_mask(int kv_len, int causal, int wl, int wr, const unsigned char* bm, int bs, int nkb) {
+    mask_t m = {kv_len, causal, wl, wr, bm, bs, nkb};
+    return m;
 }
 
 static int kvlen_of(const int* kv_lens, int b, int N) {
@@ -116,11 +134,11 @@ static void run_items(item_fn fn, void* arg, long n_items, int nthreads) {
  * LSE.  Returns nothing; S and P are caller scratch. */
 static void naive_head_forward(const double* q, const double* k, const double* v,
                                double* o, double* lse, double* S, double* P,
-                               int N, int d, double scale, int causal, int kv_len, int wl, int wr) {
+                               int N, int d, double scale, const mask_t* mk) {
     for (int i = 0; i < N; ++i) {
         for (int j = 0; j < N; ++j) {
             double s = -INFINITY;
-            if (visible(i, j, kv_len, causal, wl, wr)) {
+            if (visible(i, j, mk)) {
                 double acc = 0.0;
                 for (int t = 0; t < d; ++t) acc += q[(size_t)i * d + t] * k[(size_t)j * d + t];
                 s = scale * acc;
@@ -157,10 +175,17 @@ static void naive_head_forward(const double* q, const double* k, const double* v
 typedef struct {
     const double *q, *k, *v, *dout;
     double *o, *lse, *dq, *dk, *dv, *Dout;
-    int B, H, N, d, causal, wl, wr;
+    int B, H, N, d;
+    mask_t mk; /* kv_len filled per batch item */
     double scale;
     const int* kv_lens;
 } naive_args;
+
+static mask_t mask_of(const naive_args* a, int b) {
+    mask_t m = a->mk;
+    m.kv_len = kvlen_of(a->kv_lens, b, a->N);
+    return m;
+}
 
 static void naive_fwd_item(void* a_, long bh) {
     naive_args* a = (naive_args*)a_;
@@ -169,18 +194,21 @@ static void naive_fwd_item(void* a_, long bh) {
     int b = (int)(bh / a->H);
     double* S = (double*)malloc(sizeof(double) * N * N);
     double* P = (double*)malloc(sizeof(double) * N * N);
+    const mask_t mk = mask_of(a, b);
     naive_head_forward(a->q + off, a->k + off, a->v + off, a->o + off, a->lse + (size_t)bh * N, S, P,
-                       a->N, a->d, a->scale, a->causal, kvlen_of(a->kv_lens, b, a->N), a->wl, a->wr);
+                       a->N, a->d, a->scale, &mk);
     free(S);
     free(P);
 }
 
-/* Forward: O = softmax(scale Q K^T + M) V and LSE, materialising S and P. */
-int oracle_fwd_win(const double* q, const double* k, const double* v, double* o, double* lse,
-                   int B, int H, int N, int d, double scale, int causal, int wl, int wr,
-                   const int* kv_lens, int nthreads) {
-    if (B <= 0 || H <= 0 || N <= 0 || d <= 0) return OR_ERR;
-    naive_args a = {q, k, v, NULL, o, lse, NULL, NULL, NULL, NULL, B, H, N, d, causal, wl, wr, scale, kv_lens};
+/* Forward: O = softmax(scale Q K^T + M) V and LSE, materialising S and P.
+ * bm: optional block mask [ceil(N/bs)][nkb], nkb = ceil(N/bs). */
+int oracle_fwd_mask(const double* q, const double* k, const double* v, double* o, double* lse,
+                    int B, int H, int N, int d, double scale, int causal, int wl, int wr,
+                    const unsigned char* bm, int bs, const int* kv_lens, int nthreads) {
+    if (B <= 0 || H <= 0 || N <= 0 || d <= 0 || (bm && bs <= 0)) return OR_ERR;
+    naive_args a = {q, k, v, NULL, o, lse, NULL, NULL, NULL, NULL, B, H, N, d,
+                    make_mask(N, causal, wl, wr, bm, bs, bm ? (N + bs - 1) / bs : 0), scale, kv_lens};
     run_items(naive_fwd_item, &a, (long)B * H, nthreads);
     return OR_OK;
 }
@@ -188,7 +216,7 @@ int oracle_fwd_win(const double* q, const double* k, const double* v, double* o,
 int oracle_fwd(const double* q, const double* k, const double* v, double* o, double* lse,
                int B, int H, int N, int d, double scale, int causal, const int* kv_lens,
                int nthreads) {
-    return oracle_fwd_win(q, k, v, o, lse, B, H, N, d, scale, causal, -1, -1, kv_lens, nthreads);
+    return oracle_fwd_mask(q, k, v, o, lse, B, H, N, d, scale, causal, -1, -1, NULL, 0, kv_lens, nthreads);
 }
 
 /* Backward of L = sum(O * dO) for one head, by the definitions of
@@ -208,8 +236,8 @@ static void naive_bwd_item(void* a_, long bh) {
     double* P = (double*)malloc(sizeof(double) * (size_t)N * N);
     double* dP = (double*)malloc(sizeof(double) * (size_t)N * N);
     double* D = (double*)malloc(sizeof(double) * (size_t)N);
-    naive_head_forward(q, k, v, o, lse, S, P, N, d, a->scale, a->causal, kvlen_of(a->kv_lens, b, N), a->wl,
-                       a->wr);
+    const mask_t mk = mask_of(a, b);
+    naive_head_forward(q, k, v, o, lse, S, P, N, d, a->scale, &mk);
     /* dP = dO V^T */
     for (int i = 0; i < N; ++i)
         for (int j = 0; j < N; ++j) {
@@ -253,12 +281,13 @@ static void naive_bwd_item(void* a_, long bh) {
 }
 
 /* Backward (also returns the forward O, LSE and, if D_out != NULL, D). */
-int oracle_bwd_win(const double* q, const double* k, const double* v, const double* dout,
-                   double* o, double* lse, double* dq, double* dk, double* dv, double* D_out,
-                   int B, int H, int N, int d, double scale, int causal, int wl, int wr,
-                   const int* kv_lens, int nthreads) {
-    if (B <= 0 || H <= 0 || N <= 0 || d <= 0) return OR_ERR;
-    naive_args a = {q, k, v, dout, o, lse, dq, dk, dv, D_out, B, H, N, d, causal, wl, wr, scale, kv_lens};
+int oracle_bwd_mask(const double* q, const double* k, const double* v, const double* dout,
+                    double* o, double* lse, double* dq, double* dk, double* dv, double* D_out,
+                    int B, int H, int N, int d, double scale, int causal, int wl, int wr,
+                    const unsigned char* bm, int bs, const int* kv_lens, int nthreads) {
+    if (B <= 0 || H <= 0 || N <= 0 || d <= 0 || (bm && bs <= 0)) return OR_ERR;
+    naive_args a = {q, k, v, dout, o, lse, dq, dk, dv, D_out, B, H, N, d,
+                    make_mask(N, causal, wl, wr, bm, bs, bm ? (N + bs - 1) / bs : 0), scale, kv_lens};
     run_items(naive_bwd_item, &a, (long)B * H, nthreads);
     return OR_OK;
 }
@@ -267,8 +296,8 @@ int oracle_bwd(const double* q, const double* k, const double* v, const double* 
                double* o, double* lse, double* dq, double* dk, double* dv, double* D_out,
                int B, int H, int N, int d, double scale, int causal, const int* kv_lens,
                int nthreads) {
-    return oracle_bwd_win(q, k, v, dout, o, lse, dq, dk, dv, D_out, B, H, N, d, scale, causal, -1, -1,
-                          kv_lens, nthreads);
+    return oracle_bwd_mask(q, k, v, dout, o, lse, dq, dk, dv, D_out, B, H, N, d, scale, causal, -1, -1, NULL, 0,
+                           kv_lens, nthreads);
 }
 
 /* ======================================================================== */
@@ -278,12 +307,13 @@ int oracle_bwd(const double* q, const double* k, const double* v, const double* 
 
 /* O and LSE of selected query rows of one head (definition applied row by
  * row: the row's scores, its safe-softmax LSE, then P V). */
-int oracle_fwd_rows_win(const double* q, const double* k, const double* v, int N, int d, double scale,
-                        int causal, int kv_len, int wl, int wr, const int* rows, int nrows,
-                        double* o_rows, double* lse_rows) {
-    if (N <= 0 || d <= 0) return OR_ERR;
+int oracle_fwd_rows_mask(const double* q, const double* k, const double* v, int N, int d, double scale,
+                         int causal, int kv_len, int wl, int wr, const unsigned char* bm, int bs,
+                         const int* rows, int nrows, double* o_rows, double* lse_rows) {
+    if (N <= 0 || d <= 0 || (bm && bs <= 0)) return OR_ERR;
     if (kv_len < 0) kv_len = 0;
     if (kv_len > N) kv_len = N;
+    const mask_t mk = make_mask(kv_len, causal, wl, wr, bm, bs, bm ? (N + bs - 1) / bs : 0);
     double* s = (double*)malloc(sizeof(double) * (size_t)N);
     for (int r = 0; r < nrows; ++r) {
         int i = rows[r];
@@ -291,7 +321,7 @@ int oracle_fwd_rows_win(const double* q, const double* k, const double* v, int N
         double mx = -INFINITY;
         for (int j = 0; j < N; ++j) {
             s[j] = -INFINITY;
-            if (visible(i, j, kv_len, causal, wl, wr)) {
+            if (visible(i, j, &mk)) {
                 double acc = 0.0;
                 for (int t = 0; t < d; ++t) acc += q[(size_t)i * d + t] * k[(size_t)j * d + t];
                 s[j] = scale * acc;
@@ -322,12 +352,14 @@ int oracle_fwd_rows_win(const double* q, const double* k, const double* v, int N
 int oracle_fwd_rows(const double* q, const double* k, const double* v, int N, int d, double scale,
                     int causal, int kv_len, const int* rows, int nrows, double* o_rows,
                     double* lse_rows) {
-    return oracle_fwd_rows_win(q, k, v, N, d, scale, causal, kv_len, -1, -1, rows, nrows, o_rows, lse_rows);
+    return oracle_fwd_rows_mask(q, k, v, N, d, scale, causal, kv_len, -1, -1, NULL, 0, rows, nrows, o_rows,
+                                lse_rows);
 }
 
 typedef struct {
     const double *q, *k, *v, *dout;
-    int N, d, causal, kv_len, wl, wr;
+    int N, d;
+    mask_t mk;
     double scale;
     double *lse, *D; /* [N] each, filled per row */
 } rowstat_args;
@@ -340,7 +372,7 @@ static void rowstat_item(void* a_, long i_) {
     double mx = -INFINITY;
     for (int j = 0; j < N; ++j) {
         s[j] = -INFINITY;
-        if (visible(i, j, a->kv_len, a->causal, a->wl, a->wr)) {
+        if (visible(i, j, &a->mk)) {
             double acc = 0.0;
             for (int t = 0; t < d; ++t) acc += a->q[(size_t)i * d + t] * a->k[(size_t)j * d + t];
             s[j] = a->scale * acc;
@@ -389,7 +421,7 @@ static void keygrad_item(void* a_, long c) {
     for (int r = 0; r < ka->nkeys; ++r) {
         int j = ka->keys[r];
         for (int i = i0; i < i1; ++i) {
-            if (!visible(i, j, a->kv_len, a->causal, a->wl, a->wr) || a->lse[i] == -INFINITY) continue;
+            if (!visible(i, j, &a->mk) || a->lse[i] == -INFINITY) continue;
             double acc = 0.0;
             for (int t = 0; t < d; ++t) acc += a->q[(size_t)i * d + t] * a->k[(size_t)j * d + t];
             double p = exp(a->scale * acc - a->lse[i]);
@@ -408,16 +440,18 @@ static void keygrad_item(void* a_, long c) {
  * LSE and D of every query row come from their definitions (rowstat_item),
  * then dQ_i = scale sum_j dS_ij k_j and dK_j = scale sum_i dS_ij q_i,
  * dV_j = sum_i P_ij dO_i.  Optionally returns the full-head LSE and D. */
-int oracle_bwd_rows_win(const double* q, const double* k, const double* v, const double* dout, int N,
-                        int d, double scale, int causal, int kv_len, int wl, int wr, const int* rows,
-                        int nrows, double* dq_rows, const int* keys, int nkeys, double* dk_rows,
-                        double* dv_rows, double* lse_all, double* D_all, int nthreads) {
-    if (N <= 0 || d <= 0) return OR_ERR;
+int oracle_bwd_rows_mask(const double* q, const double* k, const double* v, const double* dout, int N,
+                         int d, double scale, int causal, int kv_len, int wl, int wr,
+                         const unsigned char* bm, int bs, const int* rows, int nrows, double* dq_rows,
+                         const int* keys, int nkeys, double* dk_rows, double* dv_rows, double* lse_all,
+                         double* D_all, int nthreads) {
+    if (N <= 0 || d <= 0 || (bm && bs <= 0)) return OR_ERR;
     if (kv_len < 0) kv_len = 0;
     if (kv_len > N) kv_len = N;
     double* lse = lse_all ? lse_all : (double*)malloc(sizeof(double) * (size_t)N);
     double* D = D_all ? D_all : (double*)malloc(sizeof(double) * (size_t)N);
-    rowstat_args rs = {q, k, v, dout, N, d, causal, kv_len, wl, wr, scale, lse, D};
+    rowstat_args rs = {q, k, v, dout, N, d, make_mask(kv_len, causal, wl, wr, bm, bs, bm ? (N + bs - 1) / bs : 0),
+                       scale, lse, D};
     run_items(rowstat_item, &rs, N, nthreads);
     for (int r = 0; r < nrows; ++r) {
         int i = rows[r];
@@ -425,7 +459,7 @@ int oracle_bwd_rows_win(const double* q, const double* k, const double* v, const
         for (int t = 0; t < d; ++t) g[t] = 0.0;
         if (lse[i] == -INFINITY) continue;
         for (int j = 0; j < N; ++j) {
-            if (!visible(i, j, kv_len, causal, wl, wr)) continue;
+            if (!visible(i, j, &rs.mk)) continue;
             double acc = 0.0;
             for (int t = 0; t < d; ++t) acc += q[(size_t)i * d + t] * k[(size_t)j * d + t];
             double p = exp(scale * acc - lse[i]);
@@ -467,8 +501,8 @@ int oracle_bwd_rows(const double* q, const double* k, const double* v, const dou
                     int d, double scale, int causal, int kv_len, const int* rows, int nrows,
                     double* dq_rows, const int* keys, int nkeys, double* dk_rows, double* dv_rows,
                     double* lse_all, double* D_all, int nthreads) {
-    return oracle_bwd_rows_win(q, k, v, dout, N, d, scale, causal, kv_len, -1, -1, rows, nrows, dq_rows, keys,
-                               nkeys, dk_rows, dv_rows, lse_all, D_all, nthreads);
+    return oracle_bwd_rows_mask(q, k, v, dout, N, d, scale, causal, kv_len, -1, -1, NULL, 0, rows, nrows, dq_rows,
+                                keys, nkeys, dk_rows, dv_rows, lse_all, D_all, nthreads);
 }
 
 /* ======================================================================== */
