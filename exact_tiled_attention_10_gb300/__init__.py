@@ -21,7 +21,8 @@ from typing import Optional, Tuple
 
 import torch
 
-__all__ = ["forward", "forward_split", "forward_varlen", "backward_varlen", "backward", "quantize_fp8", "forward_fp8", "forward_fp8_split",
+__all__ = ["forward", "forward_split", "forward_varlen", "backward_varlen", "backward",
+           "block_lists", "forward_block_sparse", "backward_block_sparse", "quantize_fp8", "forward_fp8", "forward_fp8_split",
            "split_count", "split_workspace_size", "check_device_status",
            "selftest_wait_timeout",
            "bwd_workspace_size", "fwd_workspace_size", "library_path", "load_library", "FAError"]
@@ -59,6 +60,9 @@ _SIGS = {
     "fa_fwd_gqa": ([_vp] * 5 + [_i, _i, _i, _i, _i, _f, _i, _vp, _vp], _i),
     "fa_fwd_window": ([_vp] * 5 + [_i, _i, _i, _i, _i, _f, _i, _i, _i, _vp, _vp], _i),
     "fa_bwd_window": ([_vp] * 9 + [_i, _i, _i, _i, _i, _f, _i, _i, _i, _vp, _vp, _sz, _vp], _i),
+    "fa_fwd_block_sparse": ([_vp] * 5 + [_i, _i, _i, _i, _i, _f, _i, _vp, _vp, _vp, _vp], _i),
+    "fa_bwd_block_sparse_workspace_size": ([_i] * 4, _sz),
+    "fa_bwd_block_sparse": ([_vp] * 9 + [_i, _i, _i, _i, _i, _f, _i, _vp, _vp, _vp, _vp, _sz, _vp], _i),
     "fa_fwd_varlen": ([_vp] * 6 + [_i, _i, _i, _i, _i, _i, _f, _i, _vp], _i),
     "fa_bwd_varlen_workspace_size": ([_i] * 4, _sz),
     "fa_bwd_varlen": ([_vp] * 10 + [_i, _i, _i, _i, _i, _i, _f, _i, _vp, _sz, _vp], _i),
@@ -238,6 +242,62 @@ def forward_split(q, k, v, causal: bool = False, scale: Optional[float] = None, 
     _check(lib.fa_fwd_split(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(l), B, H, N, d, scale,
                             int(bool(causal)), _ptr(kv), int(num_splits), wsp, wsz, _stream(q)))
     return o, l
+
+
+def block_lists(block_mask, device) -> Tuple[torch.Tensor, torch.Tensor]:
+    """(row_ptr, col_idx) int32 device tensors of a 0/1 block mask
+    [nb][nb] (query block x key block, 128 x 128 blocks)."""
+    bm = torch.as_tensor(block_mask).to("cpu").bool()
+    if bm.dim() != 2 or bm.shape[0] != bm.shape[1]:
+        raise ValueError("block_mask must be a square [nb, nb] matrix")
+    counts = bm.sum(dim=1).to(torch.int32)
+    row_ptr = torch.zeros(bm.shape[0] + 1, dtype=torch.int32)
+    row_ptr[1:] = torch.cumsum(counts, 0)
+    col_idx = bm.nonzero()[:, 1].to(torch.int32)  # row-major: ascending within each row
+    return row_ptr.to(device), col_idx.to(device)
+
+
+def forward_block_sparse(q, k, v, row_ptr, col_idx, causal: bool = False, scale: Optional[float] = None,
+                         kv_lens=None, out: Optional[torch.Tensor] = None,
+                         lse: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Block-sparse forward (128 x 128 blocks): query block i attends to the
+    key blocks col_idx[row_ptr[i]:row_ptr[i+1]] only (see block_lists)."""
+    lib = load_library()
+    _need_cuda(q, k, v, row_ptr, col_idx)
+    B, H, N, d = q.shape
+    Hkv = k.shape[1]
+    if q.dtype != torch.bfloat16 or k.shape != (B, Hkv, N, d) or v.shape != k.shape or H % Hkv != 0:
+        raise ValueError("q [B,H,N,d]; k, v [B,Hkv,N,d] bfloat16 with H a multiple of Hkv")
+    if row_ptr.dtype != torch.int32 or col_idx.dtype != torch.int32 or row_ptr.numel() != (N + 127) // 128 + 1:
+        raise ValueError("row_ptr int32 [ceil(N/128) + 1], col_idx int32")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    kv = _kv(kv_lens, B, q.device)
+    o = torch.empty_like(q) if out is None else out
+    l = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check(lib.fa_fwd_block_sparse(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(l), B, H, Hkv, N, d, scale,
+                                   int(bool(causal)), _ptr(row_ptr), _ptr(col_idx), _ptr(kv), _stream(q)))
+    return o, l
+
+
+def backward_block_sparse(q, k, v, o, lse, dout, row_ptr, col_idx, causal: bool = False,
+                          scale: Optional[float] = None, kv_lens=None, workspace: Optional[torch.Tensor] = None):
+    """Backward of forward_block_sparse: dQ [B,H,N,d], dK, dV [B,Hkv,N,d]."""
+    lib = load_library()
+    _need_cuda(q, k, v, o, lse, dout, row_ptr, col_idx)
+    B, H, N, d = q.shape
+    Hkv = k.shape[1]
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    kv = _kv(kv_lens, B, q.device)
+    wsz = int(lib.fa_bwd_block_sparse_workspace_size(B, H, N, d))
+    ws = workspace
+    if ws is None or ws.numel() * ws.element_size() < wsz:
+        ws = torch.empty(wsz, dtype=torch.uint8, device=q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    _check(lib.fa_bwd_block_sparse(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
+                                   _ptr(dv), B, H, Hkv, N, d, scale, int(bool(causal)), _ptr(row_ptr),
+                                   _ptr(col_idx), _ptr(kv), _ptr(ws), ws.numel() * ws.element_size(),
+                                   _stream(q)))
+    return dq, dk, dv
 
 
 def _cu(cu_seqlens, device):

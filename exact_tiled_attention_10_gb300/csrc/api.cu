@@ -231,8 +231,14 @@ fa_status fwd_impl(fa_dtype dtype, int block_c, bool fp8, const void* q, const v
                    const float* sk, const float* sv, void* o, float* lse, int B, int H, int N, int d, float scale,
                    int causal, const int* kv_lens, void* workspace, size_t workspace_bytes, cudaStream_t stream,
                    int num_splits = 1, void* split_ws = nullptr, size_t split_ws_bytes = 0, int Hkv = 0,
-                   int win_left = -1, int win_right = -1) {
+                   int win_left = -1, int win_right = -1, const int* row_ptr = nullptr,
+                   const int* col_idx = nullptr) {
     FA_TRY(check_common(B, H, N, d, scale));
+    const bool sparse = row_ptr != nullptr;
+    if (sparse && (dtype != FA_BF16 || fp8)) return fail(FA_ERR_UNSUPPORTED, "block-sparse attention needs bf16 inputs");
+    if (sparse && !col_idx) return fail(FA_ERR_INVALID_ARG, "col_idx must not be NULL");
+    if (sparse && (win_left >= 0 || win_right >= 0))
+        return fail(FA_ERR_UNSUPPORTED, "block lists and a sliding window cannot be combined");
     if (win_left < -1 || win_right < -1) return fail(FA_ERR_INVALID_ARG, "window edges must be >= -1");
     const bool window = win_left >= 0 || win_right >= 0;
     if (window && (dtype != FA_BF16 || fp8)) return fail(FA_ERR_UNSUPPORTED, "the sliding window needs bf16 inputs");
@@ -282,10 +288,10 @@ fa_status fwd_impl(fa_dtype dtype, int block_c, bool fp8, const void* q, const v
         if (block_c == 0) block_c = (d == 128 || N <= 128) ? 64 : 128;
     }
     if (num_splits < 0) return fail(FA_ERR_INVALID_ARG, "num_splits must be >= 0");
-    const SplitPlan P = (dtype == FA_BF16 && !window)
+    const SplitPlan P = (dtype == FA_BF16 && !window && !sparse)
                             ? plan_split(B, H, N, d, causal != 0, kv_lens != nullptr, num_splits, dev->sms)
                             : SplitPlan{};
-    if (window) block_c = 128;
+    if (window || sparse) block_c = 128;
     if (P.splits > 1) block_c = 128;  // the split-key instances use 128-key blocks
     if (block_c == 0) block_c = (N <= 128 && !fp8) ? 64 : 128;
     fa::FwdMaps m;
@@ -328,7 +334,16 @@ fa_status fwd_impl(fa_dtype dtype, int block_c, bool fp8, const void* q, const v
     }
     const int grid = grid_for_items(p.num_units, dev->sms);
     cudaError_t e;
-    if (window) {
+    if (sparse) {
+        fa::FwdParamsSparse ps;
+        memset(&ps, 0, sizeof(ps));
+        static_cast<fa::FwdParams&>(ps) = p;
+        ps.row_ptr = row_ptr;
+        ps.col_idx = col_idx;
+        ps.nqb = (N + 127) / 128;
+        ps.nkb = (N + 127) / 128;
+        e = fa::launch_fwd_sparse(d, causal != 0, m, ps, grid, stream);
+    } else if (window) {
         // causal = the window's right edge at 0
         fa::FwdParamsWin pw;
         memset(&pw, 0, sizeof(pw));
@@ -424,6 +439,15 @@ fa_status fa_fwd_window(const void* q, const void* k, const void* v, void* o, fl
     if (Hkv < 1 || H % Hkv != 0) return fail(FA_ERR_INVALID_ARG, "H (%d) must be a multiple of Hkv (%d)", H, Hkv);
     return fwd_impl(FA_BF16, 0, false, q, k, v, nullptr, nullptr, nullptr, o, lse, B, H, N, d, scale, causal, kv_lens,
                     nullptr, 0, stream, 1, nullptr, 0, Hkv, window_left, window_right);
+}
+
+fa_status fa_fwd_block_sparse(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                              int Hkv, int N, int d, float scale, int causal, const int* row_ptr,
+                              const int* col_idx, const int* kv_lens, fa_stream_t stream) {
+    if (Hkv < 1 || H % Hkv != 0) return fail(FA_ERR_INVALID_ARG, "H (%d) must be a multiple of Hkv (%d)", H, Hkv);
+    if (!row_ptr || !col_idx) return fail(FA_ERR_INVALID_ARG, "row_ptr and col_idx must not be NULL");
+    return fwd_impl(FA_BF16, 0, false, q, k, v, nullptr, nullptr, nullptr, o, lse, B, H, N, d, scale, causal, kv_lens,
+                    nullptr, 0, stream, 1, nullptr, 0, Hkv, -1, -1, row_ptr, col_idx);
 }
 
 fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens,
@@ -535,7 +559,8 @@ fa_status make_map_dqacc(CUtensorMap* m, float* dqacc, int d, long long rows) {
 
 fa_status bwd_main_impl(const BwdCtx& c, bool f32, const void* qb, const void* kb, const void* vb, const void* gb,
                         void* dk, void* dv, int B, int H, int N, int d, float scale, int causal, const int* kv_lens,
-                        cudaStream_t stream, int Hkv = 0, int win_left = -1, int win_right = -1) {
+                        cudaStream_t stream, int Hkv = 0, int win_left = -1, int win_right = -1,
+                        const int* col_ptr = nullptr, const int* row_idx = nullptr) {
     const int BH = c.BH, Np = c.Np;
     if (Hkv == 0) Hkv = H;
     if (Hkv < 1 || H % Hkv != 0) return fail(FA_ERR_INVALID_ARG, "H (%d) must be a multiple of Hkv (%d)", H, Hkv);
@@ -564,7 +589,16 @@ fa_status bwd_main_impl(const BwdCtx& c, bool f32, const void* qb, const void* k
     p.err = c.dev->err_word;
     const int grid = grid_for_items(p.num_items, c.dev->sms);
     cudaError_t e;
-    if (win_left >= 0 || win_right >= 0) {
+    if (col_ptr) {
+        fa::BwdParamsSparse ps;
+        memset(&ps, 0, sizeof(ps));
+        static_cast<fa::BwdParams&>(ps) = p;
+        ps.col_ptr = col_ptr;
+        ps.row_idx = row_idx;
+        ps.nqb = (N + 127) / 128;
+        ps.nkb = (N + 127) / 128;
+        e = fa::launch_bwd_main_sparse(d, causal != 0, tq, tk, tv, tdo, tdq, ps, grid, stream);
+    } else if (win_left >= 0 || win_right >= 0) {
         // causal = the window's right edge at 0
         fa::BwdParamsWin pw;
         memset(&pw, 0, sizeof(pw));
@@ -671,6 +705,53 @@ fa_status fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o,
     FA_TRY(bwd_setup(FA_BF16, B, H, N, d, scale, workspace, workspace_bytes, &c));
     FA_TRY(bwd_pre_impl(c, false, o, lse, dout, N, d, stream));
     FA_TRY(bwd_main_impl(c, false, q, k, v, dout, dk, dv, B, H, N, d, scale, causal, kv_lens, stream, Hkv));
+    return bwd_dq_impl(c, false, dq, N, d, scale, stream);
+}
+
+// Block lists of 128 x 128 blocks: the transposed lists live after the
+// backward's own workspace, 256-byte aligned.
+constexpr int kMaxSparseBlocks = 12000;  // the transposition keeps nkb + 1 counters in shared memory
+
+static size_t sparse_lists_bytes(int N) {
+    const size_t nb = (size_t)(N + 127) / 128;
+    return round_up((nb + 1 + nb * nb) * sizeof(int), 256);
+}
+
+size_t fa_bwd_block_sparse_workspace_size(int B, int H, int N, int d) {
+    if (B <= 0 || H <= 0 || N <= 0 || (d != 64 && d != 128)) return 0;
+    return round_up(fa_bwd_workspace_size(FA_BF16, B, H, N, d), 256) + sparse_lists_bytes(N);
+}
+
+fa_status fa_bwd_block_sparse(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                              const void* dout, void* dq, void* dk, void* dv, int B, int H, int Hkv, int N, int d,
+                              float scale, int causal, const int* row_ptr, const int* col_idx, const int* kv_lens,
+                              void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+    FA_CHECK_PTR(q);
+    FA_CHECK_PTR(k);
+    FA_CHECK_PTR(v);
+    FA_CHECK_PTR(o);
+    FA_CHECK_PTR(lse);
+    FA_CHECK_PTR(dout);
+    FA_CHECK_PTR(dq);
+    FA_CHECK_PTR(dk);
+    FA_CHECK_PTR(dv);
+    if (!row_ptr || !col_idx) return fail(FA_ERR_INVALID_ARG, "row_ptr and col_idx must not be NULL");
+    if (Hkv < 1 || H % Hkv != 0) return fail(FA_ERR_INVALID_ARG, "H (%d) must be a multiple of Hkv (%d)", H, Hkv);
+    if (N > 0 && (N + 127) / 128 > kMaxSparseBlocks)
+        return fail(FA_ERR_UNSUPPORTED, "block-sparse attention takes at most %d blocks", kMaxSparseBlocks);
+    const size_t need = fa_bwd_block_sparse_workspace_size(B, H, N, d);
+    if (workspace_bytes < need)
+        return fail(FA_ERR_INVALID_ARG, "workspace too small (%zu < %zu bytes)", workspace_bytes, need);
+    BwdCtx c{};
+    FA_TRY(bwd_setup(FA_BF16, B, H, N, d, scale, workspace, workspace_bytes, &c));
+    const int nb = (N + 127) / 128;
+    int* col_ptr = reinterpret_cast<int*>(c.ws + round_up(fa_bwd_workspace_size(FA_BF16, B, H, N, d), 256));
+    int* row_idx = col_ptr + nb + 1;
+    cudaError_t e = fa::launch_block_lists_transpose(row_ptr, col_idx, nb, nb, col_ptr, row_idx, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "block list transposition launch");
+    FA_TRY(bwd_pre_impl(c, false, o, lse, dout, N, d, stream));
+    FA_TRY(bwd_main_impl(c, false, q, k, v, dout, dk, dv, B, H, N, d, scale, causal, kv_lens, stream, Hkv, -1, -1,
+                         col_ptr, row_idx));
     return bwd_dq_impl(c, false, dq, N, d, scale, stream);
 }
 

@@ -353,6 +353,57 @@ __global__ void wait_selftest_kernel(unsigned int* err, unsigned long long limit
 
 }  // namespace
 
+// Block-sparse lists transposed: for every key block k, the query blocks i
+// whose list holds k, ascending in i (one CTA, one thread per key block).
+// Membership is decided by one binary search per (i, k) in both passes, so
+// the counts and the entries written agree even for lists that are not
+// ascending; entries outside [0, nkb) are ignored.
+__device__ __forceinline__ bool list_holds(const int* __restrict__ col_idx, int a, int e, int k) {
+    while (a < e) {
+        const int mid = (a + e) >> 1;
+        const int v = __ldg(col_idx + mid);
+        if (v == k) return true;
+        if (v < k) a = mid + 1;
+        else e = mid;
+    }
+    return false;
+}
+
+__global__ void __launch_bounds__(1024) block_lists_transpose_kernel(const int* __restrict__ row_ptr,
+                                                                     const int* __restrict__ col_idx, int nqb, int nkb,
+                                                                     int* __restrict__ col_ptr,
+                                                                     int* __restrict__ row_idx) {
+    extern __shared__ int cnt[];  // [nkb + 1]
+    const int nnz = __ldg(row_ptr + nqb);
+    for (int k = threadIdx.x; k < nkb; k += blockDim.x) {
+        int c = 0;
+        for (int i = 0; i < nqb; ++i) {
+            const int a = min(max(__ldg(row_ptr + i), 0), nnz), e = min(max(__ldg(row_ptr + i + 1), a), nnz);
+            c += list_holds(col_idx, a, e, k);
+        }
+        cnt[k] = c;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int run = 0;
+        for (int k = 0; k < nkb; ++k) {
+            const int c = cnt[k];
+            cnt[k] = run;
+            col_ptr[k] = run;
+            run += c;
+        }
+        col_ptr[nkb] = run;
+    }
+    __syncthreads();
+    for (int k = threadIdx.x; k < nkb; k += blockDim.x) {
+        int pos = cnt[k];
+        for (int i = 0; i < nqb; ++i) {
+            const int a = min(max(__ldg(row_ptr + i), 0), nnz), e = min(max(__ldg(row_ptr + i + 1), a), nnz);
+            if (list_holds(col_idx, a, e, k)) row_idx[pos++] = i;
+        }
+    }
+}
+
 cudaError_t launch_lse_merge(const float* o_part, const float* lse_part, int num_whole, int num_tail, int splits,
                              bool causal, int BH, int num_qp, int N, int d, void* o, float* lse, cudaStream_t stream) {
     if (num_tail <= 0 || splits <= 1) return cudaSuccess;
@@ -419,6 +470,14 @@ cudaError_t launch_bwd_dq(const float* dq_acc, void* dq, bool out_f32, float sca
                           int grid, cudaStream_t s) {
     if (out_f32) bwd_dq_kernel<true><<<grid, 256, 0, s>>>(dq_acc, dq, scale, BH, N, Np, d);
     else bwd_dq_kernel<false><<<grid, 256, 0, s>>>(dq_acc, dq, scale, BH, N, Np, d);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_block_lists_transpose(const int* row_ptr, const int* col_idx, int nqb, int nkb, int* col_ptr,
+                                         int* row_idx, cudaStream_t s) {
+    const int threads = nkb < 1024 ? ((nkb + 31) / 32) * 32 : 1024;
+    block_lists_transpose_kernel<<<1, threads, (nkb + 1) * sizeof(int), s>>>(row_ptr, col_idx, nqb, nkb, col_ptr,
+                                                                             row_idx);
     return cudaGetLastError();
 }
 

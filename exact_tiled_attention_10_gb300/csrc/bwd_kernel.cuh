@@ -116,11 +116,15 @@ struct Item {
 // rows are tokens tb + key, and the statistics rows are (h * B + b) * Np + ...
 // WINDOW: the sliding-window instance (p is a BwdParamsWin; causal is folded
 // into the window's right edge by the caller).
-template <bool WINDOW>
-using ParamsT = typename std::conditional<WINDOW, BwdParamsWin, BwdParams>::type;
+// SPARSE: the block-sparse instance (p is a BwdParamsSparse): key block kt
+// visits the 128-row query blocks row_idx[i0 .. i0 + ni / R - 1] (R steps
+// per query block), per query head of its group.
+template <bool WINDOW, bool SPARSE = false>
+using ParamsT = typename std::conditional<WINDOW, BwdParamsWin,
+                                          typename std::conditional<SPARSE, BwdParamsSparse, BwdParams>::type>::type;
 
-template <class C, bool CAUSAL, bool GQA, bool VARLEN = false, bool WINDOW = false>
-__device__ __forceinline__ Item get_item(int it, const ParamsT<WINDOW>& p) {
+template <class C, bool CAUSAL, bool GQA, bool VARLEN = false, bool WINDOW = false, bool SPARSE = false>
+__device__ __forceinline__ Item get_item(int it, const ParamsT<WINDOW, SPARSE>& p) {
     Item I;
     const int Hkv = GQA ? p.Hkv : p.H;
     const int BH = p.B * Hkv;
@@ -148,7 +152,21 @@ __device__ __forceinline__ Item get_item(int it, const ParamsT<WINDOW>& p) {
     const int key0 = I.kt * C::BC;
     const int iend = ((VARLEN ? I.seqlen : p.N) + C::BR - 1) / C::BR;
     I.i0 = CAUSAL ? key0 / C::BR : 0;
-    if constexpr (WINDOW) {
+    if constexpr (SPARSE) {
+        // the block's query blocks, without those entirely above the causal
+        // diagonal (all query rows before the block's first key)
+        constexpr int R = 128 / C::BR;
+        const int nnz = __ldg(p.col_ptr + p.nkb);
+        int off = min(max(__ldg(p.col_ptr + I.kt), 0), nnz);
+        int cnt = min(max(min(__ldg(p.col_ptr + I.kt + 1), nnz) - off, 0), p.nqb);
+        if (CAUSAL)
+            while (cnt > 0 && (__ldg(p.row_idx + off) + 1) * 128 <= key0) {
+                ++off;
+                --cnt;
+            }
+        I.i0 = off;
+        I.ni = (key0 >= kvl) ? 0 : cnt * R;
+    } else if constexpr (WINDOW) {
         // query rows that see some key of the block: [key0 - right, last key + left]
         int ie = iend;
         if (p.win_right >= 0) I.i0 = max(I.i0, max(0, key0 - p.win_right) / C::BR);
@@ -162,6 +180,15 @@ __device__ __forceinline__ Item get_item(int it, const ParamsT<WINDOW>& p) {
 }
 // Query head row bhq and query block i of consecutive steps of an item:
 // start with (qh0, i0), advance once per step (one query head: i = i0 + s).
+// Block-sparse: query head row and query block (in C::BR units) of step s.
+template <class C>
+__device__ __forceinline__ void sparse_step(const Item& I, const BwdParamsSparse& p, int s, int& bhq, int& i) {
+    constexpr int R = 128 / C::BR;
+    const int h = s / I.ni, local = s - h * I.ni;
+    bhq = I.qh0 + h;
+    i = min(max(__ldg(p.row_idx + I.i0 + local / R), 0), p.nqb - 1) * R + local % R;
+}
+
 template <bool GQA>
 __device__ __forceinline__ void step_next(const Item& I, int& bhq, int& i) {
     ++i;
@@ -241,11 +268,12 @@ __device__ __forceinline__ void mma_dq(uint32_t d_tmem, uint64_t k_mn, uint64_t 
     }
 }
 
-template <class C, bool CAUSAL, bool OUT_F32, bool GQA, bool VARLEN = false, bool WINDOW = false>
+template <class C, bool CAUSAL, bool OUT_F32, bool GQA, bool VARLEN = false, bool WINDOW = false,
+          bool SPARSE = false>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
-               const __grid_constant__ CUtensorMap tdq, const ParamsT<WINDOW> p) {
+               const __grid_constant__ CUtensorMap tdq, const ParamsT<WINDOW, SPARSE> p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -300,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int rd = 0; rd < snake_rounds(p.num_items) && ok; ++rd) {
             const int it = snake_item(rd, p.num_items);
             if (it < 0) continue;
-            const Item I = get_item<C, CAUSAL, GQA, VARLEN, WINDOW>(it, p);
+            const Item I = get_item<C, CAUSAL, GQA, VARLEN, WINDOW, SPARSE>(it, p);
             if (I.n == 0) continue;
             if (!(ok = wait_bounded_warp(BAR(C::B_KVEMPTY), kve ^ 1, abort_flag, p.err, kErrWaitBwdProducer))) break;
             kve ^= 1;
@@ -315,6 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             int bhq = I.qh0, i = I.i0;
             for (int s = 0; s < I.n; ++s, step_next<GQA>(I, bhq, i)) {
+                if constexpr (SPARSE) sparse_step<C>(I, p, s, bhq, i);
                 if (!(ok = wait_bounded_warp(BAR(C::B_QEMPTY + st), ph ^ 1, abort_flag, p.err, kErrWaitBwdProducer))) break;
                 if (lane == 0) {
                     const uint32_t bar = BAR(C::B_QFULL + st);
@@ -376,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int rd = 0; rd < snake_rounds(p.num_items) && ok; ++rd) {
             const int it = snake_item(rd, p.num_items);
             if (it < 0) continue;
-            const Item I = get_item<C, CAUSAL, GQA, VARLEN, WINDOW>(it, p);
+            const Item I = get_item<C, CAUSAL, GQA, VARLEN, WINDOW, SPARSE>(it, p);
             if (I.n == 0) continue;
             if (!(ok = wait_bounded_warp(BAR(C::B_KVFULL), kvph, abort_flag, p.err, kErrWaitBwdMma))) break;
             kvph ^= 1;
@@ -437,7 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int rd = 0; rd < snake_rounds(p.num_items) && ok; ++rd) {
             const int it = snake_item(rd, p.num_items);
             if (it < 0) continue;
-            const Item I = get_item<C, CAUSAL, GQA, VARLEN, WINDOW>(it, p);
+            const Item I = get_item<C, CAUSAL, GQA, VARLEN, WINDOW, SPARSE>(it, p);
             const int key = I.kt * C::BC + kr;
             // dK, dV row: [B,Hkv,N,d], or token-major [total, Hkv, d] for packed sequences
             const size_t krow = VARLEN ? (size_t)(I.tb + key) * p.Hkv + I.kvh : (size_t)I.bh * p.N + key;
@@ -454,6 +483,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             int bhq = I.qh0, i = I.i0;
             for (int s = 0; s < I.n; ++s, step_next<GQA>(I, bhq, i)) {
+                if constexpr (SPARSE) sparse_step<C>(I, p, s, bhq, i);
                 const int slot = s % C::NSLOT;
                 const int dsb = s & 1;
                 const int q0 = i * C::BR + h * C::HALF;  // first query column of this half
@@ -582,9 +612,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int rd = 0; rd < snake_rounds(p.num_items) && ok; ++rd) {
             const int it = snake_item(rd, p.num_items);
             if (it < 0) continue;
-            const Item I = get_item<C, CAUSAL, GQA, VARLEN, WINDOW>(it, p);
+            const Item I = get_item<C, CAUSAL, GQA, VARLEN, WINDOW, SPARSE>(it, p);
             int bhq = I.qh0, i = I.i0;
             for (int s = 0; s < I.n; ++s, step_next<GQA>(I, bhq, i)) {
+                if constexpr (SPARSE) sparse_step<C>(I, p, s, bhq, i);
                 const int dqs = C::DQ_ALIAS ? (s % C::NSLOT) : 0;
                 if (!(ok = wait_bounded_warp(BAR(C::B_DQFULL + dqs), dqph[dqs], abort_flag, p.err, kErrWaitBwdDq))) break;
                 dqph[dqs] ^= 1;
@@ -642,11 +673,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <class C, bool CAUSAL, bool OUT_F32, bool GQA = false, bool VARLEN = false, bool WINDOW = false>
+template <class C, bool CAUSAL, bool OUT_F32, bool GQA = false, bool VARLEN = false, bool WINDOW = false,
+          bool SPARSE = false>
 cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                   const CUtensorMap& tdo, const CUtensorMap& tdq, const ParamsT<WINDOW>& p, int grid,
+                   const CUtensorMap& tdo, const CUtensorMap& tdq, const ParamsT<WINDOW, SPARSE>& p, int grid,
                    cudaStream_t stream) {
-    auto kern = bwd_kernel<C, CAUSAL, OUT_F32, GQA, VARLEN, WINDOW>;
+    auto kern = bwd_kernel<C, CAUSAL, OUT_F32, GQA, VARLEN, WINDOW, SPARSE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     kern<<<grid, kThreads, C::SMEM, stream>>>(tq, tk, tv, tdo, tdq, p);

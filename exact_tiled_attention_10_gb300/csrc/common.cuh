@@ -117,6 +117,22 @@ struct BwdParamsWin : BwdParams {
     int win_left, win_right;
 };
 
+// Block-sparse attention (chapter 18 §18.8.1): the 128-row query block i
+// computes only the 128-key blocks col_idx[row_ptr[i] .. row_ptr[i+1]-1]
+// (ascending), one list for every batch item and head.  The backward reads
+// the transposed lists (per key block, its query blocks, ascending), which
+// the library builds in the workspace.
+struct FwdParamsSparse : FwdParams {
+    const int* row_ptr;  // [nqb + 1]
+    const int* col_idx;  // [row_ptr[nqb]]
+    int nqb, nkb;
+};
+struct BwdParamsSparse : BwdParams {
+    const int* col_ptr;  // [nkb + 1]
+    const int* row_idx;
+    int nqb, nkb;
+};
+
 // Launch helpers implemented in the kernel translation units.  They return a
 // cudaError_t from the launch itself.
 // Tensor maps of one forward launch: q, k, v and, for float32 inputs carried
@@ -129,6 +145,14 @@ cudaError_t launch_fwd_bf16_d64(int block_c, bool causal, bool out_f32, bool spl
 cudaError_t launch_fwd_bf16_d128(int block_c, bool causal, bool out_f32, bool split, const FwdMaps& m,
                                  const FwdParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_fwd_window(int d, const FwdMaps& m, const FwdParamsWin& p, int grid, cudaStream_t stream);
+cudaError_t launch_fwd_sparse(int d, bool causal, const FwdMaps& m, const FwdParamsSparse& p, int grid,
+                              cudaStream_t stream);
+cudaError_t launch_bwd_main_sparse(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
+                                   const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
+                                   const BwdParamsSparse& p, int grid, cudaStream_t stream);
+// Transposes the query-block lists into per-key-block lists (one CTA).
+cudaError_t launch_block_lists_transpose(const int* row_ptr, const int* col_idx, int nqb, int nkb, int* col_ptr,
+                                         int* row_idx, cudaStream_t stream);
 cudaError_t launch_bwd_main_window(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                    const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParamsWin& p, int grid,
                                    cudaStream_t stream);

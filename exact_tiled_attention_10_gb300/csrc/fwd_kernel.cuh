@@ -153,17 +153,57 @@ struct ItemWin : Item {
     int a[2];
 };
 
-template <bool VARLEN, bool WINDOW = false>
-using ItemT = typename std::conditional<VARLEN, ItemPacked,
-                                        typename std::conditional<WINDOW, ItemWin, Item>::type>::type;
+// Block-sparse: tile t computes the key blocks col_idx[off[t] .. off[t] +
+// n[t] - 1]; the K / V stream is the ascending union of the two lists (nmax
+// blocks), walked by BlockMerge in every role.
+struct ItemSparse : Item {
+    int off[2];
+};
 
-template <bool WINDOW>
-using ParamsT = typename std::conditional<WINDOW, FwdParamsWin, FwdParams>::type;
+template <bool VARLEN, bool WINDOW = false, bool SPARSE = false>
+using ItemT = typename std::conditional<
+    VARLEN, ItemPacked,
+    typename std::conditional<WINDOW, ItemWin, typename std::conditional<SPARSE, ItemSparse, Item>::type>::type>::type;
+
+template <bool WINDOW, bool SPARSE = false>
+using ParamsT = typename std::conditional<WINDOW, FwdParamsWin,
+                                          typename std::conditional<SPARSE, FwdParamsSparse, FwdParams>::type>::type;
+
+// Walks the ascending union of the two tiles' key-block lists: each call
+// returns the next block and which tiles compute it (a list that is not
+// ascending still yields every entry exactly once).
+struct BlockMerge {
+    const int* l0;
+    const int* l1;
+    int n0, n1, c0, c1;
+    __device__ __forceinline__ int next(bool& a0, bool& a1) {
+        const int x0 = c0 < n0 ? __ldg(l0 + c0) : 0x7fffffff;
+        const int x1 = c1 < n1 ? __ldg(l1 + c1) : 0x7fffffff;
+        const int b = min(x0, x1);
+        a0 = c0 < n0 && x0 == b;
+        a1 = c1 < n1 && x1 == b;
+        c0 += a0;
+        c1 += a1;
+        return b;
+    }
+};
+
+__device__ __forceinline__ BlockMerge block_merge(const ItemSparse& I, const FwdParamsSparse& p) {
+    BlockMerge m;
+    m.l0 = p.col_idx + I.off[0];
+    m.l1 = p.col_idx + I.off[1];
+    m.n0 = I.n[0];
+    m.n1 = I.n[1];
+    m.c0 = m.c1 = 0;
+    return m;
+}
 
 template <class IT>
 __host__ __device__ constexpr bool is_packed() { return std::is_same<IT, ItemPacked>::value; }
 template <class IT>
 __host__ __device__ constexpr bool is_window() { return std::is_same<IT, ItemWin>::value; }
+template <class IT>
+__host__ __device__ constexpr bool is_sparse() { return std::is_same<IT, ItemSparse>::value; }
 
 // First key block of tile t, relative to the unit's j0 (0 without a window).
 template <class IT>
@@ -177,7 +217,7 @@ __device__ __forceinline__ int item_a(const IT& I, int t) {
 // directly, which schedules better.
 template <class IT>
 __device__ __forceinline__ int item_n(const IT& I, int t) {
-    if constexpr (is_packed<IT>() || is_window<IT>()) return t ? I.n[1] : I.n[0];
+    if constexpr (is_packed<IT>() || is_window<IT>() || is_sparse<IT>()) return t ? I.n[1] : I.n[0];
     else return I.n[t];
 }
 
@@ -219,9 +259,9 @@ __device__ __forceinline__ size_t lse_index(const IT& I, int row, const FwdParam
 // separately so that the plain forward carries none of their bookkeeping).
 // VARLEN: the instance for packed variable-length sequences.
 // WINDOW: the sliding-window instance (p is a FwdParamsWin).
-template <class C, bool CAUSAL, bool SPLITK, bool VARLEN, bool WINDOW = false>
-__device__ __forceinline__ ItemT<VARLEN, WINDOW> get_item(int unit, const ParamsT<WINDOW>& p) {
-    ItemT<VARLEN, WINDOW> I;
+template <class C, bool CAUSAL, bool SPLITK, bool VARLEN, bool WINDOW = false, bool SPARSE = false>
+__device__ __forceinline__ ItemT<VARLEN, WINDOW, SPARSE> get_item(int unit, const ParamsT<WINDOW, SPARSE>& p) {
+    ItemT<VARLEN, WINDOW, SPARSE> I;
     const int BH = p.B * p.H;
     int it = unit, s = 0, S = 1;
     I.part = -1;
@@ -251,7 +291,35 @@ __device__ __forceinline__ ItemT<VARLEN, WINDOW> get_item(int unit, const Params
     I.kvl = kvl;
     I.row0 = qp * (C::QT * C::BR);
     I.nmax = 0;
-    if constexpr (WINDOW) {
+    if constexpr (SPARSE) {
+        // each tile's list, without the trailing blocks that hold no visible
+        // key for any of its rows (beyond kv_len, or above the causal diagonal)
+        const int nnz = __ldg(p.row_ptr + p.nqb);
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            const int r0 = I.row0 + t * C::BR;
+            int off = 0, cnt = 0;
+            if (r0 < rows) {
+                const int qb = r0 / C::BR;
+                off = min(max(__ldg(p.row_ptr + qb), 0), nnz);
+                cnt = min(max(min(__ldg(p.row_ptr + qb + 1), nnz) - off, 0), p.nkb);
+                int lim = kvl;
+                if (CAUSAL) lim = min(lim, min(r0 + C::BR, rows));
+                while (cnt > 0 && __ldg(p.col_idx + off + cnt - 1) * C::BC >= lim) --cnt;
+            }
+            I.off[t] = off;
+            I.n[t] = cnt;
+        }
+        BlockMerge mg = block_merge(I, p);
+        int u = 0;
+        bool a0, a1;
+        while (mg.c0 < mg.n0 || mg.c1 < mg.n1) {
+            mg.next(a0, a1);
+            ++u;
+        }
+        I.nmax = u;
+        I.j0 = 0;
+    } else if constexpr (WINDOW) {
         // keys [lo, hi) cover every row of tile t: lo from its first row's left
         // edge, hi from its last row's right edge (and kv_len / causal)
         int lb[2], nb[2], J0 = 0x7fffffff, J1 = 0;
@@ -420,11 +488,12 @@ __device__ __forceinline__ void store_row_chunk(void* o_row, int c0, const float
     }
 }
 
-template <class C, bool CAUSAL, bool OUT_F32, bool SPLITK, bool VARLEN = false, bool WINDOW = false>
+template <class C, bool CAUSAL, bool OUT_F32, bool SPLITK, bool VARLEN = false, bool WINDOW = false,
+          bool SPARSE = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tql,
-               const __grid_constant__ CUtensorMap tkl, const ParamsT<WINDOW> p) {
+               const __grid_constant__ CUtensorMap tkl, const ParamsT<WINDOW, SPARSE> p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -488,7 +557,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int rd = 0; rd < snake_rounds(p.num_units) && ok; ++rd) {
             const int it = snake_item(rd, p.num_units);
             if (it < 0) continue;
-            const auto I = get_item<C, CAUSAL, SPLITK, VARLEN, WINDOW>(it, p);
+            const auto I = get_item<C, CAUSAL, SPLITK, VARLEN, WINDOW, SPARSE>(it, p);
             if (I.nmax == 0) continue;
             // Q tile t of this item may load as soon as the previous item's last
             // S_t MMA has consumed the buffer (per-tile barriers), overlapping
@@ -510,12 +579,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             qe ^= 1;
             // K runs one tile ahead of V (K_0 K_1 V_0 K_2 V_1 ...): S(j+1) needs K_{j+1}
             // before P V(j+1) needs V_{j+1}
+            [[maybe_unused]] BlockMerge mg;
+            [[maybe_unused]] int kb_cur = 0, kb_prev = 0;  // block-sparse: key blocks of the stream
+            if constexpr (SPARSE) mg = block_merge(I, p);
             for (int idx = 0; idx <= I.nmax && ok; ++idx) {
+                if constexpr (SPARSE) {
+                    kb_prev = kb_cur;
+                    if (idx < I.nmax) {
+                        bool a0, a1;
+                        kb_cur = mg.next(a0, a1);
+                    }
+                }
                 if (idx < I.nmax) {
                     if (!(ok = wait_bounded_warp(BAR(C::B_KEMPTY + kst), kph ^ 1, abort_flag, p.err, kErrWaitFwdProducer))) break;
                     if (lane == 0) {
                         int y, z;
-                        kv_coords(I, (I.j0 + idx) * C::BC, p, y, z);
+                        kv_coords(I, (SPARSE ? kb_cur : I.j0 + idx) * C::BC, p, y, z);
                         mbar_arrive_expect_tx(BAR(C::B_KFULL + kst), C::K_STAGE);
                         for (int part = 0; part < C::NPART; ++part)
                             for (int bx = 0; bx < C::NBOX; ++bx)
@@ -530,7 +609,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!(ok = wait_bounded_warp(BAR(C::B_VEMPTY + vst), vph ^ 1, abort_flag, p.err, kErrWaitFwdProducer))) break;
                     if (lane == 0) {
                         int y, z;
-                        kv_coords(I, (I.j0 + j) * C::BC, p, y, z);
+                        kv_coords(I, (SPARSE ? kb_prev : I.j0 + j) * C::BC, p, y, z);
                         mbar_arrive_expect_tx(BAR(C::B_VFULL + vst), C::KV_TILE);
                         for (int bx = 0; bx < C::NBOX; ++bx)
                             tma_load_3d(sbase + C::OFF_V + vst * C::KV_TILE + bx * C::KV_BOX, &tv, BAR(C::B_VFULL + vst),
@@ -561,7 +640,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int rd = 0; rd < snake_rounds(p.num_units) && ok; ++rd) {
             const int it = snake_item(rd, p.num_units);
             if (it < 0) continue;
-            const auto I = get_item<C, CAUSAL, SPLITK, VARLEN, WINDOW>(it, p);
+            const auto I = get_item<C, CAUSAL, SPLITK, VARLEN, WINDOW, SPARSE>(it, p);
             if (I.nmax == 0) continue;
             for (int t = 0; t < 2 && ok; ++t)
                 ok = wait_bounded_warp(BAR(C::B_QFULL + t), qph, abort_flag, p.err, kErrWaitFwdMma);
@@ -569,23 +648,46 @@ __global__ void __launch_bounds__(kThreads, 1)
             qph ^= 1;
             if (!(ok = wait_bounded_warp(BAR(C::B_KFULL + kst), kph, abort_flag, p.err, kErrWaitFwdMma))) break;
             tc_fence_after();
-            for (int t = 0; t < 2; ++t) {
-                if (item_a(I, t) == 0) {  // (a tile that starts later issues its first S in the loop)
-                    if (item_n(I, t) > 0) {
+            if constexpr (SPARSE) {
+                // union step u: P V for the tiles that compute block u, then S for
+                // the tiles that compute block u + 1 (a tile may skip blocks)
+                BlockMerge mg = block_merge(I, p);
+                bool cu[2], nx[2];
+                mg.next(cu[0], cu[1]);
+                int sd[2] = {0, 0}, pd[2] = {0, 0};  // S / P V products issued per tile
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                    if (cu[t]) {
                         issue_S<C>(tS(t), q_desc(t), k_desc(kst));
                         mma_commit_w(BAR(C::B_SFULL + t));
+                        ++sd[t];
                     }
-                    if (item_n(I, t) <= 1) mma_commit_w(BAR(C::B_QEMPTY + t));  // Q_t no longer needed
+                    if (sd[t] == item_n(I, t)) mma_commit_w(BAR(C::B_QEMPTY + t));  // Q_t no longer needed
                 }
-            }
-            mma_commit_w(BAR(C::B_KEMPTY + kst));
-            if (++kst == C::KSTAGES) { kst = 0; kph ^= 1; }
-            for (int j = 0; j < I.nmax && ok; ++j) {
-                bool vw = false, kw = false;
-                for (int t = 0; t < 2; ++t) {
-                    const int ta = item_a(I, t), te = ta + item_n(I, t);  // tile t: blocks [ta, te)
-                    if (j < ta || j >= te) {
-                        if (j + 1 == ta) {  // tile t starts with the next block: its first S
+                mma_commit_w(BAR(C::B_KEMPTY + kst));
+                if (++kst == C::KSTAGES) { kst = 0; kph ^= 1; }
+                for (int u = 0; u < I.nmax && ok; ++u) {
+                    nx[0] = nx[1] = false;
+                    if (u + 1 < I.nmax) mg.next(nx[0], nx[1]);
+                    bool vw = false, kw = false;
+#pragma unroll
+                    for (int t = 0; t < 2; ++t) {
+                        if (cu[t]) {
+                            if (!(ok = wait_bounded_warp(BAR(C::B_PFULL + t), pph[t], abort_flag, p.err, kErrWaitFwdMma))) break;
+                            pph[t] ^= 1;
+                            if (pd[t] == 0) {
+                                if (!(ok = wait_bounded_warp(BAR(C::B_OEMPTY + t), oeph[t] ^ 1, abort_flag, p.err, kErrWaitFwdMma))) break;
+                                oeph[t] ^= 1;
+                            }
+                            if (!vw) {
+                                if (!(ok = wait_bounded_warp(BAR(C::B_VFULL + vst), vph, abort_flag, p.err, kErrWaitFwdMma))) break;
+                                vw = true;
+                            }
+                            tc_fence_after();
+                            issue_PV<C>(tO(t), tS(t), v_desc(vst), pd[t] > 0);
+                            if (++pd[t] == item_n(I, t)) mma_commit_w(BAR(C::B_OFULL + t));
+                        }
+                        if (nx[t]) {
                             if (!kw) {
                                 if (!(ok = wait_bounded_warp(BAR(C::B_KFULL + kst), kph, abort_flag, p.err, kErrWaitFwdMma))) break;
                                 kw = true;
@@ -593,41 +695,80 @@ __global__ void __launch_bounds__(kThreads, 1)
                             }
                             issue_S<C>(tS(t), q_desc(t), k_desc(kst));
                             mma_commit_w(BAR(C::B_SFULL + t));
-                            if (te - ta == 1) mma_commit_w(BAR(C::B_QEMPTY + t));
+                            if (++sd[t] == item_n(I, t)) mma_commit_w(BAR(C::B_QEMPTY + t));
                         }
-                        continue;
                     }
-                    if (!(ok = wait_bounded_warp(BAR(C::B_PFULL + t), pph[t], abort_flag, p.err, kErrWaitFwdMma))) break;
-                    pph[t] ^= 1;
-                    if (j == ta) {
-                        if (!(ok = wait_bounded_warp(BAR(C::B_OEMPTY + t), oeph[t] ^ 1, abort_flag, p.err, kErrWaitFwdMma))) break;
-                        oeph[t] ^= 1;
+                    if (!ok) break;
+                    mma_commit_w(BAR(C::B_VEMPTY + vst));
+                    if (++vst == C::VSTAGES) { vst = 0; vph ^= 1; }
+                    if (kw) {
+                        mma_commit_w(BAR(C::B_KEMPTY + kst));
+                        if (++kst == C::KSTAGES) { kst = 0; kph ^= 1; }
                     }
-                    if (!vw) {
-                        if (!(ok = wait_bounded_warp(BAR(C::B_VFULL + vst), vph, abort_flag, p.err, kErrWaitFwdMma))) break;
-                        vw = true;
-                    }
-                    tc_fence_after();
-                    issue_PV<C>(tO(t), tS(t), v_desc(vst), j > ta);
-                    if (j == te - 1) {
-                        mma_commit_w(BAR(C::B_OFULL + t));
-                    } else {
-                        if (!kw) {
-                            if (!(ok = wait_bounded_warp(BAR(C::B_KFULL + kst), kph, abort_flag, p.err, kErrWaitFwdMma))) break;
-                            kw = true;
-                            tc_fence_after();
+                    cu[0] = nx[0];
+                    cu[1] = nx[1];
+                }
+            } else {
+                for (int t = 0; t < 2; ++t) {
+                    if (item_a(I, t) == 0) {  // (a tile that starts later issues its first S in the loop)
+                        if (item_n(I, t) > 0) {
+                            issue_S<C>(tS(t), q_desc(t), k_desc(kst));
+                            mma_commit_w(BAR(C::B_SFULL + t));
                         }
-                        issue_S<C>(tS(t), q_desc(t), k_desc(kst));
-                        mma_commit_w(BAR(C::B_SFULL + t));
-                        if (j + 2 == te) mma_commit_w(BAR(C::B_QEMPTY + t));  // last S_t issued
+                        if (item_n(I, t) <= 1) mma_commit_w(BAR(C::B_QEMPTY + t));  // Q_t no longer needed
                     }
                 }
-                if (!ok) break;
-                mma_commit_w(BAR(C::B_VEMPTY + vst));
-                if (++vst == C::VSTAGES) { vst = 0; vph ^= 1; }
-                if (kw) {
-                    mma_commit_w(BAR(C::B_KEMPTY + kst));
-                    if (++kst == C::KSTAGES) { kst = 0; kph ^= 1; }
+                mma_commit_w(BAR(C::B_KEMPTY + kst));
+                if (++kst == C::KSTAGES) { kst = 0; kph ^= 1; }
+                for (int j = 0; j < I.nmax && ok; ++j) {
+                    bool vw = false, kw = false;
+                    for (int t = 0; t < 2; ++t) {
+                        const int ta = item_a(I, t), te = ta + item_n(I, t);  // tile t: blocks [ta, te)
+                        if (j < ta || j >= te) {
+                            if (j + 1 == ta) {  // tile t starts with the next block: its first S
+                                if (!kw) {
+                                    if (!(ok = wait_bounded_warp(BAR(C::B_KFULL + kst), kph, abort_flag, p.err, kErrWaitFwdMma))) break;
+                                    kw = true;
+                                    tc_fence_after();
+                                }
+                                issue_S<C>(tS(t), q_desc(t), k_desc(kst));
+                                mma_commit_w(BAR(C::B_SFULL + t));
+                                if (te - ta == 1) mma_commit_w(BAR(C::B_QEMPTY + t));
+                            }
+                            continue;
+                        }
+                        if (!(ok = wait_bounded_warp(BAR(C::B_PFULL + t), pph[t], abort_flag, p.err, kErrWaitFwdMma))) break;
+                        pph[t] ^= 1;
+                        if (j == ta) {
+                            if (!(ok = wait_bounded_warp(BAR(C::B_OEMPTY + t), oeph[t] ^ 1, abort_flag, p.err, kErrWaitFwdMma))) break;
+                            oeph[t] ^= 1;
+                        }
+                        if (!vw) {
+                            if (!(ok = wait_bounded_warp(BAR(C::B_VFULL + vst), vph, abort_flag, p.err, kErrWaitFwdMma))) break;
+                            vw = true;
+                        }
+                        tc_fence_after();
+                        issue_PV<C>(tO(t), tS(t), v_desc(vst), j > ta);
+                        if (j == te - 1) {
+                            mma_commit_w(BAR(C::B_OFULL + t));
+                        } else {
+                            if (!kw) {
+                                if (!(ok = wait_bounded_warp(BAR(C::B_KFULL + kst), kph, abort_flag, p.err, kErrWaitFwdMma))) break;
+                                kw = true;
+                                tc_fence_after();
+                            }
+                            issue_S<C>(tS(t), q_desc(t), k_desc(kst));
+                            mma_commit_w(BAR(C::B_SFULL + t));
+                            if (j + 2 == te) mma_commit_w(BAR(C::B_QEMPTY + t));  // last S_t issued
+                        }
+                    }
+                    if (!ok) break;
+                    mma_commit_w(BAR(C::B_VEMPTY + vst));
+                    if (++vst == C::VSTAGES) { vst = 0; vph ^= 1; }
+                    if (kw) {
+                        mma_commit_w(BAR(C::B_KEMPTY + kst));
+                        if (++kst == C::KSTAGES) { kst = 0; kph ^= 1; }
+                    }
                 }
             }
             if (!ok) break;
@@ -648,7 +789,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int rd = 0; rd < snake_rounds(p.num_units); ++rd) {
             const int it = snake_item(rd, p.num_units);
             if (it < 0) continue;
-            const auto I = get_item<C, CAUSAL, SPLITK, VARLEN, WINDOW>(it, p);
+            const auto I = get_item<C, CAUSAL, SPLITK, VARLEN, WINDOW, SPARSE>(it, p);
             const int n = item_n(I, t);
             const int tile_row0 = I.row0 + t * C::BR;
             const int row = tile_row0 + r_in;
@@ -735,7 +876,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float s[C::BC];
 #pragma unroll
                 for (int c = 0; c < C::BC; ++c) s[c] = __uint_as_float(sr[c]);
-                const int col0 = (I.j0 + item_a(I, t) + j) * C::BC;
+                int col0 = (I.j0 + item_a(I, t) + j) * C::BC;
+                if constexpr (SPARSE) col0 = __ldg(p.col_idx + (t ? I.off[1] : I.off[0]) + j) * C::BC;
                 bool need_mask = (col0 + C::BC > I.kvl) || (CAUSAL && col0 + C::BC - 1 > tile_row0);
                 if constexpr (WINDOW)  // blocks crossing some row's window edge
                     need_mask = need_mask || (p.win_right >= 0 && col0 + C::BC - 1 > tile_row0 + p.win_right) ||
@@ -843,13 +985,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <class C, bool CAUSAL, bool OUT_F32, bool SPLITK = false, bool VARLEN = false, bool WINDOW = false>
-cudaError_t launch(const FwdMaps& m, const ParamsT<WINDOW>& p, int grid, cudaStream_t stream) {
-    auto kern = fwd_kernel<C, CAUSAL, OUT_F32, SPLITK, VARLEN, WINDOW>;
+template <class C, bool CAUSAL, bool OUT_F32, bool SPLITK = false, bool VARLEN = false, bool WINDOW = false,
+          bool SPARSE = false>
+cudaError_t launch(const FwdMaps& m, const ParamsT<WINDOW, SPARSE>& p, int grid, cudaStream_t stream) {
+    auto kern = fwd_kernel<C, CAUSAL, OUT_F32, SPLITK, VARLEN, WINDOW, SPARSE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     kern<<<grid, kThreads, C::SMEM, stream>>>(m.q, m.k, m.v, m.q_lo, m.k_lo, p);
     return cudaGetLastError();
+}
+
+// Block-sparse (block lists of 128 x 128 blocks).
+template <class C>
+cudaError_t launch_sparse(bool causal, const FwdMaps& m, const FwdParamsSparse& p, int grid, cudaStream_t s) {
+    return causal ? launch<C, true, false, false, false, false, true>(m, p, grid, s)
+                  : launch<C, false, false, false, false, false, true>(m, p, grid, s);
 }
 
 // Sliding window (causal folded into the window's right edge by the caller).

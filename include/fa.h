@@ -156,6 +156,23 @@ fa_status fa_fwd_window(const void* q, const void* k, const void* v, void* o, fl
                         int window_left, int window_right, const int* kv_lens,
                         fa_stream_t stream);
 
+/* Block-sparse attention ([CH18] §18.8.1: per query block the list of key
+ * blocks to compute; the others are neither loaded nor multiplied), bf16,
+ * shapes as fa_fwd_gqa.  Blocks are 128 x 128: query block i (rows
+ * 128 i .. 128 i + 127) attends to the keys of the key blocks
+ * col_idx[row_ptr[i] .. row_ptr[i+1]-1] only, on top of the causal and key
+ * padding masks; the same lists serve every batch item and head.
+ * row_ptr: device int32 [nb + 1], nb = ceil(N / 128), non-decreasing, with
+ * row_ptr[nb] = the number of entries of col_idx; col_idx: device int32,
+ * each list ascending without repeats, entries in [0, nb).  The kernels
+ * clamp list bounds to [0, row_ptr[nb]] but do not otherwise validate the
+ * lists (malformed lists give wrong results).  A query block with an empty
+ * list gets O = 0, LSE = -inf. */
+fa_status fa_fwd_block_sparse(const void* q, const void* k, const void* v, void* o, float* lse,
+                              int B, int H, int Hkv, int N, int d, float scale, int causal,
+                              const int* row_ptr, const int* col_idx, const int* kv_lens,
+                              fa_stream_t stream);
+
 /* Packed variable-length sequences (flash_attn_varlen_func, [CH18] §18.7.1),
  * bf16: sequence b holds tokens cu_seqlens[b] .. cu_seqlens[b+1]-1 of the
  * token-major tensors q, o [total, H, d] and k, v [total, Hkv, d] (Hkv = H
@@ -206,6 +223,20 @@ fa_status fa_bwd_window(const void* q, const void* k, const void* v, const void*
                         int B, int H, int Hkv, int N, int d, float scale, int causal,
                         int window_left, int window_right, const int* kv_lens,
                         void* workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/* Backward of fa_fwd_block_sparse (same lists and masks), bf16: dq
+ * [B,H,N,d]; dk, dv [B,Hkv,N,d] summed over the query heads sharing a
+ * key/value head.  A one-CTA kernel first transposes the lists into the
+ * workspace (for every key block, its query blocks); each key block then
+ * visits only those.  Workspace: fa_bwd_block_sparse_workspace_size(B, H, N,
+ * d) bytes (fa_bwd_workspace_size plus the transposed lists).
+ * FA_ERR_UNSUPPORTED beyond 12000 blocks (N > 1,536,000). */
+size_t fa_bwd_block_sparse_workspace_size(int B, int H, int N, int d);
+fa_status fa_bwd_block_sparse(const void* q, const void* k, const void* v, const void* o,
+                              const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                              int B, int H, int Hkv, int N, int d, float scale, int causal,
+                              const int* row_ptr, const int* col_idx, const int* kv_lens,
+                              void* workspace, size_t workspace_bytes, fa_stream_t stream);
 
 /* Backward of fa_fwd_varlen (packed variable-length sequences, bf16): dq
  * [total, H, d], dk, dv [total, Hkv, d] (summed over the query heads sharing
