@@ -62,6 +62,7 @@ _SIGS = {
     "fa_bwd_window": ([_vp] * 9 + [_i, _i, _i, _i, _i, _f, _i, _i, _i, _vp, _vp, _sz, _vp], _i),
     "fa_fwd_block_sparse": ([_vp] * 5 + [_i, _i, _i, _i, _i, _f, _i, _vp, _vp, _vp, _vp], _i),
     "fa_bwd_block_sparse_workspace_size": ([_i] * 4, _sz),
+    "fa_bwd_gqa_workspace_size": ([_i] * 5, _sz),
     "fa_bwd_block_sparse": ([_vp] * 9 + [_i, _i, _i, _i, _i, _f, _i, _vp, _vp, _vp, _vp, _sz, _vp], _i),
     "fa_fwd_varlen": ([_vp] * 6 + [_i, _i, _i, _i, _i, _i, _f, _i, _vp], _i),
     "fa_bwd_varlen_workspace_size": ([_i] * 4, _sz),
@@ -364,7 +365,10 @@ def backward(q, k, v, o, lse, dout, causal: bool = False, scale: Optional[float]
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     kv = _kv(kv_lens, B, q.device)
     dt = FA_F32 if q.dtype == torch.float32 else FA_BF16
-    wsz = int(lib.fa_bwd_workspace_size(dt, B, H, N, d))
+    wl, wr = _window(window)
+    grouped = Hkv != H or wl >= 0 or wr >= 0
+    wsz = int(lib.fa_bwd_gqa_workspace_size(B, H, Hkv, N, d) if grouped and dt == FA_BF16
+              else lib.fa_bwd_workspace_size(dt, B, H, N, d))
     ws = workspace
     if ws is None or ws.numel() * ws.element_size() < wsz:
         ws = torch.empty(wsz, dtype=torch.uint8, device=q.device)
@@ -372,7 +376,6 @@ def backward(q, k, v, o, lse, dout, causal: bool = False, scale: Optional[float]
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     _need_cuda(dq, dk, dv)
-    wl, wr = _window(window)
     if wl >= 0 or wr >= 0:
         if q.dtype != torch.bfloat16 or H % Hkv != 0:
             raise ValueError("the sliding window needs bfloat16 tensors and H a multiple of Hkv")

@@ -557,10 +557,23 @@ fa_status make_map_dqacc(CUtensorMap* m, float* dqacc, int d, long long rows) {
     return FA_OK;
 }
 
+// Units per key block for the grouped backward: the smallest divisor g of the
+// group with items * g >= 2 * SMs (1 when the key blocks already fill the GPU
+// twice over), so that the longest unit is short next to a CTA's share.
+int choose_gsplit(long items, int group, int sms) {
+    if (items >= 2L * sms || group < 2) return 1;
+    for (int g = 2; g < group; ++g)
+        if (group % g == 0 && items * g >= 2L * sms) return g;
+    return group;
+}
+
+size_t dkv_part_bytes(int g, int B, int Hkv, int N, int d) { return (size_t)g * 2 * B * Hkv * N * d * sizeof(float); }
+
 fa_status bwd_main_impl(const BwdCtx& c, bool f32, const void* qb, const void* kb, const void* vb, const void* gb,
                         void* dk, void* dv, int B, int H, int N, int d, float scale, int causal, const int* kv_lens,
                         cudaStream_t stream, int Hkv = 0, int win_left = -1, int win_right = -1,
-                        const int* col_ptr = nullptr, const int* row_idx = nullptr) {
+                        const int* col_ptr = nullptr, const int* row_idx = nullptr, float* dkv_part = nullptr,
+                        size_t part_bytes = 0) {
     const int BH = c.BH, Np = c.Np;
     if (Hkv == 0) Hkv = H;
     if (Hkv < 1 || H % Hkv != 0) return fail(FA_ERR_INVALID_ARG, "H (%d) must be a multiple of Hkv (%d)", H, Hkv);
@@ -587,6 +600,18 @@ fa_status bwd_main_impl(const BwdCtx& c, bool f32, const void* qb, const void* k
     p.dk = dk;
     p.dv = dv;
     p.err = c.dev->err_word;
+    // the grouped instances (shared heads, window, block lists) may split a
+    // key block's query heads over several units when key blocks are few
+    const bool grouped = Hkv != H || col_ptr || win_left >= 0 || win_right >= 0;
+    p.gsplit = 1;
+    if (grouped && dkv_part) {
+        const int g = choose_gsplit(p.num_items, H / Hkv, c.dev->sms);
+        if (g > 1 && part_bytes >= dkv_part_bytes(g, B, Hkv, N, d)) {
+            p.gsplit = g;
+            p.dkv_part = dkv_part;
+            p.num_items *= g;
+        }
+    }
     const int grid = grid_for_items(p.num_items, c.dev->sms);
     cudaError_t e;
     if (col_ptr) {
@@ -611,6 +636,10 @@ fa_status bwd_main_impl(const BwdCtx& c, bool f32, const void* qb, const void* k
                        : fa::launch_bwd_main(d, causal != 0, f32, tq, tk, tv, tdo, tdq, p, grid, stream);
     }
     if (e != cudaSuccess) return cuda_fail(e, "backward main launch");
+    if (p.gsplit > 1) {
+        e = fa::launch_dkv_sum(dkv_part, p.gsplit, (size_t)B * Hkv * N * d, dk, dv, bw_grid(c.dev), stream);
+        if (e != cudaSuccess) return cuda_fail(e, "dK / dV partial sum launch");
+    }
     return FA_OK;
 }
 
@@ -704,7 +733,10 @@ fa_status fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o,
     BwdCtx c{};
     FA_TRY(bwd_setup(FA_BF16, B, H, N, d, scale, workspace, workspace_bytes, &c));
     FA_TRY(bwd_pre_impl(c, false, o, lse, dout, N, d, stream));
-    FA_TRY(bwd_main_impl(c, false, q, k, v, dout, dk, dv, B, H, N, d, scale, causal, kv_lens, stream, Hkv));
+    const size_t base = round_up(c.L.total, 256);
+    float* part = workspace_bytes > base ? reinterpret_cast<float*>(c.ws + base) : nullptr;
+    FA_TRY(bwd_main_impl(c, false, q, k, v, dout, dk, dv, B, H, N, d, scale, causal, kv_lens, stream, Hkv, -1, -1,
+                         nullptr, nullptr, part, part ? workspace_bytes - base : 0));
     return bwd_dq_impl(c, false, dq, N, d, scale, stream);
 }
 
@@ -755,6 +787,13 @@ fa_status fa_bwd_block_sparse(const void* q, const void* k, const void* v, const
     return bwd_dq_impl(c, false, dq, N, d, scale, stream);
 }
 
+size_t fa_bwd_gqa_workspace_size(int B, int H, int Hkv, int N, int d) {
+    if (B <= 0 || H <= 0 || N <= 0 || Hkv < 1 || H % Hkv != 0 || (d != 64 && d != 128)) return 0;
+    const size_t base = round_up(fa_bwd_workspace_size(FA_BF16, B, H, N, d), 256);
+    const int g = choose_gsplit((long)B * Hkv * ((N + 127) / 128), H / Hkv, sm_count_or_default());
+    return g > 1 ? base + dkv_part_bytes(g, B, Hkv, N, d) : base;
+}
+
 fa_status fa_bwd_window(const void* q, const void* k, const void* v, const void* o, const float* lse,
                         const void* dout, void* dq, void* dk, void* dv, int B, int H, int Hkv, int N, int d,
                         float scale, int causal, int window_left, int window_right, const int* kv_lens,
@@ -773,8 +812,10 @@ fa_status fa_bwd_window(const void* q, const void* k, const void* v, const void*
     BwdCtx c{};
     FA_TRY(bwd_setup(FA_BF16, B, H, N, d, scale, workspace, workspace_bytes, &c));
     FA_TRY(bwd_pre_impl(c, false, o, lse, dout, N, d, stream));
+    const size_t base = round_up(c.L.total, 256);
+    float* part = workspace_bytes > base ? reinterpret_cast<float*>(c.ws + base) : nullptr;
     FA_TRY(bwd_main_impl(c, false, q, k, v, dout, dk, dv, B, H, N, d, scale, causal, kv_lens, stream, Hkv, window_left,
-                         window_right));
+                         window_right, nullptr, nullptr, part, part ? workspace_bytes - base : 0));
     return bwd_dq_impl(c, false, dq, N, d, scale, stream);
 }
 

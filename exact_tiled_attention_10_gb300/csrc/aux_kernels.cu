@@ -353,6 +353,26 @@ __global__ void wait_selftest_kernel(unsigned int* err, unsigned long long limit
 
 }  // namespace
 
+// dv[e], dk[e] = sum over s of the split group's partial slices
+// part[s][0 (dV) / 1 (dK)][e] (float32, dK already scaled), as bf16.
+__global__ void __launch_bounds__(256) dkv_sum_kernel(const float* __restrict__ part, int gsplit, size_t n,
+                                                      __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv) {
+    const size_t n8 = n / 8;
+    for (size_t g = (size_t)blockIdx.x * blockDim.x + threadIdx.x; g < 2 * n8; g += (size_t)gridDim.x * blockDim.x) {
+        const int which = g >= n8;  // 0: dV, 1: dK
+        const size_t e = (g - which * n8) * 8;
+        float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int sidx = 0; sidx < gsplit; ++sidx) {
+            const float4* src = reinterpret_cast<const float4*>(part + ((size_t)(sidx * 2 + which)) * n + e);
+            const float4 x = __ldg(src), y = __ldg(src + 1);
+            a[0] += x.x; a[1] += x.y; a[2] += x.z; a[3] += x.w;
+            a[4] += y.x; a[5] += y.y; a[6] += y.z; a[7] += y.w;
+        }
+        *reinterpret_cast<uint4*>((which ? dk : dv) + e) =
+            make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]), pack_bf16x2(a[4], a[5]), pack_bf16x2(a[6], a[7]));
+    }
+}
+
 // Block-sparse lists transposed: for every key block k, the query blocks i
 // whose list holds k, ascending in i (one CTA, one thread per key block).
 // Membership is decided by one binary search per (i, k) in both passes, so
@@ -470,6 +490,12 @@ cudaError_t launch_bwd_dq(const float* dq_acc, void* dq, bool out_f32, float sca
                           int grid, cudaStream_t s) {
     if (out_f32) bwd_dq_kernel<true><<<grid, 256, 0, s>>>(dq_acc, dq, scale, BH, N, Np, d);
     else bwd_dq_kernel<false><<<grid, 256, 0, s>>>(dq_acc, dq, scale, BH, N, Np, d);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dkv_sum(const float* part, int gsplit, size_t n, void* dk, void* dv, int grid, cudaStream_t s) {
+    dkv_sum_kernel<<<grid, 256, 0, s>>>(part, gsplit, n, reinterpret_cast<__nv_bfloat16*>(dk),
+                                        reinterpret_cast<__nv_bfloat16*>(dv));
     return cudaGetLastError();
 }
 

@@ -107,6 +107,7 @@ struct Item {
     int bh, b, kt, kvl, i0, n;
     int qh0, ni;  // first query head row (b * H + ...), query blocks per query head
     int kvh, tb, seqlen;  // packed sequences: key/value head in the sequence, first token, length
+    int sub;              // split group: which part of the query heads (0 .. gsplit - 1)
 };
 
 // GQA: the kernel instance for shared key/value heads (compiled separately so
@@ -128,6 +129,13 @@ __device__ __forceinline__ Item get_item(int it, const ParamsT<WINDOW, SPARSE>& 
     Item I;
     const int Hkv = GQA ? p.Hkv : p.H;
     const int BH = p.B * Hkv;
+    // split group (GQA, not packed): consecutive units share a key block
+    const int gs = (GQA && !VARLEN) ? max(p.gsplit, 1) : 1;
+    I.sub = 0;
+    if (gs > 1) {
+        I.sub = it % gs;
+        it /= gs;
+    }
     if (CAUSAL) {  // key blocks near the start see the most query rows: first
         I.kt = it / BH;
         I.bh = it % BH;
@@ -137,8 +145,9 @@ __device__ __forceinline__ Item get_item(int it, const ParamsT<WINDOW, SPARSE>& 
     }
     I.b = I.bh / Hkv;
     const int group = GQA ? p.H / Hkv : 1;
+    const int gper = group / gs;  // query heads of this unit
     I.kvh = I.bh - I.b * Hkv;
-    I.qh0 = VARLEN ? I.kvh * group : GQA ? I.b * p.H + I.kvh * group : I.bh;
+    I.qh0 = VARLEN ? I.kvh * group : GQA ? I.b * p.H + I.kvh * group + I.sub * gper : I.bh;
     I.tb = 0;
     I.seqlen = p.N;
     if (VARLEN) {
@@ -175,7 +184,7 @@ __device__ __forceinline__ Item get_item(int it, const ParamsT<WINDOW, SPARSE>& 
     } else {
         I.ni = (key0 >= kvl) ? 0 : max(iend - I.i0, 0);
     }
-    I.n = I.ni * group;
+    I.n = I.ni * gper;
     return I;
 }
 // Query head row bhq and query block i of consecutive steps of an item:
@@ -475,9 +484,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float z[32];
 #pragma unroll
                     for (int e = 0; e < 32; ++e) z[e] = 0.f;
-                    void* dst = h ? p.dk : p.dv;
+                    if (GQA && p.gsplit > 1) {
+                        float* part = p.dkv_part + (size_t)(I.sub * 2 + h) * p.B * p.Hkv * p.N * C::D;
 #pragma unroll
-                    for (int c = 0; c < C::D; c += 32) store_chunk32<OUT_F32>(dst, krow * C::D + c, z);
+                        for (int c = 0; c < C::D; c += 32) store_chunk32<true>(part, krow * C::D + c, z);
+                    } else {
+                        void* dst = h ? p.dk : p.dv;
+#pragma unroll
+                        for (int c = 0; c < C::D; c += 32) store_chunk32<OUT_F32>(dst, krow * C::D + c, z);
+                    }
                 }
                 continue;
             }
@@ -588,6 +603,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const float mul = h ? p.scale : 1.f;
             void* dst = h ? p.dk : p.dv;
+            const bool to_part = GQA && !VARLEN && p.gsplit > 1;  // split group: float32 partial slice
+            float* part = to_part ? p.dkv_part + (size_t)(I.sub * 2 + h) * p.B * p.Hkv * p.N * C::D : nullptr;
             const uint32_t tacc = tmem + lane_off + (h ? C::TM_DK : C::TM_DV);
 #pragma unroll 1
             for (int c = 0; c < C::D; c += 32) {
@@ -596,7 +613,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float f[32];
 #pragma unroll
                 for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(a[e]) * mul;
-                if (key < (VARLEN ? I.seqlen : p.N)) store_chunk32<OUT_F32>(dst, krow * C::D + c, f);
+                if (key < (VARLEN ? I.seqlen : p.N)) {
+                    if (to_part)
+                        store_chunk32<true>(part, krow * C::D + c, f);
+                    else
+                        store_chunk32<OUT_F32>(dst, krow * C::D + c, f);
+                }
             }
             tc_fence_before();
             mbar_arrive(BAR(C::B_ACCEMPTY));

@@ -104,6 +104,12 @@ struct BwdParams {
     const int* cu_seqlens;
     int total;
     unsigned int* err;
+    // Shared key/value heads with few key blocks: each key block's group of
+    // query heads is split over gsplit work units; unit s writes float32
+    // partial dV, scale * dK to dkv_part [gsplit][2 (dV, dK)][B*Hkv][N][d],
+    // summed into dv, dk by a separate kernel.  gsplit = 1: written directly.
+    int gsplit;
+    float* dkv_part;
 };
 
 // Sliding window (flash_attn_func's window_size, chapter 18 §18.7.1): key j
@@ -150,6 +156,8 @@ cudaError_t launch_fwd_sparse(int d, bool causal, const FwdMaps& m, const FwdPar
 cudaError_t launch_bwd_main_sparse(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
                                    const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
                                    const BwdParamsSparse& p, int grid, cudaStream_t stream);
+// dv, dk = sums of the gsplit partial slices (bf16).
+cudaError_t launch_dkv_sum(const float* part, int gsplit, size_t n, void* dk, void* dv, int grid, cudaStream_t stream);
 // Transposes the query-block lists into per-key-block lists (one CTA).
 cudaError_t launch_block_lists_transpose(const int* row_ptr, const int* col_idx, int nqb, int nkb, int* col_ptr,
                                          int* row_idx, cudaStream_t stream);

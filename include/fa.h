@@ -207,7 +207,13 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o,
 /* Backward with shared key/value heads (see fa_fwd_gqa), bf16: dq is
  * [B,H,N,d]; dk, dv are [B,Hkv,N,d] and hold the sum over the H / Hkv query
  * heads that share each key/value head (the gradient of the broadcast).
- * Workspace: fa_bwd_workspace_size(FA_BF16, B, H, N, d). */
+ * Workspace: at least fa_bwd_workspace_size(FA_BF16, B, H, N, d) bytes.
+ * With fa_bwd_gqa_workspace_size(B, H, Hkv, N, d) bytes (larger when there
+ * are fewer than 2 x SMs key blocks in all), each key block's query heads
+ * are split over several work units that write float32 partial dK / dV to
+ * the extra space, summed by one more kernel: the causal longest-first
+ * schedule then stays balanced.  fa_bwd_window uses the same extra space. */
+size_t fa_bwd_gqa_workspace_size(int B, int H, int Hkv, int N, int d);
 fa_status fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o,
                      const float* lse, const void* dout, void* dq, void* dk, void* dv,
                      int B, int H, int Hkv, int N, int d, float scale, int causal,
