@@ -308,6 +308,65 @@ def max_over_ranks(ws, x, device):
     return float(t.item())
 
 
+def e2e_pipelined(step_a, step_b, steps):
+    """End to end through the C ABI with pinned host buffers: every step copies
+    its inputs (Q, K, V, dO) in from the host, runs the whole step and copies
+    its results (O, LSE, dQ, dK, dV, FP8 O) back.  The copies of step k+1 (in)
+    and k-1 (out) run on their own streams while step k computes, on two sets
+    of device buffers; events keep a buffer from being overwritten while it is
+    still read or written.  Returns the milliseconds of `steps` steps, from
+    the first copy in to the last copy out."""
+    import torch
+    dev = step_a.dev
+    steps_ = (step_a, step_b)
+    ins = lambda st: (st.q, st.k, st.v, st.do)
+    outs = lambda st: (st.o, st.lse, st.dq, st.dk, st.dv, st.o8)
+    hin = [[t.cpu().pin_memory() for t in ins(st)] for st in steps_]
+    hout = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs(st)] for st in steps_]
+    s_in, s_c, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+    ev = lambda: torch.cuda.Event()
+
+    def run(n, timed):
+        done_c = [None, None]   # compute of the last step on buffer b
+        done_o = [None, None]   # copy out of the last step on buffer b
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        s_in.record_event(t0)
+        for k in range(n):
+            b = k % 2
+            st = steps_[b]
+            with torch.cuda.stream(s_in):
+                if done_c[b] is not None:
+                    s_in.wait_event(done_c[b])
+                for dd, hh in zip(ins(st), hin[b]):
+                    dd.copy_(hh, non_blocking=True)
+                e_in = ev()
+                s_in.record_event(e_in)
+            with torch.cuda.stream(s_c):
+                s_c.wait_event(e_in)
+                if done_o[b] is not None:
+                    s_c.wait_event(done_o[b])
+                st.run()
+                done_c[b] = ev()
+                s_c.record_event(done_c[b])
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(done_c[b])
+                for hh, dd in zip(hout[b], outs(st)):
+                    hh.copy_(dd, non_blocking=True)
+                done_o[b] = ev()
+                s_out.record_event(done_o[b])
+        for e in done_o:
+            if e is not None:
+                s_in.wait_event(e)
+        s_in.record_event(t1)
+        torch.cuda.synchronize(dev)
+        return t0.elapsed_time(t1)
+
+    run(3, False)  # warm-up
+    return run(steps, True)
+
+
 def main():
     args = parse_args()
     ws, rank, local = dist_setup(args.gpus)
@@ -393,28 +452,10 @@ def main():
 
     # ---- end to end through the public API with pinned host buffers
     e2e_steps = args.e2e_steps or min(args.steps, 100)
-    hin = [t.cpu().pin_memory() for t in (step.q, step.k, step.v, step.do)]
-    hout = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-            for t in (step.o, step.lse, step.dq, step.dk, step.dv, step.o8)]
-    dins = (step.q, step.k, step.v, step.do)
-    douts = (step.o, step.lse, step.dq, step.dk, step.dv, step.o8)
-    h2d = sum(t.numel() * t.element_size() for t in hin)
-    d2h = sum(t.numel() * t.element_size() for t in hout)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e2e_ms = 0.0
-    for i in range(e2e_steps + 2):
-        step.flush_l2()
-        torch.cuda.synchronize()
-        e0.record()
-        for dd, hh in zip(dins, hin):
-            dd.copy_(hh, non_blocking=True)
-        step.run()
-        for hh, dd in zip(hout, douts):
-            hh.copy_(dd, non_blocking=True)
-        e1.record()
-        torch.cuda.synchronize()
-        if i >= 2:
-            e2e_ms += e0.elapsed_time(e1)
+    e2e_ms = e2e_pipelined(step, Step(w, causal, device, seed_offset=1000 * rank), e2e_steps)
+    hin_bytes = sum(t.numel() * t.element_size() for t in (step.q, step.k, step.v, step.do))
+    hout_bytes = sum(t.numel() * t.element_size() for t in (step.o, step.lse, step.dq, step.dk, step.dv, step.o8))
+    h2d, d2h = hin_bytes, hout_bytes
     e2e_ms = max_over_ranks(ws, e2e_ms, device)
     e2e_value = ws * flops_step * e2e_steps / (e2e_ms / 1e3) / 1e12
 
@@ -441,7 +482,11 @@ def main():
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": {"value": round(e2e_value, 2), "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+                    "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                    "how": "C ABI with pinned host buffers; every step copies Q, K, V, dO in and O, LSE, "
+                           "dQ, dK, dV, FP8 O out; copies of neighbouring steps overlap compute (two "
+                           "device buffer sets, three streams); inputs of %.0f MB per step, "
+                           "L2 129 MB" % (h2d / 1e6)},
             "gpu_launches": step.launches_per_step * args.steps,
             "clocks": clk,
             "wall_s": round(wall, 3),
