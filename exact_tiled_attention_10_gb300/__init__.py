@@ -63,6 +63,7 @@ _SIGS = {
     "fa_fwd_block_sparse": ([_vp] * 5 + [_i, _i, _i, _i, _i, _f, _i, _vp, _vp, _vp, _vp], _i),
     "fa_bwd_block_sparse_workspace_size": ([_i] * 4, _sz),
     "fa_bwd_gqa_workspace_size": ([_i] * 5, _sz),
+    "fa_selftest_quantiser_division": ([_vp, _vp, _i, _sz, _vp, _vp, _vp], _i),
     "fa_bwd_block_sparse": ([_vp] * 9 + [_i, _i, _i, _i, _i, _f, _i, _vp, _vp, _vp, _vp, _sz, _vp], _i),
     "fa_fwd_varlen": ([_vp] * 6 + [_i, _i, _i, _i, _i, _i, _f, _i, _vp], _i),
     "fa_bwd_varlen_workspace_size": ([_i] * 4, _sz),

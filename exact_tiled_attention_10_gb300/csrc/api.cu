@@ -393,6 +393,15 @@ fa_status fa_check_device_status(fa_stream_t stream) {
     return FA_OK;
 }
 
+fa_status fa_selftest_quantiser_division(const float* x, const float* s, int ns, size_t n, float* q_fast,
+                                        float* q_ieee, fa_stream_t stream) {
+    if (!x || !s || !q_fast || !q_ieee) return fail(FA_ERR_INVALID_ARG, "null pointer");
+    if (ns <= 0) return fail(FA_ERR_INVALID_ARG, "ns must be positive");
+    cudaError_t e = fa::launch_shared_div_check(x, s, ns, n, q_fast, q_ieee, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "division self-test launch");
+    return FA_OK;
+}
+
 fa_status fa_selftest_wait_timeout(unsigned int limit_us, int* waited_out, fa_stream_t stream) {
     FA_CHECK_PTR(waited_out);
     if (limit_us == 0 || limit_us > 1000000u) return fail(FA_ERR_INVALID_ARG, "limit_us must be in [1, 1e6]");

@@ -193,10 +193,38 @@ __global__ void __launch_bounds__(256) bwd_dq_varlen_kernel(const float* __restr
     }
 }
 
+// x / s correctly rounded (IEEE float32 division) for a divisor shared by
+// many dividends, by Markstein's method (P. Markstein, "Computation of
+// elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
+// Dev. 34(1), 1990): with r = 1/s correctly rounded and q = RN(x r), the
+// residual x - q s is exact under a fused multiply-add and RN(q + (x - q s) r)
+// is the correctly rounded quotient.  Valid while s, 1/s and the quotients
+// stay normal; callers use it for 2^-100 < s < 2^100 (quotients below the
+// normal range are far below the smallest E4M3 step and quantise to 0 either
+// way) and take __fdiv_rn otherwise.
+struct SharedDivisor {
+    float s, r;
+    __device__ __forceinline__ float div(float x) const {
+        const float q = __fmul_rn(x, r);
+        const float res = fmaf(-q, s, x);
+        return fmaf(res, r, q);
+    }
+};
+
+__device__ __forceinline__ SharedDivisor shared_divisor(float s) {
+    SharedDivisor d;
+    d.s = s;
+    d.r = __frcp_rn(s);
+    return d;
+}
+
+__device__ __forceinline__ bool shared_divisor_ok(float s) { return s > 0x1p-100f && s < 0x1p100f; }
+
 // One CTA (256 threads) per (head, 64-row block); d = 128 -> 8192 elements,
 // 32 per thread, read once and kept in registers across the block's absmax
-// reduction.  s = amax / 448 and x / s are IEEE float32 divisions; the
-// conversion rounds to nearest even and saturates to +-448.
+// reduction.  s = amax / 448 and x / s are IEEE float32 divisions (x / s by
+// SharedDivisor, which gives the same quotients); the conversion rounds to
+// nearest even and saturates to +-448.
 __global__ void __launch_bounds__(256) quantize_fp8_kernel(const __nv_bfloat16* __restrict__ x,
                                                            uint8_t* __restrict__ x8, float* __restrict__ scales,
                                                            int BH, int N, int D, int nblk) {
@@ -235,15 +263,19 @@ __global__ void __launch_bounds__(256) quantize_fp8_kernel(const __nv_bfloat16* 
         for (int w = 1; w < 8; ++w) m = fmaxf(m, red[par][w]);
         const float s = (m > 0.f) ? __fdiv_rn(m, 448.f) : 1.f;
         if (threadIdx.x == 0) scales[blk] = s;
+        const SharedDivisor dv = shared_divisor(s);
+        const bool fast = shared_divisor_ok(s);  // uniform over the CTA
 #pragma unroll
         for (int i = 0; i < G; ++i) {
             const int g = threadIdx.x + i * 256;
             if (g >= ng) continue;
             float f[8];
             unpack8(raw[i], f);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) f[k] = fast ? dv.div(f[k]) : __fdiv_rn(f[k], s);
             uint2 out;
-            out.x = pack_e4m3x4(__fdiv_rn(f[0], s), __fdiv_rn(f[1], s), __fdiv_rn(f[2], s), __fdiv_rn(f[3], s));
-            out.y = pack_e4m3x4(__fdiv_rn(f[4], s), __fdiv_rn(f[5], s), __fdiv_rn(f[6], s), __fdiv_rn(f[7], s));
+            out.x = pack_e4m3x4(f[0], f[1], f[2], f[3]);
+            out.y = pack_e4m3x4(f[4], f[5], f[6], f[7]);
             reinterpret_cast<uint2*>(x8 + base)[g] = out;
         }
     }
@@ -504,6 +536,22 @@ cudaError_t launch_block_lists_transpose(const int* row_ptr, const int* col_idx,
     const int threads = nkb < 1024 ? ((nkb + 31) / 32) * 32 : 1024;
     block_lists_transpose_kernel<<<1, threads, (nkb + 1) * sizeof(int), s>>>(row_ptr, col_idx, nqb, nkb, col_ptr,
                                                                              row_idx);
+    return cudaGetLastError();
+}
+
+// Test hook: q[i] = x[i] / s[i % ns] by SharedDivisor and by __fdiv_rn.
+__global__ void shared_div_check_kernel(const float* __restrict__ x, const float* __restrict__ s, int ns, size_t n,
+                                        float* __restrict__ q_fast, float* __restrict__ q_ieee) {
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+        const float d = s[i % ns];
+        q_fast[i] = shared_divisor(d).div(x[i]);
+        q_ieee[i] = __fdiv_rn(x[i], d);
+    }
+}
+
+cudaError_t launch_shared_div_check(const float* x, const float* s, int ns, size_t n, float* q_fast, float* q_ieee,
+                                    cudaStream_t st) {
+    shared_div_check_kernel<<<1024, 256, 0, st>>>(x, s, ns, n, q_fast, q_ieee);
     return cudaGetLastError();
 }
 

@@ -156,6 +156,10 @@ cudaError_t launch_fwd_sparse(int d, bool causal, const FwdMaps& m, const FwdPar
 cudaError_t launch_bwd_main_sparse(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
                                    const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
                                    const BwdParamsSparse& p, int grid, cudaStream_t stream);
+// Test hook of the quantiser's division: q_fast = x / s by the shared-divisor
+// method, q_ieee = __fdiv_rn(x, s), s[i % ns] for element i.
+cudaError_t launch_shared_div_check(const float* x, const float* s, int ns, size_t n, float* q_fast, float* q_ieee,
+                                    cudaStream_t stream);
 // dv, dk = sums of the gsplit partial slices (bf16).
 cudaError_t launch_dkv_sum(const float* part, int gsplit, size_t n, void* dk, void* dv, int grid, cudaStream_t stream);
 // Transposes the query-block lists into per-key-block lists (one CTA).

@@ -79,6 +79,15 @@ fa_status fa_check_device_status(fa_stream_t stream);
  * FA_ERR_TIMEOUT and clears the word.  No trap, no hang, no fault. */
 fa_status fa_selftest_wait_timeout(unsigned int limit_us, int* waited_out, fa_stream_t stream);
 
+/* Self-test of the E4M3 quantiser's division (fa_quantize_fp8 divides every
+ * element of a 64-row block by the block's scale s = amax / 448, [CH18]
+ * §18.6.2): for n float32 device elements, q_fast[i] = x[i] / s[i % ns] by
+ * the quantiser's shared-divisor method and q_ieee[i] = the IEEE float32
+ * quotient; the two must agree bit for bit.  Device pointers; asynchronous on
+ * `stream`. */
+fa_status fa_selftest_quantiser_division(const float* x, const float* s, int ns, size_t n,
+                                         float* q_fast, float* q_ieee, fa_stream_t stream);
+
 /* ---------------------------------------------------------------- forward */
 
 /* bf16 forward ([FA2] §4 Algorithm 1).  q,k,v: bf16 inputs; o: bf16 output;

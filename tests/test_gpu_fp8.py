@@ -46,6 +46,43 @@ def test_quantiser_bit_exact_long_seq_head():
     np.testing.assert_array_equal(c[:, :2].cpu().numpy(), rc)
 
 
+def test_quantiser_division_matches_ieee_bitwise():
+    """The quantiser divides by a scale shared by a whole block with one
+    reciprocal and a fused-multiply-add correction (Markstein's method); its
+    quotients must equal IEEE float32 division bit for bit, or the E4M3 codes
+    could differ from the oracle's at rounding midpoints."""
+    import ctypes
+    from exact_tiled_attention_10_gb300 import load_library
+    g = torch.Generator(device="cpu").manual_seed(77)
+    n, ns = 1 << 24, 4096
+    x = (torch.randn(n, generator=g) * torch.exp2(torch.randint(-20, 21, (n,), generator=g).float()))
+    x = x.to(torch.bfloat16).float()  # the quantiser's dividends are bf16 values
+    amax = torch.rand(ns, generator=g) * torch.exp2(torch.randint(-60, 61, (ns,), generator=g).float())
+    s = (amax.to(torch.bfloat16).float() / 448.0).clamp_min(1e-30)
+    s[:64] = torch.exp2(torch.arange(-32, 32).float())  # exact powers of two
+    x, s = x.to(DEV), s.to(DEV)
+    qf, qi = torch.empty_like(x), torch.empty_like(x)
+    lib = load_library()
+    st = lib.fa_selftest_quantiser_division(x.data_ptr(), s.data_ptr(), ns, n, qf.data_ptr(), qi.data_ptr(),
+                                            torch.cuda.current_stream().cuda_stream)
+    assert st == 0
+    torch.cuda.synchronize()
+    bad = (qf.view(torch.int32) != qi.view(torch.int32)).sum().item()
+    assert bad == 0, "%d quotients differ from IEEE division" % bad
+
+
+@pytest.mark.parametrize("mag", [1e35, 1e-35, 1e-3, 1e3])
+def test_quantiser_bit_exact_extreme_scales(mag):
+    """Scales outside the shared-divisor range take IEEE division; both paths
+    must still reproduce the oracle's codes."""
+    x = (qkv(1, 2, 200, 128, 91, device=DEV, with_dout=False)[0].float() * mag).to(torch.bfloat16)
+    c, s = quantize_fp8(x)
+    torch.cuda.synchronize()
+    rc, rs = oracle.quantize_fp8(x)
+    np.testing.assert_array_equal(s.cpu().numpy(), rs)
+    np.testing.assert_array_equal(c.cpu().numpy(), rc)
+
+
 def _fp8_run(B, H, N, seed, causal, kv=None):
     q, k, v = qkv(B, H, N, 128, seed, device=DEV, with_dout=False)
     (q8, sq), (k8, sk), (v8, sv) = (quantize_fp8(t) for t in (q, k, v))
