@@ -256,7 +256,7 @@ class Step:
                       "bwd_dq": B * H * Np * d * 4 + n * 2,
                       "quant_fp8": 3 * (n * 2 + n + B * H * nb * 4),
                       "fwd_fp8": 3 * n + n * 2 + B * H * N * 4}
-        self.launches_per_step = 8 + int(self.split_bf16 > 1) + int(self.split_fp8 > 1)
+        self.launches_per_step = 6 + int(self.split_bf16 > 1) + int(self.split_fp8 > 1)
 
     def _ck(self, st):
         if st != 0:
@@ -280,8 +280,9 @@ class Step:
         rec(3)
         self._ck(lib.fa_bwd_dq(p(self.dq), B, H, N, d, self.scale, p(self.ws), self.ws_bytes, s))
         rec(4)
-        for x, x8, sc in zip((self.q, self.k, self.v), self.x8, self.sc):
-            self._ck(lib.fa_quantize_fp8(p(x), p(x8), p(sc), B, H, N, d, s))
+        self._ck(lib.fa_quantize_fp8_qkv(p(self.q), p(self.k), p(self.v), p(self.x8[0]), p(self.x8[1]),
+                                         p(self.x8[2]), p(self.sc[0]), p(self.sc[1]), p(self.sc[2]), B, H, H, N, d,
+                                         s))
         rec(5)
         self._ck(lib.fa_fwd_fp8_split(p(self.x8[0]), p(self.x8[1]), p(self.x8[2]), p(self.sc[0]),
                                       p(self.sc[1]), p(self.sc[2]), p(self.o8), p(self.lse8), B, H, N, d,

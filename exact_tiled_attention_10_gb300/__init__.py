@@ -22,7 +22,7 @@ from typing import Optional, Tuple
 import torch
 
 __all__ = ["forward", "forward_split", "forward_varlen", "backward_varlen", "backward",
-           "block_lists", "forward_block_sparse", "backward_block_sparse", "quantize_fp8", "forward_fp8", "forward_fp8_split",
+           "block_lists", "forward_block_sparse", "backward_block_sparse", "quantize_fp8_qkv", "quantize_fp8", "forward_fp8", "forward_fp8_split",
            "split_count", "split_workspace_size", "check_device_status",
            "selftest_wait_timeout",
            "bwd_workspace_size", "fwd_workspace_size", "library_path", "load_library", "FAError"]
@@ -64,6 +64,7 @@ _SIGS = {
     "fa_bwd_block_sparse_workspace_size": ([_i] * 4, _sz),
     "fa_bwd_gqa_workspace_size": ([_i] * 5, _sz),
     "fa_selftest_quantiser_division": ([_vp, _vp, _i, _sz, _vp, _vp, _vp], _i),
+    "fa_quantize_fp8_qkv": ([_vp] * 9 + [_i] * 5 + [_vp], _i),
     "fa_bwd_block_sparse": ([_vp] * 9 + [_i, _i, _i, _i, _i, _f, _i, _vp, _vp, _vp, _vp, _sz, _vp], _i),
     "fa_fwd_varlen": ([_vp] * 6 + [_i, _i, _i, _i, _i, _i, _f, _i, _vp], _i),
     "fa_bwd_varlen_workspace_size": ([_i] * 4, _sz),
@@ -410,6 +411,25 @@ def quantize_fp8(x: torch.Tensor, out: Optional[torch.Tensor] = None,
         if scales is None else scales
     _check(lib.fa_quantize_fp8(_ptr(x), _ptr(x8), _ptr(sc), B, H, N, d, _stream(x)))
     return x8, sc
+
+
+def quantize_fp8_qkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor):
+    """quantize_fp8 of q [B,H,N,d], k, v [B,Hkv,N,d] (bf16) in one launch:
+    ((q8, sq), (k8, sk), (v8, sv))."""
+    lib = load_library()
+    _need_cuda(q, k, v)
+    if q.dtype != torch.bfloat16 or k.dtype != q.dtype or v.dtype != q.dtype or k.shape != v.shape:
+        raise ValueError("q [B,H,N,d], k, v [B,Hkv,N,d] bfloat16")
+    B, H, N, d = q.shape
+    Hkv = k.shape[1]
+    nb = lib.fa_fp8_num_blocks(N)
+    out = []
+    for t, h in ((q, H), (k, Hkv), (v, Hkv)):
+        out.append((torch.empty(t.shape, dtype=torch.uint8, device=t.device),
+                    torch.empty((B, h, nb), dtype=torch.float32, device=t.device)))
+    _check(lib.fa_quantize_fp8_qkv(_ptr(q), _ptr(k), _ptr(v), _ptr(out[0][0]), _ptr(out[1][0]), _ptr(out[2][0]),
+                                   _ptr(out[0][1]), _ptr(out[1][1]), _ptr(out[2][1]), B, H, Hkv, N, d, _stream(q)))
+    return tuple(out)
 
 
 def forward_fp8(q8, k8, v8, sq, sk, sv, causal: bool = False, scale: Optional[float] = None,

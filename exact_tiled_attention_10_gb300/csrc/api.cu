@@ -912,7 +912,34 @@ fa_status fa_quantize_fp8(const void* x_bf16, void* x_e4m3, float* scales, int B
     FA_CHECK_PTR(scales);
     DeviceInfo* dev = nullptr;
     FA_TRY(device_info(&dev));
-    cudaError_t e = fa::launch_quantize_fp8(x_bf16, x_e4m3, scales, B * H, N, d, dev->sms * 8, stream);
+    fa::QuantJobs jobs;
+    memset(&jobs, 0, sizeof(jobs));
+    jobs.x[0] = x_bf16;
+    jobs.x8[0] = x_e4m3;
+    jobs.scales[0] = scales;
+    jobs.heads[0] = B * H;
+    cudaError_t e = fa::launch_quantize_fp8(jobs, N, d, dev->sms * 8, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "quantiser launch");
+    return FA_OK;
+}
+
+fa_status fa_quantize_fp8_qkv(const void* q, const void* k, const void* v, void* q8, void* k8, void* v8, float* sq,
+                              float* sk, float* sv, int B, int H, int Hkv, int N, int d, fa_stream_t stream) {
+    FA_TRY(check_common(B, H, N, d, 1.0f));
+    if (Hkv < 1 || H % Hkv != 0) return fail(FA_ERR_INVALID_ARG, "H (%d) must be a multiple of Hkv (%d)", H, Hkv);
+    FA_CHECK_PTR(q);
+    FA_CHECK_PTR(k);
+    FA_CHECK_PTR(v);
+    FA_CHECK_PTR(q8);
+    FA_CHECK_PTR(k8);
+    FA_CHECK_PTR(v8);
+    FA_CHECK_PTR(sq);
+    FA_CHECK_PTR(sk);
+    FA_CHECK_PTR(sv);
+    DeviceInfo* dev = nullptr;
+    FA_TRY(device_info(&dev));
+    const fa::QuantJobs jobs = {{q, k, v}, {q8, k8, v8}, {sq, sk, sv}, {B * H, B * Hkv, B * Hkv}};
+    cudaError_t e = fa::launch_quantize_fp8(jobs, N, d, dev->sms * 8, stream);
     if (e != cudaSuccess) return cuda_fail(e, "quantiser launch");
     return FA_OK;
 }

@@ -225,15 +225,22 @@ __device__ __forceinline__ bool shared_divisor_ok(float s) { return s > 0x1p-100
 // reduction.  s = amax / 448 and x / s are IEEE float32 divisions (x / s by
 // SharedDivisor, which gives the same quotients); the conversion rounds to
 // nearest even and saturates to +-448.
-__global__ void __launch_bounds__(256) quantize_fp8_kernel(const __nv_bfloat16* __restrict__ x,
-                                                           uint8_t* __restrict__ x8, float* __restrict__ scales,
-                                                           int BH, int N, int D, int nblk) {
+// The blocks of up to three tensors in one launch (Q, K, V): tensor t has
+// rows[t] = B * heads_t heads of N rows each.
+__global__ void __launch_bounds__(256) quantize_fp8_kernel(QuantJobs jobs, int N, int D, int nblk) {
     constexpr int G = 4;  // uint4 groups (8 elements) per thread: 256 * 4 * 8 = 64 rows x 128
     __shared__ float red[2][8];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int per_row = D / 8;  // uint4 groups per row
+    const long n0 = (long)jobs.heads[0] * nblk, n1 = n0 + (long)jobs.heads[1] * nblk;
+    const long total = n1 + (long)jobs.heads[2] * nblk;
     int par = 0;
-    for (long blk = blockIdx.x; blk < (long)BH * nblk; blk += gridDim.x, par ^= 1) {
+    for (long gblk = blockIdx.x; gblk < total; gblk += gridDim.x, par ^= 1) {
+        const int t = gblk < n0 ? 0 : gblk < n1 ? 1 : 2;
+        const long blk = gblk - (t == 0 ? 0 : t == 1 ? n0 : n1);
+        const __nv_bfloat16* __restrict__ x = reinterpret_cast<const __nv_bfloat16*>(jobs.x[t]);
+        uint8_t* __restrict__ x8 = reinterpret_cast<uint8_t*>(jobs.x8[t]);
+        float* __restrict__ scales = jobs.scales[t];
         const long bh = blk / nblk;
         const int ib = (int)(blk - bh * nblk);
         const int r0 = ib * 64;
@@ -555,11 +562,9 @@ cudaError_t launch_shared_div_check(const float* x, const float* s, int ns, size
     return cudaGetLastError();
 }
 
-cudaError_t launch_quantize_fp8(const void* x, void* x8, float* scales, int BH, int N, int d, int grid,
-                                cudaStream_t s) {
+cudaError_t launch_quantize_fp8(const QuantJobs& jobs, int N, int d, int grid, cudaStream_t s) {
     const int nblk = (N + 63) / 64;
-    quantize_fp8_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(x), reinterpret_cast<uint8_t*>(x8),
-                                             scales, BH, N, d, nblk);
+    quantize_fp8_kernel<<<grid, 256, 0, s>>>(jobs, N, d, nblk);
     return cudaGetLastError();
 }
 

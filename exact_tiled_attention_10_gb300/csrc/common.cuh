@@ -189,8 +189,14 @@ cudaError_t launch_bwd_pre(const void* o, const void* dout, bool in_f32, const f
                            int grid, cudaStream_t stream);
 cudaError_t launch_bwd_dq(const float* dq_acc, void* dq, bool out_f32, float scale, int BH, int N,
                           int Np, int d, int grid, cudaStream_t stream);
-cudaError_t launch_quantize_fp8(const void* x, void* x8, float* scales, int BH, int N, int d,
-                                int grid, cudaStream_t stream);
+// Up to three tensors quantised by one launch (unused slots: heads = 0).
+struct QuantJobs {
+    const void* x[3];  // bf16
+    void* x8[3];       // E4M3 codes
+    float* scales[3];
+    int heads[3];  // B * heads of each tensor
+};
+cudaError_t launch_quantize_fp8(const QuantJobs& jobs, int N, int d, int grid, cudaStream_t stream);
 // Merges the split-key partials of the forward into O (bf16) and LSE.
 cudaError_t launch_lse_merge(const float* o_part, const float* lse_part, int num_whole, int num_tail, int splits,
                              bool causal, int BH, int num_qp, int N, int d, void* o, float* lse, cudaStream_t stream);

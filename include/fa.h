@@ -327,6 +327,14 @@ int fa_fp8_num_blocks(int N);
 fa_status fa_quantize_fp8(const void* x_bf16, void* x_e4m3, float* scales,
                           int B, int H, int N, int d, fa_stream_t stream);
 
+/* fa_quantize_fp8 of q [B,H,N,d], k and v [B,Hkv,N,d] in one launch (the
+ * three inputs of fa_fwd_fp8 / fa_fwd_fp8_split), same codes and scales as
+ * three separate calls: sq [B,H,ceil(N/64)], sk, sv [B,Hkv,ceil(N/64)].
+ * FA_ERR_INVALID_ARG if H % Hkv != 0. */
+fa_status fa_quantize_fp8_qkv(const void* q, const void* k, const void* v, void* q8, void* k8,
+                              void* v8, float* sq, float* sk, float* sv, int B, int H, int Hkv,
+                              int N, int d, fa_stream_t stream);
+
 /* FP8 forward: q8/k8/v8 are E4M3 [B,H,N,d] with per-64-row-block scales
  * sq/sk/sv (as written by fa_quantize_fp8), so that X ~= s_block * X8.
  * S = scale * (s_q s_k) (Q8 K8^T) accumulates in float32; the softmax runs in

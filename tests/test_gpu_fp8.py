@@ -83,6 +83,18 @@ def test_quantiser_bit_exact_extreme_scales(mag):
     np.testing.assert_array_equal(c.cpu().numpy(), rc)
 
 
+def test_quantise_qkv_in_one_launch_equals_separate_calls():
+    from exact_tiled_attention_10_gb300 import quantize_fp8_qkv
+    q = qkv(2, 4, 333, 128, 95, device=DEV, with_dout=False)[0]
+    _, k, v = qkv(2, 2, 333, 128, 96, device=DEV, with_dout=False)
+    fused = quantize_fp8_qkv(q, k, v)
+    torch.cuda.synchronize()
+    for (c, s), x in zip(fused, (q, k, v)):
+        c1, s1 = quantize_fp8(x)
+        torch.cuda.synchronize()
+        assert torch.equal(c, c1) and torch.equal(s, s1)
+
+
 def _fp8_run(B, H, N, seed, causal, kv=None):
     q, k, v = qkv(B, H, N, 128, seed, device=DEV, with_dout=False)
     (q8, sq), (k8, sk), (v8, sv) = (quantize_fp8(t) for t in (q, k, v))
