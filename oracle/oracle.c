@@ -301,6 +301,76 @@ int oracle_bwd(const double* q, const double* k, const double* v, const double* 
 }
 
 /* ======================================================================== */
+/* 1b. Rectangular attention (N_q query rows, N_k keys): decoding against a  */
+/*     key/value cache and cross-attention ([CH18] §18.8.2: the query of a   */
+/*     decode step is [b, n_q, d] with n_q << n_kv; §18.7.1 varlen API with  */
+/*     separate query and key lengths).  With the causal mask the queries    */
+/*     are the last N_q positions of the N_k-long sequence: query i sees key */
+/*     j iff j <= i + (N_k - N_q); key padding as above.                     */
+/* ======================================================================== */
+
+static void rect_head_forward(const double* q, const double* k, const double* v, double* o, double* lse,
+                              double* s, int Nq, int Nk, int d, double scale, int causal, int kv_len) {
+    const int off = Nk - Nq;
+    for (int i = 0; i < Nq; ++i) {
+        double mx = -INFINITY;
+        for (int j = 0; j < Nk; ++j) {
+            s[j] = -INFINITY;
+            if (j < kv_len && (!causal || j <= i + off)) {
+                double acc = 0.0;
+                for (int t = 0; t < d; ++t) acc += q[(size_t)i * d + t] * k[(size_t)j * d + t];
+                s[j] = scale * acc;
+                if (s[j] > mx) mx = s[j];
+            }
+        }
+        double* orow = o + (size_t)i * d;
+        for (int t = 0; t < d; ++t) orow[t] = 0.0;
+        if (mx == -INFINITY) { /* no visible key */
+            lse[i] = -INFINITY;
+            continue;
+        }
+        double sum = 0.0;
+        for (int j = 0; j < Nk; ++j) sum += (s[j] == -INFINITY) ? 0.0 : exp(s[j] - mx);
+        const double L = mx + log(sum);
+        lse[i] = L;
+        for (int j = 0; j < Nk; ++j) {
+            if (s[j] == -INFINITY) continue;
+            const double pj = exp(s[j] - L);
+            for (int t = 0; t < d; ++t) orow[t] += pj * v[(size_t)j * d + t];
+        }
+    }
+}
+
+typedef struct {
+    const double *q, *k, *v;
+    double *o, *lse;
+    int H, Nq, Nk, d, causal;
+    double scale;
+    const int* kv_lens;
+} rect_args;
+
+static void rect_item(void* a_, long bh) {
+    rect_args* a = (rect_args*)a_;
+    const int b = (int)(bh / a->H);
+    double* s = (double*)malloc(sizeof(double) * (size_t)a->Nk);
+    rect_head_forward(a->q + (size_t)bh * a->Nq * a->d, a->k + (size_t)bh * a->Nk * a->d,
+                      a->v + (size_t)bh * a->Nk * a->d, a->o + (size_t)bh * a->Nq * a->d,
+                      a->lse + (size_t)bh * a->Nq, s, a->Nq, a->Nk, a->d, a->scale, a->causal,
+                      kvlen_of(a->kv_lens, b, a->Nk));
+    free(s);
+}
+
+/* Forward of rectangular attention: q [B,H,Nq,d], k, v [B,H,Nk,d] -> o
+ * [B,H,Nq,d], lse [B,H,Nq]; kv_lens [B] or NULL (clamped to [0, Nk]). */
+int oracle_fwd_rect(const double* q, const double* k, const double* v, double* o, double* lse, int B, int H,
+                    int Nq, int Nk, int d, double scale, int causal, const int* kv_lens, int nthreads) {
+    if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0 || d <= 0) return OR_ERR;
+    rect_args a = {q, k, v, o, lse, H, Nq, Nk, d, causal, scale, kv_lens};
+    run_items(rect_item, &a, (long)B * H, nthreads);
+    return OR_OK;
+}
+
+/* ======================================================================== */
 /* 2. Row-sampled forms of the same definitions, for shapes whose N x N      */
 /*    matrices are too large to materialise.  One head per call.            */
 /* ======================================================================== */
