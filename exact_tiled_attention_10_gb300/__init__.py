@@ -22,7 +22,7 @@ from typing import Optional, Tuple
 import torch
 
 __all__ = ["forward", "forward_split", "forward_varlen", "backward_varlen", "backward",
-           "block_lists", "forward_block_sparse", "backward_block_sparse", "quantize_fp8_qkv", "quantize_fp8", "forward_fp8", "forward_fp8_split",
+           "block_lists", "forward_block_sparse", "backward_block_sparse", "quantize_fp8_qkv", "forward_rect", "quantize_fp8", "forward_fp8", "forward_fp8_split",
            "split_count", "split_workspace_size", "check_device_status",
            "selftest_wait_timeout",
            "bwd_workspace_size", "fwd_workspace_size", "library_path", "load_library", "FAError"]
@@ -65,6 +65,9 @@ _SIGS = {
     "fa_bwd_gqa_workspace_size": ([_i] * 5, _sz),
     "fa_selftest_quantiser_division": ([_vp, _vp, _i, _sz, _vp, _vp, _vp], _i),
     "fa_quantize_fp8_qkv": ([_vp] * 9 + [_i] * 5 + [_vp], _i),
+    "fa_fwd_rect_workspace_size": ([_i] * 7, _sz),
+    "fa_fwd_rect_split_count": ([_i] * 7, _i),
+    "fa_fwd_rect": ([_vp] * 5 + [_i] * 6 + [_f, _i, _vp, _i, _vp, _sz, _vp], _i),
     "fa_bwd_block_sparse": ([_vp] * 9 + [_i, _i, _i, _i, _i, _f, _i, _vp, _vp, _vp, _vp, _sz, _vp], _i),
     "fa_fwd_varlen": ([_vp] * 6 + [_i, _i, _i, _i, _i, _i, _f, _i, _vp], _i),
     "fa_bwd_varlen_workspace_size": ([_i] * 4, _sz),
@@ -301,6 +304,33 @@ def backward_block_sparse(q, k, v, o, lse, dout, row_ptr, col_idx, causal: bool 
                                    _ptr(col_idx), _ptr(kv), _ptr(ws), ws.numel() * ws.element_size(),
                                    _stream(q)))
     return dq, dk, dv
+
+
+def forward_rect(q, k, v, causal: bool = False, scale: Optional[float] = None, kv_lens=None,
+                 num_splits: int = 0, out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                 workspace: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Nq queries against Nk keys (decoding against a key/value cache,
+    cross-attention): q [B,H,Nq,d], k, v [B,Hkv,Nk,d] bf16.  Causal: the
+    queries are the last Nq positions (query i sees keys j <= i + Nk - Nq)."""
+    lib = load_library()
+    _need_cuda(q, k, v)
+    B, H, Nq, d = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    if (q.dtype != torch.bfloat16 or k.dtype != q.dtype or v.dtype != q.dtype or k.shape != (B, Hkv, Nk, d)
+            or v.shape != k.shape or H % Hkv != 0):
+        raise ValueError("q [B,H,Nq,d]; k, v [B,Hkv,Nk,d] bfloat16 with H a multiple of Hkv")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    kv = _kv(kv_lens, B, q.device)
+    o = torch.empty_like(q) if out is None else out
+    l = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device) if lse is None else lse
+    wsz = int(lib.fa_fwd_rect_workspace_size(B, H, Hkv, Nq, Nk, d, int(num_splits)))
+    ws = workspace
+    if wsz and (ws is None or ws.numel() * ws.element_size() < wsz):
+        ws = torch.empty(wsz, dtype=torch.uint8, device=q.device)
+    _check(lib.fa_fwd_rect(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(l), B, H, Hkv, Nq, Nk, d, scale,
+                           int(bool(causal)), _ptr(kv), int(num_splits), _ptr(ws) if wsz else None, wsz,
+                           _stream(q)))
+    return o, l
 
 
 def _cu(cu_seqlens, device):

@@ -227,6 +227,36 @@ SplitPlan plan_split(int B, int H, int N, int d, bool causal, bool has_kv, int r
     return P;
 }
 
+// Split plan of rectangular attention (Nq query rows, Nk keys).  Decode shapes
+// have few items (B * H * ceil(Nq / 256)) of similar length whatever the
+// masks, so when they fill less than half the GPU every item is cut into
+// enough key ranges for ~2 x SMs units (at most one per key block, at most
+// 64); with more items nothing is split unless num_splits asks for it.
+SplitPlan plan_split_rect(int B, int H, int Nq, int Nk, int d, int requested, int sms) {
+    const long long items = (long long)B * H * ((Nq + 255) / 256);
+    const int nb = (Nk + 127) / 128;
+    SplitPlan P;
+    int S = 1;
+    long long whole = items;
+    if (requested >= 2) {
+        S = requested < 64 ? requested : 64;
+        whole = 0;
+    } else if (requested == 0 && items * 2 <= sms && nb >= 2) {
+        S = (int)((2LL * sms + items - 1) / items);
+        S = S < nb ? S : nb;
+        S = S < 64 ? S : 64;
+        whole = 0;
+    }
+    P.num_whole = (int)whole;
+    if (S > 1) {
+        P.splits = S;
+        P.partials = (items - whole) * S;
+        P.o_bytes = round_up((size_t)P.partials * 256 * d * 4, 256);
+        P.bytes = P.o_bytes + round_up((size_t)P.partials * 256 * 4, 256);
+    }
+    return P;
+}
+
 fa_status fwd_impl(fa_dtype dtype, int block_c, bool fp8, const void* q, const void* k, const void* v, const float* sq,
                    const float* sk, const float* sv, void* o, float* lse, int B, int H, int N, int d, float scale,
                    int causal, const int* kv_lens, void* workspace, size_t workspace_bytes, cudaStream_t stream,
@@ -433,6 +463,80 @@ fa_status fa_fwd_split(const void* q, const void* k, const void* v, void* o, flo
                        size_t workspace_bytes, fa_stream_t stream) {
     return fwd_impl(FA_BF16, 0, false, q, k, v, nullptr, nullptr, nullptr, o, lse, B, H, N, d, scale, causal, kv_lens,
                     nullptr, 0, stream, num_splits, workspace, workspace_bytes);
+}
+
+// The rectangular forward packs the query rows of each key/value head's
+// group (contiguous in [B, H, Nq, d]): B * Hkv "heads" of (H / Hkv) * Nq rows.
+size_t fa_fwd_rect_workspace_size(int B, int H, int Hkv, int Nq, int Nk, int d, int num_splits) {
+    if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0 || Hkv < 1 || H % Hkv != 0 || (d != 64 && d != 128) ||
+        num_splits < 0)
+        return 0;
+    return plan_split_rect(B, Hkv, (H / Hkv) * Nq, Nk, d, num_splits, sm_count_or_default()).bytes;
+}
+
+int fa_fwd_rect_split_count(int B, int H, int Hkv, int Nq, int Nk, int d, int num_splits) {
+    if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0 || Hkv < 1 || H % Hkv != 0 || (d != 64 && d != 128) ||
+        num_splits < 0)
+        return 1;
+    return plan_split_rect(B, Hkv, (H / Hkv) * Nq, Nk, d, num_splits, sm_count_or_default()).splits;
+}
+
+fa_status fa_fwd_rect(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv, int Nq,
+                      int Nk, int d, float scale, int causal, const int* kv_lens, int num_splits, void* workspace,
+                      size_t workspace_bytes, fa_stream_t stream) {
+    FA_TRY(check_common(B, H, Nq, d, scale));
+    if (Nk <= 0) return fail(FA_ERR_INVALID_ARG, "Nk must be positive");
+    if (Hkv < 1 || H % Hkv != 0) return fail(FA_ERR_INVALID_ARG, "H (%d) must be a multiple of Hkv (%d)", H, Hkv);
+    if (num_splits < 0) return fail(FA_ERR_INVALID_ARG, "num_splits must be >= 0");
+    FA_CHECK_PTR(q);
+    FA_CHECK_PTR(k);
+    FA_CHECK_PTR(v);
+    FA_CHECK_PTR(o);
+    FA_CHECK_PTR(lse);
+    DeviceInfo* dev = nullptr;
+    FA_TRY(device_info(&dev));
+    const int R = (H / Hkv) * Nq;  // packed query rows per key/value head
+    if ((long long)(H / Hkv) * Nq > (1LL << 30)) return fail(FA_ERR_INVALID_ARG, "too many query rows");
+    const SplitPlan P = plan_split_rect(B, Hkv, R, Nk, d, num_splits, dev->sms);
+    const int BHkv = B * Hkv;
+    const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    fa::FwdMaps m;
+    FA_TRY(make_map_3d(&m.q, bf, 2, q, d, R, BHkv, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B));
+    FA_TRY(make_map_3d(&m.k, bf, 2, k, d, Nk, BHkv, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B));
+    FA_TRY(make_map_3d(&m.v, bf, 2, v, d, Nk, BHkv, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B));
+    m.q_lo = m.q;
+    m.k_lo = m.k;
+    fa::FwdParamsRect p;
+    memset(&p, 0, sizeof(p));
+    p.B = B; p.H = Hkv; p.N = R; p.Hkv = Hkv;
+    p.num_qp = (R + 255) / 256;
+    p.num_items = BHkv * p.num_qp;
+    p.scale = scale;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.kv_lens = kv_lens;
+    p.o = o;
+    p.lse = lse;
+    p.err = dev->err_word;
+    p.num_whole = (P.splits > 1) ? P.num_whole : p.num_items;
+    p.splits = P.splits;
+    p.num_units = p.num_whole + (int)P.partials;
+    p.Nk = Nk;
+    p.coff = Nk - Nq;
+    p.qmod = Nq;
+    if (P.splits > 1) {
+        if (!workspace || workspace_bytes < P.bytes)
+            return fail(FA_ERR_INVALID_ARG, "split workspace too small (%zu bytes, need %zu)", workspace_bytes, P.bytes);
+        p.o_part = reinterpret_cast<float*>(workspace);
+        p.lse_part = reinterpret_cast<float*>(reinterpret_cast<char*>(workspace) + P.o_bytes);
+    }
+    cudaError_t e = fa::launch_fwd_rect(d, causal != 0, m, p, grid_for_items(p.num_units, dev->sms), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "rectangular forward launch");
+    if (P.splits > 1) {
+        e = fa::launch_lse_merge(p.o_part, p.lse_part, P.num_whole, p.num_items - P.num_whole, P.splits, causal != 0,
+                                 BHkv, p.num_qp, R, d, o, lse, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "split merge launch");
+    }
+    return FA_OK;
 }
 
 fa_status fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv, int N,

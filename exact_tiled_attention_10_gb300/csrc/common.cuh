@@ -123,6 +123,16 @@ struct BwdParamsWin : BwdParams {
     int win_left, win_right;
 };
 
+// Rectangular attention (decoding against a key/value cache, cross-attention):
+// Nk keys (K, V have Nk rows).  The query rows of the g heads sharing a
+// key/value head are contiguous in [B, H, Nq, d], so they are packed as the
+// N = g * Nq rows of one "head" (H here is the number of key/value heads):
+// row r is query r % qmod (qmod = Nq) of its head, and with the causal mask
+// it sees keys j <= r % qmod + coff, coff = Nk - Nq.
+struct FwdParamsRect : FwdParams {
+    int Nk, coff, qmod;
+};
+
 // Block-sparse attention (chapter 18 §18.8.1): the 128-row query block i
 // computes only the 128-key blocks col_idx[row_ptr[i] .. row_ptr[i+1]-1]
 // (ascending), one list for every batch item and head.  The backward reads
@@ -151,6 +161,8 @@ cudaError_t launch_fwd_bf16_d64(int block_c, bool causal, bool out_f32, bool spl
 cudaError_t launch_fwd_bf16_d128(int block_c, bool causal, bool out_f32, bool split, const FwdMaps& m,
                                  const FwdParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_fwd_window(int d, const FwdMaps& m, const FwdParamsWin& p, int grid, cudaStream_t stream);
+cudaError_t launch_fwd_rect(int d, bool causal, const FwdMaps& m, const FwdParamsRect& p, int grid,
+                            cudaStream_t stream);
 cudaError_t launch_fwd_sparse(int d, bool causal, const FwdMaps& m, const FwdParamsSparse& p, int grid,
                               cudaStream_t stream);
 cudaError_t launch_bwd_main_sparse(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,

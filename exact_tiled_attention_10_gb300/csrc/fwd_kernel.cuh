@@ -165,9 +165,11 @@ using ItemT = typename std::conditional<
     VARLEN, ItemPacked,
     typename std::conditional<WINDOW, ItemWin, typename std::conditional<SPARSE, ItemSparse, Item>::type>::type>::type;
 
-template <bool WINDOW, bool SPARSE = false>
-using ParamsT = typename std::conditional<WINDOW, FwdParamsWin,
-                                          typename std::conditional<SPARSE, FwdParamsSparse, FwdParams>::type>::type;
+template <bool WINDOW, bool SPARSE = false, bool RECT = false>
+using ParamsT = typename std::conditional<
+    WINDOW, FwdParamsWin,
+    typename std::conditional<SPARSE, FwdParamsSparse,
+                              typename std::conditional<RECT, FwdParamsRect, FwdParams>::type>::type>::type;
 
 // Walks the ascending union of the two tiles' key-block lists: each call
 // returns the next block and which tiles compute it (a list that is not
@@ -259,8 +261,9 @@ __device__ __forceinline__ size_t lse_index(const IT& I, int row, const FwdParam
 // separately so that the plain forward carries none of their bookkeeping).
 // VARLEN: the instance for packed variable-length sequences.
 // WINDOW: the sliding-window instance (p is a FwdParamsWin).
-template <class C, bool CAUSAL, bool SPLITK, bool VARLEN, bool WINDOW = false, bool SPARSE = false>
-__device__ __forceinline__ ItemT<VARLEN, WINDOW, SPARSE> get_item(int unit, const ParamsT<WINDOW, SPARSE>& p) {
+// RECT: rectangular attention (p is a FwdParamsRect): Nk keys, causal offset coff.
+template <class C, bool CAUSAL, bool SPLITK, bool VARLEN, bool WINDOW = false, bool SPARSE = false, bool RECT = false>
+__device__ __forceinline__ ItemT<VARLEN, WINDOW, SPARSE> get_item(int unit, const ParamsT<WINDOW, SPARSE, RECT>& p) {
     ItemT<VARLEN, WINDOW, SPARSE> I;
     const int BH = p.B * p.H;
     int it = unit, s = 0, S = 1;
@@ -284,6 +287,10 @@ __device__ __forceinline__ ItemT<VARLEN, WINDOW, SPARSE> get_item(int unit, cons
         I.tb = a;
         I.seqlen = max(0, min(e - a, p.N));
         kvl = rows = I.seqlen;
+    } else if constexpr (RECT) {
+        rows = p.N;
+        kvl = p.Nk;
+        if (p.kv_lens) kvl = min(max(__ldg(p.kv_lens + I.b), 0), p.Nk);
     } else {
         kvl = rows = p.N;
         if (p.kv_lens) kvl = min(max(__ldg(p.kv_lens + I.b), 0), p.N);
@@ -355,7 +362,14 @@ __device__ __forceinline__ ItemT<VARLEN, WINDOW, SPARSE> get_item(int unit, cons
             int n = 0;
             if (r0 < rows) {
                 int cols = kvl;
-                if (CAUSAL) cols = min(cols, r0 + C::BR);
+                if constexpr (RECT) {
+                    // the tile's largest query index (rows r0 .. rl, query = row % qmod)
+                    const int rl = min(r0 + C::BR, rows) - 1;
+                    const int qmax = (rl / p.qmod != r0 / p.qmod) ? p.qmod - 1 : rl % p.qmod;
+                    if (CAUSAL) cols = min(cols, max(0, qmax + 1 + p.coff));
+                } else {
+                    if (CAUSAL) cols = min(cols, r0 + C::BR);
+                }
                 n = (cols + C::BC - 1) / C::BC;
             }
             I.n[t] = n;
@@ -489,11 +503,11 @@ __device__ __forceinline__ void store_row_chunk(void* o_row, int c0, const float
 }
 
 template <class C, bool CAUSAL, bool OUT_F32, bool SPLITK, bool VARLEN = false, bool WINDOW = false,
-          bool SPARSE = false>
+          bool SPARSE = false, bool RECT = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tql,
-               const __grid_constant__ CUtensorMap tkl, const ParamsT<WINDOW, SPARSE> p) {
+               const __grid_constant__ CUtensorMap tkl, const ParamsT<WINDOW, SPARSE, RECT> p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -557,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int rd = 0; rd < snake_rounds(p.num_units) && ok; ++rd) {
             const int it = snake_item(rd, p.num_units);
             if (it < 0) continue;
-            const auto I = get_item<C, CAUSAL, SPLITK, VARLEN, WINDOW, SPARSE>(it, p);
+            const auto I = get_item<C, CAUSAL, SPLITK, VARLEN, WINDOW, SPARSE, RECT>(it, p);
             if (I.nmax == 0) continue;
             // Q tile t of this item may load as soon as the previous item's last
             // S_t MMA has consumed the buffer (per-tile barriers), overlapping
@@ -640,7 +654,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int rd = 0; rd < snake_rounds(p.num_units) && ok; ++rd) {
             const int it = snake_item(rd, p.num_units);
             if (it < 0) continue;
-            const auto I = get_item<C, CAUSAL, SPLITK, VARLEN, WINDOW, SPARSE>(it, p);
+            const auto I = get_item<C, CAUSAL, SPLITK, VARLEN, WINDOW, SPARSE, RECT>(it, p);
             if (I.nmax == 0) continue;
             for (int t = 0; t < 2 && ok; ++t)
                 ok = wait_bounded_warp(BAR(C::B_QFULL + t), qph, abort_flag, p.err, kErrWaitFwdMma);
@@ -789,7 +803,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int rd = 0; rd < snake_rounds(p.num_units); ++rd) {
             const int it = snake_item(rd, p.num_units);
             if (it < 0) continue;
-            const auto I = get_item<C, CAUSAL, SPLITK, VARLEN, WINDOW, SPARSE>(it, p);
+            const auto I = get_item<C, CAUSAL, SPLITK, VARLEN, WINDOW, SPARSE, RECT>(it, p);
             const int n = item_n(I, t);
             const int tile_row0 = I.row0 + t * C::BR;
             const int row = tile_row0 + r_in;
@@ -878,7 +892,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < C::BC; ++c) s[c] = __uint_as_float(sr[c]);
                 int col0 = (I.j0 + item_a(I, t) + j) * C::BC;
                 if constexpr (SPARSE) col0 = __ldg(p.col_idx + (t ? I.off[1] : I.off[0]) + j) * C::BC;
-                bool need_mask = (col0 + C::BC > I.kvl) || (CAUSAL && col0 + C::BC - 1 > tile_row0);
+                // causal limit of a row: its query index (+ the rectangular offset)
+                int coff = 0, qmin = tile_row0, qrow = row;
+                if constexpr (RECT) {
+                    const int rl = tile_row0 + C::BR - 1;
+                    coff = p.coff;
+                    qmin = (rl / p.qmod != tile_row0 / p.qmod) ? 0 : tile_row0 % p.qmod;
+                    qrow = row % p.qmod;
+                }
+                bool need_mask = (col0 + C::BC > I.kvl) || (CAUSAL && col0 + C::BC - 1 > qmin + coff);
                 if constexpr (WINDOW)  // blocks crossing some row's window edge
                     need_mask = need_mask || (p.win_right >= 0 && col0 + C::BC - 1 > tile_row0 + p.win_right) ||
                                 (p.win_left >= 0 && col0 < tile_row0 + C::BR - 1 - p.win_left);
@@ -886,7 +908,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int c = 0; c < C::BC; ++c) {
                         const int col = col0 + c;
-                        bool off = col >= I.kvl || (CAUSAL && col > row);
+                        bool off = col >= I.kvl || (CAUSAL && col > qrow + coff);
                         if constexpr (WINDOW)
                             off = off || (p.win_right >= 0 && col > row + p.win_right) ||
                                   (p.win_left >= 0 && col < row - p.win_left);
@@ -986,13 +1008,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <class C, bool CAUSAL, bool OUT_F32, bool SPLITK = false, bool VARLEN = false, bool WINDOW = false,
-          bool SPARSE = false>
-cudaError_t launch(const FwdMaps& m, const ParamsT<WINDOW, SPARSE>& p, int grid, cudaStream_t stream) {
-    auto kern = fwd_kernel<C, CAUSAL, OUT_F32, SPLITK, VARLEN, WINDOW, SPARSE>;
+          bool SPARSE = false, bool RECT = false>
+cudaError_t launch(const FwdMaps& m, const ParamsT<WINDOW, SPARSE, RECT>& p, int grid, cudaStream_t stream) {
+    auto kern = fwd_kernel<C, CAUSAL, OUT_F32, SPLITK, VARLEN, WINDOW, SPARSE, RECT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     kern<<<grid, kThreads, C::SMEM, stream>>>(m.q, m.k, m.v, m.q_lo, m.k_lo, p);
     return cudaGetLastError();
+}
+
+// Rectangular attention (Nq != Nk), through the split-key instance.
+template <class C>
+cudaError_t launch_rect(bool causal, const FwdMaps& m, const FwdParamsRect& p, int grid, cudaStream_t s) {
+    return causal ? launch<C, true, false, true, false, false, false, true>(m, p, grid, s)
+                  : launch<C, false, false, true, false, false, false, true>(m, p, grid, s);
 }
 
 // Block-sparse (block lists of 128 x 128 blocks).

@@ -142,6 +142,27 @@ fa_status fa_fwd_split(const void* q, const void* k, const void* v, void* o, flo
                        int num_splits, void* workspace, size_t workspace_bytes,
                        fa_stream_t stream);
 
+/* Rectangular attention, bf16: Nq queries against Nk keys -- a decoding step
+ * against a key/value cache (FlashDecoding, [CH18] §18.8.2: the query is
+ * [b, n_q, d] with n_q << n_kv) or cross-attention.  q, o: [B,H,Nq,d]; k, v:
+ * [B,Hkv,Nk,d]; lse [B,H,Nq]; kv_lens [B] (valid cache length per batch
+ * item, clamped to [0, Nk]) or NULL.  With causal the queries are the last
+ * Nq positions: query i sees keys j <= i + Nk - Nq.  Runs the split-key
+ * form: num_splits = 0 plans the split (every item is cut into key ranges
+ * when the items fill less than half the GPU), 1 = unsplit, >= 2 = that
+ * many ranges per item (capped at 64).  Workspace:
+ * fa_fwd_rect_workspace_size(...) bytes (0 when unsplit);
+ * fa_fwd_rect_split_count gives the ranges per item the call will use.  The
+ * query rows of the H / Hkv heads sharing a key/value head are processed as
+ * one block of rows (they are contiguous in q), so each K / V tile is read
+ * once per group. */
+size_t fa_fwd_rect_workspace_size(int B, int H, int Hkv, int Nq, int Nk, int d, int num_splits);
+int fa_fwd_rect_split_count(int B, int H, int Hkv, int Nq, int Nk, int d, int num_splits);
+fa_status fa_fwd_rect(const void* q, const void* k, const void* v, void* o, float* lse,
+                      int B, int H, int Hkv, int Nq, int Nk, int d, float scale, int causal,
+                      const int* kv_lens, int num_splits, void* workspace, size_t workspace_bytes,
+                      fa_stream_t stream);
+
 /* Shared key/value heads (grouped-query attention; multi-query for Hkv = 1),
  * bf16.  q, o: [B,H,N,d]; k, v: [B,Hkv,N,d] with H a multiple of Hkv; query
  * head h attends with key/value head h / (H / Hkv) -- the head broadcast of
