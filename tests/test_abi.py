@@ -113,3 +113,51 @@ def test_binding_refuses_cpu_tensors():
     x = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         fa.forward(x, x, x)
+
+
+def _prototype_arity():
+    src = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    out = {}
+    for m in re.finditer(r"\b(fa_[a-z0-9_]+)\s*\(([^;{]*?)\)\s*;", src):
+        args = m.group(2).strip()
+        out[m.group(1)] = 0 if args in ("", "void") else args.count(",") + 1
+    return out
+
+
+def test_binding_argument_counts_match_the_prototypes():
+    import exact_tiled_attention_10_gb300 as fa
+    arity = _prototype_arity()
+    for name, (argtypes, _) in fa._SIGS.items():
+        assert name in arity, name
+        assert len(argtypes) == arity[name], (name, len(argtypes), arity[name])
+
+
+def test_host_validation_of_the_variant_entry_points():
+    """Bad arguments of the window, block-sparse, rectangular, grouped and
+    fused-quantiser entry points are refused on the host, before any CUDA
+    call (so this runs without a GPU)."""
+    import exact_tiled_attention_10_gb300 as fa
+    lib = fa.load_library()
+    A = 4096
+    # window: an edge below -1, heads not a multiple of the key/value heads
+    assert lib.fa_fwd_window(A, A, A, A, A, 1, 4, 4, 256, 128, 0.1, 0, -2, 5, None, None) == 1
+    assert lib.fa_fwd_window(A, A, A, A, A, 1, 4, 3, 256, 128, 0.1, 0, 5, 5, None, None) == 1
+    # block-sparse: missing lists, workspace too small
+    assert lib.fa_fwd_block_sparse(A, A, A, A, A, 1, 4, 4, 256, 128, 0.1, 0, None, A, None, None) == 1
+    need = lib.fa_bwd_block_sparse_workspace_size(1, 4, 256, 128)
+    assert need > lib.fa_bwd_workspace_size(0, 1, 4, 256, 128)
+    assert lib.fa_bwd_block_sparse(A, A, A, A, A, A, A, A, A, 1, 4, 4, 256, 128, 0.1, 0, A, A, None, A, need - 1,
+                                   None) == 1
+    # rectangular: no keys, bad group, negative split count
+    assert lib.fa_fwd_rect(A, A, A, A, A, 1, 4, 4, 1, 0, 128, 0.1, 1, None, 0, None, 0, None) == 1
+    assert lib.fa_fwd_rect(A, A, A, A, A, 1, 4, 3, 1, 100, 128, 0.1, 1, None, 0, None, 0, None) == 1
+    assert lib.fa_fwd_rect(A, A, A, A, A, 1, 4, 4, 1, 100, 128, 0.1, 1, None, -1, None, 0, None) == 1
+    assert lib.fa_fwd_rect_workspace_size(1, 4, 3, 1, 100, 128, 0) == 0
+    # a decode step (one query per head, long cache) is split; a long prefill is not
+    assert lib.fa_fwd_rect_split_count(1, 32, 8, 1, 131072, 128, 0) > 1
+    assert lib.fa_fwd_rect_split_count(8, 32, 8, 4096, 4096, 128, 0) == 1
+    # fused quantiser: bad group
+    assert lib.fa_quantize_fp8_qkv(A, A, A, A, A, A, A, A, A, 1, 4, 3, 256, 128, None) == 1
+    # grouped backward: the split workspace is larger only when key blocks are few
+    assert lib.fa_bwd_gqa_workspace_size(2, 16, 2, 4096, 128) > lib.fa_bwd_workspace_size(0, 2, 16, 4096, 128)
+    assert lib.fa_bwd_gqa_workspace_size(64, 16, 16, 4096, 128) <= lib.fa_bwd_workspace_size(0, 64, 16, 4096, 128) + 256
