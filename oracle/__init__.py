@@ -24,12 +24,14 @@ Entry points and what pins each one (tests/test_oracle_*.py):
   closed form (each query sees only its own key: O_i = v_i, LSE_i = S_ii,
   dQ = dK = 0, dV_i = dO_i), window (-1, 0) equal to the causal mask,
   windows wider than N equal to no window, and central finite differences.
-* ``fwd_rect`` -- rectangular attention (Nq queries, Nk keys: decoding
+* ``fwd_rect`` / ``bwd_rect`` -- rectangular attention (Nq queries, Nk keys: decoding
   against a key/value cache, cross-attention; chapter 18 §18.8.2), causal
   with the queries as the last Nq positions.  Pinned by: Nq = Nk equal to
   ``fwd`` exactly, the causal case equal to the last Nq rows of ``fwd`` on
   the full Nk-row sequence exactly, float64 torch softmax with an explicit
-  mask, and the one-query closed form (LSE = logsumexp of its scores).
+  mask, and the one-query closed form (LSE = logsumexp of its scores);
+  the backward by float64 autograd with the same mask, Nq = Nk equal to
+  ``bwd`` exactly, and central finite differences.
 * the block-sparse mask (``block_mask`` [nb][nb] of 0/1 over block_size
   blocks, chapter 18 §18.8.1).  Pinned by: float64 autograd with the mask
   expanded to elements by a Kronecker product, the all-ones mask equal to no
@@ -104,6 +106,8 @@ def _load():
                                              ctypes.c_int, ctypes.c_int, ctypes.c_int]
             lib.oracle_fwd_rect.argtypes = [_dp, _dp, _dp, _dp, _dp, _i, _i, _i, _i, _i, ctypes.c_double, _i,
                                             _ip, _i]
+            lib.oracle_bwd_rect.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, _dp, _i, _i, _i, _i, _i,
+                                            ctypes.c_double, _i, _ip, _i]
             lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
             lib.oracle_e4m3_decode.restype = ctypes.c_double
             lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
@@ -216,6 +220,22 @@ def fwd_rect(q, k, v, scale, causal=False, kv_lens=None, nthreads=0):
                              Nk, d, float(scale), int(bool(causal)), kvp, int(nthreads))
     assert rc == 0
     return o, lse
+
+
+def bwd_rect(q, k, v, dout, scale, causal=False, kv_lens=None, nthreads=0):
+    """Backward of fwd_rect (L = sum(O * dout)): dict dq [B,H,Nq,d], dk, dv [B,H,Nk,d]."""
+    lib = _load()
+    q, k, v, g = _f64(q), _f64(k), _f64(v), _f64(dout)
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    assert k.shape == (B, H, Nk, d) and v.shape == k.shape and g.shape == q.shape
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    kv, kvp = _kv(kv_lens, B)
+    rc = lib.oracle_bwd_rect(_ptr(q, _dp), _ptr(k, _dp), _ptr(v, _dp), _ptr(g, _dp), _ptr(dq, _dp),
+                             _ptr(dk, _dp), _ptr(dv, _dp), B, H, Nq, Nk, d, float(scale), int(bool(causal)),
+                             kvp, int(nthreads))
+    assert rc == 0
+    return dict(dq=dq, dk=dk, dv=dv)
 
 
 def fwd_rows(q_head, k_head, v_head, scale, causal, kv_len, rows, window=None, block_mask=None,

@@ -370,6 +370,92 @@ int oracle_fwd_rect(const double* q, const double* k, const double* v, double* o
     return OR_OK;
 }
 
+/* Backward of rectangular attention for one head, by the same definitions as
+ * naive_bwd_item: P materialised (Nq x Nk), dP = dO V^T, D_i = sum_j P_ij
+ * dP_ij, dS = P (dP - D), dQ = scale dS K, dK = scale dS^T Q, dV = P^T dO. */
+static void rect_head_backward(const double* q, const double* k, const double* v, const double* dO,
+                               double* dq, double* dk, double* dv, int Nq, int Nk, int d, double scale,
+                               int causal, int kv_len) {
+    const int off = Nk - Nq;
+    double* P = (double*)malloc(sizeof(double) * (size_t)Nq * Nk);
+    double* dS = (double*)malloc(sizeof(double) * (size_t)Nq * Nk);
+    for (int i = 0; i < Nq; ++i) {
+        double* Pi = P + (size_t)i * Nk;
+        double mx = -INFINITY;
+        for (int j = 0; j < Nk; ++j) {
+            Pi[j] = -INFINITY;
+            if (j < kv_len && (!causal || j <= i + off)) {
+                double acc = 0.0;
+                for (int t = 0; t < d; ++t) acc += q[(size_t)i * d + t] * k[(size_t)j * d + t];
+                Pi[j] = scale * acc;
+                if (Pi[j] > mx) mx = Pi[j];
+            }
+        }
+        if (mx == -INFINITY) {
+            for (int j = 0; j < Nk; ++j) Pi[j] = 0.0;
+            continue;
+        }
+        double sum = 0.0;
+        for (int j = 0; j < Nk; ++j) sum += (Pi[j] == -INFINITY) ? 0.0 : exp(Pi[j] - mx);
+        const double L = mx + log(sum);
+        for (int j = 0; j < Nk; ++j) Pi[j] = (Pi[j] == -INFINITY) ? 0.0 : exp(Pi[j] - L);
+    }
+    for (int i = 0; i < Nq; ++i) {
+        double Di = 0.0;
+        for (int j = 0; j < Nk; ++j) {
+            double dp = 0.0;
+            for (int t = 0; t < d; ++t) dp += dO[(size_t)i * d + t] * v[(size_t)j * d + t];
+            dS[(size_t)i * Nk + j] = dp;
+            Di += P[(size_t)i * Nk + j] * dp;
+        }
+        for (int j = 0; j < Nk; ++j) dS[(size_t)i * Nk + j] = P[(size_t)i * Nk + j] * (dS[(size_t)i * Nk + j] - Di);
+    }
+    for (int i = 0; i < Nq; ++i)
+        for (int t = 0; t < d; ++t) {
+            double acc = 0.0;
+            for (int j = 0; j < Nk; ++j) acc += dS[(size_t)i * Nk + j] * k[(size_t)j * d + t];
+            dq[(size_t)i * d + t] = scale * acc;
+        }
+    for (int j = 0; j < Nk; ++j)
+        for (int t = 0; t < d; ++t) {
+            double acck = 0.0, accv = 0.0;
+            for (int i = 0; i < Nq; ++i) {
+                acck += dS[(size_t)i * Nk + j] * q[(size_t)i * d + t];
+                accv += P[(size_t)i * Nk + j] * dO[(size_t)i * d + t];
+            }
+            dk[(size_t)j * d + t] = scale * acck;
+            dv[(size_t)j * d + t] = accv;
+        }
+    free(P);
+    free(dS);
+}
+
+typedef struct {
+    const double *q, *k, *v, *dO;
+    double *dq, *dk, *dv;
+    int H, Nq, Nk, d, causal;
+    double scale;
+    const int* kv_lens;
+} rect_bwd_args;
+
+static void rect_bwd_item(void* a_, long bh) {
+    rect_bwd_args* a = (rect_bwd_args*)a_;
+    const int b = (int)(bh / a->H);
+    const size_t oq = (size_t)bh * a->Nq * a->d, ok = (size_t)bh * a->Nk * a->d;
+    rect_head_backward(a->q + oq, a->k + ok, a->v + ok, a->dO + oq, a->dq + oq, a->dk + ok, a->dv + ok, a->Nq,
+                       a->Nk, a->d, a->scale, a->causal, kvlen_of(a->kv_lens, b, a->Nk));
+}
+
+/* Backward of oracle_fwd_rect: dq [B,H,Nq,d], dk, dv [B,H,Nk,d]. */
+int oracle_bwd_rect(const double* q, const double* k, const double* v, const double* dout, double* dq,
+                    double* dk, double* dv, int B, int H, int Nq, int Nk, int d, double scale, int causal,
+                    const int* kv_lens, int nthreads) {
+    if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0 || d <= 0) return OR_ERR;
+    rect_bwd_args a = {q, k, v, dout, dq, dk, dv, H, Nq, Nk, d, causal, scale, kv_lens};
+    run_items(rect_bwd_item, &a, (long)B * H, nthreads);
+    return OR_OK;
+}
+
 /* ======================================================================== */
 /* 2. Row-sampled forms of the same definitions, for shapes whose N x N      */
 /*    matrices are too large to materialise.  One head per call.            */
