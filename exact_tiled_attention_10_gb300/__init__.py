@@ -22,7 +22,7 @@ from typing import Optional, Tuple
 import torch
 
 __all__ = ["forward", "forward_split", "forward_varlen", "backward_varlen", "backward",
-           "block_lists", "forward_block_sparse", "backward_block_sparse", "quantize_fp8_qkv", "forward_rect", "quantize_fp8", "forward_fp8", "forward_fp8_split",
+           "block_lists", "forward_block_sparse", "backward_block_sparse", "quantize_fp8_qkv", "forward_rect", "backward_rect", "quantize_fp8", "forward_fp8", "forward_fp8_split",
            "split_count", "split_workspace_size", "check_device_status",
            "selftest_wait_timeout",
            "bwd_workspace_size", "fwd_workspace_size", "library_path", "load_library", "FAError"]
@@ -68,6 +68,8 @@ _SIGS = {
     "fa_fwd_rect_workspace_size": ([_i] * 7, _sz),
     "fa_fwd_rect_split_count": ([_i] * 7, _i),
     "fa_fwd_rect": ([_vp] * 5 + [_i] * 6 + [_f, _i, _vp, _i, _vp, _sz, _vp], _i),
+    "fa_bwd_rect_workspace_size": ([_i] * 6, _sz),
+    "fa_bwd_rect": ([_vp] * 9 + [_i] * 6 + [_f, _i, _vp, _vp, _sz, _vp], _i),
     "fa_bwd_block_sparse": ([_vp] * 9 + [_i, _i, _i, _i, _i, _f, _i, _vp, _vp, _vp, _vp, _sz, _vp], _i),
     "fa_fwd_varlen": ([_vp] * 6 + [_i, _i, _i, _i, _i, _i, _f, _i, _vp], _i),
     "fa_bwd_varlen_workspace_size": ([_i] * 4, _sz),
@@ -331,6 +333,26 @@ def forward_rect(q, k, v, causal: bool = False, scale: Optional[float] = None, k
                            int(bool(causal)), _ptr(kv), int(num_splits), _ptr(ws) if wsz else None, wsz,
                            _stream(q)))
     return o, l
+
+
+def backward_rect(q, k, v, o, lse, dout, causal: bool = False, scale: Optional[float] = None, kv_lens=None,
+                  workspace: Optional[torch.Tensor] = None):
+    """Backward of forward_rect: dQ [B,H,Nq,d], dK, dV [B,Hkv,Nk,d]."""
+    lib = load_library()
+    _need_cuda(q, k, v, o, lse, dout)
+    B, H, Nq, d = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    kv = _kv(kv_lens, B, q.device)
+    wsz = int(lib.fa_bwd_rect_workspace_size(B, H, Hkv, Nq, Nk, d))
+    ws = workspace
+    if ws is None or ws.numel() * ws.element_size() < wsz:
+        ws = torch.empty(wsz, dtype=torch.uint8, device=q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    _check(lib.fa_bwd_rect(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
+                           B, H, Hkv, Nq, Nk, d, scale, int(bool(causal)), _ptr(kv), _ptr(ws),
+                           ws.numel() * ws.element_size(), _stream(q)))
+    return dq, dk, dv
 
 
 def _cu(cu_seqlens, device):

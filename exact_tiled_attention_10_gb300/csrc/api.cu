@@ -686,8 +686,10 @@ fa_status bwd_main_impl(const BwdCtx& c, bool f32, const void* qb, const void* k
                         void* dk, void* dv, int B, int H, int N, int d, float scale, int causal, const int* kv_lens,
                         cudaStream_t stream, int Hkv = 0, int win_left = -1, int win_right = -1,
                         const int* col_ptr = nullptr, const int* row_idx = nullptr, float* dkv_part = nullptr,
-                        size_t part_bytes = 0) {
+                        size_t part_bytes = 0, int Nk = -1) {
     const int BH = c.BH, Np = c.Np;
+    const bool rect = Nk >= 0;  // rectangular: N query rows, Nk keys
+    if (!rect) Nk = N;
     if (Hkv == 0) Hkv = H;
     if (Hkv < 1 || H % Hkv != 0) return fail(FA_ERR_INVALID_ARG, "H (%d) must be a multiple of Hkv (%d)", H, Hkv);
     const int BHkv = B * Hkv;
@@ -696,13 +698,13 @@ fa_status bwd_main_impl(const BwdCtx& c, bool f32, const void* qb, const void* k
     CUtensorMap tq, tk, tv, tdo, tdq;
     FA_TRY(make_map_3d(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, qb, d, N, BH, 64, BR, CU_TENSOR_MAP_SWIZZLE_128B));
     FA_TRY(make_map_3d(&tdo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, gb, d, N, BH, 64, BR, CU_TENSOR_MAP_SWIZZLE_128B));
-    FA_TRY(make_map_3d(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kb, d, N, BHkv, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B));
-    FA_TRY(make_map_3d(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, vb, d, N, BHkv, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B));
+    FA_TRY(make_map_3d(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kb, d, Nk, BHkv, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B));
+    FA_TRY(make_map_3d(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, vb, d, Nk, BHkv, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B));
     FA_TRY(make_map_dqacc(&tdq, dqacc, d, (long long)BH * Np));
     fa::BwdParams p;
     memset(&p, 0, sizeof(p));
     p.B = B; p.H = H; p.N = N; p.Np = Np; p.Hkv = Hkv;
-    p.num_kt = (N + 127) / 128;
+    p.num_kt = (Nk + 127) / 128;
     p.num_items = BHkv * p.num_kt;
     p.scale = scale;
     p.scale_log2 = scale * 1.4426950408889634f;
@@ -715,11 +717,11 @@ fa_status bwd_main_impl(const BwdCtx& c, bool f32, const void* qb, const void* k
     p.err = c.dev->err_word;
     // the grouped instances (shared heads, window, block lists) may split a
     // key block's query heads over several units when key blocks are few
-    const bool grouped = Hkv != H || col_ptr || win_left >= 0 || win_right >= 0;
+    const bool grouped = Hkv != H || col_ptr || win_left >= 0 || win_right >= 0 || rect;
     p.gsplit = 1;
     if (grouped && dkv_part) {
         const int g = choose_gsplit(p.num_items, H / Hkv, c.dev->sms);
-        if (g > 1 && part_bytes >= dkv_part_bytes(g, B, Hkv, N, d)) {
+        if (g > 1 && part_bytes >= dkv_part_bytes(g, B, Hkv, Nk, d)) {
             p.gsplit = g;
             p.dkv_part = dkv_part;
             p.num_items *= g;
@@ -727,7 +729,14 @@ fa_status bwd_main_impl(const BwdCtx& c, bool f32, const void* qb, const void* k
     }
     const int grid = grid_for_items(p.num_items, c.dev->sms);
     cudaError_t e;
-    if (col_ptr) {
+    if (rect) {
+        fa::BwdParamsRect pr;
+        memset(&pr, 0, sizeof(pr));
+        static_cast<fa::BwdParams&>(pr) = p;
+        pr.Nk = Nk;
+        pr.coff = Nk - N;
+        e = fa::launch_bwd_main_rect(d, causal != 0, tq, tk, tv, tdo, tdq, pr, grid, stream);
+    } else if (col_ptr) {
         fa::BwdParamsSparse ps;
         memset(&ps, 0, sizeof(ps));
         static_cast<fa::BwdParams&>(ps) = p;
@@ -750,7 +759,7 @@ fa_status bwd_main_impl(const BwdCtx& c, bool f32, const void* qb, const void* k
     }
     if (e != cudaSuccess) return cuda_fail(e, "backward main launch");
     if (p.gsplit > 1) {
-        e = fa::launch_dkv_sum(dkv_part, p.gsplit, (size_t)B * Hkv * N * d, dk, dv, bw_grid(c.dev), stream);
+        e = fa::launch_dkv_sum(dkv_part, p.gsplit, (size_t)B * Hkv * Nk * d, dk, dv, bw_grid(c.dev), stream);
         if (e != cudaSuccess) return cuda_fail(e, "dK / dV partial sum launch");
     }
     return FA_OK;
@@ -898,6 +907,37 @@ fa_status fa_bwd_block_sparse(const void* q, const void* k, const void* v, const
     FA_TRY(bwd_main_impl(c, false, q, k, v, dout, dk, dv, B, H, N, d, scale, causal, kv_lens, stream, Hkv, -1, -1,
                          col_ptr, row_idx));
     return bwd_dq_impl(c, false, dq, N, d, scale, stream);
+}
+
+size_t fa_bwd_rect_workspace_size(int B, int H, int Hkv, int Nq, int Nk, int d) {
+    if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0 || Hkv < 1 || H % Hkv != 0 || (d != 64 && d != 128)) return 0;
+    const size_t base = round_up(fa_bwd_workspace_size(FA_BF16, B, H, Nq, d), 256);
+    const int g = choose_gsplit((long)B * Hkv * ((Nk + 127) / 128), H / Hkv, sm_count_or_default());
+    return g > 1 ? base + dkv_part_bytes(g, B, Hkv, Nk, d) : base;
+}
+
+fa_status fa_bwd_rect(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                      void* dq, void* dk, void* dv, int B, int H, int Hkv, int Nq, int Nk, int d, float scale,
+                      int causal, const int* kv_lens, void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+    FA_CHECK_PTR(q);
+    FA_CHECK_PTR(k);
+    FA_CHECK_PTR(v);
+    FA_CHECK_PTR(o);
+    FA_CHECK_PTR(lse);
+    FA_CHECK_PTR(dout);
+    FA_CHECK_PTR(dq);
+    FA_CHECK_PTR(dk);
+    FA_CHECK_PTR(dv);
+    if (Nk <= 0) return fail(FA_ERR_INVALID_ARG, "Nk must be positive");
+    if (Hkv < 1 || H % Hkv != 0) return fail(FA_ERR_INVALID_ARG, "H (%d) must be a multiple of Hkv (%d)", H, Hkv);
+    BwdCtx c{};
+    FA_TRY(bwd_setup(FA_BF16, B, H, Nq, d, scale, workspace, workspace_bytes, &c));
+    FA_TRY(bwd_pre_impl(c, false, o, lse, dout, Nq, d, stream));
+    const size_t base = round_up(c.L.total, 256);
+    float* part = workspace_bytes > base ? reinterpret_cast<float*>(c.ws + base) : nullptr;
+    FA_TRY(bwd_main_impl(c, false, q, k, v, dout, dk, dv, B, H, Nq, d, scale, causal, kv_lens, stream, Hkv, -1, -1,
+                         nullptr, nullptr, part, part ? workspace_bytes - base : 0, Nk));
+    return bwd_dq_impl(c, false, dq, Nq, d, scale, stream);
 }
 
 size_t fa_bwd_gqa_workspace_size(int B, int H, int Hkv, int N, int d) {

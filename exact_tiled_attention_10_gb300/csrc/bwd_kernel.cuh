@@ -120,12 +120,28 @@ struct Item {
 // SPARSE: the block-sparse instance (p is a BwdParamsSparse): key block kt
 // visits the 128-row query blocks row_idx[i0 .. i0 + ni / R - 1] (R steps
 // per query block), per query head of its group.
-template <bool WINDOW, bool SPARSE = false>
-using ParamsT = typename std::conditional<WINDOW, BwdParamsWin,
-                                          typename std::conditional<SPARSE, BwdParamsSparse, BwdParams>::type>::type;
+// RECT: the rectangular instance (p is a BwdParamsRect): N query rows, Nk keys.
+template <bool WINDOW, bool SPARSE = false, bool RECT = false>
+using ParamsT = typename std::conditional<
+    WINDOW, BwdParamsWin,
+    typename std::conditional<SPARSE, BwdParamsSparse,
+                              typename std::conditional<RECT, BwdParamsRect, BwdParams>::type>::type>::type;
 
-template <class C, bool CAUSAL, bool GQA, bool VARLEN = false, bool WINDOW = false, bool SPARSE = false>
-__device__ __forceinline__ Item get_item(int it, const ParamsT<WINDOW, SPARSE>& p) {
+// Keys of a head (K, V, dK, dV rows) and the causal offset.
+template <class PT>
+__device__ __forceinline__ int key_count(const PT& p) {
+    if constexpr (std::is_same<PT, BwdParamsRect>::value) return p.Nk;
+    else return p.N;
+}
+template <class PT>
+__device__ __forceinline__ int causal_offset(const PT& p) {
+    if constexpr (std::is_same<PT, BwdParamsRect>::value) return p.coff;
+    else return 0;
+}
+
+template <class C, bool CAUSAL, bool GQA, bool VARLEN = false, bool WINDOW = false, bool SPARSE = false,
+          bool RECT = false>
+__device__ __forceinline__ Item get_item(int it, const ParamsT<WINDOW, SPARSE, RECT>& p) {
     Item I;
     const int Hkv = GQA ? p.Hkv : p.H;
     const int BH = p.B * Hkv;
@@ -156,11 +172,12 @@ __device__ __forceinline__ Item get_item(int it, const ParamsT<WINDOW, SPARSE>& 
         I.seqlen = max(0, min(e - a, p.N));
     }
     int kvl = I.seqlen;
-    if (!VARLEN && p.kv_lens) kvl = min(max(__ldg(p.kv_lens + I.b), 0), p.N);
+    if constexpr (RECT) kvl = p.Nk;
+    if (!VARLEN && p.kv_lens) kvl = min(max(__ldg(p.kv_lens + I.b), 0), key_count(p));
     I.kvl = kvl;
     const int key0 = I.kt * C::BC;
     const int iend = ((VARLEN ? I.seqlen : p.N) + C::BR - 1) / C::BR;
-    I.i0 = CAUSAL ? key0 / C::BR : 0;
+    I.i0 = CAUSAL ? (RECT ? max(0, key0 - causal_offset(p)) : key0) / C::BR : 0;
     if constexpr (SPARSE) {
         // the block's query blocks, without those entirely above the causal
         // diagonal (all query rows before the block's first key)
@@ -278,11 +295,11 @@ __device__ __forceinline__ void mma_dq(uint32_t d_tmem, uint64_t k_mn, uint64_t 
 }
 
 template <class C, bool CAUSAL, bool OUT_F32, bool GQA, bool VARLEN = false, bool WINDOW = false,
-          bool SPARSE = false>
+          bool SPARSE = false, bool RECT = false>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
-               const __grid_constant__ CUtensorMap tdq, const ParamsT<WINDOW, SPARSE> p) {
+               const __grid_constant__ CUtensorMap tdq, const ParamsT<WINDOW, SPARSE, RECT> p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -337,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int rd = 0; rd < snake_rounds(p.num_items) && ok; ++rd) {
             const int it = snake_item(rd, p.num_items);
             if (it < 0) continue;
-            const Item I = get_item<C, CAUSAL, GQA, VARLEN, WINDOW, SPARSE>(it, p);
+            const Item I = get_item<C, CAUSAL, GQA, VARLEN, WINDOW, SPARSE, RECT>(it, p);
             if (I.n == 0) continue;
             if (!(ok = wait_bounded_warp(BAR(C::B_KVEMPTY), kve ^ 1, abort_flag, p.err, kErrWaitBwdProducer))) break;
             kve ^= 1;
@@ -414,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int rd = 0; rd < snake_rounds(p.num_items) && ok; ++rd) {
             const int it = snake_item(rd, p.num_items);
             if (it < 0) continue;
-            const Item I = get_item<C, CAUSAL, GQA, VARLEN, WINDOW, SPARSE>(it, p);
+            const Item I = get_item<C, CAUSAL, GQA, VARLEN, WINDOW, SPARSE, RECT>(it, p);
             if (I.n == 0) continue;
             if (!(ok = wait_bounded_warp(BAR(C::B_KVFULL), kvph, abort_flag, p.err, kErrWaitBwdMma))) break;
             kvph ^= 1;
@@ -475,17 +492,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int rd = 0; rd < snake_rounds(p.num_items) && ok; ++rd) {
             const int it = snake_item(rd, p.num_items);
             if (it < 0) continue;
-            const Item I = get_item<C, CAUSAL, GQA, VARLEN, WINDOW, SPARSE>(it, p);
+            const Item I = get_item<C, CAUSAL, GQA, VARLEN, WINDOW, SPARSE, RECT>(it, p);
             const int key = I.kt * C::BC + kr;
             // dK, dV row: [B,Hkv,N,d], or token-major [total, Hkv, d] for packed sequences
-            const size_t krow = VARLEN ? (size_t)(I.tb + key) * p.Hkv + I.kvh : (size_t)I.bh * p.N + key;
+            const int nkeys = key_count(p);
+            const size_t krow = VARLEN ? (size_t)(I.tb + key) * p.Hkv + I.kvh : (size_t)I.bh * nkeys + key;
             if (I.n == 0) {  // key block entirely beyond kv_len: zero gradients (packed: nothing to write)
-                if (!VARLEN && key < p.N) {
+                if (!VARLEN && key < nkeys) {
                     float z[32];
 #pragma unroll
                     for (int e = 0; e < 32; ++e) z[e] = 0.f;
                     if (GQA && p.gsplit > 1) {
-                        float* part = p.dkv_part + (size_t)(I.sub * 2 + h) * p.B * p.Hkv * p.N * C::D;
+                        float* part = p.dkv_part + (size_t)(I.sub * 2 + h) * p.B * p.Hkv * nkeys * C::D;
 #pragma unroll
                         for (int c = 0; c < C::D; c += 32) store_chunk32<true>(part, krow * C::D + c, z);
                     } else {
@@ -514,7 +532,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ld32_wait(tmem + lane_off + C::s_col(slot) + h * C::HALF, *reinterpret_cast<uint32_t(*)[32]>(sr));
                 else
                     tmem_ld64_wait(tmem + lane_off + C::s_col(slot) + h * C::HALF, *reinterpret_cast<uint32_t(*)[64]>(sr));
-                bool need_mask = (I.kt * C::BC + C::BC > I.kvl) || (CAUSAL && I.kt * C::BC + C::BC - 1 > i * C::BR);
+                const int coff = causal_offset(p);  // 0 unless rectangular
+                bool need_mask = (I.kt * C::BC + C::BC > I.kvl) || (CAUSAL && I.kt * C::BC + C::BC - 1 > i * C::BR + coff);
                 if constexpr (WINDOW)  // some pair of the tile outside the window
                     need_mask = need_mask || (p.win_right >= 0 && I.kt * C::BC + C::BC - 1 > i * C::BR + p.win_right) ||
                                 (p.win_left >= 0 && I.kt * C::BC < i * C::BR + C::BR - 1 - p.win_left);
@@ -537,7 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int c = 0; c < C::HALF; ++c) {
                         const int q = q0 + c;
-                        bool off = !key_ok || (CAUSAL && key > q);
+                        bool off = !key_ok || (CAUSAL && key > q + coff);
                         if constexpr (WINDOW)
                             off = off || (p.win_right >= 0 && key > q + p.win_right) || (p.win_left >= 0 && key < q - p.win_left);
                         if (off) pv[c] = 0.f;
@@ -604,7 +623,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float mul = h ? p.scale : 1.f;
             void* dst = h ? p.dk : p.dv;
             const bool to_part = GQA && !VARLEN && p.gsplit > 1;  // split group: float32 partial slice
-            float* part = to_part ? p.dkv_part + (size_t)(I.sub * 2 + h) * p.B * p.Hkv * p.N * C::D : nullptr;
+            float* part = to_part ? p.dkv_part + (size_t)(I.sub * 2 + h) * p.B * p.Hkv * nkeys * C::D : nullptr;
             const uint32_t tacc = tmem + lane_off + (h ? C::TM_DK : C::TM_DV);
 #pragma unroll 1
             for (int c = 0; c < C::D; c += 32) {
@@ -613,7 +632,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float f[32];
 #pragma unroll
                 for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(a[e]) * mul;
-                if (key < (VARLEN ? I.seqlen : p.N)) {
+                if (key < (VARLEN ? I.seqlen : nkeys)) {
                     if (to_part)
                         store_chunk32<true>(part, krow * C::D + c, f);
                     else
@@ -634,7 +653,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int rd = 0; rd < snake_rounds(p.num_items) && ok; ++rd) {
             const int it = snake_item(rd, p.num_items);
             if (it < 0) continue;
-            const Item I = get_item<C, CAUSAL, GQA, VARLEN, WINDOW, SPARSE>(it, p);
+            const Item I = get_item<C, CAUSAL, GQA, VARLEN, WINDOW, SPARSE, RECT>(it, p);
             int bhq = I.qh0, i = I.i0;
             for (int s = 0; s < I.n; ++s, step_next<GQA>(I, bhq, i)) {
                 if constexpr (SPARSE) sparse_step<C>(I, p, s, bhq, i);
@@ -696,11 +715,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <class C, bool CAUSAL, bool OUT_F32, bool GQA = false, bool VARLEN = false, bool WINDOW = false,
-          bool SPARSE = false>
+          bool SPARSE = false, bool RECT = false>
 cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                   const CUtensorMap& tdo, const CUtensorMap& tdq, const ParamsT<WINDOW, SPARSE>& p, int grid,
+                   const CUtensorMap& tdo, const CUtensorMap& tdq, const ParamsT<WINDOW, SPARSE, RECT>& p, int grid,
                    cudaStream_t stream) {
-    auto kern = bwd_kernel<C, CAUSAL, OUT_F32, GQA, VARLEN, WINDOW, SPARSE>;
+    auto kern = bwd_kernel<C, CAUSAL, OUT_F32, GQA, VARLEN, WINDOW, SPARSE, RECT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     kern<<<grid, kThreads, C::SMEM, stream>>>(tq, tk, tv, tdo, tdq, p);

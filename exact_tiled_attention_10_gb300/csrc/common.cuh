@@ -143,6 +143,11 @@ struct FwdParamsSparse : FwdParams {
     const int* col_idx;  // [row_ptr[nqb]]
     int nqb, nkb;
 };
+// Rectangular backward: N query rows (statistics, dQ), Nk keys (K, V, dK,
+// dV); with the causal mask query i sees keys j <= i + coff, coff = Nk - N.
+struct BwdParamsRect : BwdParams {
+    int Nk, coff;
+};
 struct BwdParamsSparse : BwdParams {
     const int* col_ptr;  // [nkb + 1]
     const int* row_idx;
@@ -174,6 +179,9 @@ cudaError_t launch_shared_div_check(const float* x, const float* s, int ns, size
                                     cudaStream_t stream);
 // dv, dk = sums of the gsplit partial slices (bf16).
 cudaError_t launch_dkv_sum(const float* part, int gsplit, size_t n, void* dk, void* dv, int grid, cudaStream_t stream);
+cudaError_t launch_bwd_main_rect(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                 const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParamsRect& p, int grid,
+                                 cudaStream_t stream);
 // Transposes the query-block lists into per-key-block lists (one CTA).
 cudaError_t launch_block_lists_transpose(const int* row_ptr, const int* col_idx, int nqb, int nkb, int* col_ptr,
                                          int* row_idx, cudaStream_t stream);

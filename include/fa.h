@@ -163,6 +163,19 @@ fa_status fa_fwd_rect(const void* q, const void* k, const void* v, void* o, floa
                       const int* kv_lens, int num_splits, void* workspace, size_t workspace_bytes,
                       fa_stream_t stream);
 
+/* Backward of the rectangular forward (cross-attention training; Nq query
+ * rows, Nk keys, same causal reading), bf16: dq [B,H,Nq,d]; dk, dv
+ * [B,Hkv,Nk,d] summed over the query heads sharing a key/value head; o and
+ * lse from fa_fwd_rect.  Workspace: fa_bwd_rect_workspace_size(...) bytes
+ * (at least fa_bwd_workspace_size(FA_BF16, B, H, Nq, d); the extra space
+ * lets few key blocks split their query heads, as fa_bwd_gqa). */
+size_t fa_bwd_rect_workspace_size(int B, int H, int Hkv, int Nq, int Nk, int d);
+fa_status fa_bwd_rect(const void* q, const void* k, const void* v, const void* o,
+                      const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                      int B, int H, int Hkv, int Nq, int Nk, int d, float scale, int causal,
+                      const int* kv_lens, void* workspace, size_t workspace_bytes,
+                      fa_stream_t stream);
+
 /* Shared key/value heads (grouped-query attention; multi-query for Hkv = 1),
  * bf16.  q, o: [B,H,N,d]; k, v: [B,Hkv,N,d] with H a multiple of Hkv; query
  * head h attends with key/value head h / (H / Hkv) -- the head broadcast of
