@@ -63,6 +63,8 @@ _SIGS = {
     "fa_fwd_block_sparse": ([_vp] * 5 + [_i, _i, _i, _i, _i, _f, _i, _vp, _vp, _vp, _vp], _i),
     "fa_bwd_block_sparse_workspace_size": ([_i] * 4, _sz),
     "fa_bwd_gqa_workspace_size": ([_i] * 5, _sz),
+    "fa_bwd_deterministic_workspace_size": ([_i] * 5, _sz),
+    "fa_bwd_deterministic": ([_vp] * 9 + [_i, _i, _i, _i, _i, _f, _i, _vp, _vp, _sz, _vp], _i),
     "fa_selftest_quantiser_division": ([_vp, _vp, _i, _sz, _vp, _vp, _vp], _i),
     "fa_quantize_fp8_qkv": ([_vp] * 9 + [_i] * 5 + [_vp], _i),
     "fa_fwd_rect_workspace_size": ([_i] * 7, _sz),
@@ -408,10 +410,13 @@ def backward_varlen(q, k, v, o, lse, dout, cu_seqlens, max_seqlen: int, causal: 
 def backward(q, k, v, o, lse, dout, causal: bool = False, scale: Optional[float] = None,
              kv_lens=None, workspace: Optional[torch.Tensor] = None,
              dq: Optional[torch.Tensor] = None, dk: Optional[torch.Tensor] = None,
-             dv: Optional[torch.Tensor] = None, window: Optional[Tuple[int, int]] = None):
+             dv: Optional[torch.Tensor] = None, window: Optional[Tuple[int, int]] = None,
+             deterministic: bool = False):
     """dQ, dK, dV of L = sum(O * dout).  With fewer key/value heads (k, v
     [B,Hkv,N,d]), dK and dV sum over the query heads sharing each one.
-    window: the forward's sliding window (see forward)."""
+    window: the forward's sliding window (see forward).
+    deterministic: bitwise-reproducible gradients (bf16, no window): the dQ
+    parts are added in key-block order."""
     lib = load_library()
     _need_cuda(q, k, v, o, lse, dout)
     B, H, N, d = q.shape
@@ -421,8 +426,13 @@ def backward(q, k, v, o, lse, dout, causal: bool = False, scale: Optional[float]
     dt = FA_F32 if q.dtype == torch.float32 else FA_BF16
     wl, wr = _window(window)
     grouped = Hkv != H or wl >= 0 or wr >= 0
-    wsz = int(lib.fa_bwd_gqa_workspace_size(B, H, Hkv, N, d) if grouped and dt == FA_BF16
-              else lib.fa_bwd_workspace_size(dt, B, H, N, d))
+    if deterministic:
+        if dt != FA_BF16 or wl >= 0 or wr >= 0 or H % Hkv != 0:
+            raise ValueError("the deterministic backward takes bfloat16 tensors, no window, H a multiple of Hkv")
+        wsz = int(lib.fa_bwd_deterministic_workspace_size(B, H, Hkv, N, d))
+    else:
+        wsz = int(lib.fa_bwd_gqa_workspace_size(B, H, Hkv, N, d) if grouped and dt == FA_BF16
+                  else lib.fa_bwd_workspace_size(dt, B, H, N, d))
     ws = workspace
     if ws is None or ws.numel() * ws.element_size() < wsz:
         ws = torch.empty(wsz, dtype=torch.uint8, device=q.device)
@@ -430,6 +440,11 @@ def backward(q, k, v, o, lse, dout, causal: bool = False, scale: Optional[float]
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     _need_cuda(dq, dk, dv)
+    if deterministic:
+        _check(lib.fa_bwd_deterministic(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
+                                        _ptr(dk), _ptr(dv), B, H, Hkv, N, d, scale, int(bool(causal)), _ptr(kv),
+                                        _ptr(ws), ws.numel() * ws.element_size(), _stream(q)))
+        return dq, dk, dv
     if wl >= 0 or wr >= 0:
         if q.dtype != torch.bfloat16 or H % Hkv != 0:
             raise ValueError("the sliding window needs bfloat16 tensors and H a multiple of Hkv")

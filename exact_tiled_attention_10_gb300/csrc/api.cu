@@ -680,13 +680,33 @@ int choose_gsplit(long items, int group, int sms) {
     return group;
 }
 
+// Deterministic backward: the number of dQ accumulators, from the shape
+// alone (so that the result does not depend on the device): enough that the
+// key blocks of one key/value head in one round of a 152-SM grid, which run
+// at the same time in key-block-major order, land in different accumulators;
+// at most 8 and at most the number of key blocks.
+constexpr int kDetMaxAcc = 8;  // the conversion kernel reads at most 8
+int det_num_acc(int B, int Hkv, int N) {
+    const long heads = (long)B * Hkv, kt = (N + 127) / 128;
+    long a = (fa::kNumSMsDefault + heads - 1) / heads + 1;
+    if (a > kDetMaxAcc) a = kDetMaxAcc;
+    if (a > kt) a = kt;
+    return (int)(a < 1 ? 1 : a);
+}
+// Turn counters: 4 per dQ tile of BR rows, per accumulator.
+size_t det_turn_bytes(int nacc, int B, int H, int N, int d) {
+    const size_t Np = round_up((size_t)N, 128);
+    return (size_t)nacc * B * H * (Np / (d == 128 ? 64 : 128)) * 4 * sizeof(int);
+}
+size_t det_acc_bytes(int B, int H, int N, int d) { return (size_t)B * H * round_up((size_t)N, 128) * d * sizeof(float); }
+
 size_t dkv_part_bytes(int g, int B, int Hkv, int N, int d) { return (size_t)g * 2 * B * Hkv * N * d * sizeof(float); }
 
 fa_status bwd_main_impl(const BwdCtx& c, bool f32, const void* qb, const void* kb, const void* vb, const void* gb,
                         void* dk, void* dv, int B, int H, int N, int d, float scale, int causal, const int* kv_lens,
                         cudaStream_t stream, int Hkv = 0, int win_left = -1, int win_right = -1,
                         const int* col_ptr = nullptr, const int* row_idx = nullptr, float* dkv_part = nullptr,
-                        size_t part_bytes = 0, int Nk = -1) {
+                        size_t part_bytes = 0, int Nk = -1, int* dq_turn = nullptr, int nacc = 1) {
     const int BH = c.BH, Np = c.Np;
     const bool rect = Nk >= 0;  // rectangular: N query rows, Nk keys
     if (!rect) Nk = N;
@@ -700,7 +720,9 @@ fa_status bwd_main_impl(const BwdCtx& c, bool f32, const void* qb, const void* k
     FA_TRY(make_map_3d(&tdo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, gb, d, N, BH, 64, BR, CU_TENSOR_MAP_SWIZZLE_128B));
     FA_TRY(make_map_3d(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kb, d, Nk, BHkv, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B));
     FA_TRY(make_map_3d(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, vb, d, Nk, BHkv, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B));
-    FA_TRY(make_map_dqacc(&tdq, dqacc, d, (long long)BH * Np));
+    if ((long long)BH * Np * nacc >= (1LL << 31))
+        return fail(FA_ERR_UNSUPPORTED, "dQ accumulator rows exceed the 32-bit tensor coordinate range");
+    FA_TRY(make_map_dqacc(&tdq, dqacc, d, (long long)BH * Np * nacc));
     fa::BwdParams p;
     memset(&p, 0, sizeof(p));
     p.B = B; p.H = H; p.N = N; p.Np = Np; p.Hkv = Hkv;
@@ -729,7 +751,17 @@ fa_status bwd_main_impl(const BwdCtx& c, bool f32, const void* qb, const void* k
     }
     const int grid = grid_for_items(p.num_items, c.dev->sms);
     cudaError_t e;
-    if (rect) {
+    if (dq_turn) {
+        // deterministic: zeroed turn counters, one per quarter of a dQ tile
+        fa::BwdParamsDet pd;
+        memset(&pd, 0, sizeof(pd));
+        static_cast<fa::BwdParams&>(pd) = p;
+        pd.nqb = Np / BR;
+        pd.dq_turn = dq_turn;
+        pd.nacc = nacc;
+        e = cudaMemsetAsync(dq_turn, 0, det_turn_bytes(nacc, B, H, N, d), stream);
+        if (e == cudaSuccess) e = fa::launch_bwd_main_det(d, causal != 0, tq, tk, tv, tdo, tdq, pd, grid, stream);
+    } else if (rect) {
         fa::BwdParamsRect pr;
         memset(&pr, 0, sizeof(pr));
         static_cast<fa::BwdParams&>(pr) = p;
@@ -1044,6 +1076,46 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  void* workspace, size_t workspace_bytes, fa_stream_t stream) {
     return fa_bwd_ex(FA_BF16, q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, causal, kv_lens, workspace,
                      workspace_bytes, stream);
+}
+
+size_t fa_bwd_deterministic_workspace_size(int B, int H, int Hkv, int N, int d) {
+    const size_t base = fa_bwd_workspace_size(FA_BF16, B, H, N, d);
+    if (base == 0 || Hkv < 1 || H % Hkv != 0) return 0;
+    const int nacc = det_num_acc(B, Hkv, N);
+    // accumulators 1 .. nacc-1 follow the first (the last region of the base layout)
+    return base + (size_t)(nacc - 1) * det_acc_bytes(B, H, N, d) + det_turn_bytes(nacc, B, H, N, d);
+}
+
+fa_status fa_bwd_deterministic(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                               const void* dout, void* dq, void* dk, void* dv, int B, int H, int Hkv, int N, int d,
+                               float scale, int causal, const int* kv_lens, void* workspace, size_t workspace_bytes,
+                               fa_stream_t stream) {
+    FA_CHECK_PTR(q);
+    FA_CHECK_PTR(k);
+    FA_CHECK_PTR(v);
+    FA_CHECK_PTR(o);
+    FA_CHECK_PTR(lse);
+    FA_CHECK_PTR(dout);
+    FA_CHECK_PTR(dq);
+    FA_CHECK_PTR(dk);
+    FA_CHECK_PTR(dv);
+    if (Hkv < 1 || H % Hkv != 0) return fail(FA_ERR_INVALID_ARG, "H (%d) must be a multiple of Hkv (%d)", H, Hkv);
+    BwdCtx c{};
+    FA_TRY(bwd_setup(FA_BF16, B, H, N, d, scale, workspace, workspace_bytes, &c));
+    const size_t need = fa_bwd_deterministic_workspace_size(B, H, Hkv, N, d);
+    if (workspace_bytes < need)
+        return fail(FA_ERR_INVALID_ARG, "workspace too small (%zu < %zu bytes)", workspace_bytes, need);
+    const int nacc = det_num_acc(B, Hkv, N);
+    if (c.L.dqacc + det_acc_bytes(B, H, N, d) != c.L.total)
+        return fail(FA_ERR_INVALID_ARG, "internal: the dQ accumulator is not the last workspace region");
+    int* turn = reinterpret_cast<int*>(c.ws + c.L.total + (size_t)(nacc - 1) * det_acc_bytes(B, H, N, d));
+    FA_TRY(bwd_pre_impl(c, false, o, lse, dout, N, d, stream));
+    FA_TRY(bwd_main_impl(c, false, q, k, v, dout, dk, dv, B, H, N, d, scale, causal, kv_lens, stream, Hkv, -1, -1,
+                         nullptr, nullptr, nullptr, 0, -1, turn, nacc));
+    cudaError_t e = fa::launch_bwd_dq_det(reinterpret_cast<float*>(c.ws + c.L.dqacc), turn, dq, scale, c.BH, N, c.Np,
+                                          d, nacc, bw_grid(c.dev), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "dQ conversion launch");
+    return FA_OK;
 }
 
 int fa_fp8_num_blocks(int N) { return N > 0 ? (N + 63) / 64 : 0; }

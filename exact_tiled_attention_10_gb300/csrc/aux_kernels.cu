@@ -110,6 +110,54 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ a
     }
 }
 
+// Deterministic backward's conversion: dQ[r, :] = scale * the sum, in order
+// a = 0, 1, ..., of the accumulators a that received a write for row r's
+// quarter of its tile (turn count > 0; the others were never written).  Tiles
+// are BR = 64 rows with quarters of 32 columns (d = 128), or BR = 128 rows with
+// quarters of 32 rows (d = 64).
+__global__ void __launch_bounds__(256) bwd_dq_det_kernel(const float* __restrict__ acc, const int* __restrict__ turn,
+                                                         __nv_bfloat16* __restrict__ dq, float scale, int BH, int N,
+                                                         int Np, int D, int nacc) {
+    constexpr int kMaxAcc = 8;
+    const int BR = (D == 128) ? 64 : 128, nqb = Np / BR;
+    const long groups_per_row = D / 8;
+    const long total = (long)BH * N * groups_per_row;
+    const size_t acc_elems = (size_t)BH * Np * D, turn_stride = (size_t)BH * nqb * 4;
+    for (long g = (long)blockIdx.x * blockDim.x + threadIdx.x; g < total; g += (long)gridDim.x * blockDim.x) {
+        const long row = g / groups_per_row;
+        const int c = (int)(g - row * groups_per_row) * 8;
+        const long bh = row / N;
+        const int i = (int)(row - bh * N);
+        const int quarter = (D == 128) ? c / 32 : (i % 128) / 32;
+        const size_t tix = ((size_t)bh * nqb + i / BR) * 4 + quarter;
+        const size_t off = ((size_t)bh * Np + i) * D + c;
+        // all counts, then all written accumulators, as independent loads
+        bool has[kMaxAcc];
+#pragma unroll
+        for (int a = 0; a < kMaxAcc; ++a) has[a] = a < nacc && __ldg(turn + a * turn_stride + tix) != 0;
+        float4 x[kMaxAcc], y[kMaxAcc];
+#pragma unroll
+        for (int a = 0; a < kMaxAcc; ++a) {
+            if (has[a]) {
+                const float4* src = reinterpret_cast<const float4*>(acc + a * acc_elems + off);
+                x[a] = __ldg(src);
+                y[a] = __ldg(src + 1);
+            }
+        }
+        float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int a = 0; a < kMaxAcc; ++a) {
+            if (has[a]) {
+                s[0] += x[a].x; s[1] += x[a].y; s[2] += x[a].z; s[3] += x[a].w;
+                s[4] += y[a].x; s[5] += y[a].y; s[6] += y[a].z; s[7] += y[a].w;
+            }
+        }
+        *reinterpret_cast<uint4*>(dq + (size_t)row * D + c) =
+            make_uint4(pack_bf16x2(s[0] * scale, s[1] * scale), pack_bf16x2(s[2] * scale, s[3] * scale),
+                       pack_bf16x2(s[4] * scale, s[5] * scale), pack_bf16x2(s[6] * scale, s[7] * scale));
+    }
+}
+
 // Packed variable-length sequences: the statistics and the dQ accumulator are
 // laid out per (head, sequence) as [H][batch][MSp] rows (MSp = max_seqlen
 // rounded up to 128), so that every query block of every sequence starts on
@@ -522,6 +570,12 @@ cudaError_t launch_bwd_pre(const void* o, const void* dout, bool in_f32, const f
         if (in_f32) bwd_pre_kernel<64, true><<<grid, 256, 0, s>>>(o, dout, lse, lse2, dvec, dq_acc, BH, N, Np);
         else bwd_pre_kernel<64, false><<<grid, 256, 0, s>>>(o, dout, lse, lse2, dvec, dq_acc, BH, N, Np);
     }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dq_det(const float* acc, const int* turn, void* dq, float scale, int BH, int N, int Np, int d,
+                              int nacc, int grid, cudaStream_t s) {
+    bwd_dq_det_kernel<<<grid, 256, 0, s>>>(acc, turn, reinterpret_cast<__nv_bfloat16*>(dq), scale, BH, N, Np, d, nacc);
     return cudaGetLastError();
 }
 

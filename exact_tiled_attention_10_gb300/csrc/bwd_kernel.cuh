@@ -48,6 +48,10 @@ constexpr int kThreads = 448;
 constexpr int kDqWarp0 = 8;
 constexpr int kProducerWarp = 12;
 constexpr int kMmaWarp = 13;
+// Deterministic instance: a drain warp passes a tile's turn on kDetLag steps
+// after writing it, when the write has completed, so that it never waits for
+// a write in flight.
+constexpr int kDetLag = 4;
 
 template <int D_>
 struct Cfg {
@@ -127,6 +131,11 @@ using ParamsT = typename std::conditional<
     typename std::conditional<SPARSE, BwdParamsSparse,
                               typename std::conditional<RECT, BwdParamsRect, BwdParams>::type>::type>::type;
 
+// DET: the deterministic instance (p is a BwdParamsDet; plain or shared heads
+// only): each drain warp adds its quarter of a dQ tile only on its turn.
+template <bool WINDOW, bool SPARSE, bool RECT, bool DET>
+using KernelParamsT = typename std::conditional<DET, BwdParamsDet, ParamsT<WINDOW, SPARSE, RECT>>::type;
+
 // Keys of a head (K, V, dK, dV rows) and the causal offset.
 template <class PT>
 __device__ __forceinline__ int key_count(const PT& p) {
@@ -140,7 +149,7 @@ __device__ __forceinline__ int causal_offset(const PT& p) {
 }
 
 template <class C, bool CAUSAL, bool GQA, bool VARLEN = false, bool WINDOW = false, bool SPARSE = false,
-          bool RECT = false>
+          bool RECT = false, bool DET = false>
 __device__ __forceinline__ Item get_item(int it, const ParamsT<WINDOW, SPARSE, RECT>& p) {
     Item I;
     const int Hkv = GQA ? p.Hkv : p.H;
@@ -152,7 +161,10 @@ __device__ __forceinline__ Item get_item(int it, const ParamsT<WINDOW, SPARSE, R
         I.sub = it % gs;
         it /= gs;
     }
-    if (CAUSAL) {  // key blocks near the start see the most query rows: first
+    // causal: key blocks near the start see the most query rows: first.
+    // DET: key block major too, so that the key blocks of a head running at
+    // the same time are few and consecutive (they use different accumulators)
+    if (CAUSAL || DET) {
         I.kt = it / BH;
         I.bh = it % BH;
     } else {
@@ -247,6 +259,13 @@ __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* m, uint32_t
         : "memory");
 }
 
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, uint32_t src, int c0, int c1) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(m)),
+                 "r"(src), "r"(c0), "r"(c1)
+                 : "memory");
+}
+
 // ---- MMA groups (warp-wide issue, one elected lane) ----
 // All descriptors arrive as precomputed bases; per-MMA offsets are constants.
 // S^T = K_j Q_i^T  or  dP^T = V_j dO_i^T  (K-major operands)
@@ -295,11 +314,12 @@ __device__ __forceinline__ void mma_dq(uint32_t d_tmem, uint64_t k_mn, uint64_t 
 }
 
 template <class C, bool CAUSAL, bool OUT_F32, bool GQA, bool VARLEN = false, bool WINDOW = false,
-          bool SPARSE = false, bool RECT = false>
+          bool SPARSE = false, bool RECT = false, bool DET = false>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
-               const __grid_constant__ CUtensorMap tdq, const ParamsT<WINDOW, SPARSE, RECT> p) {
+               const __grid_constant__ CUtensorMap tdq, const KernelParamsT<WINDOW, SPARSE, RECT, DET> p) {
+    static_assert(!DET || (!VARLEN && !WINDOW && !SPARSE && !RECT), "deterministic: plain or shared heads only");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -354,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int rd = 0; rd < snake_rounds(p.num_items) && ok; ++rd) {
             const int it = snake_item(rd, p.num_items);
             if (it < 0) continue;
-            const Item I = get_item<C, CAUSAL, GQA, VARLEN, WINDOW, SPARSE, RECT>(it, p);
+            const Item I = get_item<C, CAUSAL, GQA, VARLEN, WINDOW, SPARSE, RECT, DET>(it, p);
             if (I.n == 0) continue;
             if (!(ok = wait_bounded_warp(BAR(C::B_KVEMPTY), kve ^ 1, abort_flag, p.err, kErrWaitBwdProducer))) break;
             kve ^= 1;
@@ -431,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int rd = 0; rd < snake_rounds(p.num_items) && ok; ++rd) {
             const int it = snake_item(rd, p.num_items);
             if (it < 0) continue;
-            const Item I = get_item<C, CAUSAL, GQA, VARLEN, WINDOW, SPARSE, RECT>(it, p);
+            const Item I = get_item<C, CAUSAL, GQA, VARLEN, WINDOW, SPARSE, RECT, DET>(it, p);
             if (I.n == 0) continue;
             if (!(ok = wait_bounded_warp(BAR(C::B_KVFULL), kvph, abort_flag, p.err, kErrWaitBwdMma))) break;
             kvph ^= 1;
@@ -492,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int rd = 0; rd < snake_rounds(p.num_items) && ok; ++rd) {
             const int it = snake_item(rd, p.num_items);
             if (it < 0) continue;
-            const Item I = get_item<C, CAUSAL, GQA, VARLEN, WINDOW, SPARSE, RECT>(it, p);
+            const Item I = get_item<C, CAUSAL, GQA, VARLEN, WINDOW, SPARSE, RECT, DET>(it, p);
             const int key = I.kt * C::BC + kr;
             // dK, dV row: [B,Hkv,N,d], or token-major [total, Hkv, d] for packed sequences
             const int nkeys = key_count(p);
@@ -650,10 +670,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         float* stage_f = reinterpret_cast<float*>(smem + C::OFF_DQ + wq * C::DQ_WARP_BYTES);
         uint32_t dqph[2] = {0, 0};
         bool ok = true;
+        // DET: pend[j] is the turn counter of the write issued j + 1 steps ago;
+        // it is passed on once that write has completed (kDetLag steps later,
+        // or at the item's end)
+        int* pend[kDetLag];
+#pragma unroll
+        for (int j = 0; j < kDetLag; ++j) pend[j] = nullptr;
         for (int rd = 0; rd < snake_rounds(p.num_items) && ok; ++rd) {
             const int it = snake_item(rd, p.num_items);
             if (it < 0) continue;
-            const Item I = get_item<C, CAUSAL, GQA, VARLEN, WINDOW, SPARSE, RECT>(it, p);
+            const Item I = get_item<C, CAUSAL, GQA, VARLEN, WINDOW, SPARSE, RECT, DET>(it, p);
             int bhq = I.qh0, i = I.i0;
             for (int s = 0; s < I.n; ++s, step_next<GQA>(I, bhq, i)) {
                 if constexpr (SPARSE) sparse_step<C>(I, p, s, bhq, i);
@@ -666,7 +692,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 mbar_arrive(BAR(C::B_DQEMPTY + dqs));
                 // the previous reduction of this warp must have finished reading the staging
-                if (lane == 0) bulk_wait_group_read<0>();
+                if (lane == 0) {
+                    bulk_wait_group_read<0>();
+                    if constexpr (DET) {
+                        if (pend[kDetLag - 1]) {
+                            bulk_wait_group<kDetLag - 1>();  // all but the last kDetLag - 1 writes are done
+                            fence_proxy_async_global();
+                            red_release_gpu_add(pend[kDetLag - 1], 1);
+                        }
+                    }
+                }
+                if constexpr (DET) {
+#pragma unroll
+                    for (int j = kDetLag - 1; j > 0; --j) pend[j] = pend[j - 1];
+                    pend[0] = nullptr;
+                }
                 __syncwarp();
                 if constexpr (C::D == 128) {
                     // lane = head-dim index (wq*32 + lane); column = query. Stage [64 q][32 d].
@@ -689,16 +729,48 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
+                int row = (VARLEN ? bhq * p.B + I.b : bhq) * p.Np + i * C::BR;
+                bool first = false;
+                if constexpr (DET) {
+                    // key block kt writes accumulator kt % nacc after the key blocks
+                    // kt - nacc, kt - 2 nacc, ..., 0 (every key block below kt visits
+                    // the query blocks kt visits); the first of them stores
+                    const int a = I.kt % p.nacc;
+                    int* turn = p.dq_turn + (((size_t)a * (p.B * p.H) + bhq) * p.nqb + i) * 4 + wq;
+                    if (!(ok = wait_turn_warp(turn, I.kt / p.nacc, abort_flag, p.err, kErrWaitBwdDqTurn))) break;
+                    pend[0] = turn;
+                    row += a * (p.B * p.H * p.Np);
+                    first = I.kt < p.nacc;
+                }
                 if (lane == 0) {
+                    if constexpr (DET) fence_proxy_async_global();
                     if constexpr (C::D == 128) {
-                        tma_reduce_add_2d(&tdq, stage, wq * 32, (VARLEN ? bhq * p.B + I.b : bhq) * p.Np + i * C::BR);
+                        if (first) tma_store_2d(&tdq, stage, wq * 32, row);
+                        else tma_reduce_add_2d(&tdq, stage, wq * 32, row);
                     } else {
-                        const int qrow = (VARLEN ? bhq * p.B + I.b : bhq) * p.Np + i * C::BR + wq * 32;
-                        tma_reduce_add_2d(&tdq, stage, 0, qrow);
-                        tma_reduce_add_2d(&tdq, stage + 4096, 32, qrow);
+                        if (first) {
+                            tma_store_2d(&tdq, stage, 0, row + wq * 32);
+                            tma_store_2d(&tdq, stage + 4096, 32, row + wq * 32);
+                        } else {
+                            tma_reduce_add_2d(&tdq, stage, 0, row + wq * 32);
+                            tma_reduce_add_2d(&tdq, stage + 4096, 32, row + wq * 32);
+                        }
                     }
                     bulk_commit_group();
                 }
+                __syncwarp();
+            }
+            if constexpr (DET) {
+                // pass the item's last turns on before the next item's waits
+                if (lane == 0) {
+                    bulk_wait_group<0>();
+                    fence_proxy_async_global();
+#pragma unroll
+                    for (int j = kDetLag - 1; j >= 0; --j)
+                        if (pend[j]) red_release_gpu_add(pend[j], 1);
+                }
+#pragma unroll
+                for (int j = 0; j < kDetLag; ++j) pend[j] = nullptr;
                 __syncwarp();
             }
         }
@@ -715,11 +787,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <class C, bool CAUSAL, bool OUT_F32, bool GQA = false, bool VARLEN = false, bool WINDOW = false,
-          bool SPARSE = false, bool RECT = false>
+          bool SPARSE = false, bool RECT = false, bool DET = false>
 cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                   const CUtensorMap& tdo, const CUtensorMap& tdq, const ParamsT<WINDOW, SPARSE, RECT>& p, int grid,
-                   cudaStream_t stream) {
-    auto kern = bwd_kernel<C, CAUSAL, OUT_F32, GQA, VARLEN, WINDOW, SPARSE, RECT>;
+                   const CUtensorMap& tdo, const CUtensorMap& tdq, const KernelParamsT<WINDOW, SPARSE, RECT, DET>& p,
+                   int grid, cudaStream_t stream) {
+    auto kern = bwd_kernel<C, CAUSAL, OUT_F32, GQA, VARLEN, WINDOW, SPARSE, RECT, DET>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     kern<<<grid, kThreads, C::SMEM, stream>>>(tq, tk, tv, tdo, tdq, p);

@@ -19,6 +19,7 @@ enum : unsigned int {
     kErrWaitBwdDq = 1u << 6,
     kErrWaitDrain = 1u << 7,
     kErrWaitSelftest = 1u << 8,
+    kErrWaitBwdDqTurn = 1u << 9,
 };
 
 constexpr int kNumSMsDefault = 152;
@@ -153,6 +154,21 @@ struct BwdParamsSparse : BwdParams {
     const int* row_idx;
     int nqb, nkb;
 };
+// Deterministic backward: nacc float32 dQ accumulators [nacc][B*H][Np][d]
+// (the first is dq_acc); key block kt writes accumulator kt % nacc, and each
+// accumulator tile of (query head row bhq, query block i) receives its key
+// blocks in increasing order: the first one stores, the others add.
+// dq_turn[((a * B*H + bhq) * nqb + i) * 4 + w] (nqb = Np / query rows per
+// step; w = the drain warp's quarter of the tile) counts the contributions to
+// quarter w of that tile of accumulator a; key block kt writes once it reaches
+// kt / nacc.  The conversion sums the accumulators with a nonzero count in
+// order a = 0, 1, ...  Key blocks that run at the same time go to different
+// accumulators, so they seldom wait for one another.
+struct BwdParamsDet : BwdParams {
+    int* dq_turn;
+    int nqb;
+    int nacc;
+};
 
 // Launch helpers implemented in the kernel translation units.  They return a
 // cudaError_t from the launch itself.
@@ -182,6 +198,13 @@ cudaError_t launch_dkv_sum(const float* part, int gsplit, size_t n, void* dk, vo
 cudaError_t launch_bwd_main_rect(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                  const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParamsRect& p, int grid,
                                  cudaStream_t stream);
+// Deterministic backward (shared key/value heads allowed; p.dq_turn zeroed),
+// and its dQ conversion: dq = scale * the sum of the written accumulators.
+cudaError_t launch_bwd_dq_det(const float* acc, const int* turn, void* dq, float scale, int BH, int N, int Np, int d,
+                              int nacc, int grid, cudaStream_t stream);
+cudaError_t launch_bwd_main_det(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParamsDet& p, int grid,
+                                cudaStream_t stream);
 // Transposes the query-block lists into per-key-block lists (one CTA).
 cudaError_t launch_block_lists_transpose(const int* row_ptr, const int* col_idx, int nqb, int nkb, int* col_ptr,
                                          int* row_idx, cudaStream_t stream);

@@ -126,6 +126,46 @@ __device__ __forceinline__ void bulk_wait_group() {
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// Order global-memory accesses of the async proxy (bulk reductions) against
+// the generic proxy's (the turn counters below), in both directions.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(reinterpret_cast<uint64_t>(p)) : "memory");
+    return v;
+}
+__device__ __forceinline__ void red_release_gpu_add(int* p, int v) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(v) : "memory");
+}
+// Warp-uniform bounded wait for a turn counter in global memory written by
+// other CTAs: lane 0 polls (acquire) until *counter >= turn, with the same
+// time limit and abort handling as the mbarrier waits.
+__device__ __forceinline__ bool wait_turn_warp(const int* counter, int turn, volatile int* abort_flag,
+                                               unsigned int* err, unsigned int code,
+                                               uint64_t limit_ns = kWaitLimitNs) {
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0 && ld_acquire_gpu(counter) < turn) {
+        const long long t0 = clock64();
+        for (uint32_t i = 1;; ++i) {
+            if (ld_acquire_gpu(counter) >= turn) break;
+            if ((i & 15u) == 0) {
+                if (*abort_flag) {
+                    ok = false;
+                    break;
+                }
+                if ((uint64_t)(clock64() - t0) > limit_ns) {
+                    atomicOr(err, code);
+                    *abort_flag = 1;
+                    ok = false;
+                    break;
+                }
+            }
+        }
+    }
+    return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
 
 // -------------------------------------------------------------- tcgen05 / TMEM
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {

@@ -247,6 +247,31 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o,
                  int B, int H, int N, int d, float scale, int causal, const int* kv_lens,
                  void* workspace, size_t workspace_bytes, fa_stream_t stream);
 
+/* Deterministic backward (flash_attn_func's `deterministic` flag, chapter 18
+ * §18.7.1): the same results as fa_bwd_gqa (Hkv = H: fa_bwd), but dq, dk
+ * and dv are bitwise identical from run to run.  In fa_bwd, the key blocks
+ * add their dQ parts into one float32 accumulator in whatever order they
+ * finish, so the rounding differs between runs.  Here key block kt writes
+ * float32 accumulator kt % A (A = 1 .. 8, from the shape: B, Hkv, N).  Each
+ * quarter of a dQ tile of accumulator a takes its key blocks in increasing
+ * order: the first stores, the others add.  A key block waits (bounded;
+ * FA_ERR_TIMEOUT through fa_check_device_status) for the quarter's turn
+ * counter.  A last kernel sums the A accumulators in order.  Key blocks that
+ * run at the same time use different accumulators, so they seldom wait.
+ * dq [B,H,N,d]; dk, dv [B,Hkv,N,d], summed over the query heads sharing a
+ * key/value head; H % Hkv == 0.  The workspace needs
+ * fa_bwd_deterministic_workspace_size(B, H, Hkv, N, d) bytes: fa_bwd's
+ * layout, A - 1 more accumulators and the counters (zeroed by the call).
+ * The kernel's CTAs (one per SM at most) wait on one another, so they must
+ * all be resident: do not overlap two of these calls on one device.  A wait
+ * that runs out ends the kernel with FA_ERR_TIMEOUT; it never hangs. */
+size_t fa_bwd_deterministic_workspace_size(int B, int H, int Hkv, int N, int d);
+fa_status fa_bwd_deterministic(const void* q, const void* k, const void* v, const void* o,
+                               const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                               int B, int H, int Hkv, int N, int d, float scale, int causal,
+                               const int* kv_lens, void* workspace, size_t workspace_bytes,
+                               fa_stream_t stream);
+
 /* Backward with shared key/value heads (see fa_fwd_gqa), bf16: dq is
  * [B,H,N,d]; dk, dv are [B,Hkv,N,d] and hold the sum over the H / Hkv query
  * heads that share each key/value head (the gradient of the broadcast).

@@ -161,3 +161,28 @@ def test_host_validation_of_the_variant_entry_points():
     # grouped backward: the split workspace is larger only when key blocks are few
     assert lib.fa_bwd_gqa_workspace_size(2, 16, 2, 4096, 128) > lib.fa_bwd_workspace_size(0, 2, 16, 4096, 128)
     assert lib.fa_bwd_gqa_workspace_size(64, 16, 16, 4096, 128) <= lib.fa_bwd_workspace_size(0, 64, 16, 4096, 128) + 256
+
+
+def test_deterministic_backward_workspace_without_gpu():
+    """fa_bwd_deterministic_workspace_size: fa_bwd's layout, then A - 1 more
+    float32 dQ accumulators and A x 4 turn counters per dQ tile, where
+    A = min(8, key blocks, ceil(152 / (B * Hkv)) + 1) depends on the shape
+    only; argument errors are caught on the host."""
+    import exact_tiled_attention_10_gb300 as fa
+    lib = fa.load_library()
+    size = lib.fa_bwd_deterministic_workspace_size
+    for (B, H, Hkv, N, d) in [(2, 16, 16, 4096, 128), (1, 8, 1, 300, 64), (64, 16, 16, 1024, 128)]:
+        Np = -(-N // 128) * 128
+        kt = -(-N // 128)
+        A = min(8, kt, -(-152 // (B * Hkv)) + 1)
+        acc = B * H * Np * d * 4
+        turns = A * B * H * (Np // (64 if d == 128 else 128)) * 4 * 4
+        assert size(B, H, Hkv, N, d) == lib.fa_bwd_workspace_size(0, B, H, N, d) + (A - 1) * acc + turns
+    assert size(1, 8, 3, 256, 128) == 0 and size(1, 8, 8, 256, 96) == 0
+    A_ = 4096
+    need = size(1, 4, 4, 256, 128)
+    # bad group; workspace below fa_bwd's own layout
+    assert lib.fa_bwd_deterministic(A_, A_, A_, A_, A_, A_, A_, A_, A_, 1, 4, 3, 256, 128, 0.1, 0, None, A_, need,
+                                    None) == 1
+    assert lib.fa_bwd_deterministic(A_, A_, A_, A_, A_, A_, A_, A_, A_, 1, 4, 4, 256, 128, 0.1, 0, None, A_, 1024,
+                                    None) == 1
