@@ -76,6 +76,9 @@ _SIGS = {
     "fa_fwd_varlen": ([_vp] * 6 + [_i, _i, _i, _i, _i, _i, _f, _i, _vp], _i),
     "fa_bwd_varlen_workspace_size": ([_i] * 4, _sz),
     "fa_bwd_varlen": ([_vp] * 10 + [_i, _i, _i, _i, _i, _i, _f, _i, _vp, _sz, _vp], _i),
+    "fa_fwd_bnhd": ([_vp] * 5 + [_i, _i, _i, _i, _i, _f, _i, _vp], _i),
+    "fa_bwd_bnhd_workspace_size": ([_i] * 4, _sz),
+    "fa_bwd_bnhd": ([_vp] * 9 + [_i, _i, _i, _i, _i, _f, _i, _vp, _sz, _vp], _i),
     "fa_bwd_gqa": ([_vp] * 9 + [_i, _i, _i, _i, _i, _f, _i, _vp, _vp, _sz, _vp], _i),
     "fa_fwd_split_workspace_size": ([_i] * 7, _sz),
     "fa_fwd_split_count": ([_i] * 7, _i),
@@ -384,6 +387,49 @@ def forward_varlen(q, k, v, cu_seqlens, max_seqlen: int, causal: bool = False,
     _check(lib.fa_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(l), _ptr(cu), cu.numel() - 1, T,
                              int(max_seqlen), H, Hkv, d, scale, int(bool(causal)), _stream(q)))
     return o, l
+
+
+def _bnhd_shapes(q, k, v):
+    B, N, H, d = q.shape
+    Hkv = k.shape[2]
+    if (q.dtype != torch.bfloat16 or k.dtype != q.dtype or v.dtype != q.dtype or k.shape != (B, N, Hkv, d)
+            or v.shape != k.shape or H % Hkv != 0):
+        raise ValueError("q [B,N,H,d], k, v [B,N,Hkv,d] bfloat16 with H a multiple of Hkv")
+    return B, N, H, Hkv, d
+
+
+def forward_bnhd(q, k, v, causal: bool = False, scale: Optional[float] = None,
+                 out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None):
+    """Forward on flash_attn_func's layout: q [B,N,H,d], k, v [B,N,Hkv,d]
+    (bf16).  Returns O [B,N,H,d] and LSE [B,H,N] (float32)."""
+    lib = load_library()
+    _need_cuda(q, k, v)
+    B, N, H, Hkv, d = _bnhd_shapes(q, k, v)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = torch.empty_like(q) if out is None else out
+    l = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check(lib.fa_fwd_bnhd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(l), B, N, H, Hkv, d, scale,
+                           int(bool(causal)), _stream(q)))
+    return o, l
+
+
+def backward_bnhd(q, k, v, o, lse, dout, causal: bool = False, scale: Optional[float] = None,
+                  workspace: Optional[torch.Tensor] = None):
+    """dQ [B,N,H,d], dK, dV [B,N,Hkv,d] of forward_bnhd (dK, dV summed over
+    the query heads sharing a key/value head)."""
+    lib = load_library()
+    _need_cuda(q, k, v, o, lse, dout)
+    B, N, H, Hkv, d = _bnhd_shapes(q, k, v)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    wsz = int(lib.fa_bwd_bnhd_workspace_size(B, N, H, d))
+    ws = workspace
+    if ws is None or ws.numel() * ws.element_size() < wsz:
+        ws = torch.empty(wsz, dtype=torch.uint8, device=q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    _check(lib.fa_bwd_bnhd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
+                           _ptr(dv), B, N, H, Hkv, d, scale, int(bool(causal)), _ptr(ws),
+                           ws.numel() * ws.element_size(), _stream(q)))
+    return dq, dk, dv
 
 
 def backward_varlen(q, k, v, o, lse, dout, cu_seqlens, max_seqlen: int, causal: bool = False,

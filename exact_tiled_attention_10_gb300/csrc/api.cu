@@ -8,6 +8,7 @@
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
+#include <climits>
 #include <cstring>
 #include <mutex>
 
@@ -563,9 +564,16 @@ fa_status fa_fwd_block_sparse(const void* q, const void* k, const void* v, void*
                     nullptr, 0, stream, 1, nullptr, 0, Hkv, -1, -1, row_ptr, col_idx);
 }
 
-fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens,
-                        int batch, int total, int max_seqlen, int H, int Hkv, int d, float scale, int causal,
-                        fa_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Token-major forward ([total, H, d] tensors): packed sequences from
+// cu_seqlens, or, with cu_seqlens NULL, batch sequences of max_seqlen tokens
+// each (the [B, N, H, d] layout, LSE [B, H, N]).
+fa_status fwd_packed_impl(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens,
+                          int batch, int total, int max_seqlen, int H, int Hkv, int d, float scale, int causal,
+                          fa_stream_t stream) {
     FA_TRY(check_common(batch, H, max_seqlen, d, scale));
     if (total <= 0) return fail(FA_ERR_INVALID_ARG, "total must be positive");
     if (Hkv < 1 || H % Hkv != 0) return fail(FA_ERR_INVALID_ARG, "H (%d) must be a multiple of Hkv (%d)", H, Hkv);
@@ -574,7 +582,6 @@ fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, fl
     FA_CHECK_PTR(v);
     FA_CHECK_PTR(o);
     FA_CHECK_PTR(lse);
-    if (!cu_seqlens) return fail(FA_ERR_INVALID_ARG, "cu_seqlens must not be NULL");
     DeviceInfo* dev = nullptr;
     FA_TRY(device_info(&dev));
     fa::FwdMaps m;
@@ -600,6 +607,23 @@ fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, fl
     cudaError_t e = fa::launch_fwd_varlen(d, causal != 0, m, p, grid_for_items(p.num_items, dev->sms), stream);
     if (e != cudaSuccess) return cuda_fail(e, "varlen forward launch");
     return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens,
+                        int batch, int total, int max_seqlen, int H, int Hkv, int d, float scale, int causal,
+                        fa_stream_t stream) {
+    if (!cu_seqlens) return fail(FA_ERR_INVALID_ARG, "cu_seqlens must not be NULL");
+    return fwd_packed_impl(q, k, v, o, lse, cu_seqlens, batch, total, max_seqlen, H, Hkv, d, scale, causal, stream);
+}
+
+fa_status fa_fwd_bnhd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int N, int H, int Hkv,
+                      int d, float scale, int causal, fa_stream_t stream) {
+    if ((long long)B * N > INT_MAX) return fail(FA_ERR_INVALID_ARG, "B * N exceeds the 32-bit token index");
+    return fwd_packed_impl(q, k, v, o, lse, nullptr, B, B * N, N, H, Hkv, d, scale, causal, stream);
 }
 
 size_t fa_fwd_workspace_size(fa_dtype dtype, int B, int H, int N, int d) {
@@ -1010,10 +1034,15 @@ size_t fa_bwd_varlen_workspace_size(int batch, int max_seqlen, int H, int d) {
     return 2 * round_up(R * 4, 256) + round_up(R * d * 4, 256);
 }
 
-fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse,
-                        const void* dout, void* dq, void* dk, void* dv, const int* cu_seqlens, int batch, int total,
-                        int max_seqlen, int H, int Hkv, int d, float scale, int causal, void* workspace,
-                        size_t workspace_bytes, fa_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Token-major backward (see fwd_packed_impl; cu_seqlens NULL = uniform lengths).
+fa_status bwd_packed_impl(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                          const void* dout, void* dq, void* dk, void* dv, const int* cu_seqlens, int batch, int total,
+                          int max_seqlen, int H, int Hkv, int d, float scale, int causal, void* workspace,
+                          size_t workspace_bytes, fa_stream_t stream) {
     FA_TRY(check_common(batch, H, max_seqlen, d, scale));
     if (total <= 0) return fail(FA_ERR_INVALID_ARG, "total must be positive");
     if (Hkv < 1 || H % Hkv != 0) return fail(FA_ERR_INVALID_ARG, "H (%d) must be a multiple of Hkv (%d)", H, Hkv);
@@ -1027,7 +1056,6 @@ fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const void*
     FA_CHECK_PTR(dk);
     FA_CHECK_PTR(dv);
     FA_CHECK_PTR(workspace);
-    if (!cu_seqlens) return fail(FA_ERR_INVALID_ARG, "cu_seqlens must not be NULL");
     const size_t need = fa_bwd_varlen_workspace_size(batch, max_seqlen, H, d);
     if (workspace_bytes < need) return fail(FA_ERR_INVALID_ARG, "workspace too small (%zu < %zu bytes)", workspace_bytes, need);
     DeviceInfo* dev = nullptr;
@@ -1069,6 +1097,29 @@ fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const void*
     e = fa::launch_bwd_dq_varlen(dqacc, cu_seqlens, dq, scale, H, batch, max_seqlen, MSp, d, bw_grid(dev), stream);
     if (e != cudaSuccess) return cuda_fail(e, "varlen dQ conversion launch");
     return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                        const void* dout, void* dq, void* dk, void* dv, const int* cu_seqlens, int batch, int total,
+                        int max_seqlen, int H, int Hkv, int d, float scale, int causal, void* workspace,
+                        size_t workspace_bytes, fa_stream_t stream) {
+    if (!cu_seqlens) return fail(FA_ERR_INVALID_ARG, "cu_seqlens must not be NULL");
+    return bwd_packed_impl(q, k, v, o, lse, dout, dq, dk, dv, cu_seqlens, batch, total, max_seqlen, H, Hkv, d, scale,
+                           causal, workspace, workspace_bytes, stream);
+}
+
+size_t fa_bwd_bnhd_workspace_size(int B, int N, int H, int d) { return fa_bwd_varlen_workspace_size(B, N, H, d); }
+
+fa_status fa_bwd_bnhd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                      void* dq, void* dk, void* dv, int B, int N, int H, int Hkv, int d, float scale, int causal,
+                      void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+    if ((long long)B * N > INT_MAX) return fail(FA_ERR_INVALID_ARG, "B * N exceeds the 32-bit token index");
+    return bwd_packed_impl(q, k, v, o, lse, dout, dq, dk, dv, nullptr, B, B * N, N, H, Hkv, d, scale, causal,
+                           workspace, workspace_bytes, stream);
 }
 
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,

@@ -164,8 +164,13 @@ __global__ void __launch_bounds__(256) bwd_dq_det_kernel(const float* __restrict
 // an aligned row and padding rows (position >= the sequence's length) carry
 // LSE*log2(e) = +inf, D = 0 (their P is 0 in the backward).  Row r = (h *
 // batch + b) * MSp + pos reads token cu_seqlens[b] + pos of O, dO [total, H, d].
+// Without cu_seqlens every sequence has max_seqlen tokens (token b *
+// max_seqlen + pos: [B, N, H, d] tensors) and the LSE is [B, H, N].
 __device__ __forceinline__ int varlen_len(const int* cu, int b, int max_seqlen) {
-    return max(0, min(__ldg(cu + b + 1) - __ldg(cu + b), max_seqlen));
+    return cu ? max(0, min(__ldg(cu + b + 1) - __ldg(cu + b), max_seqlen)) : max_seqlen;
+}
+__device__ __forceinline__ long varlen_token(const int* cu, int b, int max_seqlen, int pos) {
+    return (cu ? (long)__ldg(cu + b) : (long)b * max_seqlen) + pos;
 }
 
 template <int D>
@@ -189,7 +194,7 @@ __global__ void __launch_bounds__(256) bwd_pre_varlen_kernel(const __nv_bfloat16
         const int pos = valid_row ? (int)(r - hb * MSp) : 0;
         const int h = (int)(hb / batch), b = (int)(hb - (long)h * batch);
         const bool real = valid_row && pos < varlen_len(cu, b, max_seqlen);
-        const long token = real ? (long)__ldg(cu + b) + pos : 0;
+        const long token = real ? varlen_token(cu, b, max_seqlen, pos) : 0;
         float acc = 0.f;
         if (real) {
             const size_t e = ((size_t)token * H + h) * D + sl * 8;
@@ -208,7 +213,8 @@ __global__ void __launch_bounds__(256) bwd_pre_varlen_kernel(const __nv_bfloat16
             if (sl == 0) {
                 float l2 = INFINITY;
                 if (real) {
-                    const float L = lse[(size_t)h * total + token];
+                    const float L = cu ? lse[(size_t)h * total + token]
+                                       : lse[((size_t)b * H + h) * max_seqlen + pos];
                     l2 = (L == -INFINITY) ? INFINITY : L * 1.4426950408889634f;
                 }
                 lse2[r] = l2;
@@ -232,7 +238,7 @@ __global__ void __launch_bounds__(256) bwd_dq_varlen_kernel(const float* __restr
         const int pos = (int)(r - hb * MSp);
         const int h = (int)(hb / batch), b = (int)(hb - (long)h * batch);
         if (pos >= varlen_len(cu, b, max_seqlen)) continue;
-        const long token = (long)__ldg(cu + b) + pos;
+        const long token = varlen_token(cu, b, max_seqlen, pos);
         const float4* src = reinterpret_cast<const float4*>(acc + (size_t)r * D + c);
         const float4 x = __ldg(src), y = __ldg(src + 1);
         *reinterpret_cast<uint4*>(dq + ((size_t)token * H + h) * D + c) =

@@ -179,7 +179,9 @@ __device__ __forceinline__ Item get_item(int it, const ParamsT<WINDOW, SPARSE, R
     I.tb = 0;
     I.seqlen = p.N;
     if (VARLEN) {
-        const int a = __ldg(p.cu_seqlens + I.b), e = __ldg(p.cu_seqlens + I.b + 1);
+        // no cu_seqlens: B sequences of N tokens each ([B, N, H, d] tensors)
+        const int a = p.cu_seqlens ? __ldg(p.cu_seqlens + I.b) : I.b * p.N;
+        const int e = p.cu_seqlens ? __ldg(p.cu_seqlens + I.b + 1) : a + p.N;
         I.tb = a;
         I.seqlen = max(0, min(e - a, p.N));
     }

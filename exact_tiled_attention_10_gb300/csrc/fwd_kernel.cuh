@@ -253,7 +253,8 @@ __device__ __forceinline__ size_t out_row(const IT& I, int row, const FwdParams&
 }
 template <class IT>
 __device__ __forceinline__ size_t lse_index(const IT& I, int row, const FwdParams& p) {
-    if constexpr (is_packed<IT>()) return (size_t)I.h * p.total + I.tb + row;
+    if constexpr (is_packed<IT>())  // [H, total]; uniform lengths (no cu_seqlens): [B, H, N]
+        return p.cu_seqlens ? (size_t)I.h * p.total + I.tb + row : ((size_t)I.b * p.H + I.h) * p.N + row;
     else return (size_t)I.bh * p.N + row;
 }
 
@@ -282,7 +283,9 @@ __device__ __forceinline__ ItemT<VARLEN, WINDOW, SPARSE> get_item(int unit, cons
     I.kvh = I.b * p.Hkv + h / (p.H / p.Hkv);
     int kvl, rows;
     if constexpr (VARLEN) {
-        const int a = __ldg(p.cu_seqlens + I.b), e = __ldg(p.cu_seqlens + I.b + 1);
+        // no cu_seqlens: B sequences of N tokens each ([B, N, H, d] tensors)
+        const int a = p.cu_seqlens ? __ldg(p.cu_seqlens + I.b) : I.b * p.N;
+        const int e = p.cu_seqlens ? __ldg(p.cu_seqlens + I.b + 1) : a + p.N;
         I.h = h;
         I.tb = a;
         I.seqlen = max(0, min(e - a, p.N));

@@ -229,6 +229,17 @@ fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, fl
                         const int* cu_seqlens, int batch, int total, int max_seqlen, int H, int Hkv,
                         int d, float scale, int causal, fa_stream_t stream);
 
+/* Forward on flash_attn_func's own layout ([CH18] §18.7.1: q is (batch,
+ * seqlen, nheads, headdim), k and v (batch, seqlen_k, nheads_k, headdim)),
+ * bf16: q, o [B, N, H, d]; k, v [B, N, Hkv, d]; lse float32 [B, H, N].  Same
+ * results as fa_fwd_gqa on the transposed tensors (no key padding: use
+ * fa_fwd_varlen for sequences of different lengths); the kernels read the
+ * rows in place through token-major tensor maps, with no transposition pass.
+ * B * N must fit in 32 bits. */
+fa_status fa_fwd_bnhd(const void* q, const void* k, const void* v, void* o, float* lse,
+                      int B, int N, int H, int Hkv, int d, float scale, int causal,
+                      fa_stream_t stream);
+
 /* --------------------------------------------------------------- backward */
 
 /* Scratch for fa_bwd / fa_bwd_ex, in bytes: the row statistics
@@ -325,6 +336,17 @@ fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const void*
                         const int* cu_seqlens, int batch, int total, int max_seqlen, int H,
                         int Hkv, int d, float scale, int causal, void* workspace,
                         size_t workspace_bytes, fa_stream_t stream);
+
+/* Backward of fa_fwd_bnhd, bf16: dq [B, N, H, d]; dk, dv [B, N, Hkv, d]
+ * (summed over the query heads sharing a key/value head); o, lse, dout as
+ * the forward wrote / read them.  Workspace:
+ * fa_bwd_bnhd_workspace_size(B, N, H, d) bytes (the statistics and the
+ * float32 dQ accumulator per (head, sequence), as for fa_bwd_varlen). */
+size_t fa_bwd_bnhd_workspace_size(int B, int N, int H, int d);
+fa_status fa_bwd_bnhd(const void* q, const void* k, const void* v, const void* o,
+                      const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                      int B, int N, int H, int Hkv, int d, float scale, int causal,
+                      void* workspace, size_t workspace_bytes, fa_stream_t stream);
 
 /* The three phases fa_bwd runs, callable one by one (bf16 tensors, same
  * workspace).  fa_bwd == fa_bwd_preprocess; fa_bwd_main; fa_bwd_dq.
