@@ -142,6 +142,12 @@ def test_host_validation_of_the_variant_entry_points():
     # window: an edge below -1, heads not a multiple of the key/value heads
     assert lib.fa_fwd_window(A, A, A, A, A, 1, 4, 4, 256, 128, 0.1, 0, -2, 5, None, None) == 1
     assert lib.fa_fwd_window(A, A, A, A, A, 1, 4, 3, 256, 128, 0.1, 0, 5, 5, None, None) == 1
+    # [B, N, H, d] layout: bad group, unsupported head dim, B * N beyond 32 bits, workspace too small
+    assert lib.fa_fwd_bnhd(A, A, A, A, A, 2, 256, 4, 3, 128, 0.1, 0, None) == 1
+    assert lib.fa_fwd_bnhd(A, A, A, A, A, 2, 256, 4, 4, 96, 0.1, 0, None) == 2
+    assert lib.fa_fwd_bnhd(A, A, A, A, A, 1 << 16, 1 << 16, 4, 4, 128, 0.1, 0, None) == 1
+    assert lib.fa_bwd_bnhd_workspace_size(2, 256, 4, 128) == lib.fa_bwd_varlen_workspace_size(2, 256, 4, 128) > 0
+    assert lib.fa_bwd_bnhd(A, A, A, A, A, A, A, A, A, 2, 256, 4, 4, 128, 0.1, 0, A, 1024, None) == 1
     # block-sparse: missing lists, workspace too small
     assert lib.fa_fwd_block_sparse(A, A, A, A, A, 1, 4, 4, 256, 128, 0.1, 0, None, A, None, None) == 1
     need = lib.fa_bwd_block_sparse_workspace_size(1, 4, 256, 128)
