@@ -79,6 +79,10 @@ _SIGS = {
     "fa_fwd_bnhd": ([_vp] * 5 + [_i, _i, _i, _i, _i, _f, _i, _vp], _i),
     "fa_bwd_bnhd_workspace_size": ([_i] * 4, _sz),
     "fa_bwd_bnhd": ([_vp] * 9 + [_i, _i, _i, _i, _i, _f, _i, _vp, _sz, _vp], _i),
+    "fa_bwd_varlen_deterministic_workspace_size": ([_i] * 5, _sz),
+    "fa_bwd_varlen_deterministic": ([_vp] * 10 + [_i, _i, _i, _i, _i, _i, _f, _i, _vp, _sz, _vp], _i),
+    "fa_bwd_bnhd_deterministic_workspace_size": ([_i] * 5, _sz),
+    "fa_bwd_bnhd_deterministic": ([_vp] * 9 + [_i, _i, _i, _i, _i, _f, _i, _vp, _sz, _vp], _i),
     "fa_bwd_gqa": ([_vp] * 9 + [_i, _i, _i, _i, _i, _f, _i, _vp, _vp, _sz, _vp], _i),
     "fa_fwd_split_workspace_size": ([_i] * 7, _sz),
     "fa_fwd_split_count": ([_i] * 7, _i),
@@ -414,27 +418,32 @@ def forward_bnhd(q, k, v, causal: bool = False, scale: Optional[float] = None,
 
 
 def backward_bnhd(q, k, v, o, lse, dout, causal: bool = False, scale: Optional[float] = None,
-                  workspace: Optional[torch.Tensor] = None):
+                  workspace: Optional[torch.Tensor] = None, deterministic: bool = False):
     """dQ [B,N,H,d], dK, dV [B,N,Hkv,d] of forward_bnhd (dK, dV summed over
-    the query heads sharing a key/value head)."""
+    the query heads sharing a key/value head).  deterministic: bitwise
+    reproducible gradients (see backward)."""
     lib = load_library()
     _need_cuda(q, k, v, o, lse, dout)
     B, N, H, Hkv, d = _bnhd_shapes(q, k, v)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    wsz = int(lib.fa_bwd_bnhd_workspace_size(B, N, H, d))
+    wsz = int(lib.fa_bwd_bnhd_deterministic_workspace_size(B, N, H, Hkv, d) if deterministic
+              else lib.fa_bwd_bnhd_workspace_size(B, N, H, d))
     ws = workspace
     if ws is None or ws.numel() * ws.element_size() < wsz:
         ws = torch.empty(wsz, dtype=torch.uint8, device=q.device)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    _check(lib.fa_bwd_bnhd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
-                           _ptr(dv), B, N, H, Hkv, d, scale, int(bool(causal)), _ptr(ws),
-                           ws.numel() * ws.element_size(), _stream(q)))
+    fn = lib.fa_bwd_bnhd_deterministic if deterministic else lib.fa_bwd_bnhd
+    _check(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
+              _ptr(dv), B, N, H, Hkv, d, scale, int(bool(causal)), _ptr(ws),
+              ws.numel() * ws.element_size(), _stream(q)))
     return dq, dk, dv
 
 
 def backward_varlen(q, k, v, o, lse, dout, cu_seqlens, max_seqlen: int, causal: bool = False,
-                    scale: Optional[float] = None, workspace: Optional[torch.Tensor] = None):
-    """Backward of forward_varlen: dQ [total, H, d], dK, dV [total, Hkv, d]."""
+                    scale: Optional[float] = None, workspace: Optional[torch.Tensor] = None,
+                    deterministic: bool = False):
+    """Backward of forward_varlen: dQ [total, H, d], dK, dV [total, Hkv, d].
+    deterministic: bitwise reproducible gradients (see backward)."""
     lib = load_library()
     _need_cuda(q, k, v, o, lse, dout)
     T, H, d = q.shape
@@ -442,14 +451,16 @@ def backward_varlen(q, k, v, o, lse, dout, cu_seqlens, max_seqlen: int, causal: 
     cu = _cu(cu_seqlens, q.device)
     batch = cu.numel() - 1
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    wsz = int(lib.fa_bwd_varlen_workspace_size(batch, int(max_seqlen), H, d))
+    wsz = int(lib.fa_bwd_varlen_deterministic_workspace_size(batch, int(max_seqlen), H, Hkv, d) if deterministic
+              else lib.fa_bwd_varlen_workspace_size(batch, int(max_seqlen), H, d))
     ws = workspace
     if ws is None or ws.numel() * ws.element_size() < wsz:
         ws = torch.empty(wsz, dtype=torch.uint8, device=q.device)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    _check(lib.fa_bwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
-                             _ptr(dv), _ptr(cu), batch, T, int(max_seqlen), H, Hkv, d, scale,
-                             int(bool(causal)), _ptr(ws), ws.numel() * ws.element_size(), _stream(q)))
+    fn = lib.fa_bwd_varlen_deterministic if deterministic else lib.fa_bwd_varlen
+    _check(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
+              _ptr(dv), _ptr(cu), batch, T, int(max_seqlen), H, Hkv, d, scale,
+              int(bool(causal)), _ptr(ws), ws.numel() * ws.element_size(), _stream(q)))
     return dq, dk, dv
 
 

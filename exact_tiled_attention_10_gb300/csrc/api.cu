@@ -1034,6 +1034,18 @@ size_t fa_bwd_varlen_workspace_size(int batch, int max_seqlen, int H, int d) {
     return 2 * round_up(R * 4, 256) + round_up(R * d * 4, 256);
 }
 
+size_t fa_bwd_varlen_deterministic_workspace_size(int batch, int max_seqlen, int H, int Hkv, int d) {
+    const size_t base = fa_bwd_varlen_workspace_size(batch, max_seqlen, H, d);
+    if (base == 0 || Hkv < 1 || H % Hkv != 0) return 0;
+    const int nacc = det_num_acc(batch, Hkv, max_seqlen);
+    return base + (size_t)(nacc - 1) * det_acc_bytes(batch, H, max_seqlen, d) +
+           det_turn_bytes(nacc, batch, H, max_seqlen, d);
+}
+
+size_t fa_bwd_bnhd_deterministic_workspace_size(int B, int N, int H, int Hkv, int d) {
+    return fa_bwd_varlen_deterministic_workspace_size(B, N, H, Hkv, d);
+}
+
 }  // extern "C"
 
 namespace {
@@ -1042,7 +1054,7 @@ namespace {
 fa_status bwd_packed_impl(const void* q, const void* k, const void* v, const void* o, const float* lse,
                           const void* dout, void* dq, void* dk, void* dv, const int* cu_seqlens, int batch, int total,
                           int max_seqlen, int H, int Hkv, int d, float scale, int causal, void* workspace,
-                          size_t workspace_bytes, fa_stream_t stream) {
+                          size_t workspace_bytes, fa_stream_t stream, bool det = false) {
     FA_TRY(check_common(batch, H, max_seqlen, d, scale));
     if (total <= 0) return fail(FA_ERR_INVALID_ARG, "total must be positive");
     if (Hkv < 1 || H % Hkv != 0) return fail(FA_ERR_INVALID_ARG, "H (%d) must be a multiple of Hkv (%d)", H, Hkv);
@@ -1056,7 +1068,9 @@ fa_status bwd_packed_impl(const void* q, const void* k, const void* v, const voi
     FA_CHECK_PTR(dk);
     FA_CHECK_PTR(dv);
     FA_CHECK_PTR(workspace);
-    const size_t need = fa_bwd_varlen_workspace_size(batch, max_seqlen, H, d);
+    const size_t base = fa_bwd_varlen_workspace_size(batch, max_seqlen, H, d);
+    const int nacc = det ? det_num_acc(batch, Hkv, max_seqlen) : 1;
+    const size_t need = det ? fa_bwd_varlen_deterministic_workspace_size(batch, max_seqlen, H, Hkv, d) : base;
     if (workspace_bytes < need) return fail(FA_ERR_INVALID_ARG, "workspace too small (%zu < %zu bytes)", workspace_bytes, need);
     DeviceInfo* dev = nullptr;
     FA_TRY(device_info(&dev));
@@ -1075,7 +1089,9 @@ fa_status bwd_packed_impl(const void* q, const void* k, const void* v, const voi
     FA_TRY(make_map_tok(&tdo, dout, d, H, total, BR));
     FA_TRY(make_map_tok(&tk, k, d, Hkv, total, 128));
     FA_TRY(make_map_tok(&tv, v, d, Hkv, total, 128));
-    FA_TRY(make_map_dqacc(&tdq, dqacc, d, (long long)R));
+    if ((long long)R * nacc >= (1LL << 31))
+        return fail(FA_ERR_UNSUPPORTED, "dQ accumulator rows exceed the 32-bit tensor coordinate range");
+    FA_TRY(make_map_dqacc(&tdq, dqacc, d, (long long)R * nacc));
     fa::BwdParams p;
     memset(&p, 0, sizeof(p));
     p.B = batch; p.H = H; p.N = max_seqlen; p.Np = MSp; p.Hkv = Hkv;
@@ -1091,6 +1107,25 @@ fa_status bwd_packed_impl(const void* q, const void* k, const void* v, const voi
     p.cu_seqlens = cu_seqlens;
     p.total = total;
     p.err = dev->err_word;
+    if (det) {
+        // accumulators 1 .. nacc-1 follow the first (the last region), then the turn counters
+        int* turn = reinterpret_cast<int*>(ws + base + (size_t)(nacc - 1) * R * d * sizeof(float));
+        fa::BwdParamsDet pd;
+        memset(&pd, 0, sizeof(pd));
+        static_cast<fa::BwdParams&>(pd) = p;
+        pd.nqb = MSp / (d == 128 ? 64 : 128);
+        pd.dq_turn = turn;
+        pd.nacc = nacc;
+        e = cudaMemsetAsync(turn, 0, det_turn_bytes(nacc, batch, H, max_seqlen, d), stream);
+        if (e == cudaSuccess)
+            e = fa::launch_bwd_main_det_varlen(d, causal != 0, tq, tk, tv, tdo, tdq, pd,
+                                               grid_for_items(p.num_items, dev->sms), stream);
+        if (e != cudaSuccess) return cuda_fail(e, "varlen deterministic backward launch");
+        e = fa::launch_bwd_dq_det_varlen(dqacc, turn, cu_seqlens, dq, scale, H, batch, max_seqlen, MSp, d, nacc,
+                                         bw_grid(dev), stream);
+        if (e != cudaSuccess) return cuda_fail(e, "varlen dQ conversion launch");
+        return FA_OK;
+    }
     e = fa::launch_bwd_main_varlen(d, causal != 0, tq, tk, tv, tdo, tdq, p, grid_for_items(p.num_items, dev->sms),
                                    stream);
     if (e != cudaSuccess) return cuda_fail(e, "varlen backward launch");
@@ -1113,6 +1148,24 @@ fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const void*
 }
 
 size_t fa_bwd_bnhd_workspace_size(int B, int N, int H, int d) { return fa_bwd_varlen_workspace_size(B, N, H, d); }
+
+fa_status fa_bwd_varlen_deterministic(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                                      const void* dout, void* dq, void* dk, void* dv, const int* cu_seqlens,
+                                      int batch, int total, int max_seqlen, int H, int Hkv, int d, float scale,
+                                      int causal, void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+    if (!cu_seqlens) return fail(FA_ERR_INVALID_ARG, "cu_seqlens must not be NULL");
+    return bwd_packed_impl(q, k, v, o, lse, dout, dq, dk, dv, cu_seqlens, batch, total, max_seqlen, H, Hkv, d, scale,
+                           causal, workspace, workspace_bytes, stream, true);
+}
+
+fa_status fa_bwd_bnhd_deterministic(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                                    const void* dout, void* dq, void* dk, void* dv, int B, int N, int H, int Hkv,
+                                    int d, float scale, int causal, void* workspace, size_t workspace_bytes,
+                                    fa_stream_t stream) {
+    if ((long long)B * N > INT_MAX) return fail(FA_ERR_INVALID_ARG, "B * N exceeds the 32-bit token index");
+    return bwd_packed_impl(q, k, v, o, lse, dout, dq, dk, dv, nullptr, B, B * N, N, H, Hkv, d, scale, causal,
+                           workspace, workspace_bytes, stream, true);
+}
 
 fa_status fa_bwd_bnhd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
                       void* dq, void* dk, void* dv, int B, int N, int H, int Hkv, int d, float scale, int causal,

@@ -224,6 +224,49 @@ __global__ void __launch_bounds__(256) bwd_pre_varlen_kernel(const __nv_bfloat16
     }
 }
 
+// Deterministic packed conversion: dQ[token, h, :] = scale * the sum, in order
+// a = 0, 1, ..., of the accumulators a whose turn count for the row's quarter
+// of its tile is nonzero; accumulator rows (h * batch + b) * MSp + pos.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_dq_det_varlen_kernel(const float* __restrict__ acc,
+                                                                const int* __restrict__ turn,
+                                                                const int* __restrict__ cu,
+                                                                __nv_bfloat16* __restrict__ dq, float scale, int H,
+                                                                int batch, int max_seqlen, int MSp, int nacc) {
+    constexpr int G = D / 8, BR = (D == 128) ? 64 : 128, kMaxAcc = 8;
+    const int nqb = MSp / BR;
+    const long total = (long)H * batch * MSp * G;
+    const size_t acc_elems = (size_t)H * batch * MSp * D, turn_stride = (size_t)H * batch * nqb * 4;
+    for (long g = (long)blockIdx.x * blockDim.x + threadIdx.x; g < total; g += (long)gridDim.x * blockDim.x) {
+        const long r = g / G;
+        const int c = (int)(g - r * G) * 8;
+        const long hb = r / MSp;
+        const int pos = (int)(r - hb * MSp);
+        const int h = (int)(hb / batch), b = (int)(hb - (long)h * batch);
+        if (pos >= varlen_len(cu, b, max_seqlen)) continue;
+        const long token = varlen_token(cu, b, max_seqlen, pos);
+        const int quarter = (D == 128) ? c / 32 : (pos % 128) / 32;
+        const size_t tix = ((size_t)hb * nqb + pos / BR) * 4 + quarter;
+        const size_t off = (size_t)r * D + c;
+        bool has[kMaxAcc];
+#pragma unroll
+        for (int a = 0; a < kMaxAcc; ++a) has[a] = a < nacc && __ldg(turn + a * turn_stride + tix) != 0;
+        float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int a = 0; a < kMaxAcc; ++a) {
+            if (has[a]) {
+                const float4* src = reinterpret_cast<const float4*>(acc + a * acc_elems + off);
+                const float4 x = __ldg(src), y = __ldg(src + 1);
+                s[0] += x.x; s[1] += x.y; s[2] += x.z; s[3] += x.w;
+                s[4] += y.x; s[5] += y.y; s[6] += y.z; s[7] += y.w;
+            }
+        }
+        *reinterpret_cast<uint4*>(dq + ((size_t)token * H + h) * D + c) =
+            make_uint4(pack_bf16x2(s[0] * scale, s[1] * scale), pack_bf16x2(s[2] * scale, s[3] * scale),
+                       pack_bf16x2(s[4] * scale, s[5] * scale), pack_bf16x2(s[6] * scale, s[7] * scale));
+    }
+}
+
 // dQ[token, h, :] = scale * dQ_acc[(h * batch + b) * MSp + pos, :] for the real rows.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_dq_varlen_kernel(const float* __restrict__ acc, const int* __restrict__ cu,
@@ -576,6 +619,19 @@ cudaError_t launch_bwd_pre(const void* o, const void* dout, bool in_f32, const f
         if (in_f32) bwd_pre_kernel<64, true><<<grid, 256, 0, s>>>(o, dout, lse, lse2, dvec, dq_acc, BH, N, Np);
         else bwd_pre_kernel<64, false><<<grid, 256, 0, s>>>(o, dout, lse, lse2, dvec, dq_acc, BH, N, Np);
     }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dq_det_varlen(const float* acc, const int* turn, const int* cu_seqlens, void* dq, float scale,
+                                     int H, int batch, int max_seqlen, int MSp, int d, int nacc, int grid,
+                                     cudaStream_t s) {
+    __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(dq);
+    if (d == 128)
+        bwd_dq_det_varlen_kernel<128><<<grid, 256, 0, s>>>(acc, turn, cu_seqlens, o, scale, H, batch, max_seqlen, MSp,
+                                                           nacc);
+    else
+        bwd_dq_det_varlen_kernel<64><<<grid, 256, 0, s>>>(acc, turn, cu_seqlens, o, scale, H, batch, max_seqlen, MSp,
+                                                          nacc);
     return cudaGetLastError();
 }
 

@@ -131,8 +131,9 @@ using ParamsT = typename std::conditional<
     typename std::conditional<SPARSE, BwdParamsSparse,
                               typename std::conditional<RECT, BwdParamsRect, BwdParams>::type>::type>::type;
 
-// DET: the deterministic instance (p is a BwdParamsDet; plain or shared heads
-// only): each drain warp adds its quarter of a dQ tile only on its turn.
+// DET: the deterministic instance (p is a BwdParamsDet; plain, shared heads or
+// packed sequences): each drain warp adds its quarter of a dQ tile only on its
+// turn.
 template <bool WINDOW, bool SPARSE, bool RECT, bool DET>
 using KernelParamsT = typename std::conditional<DET, BwdParamsDet, ParamsT<WINDOW, SPARSE, RECT>>::type;
 
@@ -321,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                const __grid_constant__ CUtensorMap tdq, const KernelParamsT<WINDOW, SPARSE, RECT, DET> p) {
-    static_assert(!DET || (!VARLEN && !WINDOW && !SPARSE && !RECT), "deterministic: plain or shared heads only");
+    static_assert(!DET || (!WINDOW && !SPARSE && !RECT), "deterministic: plain, shared heads or packed only");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -738,7 +739,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // kt - nacc, kt - 2 nacc, ..., 0 (every key block below kt visits
                     // the query blocks kt visits); the first of them stores
                     const int a = I.kt % p.nacc;
-                    int* turn = p.dq_turn + (((size_t)a * (p.B * p.H) + bhq) * p.nqb + i) * 4 + wq;
+                    const int srow = VARLEN ? bhq * p.B + I.b : bhq;  // statistics row group of the tile
+                    int* turn = p.dq_turn + (((size_t)a * (p.B * p.H) + srow) * p.nqb + i) * 4 + wq;
                     if (!(ok = wait_turn_warp(turn, I.kt / p.nacc, abort_flag, p.err, kErrWaitBwdDqTurn))) break;
                     pend[0] = turn;
                     row += a * (p.B * p.H * p.Np);

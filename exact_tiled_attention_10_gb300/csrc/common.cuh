@@ -202,6 +202,13 @@ cudaError_t launch_bwd_main_rect(int d, bool causal, const CUtensorMap& tq, cons
 // and its dQ conversion: dq = scale * the sum of the written accumulators.
 cudaError_t launch_bwd_dq_det(const float* acc, const int* turn, void* dq, float scale, int BH, int N, int Np, int d,
                               int nacc, int grid, cudaStream_t stream);
+cudaError_t launch_bwd_main_det_varlen(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
+                                       const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
+                                       const BwdParamsDet& p, int grid, cudaStream_t stream);
+// Packed layout ([H][batch][MSp] accumulator rows, token-major dq):
+cudaError_t launch_bwd_dq_det_varlen(const float* acc, const int* turn, const int* cu_seqlens, void* dq, float scale,
+                                     int H, int batch, int max_seqlen, int MSp, int d, int nacc, int grid,
+                                     cudaStream_t stream);
 cudaError_t launch_bwd_main_det(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                 const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParamsDet& p, int grid,
                                 cudaStream_t stream);

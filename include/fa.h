@@ -348,6 +348,29 @@ fa_status fa_bwd_bnhd(const void* q, const void* k, const void* v, const void* o
                       int B, int N, int H, int Hkv, int d, float scale, int causal,
                       void* workspace, size_t workspace_bytes, fa_stream_t stream);
 
+/* Deterministic versions of fa_bwd_varlen and fa_bwd_bnhd (the
+ * `deterministic` flag of flash_attn_varlen_func / flash_attn_func,
+ * [CH18] §18.7.1): same arguments and results, with dq, dk and dv bitwise
+ * identical from run to run.  The fixed order, the A float32 accumulators
+ * and the turn counters are those of fa_bwd_deterministic, per (head,
+ * sequence) row group; A comes from (batch, Hkv, max_seqlen).  Workspace: the
+ * *_deterministic_workspace_size bytes (the packed layout, A - 1 more
+ * accumulators, the counters).  The same residency note as
+ * fa_bwd_deterministic applies: do not overlap two of these calls on one
+ * device. */
+size_t fa_bwd_varlen_deterministic_workspace_size(int batch, int max_seqlen, int H, int Hkv, int d);
+fa_status fa_bwd_varlen_deterministic(const void* q, const void* k, const void* v, const void* o,
+                                      const float* lse, const void* dout, void* dq, void* dk,
+                                      void* dv, const int* cu_seqlens, int batch, int total,
+                                      int max_seqlen, int H, int Hkv, int d, float scale,
+                                      int causal, void* workspace, size_t workspace_bytes,
+                                      fa_stream_t stream);
+size_t fa_bwd_bnhd_deterministic_workspace_size(int B, int N, int H, int Hkv, int d);
+fa_status fa_bwd_bnhd_deterministic(const void* q, const void* k, const void* v, const void* o,
+                                    const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                                    int B, int N, int H, int Hkv, int d, float scale, int causal,
+                                    void* workspace, size_t workspace_bytes, fa_stream_t stream);
+
 /* The three phases fa_bwd runs, callable one by one (bf16 tensors, same
  * workspace).  fa_bwd == fa_bwd_preprocess; fa_bwd_main; fa_bwd_dq.
  *   fa_bwd_preprocess: D = rowsum(dout * o) ([FA2] §5.2), LSE * log2(e) and

@@ -10,7 +10,8 @@ import pytest
 import torch
 
 import oracle
-from exact_tiled_attention_10_gb300 import backward, check_device_status, forward, load_library
+from exact_tiled_attention_10_gb300 import (backward, backward_bnhd, backward_varlen, check_device_status, forward,
+                                           forward_bnhd, forward_varlen, load_library)
 from exact_tiled_attention_10_gb300.inputs import qkv, randn
 from parity_util import assert_grad, to64
 
@@ -100,3 +101,46 @@ def test_full_size_repeat_bitwise():
     check_device_status()
     for x, y in zip(a, b):
         assert torch.equal(x, y)
+
+
+def test_packed_sequences_repeat_bitwise():
+    """Packed sequences (lengths 1000, 0, 513, 2048, 77; shared heads): three
+    deterministic runs on 0xFF-filled workspaces agree bitwise."""
+    lens = [1000, 0, 513, 2048, 77]
+    T, H, Hkv, d = sum(lens), 8, 2, 128
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32, device=DEV)
+    q, do = (randn((T, H, d), 101 + i, device=DEV) for i in range(2))
+    k, v = (randn((T, Hkv, d), 103 + i, device=DEV) for i in range(2))
+    o, lse = forward_varlen(q, k, v, cu, max(lens), causal=True)
+    first = backward_varlen(q, k, v, o, lse, do, cu, max(lens), causal=True, deterministic=True)
+    wsz = int(load_library().fa_bwd_varlen_deterministic_workspace_size(len(lens), max(lens), H, Hkv, d))
+    for rep in range(3):
+        ws = torch.full((wsz,), 0xFF, dtype=torch.uint8, device=DEV)
+        again = backward_varlen(q, k, v, o, lse, do, cu, max(lens), causal=True, deterministic=True, workspace=ws)
+        torch.cuda.synchronize()
+        for a, b in zip(first, again):
+            assert torch.equal(a, b), "repeat %d" % rep
+    check_device_status()
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bnhd_deterministic_matches_oracle_and_repeats(causal):
+    """flash_attn_func's layout [B, N, H, d] with deterministic=True: parity
+    with the oracle on the transposed tensors, and bitwise repeats."""
+    B, N, H, Hkv, d = 2, 700, 4, 2, 128
+    q, do = (randn((B, N, H, d), 111 + i, device=DEV) for i in range(2))
+    k, v = (randn((B, N, Hkv, d), 113 + i, device=DEV) for i in range(2))
+    o, lse = forward_bnhd(q, k, v, causal=causal)
+    g1 = backward_bnhd(q, k, v, o, lse, do, causal=causal, deterministic=True)
+    g2 = backward_bnhd(q, k, v, o, lse, do, causal=causal, deterministic=True)
+    torch.cuda.synchronize()
+    check_device_status()
+    for a, b in zip(g1, g2):
+        assert torch.equal(a, b)
+    t = lambda x: np.ascontiguousarray(np.transpose(to64(x), (0, 2, 1, 3)))
+    g = H // Hkv
+    r = oracle.bwd(t(q), np.repeat(t(k), g, axis=1), np.repeat(t(v), g, axis=1), t(do), 1.0 / math.sqrt(d),
+                   causal=causal)
+    assert_grad(t(g1[0]), r["dq"], "dQ")
+    assert_grad(t(g1[1]), r["dk"].reshape(B, Hkv, g, N, d).sum(axis=2), "dK")
+    assert_grad(t(g1[2]), r["dv"].reshape(B, Hkv, g, N, d).sum(axis=2), "dV")

@@ -127,6 +127,8 @@ def test_varlen_with_an_empty_sequence(monkeypatch):
     q, k, v, do = (randn((T, 4, 128), 25 + i, device=DEV) for i in range(4))
     o, lse = _run_both(monkeypatch, lambda: fa.forward_varlen(q, k, v, cu, max(lens), causal=True))
     _run_both(monkeypatch, lambda: fa.backward_varlen(q, k, v, o, lse, do, cu, max(lens), causal=True)[1:])
+    _run_both(monkeypatch,
+              lambda: fa.backward_varlen(q, k, v, o, lse, do, cu, max(lens), causal=True, deterministic=True))
 
 
 def test_bnhd(monkeypatch):

@@ -21,7 +21,7 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-def _case(lens, H, Hkv, d, causal, seed):
+def _case(lens, H, Hkv, d, causal, seed, deterministic=False):
     T = int(sum(lens))
     cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32, device=DEV)
     q = randn((T, H, d), seed, device=DEV)
@@ -30,7 +30,8 @@ def _case(lens, H, Hkv, d, causal, seed):
     do = randn((T, H, d), seed + 3, device=DEV)
     scale = 1.0 / math.sqrt(d)
     o, lse = forward_varlen(q, k, v, cu, max(lens), causal=causal, scale=scale)
-    dq, dk, dv = backward_varlen(q, k, v, o, lse, do, cu, max(lens), causal=causal, scale=scale)
+    dq, dk, dv = backward_varlen(q, k, v, o, lse, do, cu, max(lens), causal=causal, scale=scale,
+                                 deterministic=deterministic)
     torch.cuda.synchronize()
     check_device_status()
     g = H // Hkv
@@ -69,3 +70,11 @@ def test_varlen_with_shared_kv_heads(causal):
 
 def test_varlen_single_sequence():
     _case([777], 2, 1, 64, True, seed=79)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_deterministic_matches_oracle(d, causal):
+    """The deterministic backward of packed sequences (flash_attn_varlen_func's
+    deterministic flag) against the same per-sequence oracle."""
+    _case([300, 1, 0, 129, 520, 64], 4, 2, d, causal, seed=91 + d, deterministic=True)
