@@ -83,6 +83,9 @@ _SIGS = {
     "fa_bwd_varlen_deterministic": ([_vp] * 10 + [_i, _i, _i, _i, _i, _i, _f, _i, _vp, _sz, _vp], _i),
     "fa_bwd_bnhd_deterministic_workspace_size": ([_i] * 5, _sz),
     "fa_bwd_bnhd_deterministic": ([_vp] * 9 + [_i, _i, _i, _i, _i, _f, _i, _vp, _sz, _vp], _i),
+    "fa_bwd_window_deterministic": ([_vp] * 9 + [_i, _i, _i, _i, _i, _f, _i, _i, _i, _vp, _vp, _sz, _vp], _i),
+    "fa_bwd_rect_deterministic_workspace_size": ([_i] * 6, _sz),
+    "fa_bwd_rect_deterministic": ([_vp] * 9 + [_i] * 6 + [_f, _i, _vp, _vp, _sz, _vp], _i),
     "fa_bwd_gqa": ([_vp] * 9 + [_i, _i, _i, _i, _i, _f, _i, _vp, _vp, _sz, _vp], _i),
     "fa_fwd_split_workspace_size": ([_i] * 7, _sz),
     "fa_fwd_split_count": ([_i] * 7, _i),
@@ -345,22 +348,25 @@ def forward_rect(q, k, v, causal: bool = False, scale: Optional[float] = None, k
 
 
 def backward_rect(q, k, v, o, lse, dout, causal: bool = False, scale: Optional[float] = None, kv_lens=None,
-                  workspace: Optional[torch.Tensor] = None):
-    """Backward of forward_rect: dQ [B,H,Nq,d], dK, dV [B,Hkv,Nk,d]."""
+                  workspace: Optional[torch.Tensor] = None, deterministic: bool = False):
+    """Backward of forward_rect: dQ [B,H,Nq,d], dK, dV [B,Hkv,Nk,d].
+    deterministic: bitwise reproducible gradients (see backward)."""
     lib = load_library()
     _need_cuda(q, k, v, o, lse, dout)
     B, H, Nq, d = q.shape
     Hkv, Nk = k.shape[1], k.shape[2]
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     kv = _kv(kv_lens, B, q.device)
-    wsz = int(lib.fa_bwd_rect_workspace_size(B, H, Hkv, Nq, Nk, d))
+    wsz = int(lib.fa_bwd_rect_deterministic_workspace_size(B, H, Hkv, Nq, Nk, d) if deterministic
+              else lib.fa_bwd_rect_workspace_size(B, H, Hkv, Nq, Nk, d))
     ws = workspace
     if ws is None or ws.numel() * ws.element_size() < wsz:
         ws = torch.empty(wsz, dtype=torch.uint8, device=q.device)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    _check(lib.fa_bwd_rect(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
-                           B, H, Hkv, Nq, Nk, d, scale, int(bool(causal)), _ptr(kv), _ptr(ws),
-                           ws.numel() * ws.element_size(), _stream(q)))
+    fn = lib.fa_bwd_rect_deterministic if deterministic else lib.fa_bwd_rect
+    _check(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
+              B, H, Hkv, Nq, Nk, d, scale, int(bool(causal)), _ptr(kv), _ptr(ws),
+              ws.numel() * ws.element_size(), _stream(q)))
     return dq, dk, dv
 
 
@@ -484,8 +490,8 @@ def backward(q, k, v, o, lse, dout, causal: bool = False, scale: Optional[float]
     wl, wr = _window(window)
     grouped = Hkv != H or wl >= 0 or wr >= 0
     if deterministic:
-        if dt != FA_BF16 or wl >= 0 or wr >= 0 or H % Hkv != 0:
-            raise ValueError("the deterministic backward takes bfloat16 tensors, no window, H a multiple of Hkv")
+        if dt != FA_BF16 or H % Hkv != 0:
+            raise ValueError("the deterministic backward takes bfloat16 tensors and H a multiple of Hkv")
         wsz = int(lib.fa_bwd_deterministic_workspace_size(B, H, Hkv, N, d))
     else:
         wsz = int(lib.fa_bwd_gqa_workspace_size(B, H, Hkv, N, d) if grouped and dt == FA_BF16
@@ -497,6 +503,11 @@ def backward(q, k, v, o, lse, dout, causal: bool = False, scale: Optional[float]
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     _need_cuda(dq, dk, dv)
+    if deterministic and (wl >= 0 or wr >= 0):
+        _check(lib.fa_bwd_window_deterministic(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
+                                               _ptr(dk), _ptr(dv), B, H, Hkv, N, d, scale, int(bool(causal)), wl, wr,
+                                               _ptr(kv), _ptr(ws), ws.numel() * ws.element_size(), _stream(q)))
+        return dq, dk, dv
     if deterministic:
         _check(lib.fa_bwd_deterministic(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
                                         _ptr(dk), _ptr(dv), B, H, Hkv, N, d, scale, int(bool(causal)), _ptr(kv),

@@ -777,14 +777,37 @@ fa_status bwd_main_impl(const BwdCtx& c, bool f32, const void* qb, const void* k
     cudaError_t e;
     if (dq_turn) {
         // deterministic: zeroed turn counters, one per quarter of a dQ tile
-        fa::BwdParamsDet pd;
-        memset(&pd, 0, sizeof(pd));
-        static_cast<fa::BwdParams&>(pd) = p;
-        pd.nqb = Np / BR;
-        pd.dq_turn = dq_turn;
-        pd.nacc = nacc;
+        auto set_det = [&](auto& pd) {
+            pd.nqb = Np / BR;
+            pd.dq_turn = dq_turn;
+            pd.nacc = nacc;
+        };
         e = cudaMemsetAsync(dq_turn, 0, det_turn_bytes(nacc, B, H, N, d), stream);
-        if (e == cudaSuccess) e = fa::launch_bwd_main_det(d, causal != 0, tq, tk, tv, tdo, tdq, pd, grid, stream);
+        if (e == cudaSuccess) {
+            if (rect) {
+                fa::BwdDet<fa::BwdParamsRect> pd;
+                memset(&pd, 0, sizeof(pd));
+                static_cast<fa::BwdParams&>(pd) = p;
+                pd.Nk = Nk;
+                pd.coff = Nk - N;
+                set_det(pd);
+                e = fa::launch_bwd_main_det_rect(d, causal != 0, tq, tk, tv, tdo, tdq, pd, grid, stream);
+            } else if (win_left >= 0 || win_right >= 0) {
+                fa::BwdDet<fa::BwdParamsWin> pd;
+                memset(&pd, 0, sizeof(pd));
+                static_cast<fa::BwdParams&>(pd) = p;
+                pd.win_left = win_left;
+                pd.win_right = causal ? 0 : win_right;
+                set_det(pd);
+                e = fa::launch_bwd_main_det_window(d, tq, tk, tv, tdo, tdq, pd, grid, stream);
+            } else {
+                fa::BwdParamsDet pd;
+                memset(&pd, 0, sizeof(pd));
+                static_cast<fa::BwdParams&>(pd) = p;
+                set_det(pd);
+                e = fa::launch_bwd_main_det(d, causal != 0, tq, tk, tv, tdo, tdq, pd, grid, stream);
+            }
+        }
     } else if (rect) {
         fa::BwdParamsRect pr;
         memset(&pr, 0, sizeof(pr));
@@ -1182,18 +1205,26 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                      workspace_bytes, stream);
 }
 
-size_t fa_bwd_deterministic_workspace_size(int B, int H, int Hkv, int N, int d) {
-    const size_t base = fa_bwd_workspace_size(FA_BF16, B, H, N, d);
-    if (base == 0 || Hkv < 1 || H % Hkv != 0) return 0;
-    const int nacc = det_num_acc(B, Hkv, N);
-    // accumulators 1 .. nacc-1 follow the first (the last region of the base layout)
-    return base + (size_t)(nacc - 1) * det_acc_bytes(B, H, N, d) + det_turn_bytes(nacc, B, H, N, d);
+}  // extern "C"
+
+namespace {
+
+// Workspace of the deterministic backward: the backward's own layout (Nq query
+// rows), A - 1 more float32 dQ accumulators, the turn counters; A from the
+// key blocks (Nk keys).
+size_t det_workspace(int B, int H, int Hkv, int Nq, int Nk, int d) {
+    const size_t base = fa_bwd_workspace_size(FA_BF16, B, H, Nq, d);
+    if (base == 0 || Nk <= 0 || Hkv < 1 || H % Hkv != 0) return 0;
+    const int nacc = det_num_acc(B, Hkv, Nk);
+    return base + (size_t)(nacc - 1) * det_acc_bytes(B, H, Nq, d) + det_turn_bytes(nacc, B, H, Nq, d);
 }
 
-fa_status fa_bwd_deterministic(const void* q, const void* k, const void* v, const void* o, const float* lse,
-                               const void* dout, void* dq, void* dk, void* dv, int B, int H, int Hkv, int N, int d,
-                               float scale, int causal, const int* kv_lens, void* workspace, size_t workspace_bytes,
-                               fa_stream_t stream) {
+// Deterministic backward, square (Nk < 0), sliding window (an edge >= 0) or
+// rectangular (Nk >= 0).
+fa_status bwd_det_impl(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                       void* dq, void* dk, void* dv, int B, int H, int Hkv, int Nq, int Nk, int d, float scale,
+                       int causal, int win_left, int win_right, const int* kv_lens, void* workspace,
+                       size_t workspace_bytes, fa_stream_t stream) {
     FA_CHECK_PTR(q);
     FA_CHECK_PTR(k);
     FA_CHECK_PTR(v);
@@ -1204,22 +1235,65 @@ fa_status fa_bwd_deterministic(const void* q, const void* k, const void* v, cons
     FA_CHECK_PTR(dk);
     FA_CHECK_PTR(dv);
     if (Hkv < 1 || H % Hkv != 0) return fail(FA_ERR_INVALID_ARG, "H (%d) must be a multiple of Hkv (%d)", H, Hkv);
+    if (win_left < -1 || win_right < -1) return fail(FA_ERR_INVALID_ARG, "window edges must be >= -1");
+    const bool rect = Nk >= 0;
+    if (rect && Nk == 0) return fail(FA_ERR_INVALID_ARG, "Nk must be positive");
+    const int nk = rect ? Nk : Nq;
     BwdCtx c{};
-    FA_TRY(bwd_setup(FA_BF16, B, H, N, d, scale, workspace, workspace_bytes, &c));
-    const size_t need = fa_bwd_deterministic_workspace_size(B, H, Hkv, N, d);
+    FA_TRY(bwd_setup(FA_BF16, B, H, Nq, d, scale, workspace, workspace_bytes, &c));
+    const size_t need = det_workspace(B, H, Hkv, Nq, nk, d);
     if (workspace_bytes < need)
         return fail(FA_ERR_INVALID_ARG, "workspace too small (%zu < %zu bytes)", workspace_bytes, need);
-    const int nacc = det_num_acc(B, Hkv, N);
-    if (c.L.dqacc + det_acc_bytes(B, H, N, d) != c.L.total)
+    const int nacc = det_num_acc(B, Hkv, nk);
+    if (c.L.dqacc + det_acc_bytes(B, H, Nq, d) != c.L.total)
         return fail(FA_ERR_INVALID_ARG, "internal: the dQ accumulator is not the last workspace region");
-    int* turn = reinterpret_cast<int*>(c.ws + c.L.total + (size_t)(nacc - 1) * det_acc_bytes(B, H, N, d));
-    FA_TRY(bwd_pre_impl(c, false, o, lse, dout, N, d, stream));
-    FA_TRY(bwd_main_impl(c, false, q, k, v, dout, dk, dv, B, H, N, d, scale, causal, kv_lens, stream, Hkv, -1, -1,
-                         nullptr, nullptr, nullptr, 0, -1, turn, nacc));
-    cudaError_t e = fa::launch_bwd_dq_det(reinterpret_cast<float*>(c.ws + c.L.dqacc), turn, dq, scale, c.BH, N, c.Np,
-                                          d, nacc, bw_grid(c.dev), stream);
+    int* turn = reinterpret_cast<int*>(c.ws + c.L.total + (size_t)(nacc - 1) * det_acc_bytes(B, H, Nq, d));
+    FA_TRY(bwd_pre_impl(c, false, o, lse, dout, Nq, d, stream));
+    FA_TRY(bwd_main_impl(c, false, q, k, v, dout, dk, dv, B, H, Nq, d, scale, causal, kv_lens, stream, Hkv, win_left,
+                         win_right, nullptr, nullptr, nullptr, 0, Nk, turn, nacc));
+    cudaError_t e = fa::launch_bwd_dq_det(reinterpret_cast<float*>(c.ws + c.L.dqacc), turn, dq, scale, c.BH, Nq,
+                                          c.Np, d, nacc, bw_grid(c.dev), stream);
     if (e != cudaSuccess) return cuda_fail(e, "dQ conversion launch");
     return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t fa_bwd_deterministic_workspace_size(int B, int H, int Hkv, int N, int d) {
+    return det_workspace(B, H, Hkv, N, N, d);
+}
+
+fa_status fa_bwd_deterministic(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                               const void* dout, void* dq, void* dk, void* dv, int B, int H, int Hkv, int N, int d,
+                               float scale, int causal, const int* kv_lens, void* workspace, size_t workspace_bytes,
+                               fa_stream_t stream) {
+    return bwd_det_impl(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, N, -1, d, scale, causal, -1, -1, kv_lens,
+                        workspace, workspace_bytes, stream);
+}
+
+fa_status fa_bwd_window_deterministic(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                                      const void* dout, void* dq, void* dk, void* dv, int B, int H, int Hkv, int N,
+                                      int d, float scale, int causal, int window_left, int window_right,
+                                      const int* kv_lens, void* workspace, size_t workspace_bytes,
+                                      fa_stream_t stream) {
+    // as fa_bwd_window: the causal mask is folded into the window's right edge
+    return bwd_det_impl(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, N, -1, d, scale, causal, window_left,
+                        window_right, kv_lens, workspace, workspace_bytes, stream);
+}
+
+size_t fa_bwd_rect_deterministic_workspace_size(int B, int H, int Hkv, int Nq, int Nk, int d) {
+    return det_workspace(B, H, Hkv, Nq, Nk, d);
+}
+
+fa_status fa_bwd_rect_deterministic(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                                    const void* dout, void* dq, void* dk, void* dv, int B, int H, int Hkv, int Nq,
+                                    int Nk, int d, float scale, int causal, const int* kv_lens, void* workspace,
+                                    size_t workspace_bytes, fa_stream_t stream) {
+    if (Nk <= 0) return fail(FA_ERR_INVALID_ARG, "Nk must be positive");
+    return bwd_det_impl(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, Nq, Nk, d, scale, causal, -1, -1, kv_lens,
+                        workspace, workspace_bytes, stream);
 }
 
 int fa_fp8_num_blocks(int N) { return N > 0 ? (N + 63) / 64 : 0; }

@@ -131,21 +131,21 @@ using ParamsT = typename std::conditional<
     typename std::conditional<SPARSE, BwdParamsSparse,
                               typename std::conditional<RECT, BwdParamsRect, BwdParams>::type>::type>::type;
 
-// DET: the deterministic instance (p is a BwdParamsDet; plain, shared heads or
-// packed sequences): each drain warp adds its quarter of a dQ tile only on its
-// turn.
+// DET: the deterministic instance (p is a BwdDet<...>; all but block-sparse):
+// each drain warp adds its quarter of a dQ tile only on its turn.
 template <bool WINDOW, bool SPARSE, bool RECT, bool DET>
-using KernelParamsT = typename std::conditional<DET, BwdParamsDet, ParamsT<WINDOW, SPARSE, RECT>>::type;
+using KernelParamsT =
+    typename std::conditional<DET, BwdDet<ParamsT<WINDOW, SPARSE, RECT>>, ParamsT<WINDOW, SPARSE, RECT>>::type;
 
 // Keys of a head (K, V, dK, dV rows) and the causal offset.
 template <class PT>
 __device__ __forceinline__ int key_count(const PT& p) {
-    if constexpr (std::is_same<PT, BwdParamsRect>::value) return p.Nk;
+    if constexpr (std::is_base_of<BwdParamsRect, PT>::value) return p.Nk;
     else return p.N;
 }
 template <class PT>
 __device__ __forceinline__ int causal_offset(const PT& p) {
-    if constexpr (std::is_same<PT, BwdParamsRect>::value) return p.coff;
+    if constexpr (std::is_base_of<BwdParamsRect, PT>::value) return p.coff;
     else return 0;
 }
 
@@ -322,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                const __grid_constant__ CUtensorMap tdq, const KernelParamsT<WINDOW, SPARSE, RECT, DET> p) {
-    static_assert(!DET || (!WINDOW && !SPARSE && !RECT), "deterministic: plain, shared heads or packed only");
+    static_assert(!DET || !SPARSE, "deterministic: no block-sparse instance");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -736,15 +736,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bool first = false;
                 if constexpr (DET) {
                     // key block kt writes accumulator kt % nacc after the key blocks
-                    // kt - nacc, kt - 2 nacc, ..., 0 (every key block below kt visits
-                    // the query blocks kt visits); the first of them stores
+                    // kt - nacc, kt - 2 nacc, ..., lo that also visit query block i
+                    // (they form the range lo .. kt: i0 and the window's end grow with
+                    // the key block); the first of them stores
+                    int lo = 0;
+                    if constexpr (WINDOW)  // first key block whose window reaches query block i
+                        if (p.win_left >= 0) lo = max(0, i * C::BR - p.win_left) / C::BC;
                     const int a = I.kt % p.nacc;
+                    const int first_a = lo + ((a - lo % p.nacc) + p.nacc) % p.nacc;
                     const int srow = VARLEN ? bhq * p.B + I.b : bhq;  // statistics row group of the tile
                     int* turn = p.dq_turn + (((size_t)a * (p.B * p.H) + srow) * p.nqb + i) * 4 + wq;
-                    if (!(ok = wait_turn_warp(turn, I.kt / p.nacc, abort_flag, p.err, kErrWaitBwdDqTurn))) break;
+                    if (!(ok = wait_turn_warp(turn, (I.kt - first_a) / p.nacc, abort_flag, p.err, kErrWaitBwdDqTurn)))
+                        break;
                     pend[0] = turn;
                     row += a * (p.B * p.H * p.Np);
-                    first = I.kt < p.nacc;
+                    first = I.kt == first_a;
                 }
                 if (lane == 0) {
                     if constexpr (DET) fence_proxy_async_global();

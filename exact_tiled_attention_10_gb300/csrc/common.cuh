@@ -161,14 +161,19 @@ struct BwdParamsSparse : BwdParams {
 // dq_turn[((a * B*H + bhq) * nqb + i) * 4 + w] (nqb = Np / query rows per
 // step; w = the drain warp's quarter of the tile) counts the contributions to
 // quarter w of that tile of accumulator a; key block kt writes once it reaches
-// kt / nacc.  The conversion sums the accumulators with a nonzero count in
-// order a = 0, 1, ...  Key blocks that run at the same time go to different
-// accumulators, so they seldom wait for one another.
-struct BwdParamsDet : BwdParams {
+// its rank among the key blocks visiting that query block in accumulator a
+// (key blocks first(i), first(i) + 1, ... visit query block i: first(i) = 0
+// except under a sliding window).  The conversion sums the accumulators with
+// a nonzero count in order a = 0, 1, ...  Key blocks that run at the same time
+// go to different accumulators, so they seldom wait for one another.  BwdDet
+// adds these fields to any of the backward parameter blocks.
+template <class Base>
+struct BwdDet : Base {
     int* dq_turn;
     int nqb;
     int nacc;
 };
+using BwdParamsDet = BwdDet<BwdParams>;
 
 // Launch helpers implemented in the kernel translation units.  They return a
 // cudaError_t from the launch itself.
@@ -202,6 +207,12 @@ cudaError_t launch_bwd_main_rect(int d, bool causal, const CUtensorMap& tq, cons
 // and its dQ conversion: dq = scale * the sum of the written accumulators.
 cudaError_t launch_bwd_dq_det(const float* acc, const int* turn, void* dq, float scale, int BH, int N, int Np, int d,
                               int nacc, int grid, cudaStream_t stream);
+cudaError_t launch_bwd_main_det_window(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                       const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdDet<BwdParamsWin>& p,
+                                       int grid, cudaStream_t stream);
+cudaError_t launch_bwd_main_det_rect(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
+                                     const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
+                                     const BwdDet<BwdParamsRect>& p, int grid, cudaStream_t stream);
 cudaError_t launch_bwd_main_det_varlen(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
                                        const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
                                        const BwdParamsDet& p, int grid, cudaStream_t stream);

@@ -371,6 +371,25 @@ fa_status fa_bwd_bnhd_deterministic(const void* q, const void* k, const void* v,
                                     int B, int N, int H, int Hkv, int d, float scale, int causal,
                                     void* workspace, size_t workspace_bytes, fa_stream_t stream);
 
+/* Deterministic versions of fa_bwd_window and fa_bwd_rect (same arguments
+ * and results).  Under a sliding window, the key blocks that visit a query
+ * block form a range that may start above 0; a key block's turn is its rank
+ * within that range.  Workspace: fa_bwd_deterministic_workspace_size(B, H,
+ * Hkv, N, d) for the window, fa_bwd_rect_deterministic_workspace_size(...)
+ * for Nq x Nk.  The block-sparse backward has no deterministic form. */
+fa_status fa_bwd_window_deterministic(const void* q, const void* k, const void* v, const void* o,
+                                      const float* lse, const void* dout, void* dq, void* dk,
+                                      void* dv, int B, int H, int Hkv, int N, int d, float scale,
+                                      int causal, int window_left, int window_right,
+                                      const int* kv_lens, void* workspace, size_t workspace_bytes,
+                                      fa_stream_t stream);
+size_t fa_bwd_rect_deterministic_workspace_size(int B, int H, int Hkv, int Nq, int Nk, int d);
+fa_status fa_bwd_rect_deterministic(const void* q, const void* k, const void* v, const void* o,
+                                    const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                                    int B, int H, int Hkv, int Nq, int Nk, int d, float scale,
+                                    int causal, const int* kv_lens, void* workspace,
+                                    size_t workspace_bytes, fa_stream_t stream);
+
 /* The three phases fa_bwd runs, callable one by one (bf16 tensors, same
  * workspace).  fa_bwd == fa_bwd_preprocess; fa_bwd_main; fa_bwd_dq.
  *   fa_bwd_preprocess: D = rowsum(dout * o) ([FA2] §5.2), LSE * log2(e) and

@@ -88,7 +88,7 @@ def test_decode_128k_cache_sampled_heads():
         assert_lse(to64(lse[:, h:h + 1]), rl)
 
 
-def _bwd_case(B, H, Hkv, Nq, Nk, d, causal, kv=None, seed=41):
+def _bwd_case(B, H, Hkv, Nq, Nk, d, causal, kv=None, seed=41, deterministic=False):
     from exact_tiled_attention_10_gb300 import backward_rect
     from parity_util import assert_grad
     q = randn((B, H, Nq, d), seed, device=DEV)
@@ -98,9 +98,15 @@ def _bwd_case(B, H, Hkv, Nq, Nk, d, causal, kv=None, seed=41):
     kvd = None if kv is None else torch.tensor(kv, dtype=torch.int32, device=DEV)
     scale = 1.0 / math.sqrt(d)
     o, lse = forward_rect(q, k, v, causal=causal, scale=scale, kv_lens=kvd)
-    dq, dk, dv = backward_rect(q, k, v, o, lse, do, causal=causal, scale=scale, kv_lens=kvd)
+    dq, dk, dv = backward_rect(q, k, v, o, lse, do, causal=causal, scale=scale, kv_lens=kvd,
+                               deterministic=deterministic)
     torch.cuda.synchronize()
     check_device_status()
+    if deterministic:  # a second run agrees bit for bit
+        again = backward_rect(q, k, v, o, lse, do, causal=causal, scale=scale, kv_lens=kvd, deterministic=True)
+        torch.cuda.synchronize()
+        for a, b in zip((dq, dk, dv), again):
+            assert torch.equal(a, b)
     g = H // Hkv
     kvn = None if kv is None else np.asarray(kv, dtype=np.int32)
     r = oracle.bwd_rect(to64(q), np.repeat(to64(k), g, axis=1), np.repeat(to64(v), g, axis=1), to64(do), scale,
@@ -119,3 +125,10 @@ def test_rect_backward_matches_oracle(d, causal, Nq, Nk):
 
 def test_rect_backward_with_cache_lengths_and_mqa():
     _bwd_case(3, 4, 1, 130, 390, 128, True, kv=[0, 100, 390], seed=53)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Nq,Nk", [(200, 1700), (900, 300)])
+def test_rect_backward_deterministic(d, causal, Nq, Nk):
+    _bwd_case(2, 4, 2, Nq, Nk, d, causal, kv=[Nk, Nk // 3], seed=Nq + Nk + d + 5, deterministic=True)

@@ -25,15 +25,22 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-def _case(B, H, Hkv, N, d, causal, window, kv=None, seed=5):
+def _case(B, H, Hkv, N, d, causal, window, kv=None, seed=5, deterministic=False):
     q, _, _, do = qkv(B, H, N, d, seed, device=DEV)
     _, k, v = qkv(B, Hkv, N, d, seed + 50, device=DEV, with_dout=False)
     kvd = None if kv is None else torch.tensor(kv, dtype=torch.int32, device=DEV)
     scale = 1.0 / math.sqrt(d)
     o, lse = forward(q, k, v, causal=causal, scale=scale, kv_lens=kvd, window=window)
-    dq, dk, dv = backward(q, k, v, o, lse, do, causal=causal, scale=scale, kv_lens=kvd, window=window)
+    dq, dk, dv = backward(q, k, v, o, lse, do, causal=causal, scale=scale, kv_lens=kvd, window=window,
+                          deterministic=deterministic)
     torch.cuda.synchronize()
     check_device_status()
+    if deterministic:  # a second run agrees bit for bit
+        again = backward(q, k, v, o, lse, do, causal=causal, scale=scale, kv_lens=kvd, window=window,
+                         deterministic=True)
+        torch.cuda.synchronize()
+        for a, b in zip((dq, dk, dv), again):
+            assert torch.equal(a, b)
     g = H // Hkv
     kvn = None if kv is None else np.asarray(kv, dtype=np.int32)
     ref = oracle.bwd(to64(q), np.repeat(to64(k), g, axis=1), np.repeat(to64(v), g, axis=1), to64(do), scale,
@@ -92,3 +99,13 @@ def test_window_long_sequence_sampled():
         assert_grad(to64(dq[0, h])[rows], g["dq"], "dQ rows", np.max(np.abs(to64(dq[0, h]))))
         assert_grad(to64(dk[0, h])[keys], g["dk"], "dK keys", np.max(np.abs(to64(dk[0, h]))))
         assert_grad(to64(dv[0, h])[keys], g["dv"], "dV keys", np.max(np.abs(to64(dv[0, h]))))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal,window", [(True, (200, 0)), (False, (100, 37)), (False, (-1, 50)),
+                                           (False, (130, 130)), (True, (64, -1))])
+def test_window_deterministic(d, causal, window):
+    """The deterministic backward under a sliding window: the key blocks that
+    visit a query block start above 0, and each takes its rank within that
+    range; parity with the oracle and a bitwise repeat."""
+    _case(2, 4, 2, 1100, d, causal, window, kv=[1100, 777], seed=91 + d + window[0], deterministic=True)
