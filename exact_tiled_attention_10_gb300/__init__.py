@@ -85,6 +85,8 @@ _SIGS = {
     "fa_bwd_bnhd_deterministic": ([_vp] * 9 + [_i, _i, _i, _i, _i, _f, _i, _vp, _sz, _vp], _i),
     "fa_bwd_window_deterministic": ([_vp] * 9 + [_i, _i, _i, _i, _i, _f, _i, _i, _i, _vp, _vp, _sz, _vp], _i),
     "fa_bwd_rect_deterministic_workspace_size": ([_i] * 6, _sz),
+    "fa_bwd_block_sparse_deterministic_workspace_size": ([_i] * 5, _sz),
+    "fa_bwd_block_sparse_deterministic": ([_vp] * 9 + [_i] * 5 + [_f, _i, _vp, _vp, _vp, _vp, _sz, _vp], _i),
     "fa_bwd_rect_deterministic": ([_vp] * 9 + [_i] * 6 + [_f, _i, _vp, _vp, _sz, _vp], _i),
     "fa_bwd_gqa": ([_vp] * 9 + [_i, _i, _i, _i, _i, _f, _i, _vp, _vp, _sz, _vp], _i),
     "fa_fwd_split_workspace_size": ([_i] * 7, _sz),
@@ -300,23 +302,27 @@ def forward_block_sparse(q, k, v, row_ptr, col_idx, causal: bool = False, scale:
 
 
 def backward_block_sparse(q, k, v, o, lse, dout, row_ptr, col_idx, causal: bool = False,
-                          scale: Optional[float] = None, kv_lens=None, workspace: Optional[torch.Tensor] = None):
-    """Backward of forward_block_sparse: dQ [B,H,N,d], dK, dV [B,Hkv,N,d]."""
+                          scale: Optional[float] = None, kv_lens=None, workspace: Optional[torch.Tensor] = None,
+                          deterministic: bool = False):
+    """Backward of forward_block_sparse: dQ [B,H,N,d], dK, dV [B,Hkv,N,d].
+    deterministic: bitwise reproducible gradients (see backward)."""
     lib = load_library()
     _need_cuda(q, k, v, o, lse, dout, row_ptr, col_idx)
     B, H, N, d = q.shape
     Hkv = k.shape[1]
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     kv = _kv(kv_lens, B, q.device)
-    wsz = int(lib.fa_bwd_block_sparse_workspace_size(B, H, N, d))
+    wsz = int(lib.fa_bwd_block_sparse_deterministic_workspace_size(B, H, Hkv, N, d) if deterministic
+              else lib.fa_bwd_block_sparse_workspace_size(B, H, N, d))
     ws = workspace
     if ws is None or ws.numel() * ws.element_size() < wsz:
         ws = torch.empty(wsz, dtype=torch.uint8, device=q.device)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    _check(lib.fa_bwd_block_sparse(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
-                                   _ptr(dv), B, H, Hkv, N, d, scale, int(bool(causal)), _ptr(row_ptr),
-                                   _ptr(col_idx), _ptr(kv), _ptr(ws), ws.numel() * ws.element_size(),
-                                   _stream(q)))
+    fn = lib.fa_bwd_block_sparse_deterministic if deterministic else lib.fa_bwd_block_sparse
+    _check(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
+              _ptr(dv), B, H, Hkv, N, d, scale, int(bool(causal)), _ptr(row_ptr),
+              _ptr(col_idx), _ptr(kv), _ptr(ws), ws.numel() * ws.element_size(),
+              _stream(q)))
     return dq, dk, dv
 
 

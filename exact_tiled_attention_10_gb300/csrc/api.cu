@@ -730,7 +730,8 @@ fa_status bwd_main_impl(const BwdCtx& c, bool f32, const void* qb, const void* k
                         void* dk, void* dv, int B, int H, int N, int d, float scale, int causal, const int* kv_lens,
                         cudaStream_t stream, int Hkv = 0, int win_left = -1, int win_right = -1,
                         const int* col_ptr = nullptr, const int* row_idx = nullptr, float* dkv_part = nullptr,
-                        size_t part_bytes = 0, int Nk = -1, int* dq_turn = nullptr, int nacc = 1) {
+                        size_t part_bytes = 0, int Nk = -1, int* dq_turn = nullptr, int nacc = 1,
+                        const int* row_ptr = nullptr, const int* col_idx = nullptr) {
     const int BH = c.BH, Np = c.Np;
     const bool rect = Nk >= 0;  // rectangular: N query rows, Nk keys
     if (!rect) Nk = N;
@@ -778,7 +779,7 @@ fa_status bwd_main_impl(const BwdCtx& c, bool f32, const void* qb, const void* k
     if (dq_turn) {
         // deterministic: zeroed turn counters, one per quarter of a dQ tile
         auto set_det = [&](auto& pd) {
-            pd.nqb = Np / BR;
+            pd.nqt = Np / BR;
             pd.dq_turn = dq_turn;
             pd.nacc = nacc;
         };
@@ -792,6 +793,18 @@ fa_status bwd_main_impl(const BwdCtx& c, bool f32, const void* qb, const void* k
                 pd.coff = Nk - N;
                 set_det(pd);
                 e = fa::launch_bwd_main_det_rect(d, causal != 0, tq, tk, tv, tdo, tdq, pd, grid, stream);
+            } else if (col_ptr) {
+                fa::BwdDet<fa::BwdParamsSparse> pd;
+                memset(&pd, 0, sizeof(pd));
+                static_cast<fa::BwdParams&>(pd) = p;
+                pd.col_ptr = col_ptr;
+                pd.row_idx = row_idx;
+                pd.nqb = (N + 127) / 128;
+                pd.nkb = (N + 127) / 128;
+                pd.row_ptr = row_ptr;
+                pd.col_idx = col_idx;
+                set_det(pd);
+                e = fa::launch_bwd_main_det_sparse(d, causal != 0, tq, tk, tv, tdo, tdq, pd, grid, stream);
             } else if (win_left >= 0 || win_right >= 0) {
                 fa::BwdDet<fa::BwdParamsWin> pd;
                 memset(&pd, 0, sizeof(pd));
@@ -1136,7 +1149,7 @@ fa_status bwd_packed_impl(const void* q, const void* k, const void* v, const voi
         fa::BwdParamsDet pd;
         memset(&pd, 0, sizeof(pd));
         static_cast<fa::BwdParams&>(pd) = p;
-        pd.nqb = MSp / (d == 128 ? 64 : 128);
+        pd.nqt = MSp / (d == 128 ? 64 : 128);
         pd.dq_turn = turn;
         pd.nacc = nacc;
         e = cudaMemsetAsync(turn, 0, det_turn_bytes(nacc, batch, H, max_seqlen, d), stream);
@@ -1224,7 +1237,8 @@ size_t det_workspace(int B, int H, int Hkv, int Nq, int Nk, int d) {
 fa_status bwd_det_impl(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
                        void* dq, void* dk, void* dv, int B, int H, int Hkv, int Nq, int Nk, int d, float scale,
                        int causal, int win_left, int win_right, const int* kv_lens, void* workspace,
-                       size_t workspace_bytes, fa_stream_t stream) {
+                       size_t workspace_bytes, fa_stream_t stream, const int* row_ptr = nullptr,
+                       const int* col_idx = nullptr) {
     FA_CHECK_PTR(q);
     FA_CHECK_PTR(k);
     FA_CHECK_PTR(v);
@@ -1241,16 +1255,25 @@ fa_status bwd_det_impl(const void* q, const void* k, const void* v, const void* 
     const int nk = rect ? Nk : Nq;
     BwdCtx c{};
     FA_TRY(bwd_setup(FA_BF16, B, H, Nq, d, scale, workspace, workspace_bytes, &c));
-    const size_t need = det_workspace(B, H, Hkv, Nq, nk, d);
+    const size_t det_need = det_workspace(B, H, Hkv, Nq, nk, d);
+    const size_t need = row_ptr ? round_up(det_need, 256) + sparse_lists_bytes(Nq) : det_need;
     if (workspace_bytes < need)
         return fail(FA_ERR_INVALID_ARG, "workspace too small (%zu < %zu bytes)", workspace_bytes, need);
     const int nacc = det_num_acc(B, Hkv, nk);
     if (c.L.dqacc + det_acc_bytes(B, H, Nq, d) != c.L.total)
         return fail(FA_ERR_INVALID_ARG, "internal: the dQ accumulator is not the last workspace region");
     int* turn = reinterpret_cast<int*>(c.ws + c.L.total + (size_t)(nacc - 1) * det_acc_bytes(B, H, Nq, d));
+    int *col_ptr = nullptr, *row_idx = nullptr;
+    if (row_ptr) {  // block lists: transposed after the counters
+        const int nb = (Nq + 127) / 128;
+        col_ptr = reinterpret_cast<int*>(c.ws + round_up(det_need, 256));
+        row_idx = col_ptr + nb + 1;
+        cudaError_t e = fa::launch_block_lists_transpose(row_ptr, col_idx, nb, nb, col_ptr, row_idx, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "block list transposition launch");
+    }
     FA_TRY(bwd_pre_impl(c, false, o, lse, dout, Nq, d, stream));
     FA_TRY(bwd_main_impl(c, false, q, k, v, dout, dk, dv, B, H, Nq, d, scale, causal, kv_lens, stream, Hkv, win_left,
-                         win_right, nullptr, nullptr, nullptr, 0, Nk, turn, nacc));
+                         win_right, col_ptr, row_idx, nullptr, 0, Nk, turn, nacc, row_ptr, col_idx));
     cudaError_t e = fa::launch_bwd_dq_det(reinterpret_cast<float*>(c.ws + c.L.dqacc), turn, dq, scale, c.BH, Nq,
                                           c.Np, d, nacc, bw_grid(c.dev), stream);
     if (e != cudaSuccess) return cuda_fail(e, "dQ conversion launch");
@@ -1281,6 +1304,23 @@ fa_status fa_bwd_window_deterministic(const void* q, const void* k, const void* 
     // as fa_bwd_window: the causal mask is folded into the window's right edge
     return bwd_det_impl(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, N, -1, d, scale, causal, window_left,
                         window_right, kv_lens, workspace, workspace_bytes, stream);
+}
+
+size_t fa_bwd_block_sparse_deterministic_workspace_size(int B, int H, int Hkv, int N, int d) {
+    const size_t w = det_workspace(B, H, Hkv, N, N, d);
+    return w ? round_up(w, 256) + sparse_lists_bytes(N) : 0;
+}
+
+fa_status fa_bwd_block_sparse_deterministic(const void* q, const void* k, const void* v, const void* o,
+                                            const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
+                                            int H, int Hkv, int N, int d, float scale, int causal,
+                                            const int* row_ptr, const int* col_idx, const int* kv_lens,
+                                            void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+    if (!row_ptr || !col_idx) return fail(FA_ERR_INVALID_ARG, "row_ptr and col_idx must not be NULL");
+    if (N > 0 && (N + 127) / 128 > kMaxSparseBlocks)
+        return fail(FA_ERR_UNSUPPORTED, "block-sparse attention takes at most %d blocks", kMaxSparseBlocks);
+    return bwd_det_impl(q, k, v, o, lse, dout, dq, dk, dv, B, H, Hkv, N, -1, d, scale, causal, -1, -1, kv_lens,
+                        workspace, workspace_bytes, stream, row_ptr, col_idx);
 }
 
 size_t fa_bwd_rect_deterministic_workspace_size(int B, int H, int Hkv, int Nq, int Nk, int d) {

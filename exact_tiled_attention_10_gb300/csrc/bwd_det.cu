@@ -1,5 +1,6 @@
 // Deterministic backward kernel instances (bf16 gradients; plain, shared
-// key/value heads, sliding window, rectangular, packed sequences): dQ tiles
+// key/value heads, sliding window, block lists, rectangular, packed
+// sequences): dQ tiles
 // take their key blocks' contributions in a fixed order, so repeated runs give
 // bitwise-identical dQ, dK and dV.
 #include "bwd_kernel.cuh"
@@ -43,6 +44,21 @@ cudaError_t launch_bwd_main_det_rect(int d, bool causal, const CUtensorMap& tq, 
                                                                                                grid, s);
     return causal ? bwd::launch<C64, true, false, true, false, false, false, true, true>(tq, tk, tv, tdo, tdq, p, grid, s)
                   : bwd::launch<C64, false, false, true, false, false, false, true, true>(tq, tk, tv, tdo, tdq, p, grid,
+                                                                                          s);
+}
+
+cudaError_t launch_bwd_main_det_sparse(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
+                                       const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
+                                       const BwdDet<BwdParamsSparse>& p, int grid, cudaStream_t s) {
+    using C128 = bwd::Cfg<128>;
+    using C64 = bwd::Cfg<64>;
+    if (d == 128)
+        return causal ? bwd::launch<C128, true, false, true, false, false, true, false, true>(tq, tk, tv, tdo, tdq, p,
+                                                                                              grid, s)
+                      : bwd::launch<C128, false, false, true, false, false, true, false, true>(tq, tk, tv, tdo, tdq, p,
+                                                                                               grid, s);
+    return causal ? bwd::launch<C64, true, false, true, false, false, true, false, true>(tq, tk, tv, tdo, tdq, p, grid, s)
+                  : bwd::launch<C64, false, false, true, false, false, true, false, true>(tq, tk, tv, tdo, tdq, p, grid,
                                                                                           s);
 }
 

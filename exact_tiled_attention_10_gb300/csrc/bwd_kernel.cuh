@@ -322,7 +322,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                const __grid_constant__ CUtensorMap tdq, const KernelParamsT<WINDOW, SPARSE, RECT, DET> p) {
-    static_assert(!DET || !SPARSE, "deterministic: no block-sparse instance");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -735,22 +734,44 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int row = (VARLEN ? bhq * p.B + I.b : bhq) * p.Np + i * C::BR;
                 bool first = false;
                 if constexpr (DET) {
-                    // key block kt writes accumulator kt % nacc after the key blocks
-                    // kt - nacc, kt - 2 nacc, ..., lo that also visit query block i
-                    // (they form the range lo .. kt: i0 and the window's end grow with
-                    // the key block); the first of them stores
-                    int lo = 0;
-                    if constexpr (WINDOW)  // first key block whose window reaches query block i
-                        if (p.win_left >= 0) lo = max(0, i * C::BR - p.win_left) / C::BC;
-                    const int a = I.kt % p.nacc;
-                    const int first_a = lo + ((a - lo % p.nacc) + p.nacc) % p.nacc;
+                    // the visitors of query block i, in increasing key block order, take
+                    // accumulators 0, 1, ..., nacc - 1, 0, ...: a key block writes after
+                    // the visitors nacc, 2 nacc, ... places before it; the first stores.
+                    // Without block lists they are the key blocks lo .. (i0 and the
+                    // window's end grow with the key block)
+                    // pos: this key block's place among the query block's visitors
+                    int pos;
+                    if constexpr (SPARSE) {
+                        // block lists: the visitors are the query block's list (ascending;
+                        // the causal and key-length cuts only drop its tail); binary search
+                        const int qb = (i * C::BR) / 128;
+                        int lo = 0;
+                        if (lane == 0) {
+                            const int nnz = __ldg(p.row_ptr + p.nqb);
+                            const int b0 = min(max(__ldg(p.row_ptr + qb), 0), nnz);
+                            int hi = min(max(__ldg(p.row_ptr + qb + 1), b0), nnz);
+                            lo = b0;
+                            while (lo < hi) {  // first position whose key block is >= kt
+                                const int mid = (lo + hi) >> 1;
+                                if (__ldg(p.col_idx + mid) < I.kt) lo = mid + 1;
+                                else hi = mid;
+                            }
+                            lo -= b0;
+                        }
+                        pos = __shfl_sync(0xffffffffu, lo, 0);
+                    } else {
+                        int lo = 0;
+                        if constexpr (WINDOW)  // first key block whose window reaches query block i
+                            if (p.win_left >= 0) lo = max(0, i * C::BR - p.win_left) / C::BC;
+                        pos = I.kt - lo;
+                    }
+                    const int a = pos % p.nacc;
                     const int srow = VARLEN ? bhq * p.B + I.b : bhq;  // statistics row group of the tile
-                    int* turn = p.dq_turn + (((size_t)a * (p.B * p.H) + srow) * p.nqb + i) * 4 + wq;
-                    if (!(ok = wait_turn_warp(turn, (I.kt - first_a) / p.nacc, abort_flag, p.err, kErrWaitBwdDqTurn)))
-                        break;
+                    int* turn = p.dq_turn + (((size_t)a * (p.B * p.H) + srow) * p.nqt + i) * 4 + wq;
+                    if (!(ok = wait_turn_warp(turn, pos / p.nacc, abort_flag, p.err, kErrWaitBwdDqTurn))) break;
                     pend[0] = turn;
                     row += a * (p.B * p.H * p.Np);
-                    first = I.kt == first_a;
+                    first = pos < p.nacc;
                 }
                 if (lane == 0) {
                     if constexpr (DET) fence_proxy_async_global();

@@ -153,12 +153,14 @@ struct BwdParamsSparse : BwdParams {
     const int* col_ptr;  // [nkb + 1]
     const int* row_idx;
     int nqb, nkb;
+    const int* row_ptr;  // the forward lists (deterministic instance only)
+    const int* col_idx;
 };
 // Deterministic backward: nacc float32 dQ accumulators [nacc][B*H][Np][d]
 // (the first is dq_acc); key block kt writes accumulator kt % nacc, and each
 // accumulator tile of (query head row bhq, query block i) receives its key
 // blocks in increasing order: the first one stores, the others add.
-// dq_turn[((a * B*H + bhq) * nqb + i) * 4 + w] (nqb = Np / query rows per
+// dq_turn[((a * B*H + bhq) * nqt + i) * 4 + w] (nqt = Np / query rows per
 // step; w = the drain warp's quarter of the tile) counts the contributions to
 // quarter w of that tile of accumulator a; key block kt writes once it reaches
 // its rank among the key blocks visiting that query block in accumulator a
@@ -170,7 +172,7 @@ struct BwdParamsSparse : BwdParams {
 template <class Base>
 struct BwdDet : Base {
     int* dq_turn;
-    int nqb;
+    int nqt;  // query tiles of BR rows per head row: Np / BR
     int nacc;
 };
 using BwdParamsDet = BwdDet<BwdParams>;
@@ -213,6 +215,9 @@ cudaError_t launch_bwd_main_det_window(int d, const CUtensorMap& tq, const CUten
 cudaError_t launch_bwd_main_det_rect(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
                                      const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
                                      const BwdDet<BwdParamsRect>& p, int grid, cudaStream_t stream);
+cudaError_t launch_bwd_main_det_sparse(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
+                                       const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
+                                       const BwdDet<BwdParamsSparse>& p, int grid, cudaStream_t stream);
 cudaError_t launch_bwd_main_det_varlen(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
                                        const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
                                        const BwdParamsDet& p, int grid, cudaStream_t stream);

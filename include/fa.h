@@ -371,18 +371,29 @@ fa_status fa_bwd_bnhd_deterministic(const void* q, const void* k, const void* v,
                                     int B, int N, int H, int Hkv, int d, float scale, int causal,
                                     void* workspace, size_t workspace_bytes, fa_stream_t stream);
 
-/* Deterministic versions of fa_bwd_window and fa_bwd_rect (same arguments
- * and results).  Under a sliding window, the key blocks that visit a query
- * block form a range that may start above 0; a key block's turn is its rank
- * within that range.  Workspace: fa_bwd_deterministic_workspace_size(B, H,
- * Hkv, N, d) for the window, fa_bwd_rect_deterministic_workspace_size(...)
- * for Nq x Nk.  The block-sparse backward has no deterministic form. */
+/* Deterministic versions of fa_bwd_window, fa_bwd_block_sparse and
+ * fa_bwd_rect (same arguments and results).  The key blocks that visit a
+ * query block take the accumulators in their order among that block's
+ * visitors: under a sliding window they form a range that may start above
+ * 0; with block lists they are the query block's list, the causal and
+ * key-length cuts dropping only its tail (found by a binary search in
+ * col_idx).  Workspace: fa_bwd_deterministic_workspace_size(B, H, Hkv, N, d)
+ * for the window, the *_deterministic_workspace_size queries for the others
+ * (block lists: plus their transposition, as for fa_bwd_block_sparse). */
 fa_status fa_bwd_window_deterministic(const void* q, const void* k, const void* v, const void* o,
                                       const float* lse, const void* dout, void* dq, void* dk,
                                       void* dv, int B, int H, int Hkv, int N, int d, float scale,
                                       int causal, int window_left, int window_right,
                                       const int* kv_lens, void* workspace, size_t workspace_bytes,
                                       fa_stream_t stream);
+size_t fa_bwd_block_sparse_deterministic_workspace_size(int B, int H, int Hkv, int N, int d);
+fa_status fa_bwd_block_sparse_deterministic(const void* q, const void* k, const void* v,
+                                            const void* o, const float* lse, const void* dout,
+                                            void* dq, void* dk, void* dv, int B, int H, int Hkv,
+                                            int N, int d, float scale, int causal,
+                                            const int* row_ptr, const int* col_idx,
+                                            const int* kv_lens, void* workspace,
+                                            size_t workspace_bytes, fa_stream_t stream);
 size_t fa_bwd_rect_deterministic_workspace_size(int B, int H, int Hkv, int Nq, int Nk, int d);
 fa_status fa_bwd_rect_deterministic(const void* q, const void* k, const void* v, const void* o,
                                     const float* lse, const void* dout, void* dq, void* dk, void* dv,

@@ -25,16 +25,23 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-def _case(B, H, Hkv, N, d, causal, bm, kv=None, seed=5):
+def _case(B, H, Hkv, N, d, causal, bm, kv=None, seed=5, deterministic=False):
     q, _, _, do = qkv(B, H, N, d, seed, device=DEV)
     _, k, v = qkv(B, Hkv, N, d, seed + 50, device=DEV, with_dout=False)
     kvd = None if kv is None else torch.tensor(kv, dtype=torch.int32, device=DEV)
     rp, ci = block_lists(bm, DEV)
     scale = 1.0 / math.sqrt(d)
     o, lse = forward_block_sparse(q, k, v, rp, ci, causal=causal, scale=scale, kv_lens=kvd)
-    dq, dk, dv = backward_block_sparse(q, k, v, o, lse, do, rp, ci, causal=causal, scale=scale, kv_lens=kvd)
+    dq, dk, dv = backward_block_sparse(q, k, v, o, lse, do, rp, ci, causal=causal, scale=scale, kv_lens=kvd,
+                                       deterministic=deterministic)
     torch.cuda.synchronize()
     check_device_status()
+    if deterministic:  # a second run agrees bit for bit
+        again = backward_block_sparse(q, k, v, o, lse, do, rp, ci, causal=causal, scale=scale, kv_lens=kvd,
+                                      deterministic=True)
+        torch.cuda.synchronize()
+        for a, b in zip((dq, dk, dv), again):
+            assert torch.equal(a, b)
     g = H // Hkv
     kvn = None if kv is None else np.asarray(kv, dtype=np.int32)
     ref = oracle.bwd(to64(q), np.repeat(to64(k), g, axis=1), np.repeat(to64(v), g, axis=1), to64(do), scale,
@@ -114,3 +121,18 @@ def test_block_sparse_long_sequence_sampled():
         assert_grad(to64(dq[0, h])[rows], g["dq"], "dQ rows", np.max(np.abs(to64(dq[0, h]))))
         assert_grad(to64(dk[0, h])[keys], g["dk"], "dK keys", np.max(np.abs(to64(dk[0, h]))))
         assert_grad(to64(dv[0, h])[keys], g["dv"], "dV keys", np.max(np.abs(to64(dv[0, h]))))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_block_sparse_deterministic(d, causal):
+    """The deterministic backward with block lists: a key block's turn is its
+    place in the query block's list (binary search); parity with the oracle,
+    shared heads, key lengths, and a bitwise repeat."""
+    N = 1300
+    nb = (N + 127) // 128
+    rng = np.random.default_rng(97 + d + causal)
+    bm = (rng.random((nb, nb)) < 0.45).astype(np.uint8)
+    bm[:, 0] = 1
+    bm[3] = 0  # an empty list
+    _case(2, 4, 2, N, d, causal, bm, kv=[N, 900], seed=101 + d, deterministic=True)
