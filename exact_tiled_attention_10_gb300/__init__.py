@@ -77,6 +77,9 @@ _SIGS = {
     "fa_bwd_varlen_workspace_size": ([_i] * 4, _sz),
     "fa_bwd_varlen": ([_vp] * 10 + [_i, _i, _i, _i, _i, _i, _f, _i, _vp, _sz, _vp], _i),
     "fa_fwd_bnhd": ([_vp] * 5 + [_i, _i, _i, _i, _i, _f, _i, _vp], _i),
+    "fa_fwd_varlen_kv": ([_vp] * 7 + [_i] * 7 + [_f, _i, _vp], _i),
+    "fa_bwd_varlen_kv_workspace_size": ([_i] * 7, _sz),
+    "fa_bwd_varlen_kv": ([_vp] * 11 + [_i] * 8 + [_f, _i, _i, _vp, _sz, _vp], _i),
     "fa_bwd_bnhd_workspace_size": ([_i] * 4, _sz),
     "fa_bwd_bnhd": ([_vp] * 9 + [_i, _i, _i, _i, _i, _f, _i, _vp, _sz, _vp], _i),
     "fa_bwd_varlen_deterministic_workspace_size": ([_i] * 5, _sz),
@@ -385,21 +388,29 @@ def _cu(cu_seqlens, device):
 
 def forward_varlen(q, k, v, cu_seqlens, max_seqlen: int, causal: bool = False,
                    scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
-                   lse: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+                   lse: Optional[torch.Tensor] = None, cu_seqlens_k=None) -> Tuple[torch.Tensor, torch.Tensor]:
     """Packed variable-length forward: q [total, H, d], k, v [total, Hkv, d]
     (bf16), sequence b = tokens cu_seqlens[b] .. cu_seqlens[b+1]-1.  Returns
-    O [total, H, d] and LSE [H, total]."""
+    O [total, H, d] and LSE [H, total].  cu_seqlens_k: the sequences' own key
+    ranges in k, v [total_k, Hkv, d] (flash_attn_varlen_func's cu_seqlens_k;
+    with causal, the queries are each sequence's last positions)."""
     lib = load_library()
     _need_cuda(q, k, v)
     T, H, d = q.shape
     Hkv = k.shape[1]
-    if (q.dtype != torch.bfloat16 or k.dtype != q.dtype or v.dtype != q.dtype or k.shape != (T, Hkv, d)
-            or v.shape != k.shape or H % Hkv != 0):
-        raise ValueError("q [total,H,d], k, v [total,Hkv,d] bfloat16 with H a multiple of Hkv")
+    Tk = k.shape[0]
+    if (q.dtype != torch.bfloat16 or k.dtype != q.dtype or v.dtype != q.dtype or k.shape != (Tk, Hkv, d)
+            or v.shape != k.shape or H % Hkv != 0 or (cu_seqlens_k is None and Tk != T)):
+        raise ValueError("q [total,H,d], k, v [total(_k),Hkv,d] bfloat16 with H a multiple of Hkv")
     cu = _cu(cu_seqlens, q.device)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     o = torch.empty_like(q) if out is None else out
     l = torch.empty((H, T), dtype=torch.float32, device=q.device) if lse is None else lse
+    if cu_seqlens_k is not None:
+        cuk = _cu(cu_seqlens_k, q.device)
+        _check(lib.fa_fwd_varlen_kv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(l), _ptr(cu), _ptr(cuk), cu.numel() - 1,
+                                    T, Tk, int(max_seqlen), H, Hkv, d, scale, int(bool(causal)), _stream(q)))
+        return o, l
     _check(lib.fa_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(l), _ptr(cu), cu.numel() - 1, T,
                              int(max_seqlen), H, Hkv, d, scale, int(bool(causal)), _stream(q)))
     return o, l
@@ -453,9 +464,10 @@ def backward_bnhd(q, k, v, o, lse, dout, causal: bool = False, scale: Optional[f
 
 def backward_varlen(q, k, v, o, lse, dout, cu_seqlens, max_seqlen: int, causal: bool = False,
                     scale: Optional[float] = None, workspace: Optional[torch.Tensor] = None,
-                    deterministic: bool = False):
-    """Backward of forward_varlen: dQ [total, H, d], dK, dV [total, Hkv, d].
-    deterministic: bitwise reproducible gradients (see backward)."""
+                    deterministic: bool = False, cu_seqlens_k=None, max_seqlen_k: Optional[int] = None):
+    """Backward of forward_varlen: dQ [total, H, d], dK, dV [total(_k), Hkv, d].
+    deterministic: bitwise reproducible gradients (see backward).
+    cu_seqlens_k / max_seqlen_k: separate key ranges (see forward_varlen)."""
     lib = load_library()
     _need_cuda(q, k, v, o, lse, dout)
     T, H, d = q.shape
@@ -463,6 +475,19 @@ def backward_varlen(q, k, v, o, lse, dout, cu_seqlens, max_seqlen: int, causal: 
     cu = _cu(cu_seqlens, q.device)
     batch = cu.numel() - 1
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    if cu_seqlens_k is not None:
+        cuk = _cu(cu_seqlens_k, q.device)
+        mk = int(max_seqlen if max_seqlen_k is None else max_seqlen_k)
+        wsz = int(lib.fa_bwd_varlen_kv_workspace_size(batch, int(max_seqlen), mk, H, Hkv, d, int(bool(deterministic))))
+        ws = workspace
+        if ws is None or ws.numel() * ws.element_size() < wsz:
+            ws = torch.empty(wsz, dtype=torch.uint8, device=q.device)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        _check(lib.fa_bwd_varlen_kv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
+                                    _ptr(dv), _ptr(cu), _ptr(cuk), batch, T, k.shape[0], int(max_seqlen), mk, H, Hkv,
+                                    d, scale, int(bool(causal)), int(bool(deterministic)), _ptr(ws),
+                                    ws.numel() * ws.element_size(), _stream(q)))
+        return dq, dk, dv
     wsz = int(lib.fa_bwd_varlen_deterministic_workspace_size(batch, int(max_seqlen), H, Hkv, d) if deterministic
               else lib.fa_bwd_varlen_workspace_size(batch, int(max_seqlen), H, d))
     ws = workspace

@@ -573,7 +573,9 @@ namespace {
 // each (the [B, N, H, d] layout, LSE [B, H, N]).
 fa_status fwd_packed_impl(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens,
                           int batch, int total, int max_seqlen, int H, int Hkv, int d, float scale, int causal,
-                          fa_stream_t stream) {
+                          fa_stream_t stream, const int* cu_seqlens_k = nullptr, int total_k = -1) {
+    if (total_k < 0) total_k = total;
+    if (total_k <= 0) return fail(FA_ERR_INVALID_ARG, "total_k must be positive");
     FA_TRY(check_common(batch, H, max_seqlen, d, scale));
     if (total <= 0) return fail(FA_ERR_INVALID_ARG, "total must be positive");
     if (Hkv < 1 || H % Hkv != 0) return fail(FA_ERR_INVALID_ARG, "H (%d) must be a multiple of Hkv (%d)", H, Hkv);
@@ -586,8 +588,8 @@ fa_status fwd_packed_impl(const void* q, const void* k, const void* v, void* o, 
     FA_TRY(device_info(&dev));
     fa::FwdMaps m;
     FA_TRY(make_map_tok(&m.q, q, d, H, total, 128));
-    FA_TRY(make_map_tok(&m.k, k, d, Hkv, total, 128));
-    FA_TRY(make_map_tok(&m.v, v, d, Hkv, total, 128));
+    FA_TRY(make_map_tok(&m.k, k, d, Hkv, total_k, 128));
+    FA_TRY(make_map_tok(&m.v, v, d, Hkv, total_k, 128));
     m.q_lo = m.q;
     m.k_lo = m.k;
     fa::FwdParams p;
@@ -602,6 +604,7 @@ fa_status fwd_packed_impl(const void* q, const void* k, const void* v, void* o, 
     p.o = o;
     p.lse = lse;
     p.cu_seqlens = cu_seqlens;
+    p.cu_seqlens_k = cu_seqlens_k;
     p.total = total;
     p.err = dev->err_word;
     cudaError_t e = fa::launch_fwd_varlen(d, causal != 0, m, p, grid_for_items(p.num_items, dev->sms), stream);
@@ -618,6 +621,14 @@ fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, fl
                         fa_stream_t stream) {
     if (!cu_seqlens) return fail(FA_ERR_INVALID_ARG, "cu_seqlens must not be NULL");
     return fwd_packed_impl(q, k, v, o, lse, cu_seqlens, batch, total, max_seqlen, H, Hkv, d, scale, causal, stream);
+}
+
+fa_status fa_fwd_varlen_kv(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens_q,
+                           const int* cu_seqlens_k, int batch, int total_q, int total_k, int max_seqlen_q, int H,
+                           int Hkv, int d, float scale, int causal, fa_stream_t stream) {
+    if (!cu_seqlens_q || !cu_seqlens_k) return fail(FA_ERR_INVALID_ARG, "cu_seqlens_q and cu_seqlens_k must not be NULL");
+    return fwd_packed_impl(q, k, v, o, lse, cu_seqlens_q, batch, total_q, max_seqlen_q, H, Hkv, d, scale, causal,
+                           stream, cu_seqlens_k, total_k);
 }
 
 fa_status fa_fwd_bnhd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int N, int H, int Hkv,
@@ -1090,7 +1101,11 @@ namespace {
 fa_status bwd_packed_impl(const void* q, const void* k, const void* v, const void* o, const float* lse,
                           const void* dout, void* dq, void* dk, void* dv, const int* cu_seqlens, int batch, int total,
                           int max_seqlen, int H, int Hkv, int d, float scale, int causal, void* workspace,
-                          size_t workspace_bytes, fa_stream_t stream, bool det = false) {
+                          size_t workspace_bytes, fa_stream_t stream, bool det = false,
+                          const int* cu_seqlens_k = nullptr, int total_k = -1, int max_seqlen_k = -1) {
+    if (total_k < 0) total_k = total;
+    if (max_seqlen_k < 0) max_seqlen_k = max_seqlen;
+    if (total_k <= 0 || max_seqlen_k <= 0) return fail(FA_ERR_INVALID_ARG, "total_k and max_seqlen_k must be positive");
     FA_TRY(check_common(batch, H, max_seqlen, d, scale));
     if (total <= 0) return fail(FA_ERR_INVALID_ARG, "total must be positive");
     if (Hkv < 1 || H % Hkv != 0) return fail(FA_ERR_INVALID_ARG, "H (%d) must be a multiple of Hkv (%d)", H, Hkv);
@@ -1105,8 +1120,10 @@ fa_status bwd_packed_impl(const void* q, const void* k, const void* v, const voi
     FA_CHECK_PTR(dv);
     FA_CHECK_PTR(workspace);
     const size_t base = fa_bwd_varlen_workspace_size(batch, max_seqlen, H, d);
-    const int nacc = det ? det_num_acc(batch, Hkv, max_seqlen) : 1;
-    const size_t need = det ? fa_bwd_varlen_deterministic_workspace_size(batch, max_seqlen, H, Hkv, d) : base;
+    const int nacc = det ? det_num_acc(batch, Hkv, max_seqlen_k) : 1;
+    const size_t need = det ? base + (size_t)(nacc - 1) * det_acc_bytes(batch, H, max_seqlen, d) +
+                                  det_turn_bytes(nacc, batch, H, max_seqlen, d)
+                            : base;
     if (workspace_bytes < need) return fail(FA_ERR_INVALID_ARG, "workspace too small (%zu < %zu bytes)", workspace_bytes, need);
     DeviceInfo* dev = nullptr;
     FA_TRY(device_info(&dev));
@@ -1123,15 +1140,15 @@ fa_status bwd_packed_impl(const void* q, const void* k, const void* v, const voi
     CUtensorMap tq, tk, tv, tdo, tdq;
     FA_TRY(make_map_tok(&tq, q, d, H, total, BR));
     FA_TRY(make_map_tok(&tdo, dout, d, H, total, BR));
-    FA_TRY(make_map_tok(&tk, k, d, Hkv, total, 128));
-    FA_TRY(make_map_tok(&tv, v, d, Hkv, total, 128));
+    FA_TRY(make_map_tok(&tk, k, d, Hkv, total_k, 128));
+    FA_TRY(make_map_tok(&tv, v, d, Hkv, total_k, 128));
     if ((long long)R * nacc >= (1LL << 31))
         return fail(FA_ERR_UNSUPPORTED, "dQ accumulator rows exceed the 32-bit tensor coordinate range");
     FA_TRY(make_map_dqacc(&tdq, dqacc, d, (long long)R * nacc));
     fa::BwdParams p;
     memset(&p, 0, sizeof(p));
     p.B = batch; p.H = H; p.N = max_seqlen; p.Np = MSp; p.Hkv = Hkv;
-    p.num_kt = (max_seqlen + 127) / 128;
+    p.num_kt = (max_seqlen_k + 127) / 128;
     p.num_items = batch * Hkv * p.num_kt;
     p.scale = scale;
     p.scale_log2 = scale * 1.4426950408889634f;
@@ -1141,6 +1158,7 @@ fa_status bwd_packed_impl(const void* q, const void* k, const void* v, const voi
     p.dk = dk;
     p.dv = dv;
     p.cu_seqlens = cu_seqlens;
+    p.cu_seqlens_k = cu_seqlens_k;
     p.total = total;
     p.err = dev->err_word;
     if (det) {
@@ -1184,6 +1202,27 @@ fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const void*
 }
 
 size_t fa_bwd_bnhd_workspace_size(int B, int N, int H, int d) { return fa_bwd_varlen_workspace_size(B, N, H, d); }
+
+size_t fa_bwd_varlen_kv_workspace_size(int batch, int max_seqlen_q, int max_seqlen_k, int H, int Hkv, int d,
+                                       int deterministic) {
+    const size_t base = fa_bwd_varlen_workspace_size(batch, max_seqlen_q, H, d);
+    if (base == 0 || max_seqlen_k <= 0 || Hkv < 1 || H % Hkv != 0) return 0;
+    if (!deterministic) return base;
+    const int nacc = det_num_acc(batch, Hkv, max_seqlen_k);
+    return base + (size_t)(nacc - 1) * det_acc_bytes(batch, H, max_seqlen_q, d) +
+           det_turn_bytes(nacc, batch, H, max_seqlen_q, d);
+}
+
+fa_status fa_bwd_varlen_kv(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                           const void* dout, void* dq, void* dk, void* dv, const int* cu_seqlens_q,
+                           const int* cu_seqlens_k, int batch, int total_q, int total_k, int max_seqlen_q,
+                           int max_seqlen_k, int H, int Hkv, int d, float scale, int causal, int deterministic,
+                           void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+    if (!cu_seqlens_q || !cu_seqlens_k) return fail(FA_ERR_INVALID_ARG, "cu_seqlens_q and cu_seqlens_k must not be NULL");
+    return bwd_packed_impl(q, k, v, o, lse, dout, dq, dk, dv, cu_seqlens_q, batch, total_q, max_seqlen_q, H, Hkv, d,
+                           scale, causal, workspace, workspace_bytes, stream, deterministic != 0, cu_seqlens_k, total_k,
+                           max_seqlen_k);
+}
 
 fa_status fa_bwd_varlen_deterministic(const void* q, const void* k, const void* v, const void* o, const float* lse,
                                       const void* dout, void* dq, void* dk, void* dv, const int* cu_seqlens,

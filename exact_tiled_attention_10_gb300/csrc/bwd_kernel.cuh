@@ -111,6 +111,7 @@ struct Item {
     int bh, b, kt, kvl, i0, n;
     int qh0, ni;  // first query head row (b * H + ...), query blocks per query head
     int kvh, tb, seqlen;  // packed sequences: key/value head in the sequence, first token, length
+    int tbk, coff;        // packed: first key token, causal offset (keys - queries) of the sequence
     int sub;              // split group: which part of the query heads (0 .. gsplit - 1)
 };
 
@@ -187,12 +188,19 @@ __device__ __forceinline__ Item get_item(int it, const ParamsT<WINDOW, SPARSE, R
         I.seqlen = max(0, min(e - a, p.N));
     }
     int kvl = I.seqlen;
+    I.tbk = I.tb;
+    I.coff = 0;
+    if (VARLEN && p.cu_seqlens_k) {  // its own key range; causal: the queries are the last len_q positions
+        I.tbk = __ldg(p.cu_seqlens_k + I.b);
+        kvl = max(0, __ldg(p.cu_seqlens_k + I.b + 1) - I.tbk);
+        I.coff = kvl - I.seqlen;
+    }
     if constexpr (RECT) kvl = p.Nk;
     if (!VARLEN && p.kv_lens) kvl = min(max(__ldg(p.kv_lens + I.b), 0), key_count(p));
     I.kvl = kvl;
     const int key0 = I.kt * C::BC;
     const int iend = ((VARLEN ? I.seqlen : p.N) + C::BR - 1) / C::BR;
-    I.i0 = CAUSAL ? (RECT ? max(0, key0 - causal_offset(p)) : key0) / C::BR : 0;
+    I.i0 = CAUSAL ? (RECT ? max(0, key0 - causal_offset(p)) : VARLEN ? max(0, key0 - I.coff) : key0) / C::BR : 0;
     if constexpr (SPARSE) {
         // the block's query blocks, without those entirely above the causal
         // diagonal (all query rows before the block's first key)
@@ -383,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) {
                 mbar_arrive_expect_tx(BAR(C::B_KVFULL), 2 * C::K_TILE);
                 for (int bx = 0; bx < C::NBOX; ++bx) {
-                    const int c1 = VARLEN ? I.kvh : I.kt * C::BC, c2 = VARLEN ? I.tb + I.kt * C::BC : I.bh;
+                    const int c1 = VARLEN ? I.kvh : I.kt * C::BC, c2 = VARLEN ? I.tbk + I.kt * C::BC : I.bh;
                     tma_load_3d(sbase + C::OFF_K + bx * C::K_BOX, &tk, BAR(C::B_KVFULL), bx * 64, c1, c2);
                     tma_load_3d(sbase + C::OFF_V + bx * C::K_BOX, &tv, BAR(C::B_KVFULL), bx * 64, c1, c2);
                 }
@@ -518,9 +526,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int key = I.kt * C::BC + kr;
             // dK, dV row: [B,Hkv,N,d], or token-major [total, Hkv, d] for packed sequences
             const int nkeys = key_count(p);
-            const size_t krow = VARLEN ? (size_t)(I.tb + key) * p.Hkv + I.kvh : (size_t)I.bh * nkeys + key;
-            if (I.n == 0) {  // key block entirely beyond kv_len: zero gradients (packed: nothing to write)
-                if (!VARLEN && key < nkeys) {
+            const size_t krow = VARLEN ? (size_t)(I.tbk + key) * p.Hkv + I.kvh : (size_t)I.bh * nkeys + key;
+            if (I.n == 0) {  // no query sees the key block: zero gradients for its keys
+                // (beyond kv_len; packed: a sequence with keys but no queries)
+                if (VARLEN ? key < I.kvl : key < nkeys) {
                     float z[32];
 #pragma unroll
                     for (int e = 0; e < 32; ++e) z[e] = 0.f;
@@ -554,7 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ld32_wait(tmem + lane_off + C::s_col(slot) + h * C::HALF, *reinterpret_cast<uint32_t(*)[32]>(sr));
                 else
                     tmem_ld64_wait(tmem + lane_off + C::s_col(slot) + h * C::HALF, *reinterpret_cast<uint32_t(*)[64]>(sr));
-                const int coff = causal_offset(p);  // 0 unless rectangular
+                const int coff = VARLEN ? I.coff : causal_offset(p);  // 0 unless rectangular / packed q != k
                 bool need_mask = (I.kt * C::BC + C::BC > I.kvl) || (CAUSAL && I.kt * C::BC + C::BC - 1 > i * C::BR + coff);
                 if constexpr (WINDOW)  // some pair of the tile outside the window
                     need_mask = need_mask || (p.win_right >= 0 && I.kt * C::BC + C::BC - 1 > i * C::BR + p.win_right) ||
@@ -654,7 +663,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float f[32];
 #pragma unroll
                 for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(a[e]) * mul;
-                if (key < (VARLEN ? I.seqlen : nkeys)) {
+                if (key < (VARLEN ? I.kvl : nkeys)) {
                     if (to_part)
                         store_chunk32<true>(part, krow * C::D + c, f);
                     else

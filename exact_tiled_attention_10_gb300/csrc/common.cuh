@@ -78,7 +78,10 @@ struct FwdParams {
     void* o;          // [B,H,N,d] bf16 or f32
     float* lse;       // [B,H,N]
     const float* sq;  // FP8 only: per-64-row-block scales [B,H,nblk]
-    const float* sk;
+    union {
+        const float* sk;
+        const int* cu_seqlens_k;  // VARLEN: [B + 1] key token ranges, or NULL (= cu_seqlens)
+    };
     const float* sv;
     union {
         int nblk;     // ceil(N / 64) (FP8)
@@ -94,7 +97,10 @@ struct BwdParams {
     int num_items;    // B * Hkv * num_kt
     float scale;
     float scale_log2;
-    const int* kv_lens;
+    union {
+        const int* kv_lens;
+        const int* cu_seqlens_k;  // packed: [B + 1] key token ranges, or NULL (= cu_seqlens)
+    };
     const float* lse2;  // [B,H,Np] LSE * log2(e), +inf on rows with no visible key / padding
     const float* dvec;  // [B,H,Np] D = rowsum(dO * O)
     float* dq_acc;      // [B,H,Np,d] float32 accumulator (unscaled)

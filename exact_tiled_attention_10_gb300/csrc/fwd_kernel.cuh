@@ -144,6 +144,7 @@ struct Item {
 // and three more fields cost several percent.)
 struct ItemPacked : Item {
     int h, tb, seqlen;
+    int tbk, coff;  // first key token; causal offset (keys - queries) of the sequence
 };
 
 // Sliding window: each query tile has its own first key block, a[t] blocks
@@ -241,7 +242,7 @@ __device__ __forceinline__ void q_coords(const IT& I, int r, int& y, int& z) {
 // TMA coordinates of key / value row r.
 template <class IT>
 __device__ __forceinline__ void kv_coords(const IT& I, int r, const FwdParams& p, int& y, int& z) {
-    if constexpr (is_packed<IT>()) { y = I.h / (p.H / p.Hkv); z = I.tb + r; }
+    if constexpr (is_packed<IT>()) { y = I.h / (p.H / p.Hkv); z = I.tbk + r; }
     else { y = r; z = I.kvh; }
 }
 
@@ -290,6 +291,13 @@ __device__ __forceinline__ ItemT<VARLEN, WINDOW, SPARSE> get_item(int unit, cons
         I.tb = a;
         I.seqlen = max(0, min(e - a, p.N));
         kvl = rows = I.seqlen;
+        I.tbk = a;
+        I.coff = 0;
+        if (p.cu_seqlens_k) {  // its own key range; causal: the queries are the last len_q positions
+            I.tbk = __ldg(p.cu_seqlens_k + I.b);
+            kvl = max(0, __ldg(p.cu_seqlens_k + I.b + 1) - I.tbk);
+            I.coff = kvl - rows;
+        }
     } else if constexpr (RECT) {
         rows = p.N;
         kvl = p.Nk;
@@ -370,6 +378,8 @@ __device__ __forceinline__ ItemT<VARLEN, WINDOW, SPARSE> get_item(int unit, cons
                     const int rl = min(r0 + C::BR, rows) - 1;
                     const int qmax = (rl / p.qmod != r0 / p.qmod) ? p.qmod - 1 : rl % p.qmod;
                     if (CAUSAL) cols = min(cols, max(0, qmax + 1 + p.coff));
+                } else if constexpr (VARLEN) {
+                    if (CAUSAL) cols = min(cols, max(0, r0 + C::BR + I.coff));
                 } else {
                     if (CAUSAL) cols = min(cols, r0 + C::BR);
                 }
@@ -897,6 +907,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if constexpr (SPARSE) col0 = __ldg(p.col_idx + (t ? I.off[1] : I.off[0]) + j) * C::BC;
                 // causal limit of a row: its query index (+ the rectangular offset)
                 int coff = 0, qmin = tile_row0, qrow = row;
+                if constexpr (VARLEN) coff = I.coff;
                 if constexpr (RECT) {
                     const int rl = tile_row0 + C::BR - 1;
                     coff = p.coff;

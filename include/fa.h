@@ -229,6 +229,21 @@ fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, fl
                         const int* cu_seqlens, int batch, int total, int max_seqlen, int H, int Hkv,
                         int d, float scale, int causal, fa_stream_t stream);
 
+/* Packed sequences with their own key ranges (flash_attn_varlen_func's
+ * cu_seqlens_q / cu_seqlens_k, [CH18] §18.7.1), bf16: sequence b has queries
+ * cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 of q, o [total_q, H, d] and keys
+ * cu_seqlens_k[b] .. cu_seqlens_k[b+1]-1 of k, v [total_k, Hkv, d]; lse
+ * float32 [H, total_q].  With causal, the queries of a sequence are its last
+ * len_q positions: query i sees keys j <= i + len_k - len_q (as in
+ * fa_fwd_rect); a query that sees no key gets O = 0, LSE = -inf.
+ * max_seqlen_q >= every query length (longer sequences are cut); key
+ * lengths are taken as given.  Same results as fa_fwd_rect on each sequence
+ * alone. */
+fa_status fa_fwd_varlen_kv(const void* q, const void* k, const void* v, void* o, float* lse,
+                           const int* cu_seqlens_q, const int* cu_seqlens_k, int batch,
+                           int total_q, int total_k, int max_seqlen_q, int H, int Hkv, int d,
+                           float scale, int causal, fa_stream_t stream);
+
 /* Forward on flash_attn_func's own layout ([CH18] §18.7.1: q is (batch,
  * seqlen, nheads, headdim), k and v (batch, seqlen_k, nheads_k, headdim)),
  * bf16: q, o [B, N, H, d]; k, v [B, N, Hkv, d]; lse float32 [B, H, N].  Same
@@ -336,6 +351,20 @@ fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const void*
                         const int* cu_seqlens, int batch, int total, int max_seqlen, int H,
                         int Hkv, int d, float scale, int causal, void* workspace,
                         size_t workspace_bytes, fa_stream_t stream);
+
+/* Backward of fa_fwd_varlen_kv, bf16: dq [total_q, H, d]; dk, dv [total_k,
+ * Hkv, d] (summed over the query heads sharing a key/value head).
+ * deterministic != 0 gives bitwise-repeatable results (see
+ * fa_bwd_deterministic).  max_seqlen_k >= every key length.  Workspace:
+ * fa_bwd_varlen_kv_workspace_size(..., deterministic) bytes. */
+size_t fa_bwd_varlen_kv_workspace_size(int batch, int max_seqlen_q, int max_seqlen_k, int H, int Hkv,
+                                       int d, int deterministic);
+fa_status fa_bwd_varlen_kv(const void* q, const void* k, const void* v, const void* o,
+                           const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                           const int* cu_seqlens_q, const int* cu_seqlens_k, int batch,
+                           int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int H,
+                           int Hkv, int d, float scale, int causal, int deterministic,
+                           void* workspace, size_t workspace_bytes, fa_stream_t stream);
 
 /* Backward of fa_fwd_bnhd, bf16: dq [B, N, H, d]; dk, dv [B, N, Hkv, d]
  * (summed over the query heads sharing a key/value head); o, lse, dout as

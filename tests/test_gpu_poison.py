@@ -149,3 +149,18 @@ def test_fp8_quantiser_and_forward(monkeypatch):
     q8, sq, k8, sk, v8, sv = _run_both(monkeypatch,
                                        lambda: tuple(t for pair in fa.quantize_fp8_qkv(q, k, v) for t in pair))
     _run_both(monkeypatch, lambda: fa.forward_fp8(q8, k8, v8, sq, sk, sv))
+
+
+def test_varlen_separate_key_ranges(monkeypatch):
+    """Separate query / key ranges, one sequence with keys but no queries:
+    its dK, dV rows must be written (zero)."""
+    lens_q, lens_k = [130, 0, 77], [60, 50, 200]
+    cuq = torch.tensor([0, 130, 130, 207], dtype=torch.int32, device=DEV)
+    cuk = torch.tensor([0, 60, 110, 310], dtype=torch.int32, device=DEV)
+    q, do = (randn((207, 4, 128), 41 + i, device=DEV) for i in range(2))
+    k, v = (randn((310, 2, 128), 43 + i, device=DEV) for i in range(2))
+    o, lse = _run_both(monkeypatch, lambda: fa.forward_varlen(q, k, v, cuq, 130, causal=True, cu_seqlens_k=cuk))
+    dq, dk, dv = _run_both(monkeypatch, lambda: fa.backward_varlen(q, k, v, o, lse, do, cuq, 130, causal=True,
+                                                                   cu_seqlens_k=cuk, max_seqlen_k=200,
+                                                                   deterministic=True))
+    assert (dk[60:110] == 0).all() and (dv[60:110] == 0).all()

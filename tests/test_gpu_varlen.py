@@ -78,3 +78,64 @@ def test_varlen_deterministic_matches_oracle(d, causal):
     """The deterministic backward of packed sequences (flash_attn_varlen_func's
     deterministic flag) against the same per-sequence oracle."""
     _case([300, 1, 0, 129, 520, 64], 4, 2, d, causal, seed=91 + d, deterministic=True)
+
+
+def _case_kv(lens_q, lens_k, H, Hkv, d, causal, seed, deterministic=False):
+    """Separate query and key ranges (flash_attn_varlen_func's cu_seqlens_q /
+    cu_seqlens_k): each sequence against the oracle's rectangular forward and
+    backward (chapter 18 §18.8.2 reading: the queries are the last len_q
+    positions under the causal mask)."""
+    Tq, Tk = int(sum(lens_q)), int(sum(lens_k))
+    cuq = torch.tensor(np.concatenate([[0], np.cumsum(lens_q)]), dtype=torch.int32, device=DEV)
+    cuk = torch.tensor(np.concatenate([[0], np.cumsum(lens_k)]), dtype=torch.int32, device=DEV)
+    q = randn((Tq, H, d), seed, device=DEV)
+    k = randn((Tk, Hkv, d), seed + 1, device=DEV)
+    v = randn((Tk, Hkv, d), seed + 2, device=DEV)
+    do = randn((Tq, H, d), seed + 3, device=DEV)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = forward_varlen(q, k, v, cuq, max(lens_q), causal=causal, scale=scale, cu_seqlens_k=cuk)
+    dq, dk, dv = backward_varlen(q, k, v, o, lse, do, cuq, max(lens_q), causal=causal, scale=scale,
+                                 deterministic=deterministic, cu_seqlens_k=cuk, max_seqlen_k=max(lens_k))
+    torch.cuda.synchronize()
+    check_device_status()
+    if deterministic:
+        again = backward_varlen(q, k, v, o, lse, do, cuq, max(lens_q), causal=causal, scale=scale,
+                                deterministic=True, cu_seqlens_k=cuk, max_seqlen_k=max(lens_k))
+        torch.cuda.synchronize()
+        for a, b in zip((dq, dk, dv), again):
+            assert torch.equal(a, b)
+    g = H // Hkv
+    ref = {"o": np.zeros((Tq, H, d)), "dq": np.zeros((Tq, H, d)), "dk": np.zeros((Tk, Hkv, d)),
+           "dv": np.zeros((Tk, Hkv, d))}
+    ref_lse = np.full((H, Tq), -np.inf)
+    aq = ak = 0
+    for nq, nk in zip(lens_q, lens_k):
+        sq, sk = slice(aq, aq + nq), slice(ak, ak + nk)
+        if nq > 0 and nk > 0:
+            per = lambda t, sl, rep: np.repeat(to64(t[sl]).transpose(1, 0, 2)[None], rep, axis=1)
+            ro, rl = oracle.fwd_rect(per(q, sq, 1), per(k, sk, g), per(v, sk, g), scale, causal=causal)
+            r = oracle.bwd_rect(per(q, sq, 1), per(k, sk, g), per(v, sk, g), per(do, sq, 1), scale, causal=causal)
+            ref["o"][sq] = ro[0].transpose(1, 0, 2)
+            ref_lse[:, sq] = rl[0]
+            ref["dq"][sq] = r["dq"][0].transpose(1, 0, 2)
+            ref["dk"][sk] = r["dk"][0].reshape(Hkv, g, nk, d).sum(axis=1).transpose(1, 0, 2)
+            ref["dv"][sk] = r["dv"][0].reshape(Hkv, g, nk, d).sum(axis=1).transpose(1, 0, 2)
+        aq += nq
+        ak += nk
+    assert_close_abs(to64(o), ref["o"], O_TOL, "O")
+    assert_lse(to64(lse), ref_lse)
+    assert_grad(to64(dq), ref["dq"], "dQ")
+    assert_grad(to64(dk), ref["dk"], "dK")
+    assert_grad(to64(dv), ref["dv"], "dV")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_separate_key_ranges(d, causal):
+    # more queries than keys, one query against many keys, an empty key range, an empty query range
+    _case_kv([300, 1, 130, 0, 77], [200, 900, 0, 50, 301], 4, 2, d, causal, seed=131 + d)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_separate_key_ranges_deterministic(causal):
+    _case_kv([500, 129, 64], [700, 129, 1000], 4, 1, 128, causal, seed=141, deterministic=True)
