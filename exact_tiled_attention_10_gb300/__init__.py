@@ -78,6 +78,7 @@ _SIGS = {
     "fa_bwd_varlen": ([_vp] * 10 + [_i, _i, _i, _i, _i, _i, _f, _i, _vp, _sz, _vp], _i),
     "fa_fwd_bnhd": ([_vp] * 5 + [_i, _i, _i, _i, _i, _f, _i, _vp], _i),
     "fa_fwd_varlen_kv": ([_vp] * 7 + [_i] * 7 + [_f, _i, _vp], _i),
+    "fa_fwd_fp8_gqa": ([_vp] * 8 + [_i] * 5 + [_f, _i, _vp, _vp], _i),
     "fa_bwd_varlen_kv_workspace_size": ([_i] * 7, _sz),
     "fa_bwd_varlen_kv": ([_vp] * 11 + [_i] * 8 + [_f, _i, _i, _vp, _sz, _vp], _i),
     "fa_bwd_bnhd_workspace_size": ([_i] * 4, _sz),
@@ -600,14 +601,20 @@ def quantize_fp8_qkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor):
 
 def forward_fp8(q8, k8, v8, sq, sk, sv, causal: bool = False, scale: Optional[float] = None,
                 kv_lens=None, out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None):
-    """FP8 E4M3 forward with per-64-row-block scales; O bf16, LSE float32."""
+    """FP8 E4M3 forward with per-64-row-block scales; O bf16, LSE float32.
+    k8, v8 may have fewer heads (shared key/value heads)."""
     lib = load_library()
     _need_cuda(q8, k8, v8, sq, sk, sv)
     B, H, N, d = q8.shape
+    Hkv = k8.shape[1]
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     kv = _kv(kv_lens, B, q8.device)
     o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q8.device) if out is None else out
     l = torch.empty((B, H, N), dtype=torch.float32, device=q8.device) if lse is None else lse
+    if Hkv != H:
+        _check(lib.fa_fwd_fp8_gqa(_ptr(q8), _ptr(k8), _ptr(v8), _ptr(sq), _ptr(sk), _ptr(sv), _ptr(o),
+                                  _ptr(l), B, H, Hkv, N, d, scale, int(bool(causal)), _ptr(kv), _stream(q8)))
+        return o, l
     _check(lib.fa_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(v8), _ptr(sq), _ptr(sk), _ptr(sv), _ptr(o),
                           _ptr(l), B, H, N, d, scale, int(bool(causal)), _ptr(kv), _stream(q8)))
     return o, l

@@ -1424,6 +1424,13 @@ fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* v8, const float
                     stream);
 }
 
+fa_status fa_fwd_fp8_gqa(const void* q8, const void* k8, const void* v8, const float* sq, const float* sk,
+                         const float* sv, void* o, float* lse, int B, int H, int Hkv, int N, int d, float scale,
+                         int causal, const int* kv_lens, fa_stream_t stream) {
+    return fwd_impl(FA_BF16, 128, true, q8, k8, v8, sq, sk, sv, o, lse, B, H, N, d, scale, causal, kv_lens, nullptr, 0,
+                    stream, 1, nullptr, 0, Hkv);
+}
+
 fa_status fa_fwd_fp8_split(const void* q8, const void* k8, const void* v8, const float* sq, const float* sk,
                            const float* sv, void* o, float* lse, int B, int H, int N, int d, float scale, int causal,
                            const int* kv_lens, int num_splits, void* workspace, size_t workspace_bytes,

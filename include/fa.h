@@ -509,6 +509,14 @@ fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* v8,
                      void* o, float* lse, int B, int H, int N, int d, float scale,
                      int causal, const int* kv_lens, fa_stream_t stream);
 
+/* FP8 forward with shared key/value heads (see fa_fwd_gqa): q8, sq for H
+ * query heads; k8, v8 [B,Hkv,N,d] and sk, sv [B,Hkv,ceil(N/64)] for Hkv key /
+ * value heads, as fa_quantize_fp8_qkv writes them; H % Hkv == 0. */
+fa_status fa_fwd_fp8_gqa(const void* q8, const void* k8, const void* v8,
+                         const float* sq, const float* sk, const float* sv,
+                         void* o, float* lse, int B, int H, int Hkv, int N, int d, float scale,
+                         int causal, const int* kv_lens, fa_stream_t stream);
+
 /* Split-key FP8 forward: fa_fwd_fp8 with the key ranges and merge of
  * fa_fwd_split (same num_splits and workspace rules; d = 128). */
 fa_status fa_fwd_fp8_split(const void* q8, const void* k8, const void* v8,

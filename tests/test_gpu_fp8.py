@@ -15,8 +15,8 @@ import pytest
 import torch
 
 import oracle
-from exact_tiled_attention_10_gb300 import check_device_status, forward_fp8, quantize_fp8
-from exact_tiled_attention_10_gb300.inputs import WORKLOADS, kv_lens_ragged, qkv
+from exact_tiled_attention_10_gb300 import check_device_status, forward_fp8, quantize_fp8, quantize_fp8_qkv
+from exact_tiled_attention_10_gb300.inputs import WORKLOADS, kv_lens_ragged, qkv, randn
 from parity_util import FP8_O_TOL, assert_close_abs, assert_lse, sample_rows, to64
 
 pytestmark = pytest.mark.gpu
@@ -169,3 +169,35 @@ def test_fp8_long_seq_config_sampled():
         ref_o, ref_l = oracle.fwd_rows(to64(q[0, h]), to64(k[0, h]), to64(v[0, h]), w.scale, False,
                                        w.N, rows)
         assert_close_abs(to64(o[0, h, rows]), ref_o, FP8_O_TOL, "FP8 O[0,%d]" % h)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Hkv", [1, 2])
+def test_fp8_forward_shared_kv_heads(causal, Hkv):
+    """FP8 forward with fewer key/value heads (quantised together with
+    fa_quantize_fp8_qkv): bitwise the same O and LSE as the FP8 forward on
+    explicitly repeated codes and scales, and, against the oracle on the
+    dequantised inputs (key/value heads broadcast), O within the E4M3
+    probability-rounding bound and LSE within its tolerance."""
+    B, H, N = 2, 4, 300
+    kv = [N, 117]
+    q = randn((B, H, N, 128), 151, device=DEV)
+    k = randn((B, Hkv, N, 128), 152, device=DEV)
+    v = randn((B, Hkv, N, 128), 153, device=DEV)
+    (q8, sq), (k8, sk), (v8, sv) = quantize_fp8_qkv(q, k, v)
+    kvd = torch.tensor(kv, dtype=torch.int32, device=DEV)
+    o, lse = forward_fp8(q8, k8, v8, sq, sk, sv, causal=causal, kv_lens=kvd)
+    g = H // Hkv
+    rep = lambda t: t.repeat_interleave(g, dim=1).contiguous()
+    o_rep, lse_rep = forward_fp8(q8, rep(k8), rep(v8), sq, rep(sk), rep(sv), causal=causal, kv_lens=kvd)
+    torch.cuda.synchronize()
+    check_device_status()
+    assert torch.equal(o, o_rep) and torch.equal(lse, lse_rep)
+    dq = oracle.dequantize_fp8(q8.cpu().numpy(), sq.cpu().numpy())
+    dk = np.repeat(oracle.dequantize_fp8(k8.cpu().numpy(), sk.cpu().numpy()), g, axis=1)
+    dv = np.repeat(oracle.dequantize_fp8(v8.cpu().numpy(), sv.cpu().numpy()), g, axis=1)
+    ref_o, ref_l = oracle.fwd(dq, dk, dv, 1 / math.sqrt(128), causal=causal, kv_lens=np.array(kv, dtype=np.int32))
+    bound = p_rounding_bound(dq, dk, dv, ref_o, ref_l, causal, kv)
+    excess = np.abs(to64(o) - ref_o) - bound
+    assert np.all(excess <= 0), "FP8 O exceeds the E4M3 probability-rounding bound by %.3e" % excess.max()
+    assert_lse(to64(lse), ref_l, what="FP8 LSE (dequantised reference)")
