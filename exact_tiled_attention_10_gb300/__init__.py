@@ -79,6 +79,8 @@ _SIGS = {
     "fa_fwd_bnhd": ([_vp] * 5 + [_i, _i, _i, _i, _i, _f, _i, _vp], _i),
     "fa_fwd_varlen_kv": ([_vp] * 7 + [_i] * 7 + [_f, _i, _vp], _i),
     "fa_fwd_fp8_gqa": ([_vp] * 8 + [_i] * 5 + [_f, _i, _vp, _vp], _i),
+    "fa_fwd_varlen_window": ([_vp] * 6 + [_i] * 6 + [_f, _i, _i, _i, _vp], _i),
+    "fa_bwd_varlen_window": ([_vp] * 10 + [_i] * 6 + [_f, _i, _i, _i, _vp, _sz, _vp], _i),
     "fa_bwd_varlen_kv_workspace_size": ([_i] * 7, _sz),
     "fa_bwd_varlen_kv": ([_vp] * 11 + [_i] * 8 + [_f, _i, _i, _vp, _sz, _vp], _i),
     "fa_bwd_bnhd_workspace_size": ([_i] * 4, _sz),
@@ -389,12 +391,14 @@ def _cu(cu_seqlens, device):
 
 def forward_varlen(q, k, v, cu_seqlens, max_seqlen: int, causal: bool = False,
                    scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
-                   lse: Optional[torch.Tensor] = None, cu_seqlens_k=None) -> Tuple[torch.Tensor, torch.Tensor]:
+                   lse: Optional[torch.Tensor] = None, cu_seqlens_k=None,
+                   window: Optional[Tuple[int, int]] = None) -> Tuple[torch.Tensor, torch.Tensor]:
     """Packed variable-length forward: q [total, H, d], k, v [total, Hkv, d]
     (bf16), sequence b = tokens cu_seqlens[b] .. cu_seqlens[b+1]-1.  Returns
     O [total, H, d] and LSE [H, total].  cu_seqlens_k: the sequences' own key
     ranges in k, v [total_k, Hkv, d] (flash_attn_varlen_func's cu_seqlens_k;
-    with causal, the queries are each sequence's last positions)."""
+    with causal, the queries are each sequence's last positions).  window:
+    the sliding window (see forward), within each sequence."""
     lib = load_library()
     _need_cuda(q, k, v)
     T, H, d = q.shape
@@ -407,6 +411,11 @@ def forward_varlen(q, k, v, cu_seqlens, max_seqlen: int, causal: bool = False,
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     o = torch.empty_like(q) if out is None else out
     l = torch.empty((H, T), dtype=torch.float32, device=q.device) if lse is None else lse
+    wl, wr = _window(window)
+    if wl >= 0 or wr >= 0:
+        _check(lib.fa_fwd_varlen_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(l), _ptr(cu), cu.numel() - 1, T,
+                                        int(max_seqlen), H, Hkv, d, scale, int(bool(causal)), wl, wr, _stream(q)))
+        return o, l
     if cu_seqlens_k is not None:
         cuk = _cu(cu_seqlens_k, q.device)
         _check(lib.fa_fwd_varlen_kv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(l), _ptr(cu), _ptr(cuk), cu.numel() - 1,
@@ -465,7 +474,8 @@ def backward_bnhd(q, k, v, o, lse, dout, causal: bool = False, scale: Optional[f
 
 def backward_varlen(q, k, v, o, lse, dout, cu_seqlens, max_seqlen: int, causal: bool = False,
                     scale: Optional[float] = None, workspace: Optional[torch.Tensor] = None,
-                    deterministic: bool = False, cu_seqlens_k=None, max_seqlen_k: Optional[int] = None):
+                    deterministic: bool = False, cu_seqlens_k=None, max_seqlen_k: Optional[int] = None,
+                    window: Optional[Tuple[int, int]] = None):
     """Backward of forward_varlen: dQ [total, H, d], dK, dV [total(_k), Hkv, d].
     deterministic: bitwise reproducible gradients (see backward).
     cu_seqlens_k / max_seqlen_k: separate key ranges (see forward_varlen)."""
@@ -476,6 +486,18 @@ def backward_varlen(q, k, v, o, lse, dout, cu_seqlens, max_seqlen: int, causal: 
     cu = _cu(cu_seqlens, q.device)
     batch = cu.numel() - 1
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    wl, wr = _window(window)
+    if wl >= 0 or wr >= 0:
+        wsz = int(lib.fa_bwd_varlen_workspace_size(batch, int(max_seqlen), H, d))
+        ws = workspace
+        if ws is None or ws.numel() * ws.element_size() < wsz:
+            ws = torch.empty(wsz, dtype=torch.uint8, device=q.device)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        _check(lib.fa_bwd_varlen_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
+                                        _ptr(dk), _ptr(dv), _ptr(cu), batch, T, int(max_seqlen), H, Hkv, d, scale,
+                                        int(bool(causal)), wl, wr, _ptr(ws), ws.numel() * ws.element_size(),
+                                        _stream(q)))
+        return dq, dk, dv
     if cu_seqlens_k is not None:
         cuk = _cu(cu_seqlens_k, q.device)
         mk = int(max_seqlen if max_seqlen_k is None else max_seqlen_k)

@@ -573,8 +573,12 @@ namespace {
 // each (the [B, N, H, d] layout, LSE [B, H, N]).
 fa_status fwd_packed_impl(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens,
                           int batch, int total, int max_seqlen, int H, int Hkv, int d, float scale, int causal,
-                          fa_stream_t stream, const int* cu_seqlens_k = nullptr, int total_k = -1) {
+                          fa_stream_t stream, const int* cu_seqlens_k = nullptr, int total_k = -1,
+                          int win_left = -1, int win_right = -1) {
     if (total_k < 0) total_k = total;
+    if (win_left < -1 || win_right < -1) return fail(FA_ERR_INVALID_ARG, "window edges must be >= -1");
+    const bool window = win_left >= 0 || win_right >= 0;
+    if (window && cu_seqlens_k) return fail(FA_ERR_UNSUPPORTED, "the sliding window needs one range per sequence");
     if (total_k <= 0) return fail(FA_ERR_INVALID_ARG, "total_k must be positive");
     FA_TRY(check_common(batch, H, max_seqlen, d, scale));
     if (total <= 0) return fail(FA_ERR_INVALID_ARG, "total must be positive");
@@ -607,7 +611,17 @@ fa_status fwd_packed_impl(const void* q, const void* k, const void* v, void* o, 
     p.cu_seqlens_k = cu_seqlens_k;
     p.total = total;
     p.err = dev->err_word;
-    cudaError_t e = fa::launch_fwd_varlen(d, causal != 0, m, p, grid_for_items(p.num_items, dev->sms), stream);
+    cudaError_t e;
+    if (window) {  // causal = the window's right edge at 0
+        fa::FwdParamsWin pw;
+        memset(&pw, 0, sizeof(pw));
+        static_cast<fa::FwdParams&>(pw) = p;
+        pw.win_left = win_left;
+        pw.win_right = causal ? 0 : win_right;
+        e = fa::launch_fwd_varlen_window(d, m, pw, grid_for_items(p.num_items, dev->sms), stream);
+    } else {
+        e = fa::launch_fwd_varlen(d, causal != 0, m, p, grid_for_items(p.num_items, dev->sms), stream);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "varlen forward launch");
     return FA_OK;
 }
@@ -621,6 +635,14 @@ fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, fl
                         fa_stream_t stream) {
     if (!cu_seqlens) return fail(FA_ERR_INVALID_ARG, "cu_seqlens must not be NULL");
     return fwd_packed_impl(q, k, v, o, lse, cu_seqlens, batch, total, max_seqlen, H, Hkv, d, scale, causal, stream);
+}
+
+fa_status fa_fwd_varlen_window(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens,
+                               int batch, int total, int max_seqlen, int H, int Hkv, int d, float scale, int causal,
+                               int window_left, int window_right, fa_stream_t stream) {
+    if (!cu_seqlens) return fail(FA_ERR_INVALID_ARG, "cu_seqlens must not be NULL");
+    return fwd_packed_impl(q, k, v, o, lse, cu_seqlens, batch, total, max_seqlen, H, Hkv, d, scale, causal, stream,
+                           nullptr, -1, window_left, window_right);
 }
 
 fa_status fa_fwd_varlen_kv(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens_q,
@@ -1102,8 +1124,13 @@ fa_status bwd_packed_impl(const void* q, const void* k, const void* v, const voi
                           const void* dout, void* dq, void* dk, void* dv, const int* cu_seqlens, int batch, int total,
                           int max_seqlen, int H, int Hkv, int d, float scale, int causal, void* workspace,
                           size_t workspace_bytes, fa_stream_t stream, bool det = false,
-                          const int* cu_seqlens_k = nullptr, int total_k = -1, int max_seqlen_k = -1) {
+                          const int* cu_seqlens_k = nullptr, int total_k = -1, int max_seqlen_k = -1,
+                          int win_left = -1, int win_right = -1) {
     if (total_k < 0) total_k = total;
+    if (win_left < -1 || win_right < -1) return fail(FA_ERR_INVALID_ARG, "window edges must be >= -1");
+    const bool window = win_left >= 0 || win_right >= 0;
+    if (window && (cu_seqlens_k || det))
+        return fail(FA_ERR_UNSUPPORTED, "the packed sliding window takes one range per sequence, not deterministic");
     if (max_seqlen_k < 0) max_seqlen_k = max_seqlen;
     if (total_k <= 0 || max_seqlen_k <= 0) return fail(FA_ERR_INVALID_ARG, "total_k and max_seqlen_k must be positive");
     FA_TRY(check_common(batch, H, max_seqlen, d, scale));
@@ -1180,8 +1207,18 @@ fa_status bwd_packed_impl(const void* q, const void* k, const void* v, const voi
         if (e != cudaSuccess) return cuda_fail(e, "varlen dQ conversion launch");
         return FA_OK;
     }
-    e = fa::launch_bwd_main_varlen(d, causal != 0, tq, tk, tv, tdo, tdq, p, grid_for_items(p.num_items, dev->sms),
-                                   stream);
+    if (window) {  // causal = the window's right edge at 0
+        fa::BwdParamsWin pw;
+        memset(&pw, 0, sizeof(pw));
+        static_cast<fa::BwdParams&>(pw) = p;
+        pw.win_left = win_left;
+        pw.win_right = causal ? 0 : win_right;
+        e = fa::launch_bwd_main_varlen_window(d, tq, tk, tv, tdo, tdq, pw, grid_for_items(p.num_items, dev->sms),
+                                              stream);
+    } else {
+        e = fa::launch_bwd_main_varlen(d, causal != 0, tq, tk, tv, tdo, tdq, p, grid_for_items(p.num_items, dev->sms),
+                                       stream);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "varlen backward launch");
     e = fa::launch_bwd_dq_varlen(dqacc, cu_seqlens, dq, scale, H, batch, max_seqlen, MSp, d, bw_grid(dev), stream);
     if (e != cudaSuccess) return cuda_fail(e, "varlen dQ conversion launch");
@@ -1202,6 +1239,17 @@ fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const void*
 }
 
 size_t fa_bwd_bnhd_workspace_size(int B, int N, int H, int d) { return fa_bwd_varlen_workspace_size(B, N, H, d); }
+
+fa_status fa_bwd_varlen_window(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                               const void* dout, void* dq, void* dk, void* dv, const int* cu_seqlens, int batch,
+                               int total, int max_seqlen, int H, int Hkv, int d, float scale, int causal,
+                               int window_left, int window_right, void* workspace, size_t workspace_bytes,
+                               fa_stream_t stream) {
+    if (!cu_seqlens) return fail(FA_ERR_INVALID_ARG, "cu_seqlens must not be NULL");
+    return bwd_packed_impl(q, k, v, o, lse, dout, dq, dk, dv, cu_seqlens, batch, total, max_seqlen, H, Hkv, d, scale,
+                           causal, workspace, workspace_bytes, stream, false, nullptr, -1, -1, window_left,
+                           window_right);
+}
 
 size_t fa_bwd_varlen_kv_workspace_size(int batch, int max_seqlen_q, int max_seqlen_k, int H, int Hkv, int d,
                                        int deterministic) {

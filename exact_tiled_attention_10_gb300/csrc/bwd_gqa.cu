@@ -29,6 +29,13 @@ cudaError_t launch_bwd_main_varlen(int d, bool causal, const CUtensorMap& tq, co
                   : bwd::launch<C64, false, false, true, true>(tq, tk, tv, tdo, tdq, p, grid, s);
 }
 
+cudaError_t launch_bwd_main_varlen_window(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                          const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParamsWin& p,
+                                          int grid, cudaStream_t s) {
+    if (d == 128) return bwd::launch<bwd::Cfg<128>, false, false, true, true, true>(tq, tk, tv, tdo, tdq, p, grid, s);
+    return bwd::launch<bwd::Cfg<64>, false, false, true, true, true>(tq, tk, tv, tdo, tdq, p, grid, s);
+}
+
 cudaError_t launch_bwd_main_window(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                    const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParamsWin& p, int grid,
                                    cudaStream_t s) {

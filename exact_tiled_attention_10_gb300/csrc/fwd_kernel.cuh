@@ -153,6 +153,10 @@ struct ItemPacked : Item {
 struct ItemWin : Item {
     int a[2];
 };
+// Packed sequences under a sliding window.
+struct ItemPackedWin : ItemPacked {
+    int a[2];
+};
 
 // Block-sparse: tile t computes the key blocks col_idx[off[t] .. off[t] +
 // n[t] - 1]; the K / V stream is the ascending union of the two lists (nmax
@@ -163,7 +167,7 @@ struct ItemSparse : Item {
 
 template <bool VARLEN, bool WINDOW = false, bool SPARSE = false>
 using ItemT = typename std::conditional<
-    VARLEN, ItemPacked,
+    VARLEN, typename std::conditional<WINDOW, ItemPackedWin, ItemPacked>::type,
     typename std::conditional<WINDOW, ItemWin, typename std::conditional<SPARSE, ItemSparse, Item>::type>::type>::type;
 
 template <bool WINDOW, bool SPARSE = false, bool RECT = false>
@@ -202,9 +206,11 @@ __device__ __forceinline__ BlockMerge block_merge(const ItemSparse& I, const Fwd
 }
 
 template <class IT>
-__host__ __device__ constexpr bool is_packed() { return std::is_same<IT, ItemPacked>::value; }
+__host__ __device__ constexpr bool is_packed() { return std::is_base_of<ItemPacked, IT>::value; }
 template <class IT>
-__host__ __device__ constexpr bool is_window() { return std::is_same<IT, ItemWin>::value; }
+__host__ __device__ constexpr bool is_window() {
+    return std::is_same<IT, ItemWin>::value || std::is_same<IT, ItemPackedWin>::value;
+}
 template <class IT>
 __host__ __device__ constexpr bool is_sparse() { return std::is_same<IT, ItemSparse>::value; }
 
@@ -1049,6 +1055,11 @@ cudaError_t launch_sparse(bool causal, const FwdMaps& m, const FwdParamsSparse& 
 template <class C>
 cudaError_t launch_window(const FwdMaps& m, const FwdParamsWin& p, int grid, cudaStream_t s) {
     return launch<C, false, false, false, false, true>(m, p, grid, s);
+}
+
+template <class C>
+cudaError_t launch_varlen_window(const FwdMaps& m, const FwdParamsWin& p, int grid, cudaStream_t s) {
+    return launch<C, false, false, false, true, true>(m, p, grid, s);
 }
 
 template <class C>

@@ -15,13 +15,13 @@ import torch
 import oracle
 from exact_tiled_attention_10_gb300 import backward_varlen, check_device_status, forward_varlen
 from exact_tiled_attention_10_gb300.inputs import randn
-from parity_util import O_TOL, assert_close_abs, assert_grad, assert_lse, to64
+from parity_util import O_TOL, assert_close_abs, assert_grad, assert_lse, assert_o_bf16, to64
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-def _case(lens, H, Hkv, d, causal, seed, deterministic=False):
+def _case(lens, H, Hkv, d, causal, seed, deterministic=False, window=None):
     T = int(sum(lens))
     cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32, device=DEV)
     q = randn((T, H, d), seed, device=DEV)
@@ -29,9 +29,9 @@ def _case(lens, H, Hkv, d, causal, seed, deterministic=False):
     v = randn((T, Hkv, d), seed + 2, device=DEV)
     do = randn((T, H, d), seed + 3, device=DEV)
     scale = 1.0 / math.sqrt(d)
-    o, lse = forward_varlen(q, k, v, cu, max(lens), causal=causal, scale=scale)
+    o, lse = forward_varlen(q, k, v, cu, max(lens), causal=causal, scale=scale, window=window)
     dq, dk, dv = backward_varlen(q, k, v, o, lse, do, cu, max(lens), causal=causal, scale=scale,
-                                 deterministic=deterministic)
+                                 deterministic=deterministic, window=window)
     torch.cuda.synchronize()
     check_device_status()
     g = H // Hkv
@@ -43,18 +43,28 @@ def _case(lens, H, Hkv, d, causal, seed, deterministic=False):
         if n > 0:
             sl = slice(a, a + n)
             per = lambda t, rep: np.repeat(to64(t[sl]).transpose(1, 0, 2)[None], rep, axis=1)
-            r = oracle.bwd(per(q, 1), per(k, g), per(v, g), per(do, 1), scale, causal=causal)
+            r = oracle.bwd(per(q, 1), per(k, g), per(v, g), per(do, 1), scale, causal=causal, window=window)
             ref["o"][sl] = r["o"][0].transpose(1, 0, 2)
             ref["dq"][sl] = r["dq"][0].transpose(1, 0, 2)
             ref["dk"][sl] = r["dk"][0].reshape(Hkv, g, n, d).sum(axis=1).transpose(1, 0, 2)
             ref["dv"][sl] = r["dv"][0].reshape(Hkv, g, n, d).sum(axis=1).transpose(1, 0, 2)
             ref_lse[:, sl] = r["lse"][0]
         a += n
-    assert_close_abs(to64(o), ref["o"], O_TOL, "O")
+    if window is None:
+        assert_close_abs(to64(o), ref["o"], O_TOL, "O")
+    else:  # narrow windows: rows average a few value rows (see the window tests)
+        assert_o_bf16(to64(o), ref["o"])
     assert_lse(to64(lse), ref_lse)
     assert_grad(to64(dq), ref["dq"], "dQ")
     assert_grad(to64(dk), ref["dk"], "dK")
     assert_grad(to64(dv), ref["dv"], "dV")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal,window", [(True, (100, 0)), (False, (64, 37)), (False, (-1, 20)), (True, (300, -1))])
+def test_varlen_sliding_window(d, causal, window):
+    """flash_attn_varlen_func's window_size: the window within each sequence."""
+    _case([300, 1, 0, 129, 520, 64], 4, 2, d, causal, seed=151 + d + window[0], window=window)
 
 
 @pytest.mark.parametrize("d", [64, 128])
