@@ -148,6 +148,14 @@ def test_host_validation_of_the_variant_entry_points():
     assert lib.fa_fwd_bnhd(A, A, A, A, A, 1 << 16, 1 << 16, 4, 4, 128, 0.1, 0, None) == 1
     assert lib.fa_bwd_bnhd_workspace_size(2, 256, 4, 128) == lib.fa_bwd_varlen_workspace_size(2, 256, 4, 128) > 0
     assert lib.fa_bwd_bnhd(A, A, A, A, A, A, A, A, A, 2, 256, 4, 4, 128, 0.1, 0, A, 1024, None) == 1
+    # packed sliding window: bad edge; separate key ranges: missing offsets, a window with them
+    assert lib.fa_fwd_varlen_window(A, A, A, A, A, A, 2, 512, 256, 4, 4, 128, 0.1, 0, -2, 0, None) == 1
+    assert lib.fa_fwd_varlen_kv(A, A, A, A, A, A, None, 2, 512, 512, 256, 4, 4, 128, 0.1, 0, None) == 1
+    assert lib.fa_bwd_varlen_kv_workspace_size(2, 256, 300, 4, 3, 128, 0) == 0
+    assert (lib.fa_bwd_varlen_kv_workspace_size(2, 256, 300, 4, 2, 128, 1) >
+            lib.fa_bwd_varlen_kv_workspace_size(2, 256, 300, 4, 2, 128, 0) > 0)
+    # FP8 with shared heads: bad group
+    assert lib.fa_fwd_fp8_gqa(A, A, A, A, A, A, A, A, 1, 4, 3, 256, 128, 0.1, 0, None, None) == 1
     # deterministic packed / [B, N, H, d]: more workspace than the default; bad group
     assert lib.fa_bwd_varlen_deterministic_workspace_size(3, 300, 8, 2, 128) > lib.fa_bwd_varlen_workspace_size(3, 300, 8, 128)
     assert lib.fa_bwd_bnhd_deterministic_workspace_size(2, 256, 4, 3, 128) == 0
