@@ -80,7 +80,7 @@ _SIGS = {
     "fa_fwd_varlen_kv": ([_vp] * 7 + [_i] * 7 + [_f, _i, _vp], _i),
     "fa_fwd_fp8_gqa": ([_vp] * 8 + [_i] * 5 + [_f, _i, _vp, _vp], _i),
     "fa_fwd_varlen_window": ([_vp] * 6 + [_i] * 6 + [_f, _i, _i, _i, _vp], _i),
-    "fa_bwd_varlen_window": ([_vp] * 10 + [_i] * 6 + [_f, _i, _i, _i, _vp, _sz, _vp], _i),
+    "fa_bwd_varlen_window": ([_vp] * 10 + [_i] * 6 + [_f, _i, _i, _i, _i, _vp, _sz, _vp], _i),
     "fa_bwd_varlen_kv_workspace_size": ([_i] * 7, _sz),
     "fa_bwd_varlen_kv": ([_vp] * 11 + [_i] * 8 + [_f, _i, _i, _vp, _sz, _vp], _i),
     "fa_bwd_bnhd_workspace_size": ([_i] * 4, _sz),
@@ -488,15 +488,16 @@ def backward_varlen(q, k, v, o, lse, dout, cu_seqlens, max_seqlen: int, causal: 
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     wl, wr = _window(window)
     if wl >= 0 or wr >= 0:
-        wsz = int(lib.fa_bwd_varlen_workspace_size(batch, int(max_seqlen), H, d))
+        wsz = int(lib.fa_bwd_varlen_deterministic_workspace_size(batch, int(max_seqlen), H, Hkv, d) if deterministic
+                  else lib.fa_bwd_varlen_workspace_size(batch, int(max_seqlen), H, d))
         ws = workspace
         if ws is None or ws.numel() * ws.element_size() < wsz:
             ws = torch.empty(wsz, dtype=torch.uint8, device=q.device)
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
         _check(lib.fa_bwd_varlen_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
                                         _ptr(dk), _ptr(dv), _ptr(cu), batch, T, int(max_seqlen), H, Hkv, d, scale,
-                                        int(bool(causal)), wl, wr, _ptr(ws), ws.numel() * ws.element_size(),
-                                        _stream(q)))
+                                        int(bool(causal)), wl, wr, int(bool(deterministic)), _ptr(ws),
+                                        ws.numel() * ws.element_size(), _stream(q)))
         return dq, dk, dv
     if cu_seqlens_k is not None:
         cuk = _cu(cu_seqlens_k, q.device)

@@ -1129,8 +1129,7 @@ fa_status bwd_packed_impl(const void* q, const void* k, const void* v, const voi
     if (total_k < 0) total_k = total;
     if (win_left < -1 || win_right < -1) return fail(FA_ERR_INVALID_ARG, "window edges must be >= -1");
     const bool window = win_left >= 0 || win_right >= 0;
-    if (window && (cu_seqlens_k || det))
-        return fail(FA_ERR_UNSUPPORTED, "the packed sliding window takes one range per sequence, not deterministic");
+    if (window && cu_seqlens_k) return fail(FA_ERR_UNSUPPORTED, "the packed sliding window takes one range per sequence");
     if (max_seqlen_k < 0) max_seqlen_k = max_seqlen;
     if (total_k <= 0 || max_seqlen_k <= 0) return fail(FA_ERR_INVALID_ARG, "total_k and max_seqlen_k must be positive");
     FA_TRY(check_common(batch, H, max_seqlen, d, scale));
@@ -1198,9 +1197,21 @@ fa_status bwd_packed_impl(const void* q, const void* k, const void* v, const voi
         pd.dq_turn = turn;
         pd.nacc = nacc;
         e = cudaMemsetAsync(turn, 0, det_turn_bytes(nacc, batch, H, max_seqlen, d), stream);
-        if (e == cudaSuccess)
+        if (e == cudaSuccess && window) {  // causal = the window's right edge at 0
+            fa::BwdDet<fa::BwdParamsWin> pw;
+            memset(&pw, 0, sizeof(pw));
+            static_cast<fa::BwdParams&>(pw) = p;
+            pw.win_left = win_left;
+            pw.win_right = causal ? 0 : win_right;
+            pw.nqt = pd.nqt;
+            pw.dq_turn = turn;
+            pw.nacc = nacc;
+            e = fa::launch_bwd_main_det_varlen_window(d, tq, tk, tv, tdo, tdq, pw, grid_for_items(p.num_items, dev->sms),
+                                                      stream);
+        } else if (e == cudaSuccess) {
             e = fa::launch_bwd_main_det_varlen(d, causal != 0, tq, tk, tv, tdo, tdq, pd,
                                                grid_for_items(p.num_items, dev->sms), stream);
+        }
         if (e != cudaSuccess) return cuda_fail(e, "varlen deterministic backward launch");
         e = fa::launch_bwd_dq_det_varlen(dqacc, turn, cu_seqlens, dq, scale, H, batch, max_seqlen, MSp, d, nacc,
                                          bw_grid(dev), stream);
@@ -1243,12 +1254,12 @@ size_t fa_bwd_bnhd_workspace_size(int B, int N, int H, int d) { return fa_bwd_va
 fa_status fa_bwd_varlen_window(const void* q, const void* k, const void* v, const void* o, const float* lse,
                                const void* dout, void* dq, void* dk, void* dv, const int* cu_seqlens, int batch,
                                int total, int max_seqlen, int H, int Hkv, int d, float scale, int causal,
-                               int window_left, int window_right, void* workspace, size_t workspace_bytes,
-                               fa_stream_t stream) {
+                               int window_left, int window_right, int deterministic, void* workspace,
+                               size_t workspace_bytes, fa_stream_t stream) {
     if (!cu_seqlens) return fail(FA_ERR_INVALID_ARG, "cu_seqlens must not be NULL");
     return bwd_packed_impl(q, k, v, o, lse, dout, dq, dk, dv, cu_seqlens, batch, total, max_seqlen, H, Hkv, d, scale,
-                           causal, workspace, workspace_bytes, stream, false, nullptr, -1, -1, window_left,
-                           window_right);
+                           causal, workspace, workspace_bytes, stream, deterministic != 0, nullptr, -1, -1,
+                           window_left, window_right);
 }
 
 size_t fa_bwd_varlen_kv_workspace_size(int batch, int max_seqlen_q, int max_seqlen_k, int H, int Hkv, int d,

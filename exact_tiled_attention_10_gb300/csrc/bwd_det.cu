@@ -62,6 +62,16 @@ cudaError_t launch_bwd_main_det_sparse(int d, bool causal, const CUtensorMap& tq
                                                                                           s);
 }
 
+cudaError_t launch_bwd_main_det_varlen_window(int d, const CUtensorMap& tq, const CUtensorMap& tk,
+                                              const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
+                                              const BwdDet<BwdParamsWin>& p, int grid, cudaStream_t s) {
+    if (d == 128)
+        return bwd::launch<bwd::Cfg<128>, false, false, true, true, true, false, false, true>(tq, tk, tv, tdo, tdq, p,
+                                                                                              grid, s);
+    return bwd::launch<bwd::Cfg<64>, false, false, true, true, true, false, false, true>(tq, tk, tv, tdo, tdq, p, grid,
+                                                                                         s);
+}
+
 cudaError_t launch_bwd_main_det_varlen(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
                                        const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
                                        const BwdParamsDet& p, int grid, cudaStream_t s) {

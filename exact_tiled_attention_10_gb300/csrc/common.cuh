@@ -228,6 +228,9 @@ cudaError_t launch_fwd_varlen_window(int d, const FwdMaps& m, const FwdParamsWin
 cudaError_t launch_bwd_main_varlen_window(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                           const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParamsWin& p,
                                           int grid, cudaStream_t stream);
+cudaError_t launch_bwd_main_det_varlen_window(int d, const CUtensorMap& tq, const CUtensorMap& tk,
+                                              const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
+                                              const BwdDet<BwdParamsWin>& p, int grid, cudaStream_t stream);
 cudaError_t launch_bwd_main_det_varlen(int d, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
                                        const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
                                        const BwdParamsDet& p, int grid, cudaStream_t stream);

@@ -233,8 +233,10 @@ fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, fl
  * window_size, [CH18] §18.7.1): fa_fwd_varlen / fa_bwd_varlen with the window
  * of fa_fwd_window applied within each sequence (positions counted from the
  * sequence's first token; -1 = unbounded; causal = right edge at 0).  The
- * backward takes fa_bwd_varlen's workspace.  Not combined with separate key
- * ranges or the deterministic backward (FA_ERR_UNSUPPORTED). */
+ * backward takes fa_bwd_varlen's workspace, or with deterministic != 0
+ * fa_bwd_varlen_deterministic_workspace_size's (bitwise-repeatable results,
+ * see fa_bwd_window_deterministic).  Not combined with separate key ranges
+ * (FA_ERR_UNSUPPORTED). */
 fa_status fa_fwd_varlen_window(const void* q, const void* k, const void* v, void* o, float* lse,
                                const int* cu_seqlens, int batch, int total, int max_seqlen, int H,
                                int Hkv, int d, float scale, int causal, int window_left,
@@ -243,8 +245,8 @@ fa_status fa_bwd_varlen_window(const void* q, const void* k, const void* v, cons
                                const float* lse, const void* dout, void* dq, void* dk, void* dv,
                                const int* cu_seqlens, int batch, int total, int max_seqlen, int H,
                                int Hkv, int d, float scale, int causal, int window_left,
-                               int window_right, void* workspace, size_t workspace_bytes,
-                               fa_stream_t stream);
+                               int window_right, int deterministic, void* workspace,
+                               size_t workspace_bytes, fa_stream_t stream);
 
 /* Packed sequences with their own key ranges (flash_attn_varlen_func's
  * cu_seqlens_q / cu_seqlens_k, [CH18] §18.7.1), bf16: sequence b has queries

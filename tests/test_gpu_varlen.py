@@ -34,6 +34,12 @@ def _case(lens, H, Hkv, d, causal, seed, deterministic=False, window=None):
                                  deterministic=deterministic, window=window)
     torch.cuda.synchronize()
     check_device_status()
+    if deterministic:  # a second run agrees bit for bit
+        again = backward_varlen(q, k, v, o, lse, do, cu, max(lens), causal=causal, scale=scale,
+                                deterministic=True, window=window)
+        torch.cuda.synchronize()
+        for a, b in zip((dq, dk, dv), again):
+            assert torch.equal(a, b)
     g = H // Hkv
     # reference, one sequence at a time
     ref = {n: np.zeros(t.shape) for n, t in (("o", q), ("dq", q), ("dk", k), ("dv", v))}
@@ -149,3 +155,8 @@ def test_varlen_separate_key_ranges(d, causal):
 @pytest.mark.parametrize("causal", [False, True])
 def test_varlen_separate_key_ranges_deterministic(causal):
     _case_kv([500, 129, 64], [700, 129, 1000], 4, 1, 128, causal, seed=141, deterministic=True)
+
+
+@pytest.mark.parametrize("causal,window", [(True, (100, 0)), (False, (64, 37))])
+def test_varlen_sliding_window_deterministic(causal, window):
+    _case([300, 1, 0, 129, 520, 64], 4, 2, 128, causal, seed=171 + window[0], window=window, deterministic=True)
