@@ -67,3 +67,23 @@ def test_bnhd_long_head_agrees_with_the_bhnd_path():
     for a, b in zip((dq, dk, dv), g2):
         a = a.transpose(1, 2).float()
         assert (a - b.float()).abs().max().item() <= 4e-2 * b.float().abs().max().item()
+
+
+def test_bnhd_long_seq_agrees_with_the_bhnd_path():
+    """B=1, N=16384, H=8, d=128, causal (the long-sequence shape): the
+    [B, N, H, d] layout against the [B, H, N, d] path on the transposed
+    tensors."""
+    B, N, H, d = 1, 16384, 8, 128
+    q, k, v, do = (randn((B, N, H, d), 1005 + i, device=DEV) for i in range(4))
+    o, lse = forward_bnhd(q, k, v, causal=True)
+    dq, dk, dv = backward_bnhd(q, k, v, o, lse, do, causal=True)
+    t = [x.transpose(1, 2).contiguous() for x in (q, k, v, do)]
+    o2, lse2 = forward(t[0], t[1], t[2], causal=True)
+    g2 = backward(t[0], t[1], t[2], o2, lse2, t[3], causal=True)
+    torch.cuda.synchronize()
+    check_device_status()
+    assert (o.transpose(1, 2).float() - o2.float()).abs().max().item() <= 2 * O_TOL
+    assert (lse - lse2).abs().max().item() <= 2e-3
+    for a, b in zip((dq, dk, dv), g2):
+        a = a.transpose(1, 2).float()
+        assert (a - b.float()).abs().max().item() <= 4e-2 * b.float().abs().max().item()

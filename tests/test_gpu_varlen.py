@@ -160,3 +160,12 @@ def test_varlen_separate_key_ranges_deterministic(causal):
 @pytest.mark.parametrize("causal,window", [(True, (100, 0)), (False, (64, 37))])
 def test_varlen_sliding_window_deterministic(causal, window):
     _case([300, 1, 0, 129, 520, 64], 4, 2, 128, causal, seed=171 + window[0], window=window, deterministic=True)
+
+
+def test_varlen_separate_key_ranges_decode_mix():
+    """A decode-like mix: 8 sequences with 1 .. 64 new queries against caches
+    of up to 8192 keys (causal: the queries are each sequence's last
+    positions), shared heads."""
+    lens_q = [1, 64, 7, 33, 1, 16, 50, 2]
+    lens_k = [8192, 4096, 1000, 3000, 129, 7777, 2048, 6000]
+    _case_kv(lens_q, lens_k, 8, 2, 128, True, seed=181)
