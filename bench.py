@@ -7,8 +7,16 @@ One STEP is one pass of the whole path over one batch of synthetic input:
 all through the C ABI of libfa_gb300.so.  Default workload: B=2, H=16,
 N=4096, d=128 (the long-head shape; the accuracy/throughput targets are stated
 for N >= 4096, d = 128).  The metric is algorithmic TFLOPS:
-  F = 4 B H N^2 d per forward, 2.5 F per backward, halved when causal;
-  the FP8 forward counts its F (non-causal).
+  F = 4 B H N^2 d per forward, 2.5 F per backward, halved when causal.
+
+The headline `value` is the bf16 rate: (F_fwd + F_bwd) over the time of the
+bf16 forward plus the whole backward call (preprocess + main + dQ
+conversion), summed over the timed steps.  The FP8 rows (quantiser + FP8
+forward) run inside the same steps and are reported on their own (`fp8`),
+against the FP8 peak; no figure mixes bf16 and E4M3 FLOPs.  Fractions use the
+measured BURST dense bf16 peak (FP8: twice that): each kernel runs for well
+under a second at a time.  `configs` holds the same figures for the other
+workload shapes (mid, ragged with its effective FLOPs, long_seq).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -47,6 +55,8 @@ def parse_args():
     ap.add_argument("--workload", default="long_head")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=0, help="0 = min(steps, 100)")
+    ap.add_argument("--no-configs", action="store_true", help="skip the other workload shapes")
+    ap.add_argument("--config-reps", type=int, default=20)
     return ap.parse_args()
 
 
@@ -216,38 +226,47 @@ class Step:
     on the current stream with an event before and after every phase."""
 
     PHASES = ["fwd", "bwd_pre", "bwd_main", "bwd_dq", "quant_fp8", "fwd_fp8"]
+    BF16 = ("fwd", "bwd_pre", "bwd_main", "bwd_dq")
 
-    def __init__(self, w, causal, device, seed_offset=0):
+    def __init__(self, w, causal, device, seed_offset=0, fp8=True):
         import torch
         import exact_tiled_attention_10_gb300 as fa
-        from exact_tiled_attention_10_gb300.inputs import qkv
-        self.fa, self.torch, self.w, self.causal = fa, torch, w, causal
+        from exact_tiled_attention_10_gb300.inputs import kv_lens_ragged, qkv
+        self.fa, self.torch, self.w, self.causal, self.with_fp8 = fa, torch, w, causal, fp8
         self.lib = fa.load_library()
         self.dev = device
         B, H, N, d = w.B, w.H, w.N, w.d
         self.q, self.k, self.v, self.do = qkv(B, H, N, d, w.seed + seed_offset, device=device)
+        self.kv = kv_lens_ragged(B, N, w.seed, device=device) if w.ragged else None
         t = lambda *s, dt=torch.bfloat16: torch.empty(*s, dtype=dt, device=device)
         self.o, self.dq, self.dk, self.dv = (t(B, H, N, d) for _ in range(4))
         self.lse = t(B, H, N, dt=torch.float32)
         self.ws_bytes = fa.bwd_workspace_size(torch.bfloat16, B, H, N, d)
         self.ws = t(self.ws_bytes, dt=torch.uint8)
         nb = self.lib.fa_fp8_num_blocks(N)
-        self.x8 = [t(B, H, N, d, dt=torch.uint8) for _ in range(3)]
-        self.sc = [t(B, H, nb, dt=torch.float32) for _ in range(3)]
-        self.o8 = t(B, H, N, d)
-        self.lse8 = t(B, H, N, dt=torch.float32)
+        if fp8:
+            self.x8 = [t(B, H, N, d, dt=torch.uint8) for _ in range(3)]
+            self.sc = [t(B, H, nb, dt=torch.float32) for _ in range(3)]
+            self.o8 = t(B, H, N, d)
+            self.lse8 = t(B, H, N, dt=torch.float32)
         self.flush = t(L2_FLUSH_BYTES, dt=torch.uint8)
         # split-key plans (automatic): the causal bf16 forward is never split;
         # the non-causal FP8 forward may be (its merge kernel is part of the call)
-        self.split_bf16 = self.lib.fa_fwd_split_count(B, H, N, d, int(causal), 0, 0)
+        has_kv = int(self.kv is not None)
+        self.split_bf16 = self.lib.fa_fwd_split_count(B, H, N, d, int(causal), has_kv, 0)
         self.split_fp8 = self.lib.fa_fwd_split_count(B, H, N, d, 0, 0, 0)
-        self.sws_bytes = max(self.lib.fa_fwd_split_workspace_size(B, H, N, d, int(causal), 0, 0),
+        self.sws_bytes = max(self.lib.fa_fwd_split_workspace_size(B, H, N, d, int(causal), has_kv, 0),
                              self.lib.fa_fwd_split_workspace_size(B, H, N, d, 0, 0, 0))
         self.sws = t(max(self.sws_bytes, 256), dt=torch.uint8)
         self.scale = 1.0 / math.sqrt(d)
         F = flops_fwd(w, causal)
         self.flops = {"fwd": F, "bwd_pre": 0.0, "bwd_main": 2.5 * F, "bwd_dq": 0.0,
                       "quant_fp8": 0.0, "fwd_fp8": flops_fwd(w, False)}
+        # the ragged workload: the FLOPs of the visible (query, key) pairs only
+        self.flops_eff = None
+        if self.kv is not None:
+            Feff = 4.0 * H * d * N * float(self.kv.sum().item()) * (0.5 if causal else 1.0)
+            self.flops_eff = {"fwd": Feff, "bwd": 2.5 * Feff}
         n = B * H * N * d
         Np = (N + 127) // 128 * 128
         self.bytes = {"fwd": 4 * n * 2 + B * H * N * 4,
@@ -256,7 +275,9 @@ class Step:
                       "bwd_dq": B * H * Np * d * 4 + n * 2,
                       "quant_fp8": 3 * (n * 2 + n + B * H * nb * 4),
                       "fwd_fp8": 3 * n + n * 2 + B * H * N * 4}
-        self.launches_per_step = 6 + int(self.split_bf16 > 1) + int(self.split_fp8 > 1)
+        self.launches_bf16 = 4 + int(self.split_bf16 > 1)
+        self.launches_fp8 = 2 + int(self.split_fp8 > 1)
+        self.launches_per_step = self.launches_bf16 + (self.launches_fp8 if fp8 else 0)
 
     def _ck(self, st):
         if st != 0:
@@ -266,20 +287,23 @@ class Step:
         lib, w, s = self.lib, self.w, self.torch.cuda.current_stream(self.dev).cuda_stream
         B, H, N, d = w.B, w.H, w.N, w.d
         p = lambda x: x.data_ptr()
+        kv = None if self.kv is None else p(self.kv)
         rec = (lambda i: events[i].record()) if events is not None else (lambda i: None)
         rec(0)
         self._ck(lib.fa_fwd_split(p(self.q), p(self.k), p(self.v), p(self.o), p(self.lse), B, H, N, d,
-                                  self.scale, int(self.causal), None, 0, p(self.sws), self.sws_bytes, s))
+                                  self.scale, int(self.causal), kv, 0, p(self.sws), self.sws_bytes, s))
         rec(1)
         self._ck(lib.fa_bwd_preprocess(p(self.o), p(self.lse), p(self.do), B, H, N, d, p(self.ws),
                                        self.ws_bytes, s))
         rec(2)
         self._ck(lib.fa_bwd_main(p(self.q), p(self.k), p(self.v), p(self.do), p(self.dk), p(self.dv),
-                                 B, H, N, d, self.scale, int(self.causal), None, p(self.ws),
+                                 B, H, N, d, self.scale, int(self.causal), kv, p(self.ws),
                                  self.ws_bytes, s))
         rec(3)
         self._ck(lib.fa_bwd_dq(p(self.dq), B, H, N, d, self.scale, p(self.ws), self.ws_bytes, s))
         rec(4)
+        if not self.with_fp8:
+            return
         self._ck(lib.fa_quantize_fp8_qkv(p(self.q), p(self.k), p(self.v), p(self.x8[0]), p(self.x8[1]),
                                          p(self.x8[2]), p(self.sc[0]), p(self.sc[1]), p(self.sc[2]), B, H, H, N, d,
                                          s))
@@ -311,8 +335,9 @@ def max_over_ranks(ws, x, device):
 
 def e2e_pipelined(step_a, step_b, steps):
     """End to end through the C ABI with pinned host buffers: every step copies
-    its inputs (Q, K, V, dO) in from the host, runs the whole step and copies
-    its results (O, LSE, dQ, dK, dV, FP8 O) back.  The copies of step k+1 (in)
+    its inputs (Q, K, V, dO) in from the host, runs the bf16 forward and
+    backward (the headline's work) and copies its results (O, LSE, dQ, dK, dV)
+    back.  The copies of step k+1 (in)
     and k-1 (out) run on their own streams while step k computes, on two sets
     of device buffers; events keep a buffer from being overwritten while it is
     still read or written.  Returns the milliseconds of `steps` steps, from
@@ -321,7 +346,7 @@ def e2e_pipelined(step_a, step_b, steps):
     dev = step_a.dev
     steps_ = (step_a, step_b)
     ins = lambda st: (st.q, st.k, st.v, st.do)
-    outs = lambda st: (st.o, st.lse, st.dq, st.dk, st.dv, st.o8)
+    outs = lambda st: (st.o, st.lse, st.dq, st.dk, st.dv)
     hin = [[t.cpu().pin_memory() for t in ins(st)] for st in steps_]
     hout = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs(st)] for st in steps_]
     s_in, s_c, s_out = (torch.cuda.Stream(dev) for _ in range(3))
@@ -366,6 +391,88 @@ def e2e_pipelined(step_a, step_b, steps):
 
     run(3, False)  # warm-up
     return run(steps, True)
+
+
+def summarise(step, phase_ms, peaks):
+    """Per-pass figures of one workload from per-step phase times (ms lists):
+    TFLOPS and fraction of the burst peak for the contractions, GB/s and
+    fraction of the copy bandwidth for the HBM-bound kernels, and the two
+    passes as the C ABI calls them: the bf16 forward (fa_fwd) and the whole
+    backward call (fa_bwd = preprocess + main + dQ conversion)."""
+    bf16_peak = peaks["bf16_tflops"]
+    passes = {}
+    for ph, ms_list in phase_ms.items():
+        if not ms_list:
+            continue
+        ms = statistics.mean(ms_list)
+        ent = {"ms": round(ms, 4)}
+        if step.flops[ph]:
+            tf = step.flops[ph] / (ms / 1e3) / 1e12
+            pk = bf16_peak * (FP8_OVER_BF16 if ph == "fwd_fp8" else 1.0)
+            ent.update({"tflops": round(tf, 1), "frac_of_peak": round(tf / pk, 4), "peak_tflops": pk})
+        ent["gbs"] = round(step.bytes[ph] / (ms / 1e3) / 1e9, 1)
+        if not step.flops[ph]:
+            ent["frac_of_hbm"] = round(ent["gbs"] / peaks["hbm_gbs"], 4)
+        passes[ph] = ent
+    fwd_ms = passes["fwd"]["ms"]
+    bwd_ms = sum(statistics.mean(phase_ms[ph]) for ph in ("bwd_pre", "bwd_main", "bwd_dq"))
+    Ff, Fb = step.flops["fwd"], step.flops["bwd_main"]
+    out = {"fwd_tflops": round(Ff / (fwd_ms / 1e3) / 1e12, 1),
+           "fwd_frac_burst": round(Ff / (fwd_ms / 1e3) / 1e12 / bf16_peak, 4),
+           "bwd_call_ms": round(bwd_ms, 4),
+           "bwd_call_tflops": round(Fb / (bwd_ms / 1e3) / 1e12, 1),
+           "bwd_call_frac_burst": round(Fb / (bwd_ms / 1e3) / 1e12 / bf16_peak, 4)}
+    if step.flops_eff is not None:
+        out["fwd_tflops_effective"] = round(step.flops_eff["fwd"] / (fwd_ms / 1e3) / 1e12, 1)
+        out["bwd_call_tflops_effective"] = round(step.flops_eff["bwd"] / (bwd_ms / 1e3) / 1e12, 1)
+    if "fwd_fp8" in passes:
+        out["fp8_fwd_tflops"] = passes["fwd_fp8"]["tflops"]
+        out["fp8_fwd_frac_burst"] = passes["fwd_fp8"]["frac_of_peak"]
+        out["quant_fp8_gbs"] = passes["quant_fp8"]["gbs"]
+    return passes, out
+
+
+def time_steps(step, steps, warmup):
+    """Runs `warmup` then `steps` steps (L2 flushed between steps, outside the
+    events) and returns {phase: [ms per step]}."""
+    import torch
+    nph = len(Step.PHASES) if step.with_fp8 else 4
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nph + 1)] for _ in range(steps)]
+    for _ in range(max(warmup, 3)):
+        step.run()
+        step.flush_l2()
+    torch.cuda.synchronize()
+    for i in range(steps):
+        step.run(ev[i])
+        step.flush_l2()
+    torch.cuda.synchronize()
+    out = {ph: [] for ph in Step.PHASES[:nph]}
+    for e in ev:
+        for j, ph in enumerate(Step.PHASES[:nph]):
+            out[ph].append(e[j].elapsed_time(e[j + 1]))
+    return out
+
+
+def other_configs(device, peaks, reps):
+    """The other workload shapes, each timed on its own (bf16 forward and
+    whole backward call; FP8 where the workload has one)."""
+    from exact_tiled_attention_10_gb300.inputs import WORKLOADS
+    res = {}
+    for name, causal, fp8 in (("mid", True, False), ("mid", False, False), ("ragged", False, False),
+                              ("long_seq", True, False), ("long_seq", False, True)):
+        w = WORKLOADS[name]
+        st = Step(w, causal, device, fp8=fp8)
+        ph = time_steps(st, reps, 3)
+        passes, summ = summarise(st, ph, peaks)
+        key = "%s_%s" % (name, "causal" if causal else "noncausal")
+        summ.update({"B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": causal, "reps": reps})
+        if w.ragged:
+            summ["kv_lens_sum"] = int(st.kv.sum().item())
+        if fp8:  # the FP8 figures are the point of this line (the pages' FP8 workload is non-causal)
+            summ["passes"] = {k: passes[k] for k in ("quant_fp8", "fwd_fp8")}
+        res[key] = summ
+        del st
+    return res
 
 
 def main():
@@ -417,48 +524,45 @@ def main():
     fa.check_device_status(device)
 
     phase_ms = {ph: [] for ph in Step.PHASES}
-    step_ms = []
+    step_ms, bf16_ms = [], []
     for e in ev:
         step_ms.append(e[0].elapsed_time(e[6]))
+        bf16_ms.append(e[0].elapsed_time(e[4]))
         for j, ph in enumerate(Step.PHASES):
             phase_ms[ph].append(e[j].elapsed_time(e[j + 1]))
     total_ms = max_over_ranks(ws, sum(step_ms), device)
-    flops_step = sum(step.flops.values())
-    value = ws * flops_step * args.steps / (total_ms / 1e3) / 1e12
+    bf16_total_ms = max_over_ranks(ws, sum(bf16_ms), device)
+    flops_bf16 = step.flops["fwd"] + step.flops["bwd_main"]
+    value = ws * flops_bf16 * args.steps / (bf16_total_ms / 1e3) / 1e12
 
     peaks, peak_src = load_peaks()
-    bf16_peak = peaks["bf16_tflops_sustained"]
-    passes = {}
-    for ph in Step.PHASES:
-        ms = statistics.mean(phase_ms[ph])
-        ent = {"ms": round(ms, 4)}
-        if step.flops[ph]:
-            tf = step.flops[ph] / (ms / 1e3) / 1e12
-            pk = bf16_peak * (FP8_OVER_BF16 if ph == "fwd_fp8" else 1.0)
-            ent.update({"tflops": round(tf, 1), "frac_of_peak": round(tf / pk, 4),
-                        "peak_tflops": pk})
-        ent["gbs"] = round(step.bytes[ph] / (ms / 1e3) / 1e9, 1)
-        if not step.flops[ph]:
-            ent["frac_of_hbm"] = round(ent["gbs"] / peaks["hbm_gbs"], 4)
-        passes[ph] = ent
+    passes, summ = summarise(step, phase_ms, peaks)
     dom = max(("fwd", "bwd_main", "fwd_fp8"), key=lambda ph: statistics.mean(phase_ms[ph]))
-    dom_ms = statistics.mean(phase_ms[dom])
-    dom_peak = bf16_peak * (FP8_OVER_BF16 if dom == "fwd_fp8" else 1.0)
-    achieved = step.flops[dom] / (dom_ms / 1e3) / 1e12
-    roofline = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1),
-                "peak": dom_peak, "unit": "TFLOP/s", "frac": round(achieved / dom_peak, 4),
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": passes[dom]["tflops"],
+                "peak": passes[dom]["peak_tflops"], "unit": "TFLOP/s", "frac": passes[dom]["frac_of_peak"],
                 "traffic": recorded_traffic(dom),
-                "peak_source": "%s (%s)" % (peak_src, "dense bf16 sustained" +
-                                            (" x2 for e4m3" if dom == "fwd_fp8" else ""))}
+                "peak_source": "%s (%s)" % (peak_src, "dense bf16 burst" +
+                                            (" x2 for e4m3" if dom == "fwd_fp8" else "")),
+                "peak_sustained": peaks["bf16_tflops_sustained"] * (FP8_OVER_BF16 if dom == "fwd_fp8" else 1.0)}
+    fp8 = {"tflops": summ["fp8_fwd_tflops"], "frac_of_fp8_peak": summ["fp8_fwd_frac_burst"],
+           "fp8_peak_tflops": peaks["bf16_tflops"] * FP8_OVER_BF16,
+           "ms": passes["fwd_fp8"]["ms"], "quant_ms": passes["quant_fp8"]["ms"],
+           "quant_gbs": passes["quant_fp8"]["gbs"], "quant_frac_of_hbm": passes["quant_fp8"]["frac_of_hbm"],
+           "workload": "non-causal forward on E4M3 codes with per-64-row block scales (quantiser timed apart)"}
 
     # ---- end to end through the public API with pinned host buffers
     e2e_steps = args.e2e_steps or min(args.steps, 100)
-    e2e_ms = e2e_pipelined(step, Step(w, causal, device, seed_offset=1000 * rank), e2e_steps)
+    e2e_ms = e2e_pipelined(Step(w, causal, device, seed_offset=1000 * rank, fp8=False),
+                           Step(w, causal, device, seed_offset=1000 * rank + 1, fp8=False), e2e_steps)
     hin_bytes = sum(t.numel() * t.element_size() for t in (step.q, step.k, step.v, step.do))
-    hout_bytes = sum(t.numel() * t.element_size() for t in (step.o, step.lse, step.dq, step.dk, step.dv, step.o8))
+    hout_bytes = sum(t.numel() * t.element_size() for t in (step.o, step.lse, step.dq, step.dk, step.dv))
     h2d, d2h = hin_bytes, hout_bytes
     e2e_ms = max_over_ranks(ws, e2e_ms, device)
-    e2e_value = ws * flops_step * e2e_steps / (e2e_ms / 1e3) / 1e12
+    e2e_value = ws * flops_bf16 * e2e_steps / (e2e_ms / 1e3) / 1e12
+
+    configs = None
+    if not args.no_configs:
+        configs = other_configs(device, peaks, args.config_reps)
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -473,21 +577,30 @@ def main():
             "metric": METRIC, "value": round(value, 2), "unit": "TFLOPS", "n_gpus": ws,
             "steps": args.steps, "warmup": max(args.warmup, 3),
             "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16+e4m3", "data": "synthetic",
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": "%s: B=%d H=%d N=%d d=%d; bf16 causal fwd + bwd, then E4M3 "
                                    "quantise Q/K/V + FP8 non-causal fwd" % (w.name, w.B, w.H, w.N, w.d),
                        "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": causal,
+                       "value_basis": "bf16 (F_fwd + F_bwd) / time of the bf16 forward and the whole backward "
+                                      "call (%.4f ms per step); ms_per_step also holds the FP8 rows" % (
+                                          bf16_total_ms / args.steps),
                        "l2": "flushed between steps (512 MiB write outside the timed events)",
                        "parallelism": "replicas" if ws > 1 else "single GPU"},
+            "targets": {"fwd_frac_burst": summ["fwd_frac_burst"], "fwd_target": 0.60,
+                        "bwd_call_frac_burst": summ["bwd_call_frac_burst"], "bwd_target": 0.45,
+                        "peak_tflops": peaks["bf16_tflops"], "peak": "%s dense bf16 burst" % peak_src},
             "passes": passes,
+            "bf16": summ,
+            "fp8": fp8,
             "roofline": roofline,
+            "configs": configs,
             "cpu_baseline": cpu,
             "e2e": {"value": round(e2e_value, 2), "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                     "how": "C ABI with pinned host buffers; every step copies Q, K, V, dO in and O, LSE, "
-                           "dQ, dK, dV, FP8 O out; copies of neighbouring steps overlap compute (two "
-                           "device buffer sets, three streams); inputs of %.0f MB per step, "
-                           "L2 129 MB" % (h2d / 1e6)},
+                           "dQ, dK, dV out around the bf16 forward + backward; copies of neighbouring steps "
+                           "overlap compute (two device buffer sets, three streams); inputs of %.0f MB per "
+                           "step, L2 129 MB" % (h2d / 1e6)},
             "gpu_launches": step.launches_per_step * args.steps,
             "clocks": clk,
             "wall_s": round(wall, 3),

@@ -10,7 +10,7 @@ e(f) = (q(f) - 2^f) / 2^f, in float64.  2^r is applied by adding r to the
 float32 exponent field, so the overall relative error is that of q.
 
 Run:  python exp2_poly_fit.py      (prints the coefficients and the error)
-The printed values are the constants kExp2C0..C3 in fwd_kernel.cuh.
+The printed values are the constants kExp2C0..C3 in ptx.cuh.
 """
 import numpy as np
 

@@ -1,21 +1,47 @@
 """Helpers shared by the GPU parity tests: run the CUDA path and the oracle on
 the same seeded, bf16-rounded inputs and compare with the stated tolerances.
 
-Tolerances (from the method's accuracy targets for bf16 inputs with float32
+Tolerances (the method's accuracy targets for bf16 inputs with float32
 accumulation):  O max-abs <= 1e-2, LSE max-abs <= 1e-3,
-dQ/dK/dV max-abs <= 2e-2 * max|dX| (the oracle's), FP8 O max-abs <= 6e-2.
+dQ/dK/dV max-abs <= 2e-2 * max|dX| (max-abs of the ORACLE's gradient),
+FP8 O max-abs <= 6e-2.
+
+O is held to the flat 1e-2 everywhere except on rows that see fewer than
+FEW_KEYS keys; there the bound is the worst case of the two bf16 roundings
+the kernel makes (see `assert_o`).
+
+Set FA_PARITY_LOG to a file name to append one JSON line per comparison
+(test, quantity, max error, bound): the measured margins.
 """
+import json
+import os
+
 import numpy as np
-import torch
 
 O_TOL = 1e-2
 LSE_TOL = 1e-3
 GRAD_REL_TOL = 2e-2
 FP8_O_TOL = 6e-2
 
+# Rows with fewer visible keys than this may use the rounding bound below.
+FEW_KEYS = 16
+# bf16 unit roundoff (8-bit significand, round to nearest): |fl(x) - x| <= 2^-8 |x|.
+BF16_U = 2.0 ** -8
+
 
 def to64(t):
     return t.detach().to("cpu").double().numpy()
+
+
+def _log(what, err, bound, **extra):
+    path = os.environ.get("FA_PARITY_LOG")
+    if not path:
+        return
+    rec = dict(test=os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0], what=what, err=float(err),
+               bound=float(bound))
+    rec.update({k: (float(v) if isinstance(v, (np.floating, float)) else v) for k, v in extra.items()})
+    with open(path, "a") as f:
+        f.write(json.dumps(rec) + "\n")
 
 
 def assert_lse(gpu, ref, tol=LSE_TOL, what="lse"):
@@ -27,34 +53,69 @@ def assert_lse(gpu, ref, tol=LSE_TOL, what="lse"):
     fin = ~ninf_r
     assert np.all(np.isfinite(gpu[fin])), "%s: non-finite values" % what
     err = np.max(np.abs(gpu[fin] - ref[fin])) if fin.any() else 0.0
+    _log(what, err, tol)
     assert err <= tol, "%s max-abs error %.3e > %.1e" % (what, err, tol)
     return err
-
-
-# O is written as bf16: its own rounding is up to 2^-9 |O| (half a bf16
-# quantum).  Where a row averages only a few value rows (narrow sliding
-# windows, the first rows of a causal mask) |O| stays near the size of single
-# value rows (2 to 4 for N(0,1) data), and that rounding plus the bf16
-# rounding of P can exceed the 1e-2 figure, which assumes many keys per row.
-O_BF16_REL = 2.0 ** -9
-
-
-def assert_o_bf16(gpu, ref, what="O"):
-    """|gpu - ref| <= 1e-2 + 2^-9 |ref| element by element."""
-    gpu = np.asarray(gpu, dtype=np.float64)
-    assert np.all(np.isfinite(gpu)), "%s: non-finite values" % what
-    excess = np.abs(gpu - ref) - (O_TOL + O_BF16_REL * np.abs(ref))
-    worst = float(np.max(excess)) if gpu.size else -1.0
-    assert worst <= 0.0, "%s error exceeds 1e-2 + 2^-9|O| by %.3e" % (what, worst)
-    return worst
 
 
 def assert_close_abs(gpu, ref, tol, what):
     gpu = np.asarray(gpu, dtype=np.float64)
     assert np.all(np.isfinite(gpu)), "%s: non-finite values" % what
     err = np.max(np.abs(gpu - ref)) if gpu.size else 0.0
+    _log(what, err, tol)
     assert err <= tol, "%s max-abs error %.3e > %.3e" % (what, err, tol)
     return err
+
+
+def rounding_context(run_fwd, q, v):
+    """Per row: the number of visible keys, and A = sum_j P_ij |v_j| per element.
+
+    Both come from two more runs of the same oracle forward `run_fwd(q, v) ->
+    (O, LSE)` with the test's mask: with q = 0 every visible score is 0, so
+    LSE = log(visible keys); with |v| in place of v, O is sum_j P_ij |v_j|."""
+    q = np.asarray(q, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    _, lse0 = run_fwd(np.zeros_like(q), v)
+    lse0 = np.asarray(lse0, dtype=np.float64)
+    nvis = np.where(np.isfinite(lse0), np.rint(np.exp(np.where(np.isfinite(lse0), lse0, 0.0))), 0.0)
+    absref, _ = run_fwd(q, np.abs(v))
+    return nvis, np.asarray(absref, dtype=np.float64)
+
+
+def assert_o(gpu, ref, what="O", nvis=None, absref=None):
+    """O against the oracle, element by element.
+
+    Rows that see FEW_KEYS keys or more: |gpu - ref| <= 1e-2 (flat).
+    Rows that see fewer (nvis, absref from `rounding_context`): the kernel
+    rounds each weight P_ij to bf16 for the P V product (relative error
+    <= 2^-8; the normaliser sums the unrounded weights) and rounds O to bf16
+    (<= 2^-8 |O|), so |gpu - ref| <= 2^-8 sum_j P_ij |v_j| + 2^-8 |O|
+    <= 2^-7 A.  Such a row averages only a handful of value rows, so A stays
+    near the size of single N(0,1) entries and the bound can pass 1e-2; the
+    bound used is max(1e-2, 2^-7 A + 1e-5) (1e-5: float32 accumulation)."""
+    gpu = np.asarray(gpu, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert np.all(np.isfinite(gpu)), "%s: non-finite values" % what
+    err = np.abs(gpu - ref)
+    if gpu.size == 0:
+        return 0.0
+    if nvis is None:
+        worst = float(np.max(err))
+        _log(what, worst, O_TOL)
+        assert worst <= O_TOL, "%s max-abs error %.3e > %.1e" % (what, worst, O_TOL)
+        return worst
+    few = (np.asarray(nvis) < FEW_KEYS)[..., None] & np.ones(ref.shape, dtype=bool)
+    bound = np.where(few, np.maximum(O_TOL, 2.0 * BF16_U * absref + 1e-5), O_TOL)
+    flat_err = float(np.max(err[~few])) if (~few).any() else 0.0
+    few_err = float(np.max(err[few])) if few.any() else 0.0
+    excess = float(np.max(err - bound))
+    _log(what, max(flat_err, few_err), O_TOL, flat_err=flat_err, few_err=few_err,
+         few_rows=int(np.sum(np.asarray(nvis) < FEW_KEYS)), few_bound_max=float(np.max(bound)))
+    assert flat_err <= O_TOL, "%s max-abs error %.3e > %.1e on rows with >= %d keys" % (
+        what, flat_err, O_TOL, FEW_KEYS)
+    assert excess <= 0.0, "%s error on rows with < %d keys exceeds max(1e-2, 2^-7 A) by %.3e" % (
+        what, FEW_KEYS, excess)
+    return max(flat_err, few_err)
 
 
 # A gradient that is identically zero in exact arithmetic (e.g. dQ with a single
@@ -64,13 +125,15 @@ def assert_close_abs(gpu, ref, tol, what):
 GRAD_ABS_FLOOR = 1e-5
 
 
-def assert_grad(gpu, ref, what, tensor_maxabs=None):
-    """max|gpu - ref| <= 2e-2 * (max-abs of the whole gradient tensor).
+def assert_grad(gpu, ref, what, ref_maxabs=None):
+    """max|gpu - ref| <= 2e-2 * (max-abs of the oracle's gradient).
 
-    `tensor_maxabs` is that max-abs when `ref` covers only sampled rows."""
+    When `ref` holds sampled rows only, its own max-abs (a lower bound of the
+    whole tensor's) is the scale unless `ref_maxabs`, the oracle's max-abs
+    over the whole tensor, is given.  The scale never comes from the GPU."""
     scale = np.max(np.abs(ref)) if ref.size else 0.0
-    if tensor_maxabs is not None:
-        scale = max(scale, float(tensor_maxabs))
+    if ref_maxabs is not None:
+        scale = max(scale, float(ref_maxabs))
     return assert_close_abs(gpu, ref, max(GRAD_REL_TOL * scale, GRAD_ABS_FLOOR), what)
 
 

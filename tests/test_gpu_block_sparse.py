@@ -7,8 +7,10 @@ lists whose two 128-row tiles of one work item use disjoint and interleaved
 blocks (the merged K/V stream then has blocks only one tile uses), empty
 lists (fully masked rows), the all-ones and diagonal masks, the causal and
 key-padding masks, shared key/value heads, ragged N, and a long sequence on
-sampled rows and keys.  O is held to 1e-2 plus its own bf16 rounding
-(2^-9 |O|), since sparse rows can average only a few value rows."""
+sampled rows and keys.  O is held to the flat 1e-2 except on rows that see
+fewer than 16 keys (the first rows of a causal diagonal block when it is the
+row's only block), which are held to the worst case of the kernel's two
+bf16 roundings (parity_util.assert_o)."""
 import math
 
 import numpy as np
@@ -19,7 +21,7 @@ import oracle
 from exact_tiled_attention_10_gb300 import (backward_block_sparse, block_lists, check_device_status, forward,
                                             forward_block_sparse)
 from exact_tiled_attention_10_gb300.inputs import qkv
-from parity_util import assert_close_abs, assert_grad, assert_lse, assert_o_bf16, sample_rows, to64
+from parity_util import assert_close_abs, assert_grad, assert_lse, assert_o, rounding_context, sample_rows, to64
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -44,9 +46,13 @@ def _case(B, H, Hkv, N, d, causal, bm, kv=None, seed=5, deterministic=False):
             assert torch.equal(a, b)
     g = H // Hkv
     kvn = None if kv is None else np.asarray(kv, dtype=np.int32)
-    ref = oracle.bwd(to64(q), np.repeat(to64(k), g, axis=1), np.repeat(to64(v), g, axis=1), to64(do), scale,
-                     causal=causal, kv_lens=kvn, block_mask=np.asarray(bm), block_size=128)
-    assert_o_bf16(to64(o), ref["o"])
+    kr, vr = np.repeat(to64(k), g, axis=1), np.repeat(to64(v), g, axis=1)
+    bma = np.asarray(bm)
+    ref = oracle.bwd(to64(q), kr, vr, to64(do), scale, causal=causal, kv_lens=kvn, block_mask=bma, block_size=128)
+    nvis, absref = rounding_context(
+        lambda qq, vv: oracle.fwd(qq, kr, vv, scale, causal=causal, kv_lens=kvn, block_mask=bma, block_size=128),
+        to64(q), vr)
+    assert_o(to64(o), ref["o"], nvis=nvis, absref=absref)
     assert_lse(to64(lse), ref["lse"])
     assert_grad(to64(dq), ref["dq"], "dQ")
     assert_grad(to64(dk), ref["dk"].reshape(B, Hkv, g, N, d).sum(axis=2), "dK")
@@ -114,13 +120,16 @@ def test_block_sparse_long_sequence_sampled():
     keys = sorted(set(sample_rows(N, 12, seed=6)))
     for h in (0, 3):
         qh, kh, vh, gh = (to64(t[0, h]) for t in (q, k, v, do))
-        o_ref, lse_ref = oracle.fwd_rows(qh, kh, vh, scale, True, N, rows, block_mask=bm, block_size=128)
-        assert_o_bf16(to64(o[0, h])[rows], o_ref, "O rows")
+        run = lambda qq, vv: oracle.fwd_rows(qq, kh, vv, scale, True, N, rows, block_mask=bm, block_size=128)
+        o_ref, lse_ref = run(qh, vh)
+        nvis, absref = rounding_context(run, qh, vh)
+        assert_o(to64(o[0, h])[rows], o_ref, "O rows", nvis=nvis, absref=absref)
         assert_lse(to64(lse[0, h])[rows], lse_ref)
+        # gradient scale: the oracle's max-abs over the sampled rows / keys
         g = oracle.bwd_rows(qh, kh, vh, gh, scale, True, N, rows, keys, block_mask=bm, block_size=128)
-        assert_grad(to64(dq[0, h])[rows], g["dq"], "dQ rows", np.max(np.abs(to64(dq[0, h]))))
-        assert_grad(to64(dk[0, h])[keys], g["dk"], "dK keys", np.max(np.abs(to64(dk[0, h]))))
-        assert_grad(to64(dv[0, h])[keys], g["dv"], "dV keys", np.max(np.abs(to64(dv[0, h]))))
+        assert_grad(to64(dq[0, h])[rows], g["dq"], "dQ rows")
+        assert_grad(to64(dk[0, h])[keys], g["dk"], "dK keys")
+        assert_grad(to64(dv[0, h])[keys], g["dv"], "dV keys")
 
 
 @pytest.mark.parametrize("d", [64, 128])

@@ -5,7 +5,10 @@ through the log-sum-exp) and cross-attention.  With the causal mask the
 queries are the last Nq positions.  The oracle's rectangular forward is the
 reference; cases cover one and a few query rows, Nq > Nk, ragged Nk, cache
 lengths per batch item (including 0), shared key/value heads, explicit and
-planned key splits, and a 128K-key decode step on sampled heads."""
+planned key splits, and a 128K-key decode step on sampled heads.  O is held
+to the flat 1e-2 except on rows that see fewer than 16 keys (N_q > N_k under
+the causal mask, short caches), which are held to the worst case of the
+kernel's two bf16 roundings (parity_util.assert_o)."""
 import math
 
 import numpy as np
@@ -15,7 +18,7 @@ import torch
 import oracle
 from exact_tiled_attention_10_gb300 import check_device_status, forward_rect, load_library
 from exact_tiled_attention_10_gb300.inputs import qkv, randn
-from parity_util import assert_lse, assert_o_bf16, to64
+from parity_util import assert_lse, assert_o, rounding_context, to64
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -32,9 +35,11 @@ def _case(B, H, Hkv, Nq, Nk, d, causal, kv=None, num_splits=0, seed=3):
     check_device_status()
     g = H // Hkv
     kvn = None if kv is None else np.asarray(kv, dtype=np.int32)
-    ro, rl = oracle.fwd_rect(to64(q), np.repeat(to64(k), g, axis=1), np.repeat(to64(v), g, axis=1), scale,
-                             causal=causal, kv_lens=kvn)
-    assert_o_bf16(to64(o), ro)
+    kr, vr = np.repeat(to64(k), g, axis=1), np.repeat(to64(v), g, axis=1)
+    run = lambda qq, vv: oracle.fwd_rect(qq, kr, vv, scale, causal=causal, kv_lens=kvn)
+    ro, rl = run(to64(q), vr)
+    nvis, absref = rounding_context(run, to64(q), vr)
+    assert_o(to64(o), ro, nvis=nvis, absref=absref)
     assert_lse(to64(lse), rl)
 
 
@@ -84,7 +89,7 @@ def test_decode_128k_cache_sampled_heads():
     for h in (0, 21):
         ro, rl = oracle.fwd_rect(to64(q[:, h:h + 1]), to64(k[:, h // g:h // g + 1]), to64(v[:, h // g:h // g + 1]),
                                  1.0 / math.sqrt(d), causal=True)
-        assert_o_bf16(to64(o[:, h:h + 1]), ro)
+        assert_o(to64(o[:, h:h + 1]), ro)
         assert_lse(to64(lse[:, h:h + 1]), rl)
 
 

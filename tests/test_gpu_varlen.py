@@ -15,7 +15,7 @@ import torch
 import oracle
 from exact_tiled_attention_10_gb300 import backward_varlen, check_device_status, forward_varlen
 from exact_tiled_attention_10_gb300.inputs import randn
-from parity_util import O_TOL, assert_close_abs, assert_grad, assert_lse, assert_o_bf16, to64
+from parity_util import FEW_KEYS, assert_grad, assert_lse, assert_o, rounding_context, to64
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -44,6 +44,8 @@ def _case(lens, H, Hkv, d, causal, seed, deterministic=False, window=None):
     # reference, one sequence at a time
     ref = {n: np.zeros(t.shape) for n, t in (("o", q), ("dq", q), ("dk", k), ("dv", v))}
     ref_lse = np.zeros((H, T))
+    nvis = np.full((T, H), FEW_KEYS, dtype=np.float64)
+    absref = np.zeros((T, H, d))
     a = 0
     for n in lens:
         if n > 0:
@@ -55,11 +57,17 @@ def _case(lens, H, Hkv, d, causal, seed, deterministic=False, window=None):
             ref["dk"][sl] = r["dk"][0].reshape(Hkv, g, n, d).sum(axis=1).transpose(1, 0, 2)
             ref["dv"][sl] = r["dv"][0].reshape(Hkv, g, n, d).sum(axis=1).transpose(1, 0, 2)
             ref_lse[:, sl] = r["lse"][0]
+            if window is not None:
+                kr = per(k, g)
+                nv, ab = rounding_context(lambda qq, vv: oracle.fwd(qq, kr, vv, scale, causal=causal, window=window),
+                                          per(q, 1), per(v, g))
+                nvis[sl] = nv[0].T
+                absref[sl] = ab[0].transpose(1, 0, 2)
         a += n
     if window is None:
-        assert_close_abs(to64(o), ref["o"], O_TOL, "O")
-    else:  # narrow windows: rows average a few value rows (see the window tests)
-        assert_o_bf16(to64(o), ref["o"])
+        assert_o(to64(o), ref["o"])
+    else:  # narrow windows: rows with few keys take the rounding bound (see the window tests)
+        assert_o(to64(o), ref["o"], nvis=nvis, absref=absref)
     assert_lse(to64(lse), ref_lse)
     assert_grad(to64(dq), ref["dq"], "dQ")
     assert_grad(to64(dk), ref["dk"], "dK")
@@ -138,7 +146,7 @@ def _case_kv(lens_q, lens_k, H, Hkv, d, causal, seed, deterministic=False):
             ref["dv"][sk] = r["dv"][0].reshape(Hkv, g, nk, d).sum(axis=1).transpose(1, 0, 2)
         aq += nq
         ak += nk
-    assert_close_abs(to64(o), ref["o"], O_TOL, "O")
+    assert_o(to64(o), ref["o"])
     assert_lse(to64(lse), ref_lse)
     assert_grad(to64(dq), ref["dq"], "dQ")
     assert_grad(to64(dk), ref["dk"], "dK")
@@ -157,9 +165,13 @@ def test_varlen_separate_key_ranges_deterministic(causal):
     _case_kv([500, 129, 64], [700, 129, 1000], 4, 1, 128, causal, seed=141, deterministic=True)
 
 
-@pytest.mark.parametrize("causal,window", [(True, (100, 0)), (False, (64, 37))])
-def test_varlen_sliding_window_deterministic(causal, window):
-    _case([300, 1, 0, 129, 520, 64], 4, 2, 128, causal, seed=171 + window[0], window=window, deterministic=True)
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal,window", [(True, (100, 0)), (False, (64, 37)), (False, (-1, 20)), (True, (300, -1))])
+def test_varlen_sliding_window_deterministic(d, causal, window):
+    """The deterministic packed-window backward: d = 64 (128-query steps, so the
+    first visitor of a query block is max(0, i * 128 - left) / 128) and d = 128
+    (64-query steps), two-sided and one-sided windows."""
+    _case([300, 1, 0, 129, 520, 64], 4, 2, d, causal, seed=171 + d + window[0], window=window, deterministic=True)
 
 
 def test_varlen_separate_key_ranges_decode_mix():
