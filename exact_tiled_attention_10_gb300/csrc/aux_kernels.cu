@@ -84,28 +84,44 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const void* __restrict__ o
     }
 }
 
-// dQ[r, :] = scale * dQ_acc[r, :] for the N real rows of every head.
+// dQ[r, :] = scale * dQ_acc[r, :] for the N real rows of every head.  Each
+// thread converts U 8-element groups per pass, all loads issued before the
+// stores, so that enough reads stay in flight to keep HBM busy.
 template <bool OUT_F32>
 __global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ acc, void* __restrict__ dq, float scale,
                                                      int BH, int N, int Np, int D) {
+    constexpr int U = 4;
     const long groups_per_row = D / 8;
     const long total = (long)BH * N * groups_per_row;
-    for (long g = (long)blockIdx.x * blockDim.x + threadIdx.x; g < total; g += (long)gridDim.x * blockDim.x) {
-        const long row = g / groups_per_row;
-        const int c = (int)(g - row * groups_per_row) * 8;
-        const long bh = row / N;
-        const long i = row - bh * N;
-        const float4* src = reinterpret_cast<const float4*>(acc + ((size_t)bh * Np + i) * D + c);
-        const float4 a = __ldg(src), b = __ldg(src + 1);
-        const size_t e = (size_t)row * D + c;
-        if constexpr (OUT_F32) {
-            float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(dq) + e);
-            dst[0] = make_float4(a.x * scale, a.y * scale, a.z * scale, a.w * scale);
-            dst[1] = make_float4(b.x * scale, b.y * scale, b.z * scale, b.w * scale);
-        } else {
-            *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(dq) + e) =
-                make_uint4(pack_bf16x2(a.x * scale, a.y * scale), pack_bf16x2(a.z * scale, a.w * scale),
-                           pack_bf16x2(b.x * scale, b.y * scale), pack_bf16x2(b.z * scale, b.w * scale));
+    const long stride = (long)gridDim.x * blockDim.x;
+    for (long g0 = (long)blockIdx.x * blockDim.x + threadIdx.x; g0 < total; g0 += U * stride) {
+        float4 a[U], b[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const long g = g0 + u * stride;
+            if (g >= total) continue;
+            const long row = g / groups_per_row;
+            const int c = (int)(g - row * groups_per_row) * 8;
+            const long bh = row / N;
+            const long i = row - bh * N;
+            const float4* src = reinterpret_cast<const float4*>(acc + ((size_t)bh * Np + i) * D + c);
+            a[u] = __ldg(src);
+            b[u] = __ldg(src + 1);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const long g = g0 + u * stride;
+            if (g >= total) continue;
+            const size_t e = (size_t)g * 8;  // row * D + c
+            if constexpr (OUT_F32) {
+                float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(dq) + e);
+                dst[0] = make_float4(a[u].x * scale, a[u].y * scale, a[u].z * scale, a[u].w * scale);
+                dst[1] = make_float4(b[u].x * scale, b[u].y * scale, b[u].z * scale, b[u].w * scale);
+            } else {
+                *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(dq) + e) = make_uint4(
+                    pack_bf16x2(a[u].x * scale, a[u].y * scale), pack_bf16x2(a[u].z * scale, a[u].w * scale),
+                    pack_bf16x2(b[u].x * scale, b[u].y * scale), pack_bf16x2(b[u].z * scale, b[u].w * scale));
+            }
         }
     }
 }
@@ -317,46 +333,74 @@ __device__ __forceinline__ SharedDivisor shared_divisor(float s) {
 
 __device__ __forceinline__ bool shared_divisor_ok(float s) { return s > 0x1p-100f && s < 0x1p100f; }
 
-// One CTA (256 threads) per (head, 64-row block); d = 128 -> 8192 elements,
-// 32 per thread, read once and kept in registers across the block's absmax
-// reduction.  s = amax / 448 and x / s are IEEE float32 divisions (x / s by
-// SharedDivisor, which gives the same quotients); the conversion rounds to
-// nearest even and saturates to +-448.
+// One CTA iteration (256 threads) per (head, 64-row block); d = 128 -> 8192
+// elements, 32 per thread, read once and kept in registers across the
+// block's absmax reduction.  The loads of the CTA's next block are issued
+// before the current block is reduced and written, so each thread keeps two
+// blocks' worth of reads in flight.  s = amax / 448 and x / s are IEEE
+// float32 divisions (x / s by SharedDivisor, which gives the same quotients);
+// the conversion rounds to nearest even and saturates to +-448.
 // The blocks of up to three tensors in one launch (Q, K, V): tensor t has
 // rows[t] = B * heads_t heads of N rows each.
-__global__ void __launch_bounds__(256) quantize_fp8_kernel(QuantJobs jobs, int N, int D, int nblk) {
+struct QuantBlock {
+    const __nv_bfloat16* x;
+    uint8_t* x8;
+    float* scale;
+    size_t base;  // first element of the block
+    int ng;       // 8-element groups in the block
+};
+
+__device__ __forceinline__ QuantBlock quant_block(const QuantJobs& jobs, long gblk, long n0, long n1, int N, int D,
+                                                  int nblk) {
+    const int t = gblk < n0 ? 0 : gblk < n1 ? 1 : 2;
+    const long blk = gblk - (t == 0 ? 0 : t == 1 ? n0 : n1);
+    const long bh = blk / nblk;
+    const int r0 = (int)(blk - bh * nblk) * 64;
+    // selects, not indexing: the parameter arrays stay in the constant bank
+    QuantBlock b;
+    b.x = reinterpret_cast<const __nv_bfloat16*>(t == 0 ? jobs.x[0] : t == 1 ? jobs.x[1] : jobs.x[2]);
+    b.x8 = reinterpret_cast<uint8_t*>(t == 0 ? jobs.x8[0] : t == 1 ? jobs.x8[1] : jobs.x8[2]);
+    b.scale = (t == 0 ? jobs.scales[0] : t == 1 ? jobs.scales[1] : jobs.scales[2]) + blk;
+    b.base = ((size_t)bh * N + r0) * D;
+    b.ng = min(64, N - r0) * (D / 8);
+    return b;
+}
+
+__global__ void __launch_bounds__(256) quantize_fp8_kernel(const __grid_constant__ QuantJobs jobs, int N, int D, int nblk) {
     constexpr int G = 4;  // uint4 groups (8 elements) per thread: 256 * 4 * 8 = 64 rows x 128
     __shared__ float red[2][8];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int per_row = D / 8;  // uint4 groups per row
     const long n0 = (long)jobs.heads[0] * nblk, n1 = n0 + (long)jobs.heads[1] * nblk;
     const long total = n1 + (long)jobs.heads[2] * nblk;
-    int par = 0;
-    for (long gblk = blockIdx.x; gblk < total; gblk += gridDim.x, par ^= 1) {
-        const int t = gblk < n0 ? 0 : gblk < n1 ? 1 : 2;
-        const long blk = gblk - (t == 0 ? 0 : t == 1 ? n0 : n1);
-        const __nv_bfloat16* __restrict__ x = reinterpret_cast<const __nv_bfloat16*>(jobs.x[t]);
-        uint8_t* __restrict__ x8 = reinterpret_cast<uint8_t*>(jobs.x8[t]);
-        float* __restrict__ scales = jobs.scales[t];
-        const long bh = blk / nblk;
-        const int ib = (int)(blk - bh * nblk);
-        const int r0 = ib * 64;
-        const int rows = min(64, N - r0);
-        const size_t base = ((size_t)bh * N + r0) * D;
-        const int ng = rows * per_row;
-        uint4 raw[G];
+    auto load = [&](const QuantBlock& b, uint4 (&raw)[G]) {
 #pragma unroll
         for (int i = 0; i < G; ++i) {
             const int g = threadIdx.x + i * 256;
-            raw[i] = (g < ng) ? __ldg(reinterpret_cast<const uint4*>(x + base) + g) : make_uint4(0u, 0u, 0u, 0u);
+            raw[i] = (g < b.ng) ? __ldg(reinterpret_cast<const uint4*>(b.x + b.base) + g) : make_uint4(0u, 0u, 0u, 0u);
         }
+    };
+    long gblk = blockIdx.x;
+    if (gblk >= total) return;
+    QuantBlock nb = quant_block(jobs, gblk, n0, n1, N, D, nblk);
+    uint4 nraw[G];
+    load(nb, nraw);
+    int par = 0;
+    for (; gblk < total; gblk += gridDim.x, par ^= 1) {
+        const QuantBlock b = nb;
+        uint4 raw[G];
+#pragma unroll
+        for (int i = 0; i < G; ++i) raw[i] = nraw[i];
+        if (gblk + gridDim.x < total) {  // the next block's reads go out now
+            nb = quant_block(jobs, gblk + gridDim.x, n0, n1, N, D, nblk);
+            load(nb, nraw);
+        }
+        float f[G][8];
         float amax = 0.f;
 #pragma unroll
         for (int i = 0; i < G; ++i) {
-            float f[8];
-            unpack8(raw[i], f);
+            unpack8(raw[i], f[i]);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fabsf(f[k]));
+            for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fabsf(f[i][k]));
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
@@ -366,21 +410,27 @@ __global__ void __launch_bounds__(256) quantize_fp8_kernel(QuantJobs jobs, int N
 #pragma unroll
         for (int w = 1; w < 8; ++w) m = fmaxf(m, red[par][w]);
         const float s = (m > 0.f) ? __fdiv_rn(m, 448.f) : 1.f;
-        if (threadIdx.x == 0) scales[blk] = s;
-        const SharedDivisor dv = shared_divisor(s);
-        const bool fast = shared_divisor_ok(s);  // uniform over the CTA
+        if (threadIdx.x == 0) *b.scale = s;
+        if (shared_divisor_ok(s)) {  // uniform over the CTA
+            const SharedDivisor dv = shared_divisor(s);
+#pragma unroll
+            for (int i = 0; i < G; ++i)
+#pragma unroll
+                for (int k = 0; k < 8; ++k) f[i][k] = dv.div(f[i][k]);
+        } else {
+#pragma unroll
+            for (int i = 0; i < G; ++i)
+#pragma unroll
+                for (int k = 0; k < 8; ++k) f[i][k] = __fdiv_rn(f[i][k], s);
+        }
 #pragma unroll
         for (int i = 0; i < G; ++i) {
             const int g = threadIdx.x + i * 256;
-            if (g >= ng) continue;
-            float f[8];
-            unpack8(raw[i], f);
-#pragma unroll
-            for (int k = 0; k < 8; ++k) f[k] = fast ? dv.div(f[k]) : __fdiv_rn(f[k], s);
+            if (g >= b.ng) continue;
             uint2 out;
-            out.x = pack_e4m3x4(f[0], f[1], f[2], f[3]);
-            out.y = pack_e4m3x4(f[4], f[5], f[6], f[7]);
-            reinterpret_cast<uint2*>(x8 + base)[g] = out;
+            out.x = pack_e4m3x4(f[i][0], f[i][1], f[i][2], f[i][3]);
+            out.y = pack_e4m3x4(f[i][4], f[i][5], f[i][6], f[i][7]);
+            reinterpret_cast<uint2*>(b.x8 + b.base)[g] = out;
         }
     }
 }

@@ -117,7 +117,12 @@ struct Cfg {
     static constexpr int B_SFULL = B_VEMPTY + VSTAGES, B_PFULL = B_SFULL + 2;
     static constexpr int B_OFULL = B_PFULL + 2, B_OEMPTY = B_OFULL + 2;
     static constexpr int B_DONE = B_OEMPTY + 2;
-    static constexpr int NBAR = B_DONE + 1;
+    // bf16: P is handed to the MMA warp in two halves of the key block (keys
+    // [0, BC/2) complete on B_PHALF, the whole block on B_PFULL), so that the
+    // first half of P V runs while the softmax computes the second half
+    static constexpr bool SPLITP = !FP8;
+    static constexpr int B_PHALF = B_DONE + 1;
+    static constexpr int NBAR = B_PHALF + 2;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM = OFF_MISC + 16 + 1024;  // + base alignment slack
     static constexpr uint32_t FMT = FP8 ? kFmtE4M3 : kFmtBF16;
@@ -433,11 +438,12 @@ __device__ __forceinline__ void issue_S(uint32_t d_tmem, uint64_t q_desc, uint64
     }
 }
 
-// O_t (+)= P_t V over the keys; P_t from TMEM, V MN-major (head dim contiguous)
-template <class C>
+// O_t (+)= P_t V over the keys; P_t from TMEM, V MN-major (head dim contiguous).
+// KK0 / KK1: the range of K steps issued (the whole block by default).
+template <class C, int KK0 = 0, int KK1 = C::PV_STEPS>
 __device__ __forceinline__ void issue_PV(uint32_t o_tmem, uint32_t p_tmem, uint64_t v_desc, bool accumulate) {
 #pragma unroll
-    for (int kk = 0; kk < C::PV_STEPS; ++kk) {
+    for (int kk = KK0; kk < KK1; ++kk) {
         const uint64_t b = desc_add(v_desc, kk * C::KSTEP * 128);
         const uint32_t acc = (accumulate || kk > 0) ? 1u : 0u;
         if constexpr (C::FP8)
@@ -458,18 +464,21 @@ __device__ __forceinline__ float2 exp2_pair(float2 x, int q) {
 // columns in TMEM as the A operand of the P V product (bf16 pairs, or E4M3
 // quadruples with the value-scale fold lg).  Returns the row sums: l (exact
 // weights, divided by the fold) and, for FP8, lq (the E4M3-rounded weights).
-template <class C, bool POLY>
+// CH0 / CH1: the range of chunks (of CH columns) computed; the whole block by
+// default.
+template <class C, bool POLY, int CH0 = 0, int CH1 = -1>
 __device__ __forceinline__ void exp_block(const float (&s)[C::BC], const float (&cm)[2], const float (&lg)[2],
                                           const float (&inv_w)[2], float mb, uint32_t tS, float& lsum,
                                           float& lqsum, float* smax = nullptr) {
     constexpr int CH = C::FP8 ? 64 : 32;  // columns per 16-word TMEM store
+    constexpr int CHE = CH1 < 0 ? C::BC / CH : CH1;
     lsum = 0.f;
     lqsum = 0.f;
     // with smax: also the max of the raw scores of the block (3-input max on
     // the ALU pipe, four independent chains)
     float mxc[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-    for (int ch = 0; ch < C::BC / CH; ++ch) {
+    for (int ch = CH0; ch < CHE; ++ch) {
         const int h = (ch * CH) / (C::BC / 2);
         const float2 cs2 = make_float2(cm[h], cm[h]), cb2 = make_float2(lg[h] - mb, lg[h] - mb);
         uint32_t w[16];
@@ -553,6 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(BAR(C::B_PFULL + t), 128);
             mbar_init(BAR(C::B_OFULL + t), 1);
             mbar_init(BAR(C::B_OEMPTY + t), 128);
+            mbar_init(BAR(C::B_PHALF + t), 128);
         }
         mbar_init(BAR(C::B_DONE), 1);
         *abort_flag = 0;
@@ -770,8 +780,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                             }
                             continue;
                         }
-                        if (!(ok = wait_bounded_warp(BAR(C::B_PFULL + t), pph[t], abort_flag, p.err, kErrWaitFwdMma))) break;
-                        pph[t] ^= 1;
+                        // bf16: the first half of P V as soon as that half of P is in TMEM
+                        if (!(ok = wait_bounded_warp(BAR((C::SPLITP ? C::B_PHALF : C::B_PFULL) + t), pph[t],
+                                                     abort_flag, p.err, kErrWaitFwdMma)))
+                            break;
                         if (j == ta) {
                             if (!(ok = wait_bounded_warp(BAR(C::B_OEMPTY + t), oeph[t] ^ 1, abort_flag, p.err, kErrWaitFwdMma))) break;
                             oeph[t] ^= 1;
@@ -781,7 +793,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                             vw = true;
                         }
                         tc_fence_after();
-                        issue_PV<C>(tO(t), tS(t), v_desc(vst), j > ta);
+                        if constexpr (C::SPLITP) {
+                            issue_PV<C, 0, C::PV_STEPS / 2>(tO(t), tS(t), v_desc(vst), j > ta);
+                            if (!(ok = wait_bounded_warp(BAR(C::B_PFULL + t), pph[t], abort_flag, p.err, kErrWaitFwdMma)))
+                                break;
+                            tc_fence_after();
+                            issue_PV<C, C::PV_STEPS / 2, C::PV_STEPS>(tO(t), tS(t), v_desc(vst), true);
+                        } else {
+                            issue_PV<C>(tO(t), tS(t), v_desc(vst), j > ta);
+                        }
+                        pph[t] ^= 1;
                         if (j == te - 1) {
                             mma_commit_w(BAR(C::B_OFULL + t));
                         } else {
@@ -967,6 +988,40 @@ __global__ void __launch_bounds__(kThreads, 1)
                         exp_block<C, true>(s, cm, lg, inv_w, mb, tS, lsum, lqsum);
                     l += lsum;
                     lq += lqsum;
+                } else if constexpr (C::SPLITP) {
+                    // the block's row max first; the reference moves (and O is
+                    // rescaled: S(j) complete means P V(j-1) has completed) only
+                    // when it grew by more than kRescaleSlack
+                    const float mx = row_max<C::BC>(s) * cm[0];
+                    if (j == 0) {
+                        m = mx;
+                    } else {
+                        const bool need = mx > m + kRescaleSlack;
+                        if (__any_sync(0xffffffffu, need)) {
+                            float alpha = 1.f;
+                            if (need) {
+                                alpha = ex2_approx(m - mx);  // 0 when m = -inf
+                                m = mx;
+                                l *= alpha;
+                            }
+                            rescale_o(alpha);
+                        }
+                    }
+                    const float mb = (m == -INFINITY) ? 0.f : m;
+                    float lsum2;
+                    constexpr int NCH = C::BC / 32;
+                    if (need_mask)
+                        exp_block<C, false, 0, NCH / 2>(s, cm, lg, inv_w, mb, tS, lsum, lqsum);
+                    else
+                        exp_block<C, true, 0, NCH / 2>(s, cm, lg, inv_w, mb, tS, lsum, lqsum);
+                    tmem_st_wait();
+                    tc_fence_before();
+                    mbar_arrive(BAR(C::B_PHALF + t));
+                    if (need_mask)
+                        exp_block<C, false, NCH / 2, NCH>(s, cm, lg, inv_w, mb, tS, lsum2, lqsum);
+                    else
+                        exp_block<C, true, NCH / 2, NCH>(s, cm, lg, inv_w, mb, tS, lsum2, lqsum);
+                    l += lsum + lsum2;
                 } else {
                     if (j == 0) m = row_max<C::BC>(s) * cm[0];  // first block: exact reference
                     float mb = (m == -INFINITY) ? 0.f : m;
