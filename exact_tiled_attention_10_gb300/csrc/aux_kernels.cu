@@ -30,6 +30,33 @@ __device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
     }
 }
 
+// L2 eviction priorities for the backward's streaming kernels.  The
+// preprocess reads O and dO once (evict first) and zeroes the float32 dQ
+// accumulator with evict-last stores, so that the zeroed lines are still in
+// L2 when the main kernel's bulk additions reach them; the dQ conversion reads
+// the accumulator for the last time (evict first).
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t p;
+    asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_last() {
+    uint64_t p;
+    asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+// 16-byte read-only load that skips L1, with an L2 eviction policy
+__device__ __forceinline__ uint4 ld_stream(const void* ptr, uint64_t pol) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(ptr), "l"(pol));
+    return v;
+}
+// 16 zero bytes, with an L2 eviction policy
+__device__ __forceinline__ void st_keep_zero(void* ptr, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %1, %1, %1}, %2;" :: "l"(ptr), "r"(0u), "l"(pol) : "memory");
+}
+
 // One group of LPR lanes per row; each lane covers 8 consecutive elements.
 template <int D, bool IN_F32>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const void* __restrict__ o, const void* __restrict__ dout,
@@ -43,6 +70,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const void* __restrict__ o
     const long total_rows = (long)BH * Np;
     const long warps = (long)gridDim.x * (blockDim.x / 32);
     const long gw = (long)blockIdx.x * (blockDim.x / 32) + (threadIdx.x / 32);
+    const uint64_t pol_first = policy_evict_first(), pol_last = policy_evict_last();
     for (long r0 = gw * RPW; r0 < total_rows; r0 += warps * RPW) {
         const long r = r0 + sub;
         const bool valid_row = r < total_rows;
@@ -59,8 +87,8 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const void* __restrict__ o
                 a[0] = o0.x; a[1] = o0.y; a[2] = o0.z; a[3] = o0.w; a[4] = o1.x; a[5] = o1.y; a[6] = o1.z; a[7] = o1.w;
                 b[0] = g0.x; b[1] = g0.y; b[2] = g0.z; b[3] = g0.w; b[4] = g1.x; b[5] = g1.y; b[6] = g1.z; b[7] = g1.w;
             } else {
-                unpack8(__ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(o) + e)), a);
-                unpack8(__ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(dout) + e)), b);
+                unpack8(ld_stream(reinterpret_cast<const __nv_bfloat16*>(o) + e, pol_first), a);
+                unpack8(ld_stream(reinterpret_cast<const __nv_bfloat16*>(dout) + e, pol_first), b);
             }
 #pragma unroll
             for (int k = 0; k < 8; ++k) acc = fmaf(a[k], b[k], acc);
@@ -69,8 +97,8 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const void* __restrict__ o
         for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
         if (valid_row) {
             float* qa = dq_acc + (size_t)r * D + sl * 8;
-            reinterpret_cast<float4*>(qa)[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-            reinterpret_cast<float4*>(qa)[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+            st_keep_zero(qa, pol_last);
+            st_keep_zero(qa + 4, pol_last);
             if (sl == 0) {
                 float l2 = INFINITY;
                 if (i < N) {
@@ -94,6 +122,7 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ a
     const long groups_per_row = D / 8;
     const long total = (long)BH * N * groups_per_row;
     const long stride = (long)gridDim.x * blockDim.x;
+    const uint64_t pol_first = policy_evict_first();
     for (long g0 = (long)blockIdx.x * blockDim.x + threadIdx.x; g0 < total; g0 += U * stride) {
         float4 a[U], b[U];
 #pragma unroll
@@ -105,8 +134,9 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ a
             const long bh = row / N;
             const long i = row - bh * N;
             const float4* src = reinterpret_cast<const float4*>(acc + ((size_t)bh * Np + i) * D + c);
-            a[u] = __ldg(src);
-            b[u] = __ldg(src + 1);
+            const uint4 ua = ld_stream(src, pol_first), ub = ld_stream(src + 1, pol_first);
+            a[u] = make_float4(__uint_as_float(ua.x), __uint_as_float(ua.y), __uint_as_float(ua.z), __uint_as_float(ua.w));
+            b[u] = make_float4(__uint_as_float(ub.x), __uint_as_float(ub.y), __uint_as_float(ub.z), __uint_as_float(ub.w));
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
