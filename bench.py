@@ -26,6 +26,7 @@ Prints ONE JSON line (rank 0).  --impl reference times the fp64 CPU oracle
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import math
@@ -252,13 +253,22 @@ class Step:
         self.flush = t(L2_FLUSH_BYTES, dt=torch.uint8)
         # split-key plans (automatic): the causal bf16 forward is never split;
         # the non-causal FP8 forward may be (its merge kernel is part of the call)
-        has_kv = int(self.kv is not None)
-        self.split_bf16 = self.lib.fa_fwd_split_count(B, H, N, d, int(causal), has_kv, 0)
-        self.split_fp8 = self.lib.fa_fwd_split_count(B, H, N, d, 0, 0, 0)
-        self.sws_bytes = max(self.lib.fa_fwd_split_workspace_size(B, H, N, d, int(causal), has_kv, 0),
-                             self.lib.fa_fwd_split_workspace_size(B, H, N, d, 0, 0, 0))
+        has_kv = self.kv is not None
+        self.split_bf16 = fa.split_count(B, H, N, d, causal, has_kv, 0)
+        self.split_fp8 = fa.split_count(B, H, N, d, False, False, 0)
+        self.sws_bytes = max(fa.split_workspace_size(B, H, N, d, causal, has_kv, 0),
+                             fa.split_workspace_size(B, H, N, d, False, False, 0))
         self.sws = t(max(self.sws_bytes, 256), dt=torch.uint8)
         self.scale = 1.0 / math.sqrt(d)
+        # the two forwards as fa_attn_fwd parameter blocks (automatic key split)
+        self.p_fwd = fa.attn_params(batch=B, heads=H, seqlen_q=N, head_dim=d, scale=self.scale, causal=int(causal),
+                                    kv_lens=self.kv, num_splits=0, q=self.q, k=self.k, v=self.v, o=self.o,
+                                    lse=self.lse, workspace=self.sws, workspace_bytes=self.sws_bytes)
+        if fp8:
+            self.p_fp8 = fa.attn_params(dtype=fa.FA_E4M3, batch=B, heads=H, seqlen_q=N, head_dim=d, scale=self.scale,
+                                        num_splits=0, q=self.x8[0], k=self.x8[1], v=self.x8[2], q_scale=self.sc[0],
+                                        k_scale=self.sc[1], v_scale=self.sc[2], o=self.o8, lse=self.lse8,
+                                        workspace=self.sws, workspace_bytes=self.sws_bytes)
         F = flops_fwd(w, causal)
         self.flops = {"fwd": F, "bwd_pre": 0.0, "bwd_main": 2.5 * F, "bwd_dq": 0.0,
                       "quant_fp8": 0.0, "fwd_fp8": flops_fwd(w, False)}
@@ -290,8 +300,7 @@ class Step:
         kv = None if self.kv is None else p(self.kv)
         rec = (lambda i: events[i].record()) if events is not None else (lambda i: None)
         rec(0)
-        self._ck(lib.fa_fwd_split(p(self.q), p(self.k), p(self.v), p(self.o), p(self.lse), B, H, N, d,
-                                  self.scale, int(self.causal), kv, 0, p(self.sws), self.sws_bytes, s))
+        self._ck(lib.fa_attn_fwd(ctypes.byref(self.p_fwd), s))
         rec(1)
         self._ck(lib.fa_bwd_preprocess(p(self.o), p(self.lse), p(self.do), B, H, N, d, p(self.ws),
                                        self.ws_bytes, s))
@@ -308,9 +317,7 @@ class Step:
                                          p(self.x8[2]), p(self.sc[0]), p(self.sc[1]), p(self.sc[2]), B, H, H, N, d,
                                          s))
         rec(5)
-        self._ck(lib.fa_fwd_fp8_split(p(self.x8[0]), p(self.x8[1]), p(self.x8[2]), p(self.sc[0]),
-                                      p(self.sc[1]), p(self.sc[2]), p(self.o8), p(self.lse8), B, H, N, d,
-                                      self.scale, 0, None, 0, p(self.sws), self.sws_bytes, s))
+        self._ck(lib.fa_attn_fwd(ctypes.byref(self.p_fp8), s))
         rec(6)
 
     def flush_l2(self):

@@ -21,11 +21,11 @@ from typing import Optional, Tuple
 
 import torch
 
-__all__ = ["forward", "forward_split", "forward_varlen", "backward_varlen", "backward",
-           "block_lists", "forward_block_sparse", "backward_block_sparse", "quantize_fp8_qkv", "forward_rect", "backward_rect", "quantize_fp8", "forward_fp8", "forward_fp8_split",
-           "split_count", "split_workspace_size", "check_device_status",
-           "selftest_wait_timeout",
-           "bwd_workspace_size", "fwd_workspace_size", "library_path", "load_library", "FAError"]
+__all__ = ["forward", "forward_split", "forward_varlen", "backward_varlen", "backward", "forward_bnhd",
+           "backward_bnhd", "block_lists", "forward_block_sparse", "backward_block_sparse", "quantize_fp8_qkv",
+           "forward_rect", "backward_rect", "rect_split_count", "quantize_fp8", "forward_fp8", "forward_fp8_split",
+           "split_count", "split_workspace_size", "check_device_status", "selftest_wait_timeout", "attn_params",
+           "AttnParams", "bwd_workspace_size", "fwd_workspace_size", "library_path", "load_library", "FAError"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libfa_gb300.so")
@@ -33,72 +33,61 @@ _lock = threading.Lock()
 _lib = None
 
 FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = 0, 1, 2, 3, 4
-FA_BF16, FA_F32 = 0, 1
+FA_BF16, FA_F32, FA_E4M3 = 0, 1, 2
+FA_LAYOUT_BHND, FA_LAYOUT_BNHD, FA_LAYOUT_PACKED = 0, 1, 2
 _STATUS = {1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_CUDA", 4: "FA_ERR_TIMEOUT"}
+
+
+class AttnParams(ctypes.Structure):
+    """ctypes mirror of fa_attn_params (include/fa.h), field for field."""
+    _fields_ = [
+        ("struct_size", ctypes.c_size_t),
+        ("dtype", ctypes.c_int), ("layout", ctypes.c_int),
+        ("batch", ctypes.c_int), ("heads", ctypes.c_int), ("kv_heads", ctypes.c_int),
+        ("seqlen_q", ctypes.c_int), ("seqlen_k", ctypes.c_int), ("head_dim", ctypes.c_int),
+        ("total_q", ctypes.c_int), ("total_k", ctypes.c_int),
+        ("scale", ctypes.c_float),
+        ("causal", ctypes.c_int),
+        ("window_left", ctypes.c_int), ("window_right", ctypes.c_int),
+        ("num_splits", ctypes.c_int), ("block_c", ctypes.c_int), ("deterministic", ctypes.c_int),
+        ("kv_lens", ctypes.c_void_p),
+        ("cu_seqlens_q", ctypes.c_void_p), ("cu_seqlens_k", ctypes.c_void_p),
+        ("block_row_ptr", ctypes.c_void_p), ("block_col_idx", ctypes.c_void_p),
+        ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+        ("q_scale", ctypes.c_void_p), ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
+        ("o", ctypes.c_void_p), ("lse", ctypes.c_void_p),
+        ("dout", ctypes.c_void_p), ("dq", ctypes.c_void_p), ("dk", ctypes.c_void_p), ("dv", ctypes.c_void_p),
+        ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+    ]
+
 
 # C signatures of include/fa.h, as ctypes argtypes
 _vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+_pp = ctypes.POINTER(AttnParams)
 _SIGS = {
     "fa_version": ([], _i),
     "fa_last_error": ([], ctypes.c_char_p),
     "fa_check_device_status": ([_vp], _i),
     "fa_selftest_wait_timeout": ([ctypes.c_uint, _vp, _vp], _i),
+    "fa_selftest_quantiser_division": ([_vp, _vp, _i, _sz, _vp, _vp, _vp], _i),
     "fa_fwd": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _vp], _i),
-    "fa_fwd_workspace_size": ([_i, _i, _i, _i, _i], _sz),
-    "fa_fwd_ex": ([_i, _i, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _vp, _sz, _vp], _i),
-    "fa_bwd_workspace_size": ([_i, _i, _i, _i, _i], _sz),
+    "fa_bwd_workspace_size": ([_i, _i, _i, _i], _sz),
     "fa_bwd": ([_vp] * 9 + [_i, _i, _i, _i, _f, _i, _vp, _vp, _sz, _vp], _i),
-    "fa_bwd_ex": ([_i] + [_vp] * 9 + [_i, _i, _i, _i, _f, _i, _vp, _vp, _sz, _vp], _i),
+    "fa_fp8_num_blocks": ([_i], _i),
+    "fa_quantize_fp8": ([_vp, _vp, _vp, _i, _i, _i, _i, _vp], _i),
+    "fa_quantize_fp8_qkv": ([_vp] * 9 + [_i] * 5 + [_vp], _i),
+    "fa_fwd_fp8": ([_vp] * 8 + [_i, _i, _i, _i, _f, _i, _vp, _vp], _i),
+    "fa_attn_params_init": ([_pp], None),
+    "fa_attn_fwd_workspace_size": ([_pp], _sz),
+    "fa_attn_fwd_splits": ([_pp], _i),
+    "fa_attn_bwd_workspace_size": ([_pp], _sz),
+    "fa_attn_fwd": ([_pp, _vp], _i),
+    "fa_attn_bwd": ([_pp, _vp], _i),
     "fa_bwd_preprocess": ([_vp, _vp, _vp, _i, _i, _i, _i, _vp, _sz, _vp], _i),
     "fa_bwd_main": ([_vp] * 6 + [_i, _i, _i, _i, _f, _i, _vp, _vp, _sz, _vp], _i),
     "fa_bwd_dq": ([_vp, _i, _i, _i, _i, _f, _vp, _sz, _vp], _i),
     "fa_bwd_noalloc_max_scratch": ([], _sz),
     "fa_bwd_noalloc": ([_vp] * 9 + [_i, _i, _i, _i, _f, _i, _vp, _vp], _i),
-    "fa_fp8_num_blocks": ([_i], _i),
-    "fa_quantize_fp8": ([_vp, _vp, _vp, _i, _i, _i, _i, _vp], _i),
-    "fa_fwd_fp8": ([_vp] * 8 + [_i, _i, _i, _i, _f, _i, _vp, _vp], _i),
-    "fa_fwd_gqa": ([_vp] * 5 + [_i, _i, _i, _i, _i, _f, _i, _vp, _vp], _i),
-    "fa_fwd_window": ([_vp] * 5 + [_i, _i, _i, _i, _i, _f, _i, _i, _i, _vp, _vp], _i),
-    "fa_bwd_window": ([_vp] * 9 + [_i, _i, _i, _i, _i, _f, _i, _i, _i, _vp, _vp, _sz, _vp], _i),
-    "fa_fwd_block_sparse": ([_vp] * 5 + [_i, _i, _i, _i, _i, _f, _i, _vp, _vp, _vp, _vp], _i),
-    "fa_bwd_block_sparse_workspace_size": ([_i] * 4, _sz),
-    "fa_bwd_gqa_workspace_size": ([_i] * 5, _sz),
-    "fa_bwd_deterministic_workspace_size": ([_i] * 5, _sz),
-    "fa_bwd_deterministic": ([_vp] * 9 + [_i, _i, _i, _i, _i, _f, _i, _vp, _vp, _sz, _vp], _i),
-    "fa_selftest_quantiser_division": ([_vp, _vp, _i, _sz, _vp, _vp, _vp], _i),
-    "fa_quantize_fp8_qkv": ([_vp] * 9 + [_i] * 5 + [_vp], _i),
-    "fa_fwd_rect_workspace_size": ([_i] * 7, _sz),
-    "fa_fwd_rect_split_count": ([_i] * 7, _i),
-    "fa_fwd_rect": ([_vp] * 5 + [_i] * 6 + [_f, _i, _vp, _i, _vp, _sz, _vp], _i),
-    "fa_bwd_rect_workspace_size": ([_i] * 6, _sz),
-    "fa_bwd_rect": ([_vp] * 9 + [_i] * 6 + [_f, _i, _vp, _vp, _sz, _vp], _i),
-    "fa_bwd_block_sparse": ([_vp] * 9 + [_i, _i, _i, _i, _i, _f, _i, _vp, _vp, _vp, _vp, _sz, _vp], _i),
-    "fa_fwd_varlen": ([_vp] * 6 + [_i, _i, _i, _i, _i, _i, _f, _i, _vp], _i),
-    "fa_bwd_varlen_workspace_size": ([_i] * 4, _sz),
-    "fa_bwd_varlen": ([_vp] * 10 + [_i, _i, _i, _i, _i, _i, _f, _i, _vp, _sz, _vp], _i),
-    "fa_fwd_bnhd": ([_vp] * 5 + [_i, _i, _i, _i, _i, _f, _i, _vp], _i),
-    "fa_fwd_varlen_kv": ([_vp] * 7 + [_i] * 7 + [_f, _i, _vp], _i),
-    "fa_fwd_fp8_gqa": ([_vp] * 8 + [_i] * 5 + [_f, _i, _vp, _vp], _i),
-    "fa_fwd_varlen_window": ([_vp] * 6 + [_i] * 6 + [_f, _i, _i, _i, _vp], _i),
-    "fa_bwd_varlen_window": ([_vp] * 10 + [_i] * 6 + [_f, _i, _i, _i, _i, _vp, _sz, _vp], _i),
-    "fa_bwd_varlen_kv_workspace_size": ([_i] * 7, _sz),
-    "fa_bwd_varlen_kv": ([_vp] * 11 + [_i] * 8 + [_f, _i, _i, _vp, _sz, _vp], _i),
-    "fa_bwd_bnhd_workspace_size": ([_i] * 4, _sz),
-    "fa_bwd_bnhd": ([_vp] * 9 + [_i, _i, _i, _i, _i, _f, _i, _vp, _sz, _vp], _i),
-    "fa_bwd_varlen_deterministic_workspace_size": ([_i] * 5, _sz),
-    "fa_bwd_varlen_deterministic": ([_vp] * 10 + [_i, _i, _i, _i, _i, _i, _f, _i, _vp, _sz, _vp], _i),
-    "fa_bwd_bnhd_deterministic_workspace_size": ([_i] * 5, _sz),
-    "fa_bwd_bnhd_deterministic": ([_vp] * 9 + [_i, _i, _i, _i, _i, _f, _i, _vp, _sz, _vp], _i),
-    "fa_bwd_window_deterministic": ([_vp] * 9 + [_i, _i, _i, _i, _i, _f, _i, _i, _i, _vp, _vp, _sz, _vp], _i),
-    "fa_bwd_rect_deterministic_workspace_size": ([_i] * 6, _sz),
-    "fa_bwd_block_sparse_deterministic_workspace_size": ([_i] * 5, _sz),
-    "fa_bwd_block_sparse_deterministic": ([_vp] * 9 + [_i] * 5 + [_f, _i, _vp, _vp, _vp, _vp, _sz, _vp], _i),
-    "fa_bwd_rect_deterministic": ([_vp] * 9 + [_i] * 6 + [_f, _i, _vp, _vp, _sz, _vp], _i),
-    "fa_bwd_gqa": ([_vp] * 9 + [_i, _i, _i, _i, _i, _f, _i, _vp, _vp, _sz, _vp], _i),
-    "fa_fwd_split_workspace_size": ([_i] * 7, _sz),
-    "fa_fwd_split_count": ([_i] * 7, _i),
-    "fa_fwd_split": ([_vp] * 5 + [_i, _i, _i, _i, _f, _i, _vp, _i, _vp, _sz, _vp], _i),
-    "fa_fwd_fp8_split": ([_vp] * 8 + [_i, _i, _i, _i, _f, _i, _vp, _i, _vp, _sz, _vp], _i),
 }
 
 
@@ -161,14 +150,58 @@ def _kv(kv_lens: Optional[torch.Tensor], B: int, device) -> Optional[torch.Tenso
     return kv
 
 
+def attn_params(**fields) -> AttnParams:
+    """An fa_attn_params block initialised by the library (defaults: bf16,
+    [B,H,N,d], no window, no split), with `fields` set; tensors are passed as
+    their device pointers."""
+    lib = load_library()
+    p = AttnParams()
+    lib.fa_attn_params_init(ctypes.byref(p))
+    for name, val in fields.items():
+        if isinstance(val, torch.Tensor):
+            val = val.data_ptr()
+        setattr(p, name, val)
+    return p
+
+
+def _scratch(nbytes: int, device, given: Optional[torch.Tensor]) -> Optional[torch.Tensor]:
+    if nbytes == 0:
+        return None
+    if given is not None and given.numel() * given.element_size() >= nbytes:
+        return given
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def _run(p: AttnParams, t: torch.Tensor, bwd: bool, workspace: Optional[torch.Tensor] = None):
+    """Size the workspace for p, then one fa_attn_fwd / fa_attn_bwd call."""
+    lib = load_library()
+    nbytes = int((lib.fa_attn_bwd_workspace_size if bwd else lib.fa_attn_fwd_workspace_size)(ctypes.byref(p)))
+    ws = _scratch(nbytes, t.device, workspace)
+    p.workspace = None if ws is None else ws.data_ptr()
+    p.workspace_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check((lib.fa_attn_bwd if bwd else lib.fa_attn_fwd)(ctypes.byref(p), _stream(t)))
+
+
+def _dtype(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return FA_BF16
+    if t.dtype == torch.float32:
+        return FA_F32
+    raise ValueError("dtype must be bfloat16 or float32")
+
+
 def fwd_workspace_size(dtype: torch.dtype, B: int, H: int, N: int, d: int) -> int:
-    dt = FA_F32 if dtype == torch.float32 else FA_BF16
-    return int(load_library().fa_fwd_workspace_size(dt, B, H, N, d))
+    """Scratch of the forward on [B,H,N,d] tensors of `dtype` (float32 only)."""
+    p = attn_params(dtype=FA_F32 if dtype == torch.float32 else FA_BF16, batch=B, heads=H, seqlen_q=N,
+                    head_dim=d, scale=1.0)
+    return int(load_library().fa_attn_fwd_workspace_size(ctypes.byref(p)))
 
 
 def bwd_workspace_size(dtype: torch.dtype, B: int, H: int, N: int, d: int) -> int:
-    dt = FA_F32 if dtype == torch.float32 else FA_BF16
-    return int(load_library().fa_bwd_workspace_size(dt, B, H, N, d))
+    """Scratch of the backward on [B,H,N,d] tensors of `dtype`."""
+    p = attn_params(dtype=FA_F32 if dtype == torch.float32 else FA_BF16, batch=B, heads=H, seqlen_q=N,
+                    head_dim=d, scale=1.0)
+    return int(load_library().fa_attn_bwd_workspace_size(ctypes.byref(p)))
 
 
 def _window(window) -> Tuple[int, int]:
@@ -182,6 +215,15 @@ def _window(window) -> Tuple[int, int]:
     return wl, wr
 
 
+def _bhnd(q, k, v, name="q [B,H,N,d]; k, v [B,Hkv,N,d] with H a multiple of Hkv; one dtype"):
+    B, H, N, d = q.shape
+    Hkv = k.shape[1]
+    if (k.shape != (B, Hkv, N, d) or v.shape != k.shape or k.dtype != q.dtype or v.dtype != q.dtype
+            or H % Hkv != 0):
+        raise ValueError(name)
+    return B, H, Hkv, N, d
+
+
 def forward(q, k, v, causal: bool = False, scale: Optional[float] = None, kv_lens=None,
             block_c: int = 0, out: Optional[torch.Tensor] = None,
             lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
@@ -191,63 +233,34 @@ def forward(q, k, v, causal: bool = False, scale: Optional[float] = None, kv_len
     multiple of Hkv; query head h uses key/value head h // (H // Hkv)).
     window = (left, right): sliding window, key j visible to query i only if
     i - left <= j <= i + right (-1 = unbounded; bf16 only)."""
-    lib = load_library()
     _need_cuda(q, k, v)
-    B, H, N, d = q.shape
-    Hkv = k.shape[1]
-    if (k.shape != (B, Hkv, N, d) or v.shape != k.shape or k.dtype != q.dtype or v.dtype != q.dtype
-            or H % Hkv != 0):
-        raise ValueError("q [B,H,N,d]; k, v [B,Hkv,N,d] with H a multiple of Hkv; one dtype")
-    if q.dtype not in (torch.bfloat16, torch.float32):
-        raise ValueError("dtype must be bfloat16 or float32")
+    B, H, Hkv, N, d = _bhnd(q, k, v)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     kv = _kv(kv_lens, B, q.device)
     o = torch.empty_like(q) if out is None else out
     l = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
     _need_cuda(o, l)
     wl, wr = _window(window)
-    if wl >= 0 or wr >= 0:
-        if q.dtype != torch.bfloat16:
-            raise ValueError("the sliding window needs bfloat16 tensors")
-        _check(lib.fa_fwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(l), B, H, Hkv, N, d, scale,
-                                 int(bool(causal)), wl, wr, _ptr(kv), _stream(q)))
-        return o, l
-    if Hkv != H:
-        if q.dtype != torch.bfloat16:
-            raise ValueError("shared key/value heads need bfloat16 tensors")
-        _check(lib.fa_fwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(l), B, H, Hkv, N, d, scale,
-                              int(bool(causal)), _ptr(kv), _stream(q)))
-        return o, l
-    dt = FA_F32 if q.dtype == torch.float32 else FA_BF16
-    wsz = int(lib.fa_fwd_workspace_size(dt, B, H, N, d))
-    ws = workspace
-    if wsz and (ws is None or ws.numel() * ws.element_size() < wsz):
-        ws = torch.empty(wsz, dtype=torch.uint8, device=q.device)
-    _check(lib.fa_fwd_ex(dt, int(block_c), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(l), B, H, N, d,
-                         scale, int(bool(causal)), _ptr(kv), _ptr(ws) if wsz else None, wsz,
-                         _stream(q)))
+    p = attn_params(dtype=_dtype(q), batch=B, heads=H, kv_heads=Hkv, seqlen_q=N, head_dim=d, scale=scale,
+                    causal=int(bool(causal)), window_left=wl, window_right=wr, block_c=int(block_c),
+                    kv_lens=kv, q=q, k=k, v=v, o=o, lse=l)
+    _run(p, q, False, workspace)
     return o, l
 
 
 def split_count(B: int, H: int, N: int, d: int, causal: bool = False, kv_lens: bool = False,
                 num_splits: int = 0) -> int:
-    """Number of key ranges fa_fwd_split uses for this call (1 = not split)."""
-    return int(load_library().fa_fwd_split_count(B, H, N, d, int(bool(causal)), int(bool(kv_lens)),
-                                                 int(num_splits)))
+    """Number of key ranges the split-key forward uses for this call (1 = not split)."""
+    p = attn_params(batch=B, heads=H, seqlen_q=N, head_dim=d, scale=1.0, causal=int(bool(causal)),
+                    kv_lens=4096 if kv_lens else None, num_splits=int(num_splits))
+    return int(load_library().fa_attn_fwd_splits(ctypes.byref(p)))
 
 
 def split_workspace_size(B: int, H: int, N: int, d: int, causal: bool = False, kv_lens: bool = False,
                          num_splits: int = 0) -> int:
-    return int(load_library().fa_fwd_split_workspace_size(B, H, N, d, int(bool(causal)), int(bool(kv_lens)),
-                                                          int(num_splits)))
-
-
-def _split_ws(B, H, N, d, causal, kv, num_splits, workspace, device):
-    wsz = split_workspace_size(B, H, N, d, causal, kv is not None, num_splits)
-    ws = workspace
-    if wsz and (ws is None or ws.numel() * ws.element_size() < wsz):
-        ws = torch.empty(wsz, dtype=torch.uint8, device=device)
-    return (_ptr(ws) if wsz else None), wsz
+    p = attn_params(batch=B, heads=H, seqlen_q=N, head_dim=d, scale=1.0, causal=int(bool(causal)),
+                    kv_lens=4096 if kv_lens else None, num_splits=int(num_splits))
+    return int(load_library().fa_attn_fwd_workspace_size(ctypes.byref(p)))
 
 
 def forward_split(q, k, v, causal: bool = False, scale: Optional[float] = None, kv_lens=None,
@@ -257,7 +270,6 @@ def forward_split(q, k, v, causal: bool = False, scale: Optional[float] = None, 
     """Split-key bf16 forward (FlashDecoding form): as forward(), with the key
     sequence of each query block cut into ranges merged by a second kernel.
     num_splits 0 = automatic, 1 = none, >= 2 = that many ranges per item."""
-    lib = load_library()
     _need_cuda(q, k, v)
     B, H, N, d = q.shape
     if q.dtype != torch.bfloat16 or k.dtype != q.dtype or v.dtype != q.dtype:
@@ -266,9 +278,9 @@ def forward_split(q, k, v, causal: bool = False, scale: Optional[float] = None, 
     kv = _kv(kv_lens, B, q.device)
     o = torch.empty_like(q) if out is None else out
     l = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
-    wsp, wsz = _split_ws(B, H, N, d, causal, kv, num_splits, workspace, q.device)
-    _check(lib.fa_fwd_split(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(l), B, H, N, d, scale,
-                            int(bool(causal)), _ptr(kv), int(num_splits), wsp, wsz, _stream(q)))
+    p = attn_params(batch=B, heads=H, seqlen_q=N, head_dim=d, scale=scale, causal=int(bool(causal)),
+                    kv_lens=kv, num_splits=int(num_splits), q=q, k=k, v=v, o=o, lse=l)
+    _run(p, q, False, workspace)
     return o, l
 
 
@@ -285,25 +297,28 @@ def block_lists(block_mask, device) -> Tuple[torch.Tensor, torch.Tensor]:
     return row_ptr.to(device), col_idx.to(device)
 
 
+def _lists(row_ptr, col_idx, N):
+    if row_ptr.dtype != torch.int32 or col_idx.dtype != torch.int32 or row_ptr.numel() != (N + 127) // 128 + 1:
+        raise ValueError("row_ptr int32 [ceil(N/128) + 1], col_idx int32")
+
+
 def forward_block_sparse(q, k, v, row_ptr, col_idx, causal: bool = False, scale: Optional[float] = None,
                          kv_lens=None, out: Optional[torch.Tensor] = None,
                          lse: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
     """Block-sparse forward (128 x 128 blocks): query block i attends to the
     key blocks col_idx[row_ptr[i]:row_ptr[i+1]] only (see block_lists)."""
-    lib = load_library()
     _need_cuda(q, k, v, row_ptr, col_idx)
-    B, H, N, d = q.shape
-    Hkv = k.shape[1]
-    if q.dtype != torch.bfloat16 or k.shape != (B, Hkv, N, d) or v.shape != k.shape or H % Hkv != 0:
-        raise ValueError("q [B,H,N,d]; k, v [B,Hkv,N,d] bfloat16 with H a multiple of Hkv")
-    if row_ptr.dtype != torch.int32 or col_idx.dtype != torch.int32 or row_ptr.numel() != (N + 127) // 128 + 1:
-        raise ValueError("row_ptr int32 [ceil(N/128) + 1], col_idx int32")
+    if q.dtype != torch.bfloat16:
+        raise ValueError("block lists take bfloat16 tensors")
+    B, H, Hkv, N, d = _bhnd(q, k, v)
+    _lists(row_ptr, col_idx, N)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     kv = _kv(kv_lens, B, q.device)
     o = torch.empty_like(q) if out is None else out
     l = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
-    _check(lib.fa_fwd_block_sparse(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(l), B, H, Hkv, N, d, scale,
-                                   int(bool(causal)), _ptr(row_ptr), _ptr(col_idx), _ptr(kv), _stream(q)))
+    p = attn_params(batch=B, heads=H, kv_heads=Hkv, seqlen_q=N, head_dim=d, scale=scale, causal=int(bool(causal)),
+                    kv_lens=kv, block_row_ptr=row_ptr, block_col_idx=col_idx, q=q, k=k, v=v, o=o, lse=l)
+    _run(p, q, False)
     return o, l
 
 
@@ -312,24 +327,25 @@ def backward_block_sparse(q, k, v, o, lse, dout, row_ptr, col_idx, causal: bool 
                           deterministic: bool = False):
     """Backward of forward_block_sparse: dQ [B,H,N,d], dK, dV [B,Hkv,N,d].
     deterministic: bitwise reproducible gradients (see backward)."""
-    lib = load_library()
     _need_cuda(q, k, v, o, lse, dout, row_ptr, col_idx)
-    B, H, N, d = q.shape
-    Hkv = k.shape[1]
+    B, H, Hkv, N, d = _bhnd(q, k, v)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     kv = _kv(kv_lens, B, q.device)
-    wsz = int(lib.fa_bwd_block_sparse_deterministic_workspace_size(B, H, Hkv, N, d) if deterministic
-              else lib.fa_bwd_block_sparse_workspace_size(B, H, N, d))
-    ws = workspace
-    if ws is None or ws.numel() * ws.element_size() < wsz:
-        ws = torch.empty(wsz, dtype=torch.uint8, device=q.device)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    fn = lib.fa_bwd_block_sparse_deterministic if deterministic else lib.fa_bwd_block_sparse
-    _check(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
-              _ptr(dv), B, H, Hkv, N, d, scale, int(bool(causal)), _ptr(row_ptr),
-              _ptr(col_idx), _ptr(kv), _ptr(ws), ws.numel() * ws.element_size(),
-              _stream(q)))
+    p = attn_params(batch=B, heads=H, kv_heads=Hkv, seqlen_q=N, head_dim=d, scale=scale, causal=int(bool(causal)),
+                    kv_lens=kv, block_row_ptr=row_ptr, block_col_idx=col_idx, deterministic=int(bool(deterministic)),
+                    q=q, k=k, v=v, o=o, lse=lse, dout=dout, dq=dq, dk=dk, dv=dv)
+    _run(p, q, True, workspace)
     return dq, dk, dv
+
+
+def _rect(q, k, v):
+    B, H, Nq, d = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    if (q.dtype != torch.bfloat16 or k.dtype != q.dtype or v.dtype != q.dtype or k.shape != (B, Hkv, Nk, d)
+            or v.shape != k.shape or H % Hkv != 0):
+        raise ValueError("q [B,H,Nq,d]; k, v [B,Hkv,Nk,d] bfloat16 with H a multiple of Hkv")
+    return B, H, Hkv, Nq, Nk, d
 
 
 def forward_rect(q, k, v, causal: bool = False, scale: Optional[float] = None, kv_lens=None,
@@ -338,47 +354,38 @@ def forward_rect(q, k, v, causal: bool = False, scale: Optional[float] = None, k
     """Nq queries against Nk keys (decoding against a key/value cache,
     cross-attention): q [B,H,Nq,d], k, v [B,Hkv,Nk,d] bf16.  Causal: the
     queries are the last Nq positions (query i sees keys j <= i + Nk - Nq)."""
-    lib = load_library()
     _need_cuda(q, k, v)
-    B, H, Nq, d = q.shape
-    Hkv, Nk = k.shape[1], k.shape[2]
-    if (q.dtype != torch.bfloat16 or k.dtype != q.dtype or v.dtype != q.dtype or k.shape != (B, Hkv, Nk, d)
-            or v.shape != k.shape or H % Hkv != 0):
-        raise ValueError("q [B,H,Nq,d]; k, v [B,Hkv,Nk,d] bfloat16 with H a multiple of Hkv")
+    B, H, Hkv, Nq, Nk, d = _rect(q, k, v)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     kv = _kv(kv_lens, B, q.device)
     o = torch.empty_like(q) if out is None else out
     l = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device) if lse is None else lse
-    wsz = int(lib.fa_fwd_rect_workspace_size(B, H, Hkv, Nq, Nk, d, int(num_splits)))
-    ws = workspace
-    if wsz and (ws is None or ws.numel() * ws.element_size() < wsz):
-        ws = torch.empty(wsz, dtype=torch.uint8, device=q.device)
-    _check(lib.fa_fwd_rect(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(l), B, H, Hkv, Nq, Nk, d, scale,
-                           int(bool(causal)), _ptr(kv), int(num_splits), _ptr(ws) if wsz else None, wsz,
-                           _stream(q)))
+    p = attn_params(batch=B, heads=H, kv_heads=Hkv, seqlen_q=Nq, seqlen_k=Nk, head_dim=d, scale=scale,
+                    causal=int(bool(causal)), kv_lens=kv, num_splits=int(num_splits), q=q, k=k, v=v, o=o, lse=l)
+    _run(p, q, False, workspace)
     return o, l
+
+
+def rect_split_count(B: int, H: int, Hkv: int, Nq: int, Nk: int, d: int, num_splits: int = 0) -> int:
+    """Key ranges per item of the rectangular forward (1 = not split)."""
+    p = attn_params(batch=B, heads=H, kv_heads=Hkv, seqlen_q=Nq, seqlen_k=Nk, head_dim=d, scale=1.0,
+                    num_splits=int(num_splits))
+    return int(load_library().fa_attn_fwd_splits(ctypes.byref(p)))
 
 
 def backward_rect(q, k, v, o, lse, dout, causal: bool = False, scale: Optional[float] = None, kv_lens=None,
                   workspace: Optional[torch.Tensor] = None, deterministic: bool = False):
     """Backward of forward_rect: dQ [B,H,Nq,d], dK, dV [B,Hkv,Nk,d].
     deterministic: bitwise reproducible gradients (see backward)."""
-    lib = load_library()
     _need_cuda(q, k, v, o, lse, dout)
-    B, H, Nq, d = q.shape
-    Hkv, Nk = k.shape[1], k.shape[2]
+    B, H, Hkv, Nq, Nk, d = _rect(q, k, v)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     kv = _kv(kv_lens, B, q.device)
-    wsz = int(lib.fa_bwd_rect_deterministic_workspace_size(B, H, Hkv, Nq, Nk, d) if deterministic
-              else lib.fa_bwd_rect_workspace_size(B, H, Hkv, Nq, Nk, d))
-    ws = workspace
-    if ws is None or ws.numel() * ws.element_size() < wsz:
-        ws = torch.empty(wsz, dtype=torch.uint8, device=q.device)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    fn = lib.fa_bwd_rect_deterministic if deterministic else lib.fa_bwd_rect
-    _check(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
-              B, H, Hkv, Nq, Nk, d, scale, int(bool(causal)), _ptr(kv), _ptr(ws),
-              ws.numel() * ws.element_size(), _stream(q)))
+    p = attn_params(batch=B, heads=H, kv_heads=Hkv, seqlen_q=Nq, seqlen_k=Nk, head_dim=d, scale=scale,
+                    causal=int(bool(causal)), kv_lens=kv, deterministic=int(bool(deterministic)),
+                    q=q, k=k, v=v, o=o, lse=lse, dout=dout, dq=dq, dk=dk, dv=dv)
+    _run(p, q, True, workspace)
     return dq, dk, dv
 
 
@@ -387,6 +394,15 @@ def _cu(cu_seqlens, device):
     if cu.dim() != 1 or cu.numel() < 2:
         raise ValueError("cu_seqlens must be a 1-D tensor of batch + 1 offsets")
     return cu
+
+
+def _packed(q, k, v, cu_seqlens_k):
+    T, H, d = q.shape
+    Hkv, Tk = k.shape[1], k.shape[0]
+    if (q.dtype != torch.bfloat16 or k.dtype != q.dtype or v.dtype != q.dtype or k.shape != (Tk, Hkv, d)
+            or v.shape != k.shape or H % Hkv != 0 or (cu_seqlens_k is None and Tk != T)):
+        raise ValueError("q [total,H,d], k, v [total(_k),Hkv,d] bfloat16 with H a multiple of Hkv")
+    return T, Tk, H, Hkv, d
 
 
 def forward_varlen(q, k, v, cu_seqlens, max_seqlen: int, causal: bool = False,
@@ -399,30 +415,18 @@ def forward_varlen(q, k, v, cu_seqlens, max_seqlen: int, causal: bool = False,
     ranges in k, v [total_k, Hkv, d] (flash_attn_varlen_func's cu_seqlens_k;
     with causal, the queries are each sequence's last positions).  window:
     the sliding window (see forward), within each sequence."""
-    lib = load_library()
     _need_cuda(q, k, v)
-    T, H, d = q.shape
-    Hkv = k.shape[1]
-    Tk = k.shape[0]
-    if (q.dtype != torch.bfloat16 or k.dtype != q.dtype or v.dtype != q.dtype or k.shape != (Tk, Hkv, d)
-            or v.shape != k.shape or H % Hkv != 0 or (cu_seqlens_k is None and Tk != T)):
-        raise ValueError("q [total,H,d], k, v [total(_k),Hkv,d] bfloat16 with H a multiple of Hkv")
+    T, Tk, H, Hkv, d = _packed(q, k, v, cu_seqlens_k)
     cu = _cu(cu_seqlens, q.device)
+    cuk = None if cu_seqlens_k is None else _cu(cu_seqlens_k, q.device)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     o = torch.empty_like(q) if out is None else out
     l = torch.empty((H, T), dtype=torch.float32, device=q.device) if lse is None else lse
     wl, wr = _window(window)
-    if wl >= 0 or wr >= 0:
-        _check(lib.fa_fwd_varlen_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(l), _ptr(cu), cu.numel() - 1, T,
-                                        int(max_seqlen), H, Hkv, d, scale, int(bool(causal)), wl, wr, _stream(q)))
-        return o, l
-    if cu_seqlens_k is not None:
-        cuk = _cu(cu_seqlens_k, q.device)
-        _check(lib.fa_fwd_varlen_kv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(l), _ptr(cu), _ptr(cuk), cu.numel() - 1,
-                                    T, Tk, int(max_seqlen), H, Hkv, d, scale, int(bool(causal)), _stream(q)))
-        return o, l
-    _check(lib.fa_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(l), _ptr(cu), cu.numel() - 1, T,
-                             int(max_seqlen), H, Hkv, d, scale, int(bool(causal)), _stream(q)))
+    p = attn_params(layout=FA_LAYOUT_PACKED, batch=cu.numel() - 1, heads=H, kv_heads=Hkv, seqlen_q=int(max_seqlen),
+                    head_dim=d, total_q=T, total_k=Tk, scale=scale, causal=int(bool(causal)), window_left=wl,
+                    window_right=wr, cu_seqlens_q=cu, cu_seqlens_k=cuk, q=q, k=k, v=v, o=o, lse=l)
+    _run(p, q, False)
     return o, l
 
 
@@ -439,14 +443,14 @@ def forward_bnhd(q, k, v, causal: bool = False, scale: Optional[float] = None,
                  out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None):
     """Forward on flash_attn_func's layout: q [B,N,H,d], k, v [B,N,Hkv,d]
     (bf16).  Returns O [B,N,H,d] and LSE [B,H,N] (float32)."""
-    lib = load_library()
     _need_cuda(q, k, v)
     B, N, H, Hkv, d = _bnhd_shapes(q, k, v)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     o = torch.empty_like(q) if out is None else out
     l = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
-    _check(lib.fa_fwd_bnhd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(l), B, N, H, Hkv, d, scale,
-                           int(bool(causal)), _stream(q)))
+    p = attn_params(layout=FA_LAYOUT_BNHD, batch=B, heads=H, kv_heads=Hkv, seqlen_q=N, head_dim=d, scale=scale,
+                    causal=int(bool(causal)), q=q, k=k, v=v, o=o, lse=l)
+    _run(p, q, False)
     return o, l
 
 
@@ -455,20 +459,14 @@ def backward_bnhd(q, k, v, o, lse, dout, causal: bool = False, scale: Optional[f
     """dQ [B,N,H,d], dK, dV [B,N,Hkv,d] of forward_bnhd (dK, dV summed over
     the query heads sharing a key/value head).  deterministic: bitwise
     reproducible gradients (see backward)."""
-    lib = load_library()
     _need_cuda(q, k, v, o, lse, dout)
     B, N, H, Hkv, d = _bnhd_shapes(q, k, v)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    wsz = int(lib.fa_bwd_bnhd_deterministic_workspace_size(B, N, H, Hkv, d) if deterministic
-              else lib.fa_bwd_bnhd_workspace_size(B, N, H, d))
-    ws = workspace
-    if ws is None or ws.numel() * ws.element_size() < wsz:
-        ws = torch.empty(wsz, dtype=torch.uint8, device=q.device)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    fn = lib.fa_bwd_bnhd_deterministic if deterministic else lib.fa_bwd_bnhd
-    _check(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
-              _ptr(dv), B, N, H, Hkv, d, scale, int(bool(causal)), _ptr(ws),
-              ws.numel() * ws.element_size(), _stream(q)))
+    p = attn_params(layout=FA_LAYOUT_BNHD, batch=B, heads=H, kv_heads=Hkv, seqlen_q=N, head_dim=d, scale=scale,
+                    causal=int(bool(causal)), deterministic=int(bool(deterministic)),
+                    q=q, k=k, v=v, o=o, lse=lse, dout=dout, dq=dq, dk=dk, dv=dv)
+    _run(p, q, True, workspace)
     return dq, dk, dv
 
 
@@ -479,49 +477,19 @@ def backward_varlen(q, k, v, o, lse, dout, cu_seqlens, max_seqlen: int, causal: 
     """Backward of forward_varlen: dQ [total, H, d], dK, dV [total(_k), Hkv, d].
     deterministic: bitwise reproducible gradients (see backward).
     cu_seqlens_k / max_seqlen_k: separate key ranges (see forward_varlen)."""
-    lib = load_library()
     _need_cuda(q, k, v, o, lse, dout)
-    T, H, d = q.shape
-    Hkv = k.shape[1]
+    T, Tk, H, Hkv, d = _packed(q, k, v, cu_seqlens_k)
     cu = _cu(cu_seqlens, q.device)
-    batch = cu.numel() - 1
+    cuk = None if cu_seqlens_k is None else _cu(cu_seqlens_k, q.device)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     wl, wr = _window(window)
-    if wl >= 0 or wr >= 0:
-        wsz = int(lib.fa_bwd_varlen_deterministic_workspace_size(batch, int(max_seqlen), H, Hkv, d) if deterministic
-                  else lib.fa_bwd_varlen_workspace_size(batch, int(max_seqlen), H, d))
-        ws = workspace
-        if ws is None or ws.numel() * ws.element_size() < wsz:
-            ws = torch.empty(wsz, dtype=torch.uint8, device=q.device)
-        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-        _check(lib.fa_bwd_varlen_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
-                                        _ptr(dk), _ptr(dv), _ptr(cu), batch, T, int(max_seqlen), H, Hkv, d, scale,
-                                        int(bool(causal)), wl, wr, int(bool(deterministic)), _ptr(ws),
-                                        ws.numel() * ws.element_size(), _stream(q)))
-        return dq, dk, dv
-    if cu_seqlens_k is not None:
-        cuk = _cu(cu_seqlens_k, q.device)
-        mk = int(max_seqlen if max_seqlen_k is None else max_seqlen_k)
-        wsz = int(lib.fa_bwd_varlen_kv_workspace_size(batch, int(max_seqlen), mk, H, Hkv, d, int(bool(deterministic))))
-        ws = workspace
-        if ws is None or ws.numel() * ws.element_size() < wsz:
-            ws = torch.empty(wsz, dtype=torch.uint8, device=q.device)
-        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-        _check(lib.fa_bwd_varlen_kv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
-                                    _ptr(dv), _ptr(cu), _ptr(cuk), batch, T, k.shape[0], int(max_seqlen), mk, H, Hkv,
-                                    d, scale, int(bool(causal)), int(bool(deterministic)), _ptr(ws),
-                                    ws.numel() * ws.element_size(), _stream(q)))
-        return dq, dk, dv
-    wsz = int(lib.fa_bwd_varlen_deterministic_workspace_size(batch, int(max_seqlen), H, Hkv, d) if deterministic
-              else lib.fa_bwd_varlen_workspace_size(batch, int(max_seqlen), H, d))
-    ws = workspace
-    if ws is None or ws.numel() * ws.element_size() < wsz:
-        ws = torch.empty(wsz, dtype=torch.uint8, device=q.device)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    fn = lib.fa_bwd_varlen_deterministic if deterministic else lib.fa_bwd_varlen
-    _check(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
-              _ptr(dv), _ptr(cu), batch, T, int(max_seqlen), H, Hkv, d, scale,
-              int(bool(causal)), _ptr(ws), ws.numel() * ws.element_size(), _stream(q)))
+    mk = 0 if cu_seqlens_k is None else int(max_seqlen if max_seqlen_k is None else max_seqlen_k)
+    p = attn_params(layout=FA_LAYOUT_PACKED, batch=cu.numel() - 1, heads=H, kv_heads=Hkv, seqlen_q=int(max_seqlen),
+                    seqlen_k=mk, head_dim=d, total_q=T, total_k=Tk, scale=scale, causal=int(bool(causal)),
+                    window_left=wl, window_right=wr, deterministic=int(bool(deterministic)), cu_seqlens_q=cu,
+                    cu_seqlens_k=cuk, q=q, k=k, v=v, o=o, lse=lse, dout=dout, dq=dq, dk=dk, dv=dv)
+    _run(p, q, True, workspace)
     return dq, dk, dv
 
 
@@ -533,58 +501,22 @@ def backward(q, k, v, o, lse, dout, causal: bool = False, scale: Optional[float]
     """dQ, dK, dV of L = sum(O * dout).  With fewer key/value heads (k, v
     [B,Hkv,N,d]), dK and dV sum over the query heads sharing each one.
     window: the forward's sliding window (see forward).
-    deterministic: bitwise-reproducible gradients (bf16, no window): the dQ
-    parts are added in key-block order."""
-    lib = load_library()
+    deterministic: bitwise-reproducible gradients (bf16): the dQ parts are
+    added in key-block order."""
     _need_cuda(q, k, v, o, lse, dout)
-    B, H, N, d = q.shape
-    Hkv = k.shape[1]
+    B, H, Hkv, N, d = _bhnd(q, k, v)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     kv = _kv(kv_lens, B, q.device)
-    dt = FA_F32 if q.dtype == torch.float32 else FA_BF16
     wl, wr = _window(window)
-    grouped = Hkv != H or wl >= 0 or wr >= 0
-    if deterministic:
-        if dt != FA_BF16 or H % Hkv != 0:
-            raise ValueError("the deterministic backward takes bfloat16 tensors and H a multiple of Hkv")
-        wsz = int(lib.fa_bwd_deterministic_workspace_size(B, H, Hkv, N, d))
-    else:
-        wsz = int(lib.fa_bwd_gqa_workspace_size(B, H, Hkv, N, d) if grouped and dt == FA_BF16
-                  else lib.fa_bwd_workspace_size(dt, B, H, N, d))
-    ws = workspace
-    if ws is None or ws.numel() * ws.element_size() < wsz:
-        ws = torch.empty(wsz, dtype=torch.uint8, device=q.device)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     _need_cuda(dq, dk, dv)
-    if deterministic and (wl >= 0 or wr >= 0):
-        _check(lib.fa_bwd_window_deterministic(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
-                                               _ptr(dk), _ptr(dv), B, H, Hkv, N, d, scale, int(bool(causal)), wl, wr,
-                                               _ptr(kv), _ptr(ws), ws.numel() * ws.element_size(), _stream(q)))
-        return dq, dk, dv
-    if deterministic:
-        _check(lib.fa_bwd_deterministic(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
-                                        _ptr(dk), _ptr(dv), B, H, Hkv, N, d, scale, int(bool(causal)), _ptr(kv),
-                                        _ptr(ws), ws.numel() * ws.element_size(), _stream(q)))
-        return dq, dk, dv
-    if wl >= 0 or wr >= 0:
-        if q.dtype != torch.bfloat16 or H % Hkv != 0:
-            raise ValueError("the sliding window needs bfloat16 tensors and H a multiple of Hkv")
-        _check(lib.fa_bwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
-                                 _ptr(dk), _ptr(dv), B, H, Hkv, N, d, scale, int(bool(causal)), wl, wr,
-                                 _ptr(kv), _ptr(ws), ws.numel() * ws.element_size(), _stream(q)))
-        return dq, dk, dv
-    if Hkv != H:
-        if q.dtype != torch.bfloat16 or H % Hkv != 0:
-            raise ValueError("shared key/value heads need bfloat16 tensors and H a multiple of Hkv")
-        _check(lib.fa_bwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
-                              _ptr(dk), _ptr(dv), B, H, Hkv, N, d, scale, int(bool(causal)), _ptr(kv),
-                              _ptr(ws), ws.numel() * ws.element_size(), _stream(q)))
-        return dq, dk, dv
-    _check(lib.fa_bwd_ex(dt, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
-                         _ptr(dk), _ptr(dv), B, H, N, d, scale, int(bool(causal)), _ptr(kv),
-                         _ptr(ws), ws.numel() * ws.element_size(), _stream(q)))
+    p = attn_params(dtype=_dtype(q), batch=B, heads=H, kv_heads=Hkv, seqlen_q=N, head_dim=d, scale=scale,
+                    causal=int(bool(causal)), window_left=wl, window_right=wr,
+                    deterministic=int(bool(deterministic)), kv_lens=kv,
+                    q=q, k=k, v=v, o=o, lse=lse, dout=dout, dq=dq, dk=dk, dv=dv)
+    _run(p, q, True, workspace)
     return dq, dk, dv
 
 
@@ -626,7 +558,14 @@ def forward_fp8(q8, k8, v8, sq, sk, sv, causal: bool = False, scale: Optional[fl
                 kv_lens=None, out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None):
     """FP8 E4M3 forward with per-64-row-block scales; O bf16, LSE float32.
     k8, v8 may have fewer heads (shared key/value heads)."""
-    lib = load_library()
+    return forward_fp8_split(q8, k8, v8, sq, sk, sv, causal=causal, scale=scale, kv_lens=kv_lens,
+                             num_splits=1, out=out, lse=lse)
+
+
+def forward_fp8_split(q8, k8, v8, sq, sk, sv, causal: bool = False, scale: Optional[float] = None,
+                      kv_lens=None, num_splits: int = 0, out: Optional[torch.Tensor] = None,
+                      lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None):
+    """Split-key FP8 forward: forward_fp8 with the key ranges of forward_split."""
     _need_cuda(q8, k8, v8, sq, sk, sv)
     B, H, N, d = q8.shape
     Hkv = k8.shape[1]
@@ -634,30 +573,10 @@ def forward_fp8(q8, k8, v8, sq, sk, sv, causal: bool = False, scale: Optional[fl
     kv = _kv(kv_lens, B, q8.device)
     o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q8.device) if out is None else out
     l = torch.empty((B, H, N), dtype=torch.float32, device=q8.device) if lse is None else lse
-    if Hkv != H:
-        _check(lib.fa_fwd_fp8_gqa(_ptr(q8), _ptr(k8), _ptr(v8), _ptr(sq), _ptr(sk), _ptr(sv), _ptr(o),
-                                  _ptr(l), B, H, Hkv, N, d, scale, int(bool(causal)), _ptr(kv), _stream(q8)))
-        return o, l
-    _check(lib.fa_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(v8), _ptr(sq), _ptr(sk), _ptr(sv), _ptr(o),
-                          _ptr(l), B, H, N, d, scale, int(bool(causal)), _ptr(kv), _stream(q8)))
-    return o, l
-
-
-def forward_fp8_split(q8, k8, v8, sq, sk, sv, causal: bool = False, scale: Optional[float] = None,
-                      kv_lens=None, num_splits: int = 0, out: Optional[torch.Tensor] = None,
-                      lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None):
-    """Split-key FP8 forward: forward_fp8 with the key ranges of forward_split."""
-    lib = load_library()
-    _need_cuda(q8, k8, v8, sq, sk, sv)
-    B, H, N, d = q8.shape
-    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    kv = _kv(kv_lens, B, q8.device)
-    o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q8.device) if out is None else out
-    l = torch.empty((B, H, N), dtype=torch.float32, device=q8.device) if lse is None else lse
-    wsp, wsz = _split_ws(B, H, N, d, causal, kv, num_splits, workspace, q8.device)
-    _check(lib.fa_fwd_fp8_split(_ptr(q8), _ptr(k8), _ptr(v8), _ptr(sq), _ptr(sk), _ptr(sv), _ptr(o),
-                                _ptr(l), B, H, N, d, scale, int(bool(causal)), _ptr(kv), int(num_splits),
-                                wsp, wsz, _stream(q8)))
+    p = attn_params(dtype=FA_E4M3, batch=B, heads=H, kv_heads=Hkv, seqlen_q=N, head_dim=d, scale=scale,
+                    causal=int(bool(causal)), kv_lens=kv, num_splits=int(num_splits), q=q8, k=k8, v=v8,
+                    q_scale=sq, k_scale=sk, v_scale=sv, o=o, lse=l)
+    _run(p, q8, False, workspace)
     return o, l
 
 

@@ -163,6 +163,13 @@ BwdLayout bwd_layout(fa_dtype dt, int B, int H, int N, int d) {
     return L;
 }
 
+// Backward scratch (statistics, dQ accumulator; float32 inputs: their bf16
+// copies), 0 for an unsupported shape.
+size_t bwd_ws_bytes(fa_dtype dtype, int B, int H, int N, int d) {
+    if (B <= 0 || H <= 0 || N <= 0 || (d != 64 && d != 128)) return 0;
+    return bwd_layout(dtype, B, H, N, d).total;
+}
+
 // SM count of the current device, or the GB300's 152 when no device is
 // visible (so that the split plan can be inspected on a host without a GPU).
 int sm_count_or_default() {
@@ -671,10 +678,7 @@ fa_status fa_fwd_ex(fa_dtype dtype, int block_c, const void* q, const void* k, c
                     kv_lens, workspace, workspace_bytes, stream);
 }
 
-size_t fa_bwd_workspace_size(fa_dtype dtype, int B, int H, int N, int d) {
-    if (B <= 0 || H <= 0 || N <= 0 || (d != 64 && d != 128)) return 0;
-    return bwd_layout(dtype, B, H, N, d).total;
-}
+size_t fa_bwd_workspace_size(int B, int H, int N, int d) { return bwd_ws_bytes(FA_BF16, B, H, N, d); }
 
 }  // extern "C"
 
@@ -998,7 +1002,7 @@ static size_t sparse_lists_bytes(int N) {
 
 size_t fa_bwd_block_sparse_workspace_size(int B, int H, int N, int d) {
     if (B <= 0 || H <= 0 || N <= 0 || (d != 64 && d != 128)) return 0;
-    return round_up(fa_bwd_workspace_size(FA_BF16, B, H, N, d), 256) + sparse_lists_bytes(N);
+    return round_up(bwd_ws_bytes(FA_BF16, B, H, N, d), 256) + sparse_lists_bytes(N);
 }
 
 fa_status fa_bwd_block_sparse(const void* q, const void* k, const void* v, const void* o, const float* lse,
@@ -1024,7 +1028,7 @@ fa_status fa_bwd_block_sparse(const void* q, const void* k, const void* v, const
     BwdCtx c{};
     FA_TRY(bwd_setup(FA_BF16, B, H, N, d, scale, workspace, workspace_bytes, &c));
     const int nb = (N + 127) / 128;
-    int* col_ptr = reinterpret_cast<int*>(c.ws + round_up(fa_bwd_workspace_size(FA_BF16, B, H, N, d), 256));
+    int* col_ptr = reinterpret_cast<int*>(c.ws + round_up(bwd_ws_bytes(FA_BF16, B, H, N, d), 256));
     int* row_idx = col_ptr + nb + 1;
     cudaError_t e = fa::launch_block_lists_transpose(row_ptr, col_idx, nb, nb, col_ptr, row_idx, stream);
     if (e != cudaSuccess) return cuda_fail(e, "block list transposition launch");
@@ -1036,7 +1040,7 @@ fa_status fa_bwd_block_sparse(const void* q, const void* k, const void* v, const
 
 size_t fa_bwd_rect_workspace_size(int B, int H, int Hkv, int Nq, int Nk, int d) {
     if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0 || Hkv < 1 || H % Hkv != 0 || (d != 64 && d != 128)) return 0;
-    const size_t base = round_up(fa_bwd_workspace_size(FA_BF16, B, H, Nq, d), 256);
+    const size_t base = round_up(bwd_ws_bytes(FA_BF16, B, H, Nq, d), 256);
     const int g = choose_gsplit((long)B * Hkv * ((Nk + 127) / 128), H / Hkv, sm_count_or_default());
     return g > 1 ? base + dkv_part_bytes(g, B, Hkv, Nk, d) : base;
 }
@@ -1067,7 +1071,7 @@ fa_status fa_bwd_rect(const void* q, const void* k, const void* v, const void* o
 
 size_t fa_bwd_gqa_workspace_size(int B, int H, int Hkv, int N, int d) {
     if (B <= 0 || H <= 0 || N <= 0 || Hkv < 1 || H % Hkv != 0 || (d != 64 && d != 128)) return 0;
-    const size_t base = round_up(fa_bwd_workspace_size(FA_BF16, B, H, N, d), 256);
+    const size_t base = round_up(bwd_ws_bytes(FA_BF16, B, H, N, d), 256);
     const int g = choose_gsplit((long)B * Hkv * ((N + 127) / 128), H / Hkv, sm_count_or_default());
     return g > 1 ? base + dkv_part_bytes(g, B, Hkv, N, d) : base;
 }
@@ -1324,7 +1328,7 @@ namespace {
 // rows), A - 1 more float32 dQ accumulators, the turn counters; A from the
 // key blocks (Nk keys).
 size_t det_workspace(int B, int H, int Hkv, int Nq, int Nk, int d) {
-    const size_t base = fa_bwd_workspace_size(FA_BF16, B, H, Nq, d);
+    const size_t base = bwd_ws_bytes(FA_BF16, B, H, Nq, d);
     if (base == 0 || Nk <= 0 || Hkv < 1 || H % Hkv != 0) return 0;
     const int nacc = det_num_acc(B, Hkv, Nk);
     return base + (size_t)(nacc - 1) * det_acc_bytes(B, H, Nq, d) + det_turn_bytes(nacc, B, H, Nq, d);
@@ -1501,6 +1505,305 @@ fa_status fa_fwd_fp8_split(const void* q8, const void* k8, const void* v8, const
 }  // extern "C"
 
 // ---------------------------------------------------------------------------
+// One call per pass: the parameter block of include/fa.h.  attn_plan is the one
+// validation routine of both passes: it names the kernel family a parameter
+// block selects, or refuses the combination (before any launch) with the
+// reason; the entry points then call that family's implementation above.
+// ---------------------------------------------------------------------------
+namespace {
+
+enum class Family {
+    Plain,        // [B,H,N,d] bf16, N_q = N_k, H = Hkv, no window / lists
+    F32,          // float32 tensors
+    Gqa,          // shared key/value heads
+    Window,       // sliding window
+    Sparse,       // block lists
+    Rect,         // N_q != N_k
+    Packed,       // packed sequences (optionally windowed)
+    PackedKv,     // packed sequences with their own key ranges
+    Bnhd,         // flash_attn_func's [B, N, H, d]
+    Fp8,          // E4M3 inputs
+};
+
+struct AttnPlan {
+    Family fam;
+    int Hkv, Nk, total_k;
+    bool window, det;
+};
+
+fa_status attn_plan(const fa_attn_params* a, bool bwd, AttnPlan* pl) {
+    if (!a) return fail(FA_ERR_INVALID_ARG, "params must not be NULL");
+    if (a->struct_size != sizeof(fa_attn_params))
+        return fail(FA_ERR_INVALID_ARG,
+                    "params->struct_size is %zu, this library's fa_attn_params has %zu bytes (initialise it with "
+                    "fa_attn_params_init from the same header version)",
+                    a->struct_size, sizeof(fa_attn_params));
+    if (a->heads <= 0 || a->batch <= 0 || a->seqlen_q <= 0)
+        return fail(FA_ERR_INVALID_ARG, "batch, heads and seqlen_q must be positive");
+    const int Hkv = a->kv_heads ? a->kv_heads : a->heads;
+    if (Hkv < 1 || a->heads % Hkv != 0)
+        return fail(FA_ERR_INVALID_ARG, "heads (%d) must be a multiple of kv_heads (%d)", a->heads, Hkv);
+    if (a->window_left < -1 || a->window_right < -1)
+        return fail(FA_ERR_INVALID_ARG, "window edges must be >= -1 (-1 = unbounded)");
+    if (a->seqlen_k < 0 || a->num_splits < 0 || a->block_c < 0)
+        return fail(FA_ERR_INVALID_ARG, "seqlen_k, num_splits and block_c must be >= 0");
+    if ((a->block_row_ptr == nullptr) != (a->block_col_idx == nullptr))
+        return fail(FA_ERR_INVALID_ARG, "block lists need both block_row_ptr and block_col_idx");
+    pl->Hkv = Hkv;
+    pl->Nk = a->seqlen_k ? a->seqlen_k : a->seqlen_q;
+    pl->total_k = a->total_k ? a->total_k : a->total_q;
+    pl->window = a->window_left >= 0 || a->window_right >= 0;
+    pl->det = a->deterministic != 0;
+    // a nonzero seqlen_k selects the rectangular kernels (also when it equals seqlen_q)
+    const bool sparse = a->block_row_ptr != nullptr, rect = a->seqlen_k != 0;
+    const bool split = a->num_splits != 1;
+    auto refuse = [](const char* what) { return fail(FA_ERR_UNSUPPORTED, "not built: %s", what); };
+    if (bwd && (a->num_splits > 1 || a->block_c)) return refuse("num_splits / block_c in a backward call");
+    if (!bwd && pl->det) return refuse("deterministic in a forward call");
+    switch (a->dtype) {
+    case FA_E4M3:
+        if (bwd) return refuse("FP8 backward (use the bf16 backward)");
+        if (a->layout != FA_LAYOUT_BHND || pl->window || sparse || rect)
+            return refuse("FP8 with the packed or [B,N,H,d] layouts, a window, block lists or N_q != N_k");
+        if (Hkv != a->heads && split) return refuse("a split FP8 forward with shared key/value heads");
+        if (a->block_c) return refuse("block_c with FP8");
+        pl->fam = Family::Fp8;
+        return FA_OK;
+    case FA_F32:
+        if (a->layout != FA_LAYOUT_BHND || pl->window || sparse || rect || Hkv != a->heads || split || pl->det)
+            return refuse("float32 tensors with options beyond causal, kv_lens and block_c");
+        pl->fam = Family::F32;
+        return FA_OK;
+    case FA_BF16:
+        break;
+    default:
+        return fail(FA_ERR_INVALID_ARG, "unknown dtype %d", (int)a->dtype);
+    }
+    if (a->layout == FA_LAYOUT_PACKED) {
+        if (!a->cu_seqlens_q) return fail(FA_ERR_INVALID_ARG, "the packed layout needs cu_seqlens_q");
+        if (a->kv_lens || sparse || split || a->block_c)
+            return refuse("kv_lens, block lists, num_splits or block_c with the packed layout");
+        if (a->total_q <= 0) return fail(FA_ERR_INVALID_ARG, "the packed layout needs total_q > 0");
+        if (a->cu_seqlens_k) {
+            if (pl->window) return refuse("a window with separate packed key ranges");
+            pl->fam = Family::PackedKv;
+        } else {
+            pl->fam = Family::Packed;
+        }
+        return FA_OK;
+    }
+    if (a->layout == FA_LAYOUT_BNHD) {
+        if (a->kv_lens || sparse || pl->window || rect || split || a->block_c)
+            return refuse("kv_lens, block lists, a window, N_q != N_k, num_splits or block_c with the [B,N,H,d] "
+                          "layout (packed sequences cover different lengths)");
+        pl->fam = Family::Bnhd;
+        return FA_OK;
+    }
+    if (a->layout != FA_LAYOUT_BHND) return fail(FA_ERR_INVALID_ARG, "unknown layout %d", (int)a->layout);
+    if (rect) {
+        if (pl->window || sparse || a->block_c) return refuse("a window, block lists or block_c with N_q != N_k");
+        pl->fam = Family::Rect;
+        return FA_OK;
+    }
+    if (sparse) {
+        if (pl->window || split || a->block_c) return refuse("block lists with a window, num_splits or block_c");
+        pl->fam = Family::Sparse;
+        return FA_OK;
+    }
+    if (pl->window) {
+        if (split || a->block_c) return refuse("a window with num_splits or block_c");
+        pl->fam = Family::Window;
+        return FA_OK;
+    }
+    if (Hkv != a->heads) {
+        if (split || a->block_c) return refuse("shared key/value heads with num_splits or block_c");
+        pl->fam = Family::Gqa;
+        return FA_OK;
+    }
+    if (split && a->block_c) return refuse("num_splits with block_c");
+    pl->fam = Family::Plain;
+    return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+void fa_attn_params_init(fa_attn_params* p) {
+    if (!p) return;
+    memset(p, 0, sizeof(*p));
+    p->struct_size = sizeof(fa_attn_params);
+    p->dtype = FA_BF16;
+    p->layout = FA_LAYOUT_BHND;
+    p->window_left = p->window_right = -1;
+    p->num_splits = 1;
+}
+
+size_t fa_attn_fwd_workspace_size(const fa_attn_params* a) {
+    AttnPlan pl;
+    if (attn_plan(a, false, &pl) != FA_OK) return 0;
+    const int B = a->batch, H = a->heads, N = a->seqlen_q, d = a->head_dim;
+    switch (pl.fam) {
+    case Family::Plain:
+    case Family::Fp8:
+        return fa_fwd_split_workspace_size(B, H, N, d, a->causal, a->kv_lens != nullptr, a->num_splits);
+    case Family::Rect:
+        return fa_fwd_rect_workspace_size(B, H, pl.Hkv, N, pl.Nk, d, a->num_splits);
+    case Family::F32:
+        return fa_fwd_workspace_size(FA_F32, B, H, N, d);
+    default:
+        return 0;
+    }
+}
+
+int fa_attn_fwd_splits(const fa_attn_params* a) {
+    AttnPlan pl;
+    if (attn_plan(a, false, &pl) != FA_OK) return 1;
+    const int B = a->batch, H = a->heads, N = a->seqlen_q, d = a->head_dim;
+    if (pl.fam == Family::Plain || pl.fam == Family::Fp8)
+        return fa_fwd_split_count(B, H, N, d, a->causal, a->kv_lens != nullptr, a->num_splits);
+    if (pl.fam == Family::Rect) return fa_fwd_rect_split_count(B, H, pl.Hkv, N, pl.Nk, d, a->num_splits);
+    return 1;
+}
+
+size_t fa_attn_bwd_workspace_size(const fa_attn_params* a) {
+    AttnPlan pl;
+    if (attn_plan(a, true, &pl) != FA_OK) return 0;
+    const int B = a->batch, H = a->heads, N = a->seqlen_q, d = a->head_dim, Hkv = pl.Hkv;
+    switch (pl.fam) {
+    case Family::Plain:
+        return pl.det ? fa_bwd_deterministic_workspace_size(B, H, Hkv, N, d) : bwd_ws_bytes(FA_BF16, B, H, N, d);
+    case Family::F32:
+        return bwd_ws_bytes(FA_F32, B, H, N, d);
+    case Family::Gqa:
+        return pl.det ? fa_bwd_deterministic_workspace_size(B, H, Hkv, N, d) : fa_bwd_gqa_workspace_size(B, H, Hkv, N, d);
+    case Family::Window:
+        return pl.det ? fa_bwd_deterministic_workspace_size(B, H, Hkv, N, d) : fa_bwd_gqa_workspace_size(B, H, Hkv, N, d);
+    case Family::Sparse:
+        return pl.det ? fa_bwd_block_sparse_deterministic_workspace_size(B, H, Hkv, N, d)
+                      : fa_bwd_block_sparse_workspace_size(B, H, N, d);
+    case Family::Rect:
+        return pl.det ? fa_bwd_rect_deterministic_workspace_size(B, H, Hkv, N, pl.Nk, d)
+                      : fa_bwd_rect_workspace_size(B, H, Hkv, N, pl.Nk, d);
+    case Family::Packed:
+        return pl.det ? fa_bwd_varlen_deterministic_workspace_size(B, N, H, Hkv, d) : fa_bwd_varlen_workspace_size(B, N, H, d);
+    case Family::PackedKv:
+        return fa_bwd_varlen_kv_workspace_size(B, N, a->seqlen_k ? a->seqlen_k : N, H, Hkv, d, a->deterministic);
+    case Family::Bnhd:
+        return pl.det ? fa_bwd_bnhd_deterministic_workspace_size(B, N, H, Hkv, d) : fa_bwd_bnhd_workspace_size(B, N, H, d);
+    default:
+        return 0;
+    }
+}
+
+fa_status fa_attn_fwd(const fa_attn_params* a, fa_stream_t stream) {
+    AttnPlan pl;
+    FA_TRY(attn_plan(a, false, &pl));
+    const int B = a->batch, H = a->heads, N = a->seqlen_q, d = a->head_dim, Hkv = pl.Hkv;
+    switch (pl.fam) {
+    case Family::Plain:
+        if (a->block_c)
+            return fa_fwd_ex(FA_BF16, a->block_c, a->q, a->k, a->v, a->o, a->lse, B, H, N, d, a->scale, a->causal,
+                             a->kv_lens, nullptr, 0, stream);
+        return fa_fwd_split(a->q, a->k, a->v, a->o, a->lse, B, H, N, d, a->scale, a->causal, a->kv_lens, a->num_splits,
+                            a->workspace, a->workspace_bytes, stream);
+    case Family::F32:
+        return fa_fwd_ex(FA_F32, a->block_c, a->q, a->k, a->v, a->o, a->lse, B, H, N, d, a->scale, a->causal,
+                         a->kv_lens, a->workspace, a->workspace_bytes, stream);
+    case Family::Gqa:
+        return fa_fwd_gqa(a->q, a->k, a->v, a->o, a->lse, B, H, Hkv, N, d, a->scale, a->causal, a->kv_lens, stream);
+    case Family::Window:
+        return fa_fwd_window(a->q, a->k, a->v, a->o, a->lse, B, H, Hkv, N, d, a->scale, a->causal, a->window_left,
+                             a->window_right, a->kv_lens, stream);
+    case Family::Sparse:
+        return fa_fwd_block_sparse(a->q, a->k, a->v, a->o, a->lse, B, H, Hkv, N, d, a->scale, a->causal,
+                                   a->block_row_ptr, a->block_col_idx, a->kv_lens, stream);
+    case Family::Rect:
+        return fa_fwd_rect(a->q, a->k, a->v, a->o, a->lse, B, H, Hkv, N, pl.Nk, d, a->scale, a->causal, a->kv_lens,
+                           a->num_splits, a->workspace, a->workspace_bytes, stream);
+    case Family::Packed:
+        if (pl.window)
+            return fa_fwd_varlen_window(a->q, a->k, a->v, a->o, a->lse, a->cu_seqlens_q, B, a->total_q, N, H, Hkv, d,
+                                        a->scale, a->causal, a->window_left, a->window_right, stream);
+        return fa_fwd_varlen(a->q, a->k, a->v, a->o, a->lse, a->cu_seqlens_q, B, a->total_q, N, H, Hkv, d, a->scale,
+                             a->causal, stream);
+    case Family::PackedKv:
+        return fa_fwd_varlen_kv(a->q, a->k, a->v, a->o, a->lse, a->cu_seqlens_q, a->cu_seqlens_k, B, a->total_q,
+                                pl.total_k, N, H, Hkv, d, a->scale, a->causal, stream);
+    case Family::Bnhd:
+        return fa_fwd_bnhd(a->q, a->k, a->v, a->o, a->lse, B, N, H, Hkv, d, a->scale, a->causal, stream);
+    case Family::Fp8:
+        if (Hkv != H)
+            return fa_fwd_fp8_gqa(a->q, a->k, a->v, a->q_scale, a->k_scale, a->v_scale, a->o, a->lse, B, H, Hkv, N, d,
+                                  a->scale, a->causal, a->kv_lens, stream);
+        return fa_fwd_fp8_split(a->q, a->k, a->v, a->q_scale, a->k_scale, a->v_scale, a->o, a->lse, B, H, N, d,
+                                a->scale, a->causal, a->kv_lens, a->num_splits, a->workspace, a->workspace_bytes,
+                                stream);
+    }
+    return fail(FA_ERR_INVALID_ARG, "internal: unknown kernel family");
+}
+
+fa_status fa_attn_bwd(const fa_attn_params* a, fa_stream_t stream) {
+    AttnPlan pl;
+    FA_TRY(attn_plan(a, true, &pl));
+    const int B = a->batch, H = a->heads, N = a->seqlen_q, d = a->head_dim, Hkv = pl.Hkv;
+    const bool det = pl.det;
+    void* ws = a->workspace;
+    const size_t wsb = a->workspace_bytes;
+    switch (pl.fam) {
+    case Family::Plain:
+        if (det)
+            return fa_bwd_deterministic(a->q, a->k, a->v, a->o, a->lse, a->dout, a->dq, a->dk, a->dv, B, H, H, N, d,
+                                        a->scale, a->causal, a->kv_lens, ws, wsb, stream);
+        return fa_bwd(a->q, a->k, a->v, a->o, a->lse, a->dout, a->dq, a->dk, a->dv, B, H, N, d, a->scale, a->causal,
+                      a->kv_lens, ws, wsb, stream);
+    case Family::F32:
+        return fa_bwd_ex(FA_F32, a->q, a->k, a->v, a->o, a->lse, a->dout, a->dq, a->dk, a->dv, B, H, N, d, a->scale,
+                         a->causal, a->kv_lens, ws, wsb, stream);
+    case Family::Gqa:
+        if (det)
+            return fa_bwd_deterministic(a->q, a->k, a->v, a->o, a->lse, a->dout, a->dq, a->dk, a->dv, B, H, Hkv, N, d,
+                                        a->scale, a->causal, a->kv_lens, ws, wsb, stream);
+        return fa_bwd_gqa(a->q, a->k, a->v, a->o, a->lse, a->dout, a->dq, a->dk, a->dv, B, H, Hkv, N, d, a->scale,
+                          a->causal, a->kv_lens, ws, wsb, stream);
+    case Family::Window:
+        return (det ? fa_bwd_window_deterministic : fa_bwd_window)(a->q, a->k, a->v, a->o, a->lse, a->dout, a->dq,
+                                                                   a->dk, a->dv, B, H, Hkv, N, d, a->scale, a->causal,
+                                                                   a->window_left, a->window_right, a->kv_lens, ws,
+                                                                   wsb, stream);
+    case Family::Sparse:
+        return (det ? fa_bwd_block_sparse_deterministic : fa_bwd_block_sparse)(
+            a->q, a->k, a->v, a->o, a->lse, a->dout, a->dq, a->dk, a->dv, B, H, Hkv, N, d, a->scale, a->causal,
+            a->block_row_ptr, a->block_col_idx, a->kv_lens, ws, wsb, stream);
+    case Family::Rect:
+        return (det ? fa_bwd_rect_deterministic : fa_bwd_rect)(a->q, a->k, a->v, a->o, a->lse, a->dout, a->dq, a->dk,
+                                                               a->dv, B, H, Hkv, N, pl.Nk, d, a->scale, a->causal,
+                                                               a->kv_lens, ws, wsb, stream);
+    case Family::Packed:
+        if (pl.window)
+            return fa_bwd_varlen_window(a->q, a->k, a->v, a->o, a->lse, a->dout, a->dq, a->dk, a->dv, a->cu_seqlens_q,
+                                        B, a->total_q, N, H, Hkv, d, a->scale, a->causal, a->window_left,
+                                        a->window_right, a->deterministic, ws, wsb, stream);
+        return (det ? fa_bwd_varlen_deterministic : fa_bwd_varlen)(a->q, a->k, a->v, a->o, a->lse, a->dout, a->dq,
+                                                                   a->dk, a->dv, a->cu_seqlens_q, B, a->total_q, N, H,
+                                                                   Hkv, d, a->scale, a->causal, ws, wsb, stream);
+    case Family::PackedKv:
+        return fa_bwd_varlen_kv(a->q, a->k, a->v, a->o, a->lse, a->dout, a->dq, a->dk, a->dv, a->cu_seqlens_q,
+                                a->cu_seqlens_k, B, a->total_q, pl.total_k, N, a->seqlen_k ? a->seqlen_k : N, H, Hkv,
+                                d, a->scale, a->causal, a->deterministic, ws, wsb, stream);
+    case Family::Bnhd:
+        return (det ? fa_bwd_bnhd_deterministic : fa_bwd_bnhd)(a->q, a->k, a->v, a->o, a->lse, a->dout, a->dq, a->dk,
+                                                               a->dv, B, N, H, Hkv, d, a->scale, a->causal, ws, wsb,
+                                                               stream);
+    case Family::Fp8:
+        break;
+    }
+    return fail(FA_ERR_INVALID_ARG, "internal: unknown kernel family");
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
 // Allocation-free backward.
 //
 // Some callers of this library cannot allocate device memory at all: for
@@ -1549,7 +1852,7 @@ fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void
                          const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale,
                          int causal, const int* kv_lens, fa_stream_t stream) {
     FA_TRY(check_common(B, H, N, d, scale));
-    const size_t need = fa_bwd_workspace_size(FA_BF16, B, H, N, d);
+    const size_t need = bwd_ws_bytes(FA_BF16, B, H, N, d);
     if (need > kNoAllocScratchBytes)
         return fail(FA_ERR_INVALID_ARG,
                     "fa_bwd_noalloc: this problem needs %zu bytes of scratch, more than the %zu-byte static array; "

@@ -11,7 +11,8 @@ import torch
 
 import oracle
 from exact_tiled_attention_10_gb300 import (backward, backward_bnhd, backward_varlen, check_device_status, forward,
-                                           forward_bnhd, forward_varlen, load_library)
+                                           forward_bnhd, forward_varlen, load_library, attn_params,
+                                           FA_LAYOUT_PACKED)
 from exact_tiled_attention_10_gb300.inputs import qkv, randn
 from parity_util import assert_grad, to64
 
@@ -48,11 +49,19 @@ def test_deterministic_matches_oracle(d, causal, H, Hkv, N, kv):
     assert_grad(to64(dv), r["dv"].reshape(B, Hkv, g, N, d).sum(axis=2), "dV")
 
 
+def attn_bwd_workspace_size(**fields) -> int:
+    """Workspace bytes the backward needs for these parameters (fa_attn_bwd_workspace_size)."""
+    import ctypes
+    p = attn_params(**fields)
+    return int(load_library().fa_attn_bwd_workspace_size(ctypes.byref(p)))
+
+
 def _repeat_bitwise(B, H, Hkv, N, d, causal, reps, seed, perturb=False):
     q, k, v, do = _inputs(B, H, Hkv, N, d, seed)
     o, lse = forward(q, k, v, causal=causal)
     first = backward(q, k, v, o, lse, do, causal=causal, deterministic=True)
-    wsz = int(load_library().fa_bwd_deterministic_workspace_size(B, H, Hkv, N, d))
+    wsz = attn_bwd_workspace_size(batch=B, heads=H, kv_heads=Hkv, seqlen_q=N, head_dim=d, scale=1.0,
+                                  deterministic=1)
     side = torch.cuda.Stream()
     for rep in range(reps):
         ws = torch.full((wsz,), 0xFF, dtype=torch.uint8, device=DEV)  # nothing may carry over
@@ -113,7 +122,9 @@ def test_packed_sequences_repeat_bitwise():
     k, v = (randn((T, Hkv, d), 103 + i, device=DEV) for i in range(2))
     o, lse = forward_varlen(q, k, v, cu, max(lens), causal=True)
     first = backward_varlen(q, k, v, o, lse, do, cu, max(lens), causal=True, deterministic=True)
-    wsz = int(load_library().fa_bwd_varlen_deterministic_workspace_size(len(lens), max(lens), H, Hkv, d))
+    wsz = attn_bwd_workspace_size(layout=FA_LAYOUT_PACKED, batch=len(lens), heads=H, kv_heads=Hkv,
+                                  seqlen_q=max(lens), total_q=T, head_dim=d, scale=1.0, deterministic=1,
+                                  cu_seqlens_q=cu)
     for rep in range(3):
         ws = torch.full((wsz,), 0xFF, dtype=torch.uint8, device=DEV)
         again = backward_varlen(q, k, v, o, lse, do, cu, max(lens), causal=True, deterministic=True, workspace=ws)

@@ -16,7 +16,7 @@ import pytest
 import torch
 
 import oracle
-from exact_tiled_attention_10_gb300 import check_device_status, forward_rect, load_library
+from exact_tiled_attention_10_gb300 import check_device_status, forward_rect, rect_split_count
 from exact_tiled_attention_10_gb300.inputs import qkv, randn
 from parity_util import assert_lse, assert_o, rounding_context, to64
 
@@ -71,8 +71,7 @@ def test_explicit_splits_agree(num_splits):
 
 
 def test_planned_split_for_decode():
-    lib = load_library()
-    assert lib.fa_fwd_rect_split_count(1, 8, 8, 1, 131072, 128, 0) > 1
+    assert rect_split_count(1, 8, 8, 1, 131072, 128, 0) > 1
 
 
 def test_decode_128k_cache_sampled_heads():

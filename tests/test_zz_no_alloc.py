@@ -36,7 +36,7 @@ def test_noalloc_backward_matches_workspace_backward_twice(d, causal):
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
 
     # reference: the existing entry point with a caller workspace
-    wsz = lib.fa_bwd_workspace_size(0, B, H, N, d)
+    wsz = lib.fa_bwd_workspace_size(B, H, N, d)
     assert 0 < wsz <= lib.fa_bwd_noalloc_max_scratch()
     ws = torch.empty(wsz, dtype=torch.uint8, device="cuda")
     ref = [torch.empty_like(q) for _ in range(3)]
@@ -62,7 +62,7 @@ def test_noalloc_rejects_problems_beyond_its_scratch():
     lib = fa.load_library()
     cap = lib.fa_bwd_noalloc_max_scratch()
     B, H, N, d = 64, 64, 4096, 128
-    assert lib.fa_bwd_workspace_size(0, B, H, N, d) > cap
+    assert lib.fa_bwd_workspace_size(B, H, N, d) > cap
     x = torch.empty(16, dtype=torch.bfloat16, device="cuda")  # never touched: rejected before launch
     lse = torch.empty(16, dtype=torch.float32, device="cuda")
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
