@@ -24,6 +24,7 @@ import torch
 __all__ = ["forward", "forward_split", "forward_varlen", "backward_varlen", "backward", "forward_bnhd",
            "backward_bnhd", "block_lists", "forward_block_sparse", "backward_block_sparse", "quantize_fp8_qkv",
            "forward_rect", "backward_rect", "rect_split_count", "quantize_fp8", "forward_fp8", "forward_fp8_split",
+           "backward_fp8",
            "split_count", "split_workspace_size", "check_device_status", "selftest_wait_timeout", "attn_params",
            "AttnParams", "bwd_workspace_size", "fwd_workspace_size", "library_path", "load_library", "FAError"]
 
@@ -578,6 +579,26 @@ def forward_fp8_split(q8, k8, v8, sq, sk, sv, causal: bool = False, scale: Optio
                     q_scale=sq, k_scale=sk, v_scale=sv, o=o, lse=l)
     _run(p, q8, False, workspace)
     return o, l
+
+
+def backward_fp8(q8, k8, v8, sq, sk, sv, o, lse, dout, causal: bool = False, scale: Optional[float] = None,
+                 kv_lens=None, workspace: Optional[torch.Tensor] = None):
+    """FP8 backward (d = 128) of forward_fp8: q8, k8, v8 E4M3 codes [B,H,N,128]
+    with their block scales, the forward's o (bf16) and lse, and the bf16
+    upstream gradient dout.  The five products run on FP8 tensor cores (dS in
+    E5M2); returns float32 dQ, dK, dV [B,H,N,128]."""
+    _need_cuda(q8, k8, v8, sq, sk, sv, o, lse, dout)
+    B, H, N, d = q8.shape
+    if k8.shape != q8.shape or v8.shape != q8.shape or dout.dtype != torch.bfloat16:
+        raise ValueError("q8, k8, v8 [B,H,N,128] E4M3 codes; dout bfloat16")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    kv = _kv(kv_lens, B, q8.device)
+    dq, dk, dv = (torch.empty((B, H, N, d), dtype=torch.float32, device=q8.device) for _ in range(3))
+    p = attn_params(dtype=FA_E4M3, batch=B, heads=H, seqlen_q=N, head_dim=d, scale=scale, causal=int(bool(causal)),
+                    kv_lens=kv, q=q8, k=k8, v=v8, q_scale=sq, k_scale=sk, v_scale=sv, o=o, lse=lse, dout=dout,
+                    dq=dq, dk=dk, dv=dv)
+    _run(p, q8, True, workspace)
+    return dq, dk, dv
 
 
 def selftest_wait_timeout(limit_us: int = 20000, device=None) -> int:

@@ -719,10 +719,10 @@ fa_status bwd_pre_impl(const BwdCtx& c, bool f32, const void* o, const float* ls
 // The float32 dQ accumulator [rows][d] as the target of the drain warps' tensor
 // reductions: d = 128: [64 queries][32 head-dim] boxes, plain; d = 64:
 // [32 queries][32 head-dim] boxes in the 128-byte swizzle they are staged in.
-fa_status make_map_dqacc(CUtensorMap* m, float* dqacc, int d, long long rows) {
+fa_status make_map_dqacc(CUtensorMap* m, float* dqacc, int d, long long rows, int box_rows = 0) {
     cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)d * 4};
-    cuuint32_t box[2] = {32, (cuuint32_t)(d == 128 ? 64 : 32)};
+    cuuint32_t box[2] = {32, (cuuint32_t)(box_rows ? box_rows : (d == 128 ? 64 : 32))};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, dqacc, dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, d == 128 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
@@ -1505,6 +1505,104 @@ fa_status fa_fwd_fp8_split(const void* q8, const void* k8, const void* v8, const
 }  // extern "C"
 
 // ---------------------------------------------------------------------------
+// FP8 backward (chapter 18 §18.6.2: FP8 tensor-core products, dS in E5M2,
+// float32 gradients).  Workspace: the bf16 backward's layout (statistics,
+// float32 dQ accumulator), then dO's E4M3 codes and block scales, then K8
+// transposed ([B*H][128][Np] codes) for the dQ product's K-major operand.
+// ---------------------------------------------------------------------------
+namespace {
+
+struct Fp8BwdLayout {
+    size_t base, do8, sdo, kt, total;
+};
+Fp8BwdLayout fp8_bwd_layout(int B, int H, int N) {
+    const size_t BH = (size_t)B * H, Np = round_up((size_t)N, 128), nblk = (N + 63) / 64;
+    Fp8BwdLayout L;
+    L.base = 0;
+    size_t off = round_up(bwd_ws_bytes(FA_BF16, B, H, N, 128), 256);
+    L.do8 = off; off = round_up(off + BH * N * 128, 256);
+    L.sdo = off; off = round_up(off + BH * nblk * 4, 256);
+    L.kt = off; off = round_up(off + BH * 128 * Np, 256);
+    L.total = off;
+    return L;
+}
+
+fa_status bwd_fp8_impl(const void* q8, const void* k8, const void* v8, const float* sq, const float* sk,
+                       const float* sv, const void* o, const float* lse, const void* dout, float* dq, float* dk,
+                       float* dv, int B, int H, int N, int d, float scale, int causal, const int* kv_lens,
+                       void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    FA_CHECK_PTR(q8);
+    FA_CHECK_PTR(k8);
+    FA_CHECK_PTR(v8);
+    FA_CHECK_PTR(sq);
+    FA_CHECK_PTR(sk);
+    FA_CHECK_PTR(sv);
+    FA_CHECK_PTR(o);
+    FA_CHECK_PTR(lse);
+    FA_CHECK_PTR(dout);
+    FA_CHECK_PTR(dq);
+    FA_CHECK_PTR(dk);
+    FA_CHECK_PTR(dv);
+    if (d != 128) return fail(FA_ERR_UNSUPPORTED, "the FP8 backward needs d = 128");
+    BwdCtx c{};
+    FA_TRY(bwd_setup(FA_BF16, B, H, N, d, scale, workspace, workspace_bytes, &c));
+    const Fp8BwdLayout L = fp8_bwd_layout(B, H, N);
+    if (workspace_bytes < L.total)
+        return fail(FA_ERR_INVALID_ARG, "workspace too small (%zu < %zu bytes)", workspace_bytes, L.total);
+    const int nblk = (N + 63) / 64, BH = c.BH, Np = c.Np;
+    uint8_t* do8 = reinterpret_cast<uint8_t*>(c.ws + L.do8);
+    float* sdo = reinterpret_cast<float*>(c.ws + L.sdo);
+    uint8_t* kt = reinterpret_cast<uint8_t*>(c.ws + L.kt);
+    // dO8; D = rowsum(dO^ * O) from the dequantised dO8, LSE * log2(e), zeroed
+    // accumulator; K8 transposed
+    fa::QuantJobs jobs;
+    memset(&jobs, 0, sizeof(jobs));
+    jobs.x[0] = dout;
+    jobs.x8[0] = do8;
+    jobs.scales[0] = sdo;
+    jobs.heads[0] = BH;
+    cudaError_t e = fa::launch_quantize_fp8(jobs, N, d, c.dev->sms * 8, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "dO quantiser launch");
+    e = fa::launch_bwd_pre_fp8(o, do8, sdo, lse, reinterpret_cast<float*>(c.ws + c.L.lse2),
+                               reinterpret_cast<float*>(c.ws + c.L.dvec), reinterpret_cast<float*>(c.ws + c.L.dqacc),
+                               BH, N, Np, bw_grid(c.dev), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "FP8 backward preprocess launch");
+    e = fa::launch_transpose_k8(k8, kt, BH, N, Np, c.dev->sms * 4, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "K transpose launch");
+    CUtensorMap tq, tk, tv, tdo, tkt, tdq;
+    const auto U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    FA_TRY(make_map_3d(&tq, U8, 1, q8, 128, N, BH, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B));
+    FA_TRY(make_map_3d(&tk, U8, 1, k8, 128, N, BH, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B));
+    FA_TRY(make_map_3d(&tv, U8, 1, v8, 128, N, BH, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B));
+    FA_TRY(make_map_3d(&tdo, U8, 1, do8, 128, N, BH, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B));
+    FA_TRY(make_map_3d(&tkt, U8, 1, kt, Np, 128, BH, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B));
+    float* dqacc = reinterpret_cast<float*>(c.ws + c.L.dqacc);
+    if ((long long)BH * Np >= (1LL << 31))
+        return fail(FA_ERR_UNSUPPORTED, "dQ accumulator rows exceed the 32-bit tensor coordinate range");
+    FA_TRY(make_map_dqacc(&tdq, dqacc, d, (long long)BH * Np, 128));
+    fa::BwdFp8Params p;
+    memset(&p, 0, sizeof(p));
+    p.B = B; p.H = H; p.N = N; p.Np = Np; p.nblk = nblk;
+    p.num_kt = (N + 127) / 128;
+    p.num_items = BH * p.num_kt;
+    p.causal = causal != 0;
+    p.scale = scale;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.kv_lens = kv_lens;
+    p.sq = sq; p.sk = sk; p.sv = sv; p.sdo = sdo;
+    p.lse2 = reinterpret_cast<float*>(c.ws + c.L.lse2);
+    p.dvec = reinterpret_cast<float*>(c.ws + c.L.dvec);
+    p.dk = dk;
+    p.dv = dv;
+    p.err = c.dev->err_word;
+    e = fa::launch_bwd_fp8(tq, tk, tv, tdo, tkt, tdq, p, grid_for_items(p.num_items, c.dev->sms), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "FP8 backward launch");
+    return bwd_dq_impl(c, true, dq, N, d, scale, stream);
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
 // One call per pass: the parameter block of include/fa.h.  attn_plan is the one
 // validation routine of both passes: it names the kernel family a parameter
 // block selects, or refuses the combination (before any launch) with the
@@ -1562,9 +1660,10 @@ fa_status attn_plan(const fa_attn_params* a, bool bwd, AttnPlan* pl) {
     if (!bwd && pl->det) return refuse("deterministic in a forward call");
     switch (a->dtype) {
     case FA_E4M3:
-        if (bwd) return refuse("FP8 backward (use the bf16 backward)");
         if (a->layout != FA_LAYOUT_BHND || pl->window || sparse || rect)
             return refuse("FP8 with the packed or [B,N,H,d] layouts, a window, block lists or N_q != N_k");
+        if (bwd && (Hkv != a->heads || pl->det)) return refuse("the FP8 backward with shared key/value heads or "
+                                                               "deterministic");
         if (Hkv != a->heads && split) return refuse("a split FP8 forward with shared key/value heads");
         if (a->block_c) return refuse("block_c with FP8");
         pl->fam = Family::Fp8;
@@ -1691,6 +1790,8 @@ size_t fa_attn_bwd_workspace_size(const fa_attn_params* a) {
         return fa_bwd_varlen_kv_workspace_size(B, N, a->seqlen_k ? a->seqlen_k : N, H, Hkv, d, a->deterministic);
     case Family::Bnhd:
         return pl.det ? fa_bwd_bnhd_deterministic_workspace_size(B, N, H, Hkv, d) : fa_bwd_bnhd_workspace_size(B, N, H, d);
+    case Family::Fp8:
+        return d == 128 ? fp8_bwd_layout(B, H, N).total : 0;
     default:
         return 0;
     }
@@ -1796,7 +1897,10 @@ fa_status fa_attn_bwd(const fa_attn_params* a, fa_stream_t stream) {
                                                                a->dv, B, N, H, Hkv, d, a->scale, a->causal, ws, wsb,
                                                                stream);
     case Family::Fp8:
-        break;
+        return bwd_fp8_impl(a->q, a->k, a->v, a->q_scale, a->k_scale, a->v_scale, a->o, a->lse, a->dout,
+                            reinterpret_cast<float*>(a->dq), reinterpret_cast<float*>(a->dk),
+                            reinterpret_cast<float*>(a->dv), B, H, N, d, a->scale, a->causal, a->kv_lens, ws, wsb,
+                            stream);
     }
     return fail(FA_ERR_INVALID_ARG, "internal: unknown kernel family");
 }

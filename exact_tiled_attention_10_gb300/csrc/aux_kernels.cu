@@ -112,6 +112,60 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const void* __restrict__ o
     }
 }
 
+// The FP8 backward's preprocess (d = 128): D = rowsum(dO^ * O) with dO^ the
+// dequantised E4M3 upstream gradient s_do * dO8 the backward's products use
+// (so that D matches their dP = dO^ V^T), LSE * log2(e), and the zeroed dQ
+// accumulator.  One group of 16 lanes per row; 8 elements per lane.
+__global__ void __launch_bounds__(256) bwd_pre_fp8_kernel(const __nv_bfloat16* __restrict__ o,
+                                                          const uint8_t* __restrict__ do8,
+                                                          const float* __restrict__ sdo, const float* __restrict__ lse,
+                                                          float* __restrict__ lse2, float* __restrict__ dvec,
+                                                          float* __restrict__ dq_acc, int BH, int N, int Np, int nblk) {
+    constexpr int D = 128, LPR = 16, RPW = 2;
+    const int lane = threadIdx.x & 31;
+    const int sub = lane / LPR, sl = lane % LPR;
+    const long total_rows = (long)BH * Np;
+    const long warps = (long)gridDim.x * (blockDim.x / 32);
+    const long gw = (long)blockIdx.x * (blockDim.x / 32) + (threadIdx.x / 32);
+    const uint64_t pol_first = policy_evict_first(), pol_last = policy_evict_last();
+    for (long r0 = gw * RPW; r0 < total_rows; r0 += warps * RPW) {
+        const long r = r0 + sub;
+        const bool valid_row = r < total_rows;
+        const long bh = valid_row ? r / Np : 0;
+        const int i = valid_row ? (int)(r - bh * Np) : 0;
+        float acc = 0.f;
+        if (valid_row && i < N) {
+            const size_t e = ((size_t)bh * N + i) * D + sl * 8;
+            float a[8];
+            unpack8(ld_stream(o + e, pol_first), a);
+            const uint2 c = *reinterpret_cast<const uint2*>(do8 + e);
+            const float s = __ldg(sdo + bh * nblk + i / 64);
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                const float2 g = __half22float2(e4m3x2_to_half2(((h < 2 ? c.x : c.y) >> (16 * (h & 1))) & 0xFFFFu));
+                acc = fmaf(a[2 * h], g.x * s, acc);
+                acc = fmaf(a[2 * h + 1], g.y * s, acc);
+            }
+        }
+#pragma unroll
+        for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (valid_row) {
+            float* qa = dq_acc + (size_t)r * D + sl * 8;
+            st_keep_zero(qa, pol_last);
+            st_keep_zero(qa + 4, pol_last);
+            if (sl == 0) {
+                float l2 = INFINITY;
+                if (i < N) {
+                    const float L = lse[(size_t)bh * N + i];
+                    l2 = (L == -INFINITY) ? INFINITY : L * 1.4426950408889634f;
+                }
+                lse2[r] = l2;
+                dvec[r] = (i < N) ? acc : 0.f;
+            }
+        }
+    }
+}
+
 // dQ[r, :] = scale * dQ_acc[r, :] for the N real rows of every head.  Each
 // thread converts U 8-element groups per pass, all loads issued before the
 // stores, so that enough reads stay in flight to keep HBM busy.
@@ -718,6 +772,14 @@ cudaError_t launch_bwd_dq_det_varlen(const float* acc, const int* turn, const in
 cudaError_t launch_bwd_dq_det(const float* acc, const int* turn, void* dq, float scale, int BH, int N, int Np, int d,
                               int nacc, int grid, cudaStream_t s) {
     bwd_dq_det_kernel<<<grid, 256, 0, s>>>(acc, turn, reinterpret_cast<__nv_bfloat16*>(dq), scale, BH, N, Np, d, nacc);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_pre_fp8(const void* o, const void* do8, const float* sdo, const float* lse, float* lse2,
+                               float* dvec, float* dq_acc, int BH, int N, int Np, int grid, cudaStream_t s) {
+    bwd_pre_fp8_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(o),
+                                            reinterpret_cast<const uint8_t*>(do8), sdo, lse, lse2, dvec, dq_acc, BH,
+                                            N, Np, (N + 63) / 64);
     return cudaGetLastError();
 }
 

@@ -183,6 +183,25 @@ struct BwdDet : Base {
 };
 using BwdParamsDet = BwdDet<BwdParams>;
 
+// FP8 backward (d = 128): E4M3 codes of Q, K, V, dO with one float32 scale
+// per 64-row block ([B*H][nblk]); float32 dK, dV [B,H,N,128]; statistics and
+// the float32 dQ accumulator as for the bf16 backward.
+struct BwdFp8Params {
+    int B, H, N, Np, nblk;
+    int num_kt, num_items, causal;
+    float scale, scale_log2;
+    const int* kv_lens;
+    const float* sq;
+    const float* sk;
+    const float* sv;
+    const float* sdo;
+    const float* lse2;
+    const float* dvec;
+    float* dk;
+    float* dv;
+    unsigned int* err;
+};
+
 // Launch helpers implemented in the kernel translation units.  They return a
 // cudaError_t from the launch itself.
 // Tensor maps of one forward launch: q, k, v and, for float32 inputs carried
@@ -263,6 +282,16 @@ cudaError_t launch_bwd_main(int d, bool causal, bool out_f32, const CUtensorMap&
                             const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
                             const CUtensorMap& tdq, const BwdParams& p, int grid,
                             cudaStream_t stream);
+// FP8 backward main kernel; tkt: the transposed K codes [B*H][128][Np].
+cudaError_t launch_bwd_fp8(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
+                           const CUtensorMap& tkt, const CUtensorMap& tdq, const BwdFp8Params& p, int grid,
+                           cudaStream_t stream);
+// FP8 backward preprocess: D = rowsum(s_do dO8 * O), LSE * log2(e), zeroed
+// dQ accumulator (d = 128; o bf16, do8 E4M3 codes with per-64-row scales).
+cudaError_t launch_bwd_pre_fp8(const void* o, const void* do8, const float* sdo, const float* lse, float* lse2,
+                               float* dvec, float* dq_acc, int BH, int N, int Np, int grid, cudaStream_t stream);
+// k8 [B*H][N][128] -> kt [B*H][128][Np] (uint8 codes; keys >= N zero).
+cudaError_t launch_transpose_k8(const void* k8, void* kt, int BH, int N, int Np, int grid, cudaStream_t stream);
 cudaError_t launch_bwd_pre(const void* o, const void* dout, bool in_f32, const float* lse,
                            float* lse2, float* dvec, float* dq_acc, int BH, int N, int Np, int d,
                            int grid, cudaStream_t stream);

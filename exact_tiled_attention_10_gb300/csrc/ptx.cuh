@@ -363,6 +363,7 @@ __host__ __device__ constexpr uint32_t idesc_make(uint32_t a_fmt, uint32_t b_fmt
 }
 constexpr uint32_t kFmtBF16 = 1;  // kind::f16
 constexpr uint32_t kFmtE4M3 = 0;  // kind::f8f6f4
+constexpr uint32_t kFmtE5M2 = 1;  // kind::f8f6f4
 
 // ------------------------------------------------------------------ numerics
 // Per-warpgroup register budget (all four warps of the warpgroup execute it).
@@ -451,6 +452,14 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
     uint16_t lo, hi;
     asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));
     asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
+    return (uint32_t)lo | ((uint32_t)hi << 16);
+}
+
+// Four floats -> four E5M2 bytes (element 0 in the low byte), RNE, saturating.
+__device__ __forceinline__ uint32_t pack_e5m2x4(float a, float b, float c, float d) {
+    uint16_t lo, hi;
+    asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));
+    asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
     return (uint32_t)lo | ((uint32_t)hi << 16);
 }
 

@@ -185,7 +185,9 @@ BWD = dict(FWD, dout=A, dq=A, dk=A, dv=A)
 def test_one_validation_routine_refuses_the_combinations_not_built():
     """fa_attn_fwd / fa_attn_bwd refuse, on the host and before any CUDA
     call, every combination the library does not build (FA_ERR_UNSUPPORTED),
-    and malformed parameter blocks (FA_ERR_INVALID_ARG)."""
+    and malformed parameter blocks (FA_ERR_INVALID_ARG).  (The d = 64 FP8
+    case runs the host checks up to the head dimension, which comes before
+    any CUDA call.)"""
     import exact_tiled_attention_10_gb300 as fa
     base = dict(batch=2, heads=4, seqlen_q=256, head_dim=128, scale=0.1)
     U, I = fa.FA_ERR_UNSUPPORTED, fa.FA_ERR_INVALID_ARG
@@ -194,7 +196,10 @@ def test_one_validation_routine_refuses_the_combinations_not_built():
     assert _status(**base, **FWD, dtype=fa.FA_E4M3, window_left=64) == U
     assert _status(**base, **FWD, dtype=fa.FA_E4M3, block_row_ptr=A, block_col_idx=A) == U
     assert _status(**base, **FWD, dtype=fa.FA_E4M3, seqlen_k=300) == U
-    assert _status(True, **base, **BWD, dtype=fa.FA_E4M3) == U
+    assert _status(True, **base, **BWD, dtype=fa.FA_E4M3, kv_heads=2) == U
+    assert _status(True, **base, **BWD, dtype=fa.FA_E4M3, deterministic=1) == U
+    assert _status(True, **dict(base, head_dim=64), **BWD, dtype=fa.FA_E4M3, q_scale=A, k_scale=A, v_scale=A, workspace=A,
+                   workspace_bytes=1 << 30) == U
     assert _status(**base, **FWD, dtype=fa.FA_E4M3, kv_heads=2, num_splits=0) == U
     # float32: anything beyond causal, kv_lens and block_c
     assert _status(**base, **FWD, dtype=fa.FA_F32, window_right=0) == U

@@ -164,3 +164,15 @@ def test_varlen_separate_key_ranges(monkeypatch):
                                                                    cu_seqlens_k=cuk, max_seqlen_k=200,
                                                                    deterministic=True))
     assert (dk[60:110] == 0).all() and (dv[60:110] == 0).all()
+
+
+def test_fp8_backward(monkeypatch):
+    """The FP8 backward's dQ, dK, dV (float32), its workspace (dO codes and
+    scales, transposed K codes, statistics, dQ accumulator) all poisoned."""
+    q, k, v, do = _qkv(2, 2, 2, 300, 128, 33)
+    (q8, sq), (k8, sk), (v8, sv) = fa.quantize_fp8_qkv(q, k, v)
+    kv = torch.tensor([0, 250], dtype=torch.int32, device=DEV)
+    o, lse = fa.forward_fp8(q8, k8, v8, sq, sk, sv, causal=True, kv_lens=kv)
+    _run_both(monkeypatch, lambda: fa.backward_fp8(q8, k8, v8, sq, sk, sv, o, lse, do, causal=True, kv_lens=kv)[1:])
+    _run_both(monkeypatch, lambda: fa.backward_fp8(q8, k8, v8, sq, sk, sv, o, lse, do, causal=True,
+                                                   kv_lens=kv)[:1], exact=False)
