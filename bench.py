@@ -460,6 +460,40 @@ def time_steps(step, steps, warmup):
     return out
 
 
+def time_fp8_backward(step, peaks, reps):
+    """The FP8 backward (chapter 18 §18.6.2) of the step's FP8 forward (same
+    codes, scales, O and LSE; non-causal), timed on its own: every kernel of
+    the call (dO quantiser, preprocess, K transpose, main kernel, dQ
+    conversion) between two events, L2 flushed between calls."""
+    import torch
+    fa, w = step.fa, step.w
+    B, H, N, d = w.B, w.H, w.N, w.d
+    f32 = lambda: torch.empty((B, H, N, d), dtype=torch.float32, device=step.dev)
+    dq, dk, dv = f32(), f32(), f32()
+    prm = fa.attn_params(dtype=fa.FA_E4M3, batch=B, heads=H, seqlen_q=N, head_dim=d, scale=step.scale,
+                         q=step.x8[0], k=step.x8[1], v=step.x8[2], q_scale=step.sc[0], k_scale=step.sc[1],
+                         v_scale=step.sc[2], o=step.o8, lse=step.lse8, dout=step.do, dq=dq, dk=dk, dv=dv)
+    nbytes = int(step.lib.fa_attn_bwd_workspace_size(ctypes.byref(prm)))
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=step.dev)
+    prm.workspace, prm.workspace_bytes = ws.data_ptr(), nbytes
+    s = torch.cuda.current_stream(step.dev).cuda_stream
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for i in range(reps + 3):
+        if i >= 3:
+            ev[i - 3][0].record()
+        step._ck(step.lib.fa_attn_bwd(ctypes.byref(prm), s))
+        if i >= 3:
+            ev[i - 3][1].record()
+        step.flush_l2()
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    F = 2.5 * flops_fwd(w, False)
+    tf = F / (ms / 1e3) / 1e12
+    pk = peaks["bf16_tflops"] * FP8_OVER_BF16
+    return {"ms": round(ms, 4), "tflops": round(tf, 1), "frac_of_fp8_peak": round(tf / pk, 4), "reps": reps,
+            "workload": "non-causal backward of the FP8 forward, float32 gradients, whole fa_attn_bwd call"}
+
+
 def other_configs(device, peaks, reps):
     """The other workload shapes, each timed on its own (bf16 forward and
     whole backward call; FP8 where the workload has one)."""
@@ -556,6 +590,8 @@ def main():
            "ms": passes["fwd_fp8"]["ms"], "quant_ms": passes["quant_fp8"]["ms"],
            "quant_gbs": passes["quant_fp8"]["gbs"], "quant_frac_of_hbm": passes["quant_fp8"]["frac_of_hbm"],
            "workload": "non-causal forward on E4M3 codes with per-64-row block scales (quantiser timed apart)"}
+
+    fp8["bwd"] = time_fp8_backward(step, peaks, args.config_reps)
 
     # ---- end to end through the public API with pinned host buffers
     e2e_steps = args.e2e_steps or min(args.steps, 100)

@@ -70,8 +70,8 @@ typedef enum {
 } fa_status;
 
 /* Element type of the attention tensors.  FA_E4M3: q, k, v are E4M3 codes
- * (uint8) with per-64-row-block float32 scales (fa_quantize_fp8), o is bf16,
- * dout / dq / dk / dv are bf16 (see fa_attn_bwd). */
+ * (uint8) with per-64-row-block float32 scales (fa_quantize_fp8), o and dout
+ * are bf16, dq / dk / dv are float32 (see fa_attn_bwd). */
 typedef enum { FA_BF16 = 0, FA_F32 = 1, FA_E4M3 = 2 } fa_dtype;
 
 /* Tensor layouts of fa_attn_params.
@@ -191,9 +191,11 @@ FA_API fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* v8,
  *                tensor-core inputs (q and k split into bf16 high and low
  *                parts for the scores, x = hi + lo with ~16 significant bits;
  *                workspace from fa_attn_fwd_workspace_size); FA_E4M3:
- *                forward only, q, k, v E4M3 codes with q_scale, k_scale,
- *                v_scale [B, H or Hkv, ceil(N/64)], [B,H,N,d] with d = 128,
- *                no sliding window, block lists or N_q != N_k.
+ *                q, k, v E4M3 codes with q_scale, k_scale, v_scale
+ *                [B, H or Hkv, ceil(N/64)], [B,H,N,d] with d = 128, no
+ *                sliding window, block lists or N_q != N_k; o, dout bf16;
+ *                the backward writes float32 dq, dk, dv and needs
+ *                Hkv = H and deterministic = 0.
  *  layout        see fa_layout.
  *  batch         B, or the number of packed sequences.
  *  heads         H (query heads).
@@ -319,8 +321,16 @@ FA_API size_t fa_attn_bwd_workspace_size(const fa_attn_params* p);
 FA_API fa_status fa_attn_fwd(const fa_attn_params* p, fa_stream_t stream);
 
 /* Backward pass ([FA2] §5.4 Algorithm 2) of the forward with the same
- * parameters.  The same refusals as fa_attn_fwd, plus FA_E4M3 (no FP8
- * backward). */
+ * parameters.  The same refusals as fa_attn_fwd, plus the FP8 backward with
+ * shared key/value heads or deterministic.
+ * FA_E4M3 ([CH18] §18.6.2): all five products of the backward run on FP8
+ * tensor cores.  dout is quantised to E4M3 per 64-row block inside the call;
+ * D = rowsum(dO^ * o) uses the dequantised dO^; P is rebuilt in float32 from
+ * the E4M3 scores and re-quantised to E4M3 for dV = P^T dO^; dS = P * (dP - D)
+ * is quantised to E5M2 with one power-of-two scale per (b, h), from a bound
+ * on |dS|, for dK = dS^T Q^ and dQ = dS K^ (E5M2 x E4M3 products).  The block scales are
+ * folded into the quantised operands; dq, dk, dv are float32 gradients with
+ * respect to the dequantised inputs Q^ = s_q Q8, K^, V^. */
 FA_API fa_status fa_attn_bwd(const fa_attn_params* p, fa_stream_t stream);
 
 /* ---------------------------------------------- the backward's phases */
