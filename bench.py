@@ -4,7 +4,11 @@
 One STEP is one pass of the whole path over one batch of synthetic input:
   bf16 forward (causal)  ->  backward: preprocess, main kernel, dQ conversion
   ->  E4M3 quantisation of Q, K, V  ->  FP8 forward (non-causal)
-all through the C ABI of libfa_gb300.so.  Default workload: B=2, H=16,
+all through the C ABI of libfa_gb300.so.  L2 is flushed before the step and
+again between its bf16 and FP8 parts, outside the timed events, so that each
+part starts cold, with no dirty lines of the other part's outputs to write
+back (the bf16 backward leaves ~100 MB of dK, dV and dQ in L2, which cost the
+HBM-bound quantiser ~15% when it ran right behind it).  Default workload: B=2, H=16,
 N=4096, d=128 (the long-head shape; the accuracy/throughput targets are stated
 for N >= 4096, d = 128).  The metric is algorithmic TFLOPS:
   F = 4 B H N^2 d per forward, 2.5 F per backward, halved when causal.
@@ -251,6 +255,7 @@ class Step:
             self.o8 = t(B, H, N, d)
             self.lse8 = t(B, H, N, dt=torch.float32)
         self.flush = t(L2_FLUSH_BYTES, dt=torch.uint8)
+        self.flush_rd = torch.ones(L2_FLUSH_BYTES // 2, dtype=torch.uint8, device=device)
         # split-key plans (automatic): the causal bf16 forward is never split;
         # the non-causal FP8 forward may be (its merge kernel is part of the call)
         has_kv = self.kv is not None
@@ -293,35 +298,49 @@ class Step:
         if st != 0:
             raise RuntimeError(self.lib.fa_last_error().decode())
 
+    def phases(self):
+        return list(self.PHASES) if self.with_fp8 else list(self.BF16)
+
+    def events(self):
+        """A start and an end event for each phase of phases()."""
+        return [self.torch.cuda.Event(enable_timing=True) for _ in range(2 * len(self.phases()))]
+
     def run(self, events=None):
+        """One step; events[2i] / events[2i + 1] bracket phase i of phases()."""
         lib, w, s = self.lib, self.w, self.torch.cuda.current_stream(self.dev).cuda_stream
         B, H, N, d = w.B, w.H, w.N, w.d
         p = lambda x: x.data_ptr()
         kv = None if self.kv is None else p(self.kv)
-        rec = (lambda i: events[i].record()) if events is not None else (lambda i: None)
-        rec(0)
+        ev = iter(events) if events is not None else None
+        rec = (lambda: next(ev).record()) if ev is not None else (lambda: None)
+        rec()
         self._ck(lib.fa_attn_fwd(ctypes.byref(self.p_fwd), s))
-        rec(1)
+        rec(), rec()
         self._ck(lib.fa_bwd_preprocess(p(self.o), p(self.lse), p(self.do), B, H, N, d, p(self.ws),
                                        self.ws_bytes, s))
-        rec(2)
+        rec(), rec()
         self._ck(lib.fa_bwd_main(p(self.q), p(self.k), p(self.v), p(self.do), p(self.dk), p(self.dv),
                                  B, H, N, d, self.scale, int(self.causal), kv, p(self.ws),
                                  self.ws_bytes, s))
-        rec(3)
+        rec(), rec()
         self._ck(lib.fa_bwd_dq(p(self.dq), B, H, N, d, self.scale, p(self.ws), self.ws_bytes, s))
-        rec(4)
+        rec()
         if not self.with_fp8:
             return
+        self.flush_l2()  # between the parts, outside every phase's events
+        rec()
         self._ck(lib.fa_quantize_fp8_qkv(p(self.q), p(self.k), p(self.v), p(self.x8[0]), p(self.x8[1]),
-                                         p(self.x8[2]), p(self.sc[0]), p(self.sc[1]), p(self.sc[2]), B, H, H, N, d,
-                                         s))
-        rec(5)
+                                         p(self.x8[2]), p(self.sc[0]), p(self.sc[1]), p(self.sc[2]), B, H, H,
+                                         N, d, s))
+        rec(), rec()
         self._ck(lib.fa_attn_fwd(ctypes.byref(self.p_fp8), s))
-        rec(6)
+        rec()
 
     def flush_l2(self):
+        """Writes a buffer four times the size of L2, then reads one twice its
+        size: L2 ends holding none of the step's data and no dirty lines."""
         self.flush.zero_()
+        self._sink = self.flush_rd.max()
 
 
 def barrier(ws):
@@ -443,8 +462,8 @@ def time_steps(step, steps, warmup):
     """Runs `warmup` then `steps` steps (L2 flushed between steps, outside the
     events) and returns {phase: [ms per step]}."""
     import torch
-    nph = len(Step.PHASES) if step.with_fp8 else 4
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nph + 1)] for _ in range(steps)]
+    phases = step.phases()
+    ev = [step.events() for _ in range(steps)]
     for _ in range(max(warmup, 3)):
         step.run()
         step.flush_l2()
@@ -453,10 +472,10 @@ def time_steps(step, steps, warmup):
         step.run(ev[i])
         step.flush_l2()
     torch.cuda.synchronize()
-    out = {ph: [] for ph in Step.PHASES[:nph]}
+    out = {ph: [] for ph in phases}
     for e in ev:
-        for j, ph in enumerate(Step.PHASES[:nph]):
-            out[ph].append(e[j].elapsed_time(e[j + 1]))
+        for j, ph in enumerate(phases):
+            out[ph].append(e[2 * j].elapsed_time(e[2 * j + 1]))
     return out
 
 
@@ -543,7 +562,7 @@ def main():
     fa.load_library()
 
     step = Step(w, causal, device, seed_offset=1000 * rank)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(args.steps)]
+    ev = [step.events() for _ in range(args.steps)]
     for _ in range(max(args.warmup, 3)):
         step.run()
         step.flush_l2()
@@ -564,13 +583,15 @@ def main():
     clk = clocks.stop()
     fa.check_device_status(device)
 
-    phase_ms = {ph: [] for ph in Step.PHASES}
+    phases = step.phases()
+    phase_ms = {ph: [] for ph in phases}
     step_ms, bf16_ms = [], []
     for e in ev:
-        step_ms.append(e[0].elapsed_time(e[6]))
-        bf16_ms.append(e[0].elapsed_time(e[4]))
-        for j, ph in enumerate(Step.PHASES):
-            phase_ms[ph].append(e[j].elapsed_time(e[j + 1]))
+        t = [e[2 * j].elapsed_time(e[2 * j + 1]) for j in range(len(phases))]
+        step_ms.append(sum(t))
+        bf16_ms.append(sum(x for ph, x in zip(phases, t) if ph in Step.BF16))
+        for ph, x in zip(phases, t):
+            phase_ms[ph].append(x)
     total_ms = max_over_ranks(ws, sum(step_ms), device)
     bf16_total_ms = max_over_ranks(ws, sum(bf16_ms), device)
     flops_bf16 = step.flops["fwd"] + step.flops["bwd_main"]
@@ -621,13 +642,14 @@ def main():
             "steps": args.steps, "warmup": max(args.warmup, 3),
             "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": "%s: B=%d H=%d N=%d d=%d; bf16 causal fwd + bwd, then E4M3 "
-                                   "quantise Q/K/V + FP8 non-causal fwd" % (w.name, w.B, w.H, w.N, w.d),
+            "config": {"workload": "%s: B=%d H=%d N=%d d=%d; bf16 causal fwd + bwd, then E4M3 quantise Q/K/V "
+                                   "+ FP8 non-causal fwd" % (w.name, w.B, w.H, w.N, w.d),
                        "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": causal,
                        "value_basis": "bf16 (F_fwd + F_bwd) / time of the bf16 forward and the whole backward "
                                       "call (%.4f ms per step); ms_per_step also holds the FP8 rows" % (
                                           bf16_total_ms / args.steps),
-                       "l2": "flushed between steps (512 MiB write outside the timed events)",
+                       "l2": "flushed before each step and between its bf16 and FP8 parts, outside the timed "
+                             "events (512 MiB written, then 256 MiB read: L2 left cold and clean)",
                        "parallelism": "replicas" if ws > 1 else "single GPU"},
             "targets": {"fwd_frac_burst": summ["fwd_frac_burst"], "fwd_target": 0.60,
                         "bwd_call_frac_burst": summ["bwd_call_frac_burst"], "bwd_target": 0.45,

@@ -4,7 +4,10 @@ Every step of the computation runs in the CUDA kernels of ``libfa_gb300.so``
 behind the C ABI of ``include/fa.h``; this module only marshals arguments
 (torch tensors -> device pointers, the current CUDA stream) and allocates
 outputs and scratch with torch.  There is no CPU fallback: if the library is
-missing or no CUDA device is present, calls raise.
+missing or no CUDA device is present, calls raise.  With FA_DEBUG=1 in the
+environment the checked build ``libfa_gb300_debug.so`` (``build(debug=True)``)
+is loaded instead; a broken access rule then surfaces as FA_ERR_CHECK from
+``check_device_status()``.
 
     o, lse = forward(q, k, v, causal=True)               # bf16 or float32
     dq, dk, dv = backward(q, k, v, o, lse, do, causal=True)
@@ -29,14 +32,14 @@ __all__ = ["forward", "forward_split", "forward_varlen", "backward_varlen", "bac
            "AttnParams", "bwd_workspace_size", "fwd_workspace_size", "library_path", "load_library", "FAError"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_LIB_PATH = os.path.join(_HERE, "libfa_gb300.so")
+_LIB_PATH = os.path.join(_HERE, "libfa_gb300_debug.so" if os.environ.get("FA_DEBUG") == "1" else "libfa_gb300.so")
 _lock = threading.Lock()
 _lib = None
 
-FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = 0, 1, 2, 3, 4
+FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT, FA_ERR_CHECK = 0, 1, 2, 3, 4, 5
 FA_BF16, FA_F32, FA_E4M3 = 0, 1, 2
 FA_LAYOUT_BHND, FA_LAYOUT_BNHD, FA_LAYOUT_PACKED = 0, 1, 2
-_STATUS = {1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_CUDA", 4: "FA_ERR_TIMEOUT"}
+_STATUS = {1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_CUDA", 4: "FA_ERR_TIMEOUT", 5: "FA_ERR_CHECK"}
 
 
 class AttnParams(ctypes.Structure):
@@ -109,8 +112,9 @@ def load_library():
         if _lib is None:
             if not os.path.exists(_LIB_PATH):
                 raise RuntimeError(
-                    "libfa_gb300.so is not built; run exact_tiled_attention_10_gb300.build.build() "
-                    "(the CUDA path has no fallback)")
+                    "%s is not built; run exact_tiled_attention_10_gb300.build.build(%s) "
+                    "(the CUDA path has no fallback)" % (os.path.basename(_LIB_PATH),
+                                                         "debug=True" if "debug" in _LIB_PATH else ""))
             lib = ctypes.CDLL(_LIB_PATH)
             for name, (args, res) in _SIGS.items():
                 fn = getattr(lib, name)

@@ -426,6 +426,8 @@ fa_status fa_check_device_status(fa_stream_t stream) {
         const unsigned int zero = 0;
         e = cudaMemcpy(dev->err_word, &zero, sizeof(zero), cudaMemcpyHostToDevice);
         if (e != cudaSuccess) return cuda_fail(e, "clearing the device error word");
+        if (word & fa::kErrCheckMask)
+            return fail(FA_ERR_CHECK, "a device access check of the checked build failed (error bits 0x%x)", word);
         return fail(FA_ERR_TIMEOUT, "a kernel pipeline wait timed out (error bits 0x%x)", word);
     }
     return FA_OK;
@@ -1454,7 +1456,7 @@ fa_status fa_quantize_fp8(const void* x_bf16, void* x_e4m3, float* scales, int B
     jobs.x8[0] = x_e4m3;
     jobs.scales[0] = scales;
     jobs.heads[0] = B * H;
-    cudaError_t e = fa::launch_quantize_fp8(jobs, N, d, dev->sms * 8, stream);
+    cudaError_t e = fa::launch_quantize_fp8(jobs, N, d, dev->sms, stream);
     if (e != cudaSuccess) return cuda_fail(e, "quantiser launch");
     return FA_OK;
 }
@@ -1475,7 +1477,7 @@ fa_status fa_quantize_fp8_qkv(const void* q, const void* k, const void* v, void*
     DeviceInfo* dev = nullptr;
     FA_TRY(device_info(&dev));
     const fa::QuantJobs jobs = {{q, k, v}, {q8, k8, v8}, {sq, sk, sv}, {B * H, B * Hkv, B * Hkv}};
-    cudaError_t e = fa::launch_quantize_fp8(jobs, N, d, dev->sms * 8, stream);
+    cudaError_t e = fa::launch_quantize_fp8(jobs, N, d, dev->sms, stream);
     if (e != cudaSuccess) return cuda_fail(e, "quantiser launch");
     return FA_OK;
 }
@@ -1561,7 +1563,7 @@ fa_status bwd_fp8_impl(const void* q8, const void* k8, const void* v8, const flo
     jobs.x8[0] = do8;
     jobs.scales[0] = sdo;
     jobs.heads[0] = BH;
-    cudaError_t e = fa::launch_quantize_fp8(jobs, N, d, c.dev->sms * 8, stream);
+    cudaError_t e = fa::launch_quantize_fp8(jobs, N, d, c.dev->sms, stream);
     if (e != cudaSuccess) return cuda_fail(e, "dO quantiser launch");
     e = fa::launch_bwd_pre_fp8(o, do8, sdo, lse, reinterpret_cast<float*>(c.ws + c.L.lse2),
                                reinterpret_cast<float*>(c.ws + c.L.dvec), reinterpret_cast<float*>(c.ws + c.L.dqacc),

@@ -13,6 +13,7 @@
 // All use 16-byte vector accesses and grid-stride loops over a grid sized in
 // multiples of the SM count.
 #include <cuda_bf16.h>
+#include <algorithm>
 
 #include "common.cuh"
 #include "ptx.cuh"
@@ -398,13 +399,15 @@ __global__ void __launch_bounds__(256) bwd_dq_varlen_kernel(const float* __restr
 // is the correctly rounded quotient.  Valid while s, 1/s and the quotients
 // stay normal; callers use it for 2^-100 < s < 2^100 (quotients below the
 // normal range are far below the smallest E4M3 step and quantise to 0 either
-// way) and take __fdiv_rn otherwise.
+// way) and take __fdiv_rn otherwise.  Two dividends at a time: q = RN(x r),
+// the residual RN(x - q s) (exact) and RN(q + residual r), each as one
+// two-lane instruction.
 struct SharedDivisor {
     float s, r;
-    __device__ __forceinline__ float div(float x) const {
-        const float q = __fmul_rn(x, r);
-        const float res = fmaf(-q, s, x);
-        return fmaf(res, r, q);
+    __device__ __forceinline__ float2 div2(float2 x) const {
+        const float2 q = fmul2(x, make_float2(r, r));
+        const float2 res = ffma2(q, make_float2(-s, -s), x);
+        return ffma2(res, make_float2(r, r), q);
     }
 };
 
@@ -450,7 +453,7 @@ __device__ __forceinline__ QuantBlock quant_block(const QuantJobs& jobs, long gb
     return b;
 }
 
-__global__ void __launch_bounds__(256) quantize_fp8_kernel(const __grid_constant__ QuantJobs jobs, int N, int D, int nblk) {
+__global__ void __launch_bounds__(256, 4) quantize_fp8_kernel(const __grid_constant__ QuantJobs jobs, int N, int D, int nblk) {
     constexpr int G = 4;  // uint4 groups (8 elements) per thread: 256 * 4 * 8 = 64 rows x 128
     __shared__ float red[2][8];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -478,14 +481,15 @@ __global__ void __launch_bounds__(256) quantize_fp8_kernel(const __grid_constant
             nb = quant_block(jobs, gblk + gridDim.x, n0, n1, N, D, nblk);
             load(nb, nraw);
         }
-        float f[G][8];
-        float amax = 0.f;
+        // absmax on the bf16 pairs (exact: a maximum of bf16 values is one of them)
+        __nv_bfloat162 m2 = __float2bfloat162_rn(0.f);
 #pragma unroll
         for (int i = 0; i < G; ++i) {
-            unpack8(raw[i], f[i]);
+            const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw[i]);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fabsf(f[i][k]));
+            for (int k = 0; k < 4; ++k) m2 = __hmax2(m2, __habs2(h[k]));
         }
+        float amax = fmaxf(__low2float(m2), __high2float(m2));
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
         if (lane == 0) red[par][warp] = amax;  // double-buffered: no second barrier per block
@@ -495,12 +499,19 @@ __global__ void __launch_bounds__(256) quantize_fp8_kernel(const __grid_constant
         for (int w = 1; w < 8; ++w) m = fmaxf(m, red[par][w]);
         const float s = (m > 0.f) ? __fdiv_rn(m, 448.f) : 1.f;
         if (threadIdx.x == 0) *b.scale = s;
+        float f[G][8];
+#pragma unroll
+        for (int i = 0; i < G; ++i) unpack8(raw[i], f[i]);
         if (shared_divisor_ok(s)) {  // uniform over the CTA
             const SharedDivisor dv = shared_divisor(s);
 #pragma unroll
             for (int i = 0; i < G; ++i)
 #pragma unroll
-                for (int k = 0; k < 8; ++k) f[i][k] = dv.div(f[i][k]);
+                for (int k = 0; k < 8; k += 2) {
+                    const float2 q = dv.div2(make_float2(f[i][k], f[i][k + 1]));
+                    f[i][k] = q.x;
+                    f[i][k + 1] = q.y;
+                }
         } else {
 #pragma unroll
             for (int i = 0; i < G; ++i)
@@ -809,7 +820,9 @@ __global__ void shared_div_check_kernel(const float* __restrict__ x, const float
                                         float* __restrict__ q_fast, float* __restrict__ q_ieee) {
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
         const float d = s[i % ns];
-        q_fast[i] = shared_divisor(d).div(x[i]);
+        // the pair form the quantiser uses, its lanes taken in turn
+        const float2 q = shared_divisor(d).div2(make_float2(x[i], x[i]));
+        q_fast[i] = (i & 1) ? q.y : q.x;
         q_ieee[i] = __fdiv_rn(x[i], d);
     }
 }
@@ -820,8 +833,22 @@ cudaError_t launch_shared_div_check(const float* x, const float* s, int ns, size
     return cudaGetLastError();
 }
 
-cudaError_t launch_quantize_fp8(const QuantJobs& jobs, int N, int d, int grid, cudaStream_t s) {
+cudaError_t launch_quantize_fp8(const QuantJobs& jobs, int N, int d, int sms, cudaStream_t s) {
     const int nblk = (N + 63) / 64;
+    // The CTAs loop over the blocks, so the grid is what fits on the GPU at
+    // once: a larger grid would run as a partial second wave, each late CTA
+    // taking its share of blocks after the others have finished.
+    static const int per_sm = [] {
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, quantize_fp8_kernel, 256, 0) != cudaSuccess) {
+            (void)cudaGetLastError();
+            n = 1;
+        }
+        return n > 0 ? n : 1;
+    }();
+    const long long blocks = (long long)(jobs.heads[0] + jobs.heads[1] + jobs.heads[2]) * nblk;
+    const int grid = (int)std::min<long long>(blocks, (long long)sms * per_sm);
+    if (grid <= 0) return cudaSuccess;
     quantize_fp8_kernel<<<grid, 256, 0, s>>>(jobs, N, d, nblk);
     return cudaGetLastError();
 }

@@ -90,6 +90,7 @@ __device__ __forceinline__ Item get_item(int it, const BwdFp8Params& p, bool cau
         I.bh = it / p.num_kt;
         I.kt = it % p.num_kt;
     }
+    dcheck(chk::tile_ok(I.bh, BH, I.kt, p.num_kt), kErrCheckTile);
     I.b = I.bh / p.H;
     I.kvl = p.kv_lens ? min(max(__ldg(p.kv_lens + I.b), 0), p.N) : p.N;
     const int key0 = I.kt * BC;
@@ -130,14 +131,8 @@ __device__ __forceinline__ float blk_scale(const float* s, int bh, int nblk, int
     return blk < nblk ? __ldg(s + (size_t)bh * nblk + blk) : 0.f;
 }
 
-__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* m, uint32_t src, int c0, int c1) {
-    asm volatile(
-        "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
-            reinterpret_cast<uint64_t>(m)),
-        "r"(src), "r"(c0), "r"(c1)
-        : "memory");
-}
-
+// 448 threads = 14 warps, 4 of them on two of the SM's four sub-partitions,
+// whose register files hold 16384 registers each: at most 128 a thread.
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_fp8_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
@@ -151,6 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const bool causal = p.causal != 0;
     auto BAR = [&](int i) -> uint32_t { return sbase + OFF_BAR + 8 * i; };
+    FA_CHECK_BIND(p.err);
 
     if (threadIdx.x == 0) {
         mbar_init(BAR(B_KVFULL), 1);
@@ -409,8 +405,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         wq4.w = pack_e5m2x4(ds[12] * qmul, ds[13] * qmul, ds[14] * qmul, ds[15] * qmul);
                         // 16-byte chunk (h * 64 + c) / 16 of the row, in the 128-byte swizzle
                         const int chunk = (h * HALF + c) / 16;
-                        *reinterpret_cast<uint4*>(xk_row + ((chunk ^ (kr & 7)) * 16)) = wk;
-                        *reinterpret_cast<uint4*>(xq_row + ((chunk ^ (kr & 7)) * 16)) = wq4;
+                        if (dcheck(chk::range_ok(kr * 128 + ((chunk ^ (kr & 7)) * 16), 16, TILE), kErrCheckSmem)) {
+                            *reinterpret_cast<uint4*>(xk_row + ((chunk ^ (kr & 7)) * 16)) = wk;
+                            *reinterpret_cast<uint4*>(xq_row + ((chunk ^ (kr & 7)) * 16)) = wq4;
+                        }
                     }
                 }
                 fence_proxy_async_smem();
@@ -468,8 +466,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int half = 0; half < 2; ++half) {
                     uint32_t v[64];
                     tmem_ld64_wait(tmem + lane_off + TM_X + half * 64, v);
+                    if (dcheck(chk::range_ok(((half * 64 + 63) * 32 + lane) * 4, 4, DQ_WARP_BYTES), kErrCheckSmem))
 #pragma unroll
-                    for (int q = 0; q < 64; ++q) stage_f[(half * 64 + q) * 32 + lane] = __uint_as_float(v[q]) * mul;
+                        for (int q = 0; q < 64; ++q) stage_f[(half * 64 + q) * 32 + lane] = __uint_as_float(v[q]) * mul;
                 }
                 tc_fence_before();
                 mbar_arrive(BAR(B_DQEMPTY));

@@ -173,6 +173,7 @@ __device__ __forceinline__ Item get_item(int it, const ParamsT<WINDOW, SPARSE, R
         I.bh = it / p.num_kt;
         I.kt = it % p.num_kt;
     }
+    dcheck(chk::tile_ok(I.bh, BH, I.kt, p.num_kt), kErrCheckTile);
     I.b = I.bh / Hkv;
     const int group = GQA ? p.H / Hkv : 1;
     const int gper = group / gs;  // query heads of this unit
@@ -262,21 +263,6 @@ __device__ __forceinline__ void store_chunk32(void* base, size_t elem_off, const
     }
 }
 
-__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* m, uint32_t src, int c0, int c1) {
-    asm volatile(
-        "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
-            reinterpret_cast<uint64_t>(m)),
-        "r"(src), "r"(c0), "r"(c1)
-        : "memory");
-}
-
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, uint32_t src, int c0, int c1) {
-    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
-                     reinterpret_cast<uint64_t>(m)),
-                 "r"(src), "r"(c0), "r"(c1)
-                 : "memory");
-}
-
 // ---- MMA groups (warp-wide issue, one elected lane) ----
 // All descriptors arrive as precomputed bases; per-MMA offsets are constants.
 // S^T = K_j Q_i^T  or  dP^T = V_j dO_i^T  (K-major operands)
@@ -337,6 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     auto BAR = [&](int i) -> uint32_t { return sbase + C::OFF_BAR + 8 * i; };
+    FA_CHECK_BIND(p.err);
 
     if (threadIdx.x == 0) {
         mbar_init(BAR(C::B_KVFULL), 1);
@@ -616,7 +603,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 dseph[dsb] ^= 1;
                 // write dS^T row `kr` (queries h*HALF .. +HALF) into the swizzled tile,
                 // 32 dP columns at a time
-                uint8_t* dsrow = smem + C::OFF_DS + dsb * C::DS_TILE;
 #pragma unroll
                 for (int cc = 0; cc < C::HALF; cc += 32) {
                     uint32_t dr[32];
@@ -638,7 +624,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const float g7 = pv[c + 7] * (__uint_as_float(dr[c8 + 7]) - d1.w);
                         const uint4 v = make_uint4(pack_bf16x2(g0, g1), pack_bf16x2(g2, g3), pack_bf16x2(g4, g5),
                                                    pack_bf16x2(g6, g7));
-                        *reinterpret_cast<uint4*>(dsrow + box * C::DS_BOX + kr * 128 + ((chunk ^ (kr & 7)) * 16)) = v;
+                        const int dso = dsb * C::DS_TILE + box * C::DS_BOX + kr * 128 + ((chunk ^ (kr & 7)) * 16);
+                        if (dcheck(chk::range_ok(dso, 16, 2 * C::DS_TILE), kErrCheckSmem))
+                            *reinterpret_cast<uint4*>(smem + C::OFF_DS + dso) = v;
                     }
                 }
                 fence_proxy_async_smem();
@@ -721,8 +709,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if constexpr (C::D == 128) {
                     // lane = head-dim index (wq*32 + lane); column = query. Stage [64 q][32 d].
+                    if (dcheck(chk::range_ok(63 * 32 * 4 + lane * 4, 4, C::DQ_WARP_BYTES), kErrCheckSmem))
 #pragma unroll
-                    for (int q = 0; q < 64; ++q) stage_f[q * 32 + lane] = __uint_as_float(v[q]);
+                        for (int q = 0; q < 64; ++q) stage_f[q * 32 + lane] = __uint_as_float(v[q]);
                 } else {
                     // lane = query (wq*32 + lane); column = head dim.  Two [32 q][32 d]
                     // boxes in the 128-byte-swizzle layout: 16-byte chunk c of row r
@@ -730,6 +719,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // banks, and every register index stays a compile-time constant;
                     // the tensor reduction undoes the swizzle on its way to global memory
                     uint8_t* stage_b = reinterpret_cast<uint8_t*>(stage_f);
+                    if (dcheck(chk::range_ok(4096 + lane * 128 + 7 * 16, 16, C::DQ_WARP_BYTES), kErrCheckSmem))
 #pragma unroll
                     for (int b = 0; b < 2; ++b)
 #pragma unroll

@@ -6,6 +6,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "checks.h"
+
 namespace fa {
 
 // Bits of the device error word (set by a kernel whose pipeline wait timed out).
@@ -304,7 +306,7 @@ struct QuantJobs {
     float* scales[3];
     int heads[3];  // B * heads of each tensor
 };
-cudaError_t launch_quantize_fp8(const QuantJobs& jobs, int N, int d, int grid, cudaStream_t stream);
+cudaError_t launch_quantize_fp8(const QuantJobs& jobs, int N, int d, int sms, cudaStream_t stream);
 // Merges the split-key partials of the forward into O (bf16) and LSE.
 cudaError_t launch_lse_merge(const float* o_part, const float* lse_part, int num_whole, int num_tail, int splits,
                              bool causal, int BH, int num_qp, int N, int d, void* o, float* lse, cudaStream_t stream);

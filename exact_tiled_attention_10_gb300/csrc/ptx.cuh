@@ -8,7 +8,47 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "checks.h"
+
+#ifndef FA_DEBUG
+#define FA_DEBUG 0
+#endif
+
 namespace fa {
+
+// ------------------------------------------------------------ FA_DEBUG checks
+// The checked build records a kErrCheck* bit (checks.h) in the device error
+// word when an access breaks one of the rules of checks.h and skips the
+// access, so the kernel runs on (its waits for a skipped copy time out,
+// bounded) and the host reports FA_ERR_CHECK.
+#if FA_DEBUG
+// The error word of the running kernel (one per translation unit; every
+// checked kernel binds it on entry).
+static __device__ unsigned int* g_check_err;
+#define FA_CHECK_BIND(errp)                        \
+    do {                                           \
+        if (threadIdx.x == 0) g_check_err = (errp); \
+        __syncthreads();                           \
+    } while (0)
+__device__ __forceinline__ bool dcheck(bool ok, unsigned int bit) {
+    if (!ok) {
+        unsigned int* e = g_check_err;
+        if (e) atomicOr(e, bit);
+    }
+    return ok;
+}
+#else
+#define FA_CHECK_BIND(errp) \
+    do {                    \
+    } while (0)
+__device__ __forceinline__ bool dcheck(bool, unsigned int) { return true; }
+#endif
+__device__ __forceinline__ uint32_t dynamic_smem_bytes() {
+    uint32_t n;
+    asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(n));
+    return n;
+}
+__device__ __forceinline__ uint32_t warp_in_cta() { return threadIdx.x >> 5; }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -90,6 +130,7 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
 // 3-D tiled load (coordinates innermost first) completing on an mbarrier.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* m, uint32_t bar, int c0,
                                             int c1, int c2) {
+    if (!dcheck(chk::tma_inner_ok(c0, 1) && chk::sw128_base_ok(dst), kErrCheckTma)) return;
     asm volatile(
         "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
@@ -98,13 +139,31 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* m, 
 }
 // Plain bulk copy global -> shared (16-byte aligned, size multiple of 16).
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    if (!dcheck(chk::bulk_ok(dst, reinterpret_cast<uint64_t>(src), bytes), kErrCheckTma)) return;
     asm volatile(
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
         : "memory");
 }
+// 2-D tiled store / float32 add-reduction shared -> global (bulk group).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, uint32_t src, int c0, int c1) {
+    if (!dcheck(chk::tma_store_ok(c0, c1, 1) && (src & 127u) == 0, kErrCheckTma)) return;
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(m)),
+                 "r"(src), "r"(c0), "r"(c1)
+                 : "memory");
+}
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* m, uint32_t src, int c0, int c1) {
+    if (!dcheck(chk::tma_store_ok(c0, c1, 1) && (src & 127u) == 0, kErrCheckTma)) return;
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(m)),
+        "r"(src), "r"(c0), "r"(c1)
+        : "memory");
+}
 // Bulk float32 add-reduction shared -> global (16-byte aligned, size multiple of 16).
 __device__ __forceinline__ void bulk_reduce_add_f32(void* dst, uint32_t src, uint32_t bytes) {
+    if (!dcheck(chk::bulk_ok(reinterpret_cast<uint64_t>(dst), src, bytes), kErrCheckTma)) return;
     asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(
                      reinterpret_cast<uint64_t>(dst)),
                  "r"(src), "r"(bytes)
@@ -282,6 +341,7 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
 #define FA_R8(i) "=r"(r[i]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), "=r"(r[i + 4]), \
                  "=r"(r[i + 5]), "=r"(r[i + 6]), "=r"(r[i + 7])
 __device__ __forceinline__ void tmem_ld32_wait(uint32_t taddr, uint32_t (&r)[32]) {
+    if (!dcheck(chk::tmem_ok(taddr, 32, warp_in_cta()), kErrCheckTmem)) return;
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
         "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
@@ -291,6 +351,7 @@ __device__ __forceinline__ void tmem_ld32_wait(uint32_t taddr, uint32_t (&r)[32]
         : "memory");
 }
 __device__ __forceinline__ void tmem_ld64_wait(uint32_t taddr, uint32_t (&r)[64]) {
+    if (!dcheck(chk::tmem_ok(taddr, 64, warp_in_cta()), kErrCheckTmem)) return;
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
         "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,"
@@ -302,6 +363,7 @@ __device__ __forceinline__ void tmem_ld64_wait(uint32_t taddr, uint32_t (&r)[64]
         : "memory");
 }
 __device__ __forceinline__ void tmem_ld128_wait(uint32_t taddr, uint32_t (&r)[128]) {
+    if (!dcheck(chk::tmem_ok(taddr, 128, warp_in_cta()), kErrCheckTmem)) return;
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x128.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
         "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,"
@@ -321,6 +383,7 @@ __device__ __forceinline__ void tmem_ld128_wait(uint32_t taddr, uint32_t (&r)[12
 #define FA_W8(i) "r"(r[i]), "r"(r[i + 1]), "r"(r[i + 2]), "r"(r[i + 3]), "r"(r[i + 4]), \
                  "r"(r[i + 5]), "r"(r[i + 6]), "r"(r[i + 7])
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    if (!dcheck(chk::tmem_ok(taddr, 16, warp_in_cta()), kErrCheckTmem)) return;
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
         "%14,%15,%16};" ::"r"(taddr),
@@ -328,6 +391,7 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
         : "memory");
 }
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    if (!dcheck(chk::tmem_ok(taddr, 32, warp_in_cta()), kErrCheckTmem)) return;
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
         "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
@@ -345,6 +409,7 @@ __device__ __forceinline__ void tmem_st_wait() {
 // leading / stride byte offsets; bits 46-47 hold the descriptor version (1)
 // and bits 61-63 the layout (2 = 128-byte swizzle).
 __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    dcheck(chk::sw128_base_ok(saddr), kErrCheckSmem);
     uint64_t d = 0;
     d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
     d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
@@ -391,6 +456,15 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
         : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
     return d;
 }
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
 __device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
     float2 d;
     asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
@@ -400,30 +474,6 @@ __device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
         : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
     return d;
 }
-// 2^x for a pair of floats on the FMA pipe (no MUFU), relative error <= 7.5e-5
-// for x >= -125 (below that the result is a tiny positive number <= 2^-124):
-//   r = round(x) (by adding 1.5*2^23), f = x - r in [-1/2, 1/2],
-//   2^f ~ c0 + c1 f + c2 f^2 + c3 f^3 (minimax in relative error on [-1/2, 1/2],
-//   coefficients from csrc/exp2_poly_fit.py), 2^r applied by adding r to the
-//   exponent field.
-constexpr float kExp2C0 = 9.999280735e-01f;
-constexpr float kExp2C1 = 6.932609855e-01f;
-constexpr float kExp2C2 = 2.426111222e-01f;
-constexpr float kExp2C3 = 5.517166906e-02f;
-__device__ __forceinline__ float2 exp2_poly2(float2 x) {
-    const float2 magic = make_float2(12582912.f, 12582912.f);
-    x.x = fmaxf(x.x, -125.f);
-    x.y = fmaxf(x.y, -125.f);
-    const float2 j = fadd2(x, magic);
-    const float2 r = fadd2(j, make_float2(-12582912.f, -12582912.f));
-    const float2 f = ffma2(r, make_float2(-1.f, -1.f), x);
-    float2 q = ffma2(make_float2(kExp2C3, kExp2C3), f, make_float2(kExp2C2, kExp2C2));
-    q = ffma2(q, f, make_float2(kExp2C1, kExp2C1));
-    q = ffma2(q, f, make_float2(kExp2C0, kExp2C0));
-    return make_float2(__uint_as_float(__float_as_uint(q.x) + (__float_as_uint(j.x) << 23)),
-                       __uint_as_float(__float_as_uint(q.y) + (__float_as_uint(j.y) << 23)));
-}
-
 // Max of n floats (n a multiple of 16, n >= 16) with 8 independent chains of
 // 3-input max, then a 3-level tree: short dependency chains, half the
 // instructions of a pairwise loop.

@@ -66,7 +66,8 @@ typedef enum {
     FA_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned pointer, ... */
     FA_ERR_UNSUPPORTED = 2, /* head dim / dtype / device not supported        */
     FA_ERR_CUDA = 3,        /* a CUDA runtime or driver call failed            */
-    FA_ERR_TIMEOUT = 4      /* a kernel gave up waiting (device error word)    */
+    FA_ERR_TIMEOUT = 4,     /* a kernel gave up waiting (device error word)    */
+    FA_ERR_CHECK = 5        /* checked build (FA_DEBUG): an access broke a rule */
 } fa_status;
 
 /* Element type of the attention tensors.  FA_E4M3: q, k, v are E4M3 codes
@@ -100,8 +101,13 @@ FA_API int fa_version(void);
 FA_API const char* fa_last_error(void);
 
 /* Waits for `stream`, then reads and clears the device error word.  Returns
- * FA_ERR_TIMEOUT if a kernel recorded a timed-out pipeline wait since the last
- * call, FA_ERR_CUDA if the stream itself reports an error, else FA_OK. */
+ * FA_ERR_CHECK if, in the checked build (compiled with FA_DEBUG=1, shipped as
+ * libfa_gb300_debug.so), a kernel found an access that breaks one of its
+ * rules -- a TMA coordinate or alignment, a TMEM lane quadrant or column
+ * range, a shared-memory tile store out of its tile, a work item decoded out
+ * of range -- and skipped it; else FA_ERR_TIMEOUT if a kernel recorded a
+ * timed-out pipeline wait since the last call; FA_ERR_CUDA if the stream
+ * itself reports an error; else FA_OK. */
 FA_API fa_status fa_check_device_status(fa_stream_t stream);
 
 /* Failure-detection self-test: launches one warp that waits, through the same

@@ -23,7 +23,7 @@ import oracle
 from exact_tiled_attention_10_gb300 import (backward_fp8, check_device_status, forward_fp8, quantize_fp8,
                                             quantize_fp8_qkv)
 from exact_tiled_attention_10_gb300.inputs import WORKLOADS, qkv
-from parity_util import assert_close_abs, sample_rows, to64
+from parity_util import _log, assert_close_abs, sample_rows, to64
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -59,6 +59,30 @@ def test_fp8_backward_matches_oracle_on_dequantised_inputs(N, causal):
     for name, x in (("dq", dq), ("dk", dk), ("dv", dv)):
         assert x.dtype == torch.float32
         _assert_fp8_grad(to64(x), r[name], name)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_backward_against_the_original_bf16_inputs(causal):
+    """Against the oracle on the ORIGINAL bf16 Q, K, V, dO (before E4M3
+    quantisation), element by element: by the triangle inequality the error
+    is at most the kernel's bound on the dequantised inputs plus the exact
+    effect of the input quantisation, |dX(Q^, K^, V^, dO^) - dX(Q, K, V, dO)|,
+    which the oracle computes on both input sets (nothing here comes from the
+    GPU).  The norm-wise relative error is logged beside it."""
+    N = 300
+    q, k, v, do = qkv(2, 2, N, 128, 311 + causal, device=DEV)
+    (q8, sq, k8, sk, v8, sv, do_hat, _), (dq, dk, dv) = _grads(2, 2, N, causal, 311 + causal)
+    sc = 1 / math.sqrt(128)
+    r_hat = oracle.bwd(_deq(q8, sq), _deq(k8, sk), _deq(v8, sv), do_hat, sc, causal=causal)
+    r = oracle.bwd(to64(q), to64(k), to64(v), to64(do), sc, causal=causal)
+    for name, x in (("dq", dq), ("dk", dk), ("dv", dv)):
+        g = to64(x)
+        bound = FP8_GRAD_REL_TOL * np.max(np.abs(r_hat[name])) + np.abs(r_hat[name] - r[name])
+        err = np.abs(g - r[name])
+        rel = np.linalg.norm(g - r[name]) / np.linalg.norm(r[name])
+        _log("%s vs original inputs (norm-wise %.4f)" % (name, rel), np.max(err / np.maximum(bound, 1e-300)), 1.0,
+             normwise=rel)
+        assert np.all(err <= bound), "%s: %d elements over the bound" % (name, int(np.sum(err > bound)))
 
 
 def test_fp8_backward_key_lengths_and_empty_items():
