@@ -46,6 +46,14 @@ WORKLOADS = {
 }
 
 
+def randn_on_device(shape, seed: int, device, dtype=torch.bfloat16) -> torch.Tensor:
+    """N(0,1) drawn by the device's own generator (seeded), for tensors too
+    large to draw on the host; the oracle then reads the sampled parts of the
+    same tensor."""
+    g = torch.Generator(device=device).manual_seed(int(seed))
+    return torch.randn(*shape, generator=g, dtype=torch.float32, device=device).to(dtype)
+
+
 def randn(shape, seed: int, dtype=torch.bfloat16, device="cpu") -> torch.Tensor:
     """N(0,1) drawn in fp32 on the CPU generator, then cast (so every device
     and dtype sees the same underlying draw)."""
