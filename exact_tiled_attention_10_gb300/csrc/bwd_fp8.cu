@@ -460,18 +460,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!(ok = wait_bounded_warp(BAR(B_DQFULL), dqph, abort_flag, p.err, kErrWaitBwdDq))) break;
                 dqph ^= 1;
                 tc_fence_after();
+                // half 0 staged, half 1 loaded, the columns released, half 1 staged
                 if (lane == 0) bulk_wait_group_read<0>();  // the previous reduction has read the staging
                 __syncwarp();
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     uint32_t v[64];
                     tmem_ld64_wait(tmem + lane_off + TM_X + half * 64, v);
+                    if (half == 1) {
+                        tc_fence_before();
+                        mbar_arrive(BAR(B_DQEMPTY));
+                    }
                     if (dcheck(chk::range_ok(((half * 64 + 63) * 32 + lane) * 4, 4, DQ_WARP_BYTES), kErrCheckSmem))
 #pragma unroll
                         for (int q = 0; q < 64; ++q) stage_f[(half * 64 + q) * 32 + lane] = __uint_as_float(v[q]) * mul;
                 }
-                tc_fence_before();
-                mbar_arrive(BAR(B_DQEMPTY));
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
