@@ -898,7 +898,7 @@ fa_status bwd_main_impl(const BwdCtx& c, bool f32, const void* qb, const void* k
 
 fa_status bwd_dq_impl(const BwdCtx& c, bool f32, void* dq, int N, int d, float scale, cudaStream_t stream) {
     cudaError_t e = fa::launch_bwd_dq(reinterpret_cast<float*>(c.ws + c.L.dqacc), dq, f32, scale, c.BH, N, c.Np, d,
-                                      bw_grid(c.dev), stream);
+                                      c.dev->sms, stream);
     if (e != cudaSuccess) return cuda_fail(e, "dQ conversion launch");
     return FA_OK;
 }

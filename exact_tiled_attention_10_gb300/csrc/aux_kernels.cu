@@ -794,10 +794,23 @@ cudaError_t launch_bwd_pre_fp8(const void* o, const void* do8, const float* sdo,
     return cudaGetLastError();
 }
 
+// CTAs that fit on the GPU at once (256 threads each), for the grid-stride
+// kernels whose grid should not spill into a partial second wave.
+template <class K>
+int resident_ctas(K kernel, int sms) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, 256, 0) != cudaSuccess) {
+        (void)cudaGetLastError();
+        n = 1;
+    }
+    return sms * (n > 0 ? n : 1);
+}
+
 cudaError_t launch_bwd_dq(const float* dq_acc, void* dq, bool out_f32, float scale, int BH, int N, int Np, int d,
-                          int grid, cudaStream_t s) {
-    if (out_f32) bwd_dq_kernel<true><<<grid, 256, 0, s>>>(dq_acc, dq, scale, BH, N, Np, d);
-    else bwd_dq_kernel<false><<<grid, 256, 0, s>>>(dq_acc, dq, scale, BH, N, Np, d);
+                          int sms, cudaStream_t s) {
+    static const int per_f32 = resident_ctas(bwd_dq_kernel<true>, 1), per_bf16 = resident_ctas(bwd_dq_kernel<false>, 1);
+    if (out_f32) bwd_dq_kernel<true><<<sms * per_f32, 256, 0, s>>>(dq_acc, dq, scale, BH, N, Np, d);
+    else bwd_dq_kernel<false><<<sms * per_bf16, 256, 0, s>>>(dq_acc, dq, scale, BH, N, Np, d);
     return cudaGetLastError();
 }
 
@@ -838,14 +851,7 @@ cudaError_t launch_quantize_fp8(const QuantJobs& jobs, int N, int d, int sms, cu
     // The CTAs loop over the blocks, so the grid is what fits on the GPU at
     // once: a larger grid would run as a partial second wave, each late CTA
     // taking its share of blocks after the others have finished.
-    static const int per_sm = [] {
-        int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, quantize_fp8_kernel, 256, 0) != cudaSuccess) {
-            (void)cudaGetLastError();
-            n = 1;
-        }
-        return n > 0 ? n : 1;
-    }();
+    static const int per_sm = resident_ctas(quantize_fp8_kernel, 1);
     const long long blocks = (long long)(jobs.heads[0] + jobs.heads[1] + jobs.heads[2]) * nblk;
     const int grid = (int)std::min<long long>(blocks, (long long)sms * per_sm);
     if (grid <= 0) return cudaSuccess;

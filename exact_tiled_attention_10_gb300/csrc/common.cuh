@@ -298,7 +298,7 @@ cudaError_t launch_bwd_pre(const void* o, const void* dout, bool in_f32, const f
                            float* lse2, float* dvec, float* dq_acc, int BH, int N, int Np, int d,
                            int grid, cudaStream_t stream);
 cudaError_t launch_bwd_dq(const float* dq_acc, void* dq, bool out_f32, float scale, int BH, int N,
-                          int Np, int d, int grid, cudaStream_t stream);
+                          int Np, int d, int sms, cudaStream_t stream);
 // Up to three tensors quantised by one launch (unused slots: heads = 0).
 struct QuantJobs {
     const void* x[3];  // bf16
