@@ -16,8 +16,11 @@
 //
 // GB300 mapping (one CTA per SM, persistent over (head, key block) items):
 //   * the key block (128 keys) is the M = 128 side of every MMA, so K_j, V_j
-//     stay in shared memory and dK_j, dV_j accumulate in TMEM for the item;
+//     stay on chip for the item and dK_j, dV_j accumulate in TMEM;
 //   * S^T = K_j Q_i^T and dP^T = V_j dO_i^T land in TMEM with one key per lane;
+//     at d = 128 their A operands K_j, V_j are read from TMEM (copied there
+//     once per item by warps 8-11), which takes 32 KB per step off the
+//     shared-memory bandwidth that bounds the products;
 //   * two compute warpgroups (warps 0-3, 4-7) each own half of the query
 //     columns: P^T goes back to TMEM (bf16, aliased on S^T) as the A operand of
 //     dV += P^T dO_i; dS^T is written to shared memory in the 128-byte-swizzle
@@ -26,10 +29,10 @@
 //   * d = 128: dQ_i^T = K_j^T dS^T (M = 128 head-dim lanes, N = 64 queries);
 //     d = 64:  dQ_i = dS K_j (M = 128 query lanes, N = 64).  Either way all
 //     MMAs have M = 128;
-//   * d = 128 keeps two step slots in TMEM (S^T, and dP^T whose columns are
-//     reused for dQ^T once dS is formed), so the MMA warp issues the next
-//     steps' S and dP while the compute warpgroups work on the current one;
-//     d = 64 has room for one slot (plus a separate dQ region);
+//   * TMEM holds one step slot: S^T, and dP^T whose columns are reused for
+//     dQ^T once dS is formed (d = 128; d = 64 has a separate dQ region).  The
+//     MMA warp issues S of the next step while the compute warpgroups work on
+//     the current one, and its dP once the current dQ^T has been drained;
 //   * warps 8-11 drain the dQ tile from TMEM into shared memory and add it to
 //     the float32 accumulator with asynchronous bulk reductions (TMA), each
 //     warp independently;
@@ -59,17 +62,23 @@ struct Cfg {
     static constexpr int BC = 128;                    // keys per item (TMEM lanes)
     static constexpr int BR = (D == 128) ? 64 : 128;  // queries per inner step
     static constexpr int HALF = BR / 2;               // query columns per compute warpgroup
-    static constexpr int NSLOT = (D == 128) ? 2 : 1;  // TMEM step slots
-    static constexpr bool DQ_ALIAS = (NSLOT == 2);    // dQ reuses the slot's dP columns
+    static constexpr int NSLOT = 1;                   // TMEM step slots
+    // d = 128: K_j and V_j are also copied into TMEM (bf16, two per column) and
+    // serve as the A operands of S^T and dP^T, so those products read only
+    // their 2 KB of Q_i / dO_i per instruction from shared memory
+    static constexpr bool KV_TMEM = (D == 128);
+    static constexpr bool DQ_ALIAS = (D == 128);      // dQ reuses the slot's dP columns
     static constexpr int ROW_BYTES = D * 2;
     static constexpr int NBOX = ROW_BYTES / 128;
     static constexpr int K_BOX = BC * 128, K_TILE = BC * ROW_BYTES;
     static constexpr int Q_BOX = BR * 128, Q_TILE = BR * ROW_BYTES;
     static constexpr int DS_BOX = BC * 128, DS_TILE = BC * BR * 2;
     static constexpr int DQ_WARP_BYTES = 8192;        // per drain warp staging
-    static constexpr int STAGES = NSLOT + 1;          // Q/dO ring
-    // TMEM columns: dV | dK | slot 0 (S, X) | slot 1 (S, X) | [dQ]
-    static constexpr int TM_DV = 0, TM_DK = D, TM_SLOT0 = 2 * D, TM_SLOT = 2 * BR;
+    static constexpr int STAGES = (D == 128) ? 3 : 2;  // Q/dO ring
+    // TMEM columns: dV | dK | [K | V] | slot (S, X) | [dQ]
+    static constexpr int TM_DV = 0, TM_DK = D;
+    static constexpr int TM_K = 2 * D, TM_V = 2 * D + D / 2;  // used when KV_TMEM
+    static constexpr int TM_SLOT0 = KV_TMEM ? 3 * D : 2 * D, TM_SLOT = 2 * BR;
     static constexpr int TM_DQ = DQ_ALIAS ? -1 : TM_SLOT0 + NSLOT * TM_SLOT;
     static constexpr int TM_COLS = 512;
     static_assert(TM_SLOT0 + NSLOT * TM_SLOT + (DQ_ALIAS ? 0 : 64) <= TM_COLS, "TMEM budget");
@@ -91,7 +100,8 @@ struct Cfg {
     static constexpr int B_DQFULL = B_DSEMPTY + 2, B_DQEMPTY = B_DQFULL + 2;
     static constexpr int B_ACCFULL = B_DQEMPTY + 2, B_ACCEMPTY = B_ACCFULL + 1;
     static constexpr int B_DONE = B_ACCEMPTY + 1;
-    static constexpr int NBAR = B_DONE + 1;
+    static constexpr int B_KVTFULL = B_DONE + 1;  // K_j, V_j copied into TMEM
+    static constexpr int NBAR = B_KVTFULL + 1;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM = OFF_MISC + 16 + 1024;
     static_assert(SMEM <= 232448, "shared memory budget");
@@ -273,6 +283,15 @@ __device__ __forceinline__ void mma_scores(uint32_t d_tmem, uint64_t kv_desc, ui
         mma_f16_ss_w(d_tmem, desc_add(kv_desc, (kk / 4) * C::K_BOX + (kk % 4) * 32),
                      desc_add(q_desc, (kk / 4) * C::Q_BOX + (kk % 4) * 32), C::IDESC_S, kk > 0);
 }
+// The same products with K_j or V_j from TMEM (kv_tmem: its first column;
+// K-major, two head-dim elements per column, 8 columns per 16-wide K step)
+template <class C>
+__device__ __forceinline__ void mma_scores_t(uint32_t d_tmem, uint32_t kv_tmem, uint64_t q_desc) {
+#pragma unroll
+    for (int kk = 0; kk < C::D / 16; ++kk)
+        mma_f16_ts_w(d_tmem, kv_tmem + kk * 8, desc_add(q_desc, (kk / 4) * C::Q_BOX + (kk % 4) * 32), C::IDESC_S,
+                     kk > 0 ? 1u : 0u);
+}
 // TMEM column of the packed P^T for queries [16 kk, 16 kk + 16): each compute
 // warpgroup h writes its half at the start of its own S^T columns (never into
 // columns the other warpgroup may still be reading).
@@ -310,6 +329,34 @@ __device__ __forceinline__ void mma_dq(uint32_t d_tmem, uint64_t k_mn, uint64_t 
     }
 }
 
+// Copy key row `kr` of the K_j and V_j tiles (128-byte-swizzle boxes of 64
+// head-dim elements: 16-byte chunk c of row r at chunk c ^ (r & 7)) into the
+// calling warp's TMEM lane, bf16 pairs in head-dim order: the K-major A
+// operand layout of tcgen05.mma with A in TMEM.
+template <class C>
+__device__ __forceinline__ void copy_kv_to_tmem(const uint8_t* smem, uint32_t t_lane, int kr) {
+#pragma unroll 1
+    for (int t = 0; t < 2; ++t) {
+        const uint8_t* tile = smem + (t ? C::OFF_V : C::OFF_K);
+#pragma unroll 1
+        for (int bx = 0; bx < C::NBOX; ++bx) {
+            uint32_t w[32];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const int off = bx * C::K_BOX + kr * 128 + ((c ^ (kr & 7)) * 16);
+                uint4 u = make_uint4(0u, 0u, 0u, 0u);
+                if (dcheck(chk::range_ok(off, 16, C::K_TILE), kErrCheckSmem))
+                    u = *reinterpret_cast<const uint4*>(tile + off);
+                w[4 * c] = u.x;
+                w[4 * c + 1] = u.y;
+                w[4 * c + 2] = u.z;
+                w[4 * c + 3] = u.w;
+            }
+            tmem_st32(t_lane + (t ? C::TM_V : C::TM_K) + bx * 32, w);
+        }
+    }
+}
+
 template <class C, bool CAUSAL, bool OUT_F32, bool GQA, bool VARLEN = false, bool WINDOW = false,
           bool SPARSE = false, bool RECT = false, bool DET = false>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -344,6 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(BAR(C::B_ACCFULL), 1);
         mbar_init(BAR(C::B_ACCEMPTY), 256);
         mbar_init(BAR(C::B_DONE), 1);
+        mbar_init(BAR(C::B_KVTFULL), 128);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -406,10 +454,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
-        // Per item, with slot(s) = s % NSLOT:
-        //   prologue: S(s), dP(s) for s < NSLOT
-        //   step s:   dV(s) | S(s+NSLOT) | dK(s), dQ(s) | dP(s+1) if not yet issued
-        // so the compute warpgroups always have a later step's S / dP in flight.
+        // Per item (one TMEM slot):
+        //   prologue: S(0), dP(0)
+        //   step s:   dV(s) | S(s+1) | dQ(s), dK(s) | dP(s+1) once dQ(s) is drained
+        // so the compute warpgroups have the next step's S in flight while they
+        // form dS(s), and dQ(s), which the next dP waits for, goes first.
         int st = 0, st_ahead = 0;  // Q ring stage of step s / of the next step to open
         uint32_t qph = 0, qph_ahead = 0, kvph = 0, aeph = 0;
         uint32_t pph[2] = {0, 0}, dsph[2] = {0, 0}, dqeph[2] = {0, 0};
@@ -427,7 +476,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto open_step = [&](int slot) -> bool {
             if (!wait_bounded_warp(BAR(C::B_QFULL + st_ahead), qph_ahead, abort_flag, p.err, kErrWaitBwdMma)) return false;
             tc_fence_after();
-            mma_scores<C>(tmem + C::s_col(slot), k_kd, desc_add(q_kd0, st_ahead * C::Q_TILE));
+            if constexpr (C::KV_TMEM)
+                mma_scores_t<C>(tmem + C::s_col(slot), tmem + C::TM_K, desc_add(q_kd0, st_ahead * C::Q_TILE));
+            else
+                mma_scores<C>(tmem + C::s_col(slot), k_kd, desc_add(q_kd0, st_ahead * C::Q_TILE));
             mma_commit_w(BAR(C::B_SFULL + slot));
             if (++st_ahead == C::STAGES) { st_ahead = 0; qph_ahead ^= 1; }
             return true;
@@ -441,7 +493,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 dqeph[slot] ^= 1;
             }
             tc_fence_after();
-            mma_scores<C>(tmem + C::x_col(slot), v_kd, desc_add(do_kd0, stage * C::Q_TILE));
+            if constexpr (C::KV_TMEM)
+                mma_scores_t<C>(tmem + C::x_col(slot), tmem + C::TM_V, desc_add(do_kd0, stage * C::Q_TILE));
+            else
+                mma_scores<C>(tmem + C::x_col(slot), v_kd, desc_add(do_kd0, stage * C::Q_TILE));
             mma_commit_w(BAR(C::B_DPFULL + slot));
             return true;
         };
@@ -451,6 +506,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const Item I = get_item<C, CAUSAL, GQA, VARLEN, WINDOW, SPARSE, RECT, DET>(it, p);
             if (I.n == 0) continue;
             if (!(ok = wait_bounded_warp(BAR(C::B_KVFULL), kvph, abort_flag, p.err, kErrWaitBwdMma))) break;
+            if constexpr (C::KV_TMEM)  // the drain warps have copied K_j, V_j into TMEM
+                if (!(ok = wait_bounded_warp(BAR(C::B_KVTFULL), kvph, abort_flag, p.err, kErrWaitBwdMma))) break;
             kvph ^= 1;
             // prologue: S of the first NSLOT steps, then their dP
             for (int s = 0; s < C::NSLOT && s < I.n && ok; ++s) ok = open_step(s);
@@ -479,10 +536,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     dqeph[0] ^= 1;
                 }
                 tc_fence_after();
-                mma_dk<C>(tmem, desc_add(ds_kd0, dsb * C::DS_TILE), desc_add(q_mn0, st * C::Q_TILE), s > 0);
-                mma_commit_w(BAR(C::B_QEMPTY + st));
                 mma_dq<C>(tmem + C::dq_col(slot), k_mn, desc_add(ds_mn0, dsb * C::DS_TILE));
                 mma_commit_w(BAR(C::B_DQFULL + dqs));
+                mma_dk<C>(tmem, desc_add(ds_kd0, dsb * C::DS_TILE), desc_add(q_mn0, st * C::Q_TILE), s > 0);
+                mma_commit_w(BAR(C::B_QEMPTY + st));
                 mma_commit_w(BAR(C::B_DSEMPTY + dsb));
                 // dP(s+1) for steps past the prologue
                 if (s + 1 < I.n && s + 1 >= C::NSLOT && !(ok = issue_dp((s + 1) % C::NSLOT, (st + 1) % C::STAGES)))
@@ -667,7 +724,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         const uint32_t stage = sbase + C::OFF_DQ + wq * C::DQ_WARP_BYTES;
         float* stage_f = reinterpret_cast<float*>(smem + C::OFF_DQ + wq * C::DQ_WARP_BYTES);
-        uint32_t dqph[2] = {0, 0};
+        uint32_t dqph[2] = {0, 0}, kvph = 0;
         bool ok = true;
         // DET: pend[j] is the turn counter of the write issued j + 1 steps ago;
         // it is passed on once that write has completed (kDetLag steps later,
@@ -679,6 +736,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int it = snake_item(rd, p.num_items);
             if (it < 0) continue;
             const Item I = get_item<C, CAUSAL, GQA, VARLEN, WINDOW, SPARSE, RECT, DET>(it, p);
+            if (C::KV_TMEM && I.n > 0) {
+                // K_j, V_j rows of this warp's lanes into TMEM.  The previous item's
+                // S and dP products, the only readers, were issued before its last dQ
+                // product, whose completion this warp has already waited for.
+                if (!(ok = wait_bounded_warp(BAR(C::B_KVFULL), kvph, abort_flag, p.err, kErrWaitBwdDq))) break;
+                kvph ^= 1;
+                copy_kv_to_tmem<C>(smem, tmem + lane_off, wq * 32 + lane);
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(BAR(C::B_KVTFULL));
+            }
             int bhq = I.qh0, i = I.i0;
             for (int s = 0; s < I.n; ++s, step_next<GQA>(I, bhq, i)) {
                 if constexpr (SPARSE) sparse_step<C>(I, p, s, bhq, i);
