@@ -239,10 +239,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto open_step = [&]() -> bool {  // S^T of the next step into the S columns
             if (!wait_bounded_warp(BAR(B_QFULL + st_ahead), qph_ahead, abort_flag, p.err, kErrWaitBwdMma)) return false;
             tc_fence_after();
+            if (elect_one()) {
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-                mma_f8_ss_w(tmem + TM_S, desc_add(k_kd, kk * 32), desc_add(q_kd0, st_ahead * TILE + kk * 32), IDESC_S,
-                            kk > 0);
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_f8_ss(tmem + TM_S, desc_add(k_kd, kk * 32), desc_add(q_kd0, st_ahead * TILE + kk * 32), IDESC_S,
+                              kk > 0);
+            }
+            __syncwarp();
             mma_commit_w(BAR(B_SFULL));
             if (++st_ahead == STAGES) { st_ahead = 0; qph_ahead ^= 1; }
             return true;
@@ -263,10 +266,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     dq_pending = false;
                 }
                 tc_fence_after();
+                if (elect_one()) {
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_f8_ss_w(tmem + TM_X, desc_add(v_kd, kk * 32), desc_add(do_kd0, st * TILE + kk * 32), IDESC_S,
-                                kk > 0);
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_f8_ss(tmem + TM_X, desc_add(v_kd, kk * 32), desc_add(do_kd0, st * TILE + kk * 32), IDESC_S,
+                                  kk > 0);
+                }
+                __syncwarp();
                 mma_commit_w(BAR(B_DPFULL));
                 // dV(s) += P''^T dO8
                 if (!(ok = wait_bounded_warp(BAR(B_PFULL), pph, abort_flag, p.err, kErrWaitBwdMma))) break;
@@ -276,24 +282,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                     aeph ^= 1;
                 }
                 tc_fence_after();
+                if (elect_one()) {
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_f8_ts_w(tmem + TM_DV, tmem + TM_S + (kk >> 1) * HALF + (kk & 1) * 8,
-                                desc_add(do_mn0, st * TILE + kk * 32 * 128), IDESC_DV, (s > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_f8_ts(tmem + TM_DV, tmem + TM_S + (kk >> 1) * HALF + (kk & 1) * 8,
+                                  desc_add(do_mn0, st * TILE + kk * 32 * 128), IDESC_DV, (s > 0 || kk > 0) ? 1u : 0u);
+                }
+                __syncwarp();
                 // S^T(s+1): the S columns (P'') are read by dV(s), issued before
                 if (s + 1 < I.n && !(ok = open_step())) break;
                 // dK(s), dQ^T(s)
                 if (!(ok = wait_bounded_warp(BAR(B_DSFULL), dsph, abort_flag, p.err, kErrWaitBwdMma))) break;
                 dsph ^= 1;
                 tc_fence_after();
+                if (elect_one()) {
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_f8_ss_w(tmem + TM_DK, desc_add(xk_kd, kk * 32), desc_add(q_mn0, st * TILE + kk * 32 * 128),
-                                IDESC_DK, (s > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_f8_ss(tmem + TM_DK, desc_add(xk_kd, kk * 32), desc_add(q_mn0, st * TILE + kk * 32 * 128),
+                                  IDESC_DK, (s > 0 || kk > 0) ? 1u : 0u);
+                }
+                __syncwarp();
                 mma_commit_w(BAR(B_QEMPTY + st));
+                if (elect_one()) {
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_f8_ss_w(tmem + TM_X, desc_add(kt_kd, kk * 32), desc_add(xq_mn, kk * 32 * 128), IDESC_DQ, kk > 0);
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_f8_ss(tmem + TM_X, desc_add(kt_kd, kk * 32), desc_add(xq_mn, kk * 32 * 128), IDESC_DQ,
+                                  kk > 0);
+                }
+                __syncwarp();
                 mma_commit_w(BAR(B_DQFULL));
                 mma_commit_w(BAR(B_DSEMPTY));
                 dq_pending = true;

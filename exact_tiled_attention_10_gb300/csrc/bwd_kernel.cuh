@@ -273,24 +273,30 @@ __device__ __forceinline__ void store_chunk32(void* base, size_t elem_off, const
     }
 }
 
-// ---- MMA groups (warp-wide issue, one elected lane) ----
+// ---- MMA groups (the MMA warp elects one lane, which issues the whole group) ----
 // All descriptors arrive as precomputed bases; per-MMA offsets are constants.
 // S^T = K_j Q_i^T  or  dP^T = V_j dO_i^T  (K-major operands)
 template <class C>
 __device__ __forceinline__ void mma_scores(uint32_t d_tmem, uint64_t kv_desc, uint64_t q_desc) {
+    if (elect_one()) {
 #pragma unroll
-    for (int kk = 0; kk < C::D / 16; ++kk)
-        mma_f16_ss_w(d_tmem, desc_add(kv_desc, (kk / 4) * C::K_BOX + (kk % 4) * 32),
-                     desc_add(q_desc, (kk / 4) * C::Q_BOX + (kk % 4) * 32), C::IDESC_S, kk > 0);
+        for (int kk = 0; kk < C::D / 16; ++kk)
+            mma_f16_ss(d_tmem, desc_add(kv_desc, (kk / 4) * C::K_BOX + (kk % 4) * 32),
+                       desc_add(q_desc, (kk / 4) * C::Q_BOX + (kk % 4) * 32), C::IDESC_S, kk > 0);
+    }
+    __syncwarp();
 }
 // The same products with K_j or V_j from TMEM (kv_tmem: its first column;
 // K-major, two head-dim elements per column, 8 columns per 16-wide K step)
 template <class C>
 __device__ __forceinline__ void mma_scores_t(uint32_t d_tmem, uint32_t kv_tmem, uint64_t q_desc) {
+    if (elect_one()) {
 #pragma unroll
-    for (int kk = 0; kk < C::D / 16; ++kk)
-        mma_f16_ts_w(d_tmem, kv_tmem + kk * 8, desc_add(q_desc, (kk / 4) * C::Q_BOX + (kk % 4) * 32), C::IDESC_S,
-                     kk > 0 ? 1u : 0u);
+        for (int kk = 0; kk < C::D / 16; ++kk)
+            mma_f16_ts(d_tmem, kv_tmem + kk * 8, desc_add(q_desc, (kk / 4) * C::Q_BOX + (kk % 4) * 32), C::IDESC_S,
+                       kk > 0 ? 1u : 0u);
+    }
+    __syncwarp();
 }
 // TMEM column of the packed P^T for queries [16 kk, 16 kk + 16): each compute
 // warpgroup h writes its half at the start of its own S^T columns (never into
@@ -302,31 +308,40 @@ __device__ __forceinline__ constexpr uint32_t p_col(int kk) {
 // dV_j (+)= P^T dO_i  (P^T from TMEM, dO_i MN-major: do_mn = MN-major base)
 template <class C>
 __device__ __forceinline__ void mma_dv(uint32_t tmem, uint32_t s_tmem, uint64_t do_mn, bool acc) {
+    if (elect_one()) {
 #pragma unroll
-    for (int kk = 0; kk < C::BR / 16; ++kk)
-        mma_f16_ts_w(tmem + C::TM_DV, s_tmem + p_col<C>(kk), desc_add(do_mn, kk * 2048), C::IDESC_ACC,
-                     (acc || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < C::BR / 16; ++kk)
+            mma_f16_ts(tmem + C::TM_DV, s_tmem + p_col<C>(kk), desc_add(do_mn, kk * 2048), C::IDESC_ACC,
+                       (acc || kk > 0) ? 1u : 0u);
+    }
+    __syncwarp();
 }
 // dK_j (+)= dS^T Q_i  (dS^T K-major in smem, Q_i MN-major)
 template <class C>
 __device__ __forceinline__ void mma_dk(uint32_t tmem, uint64_t ds_k, uint64_t q_mn, bool acc) {
+    if (elect_one()) {
 #pragma unroll
-    for (int kk = 0; kk < C::BR / 16; ++kk)
-        mma_f16_ss_w(tmem + C::TM_DK, desc_add(ds_k, (kk / 4) * C::DS_BOX + (kk % 4) * 32),
-                     desc_add(q_mn, kk * 2048), C::IDESC_ACC, (acc || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < C::BR / 16; ++kk)
+            mma_f16_ss(tmem + C::TM_DK, desc_add(ds_k, (kk / 4) * C::DS_BOX + (kk % 4) * 32),
+                       desc_add(q_mn, kk * 2048), C::IDESC_ACC, (acc || kk > 0) ? 1u : 0u);
+    }
+    __syncwarp();
 }
 // d=128: dQ^T = K_j^T dS^T ; d=64: dQ = dS K_j  (both operands MN-major)
 template <class C>
 __device__ __forceinline__ void mma_dq(uint32_t d_tmem, uint64_t k_mn, uint64_t ds_mn) {
+    if (elect_one()) {
 #pragma unroll
-    for (int kk = 0; kk < C::BC / 16; ++kk) {
-        const uint64_t dk = desc_add(k_mn, kk * 2048);
-        const uint64_t ds = desc_add(ds_mn, kk * 2048);
-        if (C::D == 128)
-            mma_f16_ss_w(d_tmem, dk, ds, C::IDESC_DQ, kk > 0);
-        else
-            mma_f16_ss_w(d_tmem, ds, dk, C::IDESC_DQ, kk > 0);
+        for (int kk = 0; kk < C::BC / 16; ++kk) {
+            const uint64_t dk = desc_add(k_mn, kk * 2048);
+            const uint64_t ds = desc_add(ds_mn, kk * 2048);
+            if (C::D == 128)
+                mma_f16_ss(d_tmem, dk, ds, C::IDESC_DQ, kk > 0);
+            else
+                mma_f16_ss(d_tmem, ds, dk, C::IDESC_DQ, kk > 0);
+        }
     }
+    __syncwarp();
 }
 
 // Copy key row `kr` of the K_j and V_j tiles (128-byte-swizzle boxes of 64

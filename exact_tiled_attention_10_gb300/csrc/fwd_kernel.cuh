@@ -406,37 +406,43 @@ __device__ __forceinline__ ItemT<VARLEN, WINDOW, SPARSE> get_item(int unit, cons
 // are compile-time constants added to the start-address field.
 template <class C>
 __device__ __forceinline__ void issue_S(uint32_t d_tmem, uint64_t q_desc, uint64_t k_desc) {
+    if (elect_one()) {
 #pragma unroll
-    for (int part = 0; part < (C::SPLIT ? 3 : 1); ++part) {
-        const uint64_t qd = desc_add(q_desc, part == 2 ? C::QT * C::Q_TILE : 0);
-        const uint64_t kd = desc_add(k_desc, part == 1 ? C::KV_TILE : 0);
+        for (int part = 0; part < (C::SPLIT ? 3 : 1); ++part) {
+            const uint64_t qd = desc_add(q_desc, part == 2 ? C::QT * C::Q_TILE : 0);
+            const uint64_t kd = desc_add(k_desc, part == 1 ? C::KV_TILE : 0);
 #pragma unroll
-        for (int kk = 0; kk < C::S_STEPS; ++kk) {
-            const uint32_t off_in = (kk % 4) * 32;
-            const uint64_t a = desc_add(qd, (kk / 4) * C::Q_BOX + off_in);
-            const uint64_t b = desc_add(kd, (kk / 4) * C::KV_BOX + off_in);
-            const uint32_t acc = (part > 0 || kk > 0) ? 1u : 0u;
-            if constexpr (C::FP8)
-                mma_f8_ss_w(d_tmem, a, b, C::IDESC_S, acc);
-            else
-                mma_f16_ss_w(d_tmem, a, b, C::IDESC_S, acc);
+            for (int kk = 0; kk < C::S_STEPS; ++kk) {
+                const uint32_t off_in = (kk % 4) * 32;
+                const uint64_t a = desc_add(qd, (kk / 4) * C::Q_BOX + off_in);
+                const uint64_t b = desc_add(kd, (kk / 4) * C::KV_BOX + off_in);
+                const uint32_t acc = (part > 0 || kk > 0) ? 1u : 0u;
+                if constexpr (C::FP8)
+                    mma_f8_ss(d_tmem, a, b, C::IDESC_S, acc);
+                else
+                    mma_f16_ss(d_tmem, a, b, C::IDESC_S, acc);
+            }
         }
     }
+    __syncwarp();
 }
 
 // O_t (+)= P_t V over the keys; P_t from TMEM, V MN-major (head dim contiguous).
 // KK0 / KK1: the range of K steps issued (the whole block by default).
 template <class C, int KK0 = 0, int KK1 = C::PV_STEPS>
 __device__ __forceinline__ void issue_PV(uint32_t o_tmem, uint32_t p_tmem, uint64_t v_desc, bool accumulate) {
+    if (elect_one()) {
 #pragma unroll
-    for (int kk = KK0; kk < KK1; ++kk) {
-        const uint64_t b = desc_add(v_desc, kk * C::KSTEP * 128);
-        const uint32_t acc = (accumulate || kk > 0) ? 1u : 0u;
-        if constexpr (C::FP8)
-            mma_f8_ts_w(o_tmem, p_tmem + kk * 8, b, C::IDESC_PV, acc);
-        else
-            mma_f16_ts_w(o_tmem, p_tmem + kk * 8, b, C::IDESC_PV, acc);
+        for (int kk = KK0; kk < KK1; ++kk) {
+            const uint64_t b = desc_add(v_desc, kk * C::KSTEP * 128);
+            const uint32_t acc = (accumulate || kk > 0) ? 1u : 0u;
+            if constexpr (C::FP8)
+                mma_f8_ts(o_tmem, p_tmem + kk * 8, b, C::IDESC_PV, acc);
+            else
+                mma_f16_ts(o_tmem, p_tmem + kk * 8, b, C::IDESC_PV, acc);
+        }
     }
+    __syncwarp();
 }
 
 // 2^x for a pair (MUFU ex2; 2^-inf = 0 exactly for masked scores)
