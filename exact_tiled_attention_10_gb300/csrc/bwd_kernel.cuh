@@ -35,7 +35,8 @@
 //     the current one, and its dP once the current dQ^T has been drained;
 //   * warps 8-11 drain the dQ tile from TMEM into shared memory and add it to
 //     the float32 accumulator with asynchronous bulk reductions (TMA), each
-//     warp independently;
+//     warp independently; at d = 128 they also copy K_j, V_j into TMEM at
+//     the start of each item;
 //   * warp 12 issues TMA loads (K_j, V_j once per item; a ring of Q_i, dO_i
 //     and the row statistics), warp 13 issues tcgen05.mma.
 #pragma once
