@@ -19,8 +19,9 @@
 //     stay on chip for the item and dK_j, dV_j accumulate in TMEM;
 //   * S^T = K_j Q_i^T and dP^T = V_j dO_i^T land in TMEM with one key per lane;
 //     at d = 128 their A operands K_j, V_j are read from TMEM (copied there
-//     once per item by warps 8-11), which takes 32 KB per step off the
-//     shared-memory bandwidth that bounds the products;
+//     once per item by warps 8-11), which takes 32 KB of operand reads per
+//     step off shared memory and lets those N = 64 products run at their
+//     math rate;
 //   * two compute warpgroups (warps 0-3, 4-7) each own half of the query
 //     columns: P^T goes back to TMEM (bf16, aliased on S^T) as the A operand of
 //     dV += P^T dO_i; dS^T is written to shared memory in the 128-byte-swizzle
